@@ -1,0 +1,206 @@
+"""Python access to the double-precision CPU oracle (``rowops_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: imported by the test suite, by the package smoke
+check and by the benchmark's CPU-baseline leg. The product path never imports
+it. Arrays go in as numpy (float32 values, which hold bf16 values exactly, or
+float64 for the single-row forms) and come out as float64.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional, Tuple
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "rowops_oracle.c")
+_LIB = os.path.join(_HERE, "librowops_oracle.so")
+
+_c_double_p = ctypes.POINTER(ctypes.c_double)
+_c_float_p = ctypes.POINTER(ctypes.c_float)
+_i64 = ctypes.c_int64
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with the system C compiler (IEEE double, no FMA contraction)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < max(
+        os.path.getmtime(_SRC), os.path.getmtime(os.path.join(_HERE, "rowops_oracle.h"))
+    ):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
+               "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB)
+        L.oracle_gelu_sqrt_2_over_pi.restype = ctypes.c_double
+        L.oracle_gelu_cubic.restype = ctypes.c_double
+        L.oracle_gelu_tanh.restype = ctypes.c_double
+        L.oracle_gelu_tanh.argtypes = [ctypes.c_double]
+        L.oracle_softmax_row.argtypes = [_c_double_p, _i64, _c_double_p]
+        L.oracle_online_softmax_row.argtypes = [_c_double_p, _i64, _i64, _c_double_p, _c_double_p, _c_double_p]
+        L.oracle_split_softmax_row.argtypes = [_c_double_p, _i64, _i64, _c_double_p, _c_double_p, _c_double_p]
+        L.oracle_layernorm_row.argtypes = [_c_double_p, _c_double_p, _c_double_p, ctypes.c_double, _i64, _c_double_p]
+        L.oracle_layernorm_gelu_row.argtypes = L.oracle_layernorm_row.argtypes
+        for name in ("oracle_softmax_rows_f32",):
+            getattr(L, name).argtypes = [_c_float_p, _i64, _i64, _i64, _c_double_p]
+            getattr(L, name).restype = ctypes.c_int
+        L.oracle_split_softmax_rows_f32.argtypes = [_c_float_p, _i64, _i64, _i64, _i64, _c_double_p]
+        L.oracle_split_softmax_rows_f32.restype = ctypes.c_int
+        for name in ("oracle_layernorm_gelu_rows_f32", "oracle_layernorm_rows_f32"):
+            getattr(L, name).argtypes = [_c_float_p, _c_float_p, _c_float_p, ctypes.c_double, _i64, _i64, _i64,
+                                         _c_double_p]
+            getattr(L, name).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _dp(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(_c_double_p)
+
+
+def _fp(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(_c_float_p)
+
+
+def _rows(x: np.ndarray) -> Tuple[np.ndarray, int, int, int]:
+    """Return a float32 2-D array with unit column stride, plus (M, N, ld)."""
+    x = np.asarray(x)
+    if x.ndim == 1:
+        x = x[None, :]
+    if x.ndim != 2:
+        raise ValueError("expected a 1-D or 2-D array")
+    if x.dtype != np.float32 or x.strides[1] != 4 or x.strides[0] % 4 != 0 or x.strides[0] < 4 * x.shape[1]:
+        x = np.ascontiguousarray(x, dtype=np.float32)
+    M, N = x.shape
+    ld = x.strides[0] // 4 if M > 1 else N
+    return x, M, N, ld
+
+
+def _f64_row(x) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64).reshape(-1))
+
+
+def _opt32(v, N) -> Optional[np.ndarray]:
+    if v is None:
+        return None
+    v = np.ascontiguousarray(np.asarray(v, dtype=np.float32).reshape(-1))
+    if v.shape[0] != N:
+        raise ValueError("w / b must have N entries")
+    return v
+
+
+def _opt64(v, N) -> Optional[np.ndarray]:
+    if v is None:
+        return None
+    v = _f64_row(v)
+    if v.shape[0] != N:
+        raise ValueError("w / b must have N entries")
+    return v
+
+
+# ---- constants ---------------------------------------------------------------
+def gelu_sqrt_2_over_pi() -> float:
+    return lib().oracle_gelu_sqrt_2_over_pi()
+
+
+def gelu_cubic() -> float:
+    return lib().oracle_gelu_cubic()
+
+
+# ---- single rows in double -----------------------------------------------------
+def softmax_row(x) -> np.ndarray:
+    xr = _f64_row(x)
+    y = np.empty_like(xr)
+    lib().oracle_softmax_row(_dp(xr), xr.size, _dp(y))
+    return y
+
+
+def online_softmax_row(x, block: int) -> Tuple[np.ndarray, float, float]:
+    xr = _f64_row(x)
+    y = np.empty_like(xr)
+    m = ctypes.c_double()
+    d = ctypes.c_double()
+    lib().oracle_online_softmax_row(_dp(xr), xr.size, int(block), _dp(y), ctypes.byref(m), ctypes.byref(d))
+    return y, m.value, d.value
+
+
+def split_softmax_row(x, chunk: int) -> Tuple[np.ndarray, float, float]:
+    xr = _f64_row(x)
+    y = np.empty_like(xr)
+    m = ctypes.c_double()
+    d = ctypes.c_double()
+    lib().oracle_split_softmax_row(_dp(xr), xr.size, int(chunk), _dp(y), ctypes.byref(m), ctypes.byref(d))
+    return y, m.value, d.value
+
+
+def layernorm_row(x, w=None, b=None, eps: float = 1e-5) -> np.ndarray:
+    xr = _f64_row(x)
+    z = np.empty_like(xr)
+    wd, bd = _opt64(w, xr.size), _opt64(b, xr.size)
+    lib().oracle_layernorm_row(_dp(xr), _dp(wd), _dp(bd), float(eps), xr.size, _dp(z))
+    return z
+
+
+def layernorm_gelu_row(x, w=None, b=None, eps: float = 1e-5) -> np.ndarray:
+    xr = _f64_row(x)
+    y = np.empty_like(xr)
+    wd, bd = _opt64(w, xr.size), _opt64(b, xr.size)
+    lib().oracle_layernorm_gelu_row(_dp(xr), _dp(wd), _dp(bd), float(eps), xr.size, _dp(y))
+    return y
+
+
+def gelu_tanh(z) -> np.ndarray:
+    f = lib().oracle_gelu_tanh
+    zz = np.asarray(z, dtype=np.float64)
+    return np.vectorize(f, otypes=[np.float64])(zz) if zz.ndim else np.float64(f(float(zz)))
+
+
+# ---- row batches (fp32-valued inputs) --------------------------------------------
+def softmax(x) -> np.ndarray:
+    """Stable softmax of every row of a 2-D fp32-valued array -> float64 (M, N)."""
+    xs, M, N, ld = _rows(x)
+    y = np.empty((M, N), dtype=np.float64)
+    if lib().oracle_softmax_rows_f32(_fp(xs), M, N, ld, _dp(y)) != 0:
+        raise ValueError("oracle_softmax_rows_f32 rejected its arguments")
+    return y
+
+
+def split_softmax(x, chunk: int) -> np.ndarray:
+    """Split-row softmax (chunk partials merged in a second pass) -> float64 (M, N)."""
+    xs, M, N, ld = _rows(x)
+    y = np.empty((M, N), dtype=np.float64)
+    if lib().oracle_split_softmax_rows_f32(_fp(xs), M, N, ld, int(chunk), _dp(y)) != 0:
+        raise ValueError("oracle_split_softmax_rows_f32 rejected its arguments")
+    return y
+
+
+def layernorm_gelu(x, w=None, b=None, eps: float = 1e-5) -> np.ndarray:
+    """LayerNorm -> affine -> tanh-GELU of every row -> float64 (M, N)."""
+    xs, M, N, ld = _rows(x)
+    y = np.empty((M, N), dtype=np.float64)
+    wf, bf = _opt32(w, N), _opt32(b, N)
+    if lib().oracle_layernorm_gelu_rows_f32(_fp(xs), _fp(wf), _fp(bf), float(eps), M, N, ld, _dp(y)) != 0:
+        raise ValueError("oracle_layernorm_gelu_rows_f32 rejected its arguments")
+    return y
+
+
+def layernorm(x, w=None, b=None, eps: float = 1e-5) -> np.ndarray:
+    """LayerNorm -> affine (no GELU) of every row -> float64 (M, N)."""
+    xs, M, N, ld = _rows(x)
+    y = np.empty((M, N), dtype=np.float64)
+    wf, bf = _opt32(w, N), _opt32(b, N)
+    if lib().oracle_layernorm_rows_f32(_fp(xs), _fp(wf), _fp(bf), float(eps), M, N, ld, _dp(y)) != 0:
+        raise ValueError("oracle_layernorm_rows_f32 rejected its arguments")
+    return y

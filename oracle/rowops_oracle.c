@@ -1,0 +1,249 @@
+/*
+ * rowops oracle: plain, slow, double-precision CPU reference.
+ *
+ * TEST INFRASTRUCTURE ONLY (see rowops_oracle.h). Written for a reader who
+ * checks it against the definitions by eye: one row at a time, the steps in
+ * the order the pages give them, plain left-to-right sums in double.
+ *
+ * Readings where the pages leave a step open (each also listed in the design
+ * notes):
+ *   - a row whose entries are all -inf has no defined softmax; the pages ask
+ *     for an explicit convention [EX §7]. Here it is all zeros.
+ *   - a NaN anywhere in a row makes the whole softmax row NaN.
+ *   - in the online / split forms a block or chunk with no finite entry has
+ *     d = 0 and is skipped when merging, so -inf - (-inf) never occurs.
+ *   - the GELU constant is 0.79788456 as printed [KT; 171]; the longer
+ *     0.7978845608028654 [FUS §三] differs by < 1e-9 relative.
+ */
+#include "rowops_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+
+static const double GELU_SQRT_2_OVER_PI = 0.79788456;
+static const double GELU_CUBIC = 0.044715;
+
+double oracle_gelu_sqrt_2_over_pi(void) { return GELU_SQRT_2_OVER_PI; }
+double oracle_gelu_cubic(void) { return GELU_CUBIC; }
+
+/* ---------------------------------------------------------------------------
+ * Stable softmax [EX §2.4; KT "Triton Softmax"]:
+ *   m = max_j x_j ; e_j = exp(x_j - m) ; d = sum_j e_j ; y_j = e_j / d
+ * Masked / padding entries are -inf and contribute exp(-inf) = 0 [EX §2.3].
+ * ------------------------------------------------------------------------- */
+void oracle_softmax_row(const double* x, int64_t n, double* y) {
+    double m = -INFINITY;
+    int has_nan = 0;
+    for (int64_t j = 0; j < n; ++j) {
+        if (isnan(x[j])) has_nan = 1;
+        else if (x[j] > m) m = x[j];
+    }
+    if (has_nan) {
+        for (int64_t j = 0; j < n; ++j) y[j] = NAN;
+        return;
+    }
+    if (m == -INFINITY) { /* no unmasked entry: convention, all zeros */
+        for (int64_t j = 0; j < n; ++j) y[j] = 0.0;
+        return;
+    }
+    double d = 0.0;
+    for (int64_t j = 0; j < n; ++j) d += exp(x[j] - m);
+    for (int64_t j = 0; j < n; ++j) y[j] = exp(x[j] - m) / d;
+}
+
+/* ---------------------------------------------------------------------------
+ * Online softmax [EX §2.5; L6 §7.2]. The state is (m, d): the largest entry
+ * seen so far and the sum of exp(x - m) over the entries seen so far. For
+ * each block B of the row, in order:
+ *   m_new = max(m_old, max(B))
+ *   d_new = d_old * exp(m_old - m_new) + sum_{x in B} exp(x - m_new)
+ * and finally y_j = exp(x_j - m) / d.
+ * ------------------------------------------------------------------------- */
+void oracle_online_softmax_row(const double* x, int64_t n, int64_t block, double* y, double* m_out,
+                               double* d_out) {
+    double m = -INFINITY, d = 0.0;
+    int has_nan = 0;
+    if (block < 1) block = 1;
+    for (int64_t start = 0; start < n; start += block) {
+        int64_t stop = start + block < n ? start + block : n;
+        double bmax = -INFINITY;
+        for (int64_t j = start; j < stop; ++j) {
+            if (isnan(x[j])) has_nan = 1;
+            else if (x[j] > bmax) bmax = x[j];
+        }
+        if (bmax == -INFINITY) continue; /* block adds nothing to d */
+        double m_new = m > bmax ? m : bmax;
+        double s = 0.0;
+        for (int64_t j = start; j < stop; ++j) s += exp(x[j] - m_new);
+        d = d * exp(m - m_new) + s; /* exp(-inf) = 0 on the first block */
+        m = m_new;
+    }
+    if (m_out) *m_out = has_nan ? NAN : m;
+    if (d_out) *d_out = has_nan ? NAN : d;
+    for (int64_t j = 0; j < n; ++j) {
+        if (has_nan) y[j] = NAN;
+        else if (d == 0.0) y[j] = 0.0; /* no unmasked entry */
+        else y[j] = exp(x[j] - m) / d;
+    }
+}
+
+/* ---------------------------------------------------------------------------
+ * Split-row softmax [EX §2.5 split_online_softmax]: first pass, each chunk c
+ * computes its own partial (m_c, d_c) = (max of chunk, sum exp(x - m_c));
+ * second pass merges the partials
+ *   m = max_c m_c ;  d = sum_c d_c * exp(m_c - m)      (chunks with d_c = 0 skipped)
+ * third step writes y_j = exp(x_j - m) / d.
+ * ------------------------------------------------------------------------- */
+void oracle_split_softmax_row(const double* x, int64_t n, int64_t chunk, double* y, double* m_out,
+                              double* d_out) {
+    if (chunk < 1) chunk = 1;
+    int64_t nchunks = (n + chunk - 1) / chunk;
+    double* pm = (double*)malloc(sizeof(double) * (size_t)(nchunks > 0 ? nchunks : 1));
+    double* pd = (double*)malloc(sizeof(double) * (size_t)(nchunks > 0 ? nchunks : 1));
+    int has_nan = 0;
+    /* first pass: independent partials */
+    for (int64_t c = 0; c < nchunks; ++c) {
+        int64_t start = c * chunk, stop = start + chunk < n ? start + chunk : n;
+        double mc = -INFINITY;
+        for (int64_t j = start; j < stop; ++j) {
+            if (isnan(x[j])) has_nan = 1;
+            else if (x[j] > mc) mc = x[j];
+        }
+        double dc = 0.0;
+        if (mc != -INFINITY)
+            for (int64_t j = start; j < stop; ++j) dc += exp(x[j] - mc);
+        pm[c] = mc;
+        pd[c] = dc;
+    }
+    /* second pass: merge */
+    double m = -INFINITY;
+    for (int64_t c = 0; c < nchunks; ++c)
+        if (pd[c] != 0.0 && pm[c] > m) m = pm[c];
+    double d = 0.0;
+    for (int64_t c = 0; c < nchunks; ++c)
+        if (pd[c] != 0.0) d += pd[c] * exp(pm[c] - m);
+    free(pm);
+    free(pd);
+    if (m_out) *m_out = has_nan ? NAN : m;
+    if (d_out) *d_out = has_nan ? NAN : d;
+    for (int64_t j = 0; j < n; ++j) {
+        if (has_nan) y[j] = NAN;
+        else if (d == 0.0) y[j] = 0.0;
+        else y[j] = exp(x[j] - m) / d;
+    }
+}
+
+/* ---------------------------------------------------------------------------
+ * LayerNorm [EX §4.1; FUS §三]:
+ *   mean = sum(x) / n
+ *   var  = sum((x - mean)^2) / n            (biased: unbiased=False in FUS §三)
+ *   z    = (x - mean) / sqrt(var + eps) * w + b
+ * Only the n real entries take part (padding never enters the variance).
+ * ------------------------------------------------------------------------- */
+void oracle_layernorm_row(const double* x, const double* w, const double* b, double eps, int64_t n,
+                          double* z) {
+    double s = 0.0;
+    for (int64_t j = 0; j < n; ++j) s += x[j];
+    double mean = s / (double)n;
+    double q = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+        double c = x[j] - mean;
+        q += c * c;
+    }
+    double var = q / (double)n;
+    double rstd = 1.0 / sqrt(var + eps);
+    for (int64_t j = 0; j < n; ++j) {
+        double wj = w ? w[j] : 1.0;
+        double bj = b ? b[j] : 0.0;
+        z[j] = (x[j] - mean) * rstd * wj + bj;
+    }
+}
+
+/* ---------------------------------------------------------------------------
+ * tanh-approximation GELU [KT "Triton GeLU"; EX §3.4; FUS §三]:
+ *   g = 0.5 * z * (1 + tanh(0.79788456 * (z + 0.044715 * z^3)))
+ * with the mathematical tanh (libm, double).
+ * ------------------------------------------------------------------------- */
+double oracle_gelu_tanh(double z) {
+    double inner = GELU_SQRT_2_OVER_PI * (z + GELU_CUBIC * z * z * z);
+    return 0.5 * z * (1.0 + tanh(inner));
+}
+
+/* LayerNorm -> affine -> GELU, one row [FUS §三 _layer_norm_gelu_kernel]. */
+void oracle_layernorm_gelu_row(const double* x, const double* w, const double* b, double eps,
+                               int64_t n, double* y) {
+    oracle_layernorm_row(x, w, b, eps, n, y);
+    for (int64_t j = 0; j < n; ++j) y[j] = oracle_gelu_tanh(y[j]);
+}
+
+/* ---------------------------------------------------------------------------
+ * Row-batch forms: row r of x starts at x + r*ld; output row r at y + r*N.
+ * ------------------------------------------------------------------------- */
+static double* widen(const float* src, int64_t n) {
+    if (!src) return NULL;
+    double* d = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    if (!d) return NULL;
+    for (int64_t j = 0; j < n; ++j) d[j] = (double)src[j];
+    return d;
+}
+
+static int bad_shape(const float* x, int64_t M, int64_t N, int64_t ld, const double* y) {
+    return M < 0 || N < 1 || ld < N || (M > 0 && (!x || !y));
+}
+
+int oracle_softmax_rows_f32(const float* x, int64_t M, int64_t N, int64_t ld, double* y) {
+    if (bad_shape(x, M, N, ld, y)) return -1;
+    double* row = (double*)malloc(sizeof(double) * (size_t)N);
+    if (!row) return -1;
+    for (int64_t r = 0; r < M; ++r) {
+        for (int64_t j = 0; j < N; ++j) row[j] = (double)x[r * ld + j];
+        oracle_softmax_row(row, N, y + r * N);
+    }
+    free(row);
+    return 0;
+}
+
+int oracle_split_softmax_rows_f32(const float* x, int64_t M, int64_t N, int64_t ld, int64_t chunk,
+                                  double* y) {
+    if (bad_shape(x, M, N, ld, y) || chunk < 1) return -1;
+    double* row = (double*)malloc(sizeof(double) * (size_t)N);
+    if (!row) return -1;
+    for (int64_t r = 0; r < M; ++r) {
+        for (int64_t j = 0; j < N; ++j) row[j] = (double)x[r * ld + j];
+        oracle_split_softmax_row(row, N, chunk, y + r * N, NULL, NULL);
+    }
+    free(row);
+    return 0;
+}
+
+static int layernorm_rows(const float* x, const float* w, const float* b, double eps, int64_t M,
+                          int64_t N, int64_t ld, double* y, int with_gelu) {
+    if (bad_shape(x, M, N, ld, y)) return -1;
+    double* row = (double*)malloc(sizeof(double) * (size_t)N);
+    double* wd = widen(w, N);
+    double* bd = widen(b, N);
+    int rc = 0;
+    if (!row || (w && !wd) || (b && !bd)) {
+        rc = -1;
+    } else {
+        for (int64_t r = 0; r < M; ++r) {
+            for (int64_t j = 0; j < N; ++j) row[j] = (double)x[r * ld + j];
+            if (with_gelu) oracle_layernorm_gelu_row(row, wd, bd, eps, N, y + r * N);
+            else oracle_layernorm_row(row, wd, bd, eps, N, y + r * N);
+        }
+    }
+    free(row);
+    free(wd);
+    free(bd);
+    return rc;
+}
+
+int oracle_layernorm_gelu_rows_f32(const float* x, const float* w, const float* b, double eps,
+                                   int64_t M, int64_t N, int64_t ld, double* y) {
+    return layernorm_rows(x, w, b, eps, M, N, ld, y, 1);
+}
+
+int oracle_layernorm_rows_f32(const float* x, const float* w, const float* b, double eps, int64_t M,
+                              int64_t N, int64_t ld, double* y) {
+    return layernorm_rows(x, w, b, eps, M, N, ld, y, 0);
+}

@@ -1,0 +1,76 @@
+/*
+ * rowops oracle: plain, slow, double-precision CPU reference for the row-wise
+ * reduce-then-normalise operations (stable softmax, online / split-row
+ * softmax, LayerNorm -> affine -> tanh-GELU).
+ *
+ * TEST INFRASTRUCTURE ONLY. The test suite, the package smoke check and the
+ * benchmark's CPU-baseline leg are the only users. The CUDA library never
+ * links or calls it, and the two share no code, header or constant.
+ *
+ * Sources (lecture notes on CS336 Lecture 6, "Kernels, Triton"):
+ *   [L6]   "第 6 讲：GPU Kernels 与 Triton" (cs336.sjfarm.cc)
+ *   [KT]   "CS336 Kernels, Triton" notes (yiwen-cai.github.io)
+ *   [EX]   "Triton Kernel 实现练习" (lizn-zn.github.io)
+ *   [171]  "【CS336】lecture6 占用率|bank冲突|Triton|GeLU算子|softmax算子|reduce算子|matmul算子"
+ *   [FUS]  "PyTorch 自定义 CUDA 算子与 Triton 编程从 Python 原型到 GPU 极致性能" (ocdem.com)
+ *
+ * Parity pins: every function here is checked by the CPU test suite against
+ * closed forms, invariants, exact-arithmetic brute force and library routines
+ * (no function is "parity unpinned").
+ */
+#ifndef ROWOPS_ORACLE_H
+#define ROWOPS_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Constants as printed on the pages. */
+double oracle_gelu_sqrt_2_over_pi(void); /* 0.79788456  [KT "Triton GeLU"; 171 "GeLU"] */
+double oracle_gelu_cubic(void);          /* 0.044715    [KT; EX §3.4; FUS §三] */
+
+/* ---- single rows, double in / double out ---------------------------------- */
+
+/* Stable softmax [EX §2.4; KT "Triton Softmax"]. y may alias x. */
+void oracle_softmax_row(const double* x, int64_t n, double* y);
+
+/* Online softmax [EX §2.5; L6 §7.2]: one scan over blocks of `block` entries
+ * with the running state (m, d). Writes y and, if non-NULL, the final m, d. */
+void oracle_online_softmax_row(const double* x, int64_t n, int64_t block, double* y, double* m_out,
+                               double* d_out);
+
+/* Split-row softmax [EX §2.5 split_online_softmax]: per-chunk partials
+ * (m_c, d_c) computed independently, merged in a second pass, then every
+ * entry normalised with the merged (m, d). */
+void oracle_split_softmax_row(const double* x, int64_t n, int64_t chunk, double* y, double* m_out,
+                              double* d_out);
+
+/* LayerNorm [EX §4.1; FUS §三]. w, b may be NULL (weight 1, bias 0). */
+void oracle_layernorm_row(const double* x, const double* w, const double* b, double eps, int64_t n,
+                          double* z);
+
+/* tanh-approximation GELU [KT "Triton GeLU"; EX §3.4; FUS §三]. */
+double oracle_gelu_tanh(double z);
+
+/* LayerNorm, then affine, then GELU [FUS §三 _layer_norm_gelu_kernel]. */
+void oracle_layernorm_gelu_row(const double* x, const double* w, const double* b, double eps,
+                               int64_t n, double* y);
+
+/* ---- M rows with a row stride `ld` (elements), output M x N contiguous ------
+ * The fp32 forms take inputs already widened to fp32 (bf16 values are exact
+ * in fp32) and widen them to double row by row. Return 0, or -1 on bad
+ * arguments / allocation failure. */
+int oracle_softmax_rows_f32(const float* x, int64_t M, int64_t N, int64_t ld, double* y);
+int oracle_split_softmax_rows_f32(const float* x, int64_t M, int64_t N, int64_t ld, int64_t chunk,
+                                  double* y);
+int oracle_layernorm_gelu_rows_f32(const float* x, const float* w, const float* b, double eps,
+                                   int64_t M, int64_t N, int64_t ld, double* y);
+int oracle_layernorm_rows_f32(const float* x, const float* w, const float* b, double eps, int64_t M,
+                              int64_t N, int64_t ld, double* y);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,117 @@
+"""Seeded synthetic inputs for the row-wise reduce-then-normalise workloads.
+
+This module holds random-number generation and the workload table (shapes,
+dtypes, value distributions, masking and outlier structure) and nothing of the
+operations' arithmetic. The CUDA path's tests and benchmark and the oracle's
+tests all draw their inputs from here, so both sides see identical values.
+
+Inputs are drawn with a ``torch.Generator`` on the requested device, seeded per
+workload: values generated on the CPU and on a GPU follow the same recipe but
+are different streams. Large workloads are generated on the device (CPU
+generation of the 1 GiB case takes most of a minute) and the rows the oracle
+checks are copied back to the host.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Dict, Optional
+
+import torch
+
+__all__ = ["Workload", "WORKLOADS", "make_inputs", "torch_dtype", "elem_size"]
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One synthetic workload: an operation, a dtype, a shape and a value recipe."""
+
+    name: str
+    op: str  # "softmax" | "online_softmax" | "layernorm_gelu"
+    dtype: str  # "f32" | "bf16"
+    M: int  # rows
+    N: int  # columns (reduction length)
+    seed: int  # seed of x; w and b use seed + 100 and seed + 200
+    x_std: float = 1.0  # x ~ N(0, x_std^2)
+    causal: bool = False  # row r keeps columns c <= r mod N, the rest are -inf
+    outlier_p: float = 0.0  # fraction of entries (Bernoulli per entry) set to outlier_value
+    outlier_value: float = 30.0
+    affine: bool = False  # layernorm: w ~ U(0.5, 1.5), b ~ N(0, 0.1^2)
+    eps: float = 1e-5
+
+    def with_shape(self, M: Optional[int] = None, N: Optional[int] = None) -> "Workload":
+        return dataclasses.replace(self, M=self.M if M is None else M, N=self.N if N is None else N)
+
+
+# The five workloads of the build's specification (plus the two ragged-tail
+# variants of the bf16 LayerNorm+GELU case), keyed by a descriptive name.
+WORKLOADS: Dict[str, Workload] = {
+    w.name: w
+    for w in [
+        Workload("softmax_f32_1024x768", "softmax", "f32", 1024, 768, seed=0),
+        Workload("layernorm_gelu_f32_4096x768", "layernorm_gelu", "f32", 4096, 768, seed=1, affine=True),
+        Workload("softmax_bf16_causal_32768x4096", "softmax", "bf16", 32768, 4096, seed=2, x_std=2.0, causal=True),
+        Workload("online_softmax_f32_64x1048576", "online_softmax", "f32", 64, 1 << 20, seed=3, outlier_p=1e-3),
+        Workload("layernorm_gelu_bf16_65536x8192", "layernorm_gelu", "bf16", 65536, 8192, seed=4, affine=True),
+        Workload("layernorm_gelu_bf16_65536x127", "layernorm_gelu", "bf16", 65536, 127, seed=4, affine=True),
+        Workload("layernorm_gelu_bf16_65536x4097", "layernorm_gelu", "bf16", 65536, 4097, seed=4, affine=True),
+    ]
+}
+
+
+def torch_dtype(dtype: str) -> torch.dtype:
+    return {"f32": torch.float32, "bf16": torch.bfloat16}[dtype]
+
+
+def elem_size(dtype: str) -> int:
+    return {"f32": 4, "bf16": 2}[dtype]
+
+
+def _gen(device: torch.device, seed: int) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def make_inputs(
+    wl: Workload,
+    device: str | torch.device = "cpu",
+    ld: Optional[int] = None,
+) -> Dict[str, torch.Tensor]:
+    """Draw the inputs of ``wl`` on ``device``.
+
+    Returns ``{"x": (M, N) view, "x_storage": (M, ld) tensor}`` and, for affine
+    LayerNorm workloads, ``"w"`` and ``"b"`` of length N. Values are drawn in
+    fp32 and rounded to the workload's dtype (round to nearest even). With
+    ``ld > N`` the padding columns of each row hold NaN so that any read past
+    column N-1 shows up in the result.
+    """
+    device = torch.device(device)
+    M, N = wl.M, wl.N
+    ld = N if ld is None else ld
+    if ld < N:
+        raise ValueError("ld must be >= N")
+    dt = torch_dtype(wl.dtype)
+    g = _gen(device, wl.seed)
+    x = torch.randn((M, N), generator=g, device=device, dtype=torch.float32)
+    if wl.x_std != 1.0:
+        x.mul_(wl.x_std)
+    if wl.outlier_p > 0.0:
+        hit = torch.rand((M, N), generator=g, device=device, dtype=torch.float32) < wl.outlier_p
+        x.masked_fill_(hit, wl.outlier_value)
+        del hit
+    if wl.causal:
+        cols = torch.arange(N, device=device).unsqueeze(0)
+        keep = (torch.arange(M, device=device) % N).unsqueeze(1)
+        x.masked_fill_(cols > keep, float("-inf"))
+    storage = torch.full((M, ld), float("nan"), device=device, dtype=dt)
+    storage[:, :N] = x.to(dt)
+    del x
+    out = {"x": storage[:, :N], "x_storage": storage}
+    if wl.affine:
+        gw = _gen(device, wl.seed + 100)
+        gb = _gen(device, wl.seed + 200)
+        w = 0.5 + torch.rand((N,), generator=gw, device=device, dtype=torch.float32)
+        b = 0.1 * torch.randn((N,), generator=gb, device=device, dtype=torch.float32)
+        out["w"] = w.to(dt)
+        out["b"] = b.to(dt)
+    return out

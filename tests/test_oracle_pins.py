@@ -1,0 +1,365 @@
+"""Pins for the CPU oracle: closed forms, invariants, exact-arithmetic brute
+force and library routines, so that the oracle is checked against something
+other than itself before it judges the CUDA path.
+
+Each test names the mistake it would catch. Nothing here needs a GPU.
+"""
+import decimal
+import math
+from decimal import Decimal
+
+import numpy as np
+import pytest
+import torch
+
+from tests import _golden
+
+CTX = decimal.Context(prec=60)
+
+
+# ----------------------------------------------------------------------------
+# exact-arithmetic brute force (Decimal, 60 digits), independent of the oracle
+# ----------------------------------------------------------------------------
+def _dec(v: float) -> Decimal:
+    return Decimal(v)  # exact conversion of the double
+
+
+def bf_softmax(xs):
+    xd = [_dec(v) for v in xs]
+    m = max(xd)
+    e = [CTX.exp(CTX.subtract(v, m)) for v in xd]
+    s = sum(e, Decimal(0))
+    return [float(CTX.divide(v, s)) for v in e]
+
+
+def bf_tanh(u: Decimal) -> Decimal:
+    if u < 0:
+        return -bf_tanh(-u)
+    t = CTX.exp(CTX.multiply(Decimal(-2), u))
+    return CTX.divide(1 - t, 1 + t)
+
+
+def bf_gelu(z: float, k0=Decimal("0.79788456"), k1=Decimal("0.044715")) -> float:
+    zd = _dec(z)
+    inner = CTX.multiply(k0, zd + CTX.multiply(k1, CTX.power(zd, 3)))
+    return float(CTX.multiply(CTX.multiply(Decimal("0.5"), zd), 1 + bf_tanh(inner)))
+
+
+def bf_layernorm(xs, w=None, b=None, eps=1e-5):
+    xd = [_dec(v) for v in xs]
+    n = len(xd)
+    mean = CTX.divide(sum(xd, Decimal(0)), n)
+    var = CTX.divide(sum((CTX.subtract(v, mean) ** 2 for v in xd), Decimal(0)), n)
+    rstd = CTX.divide(1, CTX.sqrt(var + _dec(eps)))
+    out = []
+    for j, v in enumerate(xd):
+        wj = _dec(w[j]) if w is not None else Decimal(1)
+        bj = _dec(b[j]) if b is not None else Decimal(0)
+        out.append(CTX.multiply(CTX.multiply(v - mean, rstd), wj) + bj)
+    return out
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+# ----------------------------------------------------------------------------
+# softmax
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("case", _golden.read_cases("softmax_closed_forms.txt"), ids=lambda c: c[0])
+def test_softmax_golden_closed_forms(oracle, case):
+    """Worked examples: catches a wrong normaliser, a missing max subtraction
+    (large_shift case overflows exp without it), -inf handling and the
+    all-masked convention."""
+    _, _, rows = case
+    x = [float(v) for v in rows["x"]]
+    want = [float(v) for v in rows["y"]]
+    # rounding x_j to double moves exp(x_j - m) by up to |x_j| 2^-52 relative
+    finite = [abs(v) for v in x if math.isfinite(v)]
+    rtol = 2e-15 + 2.0 ** -51 * max(finite, default=0.0)
+    outs = [oracle.softmax_row(x)]
+    # the online and split forms reach the same closed forms
+    for blk in (1, 2, 3, len(x) + 1):
+        outs.append(oracle.online_softmax_row(x, blk)[0])
+        outs.append(oracle.split_softmax_row(x, blk)[0])
+    for got in outs:
+        for g, w in zip(got, want):
+            if w == 0.0:
+                assert g == 0.0
+            else:
+                assert abs(g - w) <= rtol * abs(w)
+
+
+def test_softmax_brute_force_tiny(oracle):
+    """3x5 random rows against 60-digit Decimal arithmetic: catches any
+    wrong term, sign or index in the definition."""
+    rng = _rng(11)
+    x = rng.normal(0.0, 3.0, size=(3, 5))
+    for row in x:
+        got = oracle.softmax_row(row)
+        want = bf_softmax(row)
+        np.testing.assert_allclose(got, want, rtol=1e-14, atol=0)
+
+
+@pytest.mark.parametrize("n", [1, 2, 5, 768, 4097])
+def test_softmax_rows_sum_to_one_and_shift_invariant(oracle, n):
+    """sum_j y_j = 1 and softmax(x + c) = softmax(x) for c = 7, 100, 1000.
+    c = 1000 overflows exp() if the row maximum is not subtracted."""
+    rng = _rng(n)
+    x = rng.normal(0.0, 2.0, size=n)
+    y = oracle.softmax_row(x)
+    assert abs(math.fsum(y) - 1.0) <= 1e-13
+    assert np.all(y > 0)
+    for c in (7.0, 100.0, 1000.0):
+        ys = oracle.softmax_row(x + c)
+        np.testing.assert_allclose(ys, y, rtol=1e-12 * max(1.0, c / 10), atol=0)
+
+
+def test_softmax_matches_torch_double(oracle):
+    """Special case reducing to a library routine: torch.softmax in float64."""
+    rng = _rng(3)
+    x = rng.normal(0.0, 4.0, size=(17, 333))
+    x[:, 100:] = np.where(rng.random((17, 233)) < 0.3, -np.inf, x[:, 100:])
+    want = torch.softmax(torch.from_numpy(x), dim=-1).numpy()
+    got = np.stack([oracle.softmax_row(r) for r in x])
+    np.testing.assert_allclose(got, want, rtol=1e-13, atol=1e-300)
+    assert np.all(got[np.isneginf(x)] == 0.0)
+
+
+def test_softmax_nan_propagates_through_row(oracle):
+    x = [0.0, 1.0, float("nan"), 2.0]
+    assert np.all(np.isnan(oracle.softmax_row(x)))
+
+
+def test_softmax_rows_batch_respects_ld_and_padding(oracle):
+    """Batch form with ld > N and NaN padding: catches a stride / padding
+    mistake (reading past N would turn rows into NaN)."""
+    rng = _rng(5)
+    M, N, ld = 6, 37, 48
+    store = np.full((M, ld), np.nan, dtype=np.float32)
+    store[:, :N] = rng.normal(0, 1, size=(M, N)).astype(np.float32)
+    got = oracle.softmax(store[:, :N])
+    assert np.all(np.isfinite(got))
+    for r in range(M):
+        np.testing.assert_array_equal(got[r], oracle.softmax_row(store[r, :N].astype(np.float64)))
+
+
+# ----------------------------------------------------------------------------
+# online / split-row softmax
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("block", [1, 2, 7, 64, 1000, 4096, 5000])
+def test_online_and_split_agree_with_two_pass(oracle, block):
+    """The (m, d) recurrence and the chunk-partial merge reach the direct
+    definition (to 1e-14), and the final state is (max x, sum exp(x - max))
+    computed exactly: catches a wrong rescale factor exp(m_old - m_new)
+    (e.g. a flipped sign) or a dropped partial."""
+    rng = _rng(block)
+    x = rng.normal(0.0, 3.0, size=4096)
+    x[rng.random(4096) < 0.01] += 25.0
+    y_ref = oracle.softmax_row(x)
+    m_exact = max(x)
+    d_exact = float(sum((CTX.exp(_dec(v) - _dec(m_exact)) for v in x), Decimal(0)))
+    for fn in (oracle.online_softmax_row, oracle.split_softmax_row):
+        y, m, d = fn(x, block)
+        np.testing.assert_allclose(y, y_ref, rtol=1e-13, atol=0)
+        assert m == m_exact
+        assert abs(d - d_exact) <= 1e-13 * d_exact
+
+
+def test_online_state_after_each_block_is_prefix_softmax_state(oracle):
+    """After any prefix of blocks the running state equals (max, sum exp(x -
+    max)) of that prefix: pins the recurrence step by step, not just its end."""
+    rng = _rng(21)
+    x = rng.normal(0, 5, size=40)
+    for k in range(1, 41):
+        _, m, d = oracle.online_softmax_row(x[:k], 6)
+        mk = max(x[:k])
+        dk = float(sum((CTX.exp(_dec(v) - _dec(mk)) for v in x[:k]), Decimal(0)))
+        assert m == mk
+        assert abs(d - dk) <= 1e-14 * dk
+
+
+def test_split_skips_fully_masked_chunks(oracle):
+    """A chunk whose entries are all -inf has d_c = 0 and must be skipped, not
+    merged through exp(-inf - (-inf)) = NaN."""
+    x = np.full(64, -np.inf)
+    x[40:48] = np.log(np.arange(1, 9))
+    for chunk in (8, 16, 5):
+        for fn in (oracle.split_softmax_row, oracle.online_softmax_row):
+            y, m, d = fn(x, chunk)
+            assert np.all(np.isfinite(y))
+            np.testing.assert_allclose(y[40:48], np.arange(1, 9) / 36.0, rtol=1e-14)
+            assert np.all(y[:40] == 0) and np.all(y[48:] == 0)
+            assert m == np.log(8.0)
+
+
+def test_split_all_masked_row_is_zero(oracle):
+    y, m, d = oracle.split_softmax_row(np.full(10, -np.inf), 3)
+    assert np.all(y == 0) and d == 0.0 and m == -np.inf
+
+
+def test_outlier_rows_closed_form(oracle):
+    """Rows like the online-softmax workload (N(0,1) with entries set to +30):
+    each outlier gets 1 / (k + S) with S = sum over the rest of exp(x - 30),
+    summed here with math.fsum."""
+    rng = _rng(8)
+    n = 1 << 14
+    x = rng.normal(0, 1, size=n)
+    hit = rng.random(n) < 1e-3
+    x[hit] = 30.0
+    k = int(hit.sum())
+    assert k > 0
+    S = math.fsum(math.exp(v - 30.0) for v in x[~hit])
+    want = 1.0 / (k + S)
+    for chunk in (1 << 10, 1 << 12, n):
+        y, _, _ = oracle.split_softmax_row(x, chunk)
+        np.testing.assert_allclose(y[hit], want, rtol=1e-13)
+    y = oracle.split_softmax(x[None, :].astype(np.float32), 1 << 11)
+    assert abs(math.fsum(y[0]) - 1.0) < 1e-12
+
+
+# ----------------------------------------------------------------------------
+# GELU
+# ----------------------------------------------------------------------------
+def test_gelu_constants_match_pages(oracle):
+    c = _golden.read_constants("gelu_constants.txt")
+    assert oracle.gelu_sqrt_2_over_pi() == float(c["gelu_sqrt_2_over_pi"])
+    assert oracle.gelu_cubic() == float(c["gelu_cubic"])
+    # the two printed forms of sqrt(2/pi) agree with the closed form
+    assert abs(float(c["gelu_sqrt_2_over_pi"]) - math.sqrt(2 / math.pi)) < 1e-8
+    assert abs(float(c["gelu_sqrt_2_over_pi_long"]) - math.sqrt(2 / math.pi)) < 1e-15
+    assert float(c["layernorm_eps_default"]) == 1e-5
+
+
+def test_gelu_special_values(oracle):
+    """GELU(0) = 0; GELU(x) = x exactly once tanh rounds to 1 in double, which
+    for u = 0.79788456 (x + 0.044715 x^3) > 19.1 holds from x = 8 on; GELU(x)
+    is in [-1e-30, 0] for x <= -10."""
+    assert oracle.gelu_tanh(0.0) == 0.0
+    for x in (8.0, 9.5, 10.0, 50.0, 1e3, 3.0e10):
+        assert oracle.gelu_tanh(x) == x
+    for x in (-10.0, -13.0, -100.0, -1e4):
+        g = oracle.gelu_tanh(x)
+        assert -1e-30 <= g <= 0.0
+
+
+def test_gelu_odd_identity(oracle):
+    """tanh is odd, so GELU(x) - GELU(-x) = x exactly in real arithmetic:
+    catches a sign error or a dropped 0.5 / '1 +' term."""
+    for x in np.linspace(-12, 12, 97):
+        assert abs(oracle.gelu_tanh(x) - oracle.gelu_tanh(-x) - x) <= 4e-16 * max(1.0, abs(x))
+
+
+def test_gelu_brute_force(oracle):
+    """Decimal (60 digits) evaluation of 0.5 z (1 + tanh(0.79788456 (z + 0.044715 z^3)))."""
+    for z in (-6.0, -3.5, -2.0, -1.0, -0.25, 1e-6, 0.3, 1.0, 2.5, 5.0, 7.0):
+        want = bf_gelu(z)
+        # the double evaluation of 1 + tanh(u) loses digits for negative z
+        tol = 1e-15 * max(1.0, abs(z)) + 4e-16 * abs(want)
+        assert abs(oracle.gelu_tanh(z) - want) <= tol, z
+
+
+def test_gelu_matches_torch_tanh_gelu(oracle):
+    """torch's tanh-approximation GELU in float64 uses sqrt(2/pi) to full
+    precision; against the printed 0.79788456 the gap is < 1e-9 relative."""
+    z = np.linspace(-9, 9, 1001)
+    want = torch.nn.functional.gelu(torch.from_numpy(z), approximate="tanh").numpy()
+    got = oracle.gelu_tanh(z)
+    np.testing.assert_allclose(got, want, rtol=0, atol=2e-9)
+
+
+# ----------------------------------------------------------------------------
+# LayerNorm, LayerNorm -> GELU
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("case", _golden.read_cases("layernorm_closed_forms.txt"), ids=lambda c: c[0])
+def test_layernorm_golden_closed_forms(oracle, case):
+    """Worked examples: catches an unbiased (n-1) variance, eps outside the
+    sqrt, a wrong affine order and shift sensitivity."""
+    _, params, rows = case
+    x = [float(v) for v in rows["x"]]
+    n = len(x)
+    eps = float(params.get("eps", Decimal("1e-5")))
+    w = [float(params["w"])] * n if "w" in params else None
+    b = [float(params["b"])] * n if "b" in params else None
+    want = [float(v) for v in rows["z"]]
+    got = oracle.layernorm_row(x, w, b, eps)
+    np.testing.assert_allclose(got, want, rtol=0, atol=2e-15 * max(1.0, max(abs(v) for v in want)))
+
+
+def test_layernorm_unit_affine_moments(oracle):
+    """With w = 1, b = 0: mean(z) = 0 and var(z) = s^2 / (s^2 + eps), where
+    s^2 is the biased sample variance (numpy.var) of the row."""
+    rng = _rng(7)
+    for n in (5, 127, 768, 4097, 8192):
+        x = rng.normal(0.3, 1.7, size=n)
+        z = oracle.layernorm_row(x, None, None, 1e-5)
+        s2 = float(np.var(x))
+        assert abs(np.mean(z)) < 1e-13
+        assert abs(np.mean(z * z) - s2 / (s2 + 1e-5)) < 1e-12
+
+
+def test_layernorm_shift_invariant(oracle):
+    rng = _rng(9)
+    x = rng.normal(0, 1, size=300)
+    w = rng.uniform(0.5, 1.5, size=300)
+    b = rng.normal(0, 0.1, size=300)
+    z0 = oracle.layernorm_row(x, w, b, 1e-5)
+    z1 = oracle.layernorm_row(x + 1000.0, w, b, 1e-5)
+    np.testing.assert_allclose(z1, z0, rtol=0, atol=5e-11)
+
+
+def test_layernorm_brute_force_with_affine(oracle):
+    rng = _rng(13)
+    x = rng.normal(0, 2, size=(3, 5))
+    w = rng.uniform(0.5, 1.5, size=5)
+    b = rng.normal(0, 0.1, size=5)
+    for row in x:
+        want = [float(v) for v in bf_layernorm(row, w, b, 1e-5)]
+        np.testing.assert_allclose(oracle.layernorm_row(row, w, b, 1e-5), want, rtol=0, atol=1e-15)
+        want_g = [bf_gelu(v) for v in want]
+        np.testing.assert_allclose(oracle.layernorm_gelu_row(row, w, b, 1e-5), want_g, rtol=0, atol=4e-15)
+
+
+def test_layernorm_matches_torch_double(oracle):
+    rng = _rng(17)
+    M, N = 9, 769
+    x = rng.normal(0, 1, size=(M, N)).astype(np.float32)
+    w = rng.uniform(0.5, 1.5, size=N).astype(np.float32)
+    b = rng.normal(0, 0.1, size=N).astype(np.float32)
+    xt, wt, bt = (torch.from_numpy(a).double() for a in (x, w, b))
+    z_t = torch.nn.functional.layer_norm(xt, (N,), wt, bt, 1e-5)
+    np.testing.assert_allclose(oracle.layernorm(x, w, b, 1e-5), z_t.numpy(), rtol=0, atol=1e-13)
+    g_t = torch.nn.functional.gelu(z_t, approximate="tanh")
+    np.testing.assert_allclose(oracle.layernorm_gelu(x, w, b, 1e-5), g_t.numpy(), rtol=0, atol=5e-9)
+
+
+def test_layernorm_gelu_is_gelu_of_layernorm(oracle):
+    """The fused form applies GELU after the affine step (not before it, not
+    to the normalised value without w, b)."""
+    rng = _rng(19)
+    x = rng.normal(0, 1, size=(4, 50)).astype(np.float32)
+    w = rng.uniform(0.5, 1.5, size=50).astype(np.float32)
+    b = rng.normal(0, 0.5, size=50).astype(np.float32)
+    z = oracle.layernorm(x, w, b, 1e-5)
+    g = oracle.layernorm_gelu(x, w, b, 1e-5)
+    np.testing.assert_array_equal(g, oracle.gelu_tanh(z))
+
+
+def test_layernorm_rows_batch_respects_ld_and_null_affine(oracle):
+    """Batch form: ld > N with NaN padding never reaches the statistics; a
+    NULL weight / bias means 1 / 0."""
+    rng = _rng(23)
+    M, N, ld = 5, 127, 136
+    store = np.full((M, ld), np.nan, dtype=np.float32)
+    store[:, :N] = rng.normal(0, 1, size=(M, N)).astype(np.float32)
+    g = oracle.layernorm_gelu(store[:, :N], None, None, 1e-5)
+    assert np.all(np.isfinite(g))
+    ones, zeros = np.ones(N, np.float32), np.zeros(N, np.float32)
+    np.testing.assert_array_equal(g, oracle.layernorm_gelu(np.ascontiguousarray(store[:, :N]), ones, zeros, 1e-5))
+    for r in range(M):
+        np.testing.assert_array_equal(g[r], oracle.layernorm_gelu_row(store[r, :N].astype(np.float64), None, None, 1e-5))
+
+
+def test_batch_rejects_bad_shapes(oracle):
+    with pytest.raises(ValueError):
+        oracle.layernorm_gelu(np.zeros((2, 3), np.float32), np.ones(4, np.float32))
