@@ -1,0 +1,529 @@
+#!/usr/bin/env python
+"""Benchmark of the row-wise reduce-then-normalise path on GB300.
+
+One step runs the whole hot path once, each operation on its full-size
+synthetic workload:
+  * rowops_softmax          bf16 32768 x 4096, causal -inf mask   (537 MB moved)
+  * rowops_online_softmax   fp32 64 x 2^20, +30 outliers          (537 MB moved)
+  * rowops_layernorm_gelu   bf16 65536 x 8192, w, b               (2148 MB moved)
+and ``value`` is the algorithmic HBM bytes of a step (each input read once,
+each output written once) times the steps, over the device time of the timed
+steps: GB/s. Each input is larger than the 129 MB L2, so no flush is needed
+between steps. The roofline entry is the dominant kernel (LayerNorm+GELU)
+against the measured copy bandwidth.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl rowops|reference]
+
+Under torchrun every rank runs its own copy of the workload (weak scaling,
+no collective on the data path); rank 0 prints one JSON line.
+``--impl reference`` times the double-precision CPU oracle on host cores on a
+bounded sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from row_wise_reduction_gb300 import workloads  # noqa: E402
+
+METRIC = "row-kernel HBM GB/s (% of GB300 peak) for softmax and LayerNorm+GELU"
+STEP = ["softmax_bf16_causal_32768x4096", "online_softmax_f32_64x1048576", "layernorm_gelu_bf16_65536x8192"]
+DOMINANT = "layernorm_gelu_bf16_65536x8192"
+KERNELS_PER_CALL = {"softmax": 1, "online_softmax": 2, "layernorm_gelu": 1}
+L2_BYTES = 129 * 10**6
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "ln_gelu_bf16_65536x8192.txt")
+DOMINANT_SOURCES = ["row_wise_reduction_gb300/csrc/ln_gelu_kernels.cuh",
+                    "row_wise_reduction_gb300/csrc/rowops_device.cuh",
+                    "row_wise_reduction_gb300/csrc/ln_gelu_inst.cuh"]
+
+
+def alg_bytes(wl: workloads.Workload) -> int:
+    es = workloads.elem_size(wl.dtype)
+    return 2 * wl.M * wl.N * es + (2 * wl.N * es if wl.affine else 0)
+
+
+def dominant_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in DOMINANT_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, if that summary was taken on the current kernel source."""
+    try:
+        kv = {}
+        with open(PROFILE_SUMMARY) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_sha") != dominant_source_hash():
+            return None
+        return int(float(kv["dram_bytes_per_launch"]))
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+def measured_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region: NVML through ctypes (read-only queries),
+# nvidia-smi as a fallback
+# ---------------------------------------------------------------------------
+REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+           0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+           0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+
+class ClockSampler:
+    def __init__(self, device: int, period_s: float = 0.005):
+        self.period = period_s
+        self.samples = []
+        self.max_mhz = None
+        self.src = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._smi = None
+        self._smi_out = None
+        self.uuid = None
+        try:
+            self.uuid = str(torch.cuda.get_device_properties(device).uuid)
+            if not self.uuid.startswith("GPU-"):
+                self.uuid = "GPU-" + self.uuid
+        except Exception:
+            self.uuid = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            h = ctypes.c_void_p()
+            if self.uuid is None or nv.nvmlDeviceGetHandleByUUID(self.uuid.encode(), ctypes.byref(h)) != 0:
+                raise OSError("no NVML handle")
+            v = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(v)) == 0:
+                self.max_mhz = v.value
+            self._nv, self._h = nv, h
+            self._reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.src = "nvml"
+        except Exception:
+            self._nv = None
+
+    def _poll(self):
+        nv, h = self._nv, self._h
+        clk, rs, pw = ctypes.c_uint(), ctypes.c_ulonglong(), ctypes.c_uint()
+        while not self._stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                r = rs.value if self._reasons(h, ctypes.byref(rs)) == 0 else 0
+                p = pw.value / 1000.0 if nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw)) == 0 else None
+                self.samples.append((clk.value, r, p))
+            time.sleep(self.period)
+
+    def start(self, csv_path=None):
+        if self._nv is not None:
+            self._thread = threading.Thread(target=self._poll, daemon=True)
+            self._thread.start()
+        if csv_path:
+            q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+            cmd = ["nvidia-smi", f"--query-gpu={q}", "--format=csv", "-lms", "200"]
+            if self.uuid:
+                cmd += ["-i", self.uuid]
+            try:
+                self._smi_out = open(csv_path, "w")
+                self._smi = subprocess.Popen(cmd, stdout=self._smi_out, stderr=subprocess.DEVNULL)
+            except OSError:
+                self._smi = None
+
+    def stop(self):
+        self._stop.set()
+        if self._thread:
+            self._thread.join()
+        if self._smi:
+            self._smi.terminate()
+            self._smi.wait()
+            self._smi_out.close()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0, "source": self.src}
+        mhz = [s[0] for s in self.samples]
+        bits = 0
+        for s in self.samples:
+            bits |= s[1]
+        reasons = [name for bit, name in REASONS.items() if bits & bit and name != "gpu_idle"]
+        power = [s[2] for s in self.samples if s[2] is not None]
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(mhz), "power_w_max": max(power) if power else None, "source": self.src}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU, launched by torchrun)
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(seconds: float, units: float, group=None):
+    """Max of the per-rank times and sum of the per-rank work over the process
+    group (identity without one)."""
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return seconds, units
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend(group) == "nccl" else "cpu"
+    t = torch.tensor([seconds], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM, group=group)
+    return float(t.item()), float(u.item())
+
+
+def barrier():
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle on a bounded sample
+# ---------------------------------------------------------------------------
+def oracle_run(oracle, wl, xs, extra):
+    if wl.op == "softmax":
+        oracle.softmax(xs)
+    elif wl.op == "online_softmax":
+        oracle.split_softmax(xs, extra["chunk"])
+    else:
+        oracle.layernorm_gelu(xs, extra["w"], extra["b"], wl.eps)
+
+
+def cpu_sample_rows(wl, rows, device=None, dev_inputs=None):
+    """fp32 host rows of ``wl`` (copied from the device inputs when given,
+    else drawn on the CPU with the causal mask of rows spread over the
+    workload) plus w, b."""
+    import numpy as np
+
+    if dev_inputs is not None:
+        idx = torch.as_tensor(rows, device=dev_inputs["x"].device)
+        xs = dev_inputs["x"][idx].float().cpu().numpy()
+        extra = {k: dev_inputs[k].float().cpu().numpy() for k in ("w", "b") if k in dev_inputs}
+    else:
+        inp = workloads.make_inputs(wl.with_shape(M=len(rows)), "cpu", row_ids=torch.as_tensor(rows))
+        xs = inp["x"].float().numpy()
+        extra = {k: inp[k].float().numpy() for k in ("w", "b") if k in inp}
+    extra.setdefault("w", None)
+    extra.setdefault("b", None)
+    extra["chunk"] = 8192
+    return np.ascontiguousarray(xs), extra
+
+
+def spread_rows(M, k):
+    if k >= M:
+        return list(range(M))
+    step = M / k
+    return [int(i * step) for i in range(k)]
+
+
+def cpu_baseline(oracle, dev_inputs=None, budget_s=12.0):
+    """Time the oracle on ~budget_s seconds of the step's workloads; return
+    GB/s on the same algorithmic-byte basis plus a description."""
+    total_bytes, total_s, desc = 0, 0.0, []
+    per_op = budget_s / len(STEP)
+    for name in STEP:
+        wl = workloads.WORKLOADS[name]
+        # calibrate on one row, then size the sample to the budget
+        xs, extra = cpu_sample_rows(wl, [wl.M // 2], dev_inputs=dev_inputs.get(name) if dev_inputs else None)
+        t0 = time.perf_counter()
+        oracle_run(oracle, wl, xs, extra)
+        dt = max(time.perf_counter() - t0, 1e-6)
+        k = max(1, min(wl.M, int(per_op / dt)))
+        rows = spread_rows(wl.M, k)
+        xs, extra = cpu_sample_rows(wl, rows, dev_inputs=dev_inputs.get(name) if dev_inputs else None)
+        t0 = time.perf_counter()
+        oracle_run(oracle, wl, xs, extra)
+        total_s += time.perf_counter() - t0
+        total_bytes += alg_bytes(wl.with_shape(M=len(rows)))
+        desc.append(f"{len(rows)} of {wl.M} rows of {name}")
+    return total_bytes / total_s / 1e9, "; ".join(desc), total_s
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle on host cores
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from oracle import oracle
+
+    oracle.build()
+    K, W = args.steps, args.warmup
+    per_step_s = max(0.3, min(3.0, args.reference_budget_s / max(1, K + W)))
+    # calibrate rows per op on one row each
+    samples = []
+    for name in STEP:
+        wl = workloads.WORKLOADS[name]
+        xs, extra = cpu_sample_rows(wl, [wl.M // 2])
+        t0 = time.perf_counter()
+        oracle_run(oracle, wl, xs, extra)
+        dt = max(time.perf_counter() - t0, 1e-6)
+        k = max(1, min(wl.M, int(per_step_s / len(STEP) / dt)))
+        rows = spread_rows(wl.M, k)
+        samples.append((wl, *cpu_sample_rows(wl, rows), len(rows)))
+    step_bytes = sum(alg_bytes(wl.with_shape(M=k)) for wl, _, _, k in samples)
+
+    def step():
+        for wl, xs, extra, _ in samples:
+            oracle_run(oracle, wl, xs, extra)
+
+    for _ in range(W):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(K):
+        step()
+    secs = time.perf_counter() - t0
+    value = step_bytes * K / secs / 1e9
+    sample = "; ".join(f"{k} of {wl.M} rows of {wl.name}" for wl, _, _, k in samples) + " per step"
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": secs / K * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": config_block(),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def config_block():
+    return {
+        "workload": " + ".join(STEP),
+        "per_step_bytes": {n: alg_bytes(workloads.WORKLOADS[n]) for n in STEP},
+        "l2": "no flush: every input (268 MB, 268 MB, 1074 MB) is larger than the 129 MB L2",
+        "bytes_basis": "algorithmic: each input element read once, each output element written once (+ w, b)",
+    }
+
+
+# ---------------------------------------------------------------------------
+# rowops arm
+# ---------------------------------------------------------------------------
+def run_rowops(args):
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "bench.py needs a CUDA GPU"}))
+        return 1
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    import row_wise_reduction_gb300 as ro
+
+    ro.library()
+    K, W = args.steps, args.warmup
+    keys = {"softmax": STEP[0], "online": STEP[1], "layernorm": STEP[2]}
+    names = [keys[o] for o in args.ops.split(",")] if args.ops else list(STEP)
+    wls = {n: workloads.WORKLOADS[n] for n in names}
+    if args.rows_scale != 1.0:
+        wls = {n: wl.with_shape(M=max(1, int(wl.M * args.rows_scale))) for n, wl in wls.items()}
+    inputs, outputs, ws = {}, {}, {}
+    for n, wl in wls.items():
+        inputs[n] = workloads.make_inputs(wl, dev)
+        outputs[n] = torch.empty_like(inputs[n]["x"])
+        if wl.op == "online_softmax":
+            nb = ro.rowops_online_softmax_workspace_bytes(wl.M, wl.N, workloads.torch_dtype(wl.dtype))
+            ws[n] = torch.empty(nb, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    def call(n, x, y):
+        wl = wls[n]
+        if wl.op == "softmax":
+            ro.rowops_softmax(x, y)
+        elif wl.op == "online_softmax":
+            ro.rowops_online_softmax(x, y, workspace=ws[n])
+        else:
+            ro.rowops_layernorm_gelu(x, inputs[n]["w"], inputs[n]["b"], wl.eps, y)
+
+    # warm-up
+    for _ in range(W):
+        for n in names:
+            call(n, inputs[n]["x"], outputs[n])
+    torch.cuda.synchronize()
+
+    # timed region: K steps, per-operation events on the launching stream
+    ev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+          for n in names}
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start(args.clocks_csv if rank == 0 else None)
+    t_start.record(stream)
+    for k in range(K):
+        for n in names:
+            a, b = ev[n][k]
+            a.record(stream)
+            call(n, inputs[n]["x"], outputs[n])
+            b.record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clocks.stop()
+    barrier()
+    secs = t_start.elapsed_time(t_end) / 1e3
+    step_bytes = sum(alg_bytes(wl) for wl in wls.values())
+    secs_max, total_bytes = aggregate(secs, step_bytes * K)
+    per_op = {}
+    for n in names:
+        ms = [a.elapsed_time(b) for a, b in ev[n]]
+        avg_s = statistics.fmean(ms) / 1e3
+        per_op[n] = {"avg_ms": avg_s * 1e3, "median_ms": statistics.median(ms), "min_ms": min(ms),
+                     "gbs": alg_bytes(wls[n]) / avg_s / 1e9}
+    peak, peak_kind = measured_peak()
+    for n in names:
+        per_op[n]["frac_of_" + peak_kind] = per_op[n]["gbs"] / peak
+    launches = K * sum(KERNELS_PER_CALL[wls[n].op] for n in names)
+
+    # end to end through the public API, host buffers: H2D inputs, kernels, D2H outputs
+    e2e = None
+    if not args.no_e2e:
+        host_in = {n: inputs[n]["x"].cpu().pin_memory() for n in names}
+        host_out = {n: torch.empty(outputs[n].shape, dtype=outputs[n].dtype).pin_memory() for n in names}
+        host_wb = {n: {k: inputs[n][k].cpu().pin_memory() for k in ("w", "b") if k in inputs[n]} for n in names}
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + \
+            sum(t.numel() * t.element_size() for d in host_wb.values() for t in d.values())
+        d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+        ke = max(2, min(K, args.e2e_steps))
+
+        def e2e_step():
+            for n in names:
+                for kk, t in host_wb[n].items():
+                    inputs[n][kk].copy_(t, non_blocking=True)
+                inputs[n]["x"].copy_(host_in[n], non_blocking=True)
+                call(n, inputs[n]["x"], outputs[n])
+                host_out[n].copy_(outputs[n], non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(ke):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        es, eb = aggregate(a.elapsed_time(b) / 1e3, step_bytes * ke)
+        e2e = {"value": eb / es / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": ke, "ms_per_step": es / ke * 1e3}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import oracle
+
+        oracle.build()
+        v, sample, spent = cpu_baseline(oracle, dev_inputs=inputs, budget_s=args.cpu_budget_s)
+        cpu = {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample,
+               "seconds": spent}
+
+    if rank != 0:
+        return 0
+    roof = None
+    if DOMINANT in per_op:
+        ach = per_op[DOMINANT]["gbs"]
+        roof = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+                "peak_kind": peak_kind, "kernel": "ln_gelu_reg_kernel<bf16, 256, 4, aligned>",
+                "traffic": profiled_traffic() if args.rows_scale == 1.0 else None,
+                "algorithmic_bytes_per_launch": alg_bytes(wls[DOMINANT])}
+    line = {
+        "metric": METRIC,
+        "value": total_bytes / secs_max / 1e9,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": secs_max / K * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": config_block() if args.rows_scale == 1.0 and not args.ops else
+        {"workload": " + ".join(f"{wl.name}[M={wl.M}]" for wl in wls.values())},
+        "roofline": roof,
+        "breakdown": per_op,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks.summary(),
+        "device": torch.cuda.get_device_name(dev),
+        "num_sms": torch.cuda.get_device_properties(dev).multi_processor_count,
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["rowops", "reference"], default="rowops")
+    ap.add_argument("--ops", default="", help="comma-separated subset of softmax,online,layernorm (profiling)")
+    ap.add_argument("--rows-scale", type=float, default=1.0, help="scale every workload's rows (profiling)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--reference-budget-s", type=float, default=90.0)
+    ap.add_argument("--clocks-csv", default=None, help="also log nvidia-smi clock samples to this CSV")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "rowops":
+        args.warmup = 3
+    return run_reference(args) if args.impl == "reference" else run_rowops(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,147 @@
+/*
+ * rowops: row-wise reduce-then-normalise kernels for one GB300 GPU (sm_103a).
+ *
+ * C ABI of librowops.so. Every operation works on an M x N row-major matrix
+ * whose rows start `ld` elements apart (ld >= N); x and y share ld. All
+ * pointers passed as x, y, w, b and workspace are DEVICE pointers owned by the
+ * caller; the library allocates nothing and keeps no state between calls
+ * except per-device caches of kernel attributes.
+ *
+ * Sources (lecture notes on CS336 Lecture 6, "Kernels, Triton"):
+ *   [L6]  "第 6 讲：GPU Kernels 与 Triton" (cs336.sjfarm.cc)
+ *   [KT]  "CS336 Kernels, Triton" notes (yiwen-cai.github.io)
+ *   [EX]  "Triton Kernel 实现练习" (lizn-zn.github.io)
+ *   [FUS] "PyTorch 自定义 CUDA 算子与 Triton 编程从 Python 原型到 GPU 极致性能" (ocdem.com)
+ *
+ * Common conventions
+ *   - Asynchronous and stream-ordered: a call validates its arguments, enqueues
+ *     its kernel(s) on `stream` (which must belong to the current device;
+ *     NULL is the legacy default stream) and returns without synchronising.
+ *   - Validation happens before any CUDA runtime call, so invalid arguments
+ *     return an error code and launch nothing. M == 0 is a no-op (ROWOPS_OK).
+ *   - x and y may be the same pointer (in place). Any other overlap between
+ *     the x and y row ranges is rejected with ROWOPS_ERR_INVALID_VALUE.
+ *   - Pointers must be aligned to their element size; 16-byte alignment of
+ *     rows (x, y 16-byte aligned and ld * element size a multiple of 16)
+ *     enables the fastest kernels, other alignments are handled by peeling
+ *     each row's unaligned head and tail.
+ *   - Accumulation is fp32 for both dtypes; bf16 results are rounded to
+ *     nearest even. Reductions use a fixed order, so repeated calls on the
+ *     same input give bitwise-identical output.
+ *   - Launch failures are reported as ROWOPS_ERR_CUDA (from cudaGetLastError
+ *     right after the launch). Errors that occur while a kernel runs surface
+ *     at the caller's next synchronisation, as for any CUDA kernel.
+ *   - Thread-safe; all entry points may be called from any host thread.
+ *
+ * Benchmarking knobs (environment, read at every call; unset = automatic):
+ *   ROWOPS_FORCE_TPR=<16..1024>   threads per row of the register-resident kernels
+ *   ROWOPS_FORCE_VPT=<1..4>       16-byte vectors per thread of those kernels
+ *   ROWOPS_FORCE_LOOPED=1         use the looped (any N) kernels
+ *   ROWOPS_CTAS_PER_SM=<k>        persistent grid of k CTAs per SM (0 = occupancy limit,
+ *                                 -1 = one CTA per row group, no persistence)
+ */
+#ifndef ROWOPS_H
+#define ROWOPS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum rowops_dtype {
+    ROWOPS_F32 = 0,  /* IEEE binary32 in and out */
+    ROWOPS_BF16 = 1, /* bfloat16 in and out, fp32 arithmetic inside */
+} rowops_dtype_t;
+
+typedef enum rowops_status {
+    ROWOPS_OK = 0,
+    ROWOPS_ERR_INVALID_VALUE = 1, /* null pointer, bad shape / stride / dtype, misaligned pointer, overlap */
+    ROWOPS_ERR_UNSUPPORTED = 2,   /* valid but outside what this build handles (e.g. N >= 2^31) */
+    ROWOPS_ERR_WORKSPACE = 3,     /* workspace missing, misaligned or smaller than the query says */
+    ROWOPS_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
+    ROWOPS_ERR_TIMEOUT = 5,       /* a device-side wait gave up (reported by the status query) */
+} rowops_status_t;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* rowops_status_string(rowops_status_t status);
+
+/*
+ * Stable softmax of every row [EX §2.4 Softmax; KT "Triton Softmax"]:
+ *   m = max_j x[r, j];  y[r, j] = exp(x[r, j] - m) / sum_k exp(x[r, k] - m)
+ * -inf entries (masked) produce exactly 0. A row whose entries are all -inf
+ * produces all zeros (the pages require an explicit convention, [EX §7]). A NaN
+ * anywhere in a row makes that row NaN.
+ *
+ *   x, y   device pointers to M rows of `ld` elements of `dtype`; y may equal x.
+ *   M      rows (>= 0); N columns (1 <= N < 2^31); ld row stride in elements (>= N).
+ * Rows of up to 16384 fp32 / 32768 bf16 entries are held in registers (one
+ * HBM read, one write); longer rows use an in-CTA online (m, d) loop that
+ * reads the row twice [L6 §7.2].
+ */
+rowops_status_t rowops_softmax(const void* x, void* y, int64_t M, int64_t N, int64_t ld,
+                               rowops_dtype_t dtype, cudaStream_t stream);
+
+/*
+ * Bytes of device workspace that rowops_online_softmax needs for an M x N
+ * problem (any chunk size the call accepts). Returns 0 for invalid arguments
+ * (M < 0, N < 1, bad dtype). Pure host arithmetic; no CUDA call.
+ */
+size_t rowops_online_softmax_workspace_bytes(int64_t M, int64_t N, rowops_dtype_t dtype);
+
+/*
+ * Split-row online softmax [EX §2.5 split_online_softmax; L6 §7.2]: each row is
+ * cut into chunks of `chunk` columns handled by different CTAs. A first pass
+ * computes every chunk's partial (m_c, d_c) = (max, sum exp(x - m_c)); a second
+ * pass merges a row's partials as
+ *   m = max_c m_c,   d = sum_c d_c * exp(m_c - m)      (chunks with d_c = 0 skipped)
+ * and writes y = exp(x - m) / d. Results equal rowops_softmax up to fp32
+ * rounding (independent of the chunk count up to rounding).
+ *
+ *   x, y, M, N, ld, dtype   as for rowops_softmax.
+ *   workspace   device pointer, 256-byte aligned, at least
+ *               rowops_online_softmax_workspace_bytes(M, N, dtype) bytes; the call
+ *               overwrites it. Calls that share a workspace must be ordered on
+ *               one stream.
+ *   chunk       columns per chunk: 0 picks one from N and the SM count; otherwise
+ *               a multiple of 16 in [256, 2^30]. Larger chunks than N are clamped.
+ */
+rowops_status_t rowops_online_softmax(const void* x, void* y, int64_t M, int64_t N, int64_t ld,
+                                      rowops_dtype_t dtype, void* workspace,
+                                      size_t workspace_bytes, int64_t chunk,
+                                      cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then reads the device-side status word that the last
+ * rowops_online_softmax call on `workspace` left: ROWOPS_OK, or
+ * ROWOPS_ERR_TIMEOUT if a bounded device-side wait gave up (the output of that
+ * call is then unspecified). ROWOPS_ERR_CUDA if the synchronisation or the
+ * read fails, ROWOPS_ERR_WORKSPACE for a NULL workspace.
+ */
+rowops_status_t rowops_online_softmax_status(const void* workspace, cudaStream_t stream);
+
+/*
+ * Fused LayerNorm -> affine -> tanh-approximation GELU of every row
+ * [FUS §三 _layer_norm_gelu_kernel; EX §4.1 LayerNorm; KT "Triton GeLU"]:
+ *   mean = sum_j x_j / N;  var = sum_j (x_j - mean)^2 / N      (biased)
+ *   z_j  = (x_j - mean) / sqrt(var + eps) * w_j + b_j
+ *   y_j  = 0.5 z_j (1 + tanh(0.79788456 (z_j + 0.044715 z_j^3)))
+ * The kernels evaluate the last line as z / (1 + exp(-2u)), which is the same
+ * function without the overflow of the pages' (e^{2u} - 1) / (e^{2u} + 1) form.
+ *
+ *   x, y   device pointers as for rowops_softmax; y may equal x.
+ *   w, b   device pointers to N entries of `dtype`, or NULL for weight 1 / bias 0
+ *          (the pages load absent entries with 1.0 and 0.0).
+ *   eps    added to the variance (the pages' default is 1e-5); must be >= 0 and finite.
+ */
+rowops_status_t rowops_layernorm_gelu(const void* x, void* y, const void* w, const void* b,
+                                      float eps, int64_t M, int64_t N, int64_t ld,
+                                      rowops_dtype_t dtype, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ROWOPS_H */

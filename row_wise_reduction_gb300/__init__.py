@@ -1,0 +1,19 @@
+"""rowops: row-wise reduce-then-normalise CUDA kernels for GB300 (sm_103a).
+
+Stable softmax, split-row online softmax and fused LayerNorm -> affine ->
+tanh-GELU, exposed through the C ABI of ``librowops.so`` (``include/rowops.h``)
+and the thin ctypes binding in :mod:`row_wise_reduction_gb300.rowops`.
+"""
+from .rowops import (  # noqa: F401
+    ROWOPS_BF16,
+    ROWOPS_F32,
+    RowopsError,
+    library,
+    library_path,
+    rowops_layernorm_gelu,
+    rowops_online_softmax,
+    rowops_online_softmax_status,
+    rowops_online_softmax_workspace_bytes,
+    rowops_softmax,
+    rowops_status_string,
+)

@@ -1,0 +1,251 @@
+// Fused LayerNorm -> affine -> tanh-approximation GELU kernels.
+//
+// Definition [PyTorch 自定义 CUDA 算子与 Triton 编程 §三 _layer_norm_gelu_kernel;
+// Triton Kernel 实现练习 §4.1 LayerNorm]: mean = sum(x)/N, var = sum((x-mean)^2)/N,
+// z = (x - mean) / sqrt(var + eps) * w + b, y = 0.5 z (1 + tanh(k0 (z + k1 z^3)))
+// with k0 = 0.79788456, k1 = 0.044715 [CS336 Kernels, Triton notes "Triton
+// GeLU"]. The row stays in registers between the two reductions (the variance
+// is taken over the centred values, padding excluded), so x is read from HBM
+// once; w and b are staged once per CTA in shared memory as fp32.
+#pragma once
+
+#include "rowops_device.cuh"
+
+namespace rowops {
+
+// 0.5 z (1 + tanh(u)) = z * sigmoid(2u) = z / (1 + exp(-2u)), u = k0 (z + k1 z^3).
+// exp(-2u) = 2^(z (c0 + c1 z^2)) with c0 = -2 k0 log2(e), c1 = c0 k1. For z -> -inf
+// the exponential overflows to +inf and the result is -0; for z -> +inf it is z.
+// This is the tanh form itself, rearranged so that nothing cancels or overflows
+// to NaN (the pages' (e^{2u} - 1) / (e^{2u} + 1) gives inf/inf for large u).
+__device__ __forceinline__ float gelu_tanh_approx(float z) {
+    constexpr float c0 = float(-2.0 * 0.79788456 * kLog2e);
+    constexpr float c1 = float(-2.0 * 0.79788456 * 0.044715 * kLog2e);
+    const float a = fmaf(c1, z * z, c0) * z;
+    return z * rcp_approx(1.f + ex2_approx(a));
+}
+
+// Shared-memory staging of w, b as fp32 (absent -> 1, 0). `sw` and `sb` hold
+// round_up(N, 4) floats each.
+template <typename T>
+__device__ __forceinline__ void stage_affine(const T* w, const T* b, int N, float* sw, float* sb) {
+    using E = Elem<T>;
+    for (int j = threadIdx.x; j < N; j += blockDim.x) {
+        sw[j] = w ? E::load(w + j) : 1.f;
+        sb[j] = b ? E::load(b + j) : 0.f;
+    }
+}
+
+__host__ __device__ constexpr int affine_pad(int n) { return (n + 3) & ~3; }
+
+// ALIGNED: every row starts on a 16-byte boundary (head = 0), so the columns of
+// a vector are a multiple of 4 and w, b are read from shared memory as float4.
+template <typename T, int TPR, int VPT, int BLOCK, bool ALIGNED>
+__global__ void __launch_bounds__(BLOCK)
+    ln_gelu_reg_kernel(const T* x, T* y, const T* w, const T* b, float eps, int64_t M, int N,
+                       int64_t ld) {
+    using E = Elem<T>;
+    constexpr int V = E::kVec;
+    constexpr int ROWS = BLOCK / TPR;
+    static_assert(BLOCK % TPR == 0 && TPR >= 16, "row group must be at least a half warp");
+    extern __shared__ float4 smem_affine[];
+    float* sw = reinterpret_cast<float*>(smem_affine);
+    float* sb = sw + affine_pad(N);
+    __shared__ float red_a[BLOCK / 32 > 0 ? BLOCK / 32 : 1];
+    __shared__ float red_b[BLOCK / 32 > 0 ? BLOCK / 32 : 1];
+
+    stage_affine(w, b, N, sw, sb);
+    __syncthreads();
+
+    const int t = threadIdx.x % TPR;
+    const int slot = threadIdx.x / TPR;
+    const int64_t ngroups = (M + ROWS - 1) / ROWS;
+    const float fN = float(N);
+
+    for (int64_t g = blockIdx.x; g < ngroups; g += gridDim.x) {
+        const int64_t row = g * ROWS + slot;
+        const bool live = row < M;
+        const T* xr = x + (live ? row : 0) * ld;
+        T* yr = y + (live ? row : 0) * ld;
+        RowGeom geo = row_geometry<T>(xr, N);
+        if (!live) geo = RowGeom{0, 0, 0};
+        const T* xv = xr + geo.head;
+        T* yv = yr + geo.head;
+
+        uint4 raw[VPT];
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            const int64_t k = t + int64_t(i) * TPR;
+            if (k < geo.nvec) raw[i] = ld_stream16(xv + k * V);
+        }
+        const bool has_ex = t < geo.extras();
+        const int ecol = has_ex ? int(extra_col(geo, t, V)) : 0;
+        float ex = has_ex ? E::load(xr + ecol) : 0.f;
+
+        // mean (padding contributes 0)
+        float v[VPT][V];
+        float s = ex;
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            const int64_t k = t + int64_t(i) * TPR;
+            if (k < geo.nvec) {
+                E::unpack(raw[i], v[i]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < V; ++j) v[i][j] = 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < V; ++j) s += v[i][j];
+        }
+        s = group_reduce<TPR>(s, red_a, OpSum());
+        const float mean = s / fN;
+
+        // variance of the centred values; padding stays out of it
+        float q = 0.f;
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            const int64_t k = t + int64_t(i) * TPR;
+            const bool ok = k < geo.nvec;
+#pragma unroll
+            for (int j = 0; j < V; ++j) {
+                v[i][j] = ok ? v[i][j] - mean : 0.f;
+                q = fmaf(v[i][j], v[i][j], q);
+            }
+        }
+        ex = has_ex ? ex - mean : 0.f;
+        q = fmaf(ex, ex, q);
+        q = group_reduce<TPR>(q, red_b, OpSum());
+        const float rstd = rsqrtf(q / fN + eps);
+
+        // affine + GELU + store
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            const int64_t k = t + int64_t(i) * TPR;
+            if (k < geo.nvec) {
+                const int c0 = geo.head + int(k) * V;
+                float o[V];
+                if constexpr (ALIGNED) {
+#pragma unroll
+                    for (int j = 0; j < V; j += 4) {
+                        const float4 ww = *reinterpret_cast<const float4*>(sw + c0 + j);
+                        const float4 bb = *reinterpret_cast<const float4*>(sb + c0 + j);
+                        o[j + 0] = gelu_tanh_approx(fmaf(v[i][j + 0] * rstd, ww.x, bb.x));
+                        o[j + 1] = gelu_tanh_approx(fmaf(v[i][j + 1] * rstd, ww.y, bb.y));
+                        o[j + 2] = gelu_tanh_approx(fmaf(v[i][j + 2] * rstd, ww.z, bb.z));
+                        o[j + 3] = gelu_tanh_approx(fmaf(v[i][j + 3] * rstd, ww.w, bb.w));
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < V; ++j)
+                        o[j] = gelu_tanh_approx(fmaf(v[i][j] * rstd, sw[c0 + j], sb[c0 + j]));
+                }
+                st_stream16(yv + k * V, E::pack(o));
+            }
+        }
+        if (has_ex) E::store(yr + ecol, gelu_tanh_approx(fmaf(ex * rstd, sw[ecol], sb[ecol])));
+    }
+}
+
+// One CTA per row, any N. Pass 1: shifted sums around the row's first entry,
+// S1 = sum(x - x0), S2 = sum((x - x0)^2), so mean = x0 + S1/N and
+// var = S2/N - (S1/N)^2 without cancellation for rows whose mean is far from 0.
+// Pass 2 re-reads x and writes y; w and b come from global memory (L1/L2).
+// `scalar`: x and y rows differ in their offset modulo 16 bytes; one element
+// at a time.
+template <typename T, int BLOCK, int UNROLL>
+__global__ void __launch_bounds__(BLOCK)
+    ln_gelu_looped_kernel(const T* x, T* y, const T* w, const T* b, float eps, int64_t M, int64_t N,
+                          int64_t ld, bool scalar) {
+    using E = Elem<T>;
+    constexpr int V = E::kVec;
+    __shared__ float red_a[2][BLOCK / 32];
+    __shared__ float red_b[2][BLOCK / 32];
+    const int t = threadIdx.x;
+    int parity = 0;
+    const float fN = float(N);
+
+    for (int64_t row = blockIdx.x; row < M; row += gridDim.x, parity ^= 1) {
+        const T* xr = x + row * ld;
+        T* yr = y + row * ld;
+        const RowGeom geo = scalar ? RowGeom{0, 0, 0} : row_geometry<T>(xr, N);
+        const T* xv = xr + geo.head;
+        T* yv = yr + geo.head;
+        const float x0 = E::load(xr);
+
+        float s1 = 0.f, s2 = 0.f;
+        if (scalar) {
+            for (int64_t c = t; c < N; c += BLOCK) {
+                const float d = E::load(xr + c) - x0;
+                s1 += d;
+                s2 = fmaf(d, d, s2);
+            }
+        }
+        if (t < geo.extras()) {
+            const float d = E::load(xr + extra_col(geo, t, V)) - x0;
+            s1 += d;
+            s2 = fmaf(d, d, s2);
+        }
+        for (int64_t k0 = t; k0 < geo.nvec; k0 += int64_t(BLOCK) * UNROLL) {
+            uint4 raw[UNROLL];
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+                const int64_t k = k0 + int64_t(u) * BLOCK;
+                if (k < geo.nvec) raw[u] = ld_stream16(xv + k * V);
+            }
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+                const int64_t k = k0 + int64_t(u) * BLOCK;
+                if (k < geo.nvec) {
+                    float f[V];
+                    E::unpack(raw[u], f);
+#pragma unroll
+                    for (int j = 0; j < V; ++j) {
+                        const float d = f[j] - x0;
+                        s1 += d;
+                        s2 = fmaf(d, d, s2);
+                    }
+                }
+            }
+        }
+        s1 = group_reduce<BLOCK>(s1, red_a[parity], OpSum());
+        s2 = group_reduce<BLOCK>(s2, red_b[parity], OpSum());
+        const float m1 = s1 / fN;
+        const float mean = x0 + m1;
+        const float var = fmaxf(s2 / fN - m1 * m1, 0.f);
+        const float rstd = rsqrtf(var + eps);
+
+        auto affine_gelu = [&](float xv_, int64_t c) {
+            const float wj = w ? E::load(w + c) : 1.f;
+            const float bj = b ? E::load(b + c) : 0.f;
+            return gelu_tanh_approx(fmaf((xv_ - mean) * rstd, wj, bj));
+        };
+        if (scalar)
+            for (int64_t c = t; c < N; c += BLOCK) E::store(yr + c, affine_gelu(E::load(xr + c), c));
+        if (t < geo.extras()) {
+            const int64_t c = extra_col(geo, t, V);
+            E::store(yr + c, affine_gelu(E::load(xr + c), c));
+        }
+        for (int64_t k0 = t; k0 < geo.nvec; k0 += int64_t(BLOCK) * UNROLL) {
+            uint4 raw[UNROLL];
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+                const int64_t k = k0 + int64_t(u) * BLOCK;
+                if (k < geo.nvec) raw[u] = ld_stream16(xv + k * V);
+            }
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+                const int64_t k = k0 + int64_t(u) * BLOCK;
+                if (k < geo.nvec) {
+                    float f[V];
+                    E::unpack(raw[u], f);
+                    const int64_t c0 = geo.head + k * V;
+#pragma unroll
+                    for (int j = 0; j < V; ++j) f[j] = affine_gelu(f[j], c0 + j);
+                    st_stream16(yv + k * V, E::pack(f));
+                }
+            }
+        }
+    }
+}
+
+}  // namespace rowops

@@ -1,0 +1,313 @@
+// C ABI of librowops.so: argument validation, kernel selection and launch.
+// The operations themselves are documented in include/rowops.h.
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "rowops.h"
+#include "rowops_launch.h"
+
+namespace rowops {
+namespace {
+
+int elem_bytes(rowops_dtype_t dt) { return dt == ROWOPS_F32 ? 4 : 2; }
+
+bool valid_dtype(rowops_dtype_t dt) { return dt == ROWOPS_F32 || dt == ROWOPS_BF16; }
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Benchmarking knobs, read at every call (see include/rowops.h).
+struct Tuning {
+    int tpr = 0;
+    int vpt = 0;
+    bool looped = false;
+    int ctas_per_sm = 0;
+};
+
+int env_int(const char* name, int dflt) {
+    const char* v = std::getenv(name);
+    if (!v || !*v) return dflt;
+    char* end = nullptr;
+    const long r = std::strtol(v, &end, 10);
+    return (end && *end == '\0') ? int(r) : dflt;
+}
+
+Tuning read_tuning() {
+    Tuning t;
+    t.tpr = env_int("ROWOPS_FORCE_TPR", 0);
+    t.vpt = env_int("ROWOPS_FORCE_VPT", 0);
+    t.looped = env_int("ROWOPS_FORCE_LOOPED", 0) != 0;
+    t.ctas_per_sm = env_int("ROWOPS_CTAS_PER_SM", 0);
+    return t;
+}
+
+// Checks shared by every entry point. M == 0 passes (callers then return).
+rowops_status_t check_rows(const void* x, const void* y, int64_t M, int64_t N, int64_t ld,
+                           rowops_dtype_t dt) {
+    if (!valid_dtype(dt) || M < 0 || N < 1 || ld < N) return ROWOPS_ERR_INVALID_VALUE;
+    if (N >= (int64_t(1) << 31)) return ROWOPS_ERR_UNSUPPORTED;
+    if (M == 0) return ROWOPS_OK;
+    if (!x || !y) return ROWOPS_ERR_INVALID_VALUE;
+    const int es = elem_bytes(dt);
+    if (!aligned(x, es) || !aligned(y, es)) return ROWOPS_ERR_INVALID_VALUE;
+    // elements spanned, (M - 1) * ld + N, must fit in int64 bytes
+    const int64_t lim = INT64_MAX / es - N;
+    if (M - 1 > lim / ld) return ROWOPS_ERR_UNSUPPORTED;
+    if (x != y) {
+        const uintptr_t span = uintptr_t(((M - 1) * ld + N) * es);
+        const uintptr_t a = reinterpret_cast<uintptr_t>(x), b = reinterpret_cast<uintptr_t>(y);
+        if (a < b + span && b < a + span) return ROWOPS_ERR_INVALID_VALUE;  // partial overlap
+    }
+    return ROWOPS_OK;
+}
+
+// ---- per-device attributes and per-kernel caches ---------------------------
+struct DeviceInfo {
+    int num_sms = 0;
+    int max_smem_optin = 0;
+};
+
+std::mutex g_mu;
+std::vector<std::pair<int, DeviceInfo>> g_devices;
+
+struct OccEntry {
+    const void* func;
+    int device, block;
+    size_t smem;
+    int blocks_per_sm;
+};
+std::vector<OccEntry> g_occ;
+
+struct SmemEntry {
+    const void* func;
+    int device;
+    size_t smem;
+};
+std::vector<SmemEntry> g_smem;
+
+cudaError_t device_info(int dev, DeviceInfo* out) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (auto& d : g_devices)
+        if (d.first == dev) {
+            *out = d.second;
+            return cudaSuccess;
+        }
+    DeviceInfo di;
+    cudaError_t e = cudaDeviceGetAttribute(&di.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&di.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    g_devices.emplace_back(dev, di);
+    *out = di;
+    return cudaSuccess;
+}
+
+rowops_status_t make_cfg(cudaStream_t stream, const Tuning& tn, LaunchCfg* cfg) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ROWOPS_ERR_CUDA;
+    DeviceInfo di;
+    if (device_info(dev, &di) != cudaSuccess) return ROWOPS_ERR_CUDA;
+    cfg->stream = stream;
+    cfg->device = dev;
+    cfg->num_sms = di.num_sms;
+    cfg->max_smem_optin = di.max_smem_optin;
+    cfg->ctas_per_sm = tn.ctas_per_sm;
+    return ROWOPS_OK;
+}
+
+rowops_status_t finish(cudaError_t e) {
+    if (e != cudaSuccess) {
+        cudaGetLastError();  // the failure is reported through the status; clear it
+        return ROWOPS_ERR_CUDA;
+    }
+    return ROWOPS_OK;
+}
+
+// Register-resident kernel choice: the smallest row group (threads per row)
+// that holds floor(N / vec) 16-byte vectors with at most kMaxVpt per thread.
+// The unaligned head and tail (< 2 vec elements) go one per thread, and
+// every group has at least 16 threads, which covers them.
+bool choose_reg(int64_t N, int es, const Tuning& tn, int* tpr_index, int* vpt) {
+    const int64_t vec = 16 / es;
+    const int64_t nvec = N / vec;
+    if (tn.tpr) {
+        int idx = -1;
+        for (int i = 0; i < kNumTpr; ++i)
+            if (kTprChoices[i] == tn.tpr) idx = i;
+        if (idx < 0) return false;
+        const int64_t need = (nvec + tn.tpr - 1) / tn.tpr;
+        const int v = tn.vpt ? tn.vpt : int(need < 1 ? 1 : need);
+        if (v < 1 || v > kMaxVpt || int64_t(v) * tn.tpr < nvec) return false;
+        *tpr_index = idx;
+        *vpt = v;
+        return true;
+    }
+    for (int i = 0; i < kNumTpr; ++i) {
+        const int64_t tpr = kTprChoices[i];
+        if (tpr * kMaxVpt >= nvec) {
+            const int64_t need = (nvec + tpr - 1) / tpr;
+            *tpr_index = i;
+            *vpt = int(need < 1 ? 1 : need);
+            return true;
+        }
+    }
+    return false;
+}
+
+bool same_phase(const void* x, const void* y) {
+    return ((reinterpret_cast<uintptr_t>(x) - reinterpret_cast<uintptr_t>(y)) & 15u) == 0;
+}
+
+// all rows of x (and, being in phase, of y) start on 16-byte boundaries
+bool rows_aligned(const void* x, const void* y, int64_t ld, int es) {
+    return aligned(x, 16) && aligned(y, 16) && ((ld * es) % 16) == 0;
+}
+
+constexpr int64_t kMinChunk = 256;
+
+}  // namespace
+
+int grid_for(const void* func, int block, size_t smem, int64_t items, const LaunchCfg& cfg) {
+    int64_t cap;
+    if (cfg.ctas_per_sm < 0) {
+        cap = items;
+    } else {
+        int per_sm = cfg.ctas_per_sm;
+        if (per_sm == 0) {
+            std::lock_guard<std::mutex> lk(g_mu);
+            for (auto& o : g_occ)
+                if (o.func == func && o.device == cfg.device && o.block == block && o.smem == smem)
+                    per_sm = o.blocks_per_sm;
+            if (per_sm == 0) {
+                int n = 0;
+                if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, func, block, smem) != cudaSuccess ||
+                    n < 1)
+                    n = 1;
+                g_occ.push_back(OccEntry{func, cfg.device, block, smem, n});
+                per_sm = n;
+            }
+        }
+        cap = int64_t(per_sm) * cfg.num_sms;
+    }
+    int64_t g = items < cap ? items : cap;
+    if (g < 1) g = 1;
+    if (g > 0x7fffffff) g = 0x7fffffff;
+    return int(g);
+}
+
+cudaError_t allow_smem(const void* func, size_t smem, const LaunchCfg& cfg) {
+    if (smem <= 48 * 1024) return cudaSuccess;
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (auto& s : g_smem)
+        if (s.func == func && s.device == cfg.device && s.smem >= smem) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e == cudaSuccess) g_smem.push_back(SmemEntry{func, cfg.device, smem});
+    return e;
+}
+
+}  // namespace rowops
+
+using namespace rowops;
+
+extern "C" {
+
+const char* rowops_status_string(rowops_status_t status) {
+    switch (status) {
+        case ROWOPS_OK: return "ROWOPS_OK";
+        case ROWOPS_ERR_INVALID_VALUE: return "ROWOPS_ERR_INVALID_VALUE";
+        case ROWOPS_ERR_UNSUPPORTED: return "ROWOPS_ERR_UNSUPPORTED";
+        case ROWOPS_ERR_WORKSPACE: return "ROWOPS_ERR_WORKSPACE";
+        case ROWOPS_ERR_CUDA: return "ROWOPS_ERR_CUDA";
+        case ROWOPS_ERR_TIMEOUT: return "ROWOPS_ERR_TIMEOUT";
+    }
+    return "ROWOPS_ERR_UNKNOWN";
+}
+
+rowops_status_t rowops_softmax(const void* x, void* y, int64_t M, int64_t N, int64_t ld,
+                               rowops_dtype_t dtype, cudaStream_t stream) {
+    rowops_status_t st = check_rows(x, y, M, N, ld, dtype);
+    if (st != ROWOPS_OK || M == 0) return st;
+    const Tuning tn = read_tuning();
+    LaunchCfg cfg;
+    if ((st = make_cfg(stream, tn, &cfg)) != ROWOPS_OK) return st;
+    const int es = elem_bytes(dtype);
+    int tpr_index = 0, vpt = 0;
+    SoftmaxLaunch fn = nullptr;
+    if (!tn.looped && same_phase(x, y) && choose_reg(N, es, tn, &tpr_index, &vpt))
+        fn = dtype == ROWOPS_F32 ? softmax_reg_f32(tpr_index, vpt) : softmax_reg_bf16(tpr_index, vpt);
+    if (!fn) fn = dtype == ROWOPS_F32 ? softmax_looped_f32() : softmax_looped_bf16();
+    return finish(fn(x, y, M, N, ld, cfg));
+}
+
+rowops_status_t rowops_layernorm_gelu(const void* x, void* y, const void* w, const void* b,
+                                      float eps, int64_t M, int64_t N, int64_t ld,
+                                      rowops_dtype_t dtype, cudaStream_t stream) {
+    rowops_status_t st = check_rows(x, y, M, N, ld, dtype);
+    if (st != ROWOPS_OK) return st;
+    if (!(eps >= 0.f) || eps == INFINITY) return ROWOPS_ERR_INVALID_VALUE;
+    if (M == 0) return ROWOPS_OK;
+    const int es = elem_bytes(dtype);
+    if ((w && !aligned(w, es)) || (b && !aligned(b, es))) return ROWOPS_ERR_INVALID_VALUE;
+    const Tuning tn = read_tuning();
+    LaunchCfg cfg;
+    if ((st = make_cfg(stream, tn, &cfg)) != ROWOPS_OK) return st;
+    int tpr_index = 0, vpt = 0;
+    LnGeluLaunch fn = nullptr;
+    // static shared memory of the kernel (reduction buffers) stays under 256 bytes
+    const bool smem_ok = ln_gelu_smem_bytes(N) + 256 <= size_t(cfg.max_smem_optin);
+    if (!tn.looped && smem_ok && same_phase(x, y) && choose_reg(N, es, tn, &tpr_index, &vpt)) {
+        const bool al = rows_aligned(x, y, ld, es);
+        fn = dtype == ROWOPS_F32 ? ln_gelu_reg_f32(tpr_index, vpt, al) : ln_gelu_reg_bf16(tpr_index, vpt, al);
+    }
+    if (!fn) fn = dtype == ROWOPS_F32 ? ln_gelu_looped_f32() : ln_gelu_looped_bf16();
+    return finish(fn(x, y, w, b, eps, M, N, ld, cfg));
+}
+
+size_t rowops_online_softmax_workspace_bytes(int64_t M, int64_t N, rowops_dtype_t dtype) {
+    if (!valid_dtype(dtype) || M < 0 || N < 1 || N >= (int64_t(1) << 31)) return 0;
+    const int64_t max_chunks = (N + kMinChunk - 1) / kMinChunk;
+    if (M > 0 && max_chunks > (INT64_MAX / 16) / M) return 0;
+    return size_t(256) + size_t(M) * size_t(max_chunks) * 8u;
+}
+
+rowops_status_t rowops_online_softmax(const void* x, void* y, int64_t M, int64_t N, int64_t ld,
+                                      rowops_dtype_t dtype, void* workspace,
+                                      size_t workspace_bytes, int64_t chunk,
+                                      cudaStream_t stream) {
+    rowops_status_t st = check_rows(x, y, M, N, ld, dtype);
+    if (st != ROWOPS_OK) return st;
+    if (chunk != 0 && (chunk < kMinChunk || chunk > (int64_t(1) << 30) || chunk % 16 != 0))
+        return ROWOPS_ERR_INVALID_VALUE;
+    if (M == 0) return ROWOPS_OK;
+    if (!workspace || !aligned(workspace, 256) ||
+        workspace_bytes < rowops_online_softmax_workspace_bytes(M, N, dtype))
+        return ROWOPS_ERR_WORKSPACE;
+    const Tuning tn = read_tuning();
+    LaunchCfg cfg;
+    if ((st = make_cfg(stream, tn, &cfg)) != ROWOPS_OK) return st;
+    const int es = elem_bytes(dtype);
+    const int64_t n16 = (N + 15) / 16 * 16;
+    if (chunk == 0) {
+        // one unrolled step of a CTA per chunk, smaller while there are fewer
+        // than four chunks per SM, never below the minimum
+        chunk = split_step_cols(es);
+        while (chunk > kMinChunk && M * ((N + chunk - 1) / chunk) < int64_t(4) * cfg.num_sms) chunk /= 2;
+    }
+    if (chunk > n16) chunk = n16 < kMinChunk ? kMinChunk : n16;
+    const int64_t nchunks = (N + chunk - 1) / chunk;
+    SplitLaunch fn = dtype == ROWOPS_F32 ? split_softmax_f32() : split_softmax_bf16();
+    return finish(fn(x, y, M, N, ld, chunk, nchunks, workspace, cfg));
+}
+
+rowops_status_t rowops_online_softmax_status(const void* workspace, cudaStream_t stream) {
+    if (!workspace) return ROWOPS_ERR_WORKSPACE;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return finish(cudaErrorUnknown);
+    unsigned word = 0;
+    if (cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return finish(cudaErrorUnknown);
+    if (word == 0u) return ROWOPS_OK;
+    return word == unsigned(ROWOPS_ERR_TIMEOUT) ? ROWOPS_ERR_TIMEOUT : ROWOPS_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,209 @@
+"""Python binding of librowops.so (argument marshalling only).
+
+Each function has the name of the C entry point it calls and does no
+arithmetic of its own: it checks shapes, takes device pointers, the row stride
+and the current CUDA stream from torch tensors, calls the C ABI through
+ctypes and raises :class:`RowopsError` on a non-OK status. PyTorch only
+supplies device memory and streams. There is no CPU fallback: if the library
+is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from .build import LIB as _LIB_PATH
+
+__all__ = [
+    "RowopsError",
+    "library",
+    "library_path",
+    "rowops_softmax",
+    "rowops_online_softmax",
+    "rowops_online_softmax_workspace_bytes",
+    "rowops_online_softmax_status",
+    "rowops_layernorm_gelu",
+    "rowops_status_string",
+    "ROWOPS_F32",
+    "ROWOPS_BF16",
+    "STATUS",
+]
+
+ROWOPS_F32 = 0
+ROWOPS_BF16 = 1
+STATUS = {
+    0: "ROWOPS_OK",
+    1: "ROWOPS_ERR_INVALID_VALUE",
+    2: "ROWOPS_ERR_UNSUPPORTED",
+    3: "ROWOPS_ERR_WORKSPACE",
+    4: "ROWOPS_ERR_CUDA",
+    5: "ROWOPS_ERR_TIMEOUT",
+}
+
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+
+
+class RowopsError(RuntimeError):
+    """A rowops entry point returned a status other than ROWOPS_OK."""
+
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} returned {STATUS.get(status, status)}")
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def library() -> ctypes.CDLL:
+    """Load librowops.so (built in-tree by ``row_wise_reduction_gb300.build``)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"{_LIB_PATH} is missing: build it with `python -m row_wise_reduction_gb300.build` "
+                "(there is no fallback implementation)"
+            )
+        L = ctypes.CDLL(_LIB_PATH)
+        L.rowops_status_string.restype = ctypes.c_char_p
+        L.rowops_status_string.argtypes = [ctypes.c_int]
+        L.rowops_softmax.restype = ctypes.c_int
+        L.rowops_softmax.argtypes = [_vp, _vp, _i64, _i64, _i64, ctypes.c_int, _vp]
+        L.rowops_online_softmax_workspace_bytes.restype = ctypes.c_size_t
+        L.rowops_online_softmax_workspace_bytes.argtypes = [_i64, _i64, ctypes.c_int]
+        L.rowops_online_softmax.restype = ctypes.c_int
+        L.rowops_online_softmax.argtypes = [_vp, _vp, _i64, _i64, _i64, ctypes.c_int, _vp, ctypes.c_size_t,
+                                            _i64, _vp]
+        L.rowops_online_softmax_status.restype = ctypes.c_int
+        L.rowops_online_softmax_status.argtypes = [_vp, _vp]
+        L.rowops_layernorm_gelu.restype = ctypes.c_int
+        L.rowops_layernorm_gelu.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, _i64, _i64, _i64,
+                                            ctypes.c_int, _vp]
+        _lib = L
+    return _lib
+
+
+def rowops_status_string(status: int) -> str:
+    return library().rowops_status_string(int(status)).decode()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return ROWOPS_F32
+    if t.dtype == torch.bfloat16:
+        return ROWOPS_BF16
+    raise TypeError(f"rowops supports float32 and bfloat16, not {t.dtype}")
+
+
+def _rows(t: torch.Tensor, name: str):
+    """(M, N, ld) of a 2-D CUDA tensor with unit column stride."""
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D (M, N)")
+    M, N = t.shape
+    if N > 0 and t.stride(1) != 1:
+        raise ValueError(f"{name} must have unit column stride")
+    ld = t.stride(0) if M > 1 else max(N, t.stride(0))
+    return M, N, ld
+
+
+def _out_like(x: torch.Tensor, y: Optional[torch.Tensor]) -> torch.Tensor:
+    if y is None:
+        return torch.empty_strided(x.shape, x.stride(), dtype=x.dtype, device=x.device)
+    if y.shape != x.shape or y.dtype != x.dtype or y.device != x.device:
+        raise ValueError("y must match x in shape, dtype and device")
+    if y.shape[0] > 1 and y.stride() != x.stride():
+        raise ValueError("x and y must share the row stride")
+    return y
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise RowopsError(fn, status)
+
+
+def rowops_softmax(x: torch.Tensor, y: Optional[torch.Tensor] = None, *, stream=None) -> torch.Tensor:
+    """Stable softmax of every row of ``x`` (M, N) into ``y`` (may be ``x``)."""
+    M, N, ld = _rows(x, "x")
+    y = _out_like(x, y)
+    st = library().rowops_softmax(x.data_ptr(), y.data_ptr(), M, N, ld, _dtype_code(x), _stream(stream))
+    _check("rowops_softmax", st)
+    return y
+
+
+def rowops_online_softmax_workspace_bytes(M: int, N: int, dtype: torch.dtype) -> int:
+    code = ROWOPS_F32 if dtype == torch.float32 else ROWOPS_BF16 if dtype == torch.bfloat16 else -1
+    return int(library().rowops_online_softmax_workspace_bytes(int(M), int(N), code))
+
+
+def rowops_online_softmax(
+    x: torch.Tensor,
+    y: Optional[torch.Tensor] = None,
+    *,
+    workspace: Optional[torch.Tensor] = None,
+    chunk: int = 0,
+    stream=None,
+) -> torch.Tensor:
+    """Split-row online softmax of every row of ``x``.
+
+    ``workspace``: a CUDA uint8 tensor of at least
+    ``rowops_online_softmax_workspace_bytes(M, N, dtype)`` bytes; allocated
+    here when omitted. ``chunk``: columns per CTA chunk (0 = automatic).
+    """
+    M, N, ld = _rows(x, "x")
+    y = _out_like(x, y)
+    need = rowops_online_softmax_workspace_bytes(M, N, x.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
+    if not workspace.is_cuda:
+        raise ValueError("workspace must be a CUDA tensor")
+    nbytes = workspace.numel() * workspace.element_size()
+    st = library().rowops_online_softmax(x.data_ptr(), y.data_ptr(), M, N, ld, _dtype_code(x),
+                                         workspace.data_ptr(), nbytes, int(chunk), _stream(stream))
+    _check("rowops_online_softmax", st)
+    return y
+
+
+def rowops_online_softmax_status(workspace: torch.Tensor, *, stream=None) -> int:
+    """Synchronise the stream and return the device-side status of the last
+    rowops_online_softmax call on ``workspace`` (0 = ROWOPS_OK)."""
+    return int(library().rowops_online_softmax_status(workspace.data_ptr(), _stream(stream)))
+
+
+def rowops_layernorm_gelu(
+    x: torch.Tensor,
+    w: Optional[torch.Tensor] = None,
+    b: Optional[torch.Tensor] = None,
+    eps: float = 1e-5,
+    y: Optional[torch.Tensor] = None,
+    *,
+    stream=None,
+) -> torch.Tensor:
+    """Fused LayerNorm -> affine -> tanh-GELU of every row of ``x``."""
+    M, N, ld = _rows(x, "x")
+    y = _out_like(x, y)
+    for name, v in (("w", w), ("b", b)):
+        if v is not None:
+            if v.dtype != x.dtype or v.device != x.device or v.numel() != N or not v.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous CUDA tensor of N entries with x's dtype")
+    st = library().rowops_layernorm_gelu(
+        x.data_ptr(), y.data_ptr(), w.data_ptr() if w is not None else None,
+        b.data_ptr() if b is not None else None, float(eps), M, N, ld, _dtype_code(x), _stream(stream))
+    _check("rowops_layernorm_gelu", st)
+    return y

@@ -76,6 +76,7 @@ def make_inputs(
     wl: Workload,
     device: str | torch.device = "cpu",
     ld: Optional[int] = None,
+    row_ids: Optional[torch.Tensor] = None,
 ) -> Dict[str, torch.Tensor]:
     """Draw the inputs of ``wl`` on ``device``.
 
@@ -83,7 +84,9 @@ def make_inputs(
     LayerNorm workloads, ``"w"`` and ``"b"`` of length N. Values are drawn in
     fp32 and rounded to the workload's dtype (round to nearest even). With
     ``ld > N`` the padding columns of each row hold NaN so that any read past
-    column N-1 shows up in the result.
+    column N-1 shows up in the result. ``row_ids`` (M integers) gives the row
+    index each generated row stands for in the causal mask pattern, so that a
+    small sample can carry the mask of rows spread over a large workload.
     """
     device = torch.device(device)
     M, N = wl.M, wl.N
@@ -101,7 +104,8 @@ def make_inputs(
         del hit
     if wl.causal:
         cols = torch.arange(N, device=device).unsqueeze(0)
-        keep = (torch.arange(M, device=device) % N).unsqueeze(1)
+        ids = torch.arange(M, device=device) if row_ids is None else torch.as_tensor(row_ids, device=device)
+        keep = (ids % N).unsqueeze(1)
         x.masked_fill_(cols > keep, float("-inf"))
     storage = torch.full((M, ld), float("nan"), device=device, dtype=dt)
     storage[:, :N] = x.to(dt)

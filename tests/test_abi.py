@@ -1,0 +1,121 @@
+"""C ABI checks that need no GPU: the library loads, exports every entry point
+include/rowops.h declares, and rejects invalid arguments with the documented
+status before any CUDA call (so these calls launch nothing)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rowops.h")
+
+OK, INVALID, UNSUPPORTED, WORKSPACE = 0, 1, 2, 3
+F32, BF16 = 0, 1
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from row_wise_reduction_gb300 import build
+    from row_wise_reduction_gb300.rowops import library
+
+    build.build()
+    return library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rowops_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("rowops_softmax", "rowops_online_softmax", "rowops_layernorm_gelu",
+              "rowops_online_softmax_workspace_bytes", "rowops_online_softmax_status", "rowops_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(lib._name)
+    for name in declared_functions():
+        assert hasattr(raw, name), f"{name} declared in rowops.h but not exported"
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "ROWOPS_OK"), (1, "ROWOPS_ERR_INVALID_VALUE"), (2, "ROWOPS_ERR_UNSUPPORTED"),
+                       (3, "ROWOPS_ERR_WORKSPACE"), (4, "ROWOPS_ERR_CUDA"), (5, "ROWOPS_ERR_TIMEOUT")]:
+        assert lib.rowops_status_string(code).decode() == name
+    assert lib.rowops_status_string(99).decode() == "ROWOPS_ERR_UNKNOWN"
+
+
+X = 0x10000  # fake device addresses: validation fails before any use
+Y = 0x90000
+
+
+@pytest.mark.parametrize(
+    "args,want",
+    [
+        ((X, Y, 4, 8, 8, 7, None), INVALID),  # bad dtype
+        ((X, Y, -1, 8, 8, F32, None), INVALID),  # M < 0
+        ((X, Y, 4, 0, 8, F32, None), INVALID),  # N < 1
+        ((X, Y, 4, 8, 7, F32, None), INVALID),  # ld < N
+        ((None, Y, 4, 8, 8, F32, None), INVALID),  # null x
+        ((X, None, 4, 8, 8, F32, None), INVALID),  # null y
+        ((X + 2, Y, 4, 8, 8, F32, None), INVALID),  # x not 4-byte aligned for fp32
+        ((X, Y + 1, 4, 8, 8, BF16, None), INVALID),  # y not 2-byte aligned for bf16
+        ((X, X + 16, 4, 8, 8, F32, None), INVALID),  # partial overlap
+        ((X, Y, 4, 1 << 31, 1 << 31, F32, None), UNSUPPORTED),  # N too large
+        ((X, Y, 1 << 62, 8, 1 << 40, F32, None), UNSUPPORTED),  # byte span overflows int64
+        ((None, None, 0, 8, 8, F32, None), OK),  # M == 0: no-op, no CUDA call
+    ],
+)
+def test_softmax_validation(lib, args, want):
+    assert lib.rowops_softmax(*args) == want
+
+
+def test_layernorm_gelu_validation(lib):
+    f = lib.rowops_layernorm_gelu
+    assert f(X, Y, None, None, -1.0, 4, 8, 8, F32, None) == INVALID  # eps < 0
+    assert f(X, Y, None, None, float("nan"), 4, 8, 8, F32, None) == INVALID
+    assert f(X, Y, None, None, float("inf"), 4, 8, 8, F32, None) == INVALID
+    assert f(X, Y, X + 0x40001, None, 1e-5, 4, 8, 8, BF16, None) == INVALID  # misaligned w
+    assert f(X, Y, None, Y + 0x40002, 1e-5, 4, 8, 8, F32, None) == INVALID  # misaligned b
+    assert f(X, Y, None, None, 1e-5, 4, 8, 4, F32, None) == INVALID  # ld < N
+    assert f(None, None, None, None, 1e-5, 0, 8, 8, F32, None) == OK
+
+
+def test_online_softmax_workspace_bytes(lib):
+    q = lib.rowops_online_softmax_workspace_bytes
+    assert q(64, 1 << 20, F32) == 256 + 64 * 4096 * 8
+    assert q(3, 1, BF16) == 256 + 3 * 1 * 8
+    assert q(5, 257, F32) == 256 + 5 * 2 * 8
+    assert q(0, 100, F32) == 256
+    assert q(-1, 100, F32) == 0
+    assert q(4, 0, F32) == 0
+    assert q(4, 100, 9) == 0
+
+
+def test_online_softmax_validation(lib):
+    f = lib.rowops_online_softmax
+    need = lib.rowops_online_softmax_workspace_bytes(4, 1000, F32)
+    WS = 0x200000
+    assert f(X, Y, 4, 1000, 1000, F32, None, need, 0, None) == WORKSPACE
+    assert f(X, Y, 4, 1000, 1000, F32, WS + 16, need, 0, None) == WORKSPACE  # not 256-byte aligned
+    assert f(X, Y, 4, 1000, 1000, F32, WS, need - 1, 0, None) == WORKSPACE
+    for bad_chunk in (-16, 16, 255, 1000, 1 << 31):
+        assert f(X, Y, 4, 1000, 1000, F32, WS, need, bad_chunk, None) == INVALID
+    assert f(X, Y, 4, 1000, 999, F32, WS, need, 0, None) == INVALID
+    assert f(None, None, 0, 1000, 1000, F32, None, 0, 0, None) == OK
+    assert lib.rowops_online_softmax_status(None, None) == WORKSPACE
+
+
+def test_binding_has_no_fallback(monkeypatch, tmp_path):
+    """The Python binding raises when the library is absent instead of
+    computing anything itself."""
+    import row_wise_reduction_gb300.rowops as r
+
+    monkeypatch.setattr(r, "_lib", None)
+    monkeypatch.setattr(r, "_LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no fallback"):
+        r.library()

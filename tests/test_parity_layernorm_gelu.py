@@ -1,0 +1,198 @@
+"""GPU parity of rowops_layernorm_gelu with the oracle, through the C ABI.
+
+The fp32 4096 x 768 workload in full; the bf16 65536 x {8192, 127, 4097}
+workloads on reduced row counts in full and at full size (benchmark launch
+configuration) on sampled rows; edge cases: NULL weight / bias, ragged and
+misaligned rows, in place, constant rows, every kernel variant, guard bands.
+"""
+import numpy as np
+import pytest
+import torch
+
+from row_wise_reduction_gb300 import rowops_layernorm_gelu, workloads
+from tests import _compare as C
+from tests import gpu_util as gu
+
+pytestmark = [pytest.mark.gpu, gu.requires_gpu]
+
+W2 = workloads.WORKLOADS["layernorm_gelu_f32_4096x768"]
+W5 = workloads.WORKLOADS["layernorm_gelu_bf16_65536x8192"]
+W5a = workloads.WORKLOADS["layernorm_gelu_bf16_65536x127"]
+W5b = workloads.WORKLOADS["layernorm_gelu_bf16_65536x4097"]
+
+
+def edge(dtype, M, N, seed=11, affine=True):
+    return workloads.Workload(f"edge_{dtype}_{M}x{N}", "layernorm_gelu", dtype, M, N, seed=seed, affine=affine)
+
+
+def host(t):
+    return None if t is None else t.float().cpu().numpy()
+
+
+def check(oracle, wl, ld=None, offset=0, yoffset=None, inplace=False, use_w=True, use_b=True, eps=None):
+    inp = gu.make_x(wl, ld=ld, offset=offset)
+    x = inp["x"]
+    w = inp.get("w") if use_w else None
+    b = inp.get("b") if use_b else None
+    eps = wl.eps if eps is None else eps
+    xin = gu.rows_f32(x)
+    if inplace:
+        y, buf, inside = x, None, None
+    else:
+        y, buf, inside = gu.guarded_like(x, offset=offset if yoffset is None else yoffset)
+    rowops_layernorm_gelu(x, w, b, eps, y)
+    torch.cuda.synchronize()
+    ref = oracle.layernorm_gelu(xin, host(w), host(b), eps)
+    err = C.assert_ln_gelu_close(C.to_f64(y), ref, wl.dtype, what=wl.name)
+    if buf is not None:
+        gu.assert_guard_untouched(buf, inside)
+    return err
+
+
+def test_ln_gelu_f32_4096x768_full(oracle):
+    check(oracle, W2)
+
+
+@pytest.mark.parametrize("wl", [W5, W5a, W5b], ids=lambda w: w.name)
+def test_ln_gelu_bf16_reduced_rows(oracle, wl):
+    check(oracle, wl.with_shape(M=1000 if wl.N > 1000 else 4099))
+
+
+@pytest.mark.parametrize("wl", [W5, W5a, W5b], ids=lambda w: w.name)
+def test_ln_gelu_bf16_full_size_sampled(oracle, wl):
+    """Full-size bf16 workloads (65536 rows) in the default launch
+    configuration: 48 sampled rows against the oracle; on every row the output
+    is finite."""
+    inp = gu.make_x(wl)
+    x, w, b = inp["x"], inp["w"], inp["b"]
+    y = rowops_layernorm_gelu(x, w, b, wl.eps)
+    torch.cuda.synchronize()
+    rows = gu.sample_rows(wl.M, 48, seed=wl.N)
+    ref = oracle.layernorm_gelu(gu.rows_f32(x, rows), host(w), host(b), wl.eps)
+    C.assert_ln_gelu_close(C.to_f64(y[torch.as_tensor(rows, device=y.device)]), ref, "bf16", what=wl.name)
+    assert torch.isfinite(y).all()
+    del x, y, inp
+
+
+RAGGED_N = [1, 2, 3, 5, 8, 9, 17, 31, 127, 128, 129, 767, 768, 769, 4095, 4097, 8192, 12288, 16385, 20000,
+            32769, 40000]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("N", RAGGED_N)
+def test_ln_gelu_ragged_n(oracle, dtype, N):
+    check(oracle, edge(dtype, 23, N, seed=N))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("N,ld,offset", [(127, 127, 1), (4097, 4097, 0), (4097, 4105, 3), (768, 780, 0),
+                                         (8192, 8192, 1), (40000, 40003, 1)])
+def test_ln_gelu_strided_and_misaligned_rows(oracle, dtype, N, ld, offset):
+    check(oracle, edge(dtype, 19, N, seed=ld), ld=ld, offset=offset)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("N", [127, 8192, 20000])
+def test_ln_gelu_x_and_y_out_of_phase(oracle, dtype, N):
+    check(oracle, edge(dtype, 7, N), offset=1, yoffset=0)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("use_w,use_b", [(False, False), (True, False), (False, True)])
+def test_ln_gelu_null_affine(oracle, dtype, use_w, use_b):
+    """NULL weight / bias act as 1 / 0."""
+    check(oracle, edge(dtype, 33, 768), use_w=use_w, use_b=use_b)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("N", [768, 8192, 40000])
+def test_ln_gelu_in_place(oracle, dtype, N):
+    check(oracle, edge(dtype, 9, N), inplace=True)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_ln_gelu_constant_and_shifted_rows(oracle, dtype):
+    """A constant row normalises to 0 (output GELU(b)); a row with a large
+    common offset normalises like the unshifted row; eps = 0 on a
+    non-constant row."""
+    N = 1000
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn(4, N, generator=g)
+    x[0] = 3.5
+    x[1] = x[2] + 100.0
+    dt = workloads.torch_dtype(dtype)
+    xt = x.to(dt).cuda()
+    w = (0.5 + torch.rand(N, generator=g)).to(dt).cuda()
+    b = (0.1 * torch.randn(N, generator=g)).to(dt).cuda()
+    for eps in (1e-5, 0.0):
+        rows = [0, 1, 2, 3] if eps > 0 else [1, 2, 3]
+        xs = xt[rows].contiguous()
+        y = rowops_layernorm_gelu(xs, w, b, eps)
+        torch.cuda.synchronize()
+        ref = oracle.layernorm_gelu(xs.float().cpu().numpy(), host(w), host(b), eps)
+        C.assert_ln_gelu_close(C.to_f64(y), ref, dtype)
+
+
+def test_ln_gelu_large_inputs_do_not_overflow(oracle):
+    """Entries far from the mean give |z| >> 10: GELU(z) = z for large
+    positive z and -0 for large negative z, never NaN."""
+    N = 64
+    x = torch.zeros(2, N)
+    x[0, 0] = 1e4
+    x[1, 0] = -1e4
+    w = torch.full((N,), 40.0)
+    xt, wt = x.cuda(), w.cuda()
+    y = rowops_layernorm_gelu(xt, wt, None, 1e-5)
+    torch.cuda.synchronize()
+    assert torch.isfinite(y).all()
+    ref = oracle.layernorm_gelu(x.numpy(), w.numpy(), None, 1e-5)
+    # |z| reaches ~317 here, where one fp32 ulp alone is 3e-5: allow 4 ulps relative
+    C.assert_ln_gelu_close(C.to_f64(y), ref, "f32", rel=2.0 ** -21)
+
+
+def test_ln_gelu_deterministic():
+    wl = edge("bf16", 300, 8192)
+    inp = gu.make_x(wl)
+    a = rowops_layernorm_gelu(inp["x"], inp["w"], inp["b"], 1e-5)
+    b = rowops_layernorm_gelu(inp["x"], inp["w"], inp["b"], 1e-5)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_ln_gelu_empty_is_noop():
+    x = torch.empty(0, 128, device="cuda")
+    y = rowops_layernorm_gelu(x, None, None, 1e-5)
+    torch.cuda.synchronize()
+    assert y.shape == (0, 128)
+
+
+VARIANTS = [(tpr, vpt) for tpr in (16, 32, 64, 128, 256, 512, 1024) for vpt in (1, 2, 3, 4)]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("tpr,vpt", VARIANTS)
+@pytest.mark.parametrize("offset", [0, 1])
+def test_ln_gelu_every_register_variant(oracle, monkeypatch, dtype, tpr, vpt, offset):
+    """Each register-resident instantiation (aligned-row form with offset 0,
+    unaligned-row form with offset 1), forced, on its largest row minus a tail."""
+    vec = 4 if dtype == "f32" else 8
+    N = tpr * vpt * vec - (0 if offset == 0 else 3)
+    if 8 * ((N + 3) // 4 * 4) > 200 * 1024:
+        pytest.skip("affine staging would not fit shared memory; the looped kernel takes this size")
+    monkeypatch.setenv("ROWOPS_FORCE_TPR", str(tpr))
+    monkeypatch.setenv("ROWOPS_FORCE_VPT", str(vpt))
+    check(oracle, edge(dtype, 2 * (1024 // tpr) + 1, N, seed=tpr + vpt), offset=offset)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("ctas", ["-1", "1", "3"])
+def test_ln_gelu_grid_modes(oracle, monkeypatch, dtype, ctas):
+    monkeypatch.setenv("ROWOPS_CTAS_PER_SM", ctas)
+    check(oracle, edge(dtype, 2001, 1024))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_ln_gelu_forced_looped(oracle, monkeypatch, dtype):
+    monkeypatch.setenv("ROWOPS_FORCE_LOOPED", "1")
+    check(oracle, edge(dtype, 41, 4097), offset=1)
+    check(oracle, edge(dtype, 41, 768))

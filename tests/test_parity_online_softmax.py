@@ -1,0 +1,146 @@
+"""GPU parity of rowops_online_softmax (split-row (m, d) partials merged in a
+second pass) with the oracle and with rowops_softmax, through the C ABI."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from row_wise_reduction_gb300 import (
+    rowops_online_softmax,
+    rowops_online_softmax_status,
+    rowops_online_softmax_workspace_bytes,
+    rowops_softmax,
+    workloads,
+)
+from tests import _compare as C
+from tests import gpu_util as gu
+
+pytestmark = [pytest.mark.gpu, gu.requires_gpu]
+
+W4 = workloads.WORKLOADS["online_softmax_f32_64x1048576"]
+
+
+def edge(dtype, M, N, seed=13, std=3.0, outlier_p=0.0):
+    return workloads.Workload(f"edge_{dtype}_{M}x{N}", "online_softmax", dtype, M, N, seed=seed, x_std=std,
+                              outlier_p=outlier_p)
+
+
+def workspace(x):
+    n = rowops_online_softmax_workspace_bytes(x.shape[0], x.shape[1], x.dtype)
+    return torch.empty(n, dtype=torch.uint8, device=x.device)
+
+
+def check(oracle, wl, chunk=0, ld=None, offset=0, yoffset=None, inplace=False):
+    inp = gu.make_x(wl, ld=ld, offset=offset)
+    x = inp["x"]
+    xin = gu.rows_f32(x)
+    ws = workspace(x)
+    if inplace:
+        y, buf, inside = x, None, None
+    else:
+        y, buf, inside = gu.guarded_like(x, offset=offset if yoffset is None else yoffset)
+    rowops_online_softmax(x, y, workspace=ws, chunk=chunk)
+    assert rowops_online_softmax_status(ws) == 0
+    ref = oracle.softmax(xin)
+    C.assert_softmax_close(C.to_f64(y), ref, wl.dtype, what=f"{wl.name} chunk={chunk}")
+    if buf is not None:
+        gu.assert_guard_untouched(buf, inside)
+    return y
+
+
+@pytest.mark.parametrize("chunk", [0, 4096, 65536])
+def test_online_softmax_reduced_rows(oracle, chunk):
+    """The 2^20-column outlier workload on its first 4 rows, at the automatic
+    chunk size and at two explicit ones (256 and 16 chunks per row)."""
+    check(oracle, W4.with_shape(M=4), chunk=chunk)
+
+
+def test_online_softmax_full_size(oracle):
+    """Full 64 x 2^20 fp32 workload, default launch configuration: 4 sampled
+    rows against the oracle; on every row the outlier entries equal
+    1 / (k + S) (k outliers, S = sum of exp(x - 30) over the rest, accumulated
+    here in float64) and every row sums to 1."""
+    inp = gu.make_x(W4)
+    x = inp["x"]
+    ws = workspace(x)
+    y = rowops_online_softmax(x, workspace=ws)
+    assert rowops_online_softmax_status(ws) == 0
+    rows = gu.sample_rows(W4.M, 4, seed=1)
+    ref = oracle.softmax(gu.rows_f32(x, rows))
+    C.assert_softmax_close(C.to_f64(y[torch.as_tensor(rows, device=y.device)]), ref, "f32")
+    hit = x == 30.0
+    k = hit.sum(dim=1, dtype=torch.float64)
+    S = torch.where(hit, 0.0, torch.exp(x.double() - 30.0)).sum(dim=1)
+    want = 1.0 / (k + S)
+    got = torch.where(hit, y.double(), 0.0).sum(dim=1) / k
+    assert torch.all((got / want - 1).abs() <= 1e-5)
+    assert torch.all((y.double().sum(dim=1) - 1).abs() <= 1e-4)
+    del x, y, inp
+
+
+def test_online_matches_two_pass_softmax():
+    """Split-row online softmax and rowops_softmax (whose 2^20-column rows take
+    the in-CTA online loop) agree within the softmax tolerance at two chunk
+    counts, on the same input."""
+    wl = W4.with_shape(M=8)
+    x = gu.make_x(wl)["x"]
+    y2 = rowops_softmax(x)
+    for chunk in (2048, 32768):
+        y1 = rowops_online_softmax(x, chunk=chunk)
+        torch.cuda.synchronize()
+        a, b = y1.double(), y2.double()
+        assert torch.all((a - b).abs() <= 1e-5 * b.abs() + C.FTZ_FLOOR)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("N,chunk", [(1, 0), (100, 256), (257, 256), (4097, 256), (8192, 1024), (30000, 0),
+                                     (100003, 4096), (100003, 0)])
+def test_online_softmax_ragged(oracle, dtype, N, chunk):
+    M = 50 if N < 10000 else 6
+    check(oracle, edge(dtype, M, N, seed=N, outlier_p=1e-3 if N > 1000 else 0.0), chunk=chunk)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("N,ld,offset,chunk", [(4097, 4097, 0, 256), (5000, 5003, 1, 512), (20000, 20000, 3, 0)])
+def test_online_softmax_misaligned(oracle, dtype, N, ld, offset, chunk):
+    """Rows and chunk starts that are not 16-byte aligned."""
+    check(oracle, edge(dtype, 7, N, seed=ld), chunk=chunk, ld=ld, offset=offset)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_online_softmax_out_of_phase_and_in_place(oracle, dtype):
+    check(oracle, edge(dtype, 5, 9000), chunk=1024, offset=1, yoffset=0)
+    check(oracle, edge(dtype, 5, 9000), chunk=1024, inplace=True)
+
+
+def test_online_softmax_masked_chunks(oracle):
+    """Whole chunks of -inf (partials with d = 0) are skipped in the merge; an
+    all-masked row gives zeros; a NaN poisons only its row."""
+    N = 8192
+    g = torch.Generator().manual_seed(3)
+    x = torch.randn(4, N, generator=g)
+    x[0, :4096] = float("-inf")
+    x[1] = float("-inf")
+    x[2, 777] = float("nan")
+    x[3, 1024:7000] = float("-inf")
+    xt = x.cuda()
+    y = rowops_online_softmax(xt, chunk=1024)
+    torch.cuda.synchronize()
+    ref = oracle.softmax(x.numpy())
+    C.assert_softmax_close(C.to_f64(y), ref, "f32")
+
+
+def test_online_softmax_deterministic():
+    x = gu.make_x(edge("f32", 16, 300000))["x"]
+    a = rowops_online_softmax(x, chunk=4096)
+    b = rowops_online_softmax(x, chunk=4096)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def test_online_softmax_empty_is_noop():
+    x = torch.empty(0, 4096, device="cuda")
+    y = rowops_online_softmax(x)
+    torch.cuda.synchronize()
+    assert y.shape == (0, 4096)
