@@ -52,7 +52,7 @@ __global__ void __launch_bounds__(BLOCK)
     float* sw = reinterpret_cast<float*>(smem_affine);
     float* sb = sw + affine_pad(N);
     __shared__ float red_a[BLOCK / 32 > 0 ? BLOCK / 32 : 1];
-    __shared__ float red_b[BLOCK / 32 > 0 ? BLOCK / 32 : 1];
+    __shared__ float red_b[BLOCK / 32 > 0 ? 2 * BLOCK / 32 : 2];
 
     stage_affine(w, b, N, sw, sb);
     __syncthreads();
@@ -100,8 +100,11 @@ __global__ void __launch_bounds__(BLOCK)
         s = group_reduce<TPR>(s, red_a, OpSum());
         const float mean = s / fN;
 
-        // variance of the centred values; padding stays out of it
-        float q = 0.f;
+        // variance of the centred values; padding stays out of it. The fp32
+        // mean carries a rounding error of order |mean| 2^-24; the residual
+        // r = sum(x - mean) measures it, delta = r / N, so that
+        // x - true mean = (x - mean) - delta and var = q / N - delta^2.
+        float q = 0.f, r = 0.f;
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
             const int64_t k = t + int64_t(i) * TPR;
@@ -110,12 +113,16 @@ __global__ void __launch_bounds__(BLOCK)
             for (int j = 0; j < V; ++j) {
                 v[i][j] = ok ? v[i][j] - mean : 0.f;
                 q = fmaf(v[i][j], v[i][j], q);
+                r += v[i][j];
             }
         }
         ex = has_ex ? ex - mean : 0.f;
         q = fmaf(ex, ex, q);
-        q = group_reduce<TPR>(q, red_b, OpSum());
-        const float rstd = rsqrtf(q / fN + eps);
+        r += ex;
+        group_reduce_sum2<TPR>(q, r, red_b);
+        const float delta = r / fN;
+        const float rstd = rsqrtf(fmaxf(q / fN - delta * delta, 0.f) + eps);
+        const float shift = -delta * rstd;  // (x - mean - delta) * rstd = fma(x - mean, rstd, shift)
 
         // affine + GELU + store
 #pragma unroll
@@ -129,20 +136,20 @@ __global__ void __launch_bounds__(BLOCK)
                     for (int j = 0; j < V; j += 4) {
                         const float4 ww = *reinterpret_cast<const float4*>(sw + c0 + j);
                         const float4 bb = *reinterpret_cast<const float4*>(sb + c0 + j);
-                        o[j + 0] = gelu_tanh_approx(fmaf(v[i][j + 0] * rstd, ww.x, bb.x));
-                        o[j + 1] = gelu_tanh_approx(fmaf(v[i][j + 1] * rstd, ww.y, bb.y));
-                        o[j + 2] = gelu_tanh_approx(fmaf(v[i][j + 2] * rstd, ww.z, bb.z));
-                        o[j + 3] = gelu_tanh_approx(fmaf(v[i][j + 3] * rstd, ww.w, bb.w));
+                        o[j + 0] = gelu_tanh_approx(fmaf(fmaf(v[i][j + 0], rstd, shift), ww.x, bb.x));
+                        o[j + 1] = gelu_tanh_approx(fmaf(fmaf(v[i][j + 1], rstd, shift), ww.y, bb.y));
+                        o[j + 2] = gelu_tanh_approx(fmaf(fmaf(v[i][j + 2], rstd, shift), ww.z, bb.z));
+                        o[j + 3] = gelu_tanh_approx(fmaf(fmaf(v[i][j + 3], rstd, shift), ww.w, bb.w));
                     }
                 } else {
 #pragma unroll
                     for (int j = 0; j < V; ++j)
-                        o[j] = gelu_tanh_approx(fmaf(v[i][j] * rstd, sw[c0 + j], sb[c0 + j]));
+                        o[j] = gelu_tanh_approx(fmaf(fmaf(v[i][j], rstd, shift), sw[c0 + j], sb[c0 + j]));
                 }
                 st_stream16(yv + k * V, E::pack(o));
             }
         }
-        if (has_ex) E::store(yr + ecol, gelu_tanh_approx(fmaf(ex * rstd, sw[ecol], sb[ecol])));
+        if (has_ex) E::store(yr + ecol, gelu_tanh_approx(fmaf(fmaf(ex, rstd, shift), sw[ecol], sb[ecol])));
     }
 }
 

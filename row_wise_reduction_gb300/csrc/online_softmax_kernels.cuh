@@ -65,9 +65,8 @@ __global__ void __launch_bounds__(BLOCK)
                         s.d *= ex2_approx((s.m - vm) * kLog2eF);
                         s.m = vm;
                     }
-                    const float nm = -s.m * kLog2eF;
 #pragma unroll
-                    for (int j = 0; j < V; ++j) s.d += exp_shifted(f[j], nm);
+                    for (int j = 0; j < V; ++j) s.d += exp_shifted(f[j], s.m);
                 }
             }
         }
@@ -124,13 +123,12 @@ __global__ void __launch_bounds__(BLOCK)
                                                red_d[parity]);
         const float m = s.d > 0.f ? s.m : 0.f;
         const float inv = safe_inverse(s.d);
-        const float nm = -m * kLog2eF;
 
         if (scalar)
-            for (int64_t cc = t; cc < n; cc += BLOCK) E::store(ys + cc, exp_shifted(E::load(xs + cc), nm) * inv);
+            for (int64_t cc = t; cc < n; cc += BLOCK) E::store(ys + cc, exp_shifted(E::load(xs + cc), m) * inv);
         if (t < geo.extras()) {
             const int64_t cc = extra_col(geo, t, V);
-            E::store(ys + cc, exp_shifted(E::load(xs + cc), nm) * inv);
+            E::store(ys + cc, exp_shifted(E::load(xs + cc), m) * inv);
         }
         for (int64_t k0 = t;; k0 += int64_t(BLOCK) * UNROLL) {
 #pragma unroll
@@ -140,7 +138,7 @@ __global__ void __launch_bounds__(BLOCK)
                     float f[V];
                     E::unpack(raw[u], f);
 #pragma unroll
-                    for (int j = 0; j < V; ++j) f[j] = exp_shifted(f[j], nm) * inv;
+                    for (int j = 0; j < V; ++j) f[j] = exp_shifted(f[j], m) * inv;
                     st_stream16(yv + k * V, E::pack(f));
                 }
             }

@@ -197,7 +197,9 @@ int grid_for(const void* func, int block, size_t smem, int64_t items, const Laun
 }
 
 cudaError_t allow_smem(const void* func, size_t smem, const LaunchCfg& cfg) {
-    if (smem <= 48 * 1024) return cudaSuccess;
+    // the default limit covers static + dynamic shared memory together; opt in
+    // well before the dynamic part alone reaches it
+    if (smem <= 32 * 1024) return cudaSuccess;
     std::lock_guard<std::mutex> lk(g_mu);
     for (auto& s : g_smem)
         if (s.func == func && s.device == cfg.device && s.smem >= smem) return cudaSuccess;

@@ -172,6 +172,35 @@ __device__ __forceinline__ float group_reduce(float v, float* red, Op op) {
     return v;
 }
 
+// Two sums reduced together (one butterfly, one barrier); `red` holds
+// 2 * BLOCK / 32 floats.
+template <int TPR>
+__device__ __forceinline__ void group_reduce_sum2(float& a, float& b, float* red) {
+    constexpr int kLanes = TPR < 32 ? TPR : 32;
+#pragma unroll
+    for (int o = kLanes / 2; o > 0; o >>= 1) {
+        a += __shfl_xor_sync(0xffffffffu, a, o);
+        b += __shfl_xor_sync(0xffffffffu, b, o);
+    }
+    if constexpr (TPR > 32) {
+        constexpr int W = TPR / 32;
+        const int warp = threadIdx.x >> 5;
+        const int first = (warp / W) * W;
+        if ((threadIdx.x & 31) == 0) {
+            red[2 * warp] = a;
+            red[2 * warp + 1] = b;
+        }
+        __syncthreads();
+        a = red[2 * first];
+        b = red[2 * first + 1];
+#pragma unroll
+        for (int i = 1; i < W; ++i) {
+            a += red[2 * (first + i)];
+            b += red[2 * (first + i) + 1];
+        }
+    }
+}
+
 // Online-softmax state (m, d): m the largest entry seen, d = sum exp(x - m).
 // Merging two states [EX §2.5; L6 §7.2]: m = max(m1, m2),
 //   d = d1 * exp(m1 - m) + d2 * exp(m2 - m); a state with d = 0 contributes nothing.
