@@ -1,0 +1,83 @@
+"""Host-side logic of bench.py that needs no GPU: the multi-rank aggregation
+(max time, summed work) over two gloo ranks on the CPU, the reference arm's
+rank-0-only rule, and the byte accounting."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, q):
+    import bench
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        secs, units = bench.aggregate(0.5 + rank, 100.0 * (rank + 1))
+        q.put((rank, secs, units))
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_aggregate_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    for rank, secs, units in got:
+        assert secs == 1.5  # the slowest rank's time
+        assert units == 300.0  # every rank's work
+
+
+def test_aggregate_without_process_group_is_identity():
+    import bench
+
+    assert bench.aggregate(2.0, 7.0) == (2.0, 7.0)
+
+
+def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
+    import bench
+
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "0"]) == 0
+    assert capsys.readouterr().out == ""
+
+
+def test_algorithmic_bytes():
+    import bench
+    from row_wise_reduction_gb300 import workloads
+
+    W = workloads.WORKLOADS
+    assert bench.alg_bytes(W["softmax_bf16_causal_32768x4096"]) == 2 * 32768 * 4096 * 2
+    assert bench.alg_bytes(W["online_softmax_f32_64x1048576"]) == 2 * 64 * (1 << 20) * 4
+    assert bench.alg_bytes(W["layernorm_gelu_bf16_65536x8192"]) == 2 * 65536 * 8192 * 2 + 2 * 8192 * 2
+
+
+def test_profiled_traffic_requires_matching_source(tmp_path, monkeypatch):
+    import bench
+
+    p = tmp_path / "summary.txt"
+    p.write_text(f"kernel_source_sha: {bench.dominant_source_hash()}\ndram_bytes_per_launch: 123\n")
+    monkeypatch.setattr(bench, "PROFILE_SUMMARY", str(p))
+    assert bench.profiled_traffic() == 123
+    p.write_text("kernel_source_sha: 0000\ndram_bytes_per_launch: 123\n")
+    assert bench.profiled_traffic() is None
