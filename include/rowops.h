@@ -124,6 +124,38 @@ rowops_status_t rowops_online_softmax(const void* x, void* y, int64_t M, int64_t
 rowops_status_t rowops_online_softmax_status(const void* workspace, cudaStream_t stream);
 
 /*
+ * rowops_online_softmax for callers that cannot allocate device memory.
+ * (No counterpart on the source pages: this is an interface convenience.)
+ *
+ * Same operation, arguments and results as rowops_online_softmax, minus the
+ * workspace: the chunk partials go to a 1 MiB array of device memory that the
+ * library itself owns. Meant for code that only holds x and y -- a plugin that
+ * a host framework calls with device pointers but no allocator or workspace
+ * hook, or a latency-critical path where a cudaMalloc (which may synchronise
+ * the device) cannot be afforded. The call allocates nothing.
+ *
+ *   x, y, M, N, ld, dtype, chunk, stream   as for rowops_online_softmax.
+ * Returns ROWOPS_ERR_WORKSPACE when the problem needs more partials than the
+ * array holds: M * nchunks must not exceed 131040 (nchunks = ceil(N / chunk),
+ * with chunk as chosen for chunk == 0 or as given).
+ *
+ * Notes:
+ *   - Every GPU that loads the library reserves that 1 MiB until the process
+ *     exits.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, no allocation) with that device current; make that
+ *     first call before any stream capture.
+ *   - All calls share the one array, which keeps the last call's contents.
+ *     Calls whose kernels may overlap on the GPU (different streams without
+ *     ordering between them) race on it and give wrong results: order them on
+ *     one stream or synchronise between them. Nothing in it needs clearing
+ *     before a call.
+ */
+rowops_status_t rowops_online_softmax_noalloc(const void* x, void* y, int64_t M, int64_t N,
+                                              int64_t ld, rowops_dtype_t dtype, int64_t chunk,
+                                              cudaStream_t stream);
+
+/*
  * Fused LayerNorm -> affine -> tanh-approximation GELU of every row
  * [FUS §三 _layer_norm_gelu_kernel; EX §4.1 LayerNorm; KT "Triton GeLU"]:
  *   mean = sum_j x_j / N;  var = sum_j (x_j - mean)^2 / N      (biased)

@@ -26,6 +26,7 @@ SOURCES = [
     "ln_gelu_f32.cu",
     "ln_gelu_bf16.cu",
     "online_softmax.cu",
+    "online_softmax_noalloc.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -25,6 +25,7 @@ __all__ = [
     "rowops_online_softmax",
     "rowops_online_softmax_workspace_bytes",
     "rowops_online_softmax_status",
+    "rowops_online_softmax_noalloc",
     "rowops_layernorm_gelu",
     "rowops_status_string",
     "ROWOPS_F32",
@@ -83,6 +84,8 @@ def library() -> ctypes.CDLL:
                                             _i64, _vp]
         L.rowops_online_softmax_status.restype = ctypes.c_int
         L.rowops_online_softmax_status.argtypes = [_vp, _vp]
+        L.rowops_online_softmax_noalloc.restype = ctypes.c_int
+        L.rowops_online_softmax_noalloc.argtypes = [_vp, _vp, _i64, _i64, _i64, ctypes.c_int, _i64, _vp]
         L.rowops_layernorm_gelu.restype = ctypes.c_int
         L.rowops_layernorm_gelu.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, _i64, _i64, _i64,
                                             ctypes.c_int, _vp]
@@ -184,6 +187,21 @@ def rowops_online_softmax_status(workspace: torch.Tensor, *, stream=None) -> int
     """Synchronise the stream and return the device-side status of the last
     rowops_online_softmax call on ``workspace`` (0 = ROWOPS_OK)."""
     return int(library().rowops_online_softmax_status(workspace.data_ptr(), _stream(stream)))
+
+
+def rowops_online_softmax_noalloc(
+    x: torch.Tensor, y: Optional[torch.Tensor] = None, *, chunk: int = 0, stream=None
+) -> torch.Tensor:
+    """rowops_online_softmax without a workspace, for callers that cannot
+    allocate device memory: the partials live in the library's own 1 MiB
+    device array (M * ceil(N / chunk) <= 131040). Calls that could overlap on
+    the GPU share that array and must be ordered."""
+    M, N, ld = _rows(x, "x")
+    y = _out_like(x, y)
+    st = library().rowops_online_softmax_noalloc(x.data_ptr(), y.data_ptr(), M, N, ld, _dtype_code(x), int(chunk),
+                                                 _stream(stream))
+    _check("rowops_online_softmax_noalloc", st)
+    return y
 
 
 def rowops_layernorm_gelu(
