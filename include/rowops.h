@@ -34,9 +34,12 @@
  *   - Thread-safe; all entry points may be called from any host thread.
  *
  * Benchmarking knobs (environment, read at every call; unset = automatic):
- *   ROWOPS_FORCE_TPR=<16..1024>   threads per row of the register-resident kernels
- *   ROWOPS_FORCE_VPT=<1..4>       16-byte vectors per thread of those kernels
- *   ROWOPS_FORCE_LOOPED=1         use the looped (any N) kernels
+ *   ROWOPS_KERNEL=tma|reg|looped  kernel family: TMA-fed row pipeline, register-resident
+ *                                 row groups, or the looped any-N kernels
+ *   ROWOPS_FORCE_TPR=<16..1024>   threads per row (tma: 64..512)
+ *   ROWOPS_FORCE_VPT=<n>          16-byte vectors per thread (reg: 1..4; tma: 1, 2, 3, 4, 8)
+ *   ROWOPS_FORCE_LOOPED=1         same as ROWOPS_KERNEL=looped
+ *   ROWOPS_RING_BUFFERS=<2..16>   rows in flight per CTA of the row pipeline
  *   ROWOPS_CTAS_PER_SM=<k>        persistent grid of k CTAs per SM (0 = occupancy limit,
  *                                 -1 = one CTA per row group, no persistence)
  */
@@ -84,6 +87,16 @@ const char* rowops_status_string(rowops_status_t status);
  */
 rowops_status_t rowops_softmax(const void* x, void* y, int64_t M, int64_t N, int64_t ld,
                                rowops_dtype_t dtype, cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the library's device error word
+ * on the current device. Kernels that wait on asynchronous copies (the TMA-fed
+ * row pipeline behind rowops_softmax and rowops_layernorm_gelu) bound every
+ * wait; if one gives up, the kernel stops, records ROWOPS_ERR_TIMEOUT there,
+ * and the outputs of that call are unspecified. Returns ROWOPS_OK,
+ * ROWOPS_ERR_TIMEOUT, or ROWOPS_ERR_CUDA if a CUDA call fails.
+ */
+rowops_status_t rowops_device_status(cudaStream_t stream);
 
 /*
  * Bytes of device workspace that rowops_online_softmax needs for an M x N

@@ -10,6 +10,7 @@ from .rowops import (  # noqa: F401
     RowopsError,
     library,
     library_path,
+    rowops_device_status,
     rowops_layernorm_gelu,
     rowops_online_softmax,
     rowops_online_softmax_status,

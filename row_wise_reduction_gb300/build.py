@@ -27,6 +27,10 @@ SOURCES = [
     "ln_gelu_bf16.cu",
     "online_softmax.cu",
     "online_softmax_noalloc.cu",
+    "tma_softmax_f32.cu",
+    "tma_softmax_bf16.cu",
+    "tma_ln_gelu_f32.cu",
+    "tma_ln_gelu_bf16.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -1,0 +1,165 @@
+// TMA-fed row pipeline: one CTA works on one row at a time while the next
+// rows stream into a ring of shared-memory buffers.
+//
+// Thread 0 copies each whole row with one bulk asynchronous copy
+// (cp.async.bulk, global -> shared, completion counted in bytes on an
+// mbarrier). Every thread waits on the buffer's mbarrier, reads its own 16-byte
+// vectors out of shared memory, and after the row's first CTA-wide reduction
+// (by which point every thread holds its data in registers) thread 0 refills
+// that buffer with the row `nbuf` iterations ahead. So `nbuf` rows per CTA are
+// always in flight regardless of how long the arithmetic of the current row
+// takes: the memory system never waits for the compute of a row.
+//
+// Requirements (checked by the dispatcher): rows start on 16-byte boundaries
+// and N * sizeof(T) is a multiple of 16 (the bulk copy's alignment rules).
+//
+// Waits are bounded. If a buffer's copy has not landed after kWaitLimitNs, the
+// thread records it; the next CTA-wide barrier (__syncthreads_or) tells every
+// thread, the CTA stops processing rows, thread 0 waits (again bounded) for the
+// copies it still has in flight, sets the library's device error word and the
+// CTA returns.
+#pragma once
+
+#include "rowops_device.cuh"
+
+namespace rowops {
+
+constexpr unsigned kDeviceErrTimeout = 5u;  // value of ROWOPS_ERR_TIMEOUT
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+// make the initialised barriers visible to the async (copy) proxy
+__device__ __forceinline__ void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity: false after kWaitLimitNs
+// (or 2^26 polls, whichever comes first).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (uint32_t i = 0; i < (1u << 26); ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 255u && global_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return false;
+}
+
+// Thread 0: expect `bytes` on `bar`, then copy them global -> shared.
+__device__ __forceinline__ void tma_load_row(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// Order this thread's earlier shared-memory reads before later async-proxy
+// writes to the same buffer.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ uint4 lds16(const void* p) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(smem_addr(p)));
+    return v;
+}
+
+// CTA-wide reductions (one row per CTA, BLOCK threads, BLOCK a multiple of 64)
+// whose barrier also ORs a per-thread failure flag across the CTA.
+template <int BLOCK, class Op>
+__device__ __forceinline__ float cta_reduce(float v, float* red, Op op, int& fail) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(0xffffffffu, v, o));
+    constexpr int W = BLOCK / 32;
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    fail = __syncthreads_or(fail);
+    v = red[0];
+#pragma unroll
+    for (int i = 1; i < W; ++i) v = op(v, red[i]);
+    return v;
+}
+
+template <int BLOCK>
+__device__ __forceinline__ void cta_reduce_sum2(float& a, float& b, float* red, int& fail) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        a += __shfl_xor_sync(0xffffffffu, a, o);
+        b += __shfl_xor_sync(0xffffffffu, b, o);
+    }
+    constexpr int W = BLOCK / 32;
+    const int w = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) {
+        red[2 * w] = a;
+        red[2 * w + 1] = b;
+    }
+    fail = __syncthreads_or(fail);
+    a = red[0];
+    b = red[1];
+#pragma unroll
+    for (int i = 1; i < W; ++i) {
+        a += red[2 * i];
+        b += red[2 * i + 1];
+    }
+}
+
+// The ring: nbuf buffers of `row_bytes` (a multiple of 128) after the barriers.
+struct RowRing {
+    uint64_t* bar;    // nbuf mbarriers
+    char* buf;        // nbuf * row_bytes
+    uint32_t row_bytes;
+    int nbuf;
+    __device__ __forceinline__ char* slot(int s) const { return buf + size_t(s) * row_bytes; }
+};
+
+// Bytes of dynamic shared memory before the row buffers (barriers, padded).
+constexpr uint32_t kRingHeader = 128;
+constexpr int kMaxRingBuffers = 16;
+
+__host__ __device__ constexpr uint32_t ring_row_bytes(int64_t N, int es) {
+    return uint32_t((N * es + 127) / 128 * 128);
+}
+
+// Thread 0, on an error exit: wait (bounded) for every copy still in flight so
+// that none lands in shared memory after the CTA is gone.
+__device__ __forceinline__ void drain_ring(const RowRing& ring, int64_t first_row_iter, int64_t row0,
+                                           int64_t stride, int64_t M) {
+    for (int d = 0; d < ring.nbuf; ++d) {
+        const int64_t i = first_row_iter + d;
+        const int64_t row = row0 + i * stride;
+        if (row >= M) break;
+        mbar_wait(ring.bar + (i % ring.nbuf), uint32_t((i / ring.nbuf) & 1));
+    }
+}
+
+}  // namespace rowops

@@ -18,11 +18,13 @@ bool valid_dtype(rowops_dtype_t dt) { return dt == ROWOPS_F32 || dt == ROWOPS_BF
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // Benchmarking knobs, read at every call (see include/rowops.h).
+enum class Family { Auto, Tma, Reg, Looped };
 struct Tuning {
     int tpr = 0;
     int vpt = 0;
-    bool looped = false;
+    Family family = Family::Auto;
     int ctas_per_sm = 0;
+    int ring = 0;
 };
 
 int env_int(const char* name, int dflt) {
@@ -37,8 +39,14 @@ Tuning read_tuning() {
     Tuning t;
     t.tpr = env_int("ROWOPS_FORCE_TPR", 0);
     t.vpt = env_int("ROWOPS_FORCE_VPT", 0);
-    t.looped = env_int("ROWOPS_FORCE_LOOPED", 0) != 0;
+    if (env_int("ROWOPS_FORCE_LOOPED", 0) != 0) t.family = Family::Looped;
+    if (const char* k = std::getenv("ROWOPS_KERNEL")) {
+        if (!std::strcmp(k, "tma")) t.family = Family::Tma;
+        else if (!std::strcmp(k, "reg")) t.family = Family::Reg;
+        else if (!std::strcmp(k, "looped")) t.family = Family::Looped;
+    }
     t.ctas_per_sm = env_int("ROWOPS_CTAS_PER_SM", 0);
+    t.ring = env_int("ROWOPS_RING_BUFFERS", 0);
     return t;
 }
 
@@ -63,9 +71,14 @@ rowops_status_t check_rows(const void* x, const void* y, int64_t M, int64_t N, i
 }
 
 // ---- per-device attributes and per-kernel caches ---------------------------
+// Device error word: the row-pipeline kernels store ROWOPS_ERR_TIMEOUT here
+// when a bounded wait gives up; rowops_device_status reads and clears it.
+__device__ unsigned g_device_error;
+
 struct DeviceInfo {
     int num_sms = 0;
     int max_smem_optin = 0;
+    unsigned* err = nullptr;  // device address of g_device_error on this device
 };
 
 std::mutex g_mu;
@@ -97,6 +110,7 @@ cudaError_t device_info(int dev, DeviceInfo* out) {
     cudaError_t e = cudaDeviceGetAttribute(&di.num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess)
         e = cudaDeviceGetAttribute(&di.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e == cudaSuccess) e = cudaGetSymbolAddress(reinterpret_cast<void**>(&di.err), g_device_error);
     if (e != cudaSuccess) return e;
     g_devices.emplace_back(dev, di);
     *out = di;
@@ -113,6 +127,7 @@ rowops_status_t make_cfg(cudaStream_t stream, const Tuning& tn, LaunchCfg* cfg) 
     cfg->num_sms = di.num_sms;
     cfg->max_smem_optin = di.max_smem_optin;
     cfg->ctas_per_sm = tn.ctas_per_sm;
+    cfg->dev_error = di.err;
     return ROWOPS_OK;
 }
 
@@ -165,6 +180,75 @@ bool rows_aligned(const void* x, const void* y, int64_t ld, int es) {
 }
 
 constexpr int64_t kMinChunk = 256;
+
+// Row-pipeline kernel choice. Needs 16-byte aligned rows whose byte length is
+// a multiple of 16 (bulk-copy rules) and at least 64 vectors. Prefers a row of
+// exactly block * vpt vectors (no predicates), trying 4, 8, 2, 3, 1 vectors per
+// thread; otherwise the smallest block that covers the row with <= 4.
+struct TmaChoice {
+    int block_index, vpt_index;
+    bool full;
+};
+
+int tma_vpt_index(int vpt) {
+    for (int j = 0; j < kNumTmaVpts; ++j)
+        if (kTmaVpts[j] == vpt) return j;
+    return -1;
+}
+
+int tma_block_index(int64_t block) {
+    for (int i = 0; i < kNumTmaBlocks; ++i)
+        if (kTmaBlocks[i] == block) return i;
+    return -1;
+}
+
+bool choose_tma(const void* x, const void* y, int64_t N, int64_t ld, int es, const Tuning& tn, TmaChoice* c) {
+    const int64_t vec = 16 / es;
+    if (!rows_aligned(x, y, ld, es) || N % vec != 0) return false;
+    const int64_t nvec = N / vec;
+    if (nvec < 64) return false;
+    if (tn.tpr) {
+        const int bi = tma_block_index(tn.tpr);
+        if (bi < 0) return false;
+        int vpt = tn.vpt ? tn.vpt : int((nvec + tn.tpr - 1) / tn.tpr);
+        if (vpt == 5 || vpt == 6 || vpt == 7) vpt = 8;
+        const int vi = tma_vpt_index(vpt);
+        if (vi < 0 || int64_t(vpt) * tn.tpr < nvec) return false;
+        *c = TmaChoice{bi, vi, int64_t(vpt) * tn.tpr == nvec};
+        return true;
+    }
+    for (int vpt : {4, 8, 2, 3, 1}) {
+        if (nvec % vpt) continue;
+        const int bi = tma_block_index(nvec / vpt);
+        if (bi >= 0) {
+            *c = TmaChoice{bi, tma_vpt_index(vpt), true};
+            return true;
+        }
+    }
+    for (int i = 0; i < kNumTmaBlocks; ++i) {
+        const int64_t block = kTmaBlocks[i];
+        if (block * 4 >= nvec) {
+            int vpt = int((nvec + block - 1) / block);
+            if (vpt == 3) vpt = 4;
+            *c = TmaChoice{i, tma_vpt_index(vpt), false};
+            return true;
+        }
+    }
+    return false;
+}
+
+// Ring depth: about 32 KB of rows in flight per CTA (2..8 buffers), fewer if
+// shared memory would not hold them next to `fixed` bytes.
+int ring_buffers(int64_t N, int es, size_t fixed, const Tuning& tn, const LaunchCfg& cfg) {
+    const size_t rb = tma_row_bytes(N, es);
+    int nbuf = tn.ring > 0 ? tn.ring : int(32768 / rb);
+    if (nbuf < 2) nbuf = 2;
+    if (nbuf > 8 && tn.ring <= 0) nbuf = 8;
+    if (nbuf > 16) nbuf = 16;
+    const size_t limit = size_t(cfg.max_smem_optin) - 1024;  // room for static reduction buffers
+    while (nbuf > 2 && tma_ring_smem(N, es, nbuf) + fixed > limit) --nbuf;
+    return tma_ring_smem(N, es, nbuf) + fixed <= limit ? nbuf : 0;
+}
 
 }  // namespace
 
@@ -234,9 +318,16 @@ rowops_status_t rowops_softmax(const void* x, void* y, int64_t M, int64_t N, int
     LaunchCfg cfg;
     if ((st = make_cfg(stream, tn, &cfg)) != ROWOPS_OK) return st;
     const int es = elem_bytes(dtype);
+    TmaChoice tc;
+    if ((tn.family == Family::Auto || tn.family == Family::Tma) && choose_tma(x, y, N, ld, es, tn, &tc)) {
+        const int nbuf = ring_buffers(N, es, 0, tn, cfg);
+        TmaSoftmaxLaunch tf = dtype == ROWOPS_F32 ? softmax_tma_f32(tc.block_index, tc.vpt_index, tc.full)
+                                                  : softmax_tma_bf16(tc.block_index, tc.vpt_index, tc.full);
+        if (nbuf > 0 && tf) return finish(tf(x, y, M, N, ld, nbuf, cfg));
+    }
     int tpr_index = 0, vpt = 0;
     SoftmaxLaunch fn = nullptr;
-    if (!tn.looped && same_phase(x, y) && choose_reg(N, es, tn, &tpr_index, &vpt))
+    if (tn.family != Family::Looped && same_phase(x, y) && choose_reg(N, es, tn, &tpr_index, &vpt))
         fn = dtype == ROWOPS_F32 ? softmax_reg_f32(tpr_index, vpt) : softmax_reg_bf16(tpr_index, vpt);
     if (!fn) fn = dtype == ROWOPS_F32 ? softmax_looped_f32() : softmax_looped_bf16();
     return finish(fn(x, y, M, N, ld, cfg));
@@ -254,11 +345,19 @@ rowops_status_t rowops_layernorm_gelu(const void* x, void* y, const void* w, con
     const Tuning tn = read_tuning();
     LaunchCfg cfg;
     if ((st = make_cfg(stream, tn, &cfg)) != ROWOPS_OK) return st;
+    TmaChoice tc;
+    if ((tn.family == Family::Auto || tn.family == Family::Tma) && choose_tma(x, y, N, ld, es, tn, &tc)) {
+        const size_t affine = tma_affine_smem(kTmaBlocks[tc.block_index], kTmaVpts[tc.vpt_index], es);
+        const int nbuf = ring_buffers(N, es, affine, tn, cfg);
+        TmaLnGeluLaunch tf = dtype == ROWOPS_F32 ? ln_gelu_tma_f32(tc.block_index, tc.vpt_index, tc.full)
+                                                 : ln_gelu_tma_bf16(tc.block_index, tc.vpt_index, tc.full);
+        if (nbuf > 0 && tf) return finish(tf(x, y, w, b, eps, M, N, ld, nbuf, cfg));
+    }
     int tpr_index = 0, vpt = 0;
     LnGeluLaunch fn = nullptr;
     // static shared memory of the kernel (reduction buffers) stays under 256 bytes
     const bool smem_ok = ln_gelu_smem_bytes(N) + 256 <= size_t(cfg.max_smem_optin);
-    if (!tn.looped && smem_ok && same_phase(x, y) && choose_reg(N, es, tn, &tpr_index, &vpt)) {
+    if (tn.family != Family::Looped && smem_ok && same_phase(x, y) && choose_reg(N, es, tn, &tpr_index, &vpt)) {
         const bool al = rows_aligned(x, y, ld, es);
         fn = dtype == ROWOPS_F32 ? ln_gelu_reg_f32(tpr_index, vpt, al) : ln_gelu_reg_bf16(tpr_index, vpt, al);
     }
@@ -300,6 +399,24 @@ rowops_status_t rowops_online_softmax(const void* x, void* y, int64_t M, int64_t
     const int64_t nchunks = (N + chunk - 1) / chunk;
     SplitLaunch fn = dtype == ROWOPS_F32 ? split_softmax_f32() : split_softmax_bf16();
     return finish(fn(x, y, M, N, ld, chunk, nchunks, workspace, cfg));
+}
+
+rowops_status_t rowops_device_status(cudaStream_t stream) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return finish(cudaErrorUnknown);
+    DeviceInfo di;
+    if (device_info(dev, &di) != cudaSuccess) return finish(cudaErrorUnknown);
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return finish(cudaErrorUnknown);
+    unsigned word = 0;
+    if (cudaMemcpy(&word, di.err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return finish(cudaErrorUnknown);
+    if (word != 0u) {
+        const unsigned zero = 0u;
+        if (cudaMemcpy(di.err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+            return finish(cudaErrorUnknown);
+    }
+    if (word == 0u) return ROWOPS_OK;
+    return word == unsigned(ROWOPS_ERR_TIMEOUT) ? ROWOPS_ERR_TIMEOUT : ROWOPS_ERR_CUDA;
 }
 
 rowops_status_t rowops_online_softmax_status(const void* workspace, cudaStream_t stream) {

@@ -14,6 +14,7 @@ struct LaunchCfg {
     int num_sms;
     int max_smem_optin;  // bytes of dynamic shared memory a CTA may opt in to
     int ctas_per_sm;     // 0: occupancy limit; -1: one CTA per work item; k > 0: k per SM
+    unsigned* dev_error; // the library's device error word on this device (row-pipeline timeouts)
 };
 
 // Persistent grid size for `items` independent work items: the occupancy
@@ -36,6 +37,28 @@ using LnGeluLaunch = cudaError_t (*)(const void* x, void* y, const void* w, cons
 using SplitLaunch = cudaError_t (*)(const void* x, void* y, int64_t M, int64_t N, int64_t ld,
                                     int64_t chunk, int64_t nchunks, void* workspace,
                                     const LaunchCfg& cfg);
+
+// TMA-fed row pipeline: one row per CTA of kTmaBlocks[i] threads, kTmaVpts[j]
+// vectors per thread; `full` when the row is exactly block * vpt vectors.
+constexpr int kTmaBlocks[] = {64, 128, 256, 512};
+constexpr int kNumTmaBlocks = 4;
+constexpr int kTmaVpts[] = {1, 2, 3, 4, 8};
+constexpr int kNumTmaVpts = 5;
+constexpr int kTmaRingHeader = 128;
+
+using TmaSoftmaxLaunch = cudaError_t (*)(const void* x, void* y, int64_t M, int64_t N, int64_t ld, int nbuf,
+                                         const LaunchCfg& cfg);
+using TmaLnGeluLaunch = cudaError_t (*)(const void* x, void* y, const void* w, const void* b, float eps,
+                                        int64_t M, int64_t N, int64_t ld, int nbuf, const LaunchCfg& cfg);
+TmaSoftmaxLaunch softmax_tma_f32(int block_index, int vpt_index, bool full);
+TmaSoftmaxLaunch softmax_tma_bf16(int block_index, int vpt_index, bool full);
+TmaLnGeluLaunch ln_gelu_tma_f32(int block_index, int vpt_index, bool full);
+TmaLnGeluLaunch ln_gelu_tma_bf16(int block_index, int vpt_index, bool full);
+
+// dynamic shared memory of the row-pipeline kernels
+inline size_t tma_row_bytes(int64_t N, int es) { return size_t((N * es + 127) / 128 * 128); }
+inline size_t tma_ring_smem(int64_t N, int es, int nbuf) { return kTmaRingHeader + size_t(nbuf) * tma_row_bytes(N, es); }
+inline size_t tma_affine_smem(int block, int vpt, int es) { return size_t(2) * vpt * block * (16 / es) * 4; }
 
 // register-resident: tpr_index into kTprChoices, vpt in 1..kMaxVpt
 SoftmaxLaunch softmax_reg_f32(int tpr_index, int vpt);

@@ -26,6 +26,7 @@ __all__ = [
     "rowops_online_softmax_workspace_bytes",
     "rowops_online_softmax_status",
     "rowops_online_softmax_noalloc",
+    "rowops_device_status",
     "rowops_layernorm_gelu",
     "rowops_status_string",
     "ROWOPS_F32",
@@ -84,6 +85,8 @@ def library() -> ctypes.CDLL:
                                             _i64, _vp]
         L.rowops_online_softmax_status.restype = ctypes.c_int
         L.rowops_online_softmax_status.argtypes = [_vp, _vp]
+        L.rowops_device_status.restype = ctypes.c_int
+        L.rowops_device_status.argtypes = [_vp]
         L.rowops_online_softmax_noalloc.restype = ctypes.c_int
         L.rowops_online_softmax_noalloc.argtypes = [_vp, _vp, _i64, _i64, _i64, ctypes.c_int, _i64, _vp]
         L.rowops_layernorm_gelu.restype = ctypes.c_int
@@ -187,6 +190,13 @@ def rowops_online_softmax_status(workspace: torch.Tensor, *, stream=None) -> int
     """Synchronise the stream and return the device-side status of the last
     rowops_online_softmax call on ``workspace`` (0 = ROWOPS_OK)."""
     return int(library().rowops_online_softmax_status(workspace.data_ptr(), _stream(stream)))
+
+
+def rowops_device_status(*, stream=None) -> int:
+    """Synchronise the stream, then read and clear the library's device error
+    word on the current device (0 = ROWOPS_OK, 5 = a bounded device-side wait
+    gave up)."""
+    return int(library().rowops_device_status(_stream(stream)))
 
 
 def rowops_online_softmax_noalloc(

@@ -179,6 +179,7 @@ def test_ln_gelu_every_register_variant(oracle, monkeypatch, dtype, tpr, vpt, of
     N = tpr * vpt * vec - (0 if offset == 0 else 3)
     if 8 * ((N + 3) // 4 * 4) > 200 * 1024:
         pytest.skip("affine staging would not fit shared memory; the looped kernel takes this size")
+    monkeypatch.setenv("ROWOPS_KERNEL", "reg")
     monkeypatch.setenv("ROWOPS_FORCE_TPR", str(tpr))
     monkeypatch.setenv("ROWOPS_FORCE_VPT", str(vpt))
     check(oracle, edge(dtype, 2 * (1024 // tpr) + 1, N, seed=tpr + vpt), offset=offset)
@@ -196,3 +197,47 @@ def test_ln_gelu_forced_looped(oracle, monkeypatch, dtype):
     monkeypatch.setenv("ROWOPS_FORCE_LOOPED", "1")
     check(oracle, edge(dtype, 41, 4097), offset=1)
     check(oracle, edge(dtype, 41, 768))
+
+
+TMA_VARIANTS = [(b, v) for b in (64, 128, 256, 512) for v in (1, 2, 3, 4, 8)]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("block,vpt", TMA_VARIANTS)
+@pytest.mark.parametrize("full", [True, False])
+def test_ln_gelu_every_tma_variant(oracle, monkeypatch, dtype, block, vpt, full):
+    """Each TMA-fed row-pipeline instantiation, forced (thread-major w/b
+    staging included): rows of exactly block * vpt vectors and one shorter."""
+    vec = 4 if dtype == "f32" else 8
+    nvec = block * vpt - (0 if full else 1)
+    if nvec < 64:
+        pytest.skip("the row pipeline takes rows of at least 64 vectors")
+    N = nvec * vec
+    es = 4 if dtype == "f32" else 2
+    if 2 * block * vpt * vec * 4 + 2 * ((N * es + 127) // 128 * 128) + 128 > 226 * 1024:
+        pytest.skip("w/b staging plus two row buffers exceed shared memory; another kernel takes this size")
+    monkeypatch.setenv("ROWOPS_KERNEL", "tma")
+    monkeypatch.setenv("ROWOPS_FORCE_TPR", str(block))
+    monkeypatch.setenv("ROWOPS_FORCE_VPT", str(vpt))
+    check(oracle, edge(dtype, 2 * 152 + 3, N, seed=block * vpt))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("ring", ["2", "5"])
+@pytest.mark.parametrize("ctas", ["0", "1", "-1"])
+@pytest.mark.parametrize("use_wb", [True, False])
+def test_ln_gelu_tma_ring_depths_grids_affine(oracle, monkeypatch, dtype, ring, ctas, use_wb):
+    monkeypatch.setenv("ROWOPS_KERNEL", "tma")
+    monkeypatch.setenv("ROWOPS_RING_BUFFERS", ring)
+    monkeypatch.setenv("ROWOPS_CTAS_PER_SM", ctas)
+    check(oracle, edge(dtype, 700, 2048), use_w=use_wb, use_b=use_wb)
+    from row_wise_reduction_gb300 import rowops_device_status
+
+    assert rowops_device_status() == 0
+
+
+def test_ln_gelu_tma_in_place_and_strided(oracle, monkeypatch):
+    monkeypatch.setenv("ROWOPS_KERNEL", "tma")
+    check(oracle, edge("bf16", 301, 8192), inplace=True)
+    check(oracle, edge("bf16", 301, 8192), ld=8192 + 64)
+    check(oracle, edge("f32", 77, 768), ld=768 + 4)

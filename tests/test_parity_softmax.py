@@ -157,6 +157,7 @@ def test_softmax_every_register_variant(oracle, monkeypatch, dtype, tpr, vpt):
     holds minus a ragged tail, on a misaligned base."""
     vec = 4 if dtype == "f32" else 8
     N = tpr * vpt * vec - 3
+    monkeypatch.setenv("ROWOPS_KERNEL", "reg")
     monkeypatch.setenv("ROWOPS_FORCE_TPR", str(tpr))
     monkeypatch.setenv("ROWOPS_FORCE_VPT", str(vpt))
     check(oracle, edge(dtype, 2 * (1024 // tpr) + 3, N, seed=tpr * 10 + vpt), offset=1)
@@ -175,3 +176,44 @@ def test_softmax_grid_modes(oracle, monkeypatch, dtype, ctas):
 def test_softmax_forced_looped(oracle, monkeypatch, dtype):
     monkeypatch.setenv("ROWOPS_FORCE_LOOPED", "1")
     check(oracle, edge(dtype, 65, 4097), offset=2)
+
+
+TMA_VARIANTS = [(b, v) for b in (64, 128, 256, 512) for v in (1, 2, 3, 4, 8)]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("block,vpt", TMA_VARIANTS)
+@pytest.mark.parametrize("full", [True, False])
+def test_softmax_every_tma_variant(oracle, monkeypatch, dtype, block, vpt, full):
+    """Each TMA-fed row-pipeline instantiation, forced: rows of exactly
+    block * vpt vectors (no predicates) and rows one vector shorter."""
+    vec = 4 if dtype == "f32" else 8
+    nvec = block * vpt - (0 if full else 1)
+    if nvec < 64:
+        pytest.skip("the row pipeline takes rows of at least 64 vectors")
+    monkeypatch.setenv("ROWOPS_KERNEL", "tma")
+    monkeypatch.setenv("ROWOPS_FORCE_TPR", str(block))
+    monkeypatch.setenv("ROWOPS_FORCE_VPT", str(vpt))
+    check(oracle, edge(dtype, 3 * 152 + 5, nvec * vec, seed=block + vpt))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("ring", ["2", "3", "7", "16"])
+@pytest.mark.parametrize("ctas", ["0", "1", "-1"])
+def test_softmax_tma_ring_depths_and_grids(oracle, monkeypatch, dtype, ring, ctas):
+    """Ring depths (rows in flight per CTA) with persistent and one-row-per-CTA
+    grids; 1000 rows so every CTA wraps around its ring several times."""
+    monkeypatch.setenv("ROWOPS_KERNEL", "tma")
+    monkeypatch.setenv("ROWOPS_RING_BUFFERS", ring)
+    monkeypatch.setenv("ROWOPS_CTAS_PER_SM", ctas)
+    check(oracle, edge(dtype, 1000, 2048))
+    from row_wise_reduction_gb300 import rowops_device_status
+
+    assert rowops_device_status() == 0
+
+
+def test_softmax_tma_in_place_and_strided(oracle, monkeypatch):
+    monkeypatch.setenv("ROWOPS_KERNEL", "tma")
+    check(oracle, edge("bf16", 301, 4096), inplace=True)
+    check(oracle, edge("bf16", 301, 4096), ld=4096 + 64)
+    check(oracle, edge("f32", 77, 1024), ld=1024 + 4)
