@@ -39,7 +39,8 @@
  *   ROWOPS_FORCE_TPR=<16..1024>   threads per row (tma: 64..512)
  *   ROWOPS_FORCE_VPT=<n>          16-byte vectors per thread (reg: 1..4; tma: 1, 2, 3, 4, 8)
  *   ROWOPS_FORCE_LOOPED=1         same as ROWOPS_KERNEL=looped
- *   ROWOPS_RING_BUFFERS=<2..16>   rows in flight per CTA of the row pipeline
+ *   ROWOPS_RING_BUFFERS=<2..16>   rows in flight per row group of the row pipeline
+ *   ROWOPS_ROWS_PER_CTA=<1|2|4>   row groups per CTA of the LayerNorm+GELU row pipeline
  *   ROWOPS_CTAS_PER_SM=<k>        persistent grid of k CTAs per SM (0 = occupancy limit,
  *                                 -1 = one CTA per row group, no persistence)
  */

@@ -95,35 +95,53 @@ __device__ __forceinline__ uint4 lds16(const void* p) {
     return v;
 }
 
-// CTA-wide reductions (one row per CTA, BLOCK threads, BLOCK a multiple of 64)
-// whose barrier also ORs a per-thread failure flag across the CTA.
-template <int BLOCK, class Op>
-__device__ __forceinline__ float cta_reduce(float v, float* red, Op op, int& fail) {
+// Row-group reductions for the pipeline kernels. A row is owned by the TPR
+// threads of group g = threadIdx.x / TPR (TPR a multiple of 64); the group
+// synchronises on its own named barrier 1 + g (0 is __syncthreads), so row
+// groups of one CTA run independently. The barrier also ORs a per-thread
+// failure flag across the group. `red` is the group's slice of TPR / 32 floats
+// (2 * TPR / 32 for the two-value form).
+__device__ __forceinline__ int group_bar_or(int id, int nthreads, int flag) {
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.s32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.s32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(flag), "r"(id), "r"(nthreads)
+        : "memory");
+    return r;
+}
+
+template <int TPR, class Op>
+__device__ __forceinline__ float row_reduce(float v, float* red, int bar_id, Op op, int& fail) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(0xffffffffu, v, o));
-    constexpr int W = BLOCK / 32;
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    fail = __syncthreads_or(fail);
+    constexpr int W = TPR / 32;
+    const int w = (threadIdx.x % TPR) >> 5;
+    if ((threadIdx.x & 31) == 0) red[w] = v;
+    fail = group_bar_or(bar_id, TPR, fail);
     v = red[0];
 #pragma unroll
     for (int i = 1; i < W; ++i) v = op(v, red[i]);
     return v;
 }
 
-template <int BLOCK>
-__device__ __forceinline__ void cta_reduce_sum2(float& a, float& b, float* red, int& fail) {
+template <int TPR>
+__device__ __forceinline__ void row_reduce_sum2(float& a, float& b, float* red, int bar_id, int& fail) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         a += __shfl_xor_sync(0xffffffffu, a, o);
         b += __shfl_xor_sync(0xffffffffu, b, o);
     }
-    constexpr int W = BLOCK / 32;
-    const int w = threadIdx.x >> 5;
+    constexpr int W = TPR / 32;
+    const int w = (threadIdx.x % TPR) >> 5;
     if ((threadIdx.x & 31) == 0) {
         red[2 * w] = a;
         red[2 * w + 1] = b;
     }
-    fail = __syncthreads_or(fail);
+    fail = group_bar_or(bar_id, TPR, fail);
     a = red[0];
     b = red[1];
 #pragma unroll
@@ -142,7 +160,8 @@ struct RowRing {
     __device__ __forceinline__ char* slot(int s) const { return buf + size_t(s) * row_bytes; }
 };
 
-// Bytes of dynamic shared memory before the row buffers (barriers, padded).
+// Bytes of dynamic shared memory before the row buffers: the mbarriers of all
+// row groups' rings (ROWS * nbuf <= 16), padded.
 constexpr uint32_t kRingHeader = 128;
 constexpr int kMaxRingBuffers = 16;
 

@@ -55,6 +55,17 @@ TmaSoftmaxLaunch softmax_tma_bf16(int block_index, int vpt_index, bool full);
 TmaLnGeluLaunch ln_gelu_tma_f32(int block_index, int vpt_index, bool full);
 TmaLnGeluLaunch ln_gelu_tma_bf16(int block_index, int vpt_index, bool full);
 
+// LayerNorm+GELU with several row groups per CTA sharing one staging of w, b
+// (full rows only): TPR in kTmaMultiTpr, VPT in kTmaMultiVpt, ROWS in kTmaMultiRows.
+constexpr int kTmaMultiTpr[] = {128, 256};
+constexpr int kNumTmaMultiTpr = 2;
+constexpr int kTmaMultiVpt[] = {2, 4, 8};
+constexpr int kNumTmaMultiVpt = 3;
+constexpr int kTmaMultiRows[] = {2, 4};
+constexpr int kNumTmaMultiRows = 2;
+TmaLnGeluLaunch ln_gelu_tma_multi_f32(int tpr_index, int vpt_index, int rows_index);
+TmaLnGeluLaunch ln_gelu_tma_multi_bf16(int tpr_index, int vpt_index, int rows_index);
+
 // dynamic shared memory of the row-pipeline kernels
 inline size_t tma_row_bytes(int64_t N, int es) { return size_t((N * es + 127) / 128 * 128); }
 inline size_t tma_ring_smem(int64_t N, int es, int nbuf) { return kTmaRingHeader + size_t(nbuf) * tma_row_bytes(N, es); }

@@ -219,7 +219,31 @@ def test_ln_gelu_every_tma_variant(oracle, monkeypatch, dtype, block, vpt, full)
     monkeypatch.setenv("ROWOPS_KERNEL", "tma")
     monkeypatch.setenv("ROWOPS_FORCE_TPR", str(block))
     monkeypatch.setenv("ROWOPS_FORCE_VPT", str(vpt))
+    monkeypatch.setenv("ROWOPS_ROWS_PER_CTA", "1")
     check(oracle, edge(dtype, 2 * 152 + 3, N, seed=block * vpt))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("tpr", [128, 256])
+@pytest.mark.parametrize("vpt", [2, 4, 8])
+@pytest.mark.parametrize("rows", [2, 4])
+def test_ln_gelu_multi_row_groups(oracle, monkeypatch, dtype, tpr, vpt, rows):
+    """Several independent row groups per CTA sharing one w/b staging, each with
+    its own ring and named barrier; M not a multiple of the group count."""
+    vec = 4 if dtype == "f32" else 8
+    es = 4 if dtype == "f32" else 2
+    N = tpr * vpt * vec
+    if 2 * tpr * vpt * vec * 4 + rows * 2 * ((N * es + 127) // 128 * 128) + 128 > 226 * 1024:
+        pytest.skip("does not fit shared memory; the dispatcher picks fewer row groups")
+    monkeypatch.setenv("ROWOPS_KERNEL", "tma")
+    monkeypatch.setenv("ROWOPS_FORCE_TPR", str(tpr))
+    monkeypatch.setenv("ROWOPS_FORCE_VPT", str(vpt))
+    monkeypatch.setenv("ROWOPS_ROWS_PER_CTA", str(rows))
+    check(oracle, edge(dtype, 152 * rows + 3, N, seed=tpr + vpt + rows))
+    check(oracle, edge(dtype, 5, N, seed=7), inplace=True)
+    from row_wise_reduction_gb300 import rowops_device_status
+
+    assert rowops_device_status() == 0
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
