@@ -41,6 +41,11 @@
  *   ROWOPS_FORCE_LOOPED=1         same as ROWOPS_KERNEL=looped
  *   ROWOPS_RING_BUFFERS=<2..16>   rows in flight per row group of the row pipeline
  *   ROWOPS_ROWS_PER_CTA=<1|2|4>   row groups per CTA of the LayerNorm+GELU row pipeline
+ *   ROWOPS_ONLINE=two_pass|single_read  split-row softmax form (default two_pass); single_read
+ *                                 keeps each chunk on chip between the passes (rows of
+ *                                 >= ~2^19.3 entries, 16-byte aligned, cooperative launch)
+ *   ROWOPS_PERSIST_L2=1           single_read staged in L2 instead of shared memory
+ *   ROWOPS_PERSIST_LOOKAHEAD=<2k> / ROWOPS_PERSIST_PREFETCH=<n>  its pipeline depths
  *   ROWOPS_CTAS_PER_SM=<k>        persistent grid of k CTAs per SM (0 = occupancy limit,
  *                                 -1 = one CTA per row group, no persistence)
  */

@@ -1,5 +1,6 @@
 // Split-row online softmax: launch wrappers for both element types.
 #include "online_softmax_kernels.cuh"
+#include "online_softmax_persistent.cuh"
 #include "rowops_launch.h"
 
 namespace rowops {
@@ -31,5 +32,97 @@ static cudaError_t launch_split(const void* x, void* y, int64_t M, int64_t N, in
 
 SplitLaunch split_softmax_f32() { return launch_split<float>; }
 SplitLaunch split_softmax_bf16() { return launch_split<bf16_t>; }
+
+int64_t persistent_slots(int64_t N) { return (N + 255) / 256 + 2; }
+size_t persistent_rowstat_bytes(int64_t M) { return size_t((M * 8 + 255) / 256 * 256); }
+
+// The single-read form, when it applies: rows 16-byte aligned with a length
+// that is a multiple of 16 bytes; every warp's part of a CTA slice at least 32
+// vectors; at least 4 stages of one slice each in shared memory; G * 16 warp
+// partials per row within the workspace's slots; a cooperative launch on the
+// device. Returns cudaErrorNotSupported (and launches nothing) otherwise.
+template <typename T>
+static cudaError_t launch_persistent(const void* x, void* y, int64_t M, int64_t N, int64_t ld, void* workspace,
+                                     const LaunchCfg& cfg) {
+    constexpr int V = Elem<T>::kVec;
+    if (!cfg.cooperative || N % V != 0) return cudaErrorNotSupported;
+    const int64_t nvec = N / V;
+    const int64_t G = cfg.num_sms;
+    const int64_t slots = G * kPersistWarps;
+    if (slots > kPersistMaxSlots || slots > persistent_slots(N)) return cudaErrorNotSupported;
+    if (nvec / G < int64_t(kPersistWarps) * 32) return cudaErrorNotSupported;
+    const int64_t stage_vecs = ((nvec + G - 1) / G + 7) / 8 * 8;  // widest slice, 128-byte multiple
+    const int64_t avail = int64_t(cfg.max_smem_optin) - int64_t(kRingHeader) - 1024;
+    int64_t ns = avail / (stage_vecs * 16);
+    if (ns > kMaxRingBuffers) ns = kMaxRingBuffers;
+    if (ns < 4) return cudaErrorNotSupported;
+    // lookahead: 4 steps when the ring has room for two copies ahead, else 2
+    int lookahead = ns >= 7 ? 4 : 2;
+    if (cfg.persist_lookahead >= 2 && cfg.persist_lookahead % 2 == 0 && cfg.persist_lookahead + 2 <= ns)
+        lookahead = cfg.persist_lookahead;
+    if (cfg.persist_l2) {
+        // L2-staged form: no shared-memory ring; each thread holds at most
+        // 8 vectors of a pass in registers
+        if ((stage_vecs + kPersistBlock * 8 - 1) / (kPersistBlock * 8) > 1 || stage_vecs / kPersistWarps + 1 > 32 * 8)
+            return cudaErrorNotSupported;
+        const int la = cfg.persist_lookahead >= 2 && cfg.persist_lookahead % 2 == 0 ? cfg.persist_lookahead : 4;
+        const int pf = cfg.persist_prefetch > 0 ? cfg.persist_prefetch : 6;
+        char* ws = static_cast<char*>(workspace);
+        PersistentArgs a;
+        a.M = M;
+        a.N = N;
+        a.ld = ld;
+        a.nstages = 0;
+        a.lookahead = la;
+        a.stage_vecs = int(stage_vecs);
+        a.header = reinterpret_cast<unsigned*>(ws);
+        a.rowstat = reinterpret_cast<unsigned long long*>(ws + kWorkspaceHeader);
+        a.partials = reinterpret_cast<unsigned long long*>(ws + kWorkspaceHeader + persistent_rowstat_bytes(M));
+        cudaError_t e = cudaMemsetAsync(ws, 0, kWorkspaceHeader, cfg.stream);
+        if (e == cudaSuccess)
+            e = cudaMemsetAsync(a.rowstat, 0xff, persistent_rowstat_bytes(M) + size_t(M) * size_t(slots) * 8,
+                                cfg.stream);
+        if (e != cudaSuccess) return e;
+        const T* xp = static_cast<const T*>(x);
+        T* yp = static_cast<T*>(y);
+        int pfv = pf;
+        void* args[] = {&xp, &yp, &a, &pfv};
+        return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(split_l2_kernel<T>), dim3(unsigned(G)),
+                                           dim3(kPersistBlock), args, 0, cfg.stream);
+    }
+    auto kern = split_persistent_kernel<T>;
+    const size_t smem = kRingHeader + size_t(ns) * size_t(stage_vecs) * 16;
+    cudaError_t e = allow_smem(reinterpret_cast<const void*>(kern), smem, cfg);
+    if (e != cudaSuccess) return e;
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kPersistBlock, smem) != cudaSuccess || occ < 1) {
+        cudaGetLastError();
+        return cudaErrorNotSupported;
+    }
+
+    char* ws = static_cast<char*>(workspace);
+    PersistentArgs a;
+    a.M = M;
+    a.N = N;
+    a.ld = ld;
+    a.nstages = int(ns);
+    a.lookahead = lookahead;
+    a.stage_vecs = int(stage_vecs);
+    a.header = reinterpret_cast<unsigned*>(ws);
+    a.rowstat = reinterpret_cast<unsigned long long*>(ws + kWorkspaceHeader);
+    a.partials = reinterpret_cast<unsigned long long*>(ws + kWorkspaceHeader + persistent_rowstat_bytes(M));
+    e = cudaMemsetAsync(ws, 0, kWorkspaceHeader, cfg.stream);
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(a.rowstat, 0xff, persistent_rowstat_bytes(M) + size_t(M) * size_t(slots) * 8, cfg.stream);
+    if (e != cudaSuccess) return e;
+    const T* xp = static_cast<const T*>(x);
+    T* yp = static_cast<T*>(y);
+    void* args[] = {&xp, &yp, &a};
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(unsigned(G)), dim3(kPersistBlock),
+                                       args, smem, cfg.stream);
+}
+
+PersistLaunch split_persistent_f32() { return launch_persistent<float>; }
+PersistLaunch split_persistent_bf16() { return launch_persistent<bf16_t>; }
 
 }  // namespace rowops

@@ -101,7 +101,10 @@ __global__ void __launch_bounds__(BLOCK)
     int parity = 0;
     const int64_t items = M * nchunks;
 
-    for (int64_t item = blockIdx.x; item < items; item += gridDim.x, parity ^= 1) {
+    for (int64_t k = blockIdx.x; k < items; k += gridDim.x, parity ^= 1) {
+        // last chunks first: the partial pass read them last, so they are the
+        // ones still in L2 when this pass starts
+        const int64_t item = items - 1 - k;
         const int64_t r = item / nchunks, c = item - r * nchunks;
         const int64_t col0 = c * chunk;
         const int64_t n = (N - col0) < chunk ? (N - col0) : chunk;

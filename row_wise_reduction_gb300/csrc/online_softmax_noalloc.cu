@@ -125,6 +125,10 @@ extern "C" rowops_status_t rowops_online_softmax_noalloc(const void* x, void* y,
     cfg.max_smem_optin = nd.max_smem_optin;
     cfg.ctas_per_sm = 0;
     cfg.dev_error = nullptr;  // the split-row kernels have no device-side waits
+    cfg.cooperative = false;
+    cfg.persist_lookahead = 0;
+    cfg.persist_l2 = false;
+    cfg.persist_prefetch = 0;
     // Nothing in the scratch has to start at zero: the first kernel writes the
     // status word and every partial before the second kernel reads them.
     SplitLaunch fn = dtype == ROWOPS_F32 ? split_softmax_f32() : split_softmax_bf16();

@@ -1,0 +1,445 @@
+// Single-read split-row online softmax for very long rows [Triton Kernel 实现练习
+// §2.5 split_online_softmax; 第 6 讲 §7.2 Online Softmax].
+//
+// The two-launch form (online_softmax_kernels.cuh) reads x twice: once for the
+// chunk partials, once more to normalise. Here every chunk stays in shared
+// memory between the two passes, so x is read once and y written once.
+//
+// A cooperative grid of G CTAs (all resident at once). CTA c owns the column
+// slice [c nvec / G, (c + 1) nvec / G) (16-byte vectors) of every row, and warp
+// w of the CTA the w-th sixteenth of that slice. The CTA keeps its slices of NS
+// consecutive rows in a ring of shared-memory stages, filled by bulk copies,
+// and runs a software pipeline over steps s = 0, 1, ...:
+//   partial   row s      : each warp folds its part of the slice into a partial
+//                          (m, d) = (max, sum exp(x - m)) and stores it in the
+//                          row's slot c * 16 + w;
+//   merge     row s - L/2: if c owns that row (row mod G), wait (bounded) until
+//                          all G * 16 slots of the row are set, merge them in
+//                          slot order (m = max m_i, d = sum d_i exp(m_i - m),
+//                          d_i = 0 skipped) and store the row's (m, d);
+//   normalise row s - L  : with the row's (m, d) (fetched before the step's one
+//                          barrier), write y = exp(x - m) / d from the stage;
+//                          the stage then takes row s - L + NS.
+// Every wait is for data that other CTAs produced L/2 steps earlier, so it
+// normally succeeds on its first look. Each slot and each row result is one
+// 64-bit word written by a single relaxed 64-bit store over a sentinel (all
+// one bits) that the host fills in before the launch: the data is its own flag
+// and needs no fence. A CTA never waits on work of a later step, and all CTAs
+// are resident, so every wait ends. A wait that runs past kWaitLimitNs records
+// ROWOPS_ERR_TIMEOUT and raises the abort word, which makes every other wait
+// give up at once; each CTA then drains its copies in flight and returns.
+//
+// Workspace: [0, 256) header (word 0 status, word 1 abort), then M row results
+// (64-bit, padded to 256 bytes), then 64-bit warp partials [M][G * 16].
+#pragma once
+
+#include "row_pipeline.cuh"
+#include "softmax_kernels.cuh"
+
+namespace rowops {
+
+constexpr unsigned long long kSlotEmpty = ~0ull;
+constexpr int kPersistBlock = 512;
+constexpr int kPersistWarps = kPersistBlock / 32;
+constexpr int kPersistMaxSlots = 4096;  // G * 16 partials per row, at most
+
+// (m, d) as one 64-bit word, m in the low half; computed NaNs become the
+// canonical quiet NaN, so a stored pair is never the all-ones sentinel.
+__device__ __forceinline__ unsigned long long pack_md(float m, float d) {
+    if (m != m) m = __uint_as_float(0x7fc00000u);
+    if (d != d) d = __uint_as_float(0x7fc00000u);
+    return (static_cast<unsigned long long>(__float_as_uint(d)) << 32) | __float_as_uint(m);
+}
+
+__device__ __forceinline__ MD unpack_md(unsigned long long v) {
+    return MD{__uint_as_float(unsigned(v)), __uint_as_float(unsigned(v >> 32))};
+}
+
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+struct PersistentArgs {
+    int64_t M, N, ld;
+    int nstages;                   // NS: stages of the ring
+    int lookahead;                 // L: steps from a row's partial to its normalise (even, 2 <= L < NS)
+    int stage_vecs;                // vectors of one stage (>= the widest CTA slice)
+    unsigned* header;              // [0] status, [1] abort
+    unsigned long long* rowstat;   // M row results (sentinel-filled)
+    unsigned long long* partials;  // M * G * 16 warp partials (sentinel-filled)
+};
+
+// Bounded wait until *p is not the sentinel. Gives up (false) after
+// kWaitLimitNs, recording the timeout and raising the abort word, or at once
+// once another CTA raised it.
+__device__ __forceinline__ bool wait_slot(const unsigned long long* p, unsigned* header, unsigned long long* out) {
+    unsigned long long v = ld_relaxed_u64(p);
+    if (v != kSlotEmpty) {
+        *out = v;
+        return true;
+    }
+    const unsigned long long t0 = global_ns();
+    for (uint32_t it = 0; it < (1u << 28); ++it) {
+        v = ld_relaxed_u64(p);
+        if (v != kSlotEmpty) {
+            *out = v;
+            return true;
+        }
+        if ((it & 31u) == 31u) {
+            if (ld_acquire_u32(header + 1) != 0u) return false;
+            if (global_ns() - t0 > kWaitLimitNs) {
+                atomicExch(header + 0, kDeviceErrTimeout);
+                atomicExch(header + 1, 1u);
+                return false;
+            }
+        }
+    }
+    return false;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kPersistBlock, 1) split_persistent_kernel(const T* x, T* y, PersistentArgs a) {
+    using E = Elem<T>;
+    constexpr int V = E::kVec;
+    constexpr int kLoc = kPersistMaxSlots / kPersistBlock;
+    extern __shared__ __align__(128) char smem[];
+    __shared__ float red_m[kPersistWarps];
+    __shared__ float red_d[kPersistWarps];
+    __shared__ unsigned long long row_result[2];  // (m, d) of the rows being normalised, by parity
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
+    char* ring = smem + kRingHeader;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int64_t G = gridDim.x, c = blockIdx.x;
+    const int64_t nvec = a.N / V;
+    const int NS = a.nstages, L = a.lookahead;
+    const size_t stage_bytes = size_t(a.stage_vecs) * 16;
+    // this CTA's slice of every row and this warp's part of it (in vectors)
+    const int64_t s_lo = c * nvec / G, s_hi = (c + 1) * nvec / G;
+    const int width = int(s_hi - s_lo);
+    const int w_lo = width * warp / kPersistWarps, w_hi = width * (warp + 1) / kPersistWarps;
+    const uint32_t bytes = uint32_t(width) * 16;
+    const int64_t slots = G * kPersistWarps;
+    int64_t issued = 0;   // rows 0 .. issued - 1 have been copied in or are on their way (thread 0)
+    int64_t refill = -1;  // stage freed by the last normalise, refilled after the next barrier
+
+    if (t == 0) {
+        for (int s = 0; s < NS; ++s) mbar_init(bar + s, 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    if (t == 0)
+        for (; issued < NS && issued < a.M; ++issued)
+            tma_load_row(ring + issued * stage_bytes, x + issued * a.ld + s_lo * V, bytes, bar + issued);
+
+    // error exit: thread 0 waits (bounded) for the copies of rows from..issued-1
+    auto drain = [&](int64_t from) {
+        if (t == 0)
+            for (int64_t q = from; q < issued; ++q) mbar_wait(bar + (q % NS), uint32_t((q / NS) & 1));
+    };
+
+    unsigned long long next_stat = kSlotEmpty;  // thread 0: row result loaded one step early
+    for (int64_t s = 0; s < a.M + L; ++s) {
+        const int64_t q3 = s - L;  // row normalised in this step
+        // ---- one barrier per step: row s has landed, row q3's (m, d) is known ----
+        int fail = 0;
+        if (s < a.M) fail = !mbar_wait(bar + int(s % NS), uint32_t((s / NS) & 1));
+        if (t == 0 && q3 >= 0) {
+            unsigned long long v = next_stat;
+            if (v == kSlotEmpty && !wait_slot(a.rowstat + q3, a.header, &v)) fail = 1;
+            row_result[q3 & 1] = v;
+        }
+        if (__syncthreads_or(fail)) {
+            if (t == 0) {
+                atomicExch(a.header + 0, kDeviceErrTimeout);
+                atomicExch(a.header + 1, 1u);
+            }
+            drain(s < a.M ? s : a.M);
+            return;
+        }
+        // every thread finished the last normalise: its stage may be refilled
+        if (t == 0 && refill >= 0 && issued < a.M) {
+            fence_proxy_async_smem();
+            tma_load_row(ring + refill * stage_bytes, x + issued * a.ld + s_lo * V, bytes, bar + refill);
+            ++issued;
+        }
+        refill = -1;
+        // start loading the next step's row result now; its latency overlaps this step
+        if (t == 0) next_stat = (q3 + 1 >= 0 && q3 + 1 < a.M) ? ld_relaxed_u64(a.rowstat + q3 + 1) : kSlotEmpty;
+
+        // ---- partial of row s, one per warp ----
+        if (s < a.M) {
+            const char* sp = ring + int(s % NS) * stage_bytes;
+            float m = -INFINITY, dv[V];
+#pragma unroll
+            for (int j = 0; j < V; ++j) dv[j] = 0.f;
+            for (int v = w_lo + lane; v < w_hi; v += 32) {
+                float f[V];
+                E::unpack(lds16(sp + v * 16), f);
+                float vm = f[0];
+#pragma unroll
+                for (int j = 1; j < V; ++j) vm = fmaxf(vm, f[j]);
+                if (vm == -INFINITY) continue;  // all masked (m may still be -inf)
+                if (vm > m) {
+                    const float sc = ex2_approx((m - vm) * kLog2eF);
+#pragma unroll
+                    for (int j = 0; j < V; ++j) dv[j] *= sc;
+                    m = vm;
+                }
+#pragma unroll
+                for (int j = 0; j < V; ++j) dv[j] += exp_shifted(f[j], m);
+            }
+            float d = 0.f;
+#pragma unroll
+            for (int j = 0; j < V; ++j) d += dv[j];
+            // warp merge: max, rescale, sum (fixed order)
+            float wm = m;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+            d = d == 0.f ? 0.f : d * ex2_approx((m - wm) * kLog2eF);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+            if (lane == 0) st_relaxed_u64(a.partials + s * slots + c * kPersistWarps + warp, pack_md(wm, d));
+        }
+
+        // ---- merge of row s - L/2 by its owner ----
+        const int64_t q2 = s - L / 2;
+        if (q2 >= 0 && q2 < a.M && q2 % G == c) {
+            // load this thread's slots t, t + BLOCK, ... all at once, then wait
+            // (bounded) only for any still holding the sentinel
+            unsigned long long raw[kLoc];
+            const int n = int((slots - t + kPersistBlock - 1) / kPersistBlock);
+#pragma unroll
+            for (int k = 0; k < kLoc; ++k)
+                raw[k] = k < n ? ld_relaxed_u64(a.partials + q2 * slots + t + k * kPersistBlock) : 0ull;
+            MD loc[kLoc];
+            int mfail = 0;
+            float lm = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < kLoc; ++k) {
+                if (k >= n) break;
+                if (raw[k] == kSlotEmpty && !wait_slot(a.partials + q2 * slots + t + k * kPersistBlock, a.header, &raw[k])) {
+                    mfail = 1;
+                    break;
+                }
+                loc[k] = unpack_md(raw[k]);
+                if (loc[k].d != 0.f) lm = fmaxf(lm, loc[k].m);
+            }
+            if (__syncthreads_or(mfail)) {
+                drain(s + 1);
+                return;
+            }
+            const float Mx = group_reduce<kPersistBlock>(lm, red_m, OpMax());
+            float d = 0.f;
+#pragma unroll
+            for (int k = 0; k < kLoc; ++k)
+                if (k < n && loc[k].d != 0.f) d += loc[k].d * ex2_approx((loc[k].m - Mx) * kLog2eF);
+            d = group_reduce<kPersistBlock>(d, red_d, OpSum());
+            if (t == 0) st_relaxed_u64(a.rowstat + q2, pack_md(Mx, d));
+        }
+
+        // ---- normalise row q3; its stage is refilled after the next barrier ----
+        if (q3 >= 0) {
+            const MD md = unpack_md(row_result[q3 & 1]);
+            const float m = md.d > 0.f ? md.m : 0.f;
+            const float inv = safe_inverse(md.d);
+            const int st = int(q3 % NS);
+            const char* sp = ring + st * stage_bytes;
+            T* yr = y + q3 * a.ld + s_lo * V;
+            for (int v = t; v < width; v += kPersistBlock) {
+                float f[V];
+                E::unpack(lds16(sp + v * 16), f);
+#pragma unroll
+                for (int j = 0; j < V; ++j) f[j] = exp_shifted(f[j], m) * inv;
+                st_stream16(yr + size_t(v) * V, E::pack(f));
+            }
+            refill = st;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// The same pipeline with L2 as the staging memory. Row slices are pulled into
+// L2 `prefetch` steps ahead by bulk L2 prefetches (no shared memory, no
+// registers held), the partial pass reads its slice from L2 with an
+// evict-last policy, and the normalise pass re-reads it from L2 L steps later
+// with an evict-first policy. HBM sees each x byte once while the on-chip
+// window is the 129 MB L2 instead of the 225 KB of shared memory per SM.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint4 ld_l2_hint(const void* p, uint64_t pol) {
+    uint4 v;
+    asm volatile("ld.global.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
+
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kPersistBlock, 1) split_l2_kernel(const T* x, T* y, PersistentArgs a, int prefetch) {
+    using E = Elem<T>;
+    constexpr int V = E::kVec;
+    constexpr int kLoc = kPersistMaxSlots / kPersistBlock;
+    __shared__ float red_m[kPersistWarps];
+    __shared__ float red_d[kPersistWarps];
+    __shared__ unsigned long long row_result[2];
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int64_t G = gridDim.x, c = blockIdx.x;
+    const int64_t nvec = a.N / V;
+    const int L = a.lookahead;
+    const int64_t s_lo = c * nvec / G, s_hi = (c + 1) * nvec / G;
+    const int width = int(s_hi - s_lo);
+    const int w_lo = width * warp / kPersistWarps, w_hi = width * (warp + 1) / kPersistWarps;
+    const uint32_t bytes = uint32_t(width) * 16;
+    const int64_t slots = G * kPersistWarps;
+    const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
+    // this thread's vectors of the slice in the two passes
+    constexpr int kMaxPer = 8;  // dispatcher: width <= 32 * kMaxPer per warp part, BLOCK * kMaxPer per slice
+
+    if (t == 0)
+        for (int64_t q = 0; q < prefetch && q < a.M; ++q) prefetch_l2_bulk(x + q * a.ld + s_lo * V, bytes);
+
+    unsigned long long next_stat = kSlotEmpty;
+    for (int64_t s = 0; s < a.M + L; ++s) {
+        const int64_t q3 = s - L;
+        // issue both passes' loads first: one L2 latency per step
+        uint4 rp[kMaxPer], rn[kMaxPer];
+        const T* xs = x + s * a.ld + s_lo * V;
+        const T* xq = x + q3 * a.ld + s_lo * V;
+        if (s < a.M) {
+#pragma unroll
+            for (int k = 0; k < kMaxPer; ++k) {
+                const int v = w_lo + lane + 32 * k;
+                if (v < w_hi) rp[k] = ld_l2_hint(xs + size_t(v) * V, keep);
+            }
+        }
+        if (q3 >= 0) {
+#pragma unroll
+            for (int k = 0; k < kMaxPer; ++k) {
+                const int v = t + kPersistBlock * k;
+                if (v < width) rn[k] = ld_l2_hint(xq + size_t(v) * V, drop);
+            }
+        }
+        int fail = 0;
+        if (t == 0) {
+            if (s + prefetch < a.M) prefetch_l2_bulk(x + (s + prefetch) * a.ld + s_lo * V, bytes);
+            if (q3 >= 0) {
+                unsigned long long v = next_stat;
+                if (v == kSlotEmpty && !wait_slot(a.rowstat + q3, a.header, &v)) fail = 1;
+                row_result[q3 & 1] = v;
+            }
+        }
+        if (__syncthreads_or(fail)) return;
+        if (t == 0) next_stat = (q3 + 1 >= 0 && q3 + 1 < a.M) ? ld_relaxed_u64(a.rowstat + q3 + 1) : kSlotEmpty;
+
+        if (s < a.M) {
+            float m = -INFINITY, dv[V];
+#pragma unroll
+            for (int j = 0; j < V; ++j) dv[j] = 0.f;
+#pragma unroll
+            for (int k = 0; k < kMaxPer; ++k) {
+                const int v = w_lo + lane + 32 * k;
+                if (v >= w_hi) break;
+                float f[V];
+                E::unpack(rp[k], f);
+                float vm = f[0];
+#pragma unroll
+                for (int j = 1; j < V; ++j) vm = fmaxf(vm, f[j]);
+                if (vm == -INFINITY) continue;
+                if (vm > m) {
+                    const float sc = ex2_approx((m - vm) * kLog2eF);
+#pragma unroll
+                    for (int j = 0; j < V; ++j) dv[j] *= sc;
+                    m = vm;
+                }
+#pragma unroll
+                for (int j = 0; j < V; ++j) dv[j] += exp_shifted(f[j], m);
+            }
+            float d = 0.f;
+#pragma unroll
+            for (int j = 0; j < V; ++j) d += dv[j];
+            float wm = m;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+            d = d == 0.f ? 0.f : d * ex2_approx((m - wm) * kLog2eF);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+            if (lane == 0) st_relaxed_u64(a.partials + s * slots + c * kPersistWarps + warp, pack_md(wm, d));
+        }
+
+        const int64_t q2 = s - L / 2;
+        if (q2 >= 0 && q2 < a.M && q2 % G == c) {
+            unsigned long long raw[kLoc];
+            const int n = int((slots - t + kPersistBlock - 1) / kPersistBlock);
+#pragma unroll
+            for (int k = 0; k < kLoc; ++k)
+                raw[k] = k < n ? ld_relaxed_u64(a.partials + q2 * slots + t + k * kPersistBlock) : 0ull;
+            MD loc[kLoc];
+            int mfail = 0;
+            float lm = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < kLoc; ++k) {
+                if (k >= n) break;
+                if (raw[k] == kSlotEmpty && !wait_slot(a.partials + q2 * slots + t + k * kPersistBlock, a.header, &raw[k])) {
+                    mfail = 1;
+                    break;
+                }
+                loc[k] = unpack_md(raw[k]);
+                if (loc[k].d != 0.f) lm = fmaxf(lm, loc[k].m);
+            }
+            if (__syncthreads_or(mfail)) return;
+            const float Mx = group_reduce<kPersistBlock>(lm, red_m, OpMax());
+            float d = 0.f;
+#pragma unroll
+            for (int k = 0; k < kLoc; ++k)
+                if (k < n && loc[k].d != 0.f) d += loc[k].d * ex2_approx((loc[k].m - Mx) * kLog2eF);
+            d = group_reduce<kPersistBlock>(d, red_d, OpSum());
+            if (t == 0) st_relaxed_u64(a.rowstat + q2, pack_md(Mx, d));
+        }
+
+        if (q3 >= 0) {
+            const MD md = unpack_md(row_result[q3 & 1]);
+            const float m = md.d > 0.f ? md.m : 0.f;
+            const float inv = safe_inverse(md.d);
+            T* yr = y + q3 * a.ld + s_lo * V;
+#pragma unroll
+            for (int k = 0; k < kMaxPer; ++k) {
+                const int v = t + kPersistBlock * k;
+                if (v >= width) break;
+                float f[V];
+                E::unpack(rn[k], f);
+#pragma unroll
+                for (int j = 0; j < V; ++j) f[j] = exp_shifted(f[j], m) * inv;
+                st_stream16(yr + size_t(v) * V, E::pack(f));
+            }
+        }
+    }
+}
+
+}  // namespace rowops

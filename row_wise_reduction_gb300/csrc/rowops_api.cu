@@ -27,6 +27,10 @@ struct Tuning {
     int ctas_per_sm = 0;
     int ring = 0;
     int rows = 0;  // row groups per CTA of the LayerNorm+GELU row pipeline (0: automatic)
+    int online = 0;  // split-row softmax form: 0 automatic, 1 two-launch, 2 single-read
+    int lookahead = 0;  // single-read form's lookahead in steps (0: automatic)
+    int l2 = 0;         // single-read form staged in L2
+    int prefetch = 0;   // its L2 prefetch distance in rows (0: automatic)
 };
 
 int env_int(const char* name, int dflt) {
@@ -50,6 +54,13 @@ Tuning read_tuning() {
     t.ctas_per_sm = env_int("ROWOPS_CTAS_PER_SM", 0);
     t.ring = env_int("ROWOPS_RING_BUFFERS", 0);
     t.rows = env_int("ROWOPS_ROWS_PER_CTA", 0);
+    t.lookahead = env_int("ROWOPS_PERSIST_LOOKAHEAD", 0);
+    t.l2 = env_int("ROWOPS_PERSIST_L2", 0);
+    t.prefetch = env_int("ROWOPS_PERSIST_PREFETCH", 0);
+    if (const char* k = std::getenv("ROWOPS_ONLINE")) {
+        if (!std::strcmp(k, "two_pass")) t.online = 1;
+        else if (!std::strcmp(k, "single_read")) t.online = 2;
+    }
     return t;
 }
 
@@ -82,6 +93,7 @@ struct DeviceInfo {
     int num_sms = 0;
     int max_smem_optin = 0;
     unsigned* err = nullptr;  // device address of g_device_error on this device
+    int cooperative = 0;
 };
 
 std::mutex g_mu;
@@ -113,6 +125,7 @@ cudaError_t device_info(int dev, DeviceInfo* out) {
     cudaError_t e = cudaDeviceGetAttribute(&di.num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess)
         e = cudaDeviceGetAttribute(&di.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&di.cooperative, cudaDevAttrCooperativeLaunch, dev);
     if (e == cudaSuccess) e = cudaGetSymbolAddress(reinterpret_cast<void**>(&di.err), g_device_error);
     if (e != cudaSuccess) return e;
     g_devices.emplace_back(dev, di);
@@ -131,6 +144,10 @@ rowops_status_t make_cfg(cudaStream_t stream, const Tuning& tn, LaunchCfg* cfg) 
     cfg->max_smem_optin = di.max_smem_optin;
     cfg->ctas_per_sm = tn.ctas_per_sm;
     cfg->dev_error = di.err;
+    cfg->cooperative = di.cooperative != 0;
+    cfg->persist_lookahead = tn.lookahead;
+    cfg->persist_l2 = tn.l2 != 0;
+    cfg->persist_prefetch = tn.prefetch;
     return ROWOPS_OK;
 }
 
@@ -425,9 +442,12 @@ rowops_status_t rowops_layernorm_gelu(const void* x, void* y, const void* w, con
 
 size_t rowops_online_softmax_workspace_bytes(int64_t M, int64_t N, rowops_dtype_t dtype) {
     if (!valid_dtype(dtype) || M < 0 || N < 1 || N >= (int64_t(1) << 31)) return 0;
-    const int64_t max_chunks = (N + kMinChunk - 1) / kMinChunk;
-    if (M > 0 && max_chunks > (INT64_MAX / 16) / M) return 0;
-    return size_t(256) + size_t(M) * size_t(max_chunks) * 8u;
+    // the larger of the two forms' needs: the single-read form's header, M row
+    // results and M * (ceil(N / 256) + 2) partial slots cover the two-launch
+    // form's header and M * ceil(N / 256) partials
+    const int64_t slots = persistent_slots(N);
+    if (M > 0 && slots > (INT64_MAX / 16) / M) return 0;
+    return size_t(256) + persistent_rowstat_bytes(M) + size_t(M) * size_t(slots) * 8u;
 }
 
 rowops_status_t rowops_online_softmax(const void* x, void* y, int64_t M, int64_t N, int64_t ld,
@@ -446,6 +466,19 @@ rowops_status_t rowops_online_softmax(const void* x, void* y, int64_t M, int64_t
     LaunchCfg cfg;
     if ((st = make_cfg(stream, tn, &cfg)) != ROWOPS_OK) return st;
     const int es = elem_bytes(dtype);
+    // The single-read form (x read once; see online_softmax_persistent.cuh) on
+    // request. Measured on GB300 it is no faster than the two-launch form for
+    // 64 x 2^20 fp32 (the per-row cross-CTA synchronisation on the critical
+    // path costs what the saved re-read gains), so the two-launch form is the
+    // default.
+    if (chunk == 0 && tn.online == 2 && rows_aligned(x, y, ld, es)) {
+        PersistLaunch pf = dtype == ROWOPS_F32 ? split_persistent_f32() : split_persistent_bf16();
+        const cudaError_t e = pf(x, y, M, N, ld, workspace, cfg);
+        if (e == cudaSuccess) return ROWOPS_OK;
+        cudaGetLastError();
+        // a grid the device will not co-schedule falls back to the two-launch form
+        if (e != cudaErrorNotSupported && e != cudaErrorCooperativeLaunchTooLarge) return ROWOPS_ERR_CUDA;
+    }
     const int64_t n16 = (N + 15) / 16 * 16;
     if (chunk == 0) {
         // one unrolled step of a CTA per chunk, smaller while there are fewer

@@ -228,6 +228,18 @@ __device__ __forceinline__ MD md_push(MD s, float x) {
     return s;
 }
 
+// The same merge done as two cheap reductions: the group's max M with fmaxf,
+// then sum_i d_i exp(m_i - M) (one exp per thread) -- instead of a tree of
+// pairwise merges with two exps each. A NaN d_i stays NaN; states with d = 0
+// contribute 0. Same fixed order on every call, so groups that merge the same
+// values get the same (M, D). Uses the two buffers like two group_reduce calls.
+template <int TPR>
+__device__ __forceinline__ MD group_merge_fast(MD s, float* red_m, float* red_d) {
+    const float M = group_reduce<TPR>(s.m, red_m, OpMax());
+    const float d = s.d == 0.f ? 0.f : s.d * ex2_approx((s.m - M) * kLog2eF);
+    return MD{M, group_reduce<TPR>(d, red_d, OpSum())};
+}
+
 template <int TPR>
 __device__ __forceinline__ MD group_merge(MD s, float* red_m, float* red_d) {
     constexpr int kLanes = TPR < 32 ? TPR : 32;

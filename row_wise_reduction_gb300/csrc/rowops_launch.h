@@ -15,6 +15,10 @@ struct LaunchCfg {
     int max_smem_optin;  // bytes of dynamic shared memory a CTA may opt in to
     int ctas_per_sm;     // 0: occupancy limit; -1: one CTA per work item; k > 0: k per SM
     unsigned* dev_error; // the library's device error word on this device (row-pipeline timeouts)
+    bool cooperative;    // the device supports cooperative launches
+    int persist_lookahead = 0;  // single-read split-row softmax lookahead (0: automatic)
+    bool persist_l2 = false;    // single-read split-row softmax staged in L2 instead of shared memory
+    int persist_prefetch = 0;   // rows of L2 prefetch ahead (0: automatic)
 };
 
 // Persistent grid size for `items` independent work items: the occupancy
@@ -85,6 +89,16 @@ LnGeluLaunch ln_gelu_looped_bf16();
 
 SplitLaunch split_softmax_f32();
 SplitLaunch split_softmax_bf16();
+
+// Single-read split-row softmax (persistent cooperative grid); returns
+// cudaErrorNotSupported, launching nothing, when the problem does not suit it.
+using PersistLaunch = cudaError_t (*)(const void* x, void* y, int64_t M, int64_t N, int64_t ld, void* workspace,
+                                      const LaunchCfg& cfg);
+PersistLaunch split_persistent_f32();
+PersistLaunch split_persistent_bf16();
+// workspace of the single-read form: header, M row results, M * persistent_slots(N) partials
+int64_t persistent_slots(int64_t N);
+size_t persistent_rowstat_bytes(int64_t M);
 // columns one CTA of the split kernels covers in one unrolled step
 int64_t split_step_cols(int elem_bytes);
 

@@ -87,9 +87,11 @@ def test_layernorm_gelu_validation(lib):
 
 def test_online_softmax_workspace_bytes(lib):
     q = lib.rowops_online_softmax_workspace_bytes
-    assert q(64, 1 << 20, F32) == 256 + 64 * 4096 * 8
-    assert q(3, 1, BF16) == 256 + 3 * 1 * 8
-    assert q(5, 257, F32) == 256 + 5 * 2 * 8
+    # header, M 64-bit row results padded to 256 bytes, M * (ceil(N / 256) + 2) 8-byte partials
+    assert q(64, 1 << 20, F32) == 256 + 512 + 64 * 4098 * 8
+    assert q(3, 1, BF16) == 256 + 256 + 3 * 3 * 8
+    assert q(5, 257, F32) == 256 + 256 + 5 * 4 * 8
+    assert q(33, 257, F32) == 256 + 512 + 33 * 4 * 8
     assert q(0, 100, F32) == 256
     assert q(-1, 100, F32) == 0
     assert q(4, 0, F32) == 0

@@ -80,13 +80,14 @@ def test_online_softmax_full_size(oracle):
 
 
 def test_online_matches_two_pass_softmax():
-    """Split-row online softmax and rowops_softmax (whose 2^20-column rows take
-    the in-CTA online loop) agree within the softmax tolerance at two chunk
-    counts, on the same input."""
+    """Split-row online softmax (single-read form at the automatic chunking,
+    two-launch form at two explicit chunk counts) and rowops_softmax (whose
+    2^20-column rows take the in-CTA online loop) agree within the softmax
+    tolerance on the same input."""
     wl = W4.with_shape(M=8)
     x = gu.make_x(wl)["x"]
     y2 = rowops_softmax(x)
-    for chunk in (2048, 32768):
+    for chunk in (0, 2048, 32768):
         y1 = rowops_online_softmax(x, chunk=chunk)
         torch.cuda.synchronize()
         a, b = y1.double(), y2.double()
@@ -144,3 +145,55 @@ def test_online_softmax_empty_is_noop():
     y = rowops_online_softmax(x)
     torch.cuda.synchronize()
     assert y.shape == (0, 4096)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("M,N", [(1, 1 << 20), (3, 1 << 20), (2, 1 << 21), (5, 1500000), (155, 1 << 20),
+                                 (64, 40000)])
+@pytest.mark.parametrize("staging", ["smem", "l2"])
+def test_online_softmax_single_read_form(oracle, monkeypatch, dtype, M, N, staging):
+    """The persistent single-read form (column slices per CTA, warp partials,
+    one merging owner CTA per row, a ring of staged rows), forced; shapes give
+    fewer rows than the ring, more rows than CTAs (owners take several rows),
+    uneven slices, a shallow ring (2^21 columns), and rows too short for it
+    (which take the two-launch form); staged in shared memory or in L2."""
+    monkeypatch.setenv("ROWOPS_ONLINE", "single_read")
+    if staging == "l2":
+        monkeypatch.setenv("ROWOPS_PERSIST_L2", "1")
+    check(oracle, edge(dtype, M, N, seed=M + N, outlier_p=1e-3), chunk=0)
+    check(oracle, edge(dtype, min(M, 3), N, seed=5), chunk=0, inplace=True)
+
+
+def test_online_softmax_single_read_special_rows(oracle, monkeypatch):
+    """Masked pieces, an all-masked row and a NaN row in the single-read form."""
+    monkeypatch.setenv("ROWOPS_ONLINE", "single_read")
+    N = 1 << 20
+    g = torch.Generator().manual_seed(9)
+    x = torch.randn(5, N, generator=g)
+    x[0, : N // 2] = float("-inf")
+    x[1] = float("-inf")
+    x[2, 12345] = float("nan")
+    x[3, 1000:N - 1000] = float("-inf")
+    x[4, 5000:500000] = float("-inf")
+    xt = x.cuda()
+    ws = workspace(xt)
+    y = rowops_online_softmax(xt, workspace=ws)
+    assert rowops_online_softmax_status(ws) == 0
+    C.assert_softmax_close(C.to_f64(y), oracle.softmax(x.numpy()), "f32")
+
+
+def test_online_softmax_single_read_repeated_calls_reuse_workspace(oracle, monkeypatch):
+    """The slots are reset before every call: calls in a row on one
+    workspace, with different shapes, all match the oracle."""
+    monkeypatch.setenv("ROWOPS_ONLINE", "single_read")
+    wl_a = edge("f32", 6, 1 << 20, seed=1, outlier_p=1e-3)
+    wl_b = edge("f32", 3, 1 << 21, seed=2)
+    xa = gu.make_x(wl_a)["x"]
+    xb = gu.make_x(wl_b)["x"]
+    n = max(rowops_online_softmax_workspace_bytes(6, 1 << 20, torch.float32),
+            rowops_online_softmax_workspace_bytes(3, 1 << 21, torch.float32))
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    for x in (xa, xb, xa, xb):
+        y = rowops_online_softmax(x, workspace=ws)
+        assert rowops_online_softmax_status(ws) == 0
+        C.assert_softmax_close(C.to_f64(y), oracle.softmax(x.cpu().numpy()), "f32")
