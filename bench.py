@@ -346,6 +346,79 @@ def config_block():
 
 
 # ---------------------------------------------------------------------------
+# the other workloads, reported beside the step (not part of its value)
+# ---------------------------------------------------------------------------
+EXTRA = ["softmax_f32_1024x768", "layernorm_gelu_f32_4096x768", "layernorm_gelu_bf16_65536x127",
+         "layernorm_gelu_bf16_65536x4097"]
+SMALL = {"softmax_f32_1024x768", "layernorm_gelu_f32_4096x768"}
+
+
+def run_extras(dev, stream, iters=50):
+    """Per workload: the kernel time with inputs hot in L2 (back to back), with
+    L2 flushed before each launch (a 512 MB write between launches, outside the
+    timed events), and per launch inside a CUDA graph of `iters` launches."""
+    import row_wise_reduction_gb300 as ro
+
+    flush = torch.empty(512 * 2**20, dtype=torch.uint8, device=dev)
+    out = {}
+    for name in EXTRA:
+        wl = workloads.WORKLOADS[name]
+        inp = workloads.make_inputs(wl, dev)
+        x, y = inp["x"], torch.empty_like(inp["x"])
+
+        def call():
+            if wl.op == "softmax":
+                ro.rowops_softmax(x, y)
+            else:
+                ro.rowops_layernorm_gelu(x, inp.get("w"), inp.get("b"), wl.eps, y)
+
+        for _ in range(5):
+            call()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(iters):
+            call()
+        b.record(stream)
+        torch.cuda.synchronize()
+        hot = a.elapsed_time(b) / iters / 1e3
+        rec = {"bytes": alg_bytes(wl), "hot_us": hot * 1e6, "hot_gbs": alg_bytes(wl) / hot / 1e9}
+        if name in SMALL:
+            cold = []
+            for _ in range(10):
+                flush.fill_(1)
+                a.record(stream)
+                call()
+                b.record(stream)
+                torch.cuda.synchronize()
+                cold.append(a.elapsed_time(b) / 1e3)
+            c = statistics.median(cold)
+            rec.update(cold_us=c * 1e6, cold_gbs=alg_bytes(wl) / c / 1e9)
+            g = torch.cuda.CUDAGraph()
+            s2 = torch.cuda.Stream()
+            s2.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s2):
+                call()
+                torch.cuda.synchronize()
+                with torch.cuda.graph(g, stream=s2):
+                    for _ in range(iters):
+                        call()
+            torch.cuda.synchronize()
+            g.replay()
+            torch.cuda.synchronize()
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            gt = a.elapsed_time(b) / iters / 1e3
+            rec.update(graph_us=gt * 1e6, graph_gbs=alg_bytes(wl) / gt / 1e9, l2_resident=True)
+        out[name] = rec
+        del inp, x, y
+    del flush
+    return out
+
+
+# ---------------------------------------------------------------------------
 # rowops arm
 # ---------------------------------------------------------------------------
 def run_rowops(args):
@@ -459,6 +532,10 @@ def run_rowops(args):
         e2e = {"value": eb / es / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "steps": ke, "ms_per_step": es / ke * 1e3}
 
+    extras = None
+    if rank == 0 and not args.no_extras and not args.ops and args.rows_scale == 1.0:
+        extras = run_extras(dev, stream)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         from oracle import oracle
@@ -497,6 +574,7 @@ def run_rowops(args):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches,
+        "extras": extras,
         "clocks": clocks.summary(),
         "device": torch.cuda.get_device_name(dev),
         "num_sms": torch.cuda.get_device_properties(dev).multi_processor_count,
@@ -516,6 +594,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the small and ragged-tail workloads")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--reference-budget-s", type=float, default=90.0)
     ap.add_argument("--clocks-csv", default=None, help="also log nvidia-smi clock samples to this CSV")

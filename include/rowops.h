@@ -48,6 +48,13 @@
  *   ROWOPS_PERSIST_LOOKAHEAD=<2k> / ROWOPS_PERSIST_PREFETCH=<n>  its pipeline depths
  *   ROWOPS_CTAS_PER_SM=<k>        persistent grid of k CTAs per SM (0 = occupancy limit,
  *                                 -1 = one CTA per row group, no persistence)
+ *   ROWOPS_WAIT_LIMIT_NS=<ns>     limit of every device-side wait (default 2 s)
+ *   ROWOPS_TEST_STALL_ROW=<row>   test hook for the timeout path: the wait that concerns this
+ *                                 row is made to run out (the row pipeline's bulk copy of it is
+ *                                 expected to bring 16 bytes more than it does; in the
+ *                                 single-read split softmax CTA 0 withholds that row's partial).
+ *                                 Nothing faults or hangs: the wait gives up at its limit, the
+ *                                 kernel records ROWOPS_ERR_TIMEOUT and returns.
  */
 #ifndef ROWOPS_H
 #define ROWOPS_H

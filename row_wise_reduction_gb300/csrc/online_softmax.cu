@@ -75,6 +75,8 @@ static cudaError_t launch_persistent(const void* x, void* y, int64_t M, int64_t 
         a.nstages = 0;
         a.lookahead = la;
         a.stage_vecs = int(stage_vecs);
+        a.wait_ns = cfg.wait_ns;
+        a.stall_row = cfg.stall_row;
         a.header = reinterpret_cast<unsigned*>(ws);
         a.rowstat = reinterpret_cast<unsigned long long*>(ws + kWorkspaceHeader);
         a.partials = reinterpret_cast<unsigned long long*>(ws + kWorkspaceHeader + persistent_rowstat_bytes(M));
@@ -108,6 +110,8 @@ static cudaError_t launch_persistent(const void* x, void* y, int64_t M, int64_t 
     a.nstages = int(ns);
     a.lookahead = lookahead;
     a.stage_vecs = int(stage_vecs);
+    a.wait_ns = cfg.wait_ns;
+    a.stall_row = cfg.stall_row;
     a.header = reinterpret_cast<unsigned*>(ws);
     a.rowstat = reinterpret_cast<unsigned long long*>(ws + kWorkspaceHeader);
     a.partials = reinterpret_cast<unsigned long long*>(ws + kWorkspaceHeader + persistent_rowstat_bytes(M));

@@ -129,6 +129,8 @@ extern "C" rowops_status_t rowops_online_softmax_noalloc(const void* x, void* y,
     cfg.persist_lookahead = 0;
     cfg.persist_l2 = false;
     cfg.persist_prefetch = 0;
+    cfg.wait_ns = 2000000000ull;
+    cfg.stall_row = -1;
     // Nothing in the scratch has to start at zero: the first kernel writes the
     // status word and every partial before the second kernel reads them.
     SplitLaunch fn = dtype == ROWOPS_F32 ? split_softmax_f32() : split_softmax_bf16();

@@ -25,7 +25,7 @@
 // 64-bit word written by a single relaxed 64-bit store over a sentinel (all
 // one bits) that the host fills in before the launch: the data is its own flag
 // and needs no fence. A CTA never waits on work of a later step, and all CTAs
-// are resident, so every wait ends. A wait that runs past kWaitLimitNs records
+// are resident, so every wait ends. A wait that runs past its limit records
 // ROWOPS_ERR_TIMEOUT and raises the abort word, which makes every other wait
 // give up at once; each CTA then drains its copies in flight and returns.
 //
@@ -79,12 +79,15 @@ struct PersistentArgs {
     unsigned* header;              // [0] status, [1] abort
     unsigned long long* rowstat;   // M row results (sentinel-filled)
     unsigned long long* partials;  // M * G * 16 warp partials (sentinel-filled)
+    unsigned long long wait_ns;    // limit of every wait
+    int64_t stall_row;             // test hook: CTA 0 withholds its partials of this row (-1: none)
 };
 
 // Bounded wait until *p is not the sentinel. Gives up (false) after
-// kWaitLimitNs, recording the timeout and raising the abort word, or at once
+// `limit_ns`, recording the timeout and raising the abort word, or at once
 // once another CTA raised it.
-__device__ __forceinline__ bool wait_slot(const unsigned long long* p, unsigned* header, unsigned long long* out) {
+__device__ __forceinline__ bool wait_slot(const unsigned long long* p, unsigned* header, unsigned long long* out,
+                                          unsigned long long limit_ns) {
     unsigned long long v = ld_relaxed_u64(p);
     if (v != kSlotEmpty) {
         *out = v;
@@ -99,7 +102,7 @@ __device__ __forceinline__ bool wait_slot(const unsigned long long* p, unsigned*
         }
         if ((it & 31u) == 31u) {
             if (ld_acquire_u32(header + 1) != 0u) return false;
-            if (global_ns() - t0 > kWaitLimitNs) {
+            if (global_ns() - t0 > limit_ns) {
                 atomicExch(header + 0, kDeviceErrTimeout);
                 atomicExch(header + 1, 1u);
                 return false;
@@ -146,7 +149,7 @@ __global__ void __launch_bounds__(kPersistBlock, 1) split_persistent_kernel(cons
     // error exit: thread 0 waits (bounded) for the copies of rows from..issued-1
     auto drain = [&](int64_t from) {
         if (t == 0)
-            for (int64_t q = from; q < issued; ++q) mbar_wait(bar + (q % NS), uint32_t((q / NS) & 1));
+            for (int64_t q = from; q < issued; ++q) mbar_wait(bar + (q % NS), uint32_t((q / NS) & 1), a.wait_ns);
     };
 
     unsigned long long next_stat = kSlotEmpty;  // thread 0: row result loaded one step early
@@ -154,10 +157,10 @@ __global__ void __launch_bounds__(kPersistBlock, 1) split_persistent_kernel(cons
         const int64_t q3 = s - L;  // row normalised in this step
         // ---- one barrier per step: row s has landed, row q3's (m, d) is known ----
         int fail = 0;
-        if (s < a.M) fail = !mbar_wait(bar + int(s % NS), uint32_t((s / NS) & 1));
+        if (s < a.M) fail = !mbar_wait(bar + int(s % NS), uint32_t((s / NS) & 1), a.wait_ns);
         if (t == 0 && q3 >= 0) {
             unsigned long long v = next_stat;
-            if (v == kSlotEmpty && !wait_slot(a.rowstat + q3, a.header, &v)) fail = 1;
+            if (v == kSlotEmpty && !wait_slot(a.rowstat + q3, a.header, &v, a.wait_ns)) fail = 1;
             row_result[q3 & 1] = v;
         }
         if (__syncthreads_or(fail)) {
@@ -210,7 +213,8 @@ __global__ void __launch_bounds__(kPersistBlock, 1) split_persistent_kernel(cons
             d = d == 0.f ? 0.f : d * ex2_approx((m - wm) * kLog2eF);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-            if (lane == 0) st_relaxed_u64(a.partials + s * slots + c * kPersistWarps + warp, pack_md(wm, d));
+            if (lane == 0 && !(c == 0 && s == a.stall_row))
+                st_relaxed_u64(a.partials + s * slots + c * kPersistWarps + warp, pack_md(wm, d));
         }
 
         // ---- merge of row s - L/2 by its owner ----
@@ -229,7 +233,7 @@ __global__ void __launch_bounds__(kPersistBlock, 1) split_persistent_kernel(cons
 #pragma unroll
             for (int k = 0; k < kLoc; ++k) {
                 if (k >= n) break;
-                if (raw[k] == kSlotEmpty && !wait_slot(a.partials + q2 * slots + t + k * kPersistBlock, a.header, &raw[k])) {
+                if (raw[k] == kSlotEmpty && !wait_slot(a.partials + q2 * slots + t + k * kPersistBlock, a.header, &raw[k], a.wait_ns)) {
                     mfail = 1;
                     break;
                 }
@@ -351,7 +355,7 @@ __global__ void __launch_bounds__(kPersistBlock, 1) split_l2_kernel(const T* x, 
             if (s + prefetch < a.M) prefetch_l2_bulk(x + (s + prefetch) * a.ld + s_lo * V, bytes);
             if (q3 >= 0) {
                 unsigned long long v = next_stat;
-                if (v == kSlotEmpty && !wait_slot(a.rowstat + q3, a.header, &v)) fail = 1;
+                if (v == kSlotEmpty && !wait_slot(a.rowstat + q3, a.header, &v, a.wait_ns)) fail = 1;
                 row_result[q3 & 1] = v;
             }
         }
@@ -390,7 +394,8 @@ __global__ void __launch_bounds__(kPersistBlock, 1) split_l2_kernel(const T* x, 
             d = d == 0.f ? 0.f : d * ex2_approx((m - wm) * kLog2eF);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-            if (lane == 0) st_relaxed_u64(a.partials + s * slots + c * kPersistWarps + warp, pack_md(wm, d));
+            if (lane == 0 && !(c == 0 && s == a.stall_row))
+                st_relaxed_u64(a.partials + s * slots + c * kPersistWarps + warp, pack_md(wm, d));
         }
 
         const int64_t q2 = s - L / 2;
@@ -406,7 +411,7 @@ __global__ void __launch_bounds__(kPersistBlock, 1) split_l2_kernel(const T* x, 
 #pragma unroll
             for (int k = 0; k < kLoc; ++k) {
                 if (k >= n) break;
-                if (raw[k] == kSlotEmpty && !wait_slot(a.partials + q2 * slots + t + k * kPersistBlock, a.header, &raw[k])) {
+                if (raw[k] == kSlotEmpty && !wait_slot(a.partials + q2 * slots + t + k * kPersistBlock, a.header, &raw[k], a.wait_ns)) {
                     mfail = 1;
                     break;
                 }

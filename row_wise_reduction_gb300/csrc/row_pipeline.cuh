@@ -13,11 +13,12 @@
 // Requirements (checked by the dispatcher): rows start on 16-byte boundaries
 // and N * sizeof(T) is a multiple of 16 (the bulk copy's alignment rules).
 //
-// Waits are bounded. If a buffer's copy has not landed after kWaitLimitNs, the
-// thread records it; the next CTA-wide barrier (__syncthreads_or) tells every
-// thread, the CTA stops processing rows, thread 0 waits (again bounded) for the
-// copies it still has in flight, sets the library's device error word and the
-// CTA returns.
+// Waits are bounded (2 s unless the launch gives a shorter limit). If a
+// buffer's copy has not landed in time, the thread records it; the row
+// group's next barrier (bar.red.or) tells every thread of the group, the group
+// stops processing rows, its producer waits (again bounded) for the copies it
+// still has in flight and sets the library's device error word, and the group
+// returns.
 #pragma once
 
 #include "rowops_device.cuh"
@@ -58,21 +59,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity: false after kWaitLimitNs
+// Bounded wait for the phase with the given parity: false after `limit_ns`
 // (or 2^26 polls, whichever comes first).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     for (uint32_t i = 0; i < (1u << 26); ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 255u && global_ns() - t0 > kWaitLimitNs) return false;
+        if ((i & 255u) == 255u && global_ns() - t0 > limit_ns) return false;
     }
     return false;
 }
 
-// Thread 0: expect `bytes` on `bar`, then copy them global -> shared.
-__device__ __forceinline__ void tma_load_row(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+// Thread 0: expect `bytes` (+ `extra`) on `bar`, then copy `bytes` global ->
+// shared. A nonzero `extra` is the test hook that makes the phase never
+// complete, so the bounded wait on it runs out (the copy itself completes).
+__device__ __forceinline__ void tma_load_row(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                             uint32_t extra = 0) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes + extra)
                  : "memory");
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -172,12 +177,12 @@ __host__ __device__ constexpr uint32_t ring_row_bytes(int64_t N, int es) {
 // Thread 0, on an error exit: wait (bounded) for every copy still in flight so
 // that none lands in shared memory after the CTA is gone.
 __device__ __forceinline__ void drain_ring(const RowRing& ring, int64_t first_row_iter, int64_t row0,
-                                           int64_t stride, int64_t M) {
+                                           int64_t stride, int64_t M, unsigned long long limit_ns) {
     for (int d = 0; d < ring.nbuf; ++d) {
         const int64_t i = first_row_iter + d;
         const int64_t row = row0 + i * stride;
         if (row >= M) break;
-        mbar_wait(ring.bar + (i % ring.nbuf), uint32_t((i / ring.nbuf) & 1));
+        mbar_wait(ring.bar + (i % ring.nbuf), uint32_t((i / ring.nbuf) & 1), limit_ns);
     }
 }
 

@@ -31,6 +31,8 @@ struct Tuning {
     int lookahead = 0;  // single-read form's lookahead in steps (0: automatic)
     int l2 = 0;         // single-read form staged in L2
     int prefetch = 0;   // its L2 prefetch distance in rows (0: automatic)
+    long long wait_ns = 0;    // device-side wait limit (0: 2 s)
+    long long stall_row = -1; // test hook (see include/rowops.h)
 };
 
 int env_int(const char* name, int dflt) {
@@ -56,6 +58,8 @@ Tuning read_tuning() {
     t.rows = env_int("ROWOPS_ROWS_PER_CTA", 0);
     t.lookahead = env_int("ROWOPS_PERSIST_LOOKAHEAD", 0);
     t.l2 = env_int("ROWOPS_PERSIST_L2", 0);
+    if (const char* v = std::getenv("ROWOPS_WAIT_LIMIT_NS")) t.wait_ns = std::strtoll(v, nullptr, 10);
+    if (const char* v = std::getenv("ROWOPS_TEST_STALL_ROW")) t.stall_row = std::strtoll(v, nullptr, 10);
     t.prefetch = env_int("ROWOPS_PERSIST_PREFETCH", 0);
     if (const char* k = std::getenv("ROWOPS_ONLINE")) {
         if (!std::strcmp(k, "two_pass")) t.online = 1;
@@ -148,6 +152,8 @@ rowops_status_t make_cfg(cudaStream_t stream, const Tuning& tn, LaunchCfg* cfg) 
     cfg->persist_lookahead = tn.lookahead;
     cfg->persist_l2 = tn.l2 != 0;
     cfg->persist_prefetch = tn.prefetch;
+    cfg->wait_ns = tn.wait_ns > 0 ? (unsigned long long)tn.wait_ns : 2000000000ull;
+    cfg->stall_row = tn.stall_row;
     return ROWOPS_OK;
 }
 

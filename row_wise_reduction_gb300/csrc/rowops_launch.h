@@ -19,6 +19,8 @@ struct LaunchCfg {
     int persist_lookahead = 0;  // single-read split-row softmax lookahead (0: automatic)
     bool persist_l2 = false;    // single-read split-row softmax staged in L2 instead of shared memory
     int persist_prefetch = 0;   // rows of L2 prefetch ahead (0: automatic)
+    unsigned long long wait_ns = 2000000000ull;  // limit of every device-side wait
+    int64_t stall_row = -1;     // test hook: the row whose wait is made to run out (-1: none)
 };
 
 // Persistent grid size for `items` independent work items: the occupancy

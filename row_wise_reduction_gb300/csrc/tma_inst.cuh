@@ -21,7 +21,7 @@ cudaError_t launch_softmax_tma(const void* x, void* y, int64_t M, int64_t N, int
     if (e != cudaSuccess) return e;
     const int grid = grid_for(reinterpret_cast<const void*>(kern), TPR, smem, M, cfg);
     kern<<<grid, TPR, smem, cfg.stream>>>(static_cast<const T*>(x), static_cast<T*>(y), M, int(N), ld, nbuf,
-                                          cfg.dev_error);
+                                          cfg.dev_error, cfg.wait_ns, cfg.stall_row);
     return cudaGetLastError();
 }
 
@@ -37,7 +37,7 @@ cudaError_t launch_ln_gelu_tma_rows(const void* x, void* y, const void* w, const
     const int grid = grid_for(reinterpret_cast<const void*>(kern), TPR * ROWS, smem, (M + ROWS - 1) / ROWS, cfg);
     kern<<<grid, TPR * ROWS, smem, cfg.stream>>>(static_cast<const T*>(x), static_cast<T*>(y),
                                                  static_cast<const T*>(w), static_cast<const T*>(b), eps, M, int(N),
-                                                 ld, nbuf, cfg.dev_error);
+                                                 ld, nbuf, cfg.dev_error, cfg.wait_ns, cfg.stall_row);
     return cudaGetLastError();
 }
 

@@ -46,9 +46,13 @@ __device__ __forceinline__ GroupPipe make_group(char* smem, int64_t N, int es, i
 
 // CTA start: thread 0 initialises every group's barriers; then each group's
 // producer issues the copies of its first nbuf rows.
+// Test hook: the copy of row `stall_row` is expected to bring 16 bytes more than
+// it does, so the wait on it runs out (-1: no such row).
+__device__ __forceinline__ uint32_t stall_extra(int64_t row, int64_t stall_row) { return row == stall_row ? 16u : 0u; }
+
 template <int ROWS>
 __device__ __forceinline__ void start_pipes(char* smem, const GroupPipe& p, const void* x, int64_t M, int64_t ld,
-                                            int es, uint32_t bytes) {
+                                            int es, uint32_t bytes, int64_t stall_row) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < ROWS * p.ring.nbuf; ++s) mbar_init(reinterpret_cast<uint64_t*>(smem) + s, 1);
         mbar_init_fence();
@@ -58,33 +62,37 @@ __device__ __forceinline__ void start_pipes(char* smem, const GroupPipe& p, cons
         for (int s = 0; s < p.ring.nbuf; ++s) {
             const int64_t row = p.first + s * p.stride;
             if (row < M)
-                tma_load_row(p.ring.slot(s), static_cast<const char*>(x) + size_t(row * ld) * es, bytes, p.ring.bar + s);
+                tma_load_row(p.ring.slot(s), static_cast<const char*>(x) + size_t(row * ld) * es, bytes, p.ring.bar + s,
+                             stall_extra(row, stall_row));
         }
 }
 
 // After the group's first reduction: refill buffer s with the row nbuf
 // iterations ahead (every thread of the group has its data in registers).
 __device__ __forceinline__ void refill(const GroupPipe& p, int s, int64_t row, const void* x, int64_t M, int64_t ld,
-                                       int es, uint32_t bytes) {
+                                       int es, uint32_t bytes, int64_t stall_row) {
     if (!p.producer) return;
     const int64_t nxt = row + int64_t(p.ring.nbuf) * p.stride;
     if (nxt < M) {
         fence_proxy_async_smem();
-        tma_load_row(p.ring.slot(s), static_cast<const char*>(x) + size_t(nxt * ld) * es, bytes, p.ring.bar + s);
+        tma_load_row(p.ring.slot(s), static_cast<const char*>(x) + size_t(nxt * ld) * es, bytes, p.ring.bar + s,
+                     stall_extra(nxt, stall_row));
     }
 }
 
 // Error exit of a group whose wait gave up: its producer waits (bounded) for
 // the copies still in flight and records the timeout.
-__device__ __forceinline__ void abandon(const GroupPipe& p, int64_t i, int64_t M, unsigned* err) {
+__device__ __forceinline__ void abandon(const GroupPipe& p, int64_t i, int64_t M, unsigned* err,
+                                        unsigned long long wait_ns) {
     if (!p.producer) return;
-    drain_ring(p.ring, i, p.first, p.stride, M);
+    drain_ring(p.ring, i, p.first, p.stride, M, wait_ns);
     atomicExch(err, kDeviceErrTimeout);
 }
 
 template <typename T, int TPR, int VPT, int ROWS, bool FULL>
 __global__ void __launch_bounds__(TPR * ROWS)
-    softmax_tma_kernel(const T* x, T* y, int64_t M, int N, int64_t ld, int nbuf, unsigned* err) {
+    softmax_tma_kernel(const T* x, T* y, int64_t M, int N, int64_t ld, int nbuf, unsigned* err,
+                       unsigned long long wait_ns, int64_t stall_row) {
     using E = Elem<T>;
     constexpr int V = E::kVec;
     static_assert(TPR % 64 == 0, "row groups of at least two warps");
@@ -95,13 +103,13 @@ __global__ void __launch_bounds__(TPR * ROWS)
     const int g = threadIdx.x / TPR, t = threadIdx.x % TPR;
     const uint32_t bytes = uint32_t(N) * E::kBytes;
     const int nvec = N / V;
-    start_pipes<ROWS>(smem, p, x, M, ld, E::kBytes, bytes);
+    start_pipes<ROWS>(smem, p, x, M, ld, E::kBytes, bytes, stall_row);
 
     for (int64_t i = 0;; ++i) {
         const int64_t row = p.first + i * p.stride;
         if (row >= M) break;
         const int s = int(i % nbuf);
-        int fail = !mbar_wait(p.ring.bar + s, uint32_t((i / nbuf) & 1));
+        int fail = !mbar_wait(p.ring.bar + s, uint32_t((i / nbuf) & 1), wait_ns);
         const char* sb = p.ring.slot(s);
 
         float v[VPT][V];
@@ -120,10 +128,10 @@ __global__ void __launch_bounds__(TPR * ROWS)
         }
         mx = row_reduce<TPR>(mx, red_max[g], p.bar_id, OpMax(), fail);
         if (fail) {
-            abandon(p, i, M, err);
+            abandon(p, i, M, err, wait_ns);
             return;
         }
-        refill(p, s, row, x, M, ld, E::kBytes, bytes);
+        refill(p, s, row, x, M, ld, E::kBytes, bytes, stall_row);
         if (mx == -INFINITY) mx = 0.f;
         float sum = 0.f;
 #pragma unroll
@@ -179,7 +187,7 @@ __host__ __device__ constexpr uint32_t tma_affine_bytes() {
 template <typename T, int TPR, int VPT, int ROWS, bool FULL>
 __global__ void __launch_bounds__(TPR * ROWS)
     ln_gelu_tma_kernel(const T* x, T* y, const T* w, const T* b, float eps, int64_t M, int N, int64_t ld,
-                       int nbuf, unsigned* err) {
+                       int nbuf, unsigned* err, unsigned long long wait_ns, int64_t stall_row) {
     using E = Elem<T>;
     constexpr int V = E::kVec, H = V / 4;
     static_assert(TPR % 64 == 0, "row groups of at least two warps");
@@ -193,7 +201,7 @@ __global__ void __launch_bounds__(TPR * ROWS)
     const uint32_t bytes = uint32_t(N) * E::kBytes;
     const int nvec = N / V;
     const float fN = float(N);
-    start_pipes<ROWS>(smem, p, x, M, ld, E::kBytes, bytes);
+    start_pipes<ROWS>(smem, p, x, M, ld, E::kBytes, bytes, stall_row);
     stage_affine_thread_major<T, TPR, VPT>(w, b, nvec, sw4, sb4);
     __syncthreads();
 
@@ -201,7 +209,7 @@ __global__ void __launch_bounds__(TPR * ROWS)
         const int64_t row = p.first + i * p.stride;
         if (row >= M) break;
         const int s = int(i % nbuf);
-        int fail = !mbar_wait(p.ring.bar + s, uint32_t((i / nbuf) & 1));
+        int fail = !mbar_wait(p.ring.bar + s, uint32_t((i / nbuf) & 1), wait_ns);
         const char* sb = p.ring.slot(s);
 
         float v[VPT][V];
@@ -220,10 +228,10 @@ __global__ void __launch_bounds__(TPR * ROWS)
         }
         sum = row_reduce<TPR>(sum, red_a[g], p.bar_id, OpSum(), fail);
         if (fail) {
-            abandon(p, i, M, err);
+            abandon(p, i, M, err, wait_ns);
             return;
         }
-        refill(p, s, row, x, M, ld, E::kBytes, bytes);
+        refill(p, s, row, x, M, ld, E::kBytes, bytes, stall_row);
         const float mean = sum / fN;
         // centred values, their squares and the residual of the fp32 mean
         float q = 0.f, r = 0.f;

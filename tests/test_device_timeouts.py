@@ -1,0 +1,84 @@
+"""The bounded device-side waits end in a recorded ROWOPS_ERR_TIMEOUT, not a
+hang, and the CUDA context stays usable afterwards.
+
+No GPU fault is involved: the test hook ROWOPS_TEST_STALL_ROW makes one wait
+unsatisfiable (the row pipeline's mbarrier expects 16 bytes more than the bulk
+copy of that row brings; the single-read split softmax withholds one partial,
+a slot nothing then sets), and ROWOPS_WAIT_LIMIT_NS shortens every wait to
+20 ms. The kernel gives up, drains its own copies, records the timeout and
+returns; the next call without the hook is correct and clean.
+"""
+import pytest
+import torch
+
+from row_wise_reduction_gb300 import (
+    rowops_device_status,
+    rowops_layernorm_gelu,
+    rowops_online_softmax,
+    rowops_online_softmax_status,
+    rowops_online_softmax_workspace_bytes,
+    rowops_softmax,
+    workloads,
+)
+from tests import _compare as C
+from tests import gpu_util as gu
+
+pytestmark = [pytest.mark.gpu, gu.requires_gpu]
+
+TIMEOUT = 5
+LIMIT_NS = "20000000"
+
+
+def _softmax_wl():
+    return workloads.Workload("timeout_softmax", "softmax", "bf16", 2000, 4096, seed=3, x_std=2.0)
+
+
+def test_row_pipeline_wait_times_out_and_context_recovers(oracle, monkeypatch):
+    x = gu.make_x(_softmax_wl())["x"]
+    assert rowops_device_status() == 0
+    monkeypatch.setenv("ROWOPS_KERNEL", "tma")
+    monkeypatch.setenv("ROWOPS_WAIT_LIMIT_NS", LIMIT_NS)
+    monkeypatch.setenv("ROWOPS_TEST_STALL_ROW", "777")
+    rowops_softmax(x)
+    assert rowops_device_status() == TIMEOUT
+    assert rowops_device_status() == 0  # the status query clears the word
+    # without the hook: same kernel, correct output, no error recorded
+    monkeypatch.delenv("ROWOPS_TEST_STALL_ROW")
+    y = rowops_softmax(x)
+    assert rowops_device_status() == 0
+    C.assert_softmax_close(C.to_f64(y), oracle.softmax(gu.rows_f32(x)), "bf16")
+
+
+def test_layernorm_row_groups_wait_times_out(oracle, monkeypatch):
+    wl = workloads.Workload("timeout_ln", "layernorm_gelu", "bf16", 1500, 8192, seed=4, affine=True)
+    inp = gu.make_x(wl)
+    monkeypatch.setenv("ROWOPS_KERNEL", "tma")
+    monkeypatch.setenv("ROWOPS_WAIT_LIMIT_NS", LIMIT_NS)
+    monkeypatch.setenv("ROWOPS_TEST_STALL_ROW", "3")
+    rowops_layernorm_gelu(inp["x"], inp["w"], inp["b"], wl.eps)
+    assert rowops_device_status() == TIMEOUT
+    monkeypatch.delenv("ROWOPS_TEST_STALL_ROW")
+    y = rowops_layernorm_gelu(inp["x"], inp["w"], inp["b"], wl.eps)
+    assert rowops_device_status() == 0
+    ref = oracle.layernorm_gelu(gu.rows_f32(inp["x"]), inp["w"].float().cpu().numpy(),
+                                inp["b"].float().cpu().numpy(), wl.eps)
+    C.assert_ln_gelu_close(C.to_f64(y), ref, "bf16")
+
+
+@pytest.mark.parametrize("staging", ["smem", "l2"])
+def test_single_read_split_softmax_wait_times_out(oracle, monkeypatch, staging):
+    wl = workloads.Workload("timeout_online", "online_softmax", "f32", 6, 1 << 20, seed=5)
+    x = gu.make_x(wl)["x"]
+    ws = torch.empty(rowops_online_softmax_workspace_bytes(6, 1 << 20, torch.float32), dtype=torch.uint8,
+                     device="cuda")
+    monkeypatch.setenv("ROWOPS_ONLINE", "single_read")
+    if staging == "l2":
+        monkeypatch.setenv("ROWOPS_PERSIST_L2", "1")
+    monkeypatch.setenv("ROWOPS_WAIT_LIMIT_NS", LIMIT_NS)
+    monkeypatch.setenv("ROWOPS_TEST_STALL_ROW", "2")
+    rowops_online_softmax(x, workspace=ws)
+    assert rowops_online_softmax_status(ws) == TIMEOUT
+    monkeypatch.delenv("ROWOPS_TEST_STALL_ROW")
+    y = rowops_online_softmax(x, workspace=ws)
+    assert rowops_online_softmax_status(ws) == 0
+    C.assert_softmax_close(C.to_f64(y), oracle.softmax(gu.rows_f32(x)), "f32")
