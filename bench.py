@@ -47,9 +47,11 @@ KERNELS_PER_CALL = {"softmax": 1, "online_softmax": 2, "layernorm_gelu": 1}
 L2_BYTES = 129 * 10**6
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "ln_gelu_bf16_65536x8192.txt")
-DOMINANT_SOURCES = ["row_wise_reduction_gb300/csrc/ln_gelu_kernels.cuh",
-                    "row_wise_reduction_gb300/csrc/rowops_device.cuh",
-                    "row_wise_reduction_gb300/csrc/ln_gelu_inst.cuh"]
+DOMINANT_SOURCES = ["row_wise_reduction_gb300/csrc/tma_row_kernels.cuh",
+                    "row_wise_reduction_gb300/csrc/row_pipeline.cuh",
+                    "row_wise_reduction_gb300/csrc/tma_inst.cuh",
+                    "row_wise_reduction_gb300/csrc/ln_gelu_kernels.cuh",
+                    "row_wise_reduction_gb300/csrc/rowops_device.cuh"]
 
 
 def alg_bytes(wl: workloads.Workload) -> int:
