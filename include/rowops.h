@@ -40,7 +40,7 @@
  *   ROWOPS_FORCE_VPT=<n>          16-byte vectors per thread (reg: 1..4; tma: 1, 2, 3, 4, 8)
  *   ROWOPS_FORCE_LOOPED=1         same as ROWOPS_KERNEL=looped
  *   ROWOPS_RING_BUFFERS=<2..16>   rows in flight per row group of the row pipeline
- *   ROWOPS_ROWS_PER_CTA=<1|2|4>   row groups per CTA of the LayerNorm+GELU row pipeline
+ *   ROWOPS_ROWS_PER_CTA=<1|2|4|8> row groups per CTA of the LayerNorm+GELU row pipeline
  *   ROWOPS_ONLINE=two_pass|single_read  split-row softmax form (default two_pass); single_read
  *                                 keeps each chunk on chip between the passes (rows of
  *                                 >= ~2^19.3 entries, 16-byte aligned, cooperative launch)

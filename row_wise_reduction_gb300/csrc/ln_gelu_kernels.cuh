@@ -38,6 +38,19 @@ __device__ __forceinline__ void stage_affine(const T* w, const T* b, int N, floa
 
 __host__ __device__ constexpr int affine_pad(int n) { return (n + 3) & ~3; }
 
+// Unaligned rows: (w, b) as fp32 pairs in column order with one unused pair
+// after every 8 columns (column c at pair c + c / 8). A warp's threads read
+// column c0 + V*v + j of their vectors v, pair 9v + const: 32 different bank
+// pairs for any c0, where plain column order gives an 8-way conflict.
+__device__ __forceinline__ int affine_pair(int c) { return c + (c >> 3); }
+
+template <typename T>
+__device__ __forceinline__ void stage_affine_pairs(const T* w, const T* b, int N, float2* swb) {
+    using E = Elem<T>;
+    for (int c = threadIdx.x; c < N; c += blockDim.x)
+        swb[affine_pair(c)] = make_float2(w ? E::load(w + c) : 1.f, b ? E::load(b + c) : 0.f);
+}
+
 // ALIGNED: every row starts on a 16-byte boundary (head = 0), so the columns of
 // a vector are a multiple of 4 and w, b are read from shared memory as float4.
 template <typename T, int TPR, int VPT, int BLOCK, bool ALIGNED>
@@ -54,7 +67,9 @@ __global__ void __launch_bounds__(BLOCK)
     __shared__ float red_a[BLOCK / 32 > 0 ? BLOCK / 32 : 1];
     __shared__ float red_b[BLOCK / 32 > 0 ? 2 * BLOCK / 32 : 2];
 
-    stage_affine(w, b, N, sw, sb);
+    const float2* swb = reinterpret_cast<const float2*>(smem_affine);
+    if constexpr (ALIGNED) stage_affine(w, b, N, sw, sb);
+    else stage_affine_pairs(w, b, N, reinterpret_cast<float2*>(smem_affine));
     __syncthreads();
 
     const int t = threadIdx.x % TPR;
@@ -143,13 +158,18 @@ __global__ void __launch_bounds__(BLOCK)
                     }
                 } else {
 #pragma unroll
-                    for (int j = 0; j < V; ++j)
-                        o[j] = gelu_tanh_approx(fmaf(fmaf(v[i][j], rstd, shift), sw[c0 + j], sb[c0 + j]));
+                    for (int j = 0; j < V; ++j) {
+                        const float2 wb = swb[affine_pair(c0 + j)];
+                        o[j] = gelu_tanh_approx(fmaf(fmaf(v[i][j], rstd, shift), wb.x, wb.y));
+                    }
                 }
                 st_stream16(yv + k * V, E::pack(o));
             }
         }
-        if (has_ex) E::store(yr + ecol, gelu_tanh_approx(fmaf(fmaf(ex, rstd, shift), sw[ecol], sb[ecol])));
+        if (has_ex) {
+            const float2 wb = ALIGNED ? make_float2(sw[ecol], sb[ecol]) : swb[affine_pair(ecol)];
+            E::store(yr + ecol, gelu_tanh_approx(fmaf(fmaf(ex, rstd, shift), wb.x, wb.y)));
+        }
     }
 }
 

@@ -10,8 +10,9 @@
 // always in flight regardless of how long the arithmetic of the current row
 // takes: the memory system never waits for the compute of a row.
 //
-// Requirements (checked by the dispatcher): rows start on 16-byte boundaries
-// and N * sizeof(T) is a multiple of 16 (the bulk copy's alignment rules).
+// The bulk copy moves whole 16-byte vectors between 16-byte-aligned addresses,
+// so it takes each row's aligned body; the kernels on the pipeline load the
+// unaligned head and tail of a row themselves (tma_row_kernels.cuh).
 //
 // Waits are bounded (2 s unless the launch gives a shorter limit). If a
 // buffer's copy has not landed in time, the thread records it; the row

@@ -207,12 +207,14 @@ bool rows_aligned(const void* x, const void* y, int64_t ld, int es) {
 
 constexpr int64_t kMinChunk = 256;
 
-// Row-pipeline kernel choice. Needs 16-byte aligned rows whose byte length is
-// a multiple of 16 (bulk-copy rules) and at least 64 vectors. Prefers a row of
-// exactly block * vpt vectors (no predicates), trying the vectors per thread in
-// `order` (measured on GB300, 8 per thread is fastest for both operations on
-// the 4096 / 8192-column bf16 rows); otherwise the smallest block that covers
-// the row with <= 4.
+// Row-pipeline kernel choice. x and y rows must share their offset modulo 16
+// bytes and a row must hold at least 64 whole vectors. Rows that start on
+// 16-byte boundaries with a length that fills TPR * VPT vectors exactly get the
+// FULL form (no predicates), trying vectors per thread in `order` (measured on
+// GB300, 8 per thread is fastest for both operations on the 4096 / 8192-column
+// bf16 rows); all other rows get the general form (bulk-copied body, unaligned
+// head and tail loaded directly) with the same preference among the tiles that
+// leave at most 1/8 of their vector slots idle.
 struct TmaChoice {
     int block_index, vpt_index;
     bool full;
@@ -233,8 +235,9 @@ int tma_block_index(int64_t block) {
 bool choose_tma(const void* x, const void* y, int64_t N, int64_t ld, int es, const Tuning& tn,
                 std::initializer_list<int> order, TmaChoice* c) {
     const int64_t vec = 16 / es;
-    if (!rows_aligned(x, y, ld, es) || N % vec != 0) return false;
-    const int64_t nvec = N / vec;
+    if (!same_phase(x, y)) return false;
+    const bool aligned = rows_aligned(x, y, ld, es) && N % vec == 0;
+    const int64_t nvec = N / vec;  // the most whole vectors any row's body holds
     if (nvec < 64) return false;
     if (tn.tpr) {
         const int bi = tma_block_index(tn.tpr);
@@ -243,27 +246,42 @@ bool choose_tma(const void* x, const void* y, int64_t N, int64_t ld, int es, con
         if (vpt == 5 || vpt == 6 || vpt == 7) vpt = 8;
         const int vi = tma_vpt_index(vpt);
         if (vi < 0 || int64_t(vpt) * tn.tpr < nvec) return false;
-        *c = TmaChoice{bi, vi, int64_t(vpt) * tn.tpr == nvec};
+        *c = TmaChoice{bi, vi, aligned && int64_t(vpt) * tn.tpr == nvec};
         return true;
     }
+    if (aligned)
+        for (int vpt : order) {
+            if (nvec % vpt) continue;
+            const int bi = tma_block_index(nvec / vpt);
+            if (bi >= 0) {
+                *c = TmaChoice{bi, tma_vpt_index(vpt), true};
+                return true;
+            }
+        }
+    // general rows: the same order of vectors per thread, taking the smallest
+    // block that covers the row with at most 1/8 of its vector slots idle; else
+    // the combination with the fewest slots
+    int best_i = -1, best_j = -1;
+    int64_t best_slots = 0;
     for (int vpt : order) {
-        if (nvec % vpt) continue;
-        const int bi = tma_block_index(nvec / vpt);
-        if (bi >= 0) {
-            *c = TmaChoice{bi, tma_vpt_index(vpt), true};
-            return true;
+        for (int i = 0; i < kNumTmaBlocks; ++i) {
+            const int64_t slots = int64_t(kTmaBlocks[i]) * vpt;
+            if (slots < nvec) continue;
+            if ((slots - nvec) * 8 <= slots) {
+                *c = TmaChoice{i, tma_vpt_index(vpt), false};
+                return true;
+            }
+            if (best_i < 0 || slots < best_slots) {
+                best_i = i;
+                best_j = tma_vpt_index(vpt);
+                best_slots = slots;
+            }
+            break;  // larger blocks only leave more slots idle
         }
     }
-    for (int i = 0; i < kNumTmaBlocks; ++i) {
-        const int64_t block = kTmaBlocks[i];
-        if (block * 4 >= nvec) {
-            int vpt = int((nvec + block - 1) / block);
-            if (vpt == 3) vpt = 4;
-            *c = TmaChoice{i, tma_vpt_index(vpt), false};
-            return true;
-        }
-    }
-    return false;
+    if (best_i < 0) return false;
+    *c = TmaChoice{best_i, best_j, false};
+    return true;
 }
 
 // Ring depth: two rows in flight per CTA by default (deeper rings measured no
@@ -281,37 +299,23 @@ int ring_buffers(int64_t N, int es, size_t fixed, const Tuning& tn, const Launch
 // Row groups per CTA for the LayerNorm+GELU row pipeline: the groups of a CTA
 // share one staging of w, b, so packing several rows into a CTA raises the warps
 // an SM can hold when that staging, not registers, limits occupancy. Picks the
-// count (1, 2 or 4; full rows with a multi-row instantiation only) that gives the
-// most resident warps per SM by shared memory and thread limits; ties go to
-// fewer groups. Returns the index into kTmaMultiRows, or -1 for one group.
-int choose_ln_rows(const TmaChoice& c, int64_t N, int es, int nbuf, const Tuning& tn, const LaunchCfg& cfg,
-                   int* multi_tpr, int* multi_vpt) {
-    const int tpr = kTmaBlocks[c.block_index], vpt = kTmaVpts[c.vpt_index];
-    *multi_tpr = *multi_vpt = -1;
-    for (int i = 0; i < kNumTmaMultiTpr; ++i)
-        if (kTmaMultiTpr[i] == tpr) *multi_tpr = i;
-    for (int j = 0; j < kNumTmaMultiVpt; ++j)
-        if (kTmaMultiVpt[j] == vpt) *multi_vpt = j;
-    if (!c.full || *multi_tpr < 0 || *multi_vpt < 0 || tn.rows == 1) return -1;
-    const size_t affine = tma_affine_smem(tpr, vpt, es);
-    const size_t per_sm = size_t(cfg.max_smem_optin) + 1024;  // the SM's shared memory, roughly
+// count (1, 2, 4 or 8, where that instantiation exists) that gives the most
+// resident warps per SM by the occupancy calculator (shared memory, registers
+// and threads of the actual kernel); ties go to fewer groups.
+using TmaLnGeluLookup = TmaLnGeluKernel (*)(int tpr, int vpt, int rows, bool full);
+
+int choose_ln_rows(TmaLnGeluLookup lookup, int tpr, int vpt, bool full, int64_t N, int nbuf, const Tuning& tn,
+                   const LaunchCfg& cfg) {
     auto warps = [&](int rows) {
-        if (rows * nbuf > 16 || tpr * rows > 1024) return 0;
-        const size_t smem = kTmaRingHeader + size_t(rows) * nbuf * tma_row_bytes(N, es) + affine + 1024;
-        if (smem > size_t(cfg.max_smem_optin)) return 0;
-        int ctas = int(per_sm / smem);
-        const int by_threads = 2048 / (tpr * rows);
-        if (ctas > by_threads) ctas = by_threads;
-        return ctas * tpr * rows / 32;
+        if (rows * nbuf > 16) return 0;
+        const TmaLnGeluKernel k = lookup(tpr, vpt, rows, full);
+        if (!k.launch) return 0;
+        return k.ctas_per_sm(N, nbuf, cfg) * tpr * rows / 32;
     };
-    if (tn.rows > 1) {
-        for (int r = 0; r < kNumTmaMultiRows; ++r)
-            if (kTmaMultiRows[r] == tn.rows && warps(tn.rows) > 0) return r;
-        return -1;
-    }
-    int best = -1, best_warps = warps(1);
-    for (int r = 0; r < kNumTmaMultiRows; ++r) {
-        const int w = warps(kTmaMultiRows[r]);
+    if (tn.rows >= 1) return warps(tn.rows) > 0 ? tn.rows : 1;
+    int best = 1, best_warps = warps(1);
+    for (int r : kTmaMultiRows) {
+        const int w = warps(r);
         if (w > best_warps) {
             best = r;
             best_warps = w;
@@ -322,26 +326,27 @@ int choose_ln_rows(const TmaChoice& c, int64_t N, int es, int nbuf, const Tuning
 
 }  // namespace
 
+int ctas_per_sm(const void* func, int block, size_t smem, const LaunchCfg& cfg) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (auto& o : g_occ)
+        if (o.func == func && o.device == cfg.device && o.block == block && o.smem == smem) return o.blocks_per_sm;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, func, block, smem) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+    }
+    g_occ.push_back(OccEntry{func, cfg.device, block, smem, n});
+    return n;
+}
+
 int grid_for(const void* func, int block, size_t smem, int64_t items, const LaunchCfg& cfg) {
     int64_t cap;
     if (cfg.ctas_per_sm < 0) {
         cap = items;
     } else {
         int per_sm = cfg.ctas_per_sm;
-        if (per_sm == 0) {
-            std::lock_guard<std::mutex> lk(g_mu);
-            for (auto& o : g_occ)
-                if (o.func == func && o.device == cfg.device && o.block == block && o.smem == smem)
-                    per_sm = o.blocks_per_sm;
-            if (per_sm == 0) {
-                int n = 0;
-                if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, func, block, smem) != cudaSuccess ||
-                    n < 1)
-                    n = 1;
-                g_occ.push_back(OccEntry{func, cfg.device, block, smem, n});
-                per_sm = n;
-            }
-        }
+        if (per_sm == 0) per_sm = ctas_per_sm(func, block, smem, cfg);
+        if (per_sm < 1) per_sm = 1;
         cap = int64_t(per_sm) * cfg.num_sms;
     }
     int64_t g = items < cap ? items : cap;
@@ -419,20 +424,14 @@ rowops_status_t rowops_layernorm_gelu(const void* x, void* y, const void* w, con
     TmaChoice tc;
     if ((tn.family == Family::Auto || tn.family == Family::Tma) &&
         choose_tma(x, y, N, ld, es, tn, {8, 4, 2, 3, 1}, &tc)) {
-        const size_t affine = tma_affine_smem(kTmaBlocks[tc.block_index], kTmaVpts[tc.vpt_index], es);
-        const int nbuf = ring_buffers(N, es, affine, tn, cfg);
-        TmaLnGeluLaunch tf = dtype == ROWOPS_F32 ? ln_gelu_tma_f32(tc.block_index, tc.vpt_index, tc.full)
-                                                 : ln_gelu_tma_bf16(tc.block_index, tc.vpt_index, tc.full);
+        const int tpr = kTmaBlocks[tc.block_index], vpt = kTmaVpts[tc.vpt_index];
+        const int nbuf = ring_buffers(N, es, tma_affine_smem(tpr, vpt, es, tc.full, N), tn, cfg);
         if (nbuf > 0) {
-            int mt = -1, mv = -1;
-            const int ri = choose_ln_rows(tc, N, es, nbuf, tn, cfg, &mt, &mv);
-            if (ri >= 0) {
-                TmaLnGeluLaunch mf = dtype == ROWOPS_F32 ? ln_gelu_tma_multi_f32(mt, mv, ri)
-                                                         : ln_gelu_tma_multi_bf16(mt, mv, ri);
-                if (mf) tf = mf;
-            }
+            const TmaLnGeluLookup lookup = dtype == ROWOPS_F32 ? ln_gelu_tma_f32 : ln_gelu_tma_bf16;
+            const int rows = choose_ln_rows(lookup, tpr, vpt, tc.full, N, nbuf, tn, cfg);
+            const TmaLnGeluKernel k = lookup(tpr, vpt, rows, tc.full);
+            if (k.launch) return finish(k.launch(x, y, w, b, eps, M, N, ld, nbuf, cfg));
         }
-        if (nbuf > 0 && tf) return finish(tf(x, y, w, b, eps, M, N, ld, nbuf, cfg));
     }
     int tpr_index = 0, vpt = 0;
     LnGeluLaunch fn = nullptr;

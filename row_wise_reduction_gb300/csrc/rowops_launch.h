@@ -8,6 +8,12 @@
 
 namespace rowops {
 
+// Rows of stride `row_bytes` start at offsets that repeat modulo 16 bytes with
+// this period: 16 / gcd(16, row_bytes).
+__host__ __device__ constexpr int row_phase_period(int64_t row_bytes) {
+    return (row_bytes & 15) == 0 ? 1 : 16 / int(row_bytes & -row_bytes & 15);
+}
+
 struct LaunchCfg {
     cudaStream_t stream;
     int device;
@@ -26,6 +32,9 @@ struct LaunchCfg {
 // Persistent grid size for `items` independent work items: the occupancy
 // limit (or the forced CTAs per SM) times the SM count, capped at `items`.
 int grid_for(const void* func, int block, size_t smem, int64_t items, const LaunchCfg& cfg);
+
+// CTAs of `func` one SM can hold at once (occupancy API, cached per device).
+int ctas_per_sm(const void* func, int block, size_t smem, const LaunchCfg& cfg);
 
 // Allow `func` to use `smem` bytes of dynamic shared memory (once per device).
 cudaError_t allow_smem(const void* func, size_t smem, const LaunchCfg& cfg);
@@ -58,24 +67,33 @@ using TmaLnGeluLaunch = cudaError_t (*)(const void* x, void* y, const void* w, c
                                         int64_t M, int64_t N, int64_t ld, int nbuf, const LaunchCfg& cfg);
 TmaSoftmaxLaunch softmax_tma_f32(int block_index, int vpt_index, bool full);
 TmaSoftmaxLaunch softmax_tma_bf16(int block_index, int vpt_index, bool full);
-TmaLnGeluLaunch ln_gelu_tma_f32(int block_index, int vpt_index, bool full);
-TmaLnGeluLaunch ln_gelu_tma_bf16(int block_index, int vpt_index, bool full);
 
-// LayerNorm+GELU with several row groups per CTA sharing one staging of w, b
-// (full rows only): TPR in kTmaMultiTpr, VPT in kTmaMultiVpt, ROWS in kTmaMultiRows.
-constexpr int kTmaMultiTpr[] = {128, 256};
-constexpr int kNumTmaMultiTpr = 2;
+// LayerNorm+GELU instantiations: ROWS = 1 with TPR in kTmaBlocks and VPT in
+// kTmaVpts, or several row groups per CTA sharing one staging of w, b with TPR
+// in kTmaMultiTpr, VPT in kTmaMultiVpt, ROWS in kTmaMultiRows (at most 512
+// threads); full rows or general (unaligned) rows. Each comes with its launcher
+// and a query of how many of its CTAs an SM holds for a given N and ring depth.
+constexpr int kTmaMultiTpr[] = {64, 128, 256};
+constexpr int kNumTmaMultiTpr = 3;
 constexpr int kTmaMultiVpt[] = {2, 4, 8};
 constexpr int kNumTmaMultiVpt = 3;
-constexpr int kTmaMultiRows[] = {2, 4};
-constexpr int kNumTmaMultiRows = 2;
-TmaLnGeluLaunch ln_gelu_tma_multi_f32(int tpr_index, int vpt_index, int rows_index);
-TmaLnGeluLaunch ln_gelu_tma_multi_bf16(int tpr_index, int vpt_index, int rows_index);
+constexpr int kTmaMultiRows[] = {2, 4, 8};
+constexpr int kNumTmaMultiRows = 3;
+using TmaCtasQuery = int (*)(int64_t N, int nbuf, const LaunchCfg& cfg);
+struct TmaLnGeluKernel {
+    TmaLnGeluLaunch launch;     // nullptr: no such instantiation
+    TmaCtasQuery ctas_per_sm;
+};
+TmaLnGeluKernel ln_gelu_tma_f32(int tpr, int vpt, int rows, bool full);
+TmaLnGeluKernel ln_gelu_tma_bf16(int tpr, int vpt, int rows, bool full);
 
 // dynamic shared memory of the row-pipeline kernels
 inline size_t tma_row_bytes(int64_t N, int es) { return size_t((N * es + 127) / 128 * 128); }
 inline size_t tma_ring_smem(int64_t N, int es, int nbuf) { return kTmaRingHeader + size_t(nbuf) * tma_row_bytes(N, es); }
-inline size_t tma_affine_smem(int block, int vpt, int es) { return size_t(2) * vpt * block * (16 / es) * 4; }
+// thread-major fp32 w, b; general rows add 256 bytes for their head/tail columns
+inline size_t tma_affine_smem(int block, int vpt, int es, bool full, int64_t /*N*/) {
+    return size_t(2) * vpt * block * (16 / es) * 4 + (full ? 0 : 256);
+}
 
 // register-resident: tpr_index into kTprChoices, vpt in 1..kMaxVpt
 SoftmaxLaunch softmax_reg_f32(int tpr_index, int vpt);
@@ -105,6 +123,12 @@ size_t persistent_rowstat_bytes(int64_t M);
 int64_t split_step_cols(int elem_bytes);
 
 // Dynamic shared memory the register-resident LN+GELU kernels need for N columns.
-inline size_t ln_gelu_smem_bytes(int64_t N) { return size_t(2) * size_t((N + 3) & ~int64_t(3)) * 4; }
+// w, b staging of the register kernel: two fp32 arrays of round_up(N, 4) for
+// aligned rows, padded (w, b) pairs (9 per 8 columns) otherwise; the larger.
+inline size_t ln_gelu_smem_bytes(int64_t N) {
+    const size_t columns = size_t(2) * size_t((N + 3) & ~int64_t(3)) * 4;
+    const size_t pairs = size_t(8) * size_t(((N + (N >> 3) + 1) + 1) & ~int64_t(1));
+    return columns > pairs ? columns : pairs;
+}
 
 }  // namespace rowops

@@ -27,24 +27,39 @@ cudaError_t launch_softmax_tma(const void* x, void* y, int64_t M, int64_t N, int
 
 // ROWS row groups per CTA share one staging of w, b; nbuf buffers per group.
 template <typename T, int TPR, int VPT, int ROWS, bool FULL>
+size_t ln_gelu_tma_smem(int64_t N, int nbuf) {
+    return kRingHeader + size_t(ROWS) * nbuf * ring_row_bytes(N, Elem<T>::kBytes) +
+           affine_stage_bytes<T, TPR, VPT, FULL>();
+}
+
+template <typename T, int TPR, int VPT, int ROWS, bool FULL>
 cudaError_t launch_ln_gelu_tma_rows(const void* x, void* y, const void* w, const void* b, float eps, int64_t M,
                                     int64_t N, int64_t ld, int nbuf, const LaunchCfg& cfg) {
     auto kern = ln_gelu_tma_kernel<T, TPR, VPT, ROWS, FULL>;
-    const size_t smem = kRingHeader + size_t(ROWS) * nbuf * ring_row_bytes(N, Elem<T>::kBytes) +
-                        tma_affine_bytes<T, TPR, VPT>();
+    const size_t smem = ln_gelu_tma_smem<T, TPR, VPT, ROWS, FULL>(N, nbuf);
     cudaError_t e = allow_smem(reinterpret_cast<const void*>(kern), smem, cfg);
     if (e != cudaSuccess) return e;
-    const int grid = grid_for(reinterpret_cast<const void*>(kern), TPR * ROWS, smem, (M + ROWS - 1) / ROWS, cfg);
+    int grid = grid_for(reinterpret_cast<const void*>(kern), TPR * ROWS, smem, (M + ROWS - 1) / ROWS, cfg);
+    if (!FULL) {  // whole phase classes: every class needs a CTA, and they share the grid evenly
+        const int period = row_phase_period(ld * int64_t(Elem<T>::kBytes));
+        grid = grid >= period ? grid - grid % period : period;
+    }
     kern<<<grid, TPR * ROWS, smem, cfg.stream>>>(static_cast<const T*>(x), static_cast<T*>(y),
                                                  static_cast<const T*>(w), static_cast<const T*>(b), eps, M, int(N),
                                                  ld, nbuf, cfg.dev_error, cfg.wait_ns, cfg.stall_row);
     return cudaGetLastError();
 }
 
-template <typename T, int TPR, int VPT, bool FULL>
-cudaError_t launch_ln_gelu_tma(const void* x, void* y, const void* w, const void* b, float eps, int64_t M,
-                               int64_t N, int64_t ld, int nbuf, const LaunchCfg& cfg) {
-    return launch_ln_gelu_tma_rows<T, TPR, VPT, 1, FULL>(x, y, w, b, eps, M, N, ld, nbuf, cfg);
+template <typename T, int TPR, int VPT, int ROWS, bool FULL>
+int ctas_ln_gelu_tma_rows(int64_t N, int nbuf, const LaunchCfg& cfg) {
+    auto kern = ln_gelu_tma_kernel<T, TPR, VPT, ROWS, FULL>;
+    const size_t smem = ln_gelu_tma_smem<T, TPR, VPT, ROWS, FULL>(N, nbuf);
+    if (smem + 1024 > size_t(cfg.max_smem_optin)) return 0;  // 1 KB for the static reduction buffers
+    if (allow_smem(reinterpret_cast<const void*>(kern), smem, cfg) != cudaSuccess) {
+        cudaGetLastError();  // a candidate that does not fit must not fail the launch that follows
+        return 0;
+    }
+    return ctas_per_sm(reinterpret_cast<const void*>(kern), TPR * ROWS, smem, cfg);
 }
 
 // tables indexed [block index into kTmaBlocks][vpt index into kTmaVpts]
@@ -61,31 +76,54 @@ TmaSoftmaxLaunch softmax_tma_table(int block_index, int vpt_index, bool full) {
     return full ? full_t[block_index][vpt_index] : part_t[block_index][vpt_index];
 }
 
-template <typename T>
-TmaLnGeluLaunch ln_gelu_tma_table(int block_index, int vpt_index, bool full) {
-    static const TmaLnGeluLaunch full_t[kNumTmaBlocks][kNumTmaVpts] = ROWOPS_TMA_TABLE(launch_ln_gelu_tma, T, true);
-    static const TmaLnGeluLaunch part_t[kNumTmaBlocks][kNumTmaVpts] = ROWOPS_TMA_TABLE(launch_ln_gelu_tma, T, false);
-    if (block_index < 0 || block_index >= kNumTmaBlocks || vpt_index < 0 || vpt_index >= kNumTmaVpts) return nullptr;
-    return full ? full_t[block_index][vpt_index] : part_t[block_index][vpt_index];
-}
 #undef ROWOPS_TMA_TABLE
 #undef ROWOPS_TMA_ROW
 
-// Multi-row LayerNorm+GELU, full rows only: [tpr index into kTmaMultiTpr]
-// [vpt index into kTmaMultiVpt][rows index into kTmaMultiRows]; nullptr where
-// TPR * ROWS would exceed 1024 threads.
-#define ROWOPS_TMA_M3(T, P, V) {launch_ln_gelu_tma_rows<T, P, V, 2, true>, launch_ln_gelu_tma_rows<T, P, V, 4, true>}
-template <typename T>
-TmaLnGeluLaunch ln_gelu_tma_multi_table(int tpr_index, int vpt_index, int rows_index) {
-    static const TmaLnGeluLaunch t[kNumTmaMultiTpr][kNumTmaMultiVpt][kNumTmaMultiRows] = {
-        {ROWOPS_TMA_M3(T, 128, 2), ROWOPS_TMA_M3(T, 128, 4), ROWOPS_TMA_M3(T, 128, 8)},
-        {ROWOPS_TMA_M3(T, 256, 2), ROWOPS_TMA_M3(T, 256, 4), ROWOPS_TMA_M3(T, 256, 8)},
-    };
-    if (tpr_index < 0 || tpr_index >= kNumTmaMultiTpr || vpt_index < 0 || vpt_index >= kNumTmaMultiVpt ||
-        rows_index < 0 || rows_index >= kNumTmaMultiRows)
-        return nullptr;
-    return t[tpr_index][vpt_index][rows_index];
+// LayerNorm+GELU instantiations by (TPR, VPT, ROWS); none where TPR * ROWS
+// would exceed 512 threads with ROWS > 1 (at 1024 threads a CTA gets at most 64
+// registers per thread and these kernels spill).
+template <typename T, int P, int V, int R, bool F>
+constexpr TmaLnGeluKernel ln_gelu_entry() {
+    if constexpr (R == 1 || P * R <= 512)
+        return TmaLnGeluKernel{launch_ln_gelu_tma_rows<T, P, V, R, F>, ctas_ln_gelu_tma_rows<T, P, V, R, F>};
+    else
+        return TmaLnGeluKernel{nullptr, nullptr};
 }
-#undef ROWOPS_TMA_M3
+#define ROWOPS_LN1(T, P, F) \
+    {ln_gelu_entry<T, P, 1, 1, F>(), ln_gelu_entry<T, P, 2, 1, F>(), ln_gelu_entry<T, P, 3, 1, F>(), \
+     ln_gelu_entry<T, P, 4, 1, F>(), ln_gelu_entry<T, P, 8, 1, F>()}
+#define ROWOPS_LN3(T, P, V, F) {ln_gelu_entry<T, P, V, 2, F>(), ln_gelu_entry<T, P, V, 4, F>(), ln_gelu_entry<T, P, V, 8, F>()}
+#define ROWOPS_LN2(T, P, F) {ROWOPS_LN3(T, P, 2, F), ROWOPS_LN3(T, P, 4, F), ROWOPS_LN3(T, P, 8, F)}
+
+template <int N>
+int index_of(const int (&a)[N], int v) {
+    for (int i = 0; i < N; ++i)
+        if (a[i] == v) return i;
+    return -1;
+}
+
+template <typename T>
+TmaLnGeluKernel ln_gelu_tma_lookup(int tpr, int vpt, int rows, bool full) {
+    static const TmaLnGeluKernel one_f[kNumTmaBlocks][kNumTmaVpts] = {
+        ROWOPS_LN1(T, 64, true), ROWOPS_LN1(T, 128, true), ROWOPS_LN1(T, 256, true), ROWOPS_LN1(T, 512, true)};
+    static const TmaLnGeluKernel one_g[kNumTmaBlocks][kNumTmaVpts] = {
+        ROWOPS_LN1(T, 64, false), ROWOPS_LN1(T, 128, false), ROWOPS_LN1(T, 256, false), ROWOPS_LN1(T, 512, false)};
+    static const TmaLnGeluKernel multi_f[kNumTmaMultiTpr][kNumTmaMultiVpt][kNumTmaMultiRows] = {
+        ROWOPS_LN2(T, 64, true), ROWOPS_LN2(T, 128, true), ROWOPS_LN2(T, 256, true)};
+    static const TmaLnGeluKernel multi_g[kNumTmaMultiTpr][kNumTmaMultiVpt][kNumTmaMultiRows] = {
+        ROWOPS_LN2(T, 64, false), ROWOPS_LN2(T, 128, false), ROWOPS_LN2(T, 256, false)};
+    const TmaLnGeluKernel none{nullptr, nullptr};
+    if (rows == 1) {
+        const int i = index_of(kTmaBlocks, tpr), j = index_of(kTmaVpts, vpt);
+        if (i < 0 || j < 0) return none;
+        return full ? one_f[i][j] : one_g[i][j];
+    }
+    const int i = index_of(kTmaMultiTpr, tpr), j = index_of(kTmaMultiVpt, vpt), r = index_of(kTmaMultiRows, rows);
+    if (i < 0 || j < 0 || r < 0) return none;
+    return full ? multi_f[i][j][r] : multi_g[i][j][r];
+}
+#undef ROWOPS_LN1
+#undef ROWOPS_LN2
+#undef ROWOPS_LN3
 
 }  // namespace rowops

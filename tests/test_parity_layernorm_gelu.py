@@ -265,3 +265,34 @@ def test_ln_gelu_tma_in_place_and_strided(oracle, monkeypatch):
     check(oracle, edge("bf16", 301, 8192), inplace=True)
     check(oracle, edge("bf16", 301, 8192), ld=8192 + 64)
     check(oracle, edge("f32", 77, 768), ld=768 + 4)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("N,ld,offset", [(4097, 4097, 0), (8191, 8191, 0), (1000, 1003, 1), (3001, 3001, 2),
+                                         (8192, 8192, 3), (12345, 12350, 1)])
+@pytest.mark.parametrize("rows", ["1", "2", "4"])
+def test_ln_gelu_tma_general_rows(oracle, monkeypatch, dtype, N, ld, offset, rows):
+    """The row pipeline's general form: rows that start anywhere (x and y in the
+    same 16-byte phase), bulk-copied aligned bodies, unaligned heads and tails
+    loaded directly, w/b read from column order with the widest access each
+    row's alignment allows; one, two or four row groups per CTA."""
+    monkeypatch.setenv("ROWOPS_KERNEL", "tma")
+    monkeypatch.setenv("ROWOPS_ROWS_PER_CTA", rows)
+    check(oracle, edge(dtype, 157, N, seed=N + offset), ld=ld, offset=offset)
+    from row_wise_reduction_gb300 import rowops_device_status
+
+    assert rowops_device_status() == 0
+
+
+@pytest.mark.parametrize("M", [1, 3, 9])
+@pytest.mark.parametrize("rows", ["1", "4"])
+def test_ln_gelu_tma_fewer_rows_than_phase_classes(oracle, monkeypatch, M, rows):
+    """4097-column bf16 rows start at 8 different offsets modulo 16 bytes; each
+    CTA of the general row pipeline takes one such class, so with fewer rows
+    than classes some CTAs have nothing to do and the rest one row each."""
+    monkeypatch.setenv("ROWOPS_KERNEL", "tma")
+    monkeypatch.setenv("ROWOPS_ROWS_PER_CTA", rows)
+    check(oracle, edge("bf16", M, 4097, seed=M))
+    from row_wise_reduction_gb300 import rowops_device_status
+
+    assert rowops_device_status() == 0

@@ -217,3 +217,15 @@ def test_softmax_tma_in_place_and_strided(oracle, monkeypatch):
     check(oracle, edge("bf16", 301, 4096), inplace=True)
     check(oracle, edge("bf16", 301, 4096), ld=4096 + 64)
     check(oracle, edge("f32", 77, 1024), ld=1024 + 4)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("N,ld,offset", [(4097, 4097, 0), (8191, 8191, 0), (1000, 1003, 1), (3001, 3001, 2),
+                                         (12345, 12350, 1)])
+def test_softmax_tma_general_rows(oracle, monkeypatch, dtype, N, ld, offset):
+    """The row pipeline's general form on rows that start anywhere."""
+    monkeypatch.setenv("ROWOPS_KERNEL", "tma")
+    check(oracle, edge(dtype, 157, N, seed=N + ld), ld=ld, offset=offset)
+    from row_wise_reduction_gb300 import rowops_device_status
+
+    assert rowops_device_status() == 0
