@@ -51,7 +51,8 @@ DOMINANT_SOURCES = ["row_wise_reduction_gb300/csrc/tma_row_kernels.cuh",
                     "row_wise_reduction_gb300/csrc/row_pipeline.cuh",
                     "row_wise_reduction_gb300/csrc/tma_inst.cuh",
                     "row_wise_reduction_gb300/csrc/ln_gelu_kernels.cuh",
-                    "row_wise_reduction_gb300/csrc/rowops_device.cuh"]
+                    "row_wise_reduction_gb300/csrc/rowops_device.cuh",
+                    "row_wise_reduction_gb300/csrc/rowops_launch.h"]
 
 
 def alg_bytes(wl: workloads.Workload) -> int:
@@ -228,6 +229,27 @@ def oracle_run(oracle, wl, xs, extra):
         oracle.layernorm_gelu(xs, extra["w"], extra["b"], wl.eps)
 
 
+def oracle_run_threads(oracle, wl, xs, extra, threads):
+    """The oracle on contiguous row slices in `threads` host threads (ctypes
+    releases the GIL inside the C calls, so the slices run on separate cores)."""
+    if threads <= 1 or len(xs) < 2:
+        oracle_run(oracle, wl, xs, extra)
+        return
+    from concurrent.futures import ThreadPoolExecutor
+
+    bounds = [len(xs) * i // threads for i in range(threads + 1)]
+    parts = [xs[a:b] for a, b in zip(bounds, bounds[1:]) if b > a]
+    with ThreadPoolExecutor(len(parts)) as ex:
+        list(ex.map(lambda part: oracle_run(oracle, wl, part, extra), parts))
+
+
+def host_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
 def cpu_sample_rows(wl, rows, device=None, dev_inputs=None):
     """fp32 host rows of ``wl`` (copied from the device inputs when given,
     else drawn on the CPU with the causal mask of rows spread over the
@@ -255,9 +277,10 @@ def spread_rows(M, k):
     return [int(i * step) for i in range(k)]
 
 
-def cpu_baseline(oracle, dev_inputs=None, budget_s=12.0):
-    """Time the oracle on ~budget_s seconds of the step's workloads; return
-    GB/s on the same algorithmic-byte basis plus a description."""
+def cpu_baseline(oracle, dev_inputs=None, budget_s=12.0, threads=1):
+    """Time the oracle on ~budget_s seconds (wall) of the step's workloads in
+    `threads` host threads; return GB/s on the same algorithmic-byte basis,
+    a description of the sample and the seconds spent."""
     total_bytes, total_s, desc = 0, 0.0, []
     per_op = budget_s / len(STEP)
     for name in STEP:
@@ -267,11 +290,11 @@ def cpu_baseline(oracle, dev_inputs=None, budget_s=12.0):
         t0 = time.perf_counter()
         oracle_run(oracle, wl, xs, extra)
         dt = max(time.perf_counter() - t0, 1e-6)
-        k = max(1, min(wl.M, int(per_op / dt)))
+        k = max(1, min(wl.M, int(per_op * threads / dt)))
         rows = spread_rows(wl.M, k)
         xs, extra = cpu_sample_rows(wl, rows, dev_inputs=dev_inputs.get(name) if dev_inputs else None)
         t0 = time.perf_counter()
-        oracle_run(oracle, wl, xs, extra)
+        oracle_run_threads(oracle, wl, xs, extra, threads)
         total_s += time.perf_counter() - t0
         total_bytes += alg_bytes(wl.with_shape(M=len(rows)))
         desc.append(f"{len(rows)} of {wl.M} rows of {name}")
@@ -289,6 +312,7 @@ def run_reference(args):
 
     oracle.build()
     K, W = args.steps, args.warmup
+    threads = host_threads()
     per_step_s = max(0.3, min(3.0, args.reference_budget_s / max(1, K + W)))
     # calibrate rows per op on one row each
     samples = []
@@ -298,14 +322,14 @@ def run_reference(args):
         t0 = time.perf_counter()
         oracle_run(oracle, wl, xs, extra)
         dt = max(time.perf_counter() - t0, 1e-6)
-        k = max(1, min(wl.M, int(per_step_s / len(STEP) / dt)))
+        k = max(1, min(wl.M, int(per_step_s * threads / len(STEP) / dt)))
         rows = spread_rows(wl.M, k)
         samples.append((wl, *cpu_sample_rows(wl, rows), len(rows)))
     step_bytes = sum(alg_bytes(wl.with_shape(M=k)) for wl, _, _, k in samples)
 
     def step():
         for wl, xs, extra, _ in samples:
-            oracle_run(oracle, wl, xs, extra)
+            oracle_run_threads(oracle, wl, xs, extra, threads)
 
     for _ in range(W):
         step()
@@ -330,7 +354,7 @@ def run_reference(args):
         "dtype": "f64",
         "data": "synthetic",
         "config": config_block(),
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -384,7 +408,8 @@ def run_extras(dev, stream, iters=50):
         b.record(stream)
         torch.cuda.synchronize()
         hot = a.elapsed_time(b) / iters / 1e3
-        rec = {"bytes": alg_bytes(wl), "hot_us": hot * 1e6, "hot_gbs": alg_bytes(wl) / hot / 1e9}
+        rec = {"bytes": alg_bytes(wl), "hot_us": hot * 1e6, "hot_gbs": alg_bytes(wl) / hot / 1e9,
+               "hot_rows_per_s": wl.M / hot}
         if name in SMALL:
             cold = []
             for _ in range(10):
@@ -420,6 +445,39 @@ def run_extras(dev, stream, iters=50):
     return out
 
 
+def run_torch_eager(wls, inputs, stream, iters=10):
+    """PyTorch's own eager kernels on the step's workloads, as context: softmax
+    along rows, and gelu(layer_norm(x)) unfused (tanh form). GB/s on the same
+    algorithmic bytes as the step (the unfused pair moves more than that)."""
+    import torch.nn.functional as F
+
+    out = {}
+    for n, wl in wls.items():
+        x = inputs[n]["x"]
+        if wl.op in ("softmax", "online_softmax"):
+            def call():
+                return torch.softmax(x, dim=-1)
+            what = "torch.softmax(x, dim=-1)"
+        else:
+            w, b = inputs[n]["w"], inputs[n]["b"]
+
+            def call():
+                return F.gelu(F.layer_norm(x, (wl.N,), w, b, wl.eps), approximate="tanh")
+            what = "F.gelu(F.layer_norm(x, (N,), w, b, eps), approximate='tanh')"
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(iters):
+            call()
+        b_.record(stream)
+        torch.cuda.synchronize()
+        t = a.elapsed_time(b_) / iters / 1e3
+        out[n] = {"call": what, "avg_ms": t * 1e3, "gbs": alg_bytes(wl) / t / 1e9}
+    return out
+
+
 # ---------------------------------------------------------------------------
 # rowops arm
 # ---------------------------------------------------------------------------
@@ -439,7 +497,14 @@ def run_rowops(args):
     ro.library()
     K, W = args.steps, args.warmup
     keys = {"softmax": STEP[0], "online": STEP[1], "layernorm": STEP[2]}
-    names = [keys[o] for o in args.ops.split(",")] if args.ops else list(STEP)
+    if args.workloads:
+        names = args.workloads.split(",")
+        unknown = [n for n in names if n not in workloads.WORKLOADS]
+        if unknown:
+            raise SystemExit(f"unknown workloads {unknown}; known: {sorted(workloads.WORKLOADS)}")
+    else:
+        names = [keys[o] for o in args.ops.split(",")] if args.ops else list(STEP)
+    subset = bool(args.ops or args.workloads)
     wls = {n: workloads.WORKLOADS[n] for n in names}
     if args.rows_scale != 1.0:
         wls = {n: wl.with_shape(M=max(1, int(wl.M * args.rows_scale))) for n, wl in wls.items()}
@@ -495,7 +560,7 @@ def run_rowops(args):
         ms = [a.elapsed_time(b) for a, b in ev[n]]
         avg_s = statistics.fmean(ms) / 1e3
         per_op[n] = {"avg_ms": avg_s * 1e3, "median_ms": statistics.median(ms), "min_ms": min(ms),
-                     "gbs": alg_bytes(wls[n]) / avg_s / 1e9}
+                     "gbs": alg_bytes(wls[n]) / avg_s / 1e9, "rows_per_s": wls[n].M / avg_s}
     peak, peak_kind = measured_peak()
     for n in names:
         per_op[n]["frac_of_" + peak_kind] = per_op[n]["gbs"] / peak
@@ -535,17 +600,23 @@ def run_rowops(args):
                "steps": ke, "ms_per_step": es / ke * 1e3}
 
     extras = None
-    if rank == 0 and not args.no_extras and not args.ops and args.rows_scale == 1.0:
+    if rank == 0 and not args.no_extras and not subset and args.rows_scale == 1.0:
         extras = run_extras(dev, stream)
+
+    eager = None
+    if rank == 0 and not args.no_torch_eager and not subset and args.rows_scale == 1.0:
+        eager = run_torch_eager(wls, inputs, stream)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         from oracle import oracle
 
         oracle.build()
-        v, sample, spent = cpu_baseline(oracle, dev_inputs=inputs, budget_s=args.cpu_budget_s)
-        cpu = {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample,
-               "seconds": spent}
+        threads = host_threads()
+        v, sample, spent = cpu_baseline(oracle, dev_inputs=inputs, budget_s=args.cpu_budget_s / 2, threads=threads)
+        v1, sample1, spent1 = cpu_baseline(oracle, dev_inputs=inputs, budget_s=args.cpu_budget_s / 2, threads=1)
+        cpu = {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample,
+               "seconds": spent, "single_core": {"value": v1, "sample": sample1, "seconds": spent1}}
 
     if rank != 0:
         return 0
@@ -569,7 +640,7 @@ def run_rowops(args):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": config_block() if args.rows_scale == 1.0 and not args.ops else
+        "config": config_block() if args.rows_scale == 1.0 and not subset else
         {"workload": " + ".join(f"{wl.name}[M={wl.M}]" for wl in wls.values())},
         "roofline": roof,
         "breakdown": per_op,
@@ -577,6 +648,7 @@ def run_rowops(args):
         "e2e": e2e,
         "gpu_launches": launches,
         "extras": extras,
+        "context_torch_eager": eager,
         "clocks": clocks.summary(),
         "device": torch.cuda.get_device_name(dev),
         "num_sms": torch.cuda.get_device_properties(dev).multi_processor_count,
@@ -597,6 +669,9 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip the small and ragged-tail workloads")
+    ap.add_argument("--no-torch-eager", action="store_true", help="skip the PyTorch eager context timings")
+    ap.add_argument("--workloads", default="",
+                    help="comma-separated workload names to time as the step instead of the default (profiling)")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--reference-budget-s", type=float, default=90.0)
     ap.add_argument("--clocks-csv", default=None, help="also log nvidia-smi clock samples to this CSV")

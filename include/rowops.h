@@ -94,9 +94,13 @@ const char* rowops_status_string(rowops_status_t status);
  *
  *   x, y   device pointers to M rows of `ld` elements of `dtype`; y may equal x.
  *   M      rows (>= 0); N columns (1 <= N < 2^31); ld row stride in elements (>= N).
- * Rows of up to 16384 fp32 / 32768 bf16 entries are held in registers (one
- * HBM read, one write); longer rows use an in-CTA online (m, d) loop that
- * reads the row twice [L6 §7.2].
+ * Rows of 64 to 4096 16-byte vectors (256..16384 fp32, 512..32768 bf16
+ * entries) whose x and y share their offset modulo 16 bytes stream through
+ * shared memory: bulk asynchronous copies fill a ring of row buffers while
+ * earlier rows are reduced and written (one HBM read, one write). Shorter rows
+ * are held in registers by row groups of 16..1024 threads; longer rows, and x
+ * and y at different offsets modulo 16 bytes, use an in-CTA online (m, d) loop
+ * that reads the row twice [L6 §7.2].
  */
 rowops_status_t rowops_softmax(const void* x, void* y, int64_t M, int64_t N, int64_t ld,
                                rowops_dtype_t dtype, cudaStream_t stream);
@@ -194,6 +198,9 @@ rowops_status_t rowops_online_softmax_noalloc(const void* x, void* y, int64_t M,
  *   w, b   device pointers to N entries of `dtype`, or NULL for weight 1 / bias 0
  *          (the pages load absent entries with 1.0 and 0.0).
  *   eps    added to the variance (the pages' default is 1e-5); must be >= 0 and finite.
+ * Kernel choice as for rowops_softmax (row pipeline / registers / looped); w and
+ * b are staged once per CTA as fp32 in shared memory, and the row pipeline runs
+ * up to 8 rows per CTA over that one staging.
  */
 rowops_status_t rowops_layernorm_gelu(const void* x, void* y, const void* w, const void* b,
                                       float eps, int64_t M, int64_t N, int64_t ld,
