@@ -62,6 +62,17 @@ def lib() -> ctypes.CDLL:
             getattr(L, name).argtypes = [_c_float_p, _c_float_p, _c_float_p, ctypes.c_double, _i64, _i64, _i64,
                                          _c_double_p]
             getattr(L, name).restype = ctypes.c_int
+        L.oracle_rmsnorm_row.argtypes = [_c_double_p, _c_double_p, ctypes.c_double, _i64, _c_double_p]
+        L.oracle_round_to.argtypes = [ctypes.c_double, ctypes.c_int]
+        L.oracle_round_to.restype = ctypes.c_double
+        L.oracle_residual_rmsnorm_row.argtypes = [_c_double_p, _c_double_p, _c_double_p, ctypes.c_double, _i64,
+                                                  ctypes.c_int, _c_double_p, _c_double_p]
+        L.oracle_rmsnorm_rows_f32.argtypes = [_c_float_p, _c_float_p, ctypes.c_double, _i64, _i64, _i64,
+                                              _c_double_p]
+        L.oracle_rmsnorm_rows_f32.restype = ctypes.c_int
+        L.oracle_residual_rmsnorm_rows_f32.argtypes = [_c_float_p, _c_float_p, _c_float_p, ctypes.c_double,
+                                                       ctypes.c_int, _i64, _i64, _i64, _c_double_p, _c_double_p]
+        L.oracle_residual_rmsnorm_rows_f32.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -161,6 +172,35 @@ def layernorm_gelu_row(x, w=None, b=None, eps: float = 1e-5) -> np.ndarray:
     return y
 
 
+STORAGE = {"exact": 0, "f32": 1, "bf16": 2}
+
+
+def round_to(v, storage: str) -> np.ndarray:
+    """Round to nearest even in the storage type ("exact", "f32", "bf16")."""
+    f = lib().oracle_round_to
+    code = STORAGE[storage]
+    vv = np.asarray(v, dtype=np.float64)
+    return np.vectorize(lambda t: f(t, code), otypes=[np.float64])(vv) if vv.ndim else np.float64(f(float(vv), code))
+
+
+def rmsnorm_row(x, w=None, eps: float = 1e-5) -> np.ndarray:
+    xr = _f64_row(x)
+    y = np.empty_like(xr)
+    lib().oracle_rmsnorm_row(_dp(xr), _dp(_opt64(w, xr.size)), float(eps), xr.size, _dp(y))
+    return y
+
+
+def residual_rmsnorm_row(x, r, w=None, eps: float = 1e-5, storage: str = "exact") -> Tuple[np.ndarray, np.ndarray]:
+    """(residual_out, out) of one row."""
+    xr, rr = _f64_row(x), _f64_row(r)
+    if rr.size != xr.size:
+        raise ValueError("x and residual must have the same length")
+    s_out, y = np.empty_like(xr), np.empty_like(xr)
+    lib().oracle_residual_rmsnorm_row(_dp(xr), _dp(rr), _dp(_opt64(w, xr.size)), float(eps), xr.size,
+                                      STORAGE[storage], _dp(s_out), _dp(y))
+    return s_out, y
+
+
 def gelu_tanh(z) -> np.ndarray:
     f = lib().oracle_gelu_tanh
     zz = np.asarray(z, dtype=np.float64)
@@ -204,3 +244,29 @@ def layernorm(x, w=None, b=None, eps: float = 1e-5) -> np.ndarray:
     if lib().oracle_layernorm_rows_f32(_fp(xs), _fp(wf), _fp(bf), float(eps), M, N, ld, _dp(y)) != 0:
         raise ValueError("oracle_layernorm_rows_f32 rejected its arguments")
     return y
+
+
+def rmsnorm(x, w=None, eps: float = 1e-5) -> np.ndarray:
+    """RMSNorm of every row -> float64 (M, N)."""
+    xs, M, N, ld = _rows(x)
+    y = np.empty((M, N), dtype=np.float64)
+    if lib().oracle_rmsnorm_rows_f32(_fp(xs), _fp(_opt32(w, N)), float(eps), M, N, ld, _dp(y)) != 0:
+        raise ValueError("oracle_rmsnorm_rows_f32 rejected its arguments")
+    return y
+
+
+def residual_rmsnorm(x, r, w=None, eps: float = 1e-5, storage: str = "exact") -> Tuple[np.ndarray, np.ndarray]:
+    """Fused residual + RMSNorm of every row -> (residual_out, out), float64 (M, N) each;
+    residual_out rounded to `storage` ("exact", "f32", "bf16") before the norm."""
+    xs, M, N, ld = _rows(x)
+    rs, Mr, Nr, ldr = _rows(r)
+    if (Mr, Nr) != (M, N):
+        raise ValueError("x and residual must have the same shape")
+    if ldr != ld:  # the batch form takes one row stride for both
+        xs, rs, ld = np.ascontiguousarray(xs), np.ascontiguousarray(rs), N
+    s_out = np.empty((M, N), dtype=np.float64)
+    y = np.empty((M, N), dtype=np.float64)
+    if lib().oracle_residual_rmsnorm_rows_f32(_fp(xs), _fp(rs), _fp(_opt32(w, N)), float(eps), STORAGE[storage],
+                                              M, N, ld, _dp(s_out), _dp(y)) != 0:
+        raise ValueError("oracle_residual_rmsnorm_rows_f32 rejected its arguments")
+    return s_out, y

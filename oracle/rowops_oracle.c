@@ -177,6 +177,57 @@ void oracle_layernorm_gelu_row(const double* x, const double* w, const double* b
 }
 
 /* ---------------------------------------------------------------------------
+ * RMSNorm [EX §4.2]:
+ *   inv_rms = 1 / sqrt(mean(x^2) + eps)        (no mean subtracted)
+ *   y       = x * inv_rms * w
+ * ------------------------------------------------------------------------- */
+void oracle_rmsnorm_row(const double* x, const double* w, double eps, int64_t n, double* y) {
+    double q = 0.0;
+    for (int64_t j = 0; j < n; ++j) q += x[j] * x[j];
+    double inv_rms = 1.0 / sqrt(q / (double)n + eps);
+    for (int64_t j = 0; j < n; ++j) {
+        double wj = w ? w[j] : 1.0;
+        y[j] = x[j] * inv_rms * wj;
+    }
+}
+
+/* Round to nearest, ties to even, keeping `bits` significant bits (normal
+ * range only: the values here are far from overflow and underflow). */
+static double round_significand(double v, int bits) {
+    if (v == 0.0 || !isfinite(v)) return v;
+    int e;
+    double m = frexp(v, &e); /* v = m * 2^e, 0.5 <= |m| < 1 */
+    return ldexp(nearbyint(ldexp(m, bits)), e - bits);
+}
+
+/* The storage types of the operations: fp32 (24 significant bits, a plain
+ * conversion to float) and bfloat16 (8 significant bits). */
+double oracle_round_to(double v, int storage) {
+    if (storage == ORACLE_STORE_F32) return (double)(float)v;
+    if (storage == ORACLE_STORE_BF16) return round_significand(v, 8);
+    return v;
+}
+
+/* ---------------------------------------------------------------------------
+ * Fused residual + RMSNorm [EX §4.3]:
+ *   residual_out = x + residual
+ *   out          = residual_out * rsqrt(mean(residual_out^2) + eps) * w
+ * residual_out is an output tensor of the operation's own type, and out is
+ * the RMSNorm of that tensor, so s is rounded to the storage type before the
+ * norm (fused and unfused then give the same out).
+ * ------------------------------------------------------------------------- */
+void oracle_residual_rmsnorm_row(const double* x, const double* r, const double* w, double eps, int64_t n,
+                                 int storage, double* s_out, double* y) {
+    double* s = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    if (!s) return;
+    for (int64_t j = 0; j < n; ++j) s[j] = oracle_round_to(x[j] + r[j], storage);
+    if (s_out)
+        for (int64_t j = 0; j < n; ++j) s_out[j] = s[j];
+    oracle_rmsnorm_row(s, w, eps, n, y);
+    free(s);
+}
+
+/* ---------------------------------------------------------------------------
  * Row-batch forms: row r of x starts at x + r*ld; output row r at y + r*N.
  * ------------------------------------------------------------------------- */
 static double* widen(const float* src, int64_t n) {
@@ -246,4 +297,47 @@ int oracle_layernorm_gelu_rows_f32(const float* x, const float* w, const float* 
 int oracle_layernorm_rows_f32(const float* x, const float* w, const float* b, double eps, int64_t M,
                               int64_t N, int64_t ld, double* y) {
     return layernorm_rows(x, w, b, eps, M, N, ld, y, 0);
+}
+
+int oracle_rmsnorm_rows_f32(const float* x, const float* w, double eps, int64_t M, int64_t N, int64_t ld,
+                            double* y) {
+    if (bad_shape(x, M, N, ld, y)) return -1;
+    double* row = (double*)malloc(sizeof(double) * (size_t)N);
+    double* wd = widen(w, N);
+    int rc = 0;
+    if (!row || (w && !wd)) {
+        rc = -1;
+    } else {
+        for (int64_t r = 0; r < M; ++r) {
+            for (int64_t j = 0; j < N; ++j) row[j] = (double)x[r * ld + j];
+            oracle_rmsnorm_row(row, wd, eps, N, y + r * N);
+        }
+    }
+    free(row);
+    free(wd);
+    return rc;
+}
+
+int oracle_residual_rmsnorm_rows_f32(const float* x, const float* r, const float* w, double eps, int storage,
+                                     int64_t M, int64_t N, int64_t ld, double* s_out, double* y) {
+    if (bad_shape(x, M, N, ld, y) || !r) return -1;
+    double* xr = (double*)malloc(sizeof(double) * (size_t)N);
+    double* rr = (double*)malloc(sizeof(double) * (size_t)N);
+    double* wd = widen(w, N);
+    int rc = 0;
+    if (!xr || !rr || (w && !wd)) {
+        rc = -1;
+    } else {
+        for (int64_t i = 0; i < M; ++i) {
+            for (int64_t j = 0; j < N; ++j) {
+                xr[j] = (double)x[i * ld + j];
+                rr[j] = (double)r[i * ld + j];
+            }
+            oracle_residual_rmsnorm_row(xr, rr, wd, eps, N, storage, s_out ? s_out + i * N : NULL, y + i * N);
+        }
+    }
+    free(xr);
+    free(rr);
+    free(wd);
+    return rc;
 }

@@ -1,7 +1,8 @@
 /*
  * rowops oracle: plain, slow, double-precision CPU reference for the row-wise
  * reduce-then-normalise operations (stable softmax, online / split-row
- * softmax, LayerNorm -> affine -> tanh-GELU).
+ * softmax, LayerNorm -> affine -> tanh-GELU, RMSNorm and fused residual +
+ * RMSNorm).
  *
  * TEST INFRASTRUCTURE ONLY. The test suite, the package smoke check and the
  * benchmark's CPU-baseline leg are the only users. The CUDA library never
@@ -58,6 +59,22 @@ double oracle_gelu_tanh(double z);
 void oracle_layernorm_gelu_row(const double* x, const double* w, const double* b, double eps,
                                int64_t n, double* y);
 
+/* RMSNorm [EX §4.2]: inv_rms = 1 / sqrt(mean_j x_j^2 + eps), y_j = x_j * inv_rms * w_j.
+ * w may be NULL (weight 1). */
+void oracle_rmsnorm_row(const double* x, const double* w, double eps, int64_t n, double* y);
+
+/* Storage types for a value that an operation writes out and then reuses. */
+enum { ORACLE_STORE_EXACT = 0, ORACLE_STORE_F32 = 1, ORACLE_STORE_BF16 = 2 };
+
+/* v rounded to nearest (ties to even) in the given storage type. */
+double oracle_round_to(double v, int storage);
+
+/* Fused residual + RMSNorm [EX §4.3]: s_j = x_j + r_j, written out in the
+ * storage type (rounded to nearest even), and y = RMSNorm(s) of the stored s.
+ * s_out may be NULL. */
+void oracle_residual_rmsnorm_row(const double* x, const double* r, const double* w, double eps, int64_t n,
+                                 int storage, double* s_out, double* y);
+
 /* ---- M rows with a row stride `ld` (elements), output M x N contiguous ------
  * The fp32 forms take inputs already widened to fp32 (bf16 values are exact
  * in fp32) and widen them to double row by row. Return 0, or -1 on bad
@@ -69,6 +86,11 @@ int oracle_layernorm_gelu_rows_f32(const float* x, const float* w, const float* 
                                    int64_t M, int64_t N, int64_t ld, double* y);
 int oracle_layernorm_rows_f32(const float* x, const float* w, const float* b, double eps, int64_t M,
                               int64_t N, int64_t ld, double* y);
+int oracle_rmsnorm_rows_f32(const float* x, const float* w, double eps, int64_t M, int64_t N, int64_t ld,
+                            double* y);
+/* x and r share the row stride; s_out may be NULL. */
+int oracle_residual_rmsnorm_rows_f32(const float* x, const float* r, const float* w, double eps, int storage,
+                                     int64_t M, int64_t N, int64_t ld, double* s_out, double* y);
 
 #ifdef __cplusplus
 }

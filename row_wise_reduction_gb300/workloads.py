@@ -26,24 +26,26 @@ class Workload:
     """One synthetic workload: an operation, a dtype, a shape and a value recipe."""
 
     name: str
-    op: str  # "softmax" | "online_softmax" | "layernorm_gelu"
+    op: str  # "softmax" | "online_softmax" | "layernorm_gelu" | "rmsnorm" | "residual_rmsnorm"
     dtype: str  # "f32" | "bf16"
     M: int  # rows
     N: int  # columns (reduction length)
-    seed: int  # seed of x; w and b use seed + 100 and seed + 200
+    seed: int  # seed of x; w, b and the residual use seed + 100, + 200 and + 300
     x_std: float = 1.0  # x ~ N(0, x_std^2)
     causal: bool = False  # row r keeps columns c <= r mod N, the rest are -inf
     outlier_p: float = 0.0  # fraction of entries (Bernoulli per entry) set to outlier_value
     outlier_value: float = 30.0
-    affine: bool = False  # layernorm: w ~ U(0.5, 1.5), b ~ N(0, 0.1^2)
+    affine: bool = False  # w ~ U(0.5, 1.5), b ~ N(0, 0.1^2) (RMSNorm uses w only)
+    residual: bool = False  # a second input of the same shape, ~ N(0, 1)
     eps: float = 1e-5
 
     def with_shape(self, M: Optional[int] = None, N: Optional[int] = None) -> "Workload":
         return dataclasses.replace(self, M=self.M if M is None else M, N=self.N if N is None else N)
 
 
-# The five workloads of the build's specification (plus the two ragged-tail
-# variants of the bf16 LayerNorm+GELU case), keyed by a descriptive name.
+# The benchmark workloads of softmax, split-row softmax and LayerNorm+GELU (with
+# the two ragged-tail variants of the bf16 LayerNorm+GELU case) and of RMSNorm,
+# keyed by a descriptive name.
 WORKLOADS: Dict[str, Workload] = {
     w.name: w
     for w in [
@@ -54,6 +56,14 @@ WORKLOADS: Dict[str, Workload] = {
         Workload("layernorm_gelu_bf16_65536x8192", "layernorm_gelu", "bf16", 65536, 8192, seed=4, affine=True),
         Workload("layernorm_gelu_bf16_65536x127", "layernorm_gelu", "bf16", 65536, 127, seed=4, affine=True),
         Workload("layernorm_gelu_bf16_65536x4097", "layernorm_gelu", "bf16", 65536, 4097, seed=4, affine=True),
+        # RMSNorm and fused residual + RMSNorm [Triton Kernel 实现练习 §4.2, §4.3], on the shapes of
+        # the LayerNorm+GELU workloads
+        Workload("rmsnorm_f32_4096x768", "rmsnorm", "f32", 4096, 768, seed=5, affine=True),
+        Workload("rmsnorm_bf16_65536x8192", "rmsnorm", "bf16", 65536, 8192, seed=6, affine=True),
+        Workload("residual_rmsnorm_f32_4096x768", "residual_rmsnorm", "f32", 4096, 768, seed=7, affine=True,
+                 residual=True),
+        Workload("residual_rmsnorm_bf16_65536x8192", "residual_rmsnorm", "bf16", 65536, 8192, seed=8, affine=True,
+                 residual=True),
     ]
 }
 
@@ -80,8 +90,9 @@ def make_inputs(
 ) -> Dict[str, torch.Tensor]:
     """Draw the inputs of ``wl`` on ``device``.
 
-    Returns ``{"x": (M, N) view, "x_storage": (M, ld) tensor}`` and, for affine
-    LayerNorm workloads, ``"w"`` and ``"b"`` of length N. Values are drawn in
+    Returns ``{"x": (M, N) view, "x_storage": (M, ld) tensor}``, for affine
+    workloads ``"w"`` and ``"b"`` of length N, and for residual workloads
+    ``"residual"`` / ``"residual_storage"`` laid out like x. Values are drawn in
     fp32 and rounded to the workload's dtype (round to nearest even). With
     ``ld > N`` the padding columns of each row hold NaN so that any read past
     column N-1 shows up in the result. ``row_ids`` (M integers) gives the row
@@ -118,4 +129,12 @@ def make_inputs(
         b = 0.1 * torch.randn((N,), generator=gb, device=device, dtype=torch.float32)
         out["w"] = w.to(dt)
         out["b"] = b.to(dt)
+    if wl.residual:
+        gr = _gen(device, wl.seed + 300)
+        r = torch.randn((M, N), generator=gr, device=device, dtype=torch.float32)
+        rs = torch.full((M, ld), float("nan"), device=device, dtype=dt)
+        rs[:, :N] = r.to(dt)
+        del r
+        out["residual"] = rs[:, :N]
+        out["residual_storage"] = rs
     return out

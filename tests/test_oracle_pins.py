@@ -360,6 +360,126 @@ def test_layernorm_rows_batch_respects_ld_and_null_affine(oracle):
         np.testing.assert_array_equal(g[r], oracle.layernorm_gelu_row(store[r, :N].astype(np.float64), None, None, 1e-5))
 
 
+# ----------------------------------------------------------------------------
+# RMSNorm, fused residual + RMSNorm
+# ----------------------------------------------------------------------------
+def bf_rmsnorm(xs, w=None, eps=1e-5):
+    xd = [_dec(v) for v in xs]
+    ms = CTX.divide(sum((v * v for v in xd), Decimal(0)), len(xd))
+    inv = CTX.divide(1, CTX.sqrt(ms + _dec(eps)))
+    return [float(CTX.multiply(CTX.multiply(v, inv), _dec(w[j]) if w is not None else Decimal(1)))
+            for j, v in enumerate(xd)]
+
+
+@pytest.mark.parametrize("case", _golden.read_cases("rmsnorm_closed_forms.txt"), ids=lambda c: c[0])
+def test_rmsnorm_golden_closed_forms(oracle, case):
+    """Worked examples: catches a subtracted mean, an (n-1) or missing 1/n,
+    eps outside the sqrt, a dropped weight and a residual that is not added."""
+    _, params, rows = case
+    x = [float(v) for v in rows["x"]]
+    eps = float(params.get("eps", Decimal("1e-5")))
+    w = [float(v) for v in rows["w"]] if "w" in rows else None
+    want = [float(v) for v in rows["y"]]
+    tol = 2e-15 * max(1.0, max(abs(v) for v in want))
+    if "r" in rows:
+        r = [float(v) for v in rows["r"]]
+        s, got = oracle.residual_rmsnorm_row(x, r, w, eps, "exact")
+        np.testing.assert_array_equal(s, [float(v) for v in rows["s"]])
+    else:
+        got = oracle.rmsnorm_row(x, w, eps)
+    np.testing.assert_allclose(got, want, rtol=0, atol=tol)
+
+
+def test_rmsnorm_unit_weight_moments_scale_and_sign(oracle):
+    """With w = 1: mean(y^2) = ms / (ms + eps) (ms = mean(x^2), from numpy);
+    with eps = 0, y is unchanged by scaling the row and odd in x; unlike
+    LayerNorm, shifting the row changes y."""
+    rng = _rng(29)
+    for n in (5, 127, 768, 4097, 8192):
+        x = rng.normal(0.3, 1.7, size=n)
+        ms = float(np.mean(x * x))
+        y = oracle.rmsnorm_row(x, None, 1e-5)
+        assert abs(np.mean(y * y) - ms / (ms + 1e-5)) < 1e-12
+        y0 = oracle.rmsnorm_row(x, None, 0.0)
+        np.testing.assert_allclose(oracle.rmsnorm_row(7.0 * x, None, 0.0), y0, rtol=0, atol=1e-14)
+        np.testing.assert_array_equal(oracle.rmsnorm_row(-x, None, 0.0), -y0)
+        assert np.max(np.abs(oracle.rmsnorm_row(x + 1.0, None, 0.0) - y0)) > 1e-3
+
+
+def test_rmsnorm_brute_force_with_weight(oracle):
+    rng = _rng(31)
+    x = rng.normal(0, 2, size=(3, 5))
+    w = rng.uniform(0.5, 1.5, size=5)
+    for row in x:
+        np.testing.assert_allclose(oracle.rmsnorm_row(row, w, 1e-5), bf_rmsnorm(row, w, 1e-5), rtol=0, atol=1e-15)
+
+
+def test_rmsnorm_matches_torch_double(oracle):
+    rng = _rng(37)
+    M, N = 9, 769
+    x = rng.normal(0, 1, size=(M, N)).astype(np.float32)
+    w = rng.uniform(0.5, 1.5, size=N).astype(np.float32)
+    xt, wt = torch.from_numpy(x).double(), torch.from_numpy(w).double()
+    y_t = torch.nn.functional.rms_norm(xt, (N,), wt, 1e-5)
+    np.testing.assert_allclose(oracle.rmsnorm(x, w, 1e-5), y_t.numpy(), rtol=0, atol=1e-13)
+
+
+def test_round_to_storage_types(oracle):
+    """bf16: the same value as torch's float32 -> bfloat16 conversion (round
+    to nearest even) on fp32 inputs, including exact ties; f32: numpy's
+    float64 -> float32 conversion."""
+    rng = _rng(41)
+    v32 = (rng.normal(0, 3, size=2000) * np.exp2(rng.integers(-20, 20, size=2000))).astype(np.float32)
+    want = torch.from_numpy(v32).to(torch.bfloat16).double().numpy()
+    np.testing.assert_array_equal(oracle.round_to(v32.astype(np.float64), "bf16"), want)
+    ties = np.array([1 + 2.0**-8, 1 + 3 * 2.0**-8, -(1 + 2.0**-8), 2 + 2.0**-7, 1 + 2.0**-8 + 2.0**-20])
+    np.testing.assert_array_equal(oracle.round_to(ties, "bf16"), [1.0, 1 + 2.0**-6, -1.0, 2.0, 1 + 2.0**-7])
+    v64 = rng.normal(0, 5, size=2000)
+    np.testing.assert_array_equal(oracle.round_to(v64, "f32"), v64.astype(np.float32).astype(np.float64))
+    np.testing.assert_array_equal(oracle.round_to(v64, "exact"), v64)
+
+
+@pytest.mark.parametrize("storage,dt", [("bf16", torch.bfloat16), ("f32", torch.float32)])
+def test_residual_rmsnorm_is_rmsnorm_of_stored_sum(oracle, storage, dt):
+    """residual_out is x + residual as the storage type holds it (torch's own
+    addition in that dtype), and out is the RMSNorm of that stored tensor, not
+    of the unrounded sum."""
+    rng = _rng(43)
+    M, N = 6, 513
+    x = torch.from_numpy(rng.normal(0, 1, size=(M, N)).astype(np.float32)).to(dt)
+    r = torch.from_numpy(rng.normal(0, 1, size=(M, N)).astype(np.float32)).to(dt)
+    w = torch.from_numpy(rng.uniform(0.5, 1.5, size=N).astype(np.float32)).to(dt)
+    s_t = x + r
+    s, y = oracle.residual_rmsnorm(x.float().numpy(), r.float().numpy(), w.float().numpy(), 1e-5, storage)
+    np.testing.assert_array_equal(s, s_t.double().numpy())
+    y_t = torch.nn.functional.rms_norm(s_t.double(), (N,), w.double(), 1e-5)
+    np.testing.assert_allclose(y, y_t.numpy(), rtol=0, atol=1e-13)
+    if storage == "bf16":  # the norm of the unrounded sum differs visibly
+        y_exact = oracle.rmsnorm((x.double() + r.double()).float().numpy(), w.float().numpy(), 1e-5)
+        assert np.max(np.abs(y_exact - y)) > 1e-4
+
+
+def test_rmsnorm_rows_batch_respects_ld_and_null_weight(oracle):
+    rng = _rng(47)
+    M, N, ld = 5, 127, 136
+    store = np.full((M, ld), np.nan, dtype=np.float32)
+    store[:, :N] = rng.normal(0, 1, size=(M, N)).astype(np.float32)
+    y = oracle.rmsnorm(store[:, :N], None, 1e-5)
+    assert np.all(np.isfinite(y))
+    np.testing.assert_array_equal(y, oracle.rmsnorm(np.ascontiguousarray(store[:, :N]), np.ones(N, np.float32), 1e-5))
+    for i in range(M):
+        np.testing.assert_array_equal(y[i], oracle.rmsnorm_row(store[i, :N].astype(np.float64), None, 1e-5))
+    # the residual form with both inputs padded to the same stride
+    rstore = np.full((M, ld), np.nan, dtype=np.float32)
+    rstore[:, :N] = rng.normal(0, 1, size=(M, N)).astype(np.float32)
+    s, yr = oracle.residual_rmsnorm(store[:, :N], rstore[:, :N], None, 1e-5, "f32")
+    assert np.all(np.isfinite(s)) and np.all(np.isfinite(yr))
+    for i in range(M):
+        si, yi = oracle.residual_rmsnorm_row(store[i, :N], rstore[i, :N], None, 1e-5, "f32")
+        np.testing.assert_array_equal(s[i], si)
+        np.testing.assert_array_equal(yr[i], yi)
+
+
 def test_batch_rejects_bad_shapes(oracle):
     with pytest.raises(ValueError):
         oracle.layernorm_gelu(np.zeros((2, 3), np.float32), np.ones(4, np.float32))
