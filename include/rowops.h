@@ -40,7 +40,7 @@
  *   ROWOPS_FORCE_VPT=<n>          16-byte vectors per thread (reg: 1..4; tma: 1, 2, 3, 4, 8)
  *   ROWOPS_FORCE_LOOPED=1         same as ROWOPS_KERNEL=looped
  *   ROWOPS_RING_BUFFERS=<2..16>   rows in flight per row group of the row pipeline
- *   ROWOPS_ROWS_PER_CTA=<1|2|4|8> row groups per CTA of the LayerNorm+GELU row pipeline
+ *   ROWOPS_ROWS_PER_CTA=<1|2|4|8> row groups per CTA of the LayerNorm+GELU and RMSNorm row pipelines
  *   ROWOPS_ONLINE=two_pass|single_read  split-row softmax form (default two_pass); single_read
  *                                 keeps each chunk on chip between the passes (rows of
  *                                 >= ~2^19.3 entries, 16-byte aligned, cooperative launch)
@@ -108,7 +108,8 @@ rowops_status_t rowops_softmax(const void* x, void* y, int64_t M, int64_t N, int
 /*
  * Synchronises `stream`, then reads and clears the library's device error word
  * on the current device. Kernels that wait on asynchronous copies (the TMA-fed
- * row pipeline behind rowops_softmax and rowops_layernorm_gelu) bound every
+ * row pipeline behind rowops_softmax, rowops_layernorm_gelu and the RMSNorm
+ * entry points) bound every
  * wait; if one gives up, the kernel stops, records ROWOPS_ERR_TIMEOUT there,
  * and the outputs of that call are unspecified. Returns ROWOPS_OK,
  * ROWOPS_ERR_TIMEOUT, or ROWOPS_ERR_CUDA if a CUDA call fails.
@@ -205,6 +206,45 @@ rowops_status_t rowops_online_softmax_noalloc(const void* x, void* y, int64_t M,
 rowops_status_t rowops_layernorm_gelu(const void* x, void* y, const void* w, const void* b,
                                       float eps, int64_t M, int64_t N, int64_t ld,
                                       rowops_dtype_t dtype, cudaStream_t stream);
+
+/*
+ * RMSNorm of every row [EX §4.2 RMSNorm]:
+ *   inv_rms = 1 / sqrt(sum_j x_j^2 / N + eps);   y_j = x_j * inv_rms * w_j
+ * (no mean is subtracted). fp32 accumulation, results cast back to `dtype`.
+ *
+ *   x, y   device pointers as for rowops_softmax; y may equal x.
+ *   w      device pointer to N entries of `dtype`, or NULL for weight 1.
+ *   eps    added to the mean square (the pages give no value; 1e-5, the pages'
+ *          LayerNorm default, is the binding's default); must be >= 0 and finite.
+ * Kernel choice as for rowops_layernorm_gelu (row pipeline with up to 8 rows
+ * per CTA over one fp32 staging of w / register row groups / looped).
+ */
+rowops_status_t rowops_rmsnorm(const void* x, void* y, const void* w, float eps, int64_t M, int64_t N,
+                               int64_t ld, rowops_dtype_t dtype, cudaStream_t stream);
+
+/*
+ * Fused residual add + RMSNorm [EX §4.3 Fused Residual RMSNorm]:
+ *   residual_out = x + residual
+ *   y            = residual_out * rsqrt(mean(residual_out^2) + eps) * w
+ * returning both tensors, in one pass (x and residual read once, y and
+ * residual_out written once). residual_out is rounded to `dtype` (nearest
+ * even) and y is the RMSNorm of that stored residual_out, so the fused call
+ * gives the same y as rowops_rmsnorm applied to its own residual_out.
+ *
+ *   x, residual        device pointers to M rows of `ld` elements (inputs).
+ *   y, residual_out    device pointers to M rows of `ld` elements (outputs).
+ *   Each output may be one of the inputs (in place: e.g. residual_out ==
+ *   residual, y == x) or must not overlap either of them; y and residual_out
+ *   must not overlap each other. x and residual may be the same. Other
+ *   overlaps are rejected with ROWOPS_ERR_INVALID_VALUE.
+ *   w, eps, M, N, ld, dtype, stream    as for rowops_rmsnorm.
+ * Rows of all four tensors at the same offset modulo 16 bytes take the row
+ * pipeline (both input rows of a ring slot arrive on one mbarrier) or the
+ * register kernels; other layouts take the looped kernel.
+ */
+rowops_status_t rowops_fused_residual_rmsnorm(const void* x, const void* residual, void* y, void* residual_out,
+                                              const void* w, float eps, int64_t M, int64_t N, int64_t ld,
+                                              rowops_dtype_t dtype, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

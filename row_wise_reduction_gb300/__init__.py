@@ -1,8 +1,9 @@
 """rowops: row-wise reduce-then-normalise CUDA kernels for GB300 (sm_103a).
 
-Stable softmax, split-row online softmax and fused LayerNorm -> affine ->
-tanh-GELU, exposed through the C ABI of ``librowops.so`` (``include/rowops.h``)
-and the thin ctypes binding in :mod:`row_wise_reduction_gb300.rowops`.
+Stable softmax, split-row online softmax, fused LayerNorm -> affine ->
+tanh-GELU, RMSNorm and fused residual + RMSNorm, exposed through the C ABI of
+``librowops.so`` (``include/rowops.h``) and the thin ctypes binding in
+:mod:`row_wise_reduction_gb300.rowops`.
 """
 from .rowops import (  # noqa: F401
     ROWOPS_BF16,
@@ -11,10 +12,12 @@ from .rowops import (  # noqa: F401
     library,
     library_path,
     rowops_device_status,
+    rowops_fused_residual_rmsnorm,
     rowops_layernorm_gelu,
     rowops_online_softmax,
     rowops_online_softmax_status,
     rowops_online_softmax_workspace_bytes,
+    rowops_rmsnorm,
     rowops_softmax,
     rowops_status_string,
 )

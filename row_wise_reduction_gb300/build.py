@@ -31,6 +31,12 @@ SOURCES = [
     "tma_softmax_bf16.cu",
     "tma_ln_gelu_f32.cu",
     "tma_ln_gelu_bf16.cu",
+    "rms_f32.cu",
+    "rms_bf16.cu",
+    "tma_rms_f32_plain.cu",
+    "tma_rms_f32_residual.cu",
+    "tma_rms_bf16_plain.cu",
+    "tma_rms_bf16_residual.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

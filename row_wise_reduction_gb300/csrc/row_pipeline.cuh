@@ -87,6 +87,21 @@ __device__ __forceinline__ void tma_load_row(void* dst, const void* src, uint32_
         : "memory");
 }
 
+// The same in two steps, for several copies completing on one barrier: one
+// expect of their total bytes, then each copy.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_copy_row(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
 // Order this thread's earlier shared-memory reads before later async-proxy
 // writes to the same buffer.
 __device__ __forceinline__ void fence_proxy_async_smem() {

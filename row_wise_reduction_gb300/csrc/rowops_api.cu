@@ -302,19 +302,14 @@ int ring_buffers(int64_t N, int es, size_t fixed, const Tuning& tn, const Launch
 // count (1, 2, 4 or 8, where that instantiation exists) that gives the most
 // resident warps per SM by the occupancy calculator (shared memory, registers
 // and threads of the actual kernel); ties go to fewer groups.
-using TmaLnGeluLookup = TmaLnGeluKernel (*)(int tpr, int vpt, int rows, bool full);
-
-int choose_ln_rows(TmaLnGeluLookup lookup, int tpr, int vpt, bool full, int64_t N, int nbuf, const Tuning& tn,
-                   const LaunchCfg& cfg) {
-    auto warps = [&](int rows) {
-        if (rows * nbuf > 16) return 0;
-        const TmaLnGeluKernel k = lookup(tpr, vpt, rows, full);
-        if (!k.launch) return 0;
-        return k.ctas_per_sm(N, nbuf, cfg) * tpr * rows / 32;
-    };
+// `ctas(rows)`: CTAs per SM of the instantiation with that many row groups (0
+// if there is none or it does not fit).
+template <class CtasOf>
+int choose_group_rows(int tpr, int nbuf, const Tuning& tn, CtasOf ctas) {
+    auto warps = [&](int rows) { return rows * nbuf > kTmaMaxSlots ? 0 : ctas(rows) * tpr * rows / 32; };
     if (tn.rows >= 1) return warps(tn.rows) > 0 ? tn.rows : 1;
     int best = 1, best_warps = warps(1);
-    for (int r : kTmaMultiRows) {
+    for (int r : {2, 4, 8}) {
         const int w = warps(r);
         if (w > best_warps) {
             best = r;
@@ -322,6 +317,68 @@ int choose_ln_rows(TmaLnGeluLookup lookup, int tpr, int vpt, bool full, int64_t 
         }
     }
     return best;
+}
+
+using TmaLnGeluLookup = TmaLnGeluKernel (*)(int tpr, int vpt, int rows, bool full);
+
+int choose_ln_rows(TmaLnGeluLookup lookup, int tpr, int vpt, bool full, int64_t N, int nbuf, const Tuning& tn,
+                   const LaunchCfg& cfg) {
+    return choose_group_rows(tpr, nbuf, tn, [&](int rows) {
+        const TmaLnGeluKernel k = lookup(tpr, vpt, rows, full);
+        return k.launch ? k.ctas_per_sm(N, nbuf, cfg) : 0;
+    });
+}
+
+using TmaRmsLookup = TmaRmsKernel (*)(int tpr, int vpt, int rows, bool full);
+
+// RMSNorm (r == NULL) or fused residual + RMSNorm, arguments already checked.
+rowops_status_t rms_dispatch(const void* x, const void* r, void* y, void* ro, const void* w, float eps, int64_t M,
+                             int64_t N, int64_t ld, rowops_dtype_t dtype, cudaStream_t stream) {
+    const bool res = r != nullptr;
+    const Tuning tn = read_tuning();
+    LaunchCfg cfg;
+    rowops_status_t st = make_cfg(stream, tn, &cfg);
+    if (st != ROWOPS_OK) return st;
+    const int es = elem_bytes(dtype);
+    // every row pointer at the same offset modulo 16 bytes
+    const bool phase = same_phase(x, y) && (!res || (same_phase(x, r) && same_phase(x, ro)));
+    TmaChoice tc;
+    if ((tn.family == Family::Auto || tn.family == Family::Tma) && phase &&
+        choose_tma(x, y, N, ld, es, tn, {8, 4, 2, 1}, &tc)) {
+        const int tpr = kTmaBlocks[tc.block_index], vpt = kTmaVpts[tc.vpt_index];
+        const int S = res ? 2 : 1;
+        const size_t stage = rms_tma_stage_smem(tpr, vpt, es, tc.full);
+        auto fits = [&](int nb) {
+            return size_t(kTmaRingHeader) + size_t(nb) * S * tma_row_bytes(N, es) + stage + 1024 <=
+                   size_t(cfg.max_smem_optin);
+        };
+        int nbuf = tn.ring > 0 ? (tn.ring < 2 ? 2 : (tn.ring > kTmaMaxSlots ? kTmaMaxSlots : tn.ring)) : 2;
+        while (nbuf > 2 && !fits(nbuf)) --nbuf;
+        if (fits(nbuf)) {
+            const TmaRmsLookup lookup = dtype == ROWOPS_F32 ? (res ? rms_tma_f32_residual : rms_tma_f32_plain)
+                                                            : (res ? rms_tma_bf16_residual : rms_tma_bf16_plain);
+            const int rows = choose_group_rows(tpr, nbuf, tn, [&](int rr) {
+                const TmaRmsKernel k = lookup(tpr, vpt, rr, tc.full);
+                return k.launch ? k.ctas_per_sm(N, nbuf, cfg) : 0;
+            });
+            const TmaRmsKernel k = lookup(tpr, vpt, rows, tc.full);
+            if (k.launch) return finish(k.launch(x, r, y, ro, w, eps, M, N, ld, nbuf, cfg));
+        }
+    }
+    int tpr_index = 0, vpt = 0;
+    RmsLaunch fn = nullptr;
+    const bool smem_ok = rms_reg_smem(N, es) + 256 <= size_t(cfg.max_smem_optin);
+    if (tn.family != Family::Looped && smem_ok && phase && choose_reg(N, es, tn, &tpr_index, &vpt))
+        fn = dtype == ROWOPS_F32 ? rms_reg_f32(tpr_index, vpt, res) : rms_reg_bf16(tpr_index, vpt, res);
+    if (!fn) fn = dtype == ROWOPS_F32 ? rms_looped_f32(res) : rms_looped_bf16(res);
+    return finish(fn(x, r, y, ro, w, eps, M, N, ld, cfg));
+}
+
+// the row ranges of a and b share no byte
+bool rows_disjoint(const void* a, const void* b, int64_t M, int64_t N, int64_t ld, int es) {
+    const uintptr_t span = uintptr_t(((M - 1) * ld + N) * es);
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return !(pa < pb + span && pb < pa + span);
 }
 
 }  // namespace
@@ -443,6 +500,33 @@ rowops_status_t rowops_layernorm_gelu(const void* x, void* y, const void* w, con
     }
     if (!fn) fn = dtype == ROWOPS_F32 ? ln_gelu_looped_f32() : ln_gelu_looped_bf16();
     return finish(fn(x, y, w, b, eps, M, N, ld, cfg));
+}
+
+rowops_status_t rowops_rmsnorm(const void* x, void* y, const void* w, float eps, int64_t M, int64_t N, int64_t ld,
+                               rowops_dtype_t dtype, cudaStream_t stream) {
+    rowops_status_t st = check_rows(x, y, M, N, ld, dtype);
+    if (st != ROWOPS_OK) return st;
+    if (!(eps >= 0.f) || eps == INFINITY) return ROWOPS_ERR_INVALID_VALUE;
+    if (M == 0) return ROWOPS_OK;
+    if (w && !aligned(w, elem_bytes(dtype))) return ROWOPS_ERR_INVALID_VALUE;
+    return rms_dispatch(x, nullptr, y, nullptr, w, eps, M, N, ld, dtype, stream);
+}
+
+rowops_status_t rowops_fused_residual_rmsnorm(const void* x, const void* residual, void* y, void* residual_out,
+                                              const void* w, float eps, int64_t M, int64_t N, int64_t ld,
+                                              rowops_dtype_t dtype, cudaStream_t stream) {
+    // each output either is one of the inputs or overlaps neither of them
+    rowops_status_t st = check_rows(x, y, M, N, ld, dtype);
+    if (st == ROWOPS_OK) st = check_rows(residual, residual_out, M, N, ld, dtype);
+    if (st == ROWOPS_OK) st = check_rows(x, residual_out, M, N, ld, dtype);
+    if (st == ROWOPS_OK) st = check_rows(residual, y, M, N, ld, dtype);
+    if (st != ROWOPS_OK) return st;
+    if (!(eps >= 0.f) || eps == INFINITY) return ROWOPS_ERR_INVALID_VALUE;
+    if (M == 0) return ROWOPS_OK;
+    const int es = elem_bytes(dtype);
+    if (!rows_disjoint(y, residual_out, M, N, ld, es)) return ROWOPS_ERR_INVALID_VALUE;
+    if (w && !aligned(w, es)) return ROWOPS_ERR_INVALID_VALUE;
+    return rms_dispatch(x, residual, y, residual_out, w, eps, M, N, ld, dtype, stream);
 }
 
 size_t rowops_online_softmax_workspace_bytes(int64_t M, int64_t N, rowops_dtype_t dtype) {

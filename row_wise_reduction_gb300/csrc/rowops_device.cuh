@@ -36,6 +36,8 @@ struct Elem<float> {
         return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
                           __float_as_uint(f[3]));
     }
+    // v as this type stores it
+    __device__ __forceinline__ static float round(float v) { return v; }
 };
 
 // two fp32 -> bf16x2, round to nearest even; `hi` lands in the upper half
@@ -67,6 +69,7 @@ struct Elem<bf16_t> {
         return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
                           pack_bf16x2(f[6], f[7]));
     }
+    __device__ __forceinline__ static float round(float v) { return __uint_as_float(pack_bf16x2(0.f, v) & 0xffff0000u); }
 };
 
 // ---------------------------------------------------------------------------

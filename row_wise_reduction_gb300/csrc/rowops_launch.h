@@ -60,6 +60,7 @@ constexpr int kNumTmaBlocks = 4;
 constexpr int kTmaVpts[] = {1, 2, 3, 4, 8};
 constexpr int kNumTmaVpts = 5;
 constexpr int kTmaRingHeader = 128;
+constexpr int kTmaMaxSlots = 16;  // ring slots of all row groups of a CTA (mbarriers in the ring header)
 
 using TmaSoftmaxLaunch = cudaError_t (*)(const void* x, void* y, int64_t M, int64_t N, int64_t ld, int nbuf,
                                          const LaunchCfg& cfg);
@@ -86,6 +87,43 @@ struct TmaLnGeluKernel {
 };
 TmaLnGeluKernel ln_gelu_tma_f32(int tpr, int vpt, int rows, bool full);
 TmaLnGeluKernel ln_gelu_tma_bf16(int tpr, int vpt, int rows, bool full);
+
+// RMSNorm / fused residual + RMSNorm: r, ro are the residual input and output
+// (NULL in the plain form).
+using RmsLaunch = cudaError_t (*)(const void* x, const void* r, void* y, void* ro, const void* w, float eps,
+                                  int64_t M, int64_t N, int64_t ld, const LaunchCfg& cfg);
+RmsLaunch rms_reg_f32(int tpr_index, int vpt, bool res);
+RmsLaunch rms_reg_bf16(int tpr_index, int vpt, bool res);
+RmsLaunch rms_looped_f32(bool res);
+RmsLaunch rms_looped_bf16(bool res);
+
+// Row-pipeline RMSNorm: TPR in kRmsTpr, VPT in kRmsVpt, ROWS in kRmsRows (TPR *
+// ROWS <= 512 unless ROWS = 1), full or general rows, plain or fused form.
+constexpr int kRmsTpr[] = {64, 128, 256, 512};
+constexpr int kNumRmsTpr = 4;
+constexpr int kRmsVpt[] = {1, 2, 4, 8};
+constexpr int kNumRmsVpt = 4;
+constexpr int kRmsRows[] = {1, 2, 4, 8};
+constexpr int kNumRmsRows = 4;
+using TmaRmsLaunch = cudaError_t (*)(const void* x, const void* r, void* y, void* ro, const void* w, float eps,
+                                     int64_t M, int64_t N, int64_t ld, int nbuf, const LaunchCfg& cfg);
+struct TmaRmsKernel {
+    TmaRmsLaunch launch;  // nullptr: no such instantiation
+    TmaCtasQuery ctas_per_sm;
+};
+TmaRmsKernel rms_tma_f32_plain(int tpr, int vpt, int rows, bool full);
+TmaRmsKernel rms_tma_f32_residual(int tpr, int vpt, int rows, bool full);
+TmaRmsKernel rms_tma_bf16_plain(int tpr, int vpt, int rows, bool full);
+TmaRmsKernel rms_tma_bf16_residual(int tpr, int vpt, int rows, bool full);
+// fp32 w staged by the register kernel: one unused slot per 16-byte vector of columns
+inline size_t rms_reg_smem(int64_t N, int es) {
+    const int64_t V = 16 / es;
+    return size_t(4) * size_t((N + N / V + 4) & ~int64_t(3));
+}
+// fp32 w staged by the row pipeline: thread-major, + 64 bytes of head/tail weights
+inline size_t rms_tma_stage_smem(int block, int vpt, int es, bool full) {
+    return size_t(vpt) * block * (16 / es) * 4 + (full ? 0 : 64);
+}
 
 // dynamic shared memory of the row-pipeline kernels
 inline size_t tma_row_bytes(int64_t N, int es) { return size_t((N * es + 127) / 128 * 128); }

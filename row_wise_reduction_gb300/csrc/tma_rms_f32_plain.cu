@@ -1,0 +1,8 @@
+// Row-pipeline RMSNorm kernels (plain form) instantiated for f32 rows.
+#include "tma_rms_inst.cuh"
+
+namespace rowops {
+TmaRmsKernel rms_tma_f32_plain(int tpr, int vpt, int rows, bool full) {
+    return rms_tma_lookup<float, false>(tpr, vpt, rows, full);
+}
+}  // namespace rowops

@@ -45,11 +45,13 @@ struct GroupPipe {
     bool producer;          // the group's first thread issues its copies
 };
 
-// `period`: number of phase classes (1: every CTA takes every kind of row).
+// `period`: number of phase classes (1: every CTA takes every kind of row);
+// `streams`: rows of that many inputs share each ring slot.
 template <int TPR, int ROWS>
-__device__ __forceinline__ GroupPipe make_group(char* smem, int64_t N, int es, int nbuf, int period = 1) {
+__device__ __forceinline__ GroupPipe make_group(char* smem, int64_t N, int es, int nbuf, int period = 1,
+                                                int streams = 1) {
     const int g = threadIdx.x / TPR;
-    const uint32_t rb = ring_row_bytes(N, es);
+    const uint32_t rb = uint32_t(streams) * ring_row_bytes(N, es);
     GroupPipe p;
     p.ring = RowRing{reinterpret_cast<uint64_t*>(smem) + g * nbuf, smem + kRingHeader + size_t(g) * nbuf * rb, rb,
                      nbuf};

@@ -28,6 +28,8 @@ __all__ = [
     "rowops_online_softmax_noalloc",
     "rowops_device_status",
     "rowops_layernorm_gelu",
+    "rowops_rmsnorm",
+    "rowops_fused_residual_rmsnorm",
     "rowops_status_string",
     "ROWOPS_F32",
     "ROWOPS_BF16",
@@ -92,6 +94,11 @@ def library() -> ctypes.CDLL:
         L.rowops_layernorm_gelu.restype = ctypes.c_int
         L.rowops_layernorm_gelu.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, _i64, _i64, _i64,
                                             ctypes.c_int, _vp]
+        L.rowops_rmsnorm.restype = ctypes.c_int
+        L.rowops_rmsnorm.argtypes = [_vp, _vp, _vp, ctypes.c_float, _i64, _i64, _i64, ctypes.c_int, _vp]
+        L.rowops_fused_residual_rmsnorm.restype = ctypes.c_int
+        L.rowops_fused_residual_rmsnorm.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _i64, _i64, _i64,
+                                                    ctypes.c_int, _vp]
         _lib = L
     return _lib
 
@@ -235,3 +242,52 @@ def rowops_layernorm_gelu(
         b.data_ptr() if b is not None else None, float(eps), M, N, ld, _dtype_code(x), _stream(stream))
     _check("rowops_layernorm_gelu", st)
     return y
+
+
+def _weight(w: Optional[torch.Tensor], x: torch.Tensor, N: int, name: str = "w"):
+    if w is None:
+        return None
+    if w.dtype != x.dtype or w.device != x.device or w.numel() != N or not w.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor of N entries with x's dtype")
+    return w.data_ptr()
+
+
+def rowops_rmsnorm(
+    x: torch.Tensor,
+    w: Optional[torch.Tensor] = None,
+    eps: float = 1e-5,
+    y: Optional[torch.Tensor] = None,
+    *,
+    stream=None,
+) -> torch.Tensor:
+    """RMSNorm of every row of ``x``: x * rsqrt(mean(x^2) + eps) * w."""
+    M, N, ld = _rows(x, "x")
+    y = _out_like(x, y)
+    st = library().rowops_rmsnorm(x.data_ptr(), y.data_ptr(), _weight(w, x, N), float(eps), M, N, ld,
+                                  _dtype_code(x), _stream(stream))
+    _check("rowops_rmsnorm", st)
+    return y
+
+
+def rowops_fused_residual_rmsnorm(
+    x: torch.Tensor,
+    residual: torch.Tensor,
+    w: Optional[torch.Tensor] = None,
+    eps: float = 1e-5,
+    y: Optional[torch.Tensor] = None,
+    residual_out: Optional[torch.Tensor] = None,
+    *,
+    stream=None,
+):
+    """residual_out = x + residual and y = RMSNorm(residual_out) * w, in one
+    pass; returns ``(y, residual_out)``. Outputs may be given (e.g.
+    ``residual_out=residual`` to update the residual stream in place)."""
+    M, N, ld = _rows(x, "x")
+    _out_like(x, residual)  # same shape, dtype, device and row stride
+    y = _out_like(x, y)
+    residual_out = _out_like(x, residual_out)
+    st = library().rowops_fused_residual_rmsnorm(
+        x.data_ptr(), residual.data_ptr(), y.data_ptr(), residual_out.data_ptr(), _weight(w, x, N), float(eps),
+        M, N, ld, _dtype_code(x), _stream(stream))
+    _check("rowops_fused_residual_rmsnorm", st)
+    return y, residual_out

@@ -81,3 +81,21 @@ def assert_ln_gelu_close(got: np.ndarray, ref: np.ndarray, dtype: str, what: str
         f"{what}: max excess {float((err - tol).max()):.3e} at got={g.flat[worst]!r} ref={r.flat[worst]!r}"
     )
     return float(err.max()) if err.size else 0.0
+
+
+def assert_rms_close(got: np.ndarray, ref: np.ndarray, dtype: str, what: str = "rmsnorm", rel: float = 0.0):
+    """RMSNorm outputs: fp32 max absolute error 1e-5 (the fp32 bar of the
+    LayerNorm+GELU workloads, whose outputs have the same O(1) magnitude);
+    bf16 within 1 bf16 ulp. y = s * inv_rms * w has no cancellation, so no
+    extra floor. ``rel`` as for assert_ln_gelu_close."""
+    got = np.asarray(got, dtype=np.float64)
+    ok = _check_nan(got, ref, what)
+    g, r = got[ok], ref[ok]
+    tol = np.full_like(r, 1e-5) if dtype == "f32" else bf16_ulp(r)
+    tol = tol + rel * np.abs(r)
+    err = np.abs(g - r)
+    worst = np.argmax(err - tol) if err.size else 0
+    assert np.all(err <= tol), (
+        f"{what}: max excess {float((err - tol).max()):.3e} at got={g.flat[worst]!r} ref={r.flat[worst]!r}"
+    )
+    return float(err.max()) if err.size else 0.0

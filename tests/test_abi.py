@@ -32,7 +32,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("rowops_softmax", "rowops_online_softmax", "rowops_layernorm_gelu",
-              "rowops_online_softmax_workspace_bytes", "rowops_online_softmax_status", "rowops_status_string"):
+              "rowops_online_softmax_workspace_bytes", "rowops_online_softmax_status", "rowops_status_string",
+              "rowops_rmsnorm", "rowops_fused_residual_rmsnorm"):
         assert n in names
 
 
@@ -83,6 +84,37 @@ def test_layernorm_gelu_validation(lib):
     assert f(X, Y, None, Y + 0x40002, 1e-5, 4, 8, 8, F32, None) == INVALID  # misaligned b
     assert f(X, Y, None, None, 1e-5, 4, 8, 4, F32, None) == INVALID  # ld < N
     assert f(None, None, None, None, 1e-5, 0, 8, 8, F32, None) == OK
+
+
+def test_rmsnorm_validation(lib):
+    f = lib.rowops_rmsnorm
+    assert f(X, Y, None, -1.0, 4, 8, 8, F32, None) == INVALID  # eps < 0
+    assert f(X, Y, None, float("nan"), 4, 8, 8, F32, None) == INVALID
+    assert f(X, Y, X + 0x40001, 1e-5, 4, 8, 8, BF16, None) == INVALID  # misaligned w
+    assert f(X, X + 16, None, 1e-5, 4, 8, 8, F32, None) == INVALID  # partial overlap
+    assert f(None, Y, None, 1e-5, 4, 8, 8, F32, None) == INVALID
+    assert f(X, Y, None, 1e-5, 4, 8, 8, 5, None) == INVALID  # bad dtype
+    assert f(None, None, None, 1e-5, 0, 8, 8, F32, None) == OK
+
+
+R, RO = 0x200000, 0x300000
+
+
+def test_fused_residual_rmsnorm_validation(lib):
+    f = lib.rowops_fused_residual_rmsnorm
+    args = lambda x=X, r=R, y=Y, ro=RO, w=None, eps=1e-5, M=4, N=8, ld=8, dt=F32: (x, r, y, ro, w, eps, M, N, ld, dt,
+                                                                                  None)
+    assert f(*args(r=None)) == INVALID  # null residual
+    assert f(*args(ro=None)) == INVALID  # null residual_out
+    assert f(*args(eps=-1.0)) == INVALID
+    assert f(*args(y=RO)) == INVALID  # y and residual_out are the same memory
+    assert f(*args(y=RO + 64)) == INVALID  # y overlaps residual_out
+    assert f(*args(ro=X + 16)) == INVALID  # residual_out partly overlaps x
+    assert f(*args(y=R + 32)) == INVALID  # y partly overlaps residual
+    assert f(*args(w=X + 0x40002, dt=F32)) == INVALID  # misaligned w
+    assert f(*args(ro=R + 1, dt=BF16)) == INVALID  # misaligned residual_out
+    assert f(*args(N=1 << 31, ld=1 << 31)) == UNSUPPORTED
+    assert f(None, None, None, None, None, 1e-5, 0, 8, 8, F32, None) == OK
 
 
 def test_online_softmax_workspace_bytes(lib):

@@ -8,6 +8,7 @@ a slot nothing then sets), and ROWOPS_WAIT_LIMIT_NS shortens every wait to
 20 ms. The kernel gives up, drains its own copies, records the timeout and
 returns; the next call without the hook is correct and clean.
 """
+import numpy as np
 import pytest
 import torch
 
@@ -82,3 +83,25 @@ def test_single_read_split_softmax_wait_times_out(oracle, monkeypatch, staging):
     y = rowops_online_softmax(x, workspace=ws)
     assert rowops_online_softmax_status(ws) == 0
     C.assert_softmax_close(C.to_f64(y), oracle.softmax(gu.rows_f32(x)), "f32")
+
+
+def test_rmsnorm_pipeline_wait_times_out(oracle, monkeypatch):
+    """The fused residual RMSNorm ring (two input rows per slot on one
+    mbarrier): the stalled row's wait gives up, the next call is correct."""
+    from row_wise_reduction_gb300 import rowops_fused_residual_rmsnorm
+
+    wl = workloads.Workload("timeout_rms", "residual_rmsnorm", "bf16", 1500, 8192, seed=6, affine=True,
+                            residual=True)
+    inp = gu.make_x(wl)
+    monkeypatch.setenv("ROWOPS_KERNEL", "tma")
+    monkeypatch.setenv("ROWOPS_WAIT_LIMIT_NS", LIMIT_NS)
+    monkeypatch.setenv("ROWOPS_TEST_STALL_ROW", "11")
+    rowops_fused_residual_rmsnorm(inp["x"], inp["residual"], inp["w"], wl.eps)
+    assert rowops_device_status() == TIMEOUT
+    monkeypatch.delenv("ROWOPS_TEST_STALL_ROW")
+    y, ro = rowops_fused_residual_rmsnorm(inp["x"], inp["residual"], inp["w"], wl.eps)
+    assert rowops_device_status() == 0
+    s_ref, y_ref = oracle.residual_rmsnorm(gu.rows_f32(inp["x"]), gu.rows_f32(inp["residual"]),
+                                           inp["w"].float().cpu().numpy(), wl.eps, "bf16")
+    np.testing.assert_array_equal(C.to_f64(ro), s_ref)
+    C.assert_rms_close(C.to_f64(y), y_ref, "bf16")
