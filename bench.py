@@ -43,7 +43,7 @@ from row_wise_reduction_gb300 import workloads  # noqa: E402
 METRIC = "row-kernel HBM GB/s (% of GB300 peak) for softmax and LayerNorm+GELU"
 STEP = ["softmax_bf16_causal_32768x4096", "online_softmax_f32_64x1048576", "layernorm_gelu_bf16_65536x8192"]
 DOMINANT = "layernorm_gelu_bf16_65536x8192"
-KERNELS_PER_CALL = {"softmax": 1, "online_softmax": 2, "layernorm_gelu": 1}
+KERNELS_PER_CALL = {"softmax": 1, "online_softmax": 2, "layernorm_gelu": 1, "rmsnorm": 1, "residual_rmsnorm": 1}
 L2_BYTES = 129 * 10**6
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "ln_gelu_bf16_65536x8192.txt")
@@ -56,8 +56,17 @@ DOMINANT_SOURCES = ["row_wise_reduction_gb300/csrc/tma_row_kernels.cuh",
 
 
 def alg_bytes(wl: workloads.Workload) -> int:
+    """Each input element read once, each output element written once, w (and
+    b) once per launch."""
     es = workloads.elem_size(wl.dtype)
-    return 2 * wl.M * wl.N * es + (2 * wl.N * es if wl.affine else 0)
+    rows = 2 * wl.M * wl.N * es
+    if wl.op == "layernorm_gelu":
+        return rows + (2 * wl.N * es if wl.affine else 0)
+    if wl.op == "rmsnorm":
+        return rows + (wl.N * es if wl.affine else 0)
+    if wl.op == "residual_rmsnorm":  # x, residual in; y, residual_out out
+        return 2 * rows + (wl.N * es if wl.affine else 0)
+    return rows
 
 
 def dominant_source_hash() -> str:
@@ -375,8 +384,10 @@ def config_block():
 # the other workloads, reported beside the step (not part of its value)
 # ---------------------------------------------------------------------------
 EXTRA = ["softmax_f32_1024x768", "layernorm_gelu_f32_4096x768", "layernorm_gelu_bf16_65536x127",
-         "layernorm_gelu_bf16_65536x4097"]
-SMALL = {"softmax_f32_1024x768", "layernorm_gelu_f32_4096x768"}
+         "layernorm_gelu_bf16_65536x4097", "rmsnorm_f32_4096x768", "residual_rmsnorm_f32_4096x768",
+         "rmsnorm_bf16_65536x8192", "residual_rmsnorm_bf16_65536x8192"]
+SMALL = {"softmax_f32_1024x768", "layernorm_gelu_f32_4096x768", "rmsnorm_f32_4096x768",
+         "residual_rmsnorm_f32_4096x768"}
 
 
 def run_extras(dev, stream, iters=50):
@@ -391,10 +402,15 @@ def run_extras(dev, stream, iters=50):
         wl = workloads.WORKLOADS[name]
         inp = workloads.make_inputs(wl, dev)
         x, y = inp["x"], torch.empty_like(inp["x"])
+        r_out = torch.empty_like(x) if wl.residual else None
 
         def call():
             if wl.op == "softmax":
                 ro.rowops_softmax(x, y)
+            elif wl.op == "rmsnorm":
+                ro.rowops_rmsnorm(x, inp.get("w"), wl.eps, y)
+            elif wl.op == "residual_rmsnorm":
+                ro.rowops_fused_residual_rmsnorm(x, inp["residual"], inp.get("w"), wl.eps, y, r_out)
             else:
                 ro.rowops_layernorm_gelu(x, inp.get("w"), inp.get("b"), wl.eps, y)
 
@@ -410,6 +426,10 @@ def run_extras(dev, stream, iters=50):
         hot = a.elapsed_time(b) / iters / 1e3
         rec = {"bytes": alg_bytes(wl), "hot_us": hot * 1e6, "hot_gbs": alg_bytes(wl) / hot / 1e9,
                "hot_rows_per_s": wl.M / hot}
+        if alg_bytes(wl) > L2_BYTES:
+            rec["frac_of_" + measured_peak()[1]] = rec["hot_gbs"] / measured_peak()[0]
+        if wl.op in ("rmsnorm", "residual_rmsnorm") and wl.M * wl.N > 10**6:
+            rec["torch_eager"] = torch_eager_time(wl, inp, stream)
         if name in SMALL:
             cold = []
             for _ in range(10):
@@ -440,9 +460,39 @@ def run_extras(dev, stream, iters=50):
             gt = a.elapsed_time(b) / iters / 1e3
             rec.update(graph_us=gt * 1e6, graph_gbs=alg_bytes(wl) / gt / 1e9, l2_resident=True)
         out[name] = rec
-        del inp, x, y
+        del inp, x, y, r_out
     del flush
     return out
+
+
+def torch_eager_time(wl, inp, stream, iters=10):
+    """PyTorch eager on an RMSNorm workload, as context: F.rms_norm, and for the
+    fused form x + residual followed by F.rms_norm (two kernels at least)."""
+    import torch.nn.functional as F
+
+    x, w = inp["x"], inp.get("w")
+    if wl.op == "rmsnorm":
+        def call():
+            return F.rms_norm(x, (wl.N,), w, wl.eps)
+        what = "F.rms_norm(x, (N,), w, eps)"
+    else:
+        r = inp["residual"]
+
+        def call():
+            s = x + r
+            return F.rms_norm(s, (wl.N,), w, wl.eps), s
+        what = "s = x + residual; F.rms_norm(s, (N,), w, eps)"
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(iters):
+        call()
+    b.record(stream)
+    torch.cuda.synchronize()
+    t = a.elapsed_time(b) / iters / 1e3
+    return {"call": what, "us": t * 1e6, "gbs": alg_bytes(wl) / t / 1e9}
 
 
 def run_torch_eager(wls, inputs, stream, iters=10):
@@ -518,12 +568,18 @@ def run_rowops(args):
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
 
+    res_out = {n: torch.empty_like(inputs[n]["x"]) for n, wl in wls.items() if wl.residual}
+
     def call(n, x, y):
         wl = wls[n]
         if wl.op == "softmax":
             ro.rowops_softmax(x, y)
         elif wl.op == "online_softmax":
             ro.rowops_online_softmax(x, y, workspace=ws[n])
+        elif wl.op == "rmsnorm":
+            ro.rowops_rmsnorm(x, inputs[n]["w"], wl.eps, y)
+        elif wl.op == "residual_rmsnorm":
+            ro.rowops_fused_residual_rmsnorm(x, inputs[n]["residual"], inputs[n]["w"], wl.eps, y, res_out[n])
         else:
             ro.rowops_layernorm_gelu(x, inputs[n]["w"], inputs[n]["b"], wl.eps, y)
 
@@ -571,10 +627,13 @@ def run_rowops(args):
     if not args.no_e2e:
         host_in = {n: inputs[n]["x"].cpu().pin_memory() for n in names}
         host_out = {n: torch.empty(outputs[n].shape, dtype=outputs[n].dtype).pin_memory() for n in names}
-        host_wb = {n: {k: inputs[n][k].cpu().pin_memory() for k in ("w", "b") if k in inputs[n]} for n in names}
+        host_wb = {n: {k: inputs[n][k].cpu().pin_memory() for k in ("w", "b", "residual") if k in inputs[n]}
+                   for n in names}
+        host_ro = {n: torch.empty(res_out[n].shape, dtype=res_out[n].dtype).pin_memory() for n in res_out}
         h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + \
             sum(t.numel() * t.element_size() for d in host_wb.values() for t in d.values())
-        d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+        d2h = sum(t.numel() * t.element_size() for t in host_out.values()) + \
+            sum(t.numel() * t.element_size() for t in host_ro.values())
         ke = max(2, min(K, args.e2e_steps))
 
         def e2e_step():
@@ -584,6 +643,8 @@ def run_rowops(args):
                 inputs[n]["x"].copy_(host_in[n], non_blocking=True)
                 call(n, inputs[n]["x"], outputs[n])
                 host_out[n].copy_(outputs[n], non_blocking=True)
+                if n in host_ro:
+                    host_ro[n].copy_(res_out[n], non_blocking=True)
 
         e2e_step()
         torch.cuda.synchronize()

@@ -48,6 +48,11 @@
  *   ROWOPS_PERSIST_LOOKAHEAD=<2k> / ROWOPS_PERSIST_PREFETCH=<n>  its pipeline depths
  *   ROWOPS_CTAS_PER_SM=<k>        persistent grid of k CTAs per SM (0 = occupancy limit,
  *                                 -1 = one CTA per row group, no persistence)
+ *   ROWOPS_SCHED=static|dynamic   row schedule of the row pipeline on full rows: static (each
+ *                                 row group a fixed share) or dynamic (work units taken with
+ *                                 cluster launch control); default dynamic for the RMSNorm
+ *                                 entry points, static otherwise
+ *   ROWOPS_UNIT_ROWS=<n>          dynamic schedule: rows per row group in one work unit (default 1)
  *   ROWOPS_WAIT_LIMIT_NS=<ns>     limit of every device-side wait (default 2 s)
  *   ROWOPS_TEST_STALL_ROW=<row>   test hook for the timeout path: the wait that concerns this
  *                                 row is made to run out (the row pipeline's bulk copy of it is

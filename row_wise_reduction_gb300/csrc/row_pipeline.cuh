@@ -87,6 +87,11 @@ __device__ __forceinline__ void tma_load_row(void* dst, const void* src, uint32_
         : "memory");
 }
 
+// One plain arrival (no bytes): completes a phase that expects nothing else.
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
 // The same in two steps, for several copies completing on one barrier: one
 // expect of their total bytes, then each copy.
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {

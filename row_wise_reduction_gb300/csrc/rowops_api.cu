@@ -33,6 +33,8 @@ struct Tuning {
     int prefetch = 0;   // its L2 prefetch distance in rows (0: automatic)
     long long wait_ns = 0;    // device-side wait limit (0: 2 s)
     long long stall_row = -1; // test hook (see include/rowops.h)
+    int sched = 0;            // full-row pipelines: 0 automatic, 1 static, 2 dynamic (cluster launch control)
+    int unit_rows = 0;        // dynamic schedule: rows per group in a work unit (0: automatic)
 };
 
 int env_int(const char* name, int dflt) {
@@ -61,6 +63,11 @@ Tuning read_tuning() {
     if (const char* v = std::getenv("ROWOPS_WAIT_LIMIT_NS")) t.wait_ns = std::strtoll(v, nullptr, 10);
     if (const char* v = std::getenv("ROWOPS_TEST_STALL_ROW")) t.stall_row = std::strtoll(v, nullptr, 10);
     t.prefetch = env_int("ROWOPS_PERSIST_PREFETCH", 0);
+    t.unit_rows = env_int("ROWOPS_UNIT_ROWS", 0);
+    if (const char* k = std::getenv("ROWOPS_SCHED")) {
+        if (!std::strcmp(k, "static")) t.sched = 1;
+        else if (!std::strcmp(k, "dynamic")) t.sched = 2;
+    }
     if (const char* k = std::getenv("ROWOPS_ONLINE")) {
         if (!std::strcmp(k, "two_pass")) t.online = 1;
         else if (!std::strcmp(k, "single_read")) t.online = 2;
@@ -154,6 +161,8 @@ rowops_status_t make_cfg(cudaStream_t stream, const Tuning& tn, LaunchCfg* cfg) 
     cfg->persist_prefetch = tn.prefetch;
     cfg->wait_ns = tn.wait_ns > 0 ? (unsigned long long)tn.wait_ns : 2000000000ull;
     cfg->stall_row = tn.stall_row;
+    // full-row pipelines: static schedule unless asked for (RMSNorm chooses its own, rms_dispatch)
+    cfg->unit_rows = tn.sched == 2 ? (tn.unit_rows > 0 ? tn.unit_rows : 1) : 0;
     return ROWOPS_OK;
 }
 
@@ -339,6 +348,10 @@ rowops_status_t rms_dispatch(const void* x, const void* r, void* y, void* ro, co
     LaunchCfg cfg;
     rowops_status_t st = make_cfg(stream, tn, &cfg);
     if (st != ROWOPS_OK) return st;
+    // Full rows take the dynamic schedule by default here: at bf16 65536 x 8192 it
+    // is 10% faster than the static one for both forms (311 vs 347 us, 614 vs
+    // 677 us on GB300), where softmax and LayerNorm+GELU run 5-10% slower with it.
+    if (tn.sched == 0) cfg.unit_rows = tn.unit_rows > 0 ? tn.unit_rows : 1;
     const int es = elem_bytes(dtype);
     // every row pointer at the same offset modulo 16 bytes
     const bool phase = same_phase(x, y) && (!res || (same_phase(x, r) && same_phase(x, ro)));

@@ -26,6 +26,8 @@ struct LaunchCfg {
     bool persist_l2 = false;    // single-read split-row softmax staged in L2 instead of shared memory
     int persist_prefetch = 0;   // rows of L2 prefetch ahead (0: automatic)
     unsigned long long wait_ns = 2000000000ull;  // limit of every device-side wait
+    int unit_rows = 0;          // full-row pipelines: 0 static schedule, else rows per group in a work
+                                // unit taken by cluster launch control
     int64_t stall_row = -1;     // test hook: the row whose wait is made to run out (-1: none)
 };
 
@@ -61,6 +63,12 @@ constexpr int kTmaVpts[] = {1, 2, 3, 4, 8};
 constexpr int kNumTmaVpts = 5;
 constexpr int kTmaRingHeader = 128;
 constexpr int kTmaMaxSlots = 16;  // ring slots of all row groups of a CTA (mbarriers in the ring header)
+// dynamic schedule: one CTA per work unit of rows_per_cta * unit_rows rows
+inline int dyn_grid(int64_t M, int rows_per_cta, int unit_rows) {
+    const int64_t unit = int64_t(rows_per_cta) * unit_rows;
+    const int64_t g = (M + unit - 1) / unit;
+    return int(g < 1 ? 1 : (g > 0x7fffffff ? 0x7fffffff : g));
+}
 
 using TmaSoftmaxLaunch = cudaError_t (*)(const void* x, void* y, int64_t M, int64_t N, int64_t ld, int nbuf,
                                          const LaunchCfg& cfg);

@@ -19,9 +19,10 @@ cudaError_t launch_softmax_tma(const void* x, void* y, int64_t M, int64_t N, int
     const size_t smem = tma_ring_bytes<T>(N, nbuf);
     cudaError_t e = allow_smem(reinterpret_cast<const void*>(kern), smem, cfg);
     if (e != cudaSuccess) return e;
-    const int grid = grid_for(reinterpret_cast<const void*>(kern), TPR, smem, M, cfg);
+    const int unit = FULL ? cfg.unit_rows : 0;  // 0: static schedule
+    const int grid = unit ? dyn_grid(M, 1, unit) : grid_for(reinterpret_cast<const void*>(kern), TPR, smem, M, cfg);
     kern<<<grid, TPR, smem, cfg.stream>>>(static_cast<const T*>(x), static_cast<T*>(y), M, int(N), ld, nbuf,
-                                          cfg.dev_error, cfg.wait_ns, cfg.stall_row);
+                                          cfg.dev_error, cfg.wait_ns, cfg.stall_row, unit);
     return cudaGetLastError();
 }
 
@@ -39,14 +40,16 @@ cudaError_t launch_ln_gelu_tma_rows(const void* x, void* y, const void* w, const
     const size_t smem = ln_gelu_tma_smem<T, TPR, VPT, ROWS, FULL>(N, nbuf);
     cudaError_t e = allow_smem(reinterpret_cast<const void*>(kern), smem, cfg);
     if (e != cudaSuccess) return e;
-    int grid = grid_for(reinterpret_cast<const void*>(kern), TPR * ROWS, smem, (M + ROWS - 1) / ROWS, cfg);
+    const int unit = FULL ? cfg.unit_rows : 0;  // 0: static schedule
+    int grid = unit ? dyn_grid(M, ROWS, unit)
+                    : grid_for(reinterpret_cast<const void*>(kern), TPR * ROWS, smem, (M + ROWS - 1) / ROWS, cfg);
     if (!FULL) {  // whole phase classes: every class needs a CTA, and they share the grid evenly
         const int period = row_phase_period(ld * int64_t(Elem<T>::kBytes));
         grid = grid >= period ? grid - grid % period : period;
     }
     kern<<<grid, TPR * ROWS, smem, cfg.stream>>>(static_cast<const T*>(x), static_cast<T*>(y),
                                                  static_cast<const T*>(w), static_cast<const T*>(b), eps, M, int(N),
-                                                 ld, nbuf, cfg.dev_error, cfg.wait_ns, cfg.stall_row);
+                                                 ld, nbuf, cfg.dev_error, cfg.wait_ns, cfg.stall_row, unit);
     return cudaGetLastError();
 }
 

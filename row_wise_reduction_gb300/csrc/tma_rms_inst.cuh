@@ -21,7 +21,9 @@ cudaError_t launch_rms_tma(const void* x, const void* r, void* y, void* ro, cons
     const size_t smem = rms_tma_smem<T, TPR, VPT, ROWS, FULL, RES>(N, nbuf);
     cudaError_t e = allow_smem(reinterpret_cast<const void*>(kern), smem, cfg);
     if (e != cudaSuccess) return e;
-    int grid = grid_for(reinterpret_cast<const void*>(kern), TPR * ROWS, smem, (M + ROWS - 1) / ROWS, cfg);
+    const int unit = FULL ? cfg.unit_rows : 0;  // 0: static schedule
+    int grid = unit ? dyn_grid(M, ROWS, unit)
+                    : grid_for(reinterpret_cast<const void*>(kern), TPR * ROWS, smem, (M + ROWS - 1) / ROWS, cfg);
     if (!FULL) {  // whole phase classes: every class needs a CTA, and they share the grid evenly
         const int period = row_phase_period(ld * int64_t(Elem<T>::kBytes));
         grid = grid >= period ? grid - grid % period : period;
@@ -29,7 +31,7 @@ cudaError_t launch_rms_tma(const void* x, const void* r, void* y, void* ro, cons
     kern<<<grid, TPR * ROWS, smem, cfg.stream>>>(static_cast<const T*>(x), static_cast<const T*>(r),
                                                  static_cast<T*>(y), static_cast<T*>(ro), static_cast<const T*>(w),
                                                  eps, M, int(N), ld, nbuf, cfg.dev_error, cfg.wait_ns,
-                                                 cfg.stall_row);
+                                                 cfg.stall_row, unit);
     return cudaGetLastError();
 }
 

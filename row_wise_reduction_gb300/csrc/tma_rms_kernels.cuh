@@ -91,13 +91,14 @@ __device__ __forceinline__ void refill_rows(const GroupPipe& p, int s, int64_t r
 template <typename T, int TPR, int VPT, int ROWS, bool FULL, bool RES>
 __global__ void __launch_bounds__(TPR * ROWS)
     rms_tma_kernel(const T* x, const T* res, T* y, T* res_out, const T* w, float eps, int64_t M, int N, int64_t ld,
-                   int nbuf, unsigned* err, unsigned long long wait_ns, int64_t stall_row) {
+                   int nbuf, unsigned* err, unsigned long long wait_ns, int64_t stall_row, int unit_rows) {
     using E = Elem<T>;
     constexpr int V = E::kVec, H = V / 4, S = RES ? 2 : 1;
     static_assert(TPR % 64 == 0, "row groups of at least two warps");
     extern __shared__ __align__(128) char smem[];
     // one reduction per row: two buffers per group used alternately
     __shared__ float red[ROWS][2][TPR / 32];
+    __shared__ ClcShared cs;
     const int period = FULL ? 1 : row_phase_period(ld * E::kBytes);
     const GroupPipe p = make_group<TPR, ROWS>(smem, N, E::kBytes, nbuf, period, S);
     const int g = threadIdx.x / TPR, t = threadIdx.x % TPR;
@@ -109,7 +110,10 @@ __global__ void __launch_bounds__(TPR * ROWS)
     // the split shared by every row of this CTA's phase class
     const RowSpan sp = row_span<T, FULL>(x + int64_t(p.cls) * ld, N);
     const T* const src[2] = {x, res};
-    start_rows<T, FULL, ROWS, S>(smem, p, src, M, N, ld, stall_row);
+    const bool dynamic = FULL && unit_rows > 0;  // unit_rows 0: static schedule
+    DynFeed f{};
+    if (dynamic) f = dyn_start<T, ROWS, S>(smem, p, cs, g, src, N, ld, M, stall_row, wait_ns, err, unit_rows);
+    else start_rows<T, FULL, ROWS, S>(smem, p, src, M, N, ld, stall_row);
     stage_weight_thread_major<T, TPR, VPT>(w, sp.head, sp.body, sw4);
     if constexpr (!FULL) {
         for (int e = threadIdx.x; e < sp.head + sp.tail; e += blockDim.x)
@@ -120,16 +124,26 @@ __global__ void __launch_bounds__(TPR * ROWS)
     const int ecol = has_ex ? span_extra_col(sp, t, V) : 0;
 
     for (int64_t i = 0;; ++i) {
-        const int64_t row = p.first + i * p.stride;
-        if (row >= M) break;
         const int s = int(i % nbuf);
+        int64_t row;
+        int fail = 0;
+        if (dynamic) {
+            row = dyn_row(p, cs, g, i, wait_ns, fail);
+            if (row < 0) {  // the end of the work (a failed wait goes on to the reduction below)
+                dyn_finish(f, cs, wait_ns);
+                return;
+            }
+        } else {
+            row = p.first + i * p.stride;
+            if (row >= M) break;
+        }
         const int64_t off = row * ld;
         float ex = 0.f;
         if (has_ex) {
             ex = E::load(x + off + ecol);
             if constexpr (RES) ex = E::round(ex + E::load(res + off + ecol));
         }
-        int fail = !mbar_wait(p.ring.bar + s, uint32_t((i / nbuf) & 1), wait_ns);
+        if (!dynamic) fail = !mbar_wait(p.ring.bar + s, uint32_t((i / nbuf) & 1), wait_ns);
         const char* sbuf = p.ring.slot(s);
 
         float v[VPT][V];
@@ -152,10 +166,15 @@ __global__ void __launch_bounds__(TPR * ROWS)
         }
         q = row_reduce<TPR>(q, red[g][i & 1], p.bar_id, OpSum(), fail);
         if (fail) {
-            abandon(p, i, M, err, wait_ns);
+            if (dynamic) dyn_abandon(p, f, cs, g, i, err, wait_ns);
+            else abandon(p, i, M, err, wait_ns);
             return;
         }
-        refill_rows<T, FULL, S>(p, s, row, src, M, N, ld, stall_row);
+        if (dynamic) {
+            if (p.producer) dyn_issue<T, ROWS, S>(p, cs, f, g, s, src, N, ld, M, stall_row, wait_ns, err);
+        } else {
+            refill_rows<T, FULL, S>(p, s, row, src, M, N, ld, stall_row);
+        }
         const float inv = rsqrtf(q / fN + eps);
         T* yb = y + off + sp.head;
 #pragma unroll

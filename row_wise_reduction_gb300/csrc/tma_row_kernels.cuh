@@ -140,31 +140,230 @@ __device__ __forceinline__ void abandon(const GroupPipe& p, int64_t i, int64_t M
     atomicExch(err, kDeviceErrTimeout);
 }
 
+// ---------------------------------------------------------------------------
+// Dynamic row schedule (full rows). A static schedule gives every row group the
+// same number of rows, and the kernel ends with its slowest SM: on GB300 the
+// busiest SM is active ~6% longer than the average one. Instead the grid is one
+// CTA per work unit of rows; the resident CTAs take the units
+// of CTAs that have not started yet with cluster launch control (a CTA cancels
+// a pending CTA and processes its unit), so fast SMs take more rows and
+// nothing but the last unit waits. A unit holds `unit_rows` rows of each group. Thread 0 keeps one steal request in flight,
+// its 16-byte response double-buffered in shared memory (`full` completes when
+// a response lands, `empty` when every group's producer has read it), and
+// issues the next request only after a successful one. Each group's producer
+// takes the rows of the units in order, writes the row of every ring slot next
+// to the slot, and marks the end of the work by a plain arrival on the slot.
+// ---------------------------------------------------------------------------
+struct __align__(16) ClcShared {
+    uint4 resp[2];
+    uint64_t full[2];
+    uint64_t empty[2];
+    int64_t slot_row[kMaxRingBuffers];  // row of ring slot s of group g at g * nbuf + s; -1: end
+};
+
+// Producer-side state of the dynamic schedule (in each group's producer thread).
+struct DynFeed {
+    int64_t unit;  // work unit whose rows are being taken
+    int c;         // next row of the unit, 0 .. rows
+    int rows;      // rows of each group in a work unit
+    int k;         // responses read: unit k came with response k - 1
+    bool end, requester, pending;
+};
+
+__device__ __forceinline__ void clc_init(ClcShared& cs, int rows) {
+    mbar_init(&cs.full[0], 1);
+    mbar_init(&cs.full[1], 1);
+    mbar_init(&cs.empty[0], unsigned(rows));
+    mbar_init(&cs.empty[1], unsigned(rows));
+}
+
+// Request r: cancel a CTA that has not started; the response lands in entry r & 1.
+__device__ __forceinline__ void clc_request(ClcShared& cs, int r) {
+    fence_proxy_async_smem();  // the entry's last response was read through the generic proxy
+    mbar_expect_tx(&cs.full[r & 1], 16u);
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
+            smem_addr(&cs.resp[r & 1])),
+        "r"(smem_addr(&cs.full[r & 1]))
+        : "memory");
+}
+
+// true and the cancelled CTA's x index (its work unit), or false: no CTA was left.
+__device__ __forceinline__ bool clc_taken(const uint4* resp, int64_t& unit) {
+    uint32_t ok, cx = 0;
+    asm volatile(
+        "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+        "ld.shared.b128 r, [%2];\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t"
+        "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t}"
+        : "=r"(ok), "+r"(cx)
+        : "r"(smem_addr(resp))
+        : "memory");
+    unit = int64_t(cx);
+    return ok != 0;
+}
+
+// The producer's next row (-1: no more work). `fail` is set if a wait on the
+// schedule gave up; the caller then ends the group's work like a finished one.
+template <int ROWS>
+__device__ __forceinline__ int64_t dyn_next_row(DynFeed& f, ClcShared& cs, int g, int64_t M,
+                                                unsigned long long wait_ns, int& fail) {
+    for (;;) {
+        if (f.end) return -1;
+        if (f.c == f.rows) {
+            const int r = f.k;  // response r carries unit r + 1
+            if (!mbar_wait(&cs.full[r & 1], uint32_t((r >> 1) & 1), wait_ns)) {
+                fail = 1;
+                f.end = true;
+                return -1;
+            }
+            int64_t unit;
+            const bool taken = clc_taken(&cs.resp[r & 1], unit);
+            mbar_arrive(&cs.empty[r & 1]);
+            if (f.requester) f.pending = false;
+            f.k = r + 1;
+            if (!taken) {
+                f.end = true;
+                return -1;
+            }
+            if (f.requester) {
+                // request r + 1 reuses the entry of response r - 1: every group must have read it
+                if (r >= 1 && !mbar_wait(&cs.empty[(r + 1) & 1], uint32_t(((r - 1) >> 1) & 1), wait_ns)) {
+                    fail = 1;
+                    f.end = true;
+                    return -1;
+                }
+                clc_request(cs, r + 1);
+                f.pending = true;
+            }
+            f.unit = unit;
+            f.c = 0;
+        }
+        const int64_t row = f.unit * (ROWS * f.rows) + int64_t(f.c) * ROWS + g;
+        ++f.c;
+        if (row < M) return row;
+    }
+}
+
+// Producer: fill ring slot s with the next row of each of the S inputs (or the
+// end mark). A schedule wait that gave up records the timeout and ends the work.
+template <typename T, int ROWS, int S>
+__device__ __forceinline__ void dyn_issue(const GroupPipe& p, ClcShared& cs, DynFeed& f, int g, int s,
+                                          const T* const* src, int N, int64_t ld, int64_t M, int64_t stall_row,
+                                          unsigned long long wait_ns, unsigned* err) {
+    int fail = 0;
+    const int64_t row = dyn_next_row<ROWS>(f, cs, g, M, wait_ns, fail);
+    if (fail) atomicExch(err, kDeviceErrTimeout);
+    cs.slot_row[g * p.ring.nbuf + s] = row;
+    if (row >= 0) {
+        const uint32_t bytes = uint32_t(N / Elem<T>::kVec) * 16u;  // full rows: the whole row
+        const uint32_t stride = p.ring.row_bytes / S;
+        fence_proxy_async_smem();  // the slot was last read through the generic proxy
+        mbar_expect_tx(p.ring.bar + s, S * bytes + stall_extra(row, stall_row));
+#pragma unroll
+        for (int k = 0; k < S; ++k) tma_copy_row(p.ring.slot(s) + k * stride, src[k] + row * ld, bytes, p.ring.bar + s);
+    } else {
+        mbar_arrive(p.ring.bar + s);
+    }
+}
+
+// CTA start of the dynamic schedule: barriers, the first steal request, and
+// each group's first nbuf rows. A work unit holds `unit_rows` rows of each group.
+template <typename T, int ROWS, int S>
+__device__ __forceinline__ DynFeed dyn_start(char* smem, const GroupPipe& p, ClcShared& cs, int g,
+                                             const T* const* src, int N, int64_t ld, int64_t M, int64_t stall_row,
+                                             unsigned long long wait_ns, unsigned* err, int unit_rows) {
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < ROWS * p.ring.nbuf; ++s) mbar_init(reinterpret_cast<uint64_t*>(smem) + s, 1);
+        clc_init(cs, ROWS);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    DynFeed f{int64_t(blockIdx.x), 0, unit_rows, 0, false, threadIdx.x == 0, false};
+    if (f.requester) {
+        clc_request(cs, 0);
+        f.pending = true;
+    }
+    if (p.producer)
+        for (int s = 0; s < p.ring.nbuf; ++s) dyn_issue<T, ROWS, S>(p, cs, f, g, s, src, N, ld, M, stall_row, wait_ns, err);
+    return f;
+}
+
+// Consumer side, iteration i: wait for the slot and read its row; -1: the
+// work has ended (every thread of the group sees it: an end mark completes its
+// slot's phase when it is written). A wait that gave up sets `fail` and hands
+// back the slot's row as written, so the thread goes on to the group's first
+// reduction, whose barrier tells the whole group to stop.
+__device__ __forceinline__ int64_t dyn_row(const GroupPipe& p, const ClcShared& cs, int g, int64_t i,
+                                           unsigned long long wait_ns, int& fail) {
+    const int nbuf = p.ring.nbuf, s = int(i % nbuf);
+    fail = !mbar_wait(p.ring.bar + s, uint32_t((i / nbuf) & 1), wait_ns);
+    const int64_t row = cs.slot_row[g * nbuf + s];
+    return fail && row < 0 ? 0 : row;
+}
+
+// End of a group's work: the steal requester waits (bounded) for a request it
+// still has in flight, so that no response lands after the CTA is gone.
+__device__ __forceinline__ void dyn_finish(const DynFeed& f, ClcShared& cs, unsigned long long wait_ns) {
+    if (f.requester && f.pending) mbar_wait(&cs.full[f.k & 1], uint32_t((f.k >> 1) & 1), wait_ns);
+}
+
+// Error exit (a wait of iteration i gave up): the producer waits (bounded) for
+// the copies of the slots it filled, then records the timeout.
+__device__ __forceinline__ void dyn_abandon(const GroupPipe& p, const DynFeed& f, ClcShared& cs, int g, int64_t i,
+                                            unsigned* err, unsigned long long wait_ns) {
+    if (!p.producer) return;
+    const int nbuf = p.ring.nbuf;
+    for (int d = 0; d < nbuf; ++d) {
+        const int64_t it = i + d;
+        const int s = int(it % nbuf);
+        if (cs.slot_row[g * nbuf + s] >= 0) mbar_wait(p.ring.bar + s, uint32_t((it / nbuf) & 1), wait_ns);
+    }
+    dyn_finish(f, cs, wait_ns);
+    atomicExch(err, kDeviceErrTimeout);
+}
+
 template <typename T, int TPR, int VPT, int ROWS, bool FULL>
 __global__ void __launch_bounds__(TPR * ROWS)
     softmax_tma_kernel(const T* x, T* y, int64_t M, int N, int64_t ld, int nbuf, unsigned* err,
-                       unsigned long long wait_ns, int64_t stall_row) {
+                       unsigned long long wait_ns, int64_t stall_row, int unit_rows) {
     using E = Elem<T>;
     constexpr int V = E::kVec;
     static_assert(TPR % 64 == 0, "row groups of at least two warps");
     extern __shared__ __align__(128) char smem[];
     __shared__ float red_max[ROWS][TPR / 32];
     __shared__ float red_sum[ROWS][TPR / 32];
+    __shared__ ClcShared cs;
     const GroupPipe p = make_group<TPR, ROWS>(smem, N, E::kBytes, nbuf);
     const int g = threadIdx.x / TPR, t = threadIdx.x % TPR;
-    start_pipes<T, FULL, ROWS>(smem, p, x, M, N, ld, stall_row);
+    const T* const src[1] = {x};
+    const bool dynamic = FULL && unit_rows > 0;  // unit_rows 0: static schedule
+    DynFeed f{};
+    if (dynamic) f = dyn_start<T, ROWS, 1>(smem, p, cs, g, src, N, ld, M, stall_row, wait_ns, err, unit_rows);
+    else start_pipes<T, FULL, ROWS>(smem, p, x, M, N, ld, stall_row);
 
     for (int64_t i = 0;; ++i) {
-        const int64_t row = p.first + i * p.stride;
-        if (row >= M) break;
         const int s = int(i % nbuf);
+        int64_t row;
+        int fail = 0;
+        if (dynamic) {
+            row = dyn_row(p, cs, g, i, wait_ns, fail);
+            if (row < 0) {  // the end of the work (a failed wait goes on to the reduction below)
+                dyn_finish(f, cs, wait_ns);
+                return;
+            }
+        } else {
+            row = p.first + i * p.stride;
+            if (row >= M) break;
+        }
         const T* xr = x + row * ld;
         const RowSpan sp = row_span<T, FULL>(xr, N);
         // unaligned head / tail elements: plain loads, in flight during the wait
         const bool has_ex = !FULL && t < sp.head + sp.tail;
         const int ecol = has_ex ? span_extra_col(sp, t, V) : 0;
         float ex = has_ex ? E::load(xr + ecol) : -INFINITY;
-        int fail = !mbar_wait(p.ring.bar + s, uint32_t((i / nbuf) & 1), wait_ns);
+        if (!dynamic) fail = !mbar_wait(p.ring.bar + s, uint32_t((i / nbuf) & 1), wait_ns);
         const char* sb = p.ring.slot(s);
 
         float v[VPT][V];
@@ -183,10 +382,15 @@ __global__ void __launch_bounds__(TPR * ROWS)
         }
         mx = row_reduce<TPR>(mx, red_max[g], p.bar_id, OpMax(), fail);
         if (fail) {
-            abandon(p, i, M, err, wait_ns);
+            if (dynamic) dyn_abandon(p, f, cs, g, i, err, wait_ns);
+            else abandon(p, i, M, err, wait_ns);
             return;
         }
-        refill<T, FULL>(p, s, row, x, M, N, ld, stall_row);
+        if (dynamic) {
+            if (p.producer) dyn_issue<T, ROWS, 1>(p, cs, f, g, s, src, N, ld, M, stall_row, wait_ns, err);
+        } else {
+            refill<T, FULL>(p, s, row, x, M, N, ld, stall_row);
+        }
         if (mx == -INFINITY) mx = 0.f;
         float sum = 0.f;
 #pragma unroll
@@ -256,13 +460,14 @@ __host__ __device__ constexpr uint32_t affine_stage_bytes() {
 template <typename T, int TPR, int VPT, int ROWS, bool FULL>
 __global__ void __launch_bounds__(TPR * ROWS)
     ln_gelu_tma_kernel(const T* x, T* y, const T* w, const T* b, float eps, int64_t M, int N, int64_t ld,
-                       int nbuf, unsigned* err, unsigned long long wait_ns, int64_t stall_row) {
+                       int nbuf, unsigned* err, unsigned long long wait_ns, int64_t stall_row, int unit_rows) {
     using E = Elem<T>;
     constexpr int V = E::kVec, H = V / 4;
     static_assert(TPR % 64 == 0, "row groups of at least two warps");
     extern __shared__ __align__(128) char smem[];
     __shared__ float red_a[ROWS][TPR / 32];
     __shared__ float red_b[ROWS][2 * TPR / 32];
+    __shared__ ClcShared cs;
     const int period = FULL ? 1 : row_phase_period(ld * E::kBytes);
     const GroupPipe p = make_group<TPR, ROWS>(smem, N, E::kBytes, nbuf, period);
     const int g = threadIdx.x / TPR, t = threadIdx.x % TPR;
@@ -273,7 +478,11 @@ __global__ void __launch_bounds__(TPR * ROWS)
     const float fN = float(N);
     // the split shared by every row of this CTA's phase class
     const RowSpan sp = row_span<T, FULL>(x + int64_t(p.cls) * ld, N);
-    start_pipes<T, FULL, ROWS>(smem, p, x, M, N, ld, stall_row);
+    const T* const src[1] = {x};
+    const bool dynamic = FULL && unit_rows > 0;  // unit_rows 0: static schedule
+    DynFeed f{};
+    if (dynamic) f = dyn_start<T, ROWS, 1>(smem, p, cs, g, src, N, ld, M, stall_row, wait_ns, err, unit_rows);
+    else start_pipes<T, FULL, ROWS>(smem, p, x, M, N, ld, stall_row);
     stage_affine_thread_major<T, TPR, VPT>(w, b, sp.head, sp.body, sw4, sb4);
     if constexpr (!FULL) {
         for (int e = threadIdx.x; e < sp.head + sp.tail; e += blockDim.x) {
@@ -286,12 +495,22 @@ __global__ void __launch_bounds__(TPR * ROWS)
     const int ecol = has_ex ? span_extra_col(sp, t, V) : 0;
 
     for (int64_t i = 0;; ++i) {
-        const int64_t row = p.first + i * p.stride;
-        if (row >= M) break;
         const int s = int(i % nbuf);
+        int64_t row;
+        int fail = 0;
+        if (dynamic) {
+            row = dyn_row(p, cs, g, i, wait_ns, fail);
+            if (row < 0) {  // the end of the work (a failed wait goes on to the reduction below)
+                dyn_finish(f, cs, wait_ns);
+                return;
+            }
+        } else {
+            row = p.first + i * p.stride;
+            if (row >= M) break;
+        }
         const T* xr = x + row * ld;
         float ex = has_ex ? E::load(xr + ecol) : 0.f;
-        int fail = !mbar_wait(p.ring.bar + s, uint32_t((i / nbuf) & 1), wait_ns);
+        if (!dynamic) fail = !mbar_wait(p.ring.bar + s, uint32_t((i / nbuf) & 1), wait_ns);
         const char* sbuf = p.ring.slot(s);
 
         float v[VPT][V];
@@ -310,10 +529,15 @@ __global__ void __launch_bounds__(TPR * ROWS)
         }
         sum = row_reduce<TPR>(sum, red_a[g], p.bar_id, OpSum(), fail);
         if (fail) {
-            abandon(p, i, M, err, wait_ns);
+            if (dynamic) dyn_abandon(p, f, cs, g, i, err, wait_ns);
+            else abandon(p, i, M, err, wait_ns);
             return;
         }
-        refill<T, FULL>(p, s, row, x, M, N, ld, stall_row);
+        if (dynamic) {
+            if (p.producer) dyn_issue<T, ROWS, 1>(p, cs, f, g, s, src, N, ld, M, stall_row, wait_ns, err);
+        } else {
+            refill<T, FULL>(p, s, row, x, M, N, ld, stall_row);
+        }
         const float mean = sum / fN;
         // centred values, their squares and the residual of the fp32 mean
         float q = 0.f, r = 0.f;

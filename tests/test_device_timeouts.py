@@ -34,10 +34,12 @@ def _softmax_wl():
     return workloads.Workload("timeout_softmax", "softmax", "bf16", 2000, 4096, seed=3, x_std=2.0)
 
 
-def test_row_pipeline_wait_times_out_and_context_recovers(oracle, monkeypatch):
+@pytest.mark.parametrize("sched", ["static", "dynamic"])
+def test_row_pipeline_wait_times_out_and_context_recovers(oracle, monkeypatch, sched):
     x = gu.make_x(_softmax_wl())["x"]
     assert rowops_device_status() == 0
     monkeypatch.setenv("ROWOPS_KERNEL", "tma")
+    monkeypatch.setenv("ROWOPS_SCHED", sched)
     monkeypatch.setenv("ROWOPS_WAIT_LIMIT_NS", LIMIT_NS)
     monkeypatch.setenv("ROWOPS_TEST_STALL_ROW", "777")
     rowops_softmax(x)
@@ -50,10 +52,12 @@ def test_row_pipeline_wait_times_out_and_context_recovers(oracle, monkeypatch):
     C.assert_softmax_close(C.to_f64(y), oracle.softmax(gu.rows_f32(x)), "bf16")
 
 
-def test_layernorm_row_groups_wait_times_out(oracle, monkeypatch):
+@pytest.mark.parametrize("sched", ["static", "dynamic"])
+def test_layernorm_row_groups_wait_times_out(oracle, monkeypatch, sched):
     wl = workloads.Workload("timeout_ln", "layernorm_gelu", "bf16", 1500, 8192, seed=4, affine=True)
     inp = gu.make_x(wl)
     monkeypatch.setenv("ROWOPS_KERNEL", "tma")
+    monkeypatch.setenv("ROWOPS_SCHED", sched)
     monkeypatch.setenv("ROWOPS_WAIT_LIMIT_NS", LIMIT_NS)
     monkeypatch.setenv("ROWOPS_TEST_STALL_ROW", "3")
     rowops_layernorm_gelu(inp["x"], inp["w"], inp["b"], wl.eps)
@@ -85,15 +89,19 @@ def test_single_read_split_softmax_wait_times_out(oracle, monkeypatch, staging):
     C.assert_softmax_close(C.to_f64(y), oracle.softmax(gu.rows_f32(x)), "f32")
 
 
-def test_rmsnorm_pipeline_wait_times_out(oracle, monkeypatch):
+@pytest.mark.parametrize("sched", ["static", "dynamic"])
+def test_rmsnorm_pipeline_wait_times_out(oracle, monkeypatch, sched):
     """The fused residual RMSNorm ring (two input rows per slot on one
-    mbarrier): the stalled row's wait gives up, the next call is correct."""
+    mbarrier): the stalled row's wait gives up, the next call is correct.
+    On the dynamic schedule the stalled group also drains a steal request it
+    may have in flight."""
     from row_wise_reduction_gb300 import rowops_fused_residual_rmsnorm
 
     wl = workloads.Workload("timeout_rms", "residual_rmsnorm", "bf16", 1500, 8192, seed=6, affine=True,
                             residual=True)
     inp = gu.make_x(wl)
     monkeypatch.setenv("ROWOPS_KERNEL", "tma")
+    monkeypatch.setenv("ROWOPS_SCHED", sched)
     monkeypatch.setenv("ROWOPS_WAIT_LIMIT_NS", LIMIT_NS)
     monkeypatch.setenv("ROWOPS_TEST_STALL_ROW", "11")
     rowops_fused_residual_rmsnorm(inp["x"], inp["residual"], inp["w"], wl.eps)

@@ -208,7 +208,10 @@ FAMILIES = [{"ROWOPS_KERNEL": "reg"}, {"ROWOPS_KERNEL": "looped"}, {"ROWOPS_KERN
             {"ROWOPS_KERNEL": "tma", "ROWOPS_RING_BUFFERS": "3"},
             {"ROWOPS_KERNEL": "tma", "ROWOPS_FORCE_TPR": "128", "ROWOPS_FORCE_VPT": "8"},
             {"ROWOPS_KERNEL": "tma", "ROWOPS_FORCE_TPR": "512", "ROWOPS_FORCE_VPT": "2"},
-            {"ROWOPS_KERNEL": "tma", "ROWOPS_FORCE_TPR": "64", "ROWOPS_FORCE_VPT": "1"}]
+            {"ROWOPS_KERNEL": "tma", "ROWOPS_FORCE_TPR": "64", "ROWOPS_FORCE_VPT": "1"},
+            {"ROWOPS_KERNEL": "tma", "ROWOPS_SCHED": "static"},
+            {"ROWOPS_KERNEL": "tma", "ROWOPS_SCHED": "dynamic", "ROWOPS_UNIT_ROWS": "3"},
+            {"ROWOPS_KERNEL": "tma", "ROWOPS_SCHED": "dynamic", "ROWOPS_ROWS_PER_CTA": "8", "ROWOPS_RING_BUFFERS": "2"}]
 
 
 @pytest.mark.parametrize("env", FAMILIES, ids=lambda e: ",".join(f"{k[7:]}={v}" for k, v in e.items()))
