@@ -63,6 +63,10 @@ def lib() -> ctypes.CDLL:
                                          _c_double_p]
             getattr(L, name).restype = ctypes.c_int
         L.oracle_rmsnorm_row.argtypes = [_c_double_p, _c_double_p, ctypes.c_double, _i64, _c_double_p]
+        L.oracle_causal_kept.argtypes = [_i64, _i64, _i64, _i64]
+        L.oracle_causal_kept.restype = _i64
+        L.oracle_softmax_causal_rows_f32.argtypes = [_c_float_p, _i64, _i64, _i64, _i64, _i64, _c_double_p]
+        L.oracle_softmax_causal_rows_f32.restype = ctypes.c_int
         L.oracle_round_to.argtypes = [ctypes.c_double, ctypes.c_int]
         L.oracle_round_to.restype = ctypes.c_double
         L.oracle_residual_rmsnorm_row.argtypes = [_c_double_p, _c_double_p, _c_double_p, ctypes.c_double, _i64,
@@ -270,3 +274,34 @@ def residual_rmsnorm(x, r, w=None, eps: float = 1e-5, storage: str = "exact") ->
                                               M, N, ld, _dp(s_out), _dp(y)) != 0:
         raise ValueError("oracle_residual_rmsnorm_rows_f32 rejected its arguments")
     return s_out, y
+
+
+def causal_kept(r: int, n: int, period: int, offset: int = 0) -> int:
+    """Columns of row r kept by the causal mask (c <= r mod period + offset)."""
+    return int(lib().oracle_causal_kept(int(r), int(n), int(period), int(offset)))
+
+
+def softmax_causal(x, period: int, offset: int = 0, row0: int = 0) -> np.ndarray:
+    """Causal softmax of every row -> float64 (M, N). ``row0``: index of the
+    first given row in the full matrix (for sampled rows, contiguous from row0)."""
+    xs, M, N, ld = _rows(x)
+    y = np.empty((M, N), dtype=np.float64)
+    if row0:
+        # the mask depends on the row index: evaluate row by row at its own index
+        for i in range(M):
+            y[i] = softmax_causal_rows_at(xs[i], row0 + i, period, offset)
+        return y
+    if lib().oracle_softmax_causal_rows_f32(_fp(xs), M, N, ld, int(period), int(offset), _dp(y)) != 0:
+        raise ValueError("oracle_softmax_causal_rows_f32 rejected its arguments")
+    return y
+
+
+def softmax_causal_rows_at(row, r: int, period: int, offset: int = 0) -> np.ndarray:
+    """Causal softmax of one row standing at index r of the matrix: the row
+    softmax of its kept prefix, 0 after it."""
+    xr = _f64_row(row)
+    kept = causal_kept(r, xr.size, period, offset)
+    y = np.zeros_like(xr)
+    if kept > 0:
+        y[:kept] = softmax_row(xr[:kept])
+    return y

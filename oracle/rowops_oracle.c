@@ -177,6 +177,18 @@ void oracle_layernorm_gelu_row(const double* x, const double* w, const double* b
 }
 
 /* ---------------------------------------------------------------------------
+ * Causal mask [EX §5.1 Naive Attention: mask = n <= m, query m sees keys n <= m].
+ * Rows stack query blocks of `period` rows (row r is query r mod period);
+ * `offset` shifts the diagonal (0: the square causal mask).
+ * ------------------------------------------------------------------------- */
+int64_t oracle_causal_kept(int64_t r, int64_t n, int64_t period, int64_t offset) {
+    int64_t kept = r % period + offset + 1;
+    if (kept < 0) kept = 0;
+    if (kept > n) kept = n;
+    return kept;
+}
+
+/* ---------------------------------------------------------------------------
  * RMSNorm [EX §4.2]:
  *   inv_rms = 1 / sqrt(mean(x^2) + eps)        (no mean subtracted)
  *   y       = x * inv_rms * w
@@ -340,4 +352,20 @@ int oracle_residual_rmsnorm_rows_f32(const float* x, const float* r, const float
     free(rr);
     free(wd);
     return rc;
+}
+
+int oracle_softmax_causal_rows_f32(const float* x, int64_t M, int64_t N, int64_t ld, int64_t period,
+                                   int64_t offset, double* y) {
+    if (bad_shape(x, M, N, ld, y) || period < 1) return -1;
+    double* row = (double*)malloc(sizeof(double) * (size_t)N);
+    if (!row) return -1;
+    for (int64_t r = 0; r < M; ++r) {
+        const int64_t kept = oracle_causal_kept(r, N, period, offset);
+        double* yr = y + r * N;
+        for (int64_t j = 0; j < kept; ++j) row[j] = (double)x[r * ld + j];
+        if (kept > 0) oracle_softmax_row(row, kept, yr);
+        for (int64_t j = kept; j < N; ++j) yr[j] = 0.0;
+    }
+    free(row);
+    return 0;
 }

@@ -59,6 +59,12 @@ double oracle_gelu_tanh(double z);
 void oracle_layernorm_gelu_row(const double* x, const double* w, const double* b, double eps,
                                int64_t n, double* y);
 
+/* Columns of row r that a causal mask keeps [EX §5.1: key n is visible to query
+ * m when n <= m], for rows that stack query blocks of `period` rows: column c
+ * is kept when c <= (r mod period) + offset, so the count is that plus one,
+ * clamped to [0, n]. */
+int64_t oracle_causal_kept(int64_t r, int64_t n, int64_t period, int64_t offset);
+
 /* RMSNorm [EX §4.2]: inv_rms = 1 / sqrt(mean_j x_j^2 + eps), y_j = x_j * inv_rms * w_j.
  * w may be NULL (weight 1). */
 void oracle_rmsnorm_row(const double* x, const double* w, double eps, int64_t n, double* y);
@@ -88,6 +94,10 @@ int oracle_layernorm_rows_f32(const float* x, const float* w, const float* b, do
                               int64_t N, int64_t ld, double* y);
 int oracle_rmsnorm_rows_f32(const float* x, const float* w, double eps, int64_t M, int64_t N, int64_t ld,
                             double* y);
+/* Causal softmax: the stable softmax of each row's kept prefix (masked
+ * entries are not read), 0 on the masked columns. */
+int oracle_softmax_causal_rows_f32(const float* x, int64_t M, int64_t N, int64_t ld, int64_t period,
+                                   int64_t offset, double* y);
 /* x and r share the row stride; s_out may be NULL. */
 int oracle_residual_rmsnorm_rows_f32(const float* x, const float* r, const float* w, double eps, int storage,
                                      int64_t M, int64_t N, int64_t ld, double* s_out, double* y);

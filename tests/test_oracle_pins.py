@@ -480,6 +480,63 @@ def test_rmsnorm_rows_batch_respects_ld_and_null_weight(oracle):
         np.testing.assert_array_equal(yr[i], yi)
 
 
+# ----------------------------------------------------------------------------
+# causal softmax
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("case", _golden.read_cases("softmax_causal_closed_forms.txt"), ids=lambda c: c[0])
+def test_softmax_causal_golden_closed_forms(oracle, case):
+    """Worked examples: catches a kept count off by one, a mask that ignores
+    the period or the offset, and masked entries that are read."""
+    _, params, rows = case
+    r, period, offset = int(params["r"]), int(params["period"]), int(params["offset"])
+    x = [float(v) for v in rows["x"]]
+    want = [float(v) for v in rows["y"]]
+    got = oracle.softmax_causal_rows_at(x, r, period, offset)
+    np.testing.assert_allclose(got, want, rtol=0, atol=2e-16)
+    # the batch form at the same row index
+    M = r + 1
+    xb = np.zeros((M, len(x)), np.float32)
+    xb[r] = np.float32(x)
+    np.testing.assert_allclose(oracle.softmax_causal(xb, period, offset)[r], want, rtol=0, atol=1e-7)
+
+
+def test_causal_kept_count(oracle):
+    """kept = clamp(r mod period + offset + 1, 0, n), against a count of the
+    columns c with c <= r mod period + offset."""
+    for n in (1, 5, 64):
+        for period in (1, 3, 64, 100):
+            for offset in (-70, -3, -1, 0, 2, 63, 1000):
+                for r in (0, 1, 2, 63, 64, 99, 12345):
+                    want = sum(1 for c in range(n) if c <= r % period + offset)
+                    assert oracle.causal_kept(r, n, period, offset) == want
+
+
+def test_softmax_causal_matches_torch_on_masked_input(oracle):
+    """Equals torch's softmax of the row with the masked columns set to -inf
+    (zeros where torch's all -inf row gives NaN), whatever the masked columns
+    hold: here NaN and +inf, which any read would propagate."""
+    rng = _rng(53)
+    M, N, period, offset = 37, 40, 16, 3
+    x = rng.normal(0, 3, size=(M, N)).astype(np.float32)
+    xm = x.copy()
+    for r in range(M):
+        keep = r % period + offset
+        xm[r, keep + 1:] = -np.inf
+        x[r, keep + 1:] = np.nan if r % 2 else np.inf
+    want = torch.softmax(torch.from_numpy(xm).double(), dim=1).numpy()
+    got = oracle.softmax_causal(x, period, offset)
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-15)
+
+
+def test_softmax_causal_degenerate_masks(oracle):
+    rng = _rng(59)
+    x = rng.normal(0, 1, size=(9, 33)).astype(np.float32)
+    # a mask that keeps everything is the plain softmax; one that keeps nothing is all zeros
+    np.testing.assert_allclose(oracle.softmax_causal(x, 1, 33), torch.softmax(torch.from_numpy(x).double(), 1).numpy(),
+                               rtol=0, atol=1e-15)
+    assert np.all(oracle.softmax_causal(x, 4, -5) == 0.0)
+
+
 def test_batch_rejects_bad_shapes(oracle):
     with pytest.raises(ValueError):
         oracle.layernorm_gelu(np.zeros((2, 3), np.float32), np.ones(4, np.float32))
