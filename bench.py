@@ -43,7 +43,8 @@ from row_wise_reduction_gb300 import workloads  # noqa: E402
 METRIC = "row-kernel HBM GB/s (% of GB300 peak) for softmax and LayerNorm+GELU"
 STEP = ["softmax_bf16_causal_32768x4096", "online_softmax_f32_64x1048576", "layernorm_gelu_bf16_65536x8192"]
 DOMINANT = "layernorm_gelu_bf16_65536x8192"
-KERNELS_PER_CALL = {"softmax": 1, "online_softmax": 2, "layernorm_gelu": 1, "rmsnorm": 1, "residual_rmsnorm": 1}
+KERNELS_PER_CALL = {"softmax": 1, "softmax_causal": 1, "online_softmax": 2, "layernorm_gelu": 1, "rmsnorm": 1,
+                    "residual_rmsnorm": 1}
 L2_BYTES = 129 * 10**6
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "ln_gelu_bf16_65536x8192.txt")
@@ -66,6 +67,8 @@ def alg_bytes(wl: workloads.Workload) -> int:
         return rows + (wl.N * es if wl.affine else 0)
     if wl.op == "residual_rmsnorm":  # x, residual in; y, residual_out out
         return 2 * rows + (wl.N * es if wl.affine else 0)
+    if wl.op == "softmax_causal":  # kept entries read, every output written
+        return causal_alg_bytes(wl, wl.N)
     return rows
 
 
@@ -383,9 +386,19 @@ def config_block():
 # ---------------------------------------------------------------------------
 # the other workloads, reported beside the step (not part of its value)
 # ---------------------------------------------------------------------------
+def causal_alg_bytes(wl: workloads.Workload, period: int, offset: int = 0) -> int:
+    """Kept entries read once, every output element written once."""
+    import numpy as np
+
+    r = np.arange(wl.M)
+    kept = np.clip(r % period + offset + 1, 0, wl.N)
+    es = workloads.elem_size(wl.dtype)
+    return int(kept.sum()) * es + wl.M * wl.N * es
+
+
 EXTRA = ["softmax_f32_1024x768", "layernorm_gelu_f32_4096x768", "layernorm_gelu_bf16_65536x127",
          "layernorm_gelu_bf16_65536x4097", "rmsnorm_f32_4096x768", "residual_rmsnorm_f32_4096x768",
-         "rmsnorm_bf16_65536x8192", "residual_rmsnorm_bf16_65536x8192"]
+         "rmsnorm_bf16_65536x8192", "residual_rmsnorm_bf16_65536x8192", "softmax_causal_bf16_32768x4096"]
 SMALL = {"softmax_f32_1024x768", "layernorm_gelu_f32_4096x768", "rmsnorm_f32_4096x768",
          "residual_rmsnorm_f32_4096x768"}
 
@@ -407,6 +420,8 @@ def run_extras(dev, stream, iters=50):
         def call():
             if wl.op == "softmax":
                 ro.rowops_softmax(x, y)
+            elif wl.op == "softmax_causal":
+                ro.rowops_softmax_causal(x, wl.N, 0, y)
             elif wl.op == "rmsnorm":
                 ro.rowops_rmsnorm(x, inp.get("w"), wl.eps, y)
             elif wl.op == "residual_rmsnorm":
@@ -574,6 +589,8 @@ def run_rowops(args):
         wl = wls[n]
         if wl.op == "softmax":
             ro.rowops_softmax(x, y)
+        elif wl.op == "softmax_causal":
+            ro.rowops_softmax_causal(x, wl.N, 0, y)
         elif wl.op == "online_softmax":
             ro.rowops_online_softmax(x, y, workspace=ws[n])
         elif wl.op == "rmsnorm":

@@ -48,10 +48,9 @@
  *   ROWOPS_PERSIST_LOOKAHEAD=<2k> / ROWOPS_PERSIST_PREFETCH=<n>  its pipeline depths
  *   ROWOPS_CTAS_PER_SM=<k>        persistent grid of k CTAs per SM (0 = occupancy limit,
  *                                 -1 = one CTA per row group, no persistence)
- *   ROWOPS_SCHED=static|dynamic   row schedule of the row pipeline on full rows: static (each
- *                                 row group a fixed share) or dynamic (work units taken with
- *                                 cluster launch control); default dynamic for the RMSNorm
- *                                 entry points, static otherwise
+ *   ROWOPS_SCHED=static|dynamic   row schedule of the RMSNorm row pipeline on full rows: static
+ *                                 (each row group a fixed share) or dynamic (default: work units
+ *                                 taken with cluster launch control)
  *   ROWOPS_UNIT_ROWS=<n>          dynamic schedule: rows per row group in one work unit (default 1)
  *   ROWOPS_WAIT_LIMIT_NS=<ns>     limit of every device-side wait (default 2 s)
  *   ROWOPS_TEST_STALL_ROW=<row>   test hook for the timeout path: the wait that concerns this
@@ -109,6 +108,29 @@ const char* rowops_status_string(rowops_status_t status);
  */
 rowops_status_t rowops_softmax(const void* x, void* y, int64_t M, int64_t N, int64_t ld,
                                rowops_dtype_t dtype, cudaStream_t stream);
+
+/*
+ * Causal softmax [EX §5.1 Naive Attention, causal mask n <= m; EX §2.4 Softmax]:
+ * rows stack query blocks of `period` rows; row r is query r mod period and
+ * keeps the columns c <= (r mod period) + offset:
+ *   kept = clamp((r mod period) + offset + 1, 0, N)
+ *   y[r, j] = exp(x[r, j] - m) / sum_{k < kept} exp(x[r, k] - m)   for j < kept
+ *   y[r, j] = 0                                                    for j >= kept
+ * with m the maximum over the kept columns. The masked columns of x are never
+ * read (they may hold anything, NaN included); a row that keeps nothing is all
+ * zeros. Within the kept columns the conventions of rowops_softmax hold (-inf
+ * entries give 0, a NaN makes the row NaN). rowops_softmax on x with -inf in
+ * the masked columns gives the same y while reading every column.
+ *
+ *   x, y, M, N, ld, dtype, stream   as for rowops_softmax.
+ *   period   >= 1 (period == N with offset 0: stacked square causal masks).
+ *   offset   shifts the diagonal; |offset| <= 2^62.
+ * Full rows (16-byte aligned, N a multiple of the 16-byte vector and of a
+ * row-pipeline tile) copy only the 16-byte vectors holding kept columns into
+ * the row ring; other layouts take a looped kernel.
+ */
+rowops_status_t rowops_softmax_causal(const void* x, void* y, int64_t M, int64_t N, int64_t ld, int64_t period,
+                                      int64_t offset, rowops_dtype_t dtype, cudaStream_t stream);
 
 /*
  * Synchronises `stream`, then reads and clears the library's device error word

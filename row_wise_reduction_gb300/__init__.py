@@ -1,6 +1,6 @@
 """rowops: row-wise reduce-then-normalise CUDA kernels for GB300 (sm_103a).
 
-Stable softmax, split-row online softmax, fused LayerNorm -> affine ->
+Stable and causal softmax, split-row online softmax, fused LayerNorm -> affine ->
 tanh-GELU, RMSNorm and fused residual + RMSNorm, exposed through the C ABI of
 ``librowops.so`` (``include/rowops.h``) and the thin ctypes binding in
 :mod:`row_wise_reduction_gb300.rowops`.
@@ -19,5 +19,6 @@ from .rowops import (  # noqa: F401
     rowops_online_softmax_workspace_bytes,
     rowops_rmsnorm,
     rowops_softmax,
+    rowops_softmax_causal,
     rowops_status_string,
 )

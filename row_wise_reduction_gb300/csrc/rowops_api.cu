@@ -161,7 +161,7 @@ rowops_status_t make_cfg(cudaStream_t stream, const Tuning& tn, LaunchCfg* cfg) 
     cfg->persist_prefetch = tn.prefetch;
     cfg->wait_ns = tn.wait_ns > 0 ? (unsigned long long)tn.wait_ns : 2000000000ull;
     cfg->stall_row = tn.stall_row;
-    // full-row pipelines: static schedule unless asked for (RMSNorm chooses its own, rms_dispatch)
+    // RMSNorm row pipeline on full rows (the other pipelines have a static schedule only)
     cfg->unit_rows = tn.sched == 2 ? (tn.unit_rows > 0 ? tn.unit_rows : 1) : 0;
     return ROWOPS_OK;
 }
@@ -348,9 +348,9 @@ rowops_status_t rms_dispatch(const void* x, const void* r, void* y, void* ro, co
     LaunchCfg cfg;
     rowops_status_t st = make_cfg(stream, tn, &cfg);
     if (st != ROWOPS_OK) return st;
-    // Full rows take the dynamic schedule by default here: at bf16 65536 x 8192 it
-    // is 10% faster than the static one for both forms (311 vs 347 us, 614 vs
-    // 677 us on GB300), where softmax and LayerNorm+GELU run 5-10% slower with it.
+    // Full rows take the dynamic schedule by default: at bf16 65536 x 8192 it is
+    // 10% faster than the static one for both forms (311 vs 347 us, 614 vs 677
+    // us on GB300). (Softmax and LayerNorm+GELU ran 5-10% slower with it.)
     if (tn.sched == 0) cfg.unit_rows = tn.unit_rows > 0 ? tn.unit_rows : 1;
     const int es = elem_bytes(dtype);
     // every row pointer at the same offset modulo 16 bytes
@@ -477,6 +477,31 @@ rowops_status_t rowops_softmax(const void* x, void* y, int64_t M, int64_t N, int
         fn = dtype == ROWOPS_F32 ? softmax_reg_f32(tpr_index, vpt) : softmax_reg_bf16(tpr_index, vpt);
     if (!fn) fn = dtype == ROWOPS_F32 ? softmax_looped_f32() : softmax_looped_bf16();
     return finish(fn(x, y, M, N, ld, cfg));
+}
+
+rowops_status_t rowops_softmax_causal(const void* x, void* y, int64_t M, int64_t N, int64_t ld, int64_t period,
+                                      int64_t offset, rowops_dtype_t dtype, cudaStream_t stream) {
+    rowops_status_t st = check_rows(x, y, M, N, ld, dtype);
+    if (st != ROWOPS_OK) return st;
+    const int64_t lim = int64_t(1) << 62;  // keeps (r mod period) + offset + 1 in range
+    if (period < 1 || offset > lim || offset < -lim) return ROWOPS_ERR_INVALID_VALUE;
+    if (M == 0) return ROWOPS_OK;
+    const Tuning tn = read_tuning();
+    LaunchCfg cfg;
+    if ((st = make_cfg(stream, tn, &cfg)) != ROWOPS_OK) return st;
+    const int es = elem_bytes(dtype);
+    TmaChoice tc;
+    // 4 vectors per thread first: on the causal bf16 32768 x 4096 input 128 x 4 ran
+    // 88 us against 104 us for 64 x 8 (the best tile of the plain softmax)
+    if ((tn.family == Family::Auto || tn.family == Family::Tma) &&
+        choose_tma(x, y, N, ld, es, tn, {4, 8, 2, 3, 1}, &tc) && tc.full) {
+        const int nbuf = ring_buffers(N, es, 0, tn, cfg);
+        TmaSoftmaxCausalLaunch tf = dtype == ROWOPS_F32 ? softmax_tma_causal_f32(tc.block_index, tc.vpt_index)
+                                                        : softmax_tma_causal_bf16(tc.block_index, tc.vpt_index);
+        if (nbuf > 0 && tf) return finish(tf(x, y, M, N, ld, nbuf, period, offset, cfg));
+    }
+    const SoftmaxCausalLaunch fn = dtype == ROWOPS_F32 ? softmax_causal_looped_f32() : softmax_causal_looped_bf16();
+    return finish(fn(x, y, M, N, ld, period, offset, cfg));
 }
 
 rowops_status_t rowops_layernorm_gelu(const void* x, void* y, const void* w, const void* b,

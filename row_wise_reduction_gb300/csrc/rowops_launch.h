@@ -76,6 +76,15 @@ using TmaLnGeluLaunch = cudaError_t (*)(const void* x, void* y, const void* w, c
                                         int64_t M, int64_t N, int64_t ld, int nbuf, const LaunchCfg& cfg);
 TmaSoftmaxLaunch softmax_tma_f32(int block_index, int vpt_index, bool full);
 TmaSoftmaxLaunch softmax_tma_bf16(int block_index, int vpt_index, bool full);
+// causal softmax on full rows (row r keeps the columns c <= (r mod period) + offset)
+using TmaSoftmaxCausalLaunch = cudaError_t (*)(const void* x, void* y, int64_t M, int64_t N, int64_t ld, int nbuf,
+                                               int64_t period, int64_t offset, const LaunchCfg& cfg);
+TmaSoftmaxCausalLaunch softmax_tma_causal_f32(int block_index, int vpt_index);
+TmaSoftmaxCausalLaunch softmax_tma_causal_bf16(int block_index, int vpt_index);
+using SoftmaxCausalLaunch = cudaError_t (*)(const void* x, void* y, int64_t M, int64_t N, int64_t ld,
+                                            int64_t period, int64_t offset, const LaunchCfg& cfg);
+SoftmaxCausalLaunch softmax_causal_looped_f32();
+SoftmaxCausalLaunch softmax_causal_looped_bf16();
 
 // LayerNorm+GELU instantiations: ROWS = 1 with TPR in kTmaBlocks and VPT in
 // kTmaVpts, or several row groups per CTA sharing one staging of w, b with TPR

@@ -39,6 +39,16 @@ cudaError_t launch_softmax_looped(const void* x, void* y, int64_t M, int64_t N, 
     return cudaGetLastError();
 }
 
+template <typename T>
+cudaError_t launch_softmax_causal_looped(const void* x, void* y, int64_t M, int64_t N, int64_t ld, int64_t period,
+                                         int64_t offset, const LaunchCfg& cfg) {
+    auto kern = softmax_causal_looped_kernel<T, kLoopedBlock>;
+    const int grid = grid_for(reinterpret_cast<const void*>(kern), kLoopedBlock, 0, M, cfg);
+    kern<<<grid, kLoopedBlock, 0, cfg.stream>>>(static_cast<const T*>(x), static_cast<T*>(y), M, N, ld, period,
+                                                offset);
+    return cudaGetLastError();
+}
+
 #define ROWOPS_SOFTMAX_ROW(T, TPR)                                                             \
     {                                                                                          \
         launch_softmax_reg<T, TPR, 1>, launch_softmax_reg<T, TPR, 2>,                          \

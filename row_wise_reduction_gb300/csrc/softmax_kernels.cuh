@@ -191,4 +191,33 @@ __global__ void __launch_bounds__(BLOCK)
     }
 }
 
+// Causal softmax, any layout ["Triton Kernel 实现练习" §5.1 causal mask, §2.4
+// softmax]: one CTA per row; row r keeps its first kept = clamp((r mod period)
+// + offset + 1, 0, N) columns. Pass 1 folds the kept entries into a per-thread
+// online (m, d) state (element-wise, coalesced), merged across the CTA; pass 2
+// re-reads them and writes y, and writes 0 on the masked columns without
+// reading them.
+template <typename T, int BLOCK>
+__global__ void __launch_bounds__(BLOCK)
+    softmax_causal_looped_kernel(const T* x, T* y, int64_t M, int64_t N, int64_t ld, int64_t period,
+                                 int64_t offset) {
+    using E = Elem<T>;
+    __shared__ float red_m[2][BLOCK / 32];
+    __shared__ float red_d[2][BLOCK / 32];
+    int parity = 0;
+    for (int64_t row = blockIdx.x; row < M; row += gridDim.x, parity ^= 1) {
+        int64_t kept = row % period + offset + 1;
+        kept = kept < 0 ? 0 : (kept > N ? N : kept);
+        const T* xr = x + row * ld;
+        T* yr = y + row * ld;
+        MD s{-INFINITY, 0.f};
+        for (int64_t c = threadIdx.x; c < kept; c += BLOCK) s = md_push(s, E::load(xr + c));
+        s = group_merge<BLOCK>(s, red_m[parity], red_d[parity]);
+        const float m = s.d > 0.f ? s.m : 0.f;
+        const float inv = safe_inverse(s.d);
+        for (int64_t c = threadIdx.x; c < N; c += BLOCK)
+            E::store(yr + c, c < kept ? exp_shifted(E::load(xr + c), m) * inv : 0.f);
+    }
+}
+
 }  // namespace rowops

@@ -12,18 +12,30 @@ inline size_t tma_ring_bytes(int64_t N, int nbuf) {
     return kRingHeader + size_t(nbuf) * ring_row_bytes(N, Elem<T>::kBytes);
 }
 
-template <typename T, int TPR, int VPT, bool FULL>
-cudaError_t launch_softmax_tma(const void* x, void* y, int64_t M, int64_t N, int64_t ld, int nbuf,
-                               const LaunchCfg& cfg) {
-    auto kern = softmax_tma_kernel<T, TPR, VPT, 1, FULL>;
+template <typename T, int TPR, int VPT, bool FULL, bool CAUSAL = false>
+cudaError_t launch_softmax_tma_mask(const void* x, void* y, int64_t M, int64_t N, int64_t ld, int nbuf,
+                                    CausalMask cm, const LaunchCfg& cfg) {
+    auto kern = softmax_tma_kernel<T, TPR, VPT, 1, FULL, CAUSAL>;
     const size_t smem = tma_ring_bytes<T>(N, nbuf);
     cudaError_t e = allow_smem(reinterpret_cast<const void*>(kern), smem, cfg);
     if (e != cudaSuccess) return e;
-    const int unit = FULL ? cfg.unit_rows : 0;  // 0: static schedule
-    const int grid = unit ? dyn_grid(M, 1, unit) : grid_for(reinterpret_cast<const void*>(kern), TPR, smem, M, cfg);
+    const int grid = grid_for(reinterpret_cast<const void*>(kern), TPR, smem, M, cfg);
     kern<<<grid, TPR, smem, cfg.stream>>>(static_cast<const T*>(x), static_cast<T*>(y), M, int(N), ld, nbuf,
-                                          cfg.dev_error, cfg.wait_ns, cfg.stall_row, unit);
+                                          cfg.dev_error, cfg.wait_ns, cfg.stall_row, cm);
     return cudaGetLastError();
+}
+
+template <typename T, int TPR, int VPT, bool FULL>
+cudaError_t launch_softmax_tma(const void* x, void* y, int64_t M, int64_t N, int64_t ld, int nbuf,
+                               const LaunchCfg& cfg) {
+    return launch_softmax_tma_mask<T, TPR, VPT, FULL, false>(x, y, M, N, ld, nbuf, CausalMask{1, 0}, cfg);
+}
+
+// the causal softmax on full rows: row r keeps the columns c <= (r mod period) + offset
+template <typename T, int TPR, int VPT, bool FULL>
+cudaError_t launch_softmax_tma_causal(const void* x, void* y, int64_t M, int64_t N, int64_t ld, int nbuf,
+                                      int64_t period, int64_t offset, const LaunchCfg& cfg) {
+    return launch_softmax_tma_mask<T, TPR, VPT, true, true>(x, y, M, N, ld, nbuf, CausalMask{period, offset}, cfg);
 }
 
 // ROWS row groups per CTA share one staging of w, b; nbuf buffers per group.
@@ -40,16 +52,14 @@ cudaError_t launch_ln_gelu_tma_rows(const void* x, void* y, const void* w, const
     const size_t smem = ln_gelu_tma_smem<T, TPR, VPT, ROWS, FULL>(N, nbuf);
     cudaError_t e = allow_smem(reinterpret_cast<const void*>(kern), smem, cfg);
     if (e != cudaSuccess) return e;
-    const int unit = FULL ? cfg.unit_rows : 0;  // 0: static schedule
-    int grid = unit ? dyn_grid(M, ROWS, unit)
-                    : grid_for(reinterpret_cast<const void*>(kern), TPR * ROWS, smem, (M + ROWS - 1) / ROWS, cfg);
+    int grid = grid_for(reinterpret_cast<const void*>(kern), TPR * ROWS, smem, (M + ROWS - 1) / ROWS, cfg);
     if (!FULL) {  // whole phase classes: every class needs a CTA, and they share the grid evenly
         const int period = row_phase_period(ld * int64_t(Elem<T>::kBytes));
         grid = grid >= period ? grid - grid % period : period;
     }
     kern<<<grid, TPR * ROWS, smem, cfg.stream>>>(static_cast<const T*>(x), static_cast<T*>(y),
                                                  static_cast<const T*>(w), static_cast<const T*>(b), eps, M, int(N),
-                                                 ld, nbuf, cfg.dev_error, cfg.wait_ns, cfg.stall_row, unit);
+                                                 ld, nbuf, cfg.dev_error, cfg.wait_ns, cfg.stall_row);
     return cudaGetLastError();
 }
 
@@ -70,6 +80,14 @@ int ctas_ln_gelu_tma_rows(int64_t N, int nbuf, const LaunchCfg& cfg) {
 #define ROWOPS_TMA_TABLE(FN, T, F)                                                                         \
     {ROWOPS_TMA_ROW(FN, T, 64, F), ROWOPS_TMA_ROW(FN, T, 128, F), ROWOPS_TMA_ROW(FN, T, 256, F),           \
      ROWOPS_TMA_ROW(FN, T, 512, F)}
+
+template <typename T>
+TmaSoftmaxCausalLaunch softmax_tma_causal_table(int block_index, int vpt_index) {
+    static const TmaSoftmaxCausalLaunch t[kNumTmaBlocks][kNumTmaVpts] =
+        ROWOPS_TMA_TABLE(launch_softmax_tma_causal, T, true);
+    if (block_index < 0 || block_index >= kNumTmaBlocks || vpt_index < 0 || vpt_index >= kNumTmaVpts) return nullptr;
+    return t[block_index][vpt_index];
+}
 
 template <typename T>
 TmaSoftmaxLaunch softmax_tma_table(int block_index, int vpt_index, bool full) {

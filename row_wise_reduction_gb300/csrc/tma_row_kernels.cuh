@@ -83,9 +83,39 @@ __device__ __forceinline__ RowSpan row_span(const T* row, int N) {
     }
 }
 
+// Causal mask of the causal softmax ["Triton Kernel 实现练习" §5.1: query m
+// sees keys n <= m]: row r is query r mod period and keeps the columns
+// c <= (r mod period) + offset; the masked columns are never read.
+struct CausalMask {
+    int64_t period, offset;
+    // columns kept by a row whose index mod period is rm
+    __device__ __forceinline__ int kept_at(int64_t rm, int N) const {
+        const int64_t k = rm + offset + 1;
+        return int(k < 0 ? 0 : (k > N ? int64_t(N) : k));
+    }
+    // (rm + step) mod period for rm, step in [0, period): no division per row
+    __device__ __forceinline__ int64_t advance(int64_t rm, int64_t step) const {
+        rm += step;
+        return rm >= period ? rm - period : rm;
+    }
+};
+
 // Test hook: the copy of row `stall_row` is expected to bring 16 bytes more than
 // it does, so the wait on it runs out (-1: no such row).
 __device__ __forceinline__ uint32_t stall_extra(int64_t row, int64_t stall_row) { return row == stall_row ? 16u : 0u; }
+
+// Causal rows (full rows): copy the 16-byte vectors that hold the kept
+// prefix; a row that keeps nothing completes its phase with a plain arrival
+// (the test hook instead expects bytes that never come).
+template <typename T>
+__device__ __forceinline__ void issue_prefix(const GroupPipe& p, int s, int64_t row, const T* x, int64_t ld,
+                                             int64_t stall_row, int kept) {
+    const int kv = (kept + Elem<T>::kVec - 1) / Elem<T>::kVec;
+    const uint32_t extra = stall_extra(row, stall_row);
+    if (kv > 0) tma_load_row(p.ring.slot(s), x + row * ld, uint32_t(kv) * 16u, p.ring.bar + s, extra);
+    else if (extra) mbar_expect_tx(p.ring.bar + s, extra);
+    else mbar_arrive(p.ring.bar + s);
+}
 
 // Producer: copy the body of `row` into buffer s.
 template <typename T, bool FULL>
@@ -98,9 +128,10 @@ __device__ __forceinline__ void issue_row(const GroupPipe& p, int s, int64_t row
 
 // CTA start: thread 0 initialises every group's barriers; then each group's
 // producer issues the copies of its first nbuf rows.
-template <typename T, bool FULL, int ROWS>
+// `cm` (CAUSAL): the first nbuf rows copy only their kept prefixes.
+template <typename T, bool FULL, int ROWS, bool CAUSAL = false>
 __device__ __forceinline__ void start_pipes(char* smem, const GroupPipe& p, const T* x, int64_t M, int N, int64_t ld,
-                                            int64_t stall_row) {
+                                            int64_t stall_row, const CausalMask& cm = CausalMask{1, 0}) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < ROWS * p.ring.nbuf; ++s) mbar_init(reinterpret_cast<uint64_t*>(smem) + s, 1);
         mbar_init_fence();
@@ -109,20 +140,24 @@ __device__ __forceinline__ void start_pipes(char* smem, const GroupPipe& p, cons
     if (p.producer)
         for (int s = 0; s < p.ring.nbuf; ++s) {
             const int64_t row = p.first + s * p.stride;
-            if (row < M) issue_row<T, FULL>(p, s, row, x, N, ld, stall_row);
+            if (row >= M) continue;
+            if constexpr (CAUSAL) issue_prefix<T>(p, s, row, x, ld, stall_row, cm.kept_at(row % cm.period, N));
+            else issue_row<T, FULL>(p, s, row, x, N, ld, stall_row);
         }
 }
 
 // After the group's first reduction: refill buffer s with the row nbuf
 // iterations ahead (every thread of the group has its data in registers).
-template <typename T, bool FULL>
+// `next_kept` (CAUSAL): the kept columns of the row nbuf iterations ahead.
+template <typename T, bool FULL, bool CAUSAL = false>
 __device__ __forceinline__ void refill(const GroupPipe& p, int s, int64_t row, const T* x, int64_t M, int N,
-                                       int64_t ld, int64_t stall_row) {
+                                       int64_t ld, int64_t stall_row, int next_kept = 0) {
     if (!p.producer) return;
     const int64_t nxt = row + int64_t(p.ring.nbuf) * p.stride;
     if (nxt < M) {
         fence_proxy_async_smem();
-        issue_row<T, FULL>(p, s, nxt, x, N, ld, stall_row);
+        if constexpr (CAUSAL) issue_prefix<T>(p, s, nxt, x, ld, stall_row, next_kept);
+        else issue_row<T, FULL>(p, s, nxt, x, N, ld, stall_row);
     }
 }
 
@@ -147,7 +182,10 @@ __device__ __forceinline__ void abandon(const GroupPipe& p, int64_t i, int64_t M
 // CTA per work unit of rows; the resident CTAs take the units
 // of CTAs that have not started yet with cluster launch control (a CTA cancels
 // a pending CTA and processes its unit), so fast SMs take more rows and
-// nothing but the last unit waits. A unit holds `unit_rows` rows of each group. Thread 0 keeps one steal request in flight,
+// nothing but the last unit waits. A unit holds `unit_rows` rows of each group.
+// Used by the RMSNorm kernels (tma_rms_kernels.cuh): on GB300 it made them
+// ~10% faster, while softmax and LayerNorm+GELU, which issue more
+// instructions per row, ran 5-10% slower with it and keep the static schedule. Thread 0 keeps one steal request in flight,
 // its 16-byte response double-buffered in shared memory (`full` completes when
 // a response lands, `empty` when every group's producer has read it), and
 // issues the next request only after a successful one. Each group's producer
@@ -324,54 +362,63 @@ __device__ __forceinline__ void dyn_abandon(const GroupPipe& p, const DynFeed& f
     atomicExch(err, kDeviceErrTimeout);
 }
 
-template <typename T, int TPR, int VPT, int ROWS, bool FULL>
+// CAUSAL (full rows only): the causal softmax; row `row` keeps cm.kept(row, N)
+// columns, only the 16-byte vectors holding them are copied, and the masked
+// columns come out as exactly 0 (their exponentials of -inf).
+template <typename T, int TPR, int VPT, int ROWS, bool FULL, bool CAUSAL = false>
 __global__ void __launch_bounds__(TPR * ROWS)
     softmax_tma_kernel(const T* x, T* y, int64_t M, int N, int64_t ld, int nbuf, unsigned* err,
-                       unsigned long long wait_ns, int64_t stall_row, int unit_rows) {
+                       unsigned long long wait_ns, int64_t stall_row, CausalMask cm) {
     using E = Elem<T>;
     constexpr int V = E::kVec;
     static_assert(TPR % 64 == 0, "row groups of at least two warps");
+    static_assert(FULL || !CAUSAL, "the causal form runs on full rows");
     extern __shared__ __align__(128) char smem[];
     __shared__ float red_max[ROWS][TPR / 32];
     __shared__ float red_sum[ROWS][TPR / 32];
-    __shared__ ClcShared cs;
     const GroupPipe p = make_group<TPR, ROWS>(smem, N, E::kBytes, nbuf);
     const int g = threadIdx.x / TPR, t = threadIdx.x % TPR;
-    const T* const src[1] = {x};
-    const bool dynamic = FULL && unit_rows > 0;  // unit_rows 0: static schedule
-    DynFeed f{};
-    if (dynamic) f = dyn_start<T, ROWS, 1>(smem, p, cs, g, src, N, ld, M, stall_row, wait_ns, err, unit_rows);
-    else start_pipes<T, FULL, ROWS>(smem, p, x, M, N, ld, stall_row);
+    start_pipes<T, FULL, ROWS, CAUSAL>(smem, p, x, M, N, ld, stall_row, cm);
+    // causal: row mod period of iteration i, its step per iteration and per ring turn
+    int64_t rm = CAUSAL ? p.first % cm.period : 0;
+    const int64_t step = CAUSAL ? p.stride % cm.period : 0;
+    const int64_t ring_step = CAUSAL ? (int64_t(nbuf) * step) % cm.period : 0;
 
     for (int64_t i = 0;; ++i) {
+        const int64_t row = p.first + i * p.stride;
+        if (row >= M) break;
         const int s = int(i % nbuf);
-        int64_t row;
-        int fail = 0;
-        if (dynamic) {
-            row = dyn_row(p, cs, g, i, wait_ns, fail);
-            if (row < 0) {  // the end of the work (a failed wait goes on to the reduction below)
-                dyn_finish(f, cs, wait_ns);
-                return;
-            }
-        } else {
-            row = p.first + i * p.stride;
-            if (row >= M) break;
-        }
         const T* xr = x + row * ld;
         const RowSpan sp = row_span<T, FULL>(xr, N);
         // unaligned head / tail elements: plain loads, in flight during the wait
         const bool has_ex = !FULL && t < sp.head + sp.tail;
         const int ecol = has_ex ? span_extra_col(sp, t, V) : 0;
         float ex = has_ex ? E::load(xr + ecol) : -INFINITY;
-        if (!dynamic) fail = !mbar_wait(p.ring.bar + s, uint32_t((i / nbuf) & 1), wait_ns);
+        int fail = !mbar_wait(p.ring.bar + s, uint32_t((i / nbuf) & 1), wait_ns);
         const char* sb = p.ring.slot(s);
+        const int kept = CAUSAL ? cm.kept_at(rm, N) : N;
 
         float v[VPT][V];
         float mx = ex;
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
             const int k = t + j * TPR;
-            if (FULL || k < sp.body) {
+            if (CAUSAL) {
+                // vectors wholly past the kept prefix were not copied and take
+                // no arithmetic (their outputs are stored as zeros below); only
+                // the vector that straddles the boundary is masked per element
+                if (k * V < kept) {
+                    E::unpack(lds16(sb + size_t(k) * 16), v[j]);
+                    if (k * V + V > kept) {
+#pragma unroll
+                        for (int e = 0; e < V; ++e)
+                            if (k * V + e >= kept) v[j][e] = -INFINITY;
+                    }
+#pragma unroll
+                    for (int e = 0; e < V; ++e) mx = fmaxf(mx, v[j][e]);
+                }
+                continue;
+            } else if (FULL || k < sp.body) {
                 E::unpack(lds16(sb + size_t(k) * 16), v[j]);
             } else {
 #pragma unroll
@@ -382,24 +429,22 @@ __global__ void __launch_bounds__(TPR * ROWS)
         }
         mx = row_reduce<TPR>(mx, red_max[g], p.bar_id, OpMax(), fail);
         if (fail) {
-            if (dynamic) dyn_abandon(p, f, cs, g, i, err, wait_ns);
-            else abandon(p, i, M, err, wait_ns);
+            abandon(p, i, M, err, wait_ns);
             return;
         }
-        if (dynamic) {
-            if (p.producer) dyn_issue<T, ROWS, 1>(p, cs, f, g, s, src, N, ld, M, stall_row, wait_ns, err);
-        } else {
-            refill<T, FULL>(p, s, row, x, M, N, ld, stall_row);
-        }
+        refill<T, FULL, CAUSAL>(p, s, row, x, M, N, ld, stall_row, CAUSAL ? cm.kept_at(cm.advance(rm, ring_step), N) : 0);
+        if (CAUSAL) rm = cm.advance(rm, step);
         if (mx == -INFINITY) mx = 0.f;
         float sum = 0.f;
 #pragma unroll
-        for (int j = 0; j < VPT; ++j)
+        for (int j = 0; j < VPT; ++j) {
+            if (CAUSAL && (t + j * TPR) * V >= kept) continue;
 #pragma unroll
             for (int e = 0; e < V; ++e) {
                 v[j][e] = exp_shifted(v[j][e], mx);
                 sum += v[j][e];
             }
+        }
         ex = exp_shifted(ex, mx);
         sum += ex;
         sum = row_reduce<TPR>(sum, red_sum[g], p.bar_id, OpSum(), fail);
@@ -409,7 +454,9 @@ __global__ void __launch_bounds__(TPR * ROWS)
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
             const int k = t + j * TPR;
-            if (FULL || k < sp.body) {
+            if (CAUSAL && k * V >= kept) {
+                st_stream16(yb + size_t(k) * V, make_uint4(0u, 0u, 0u, 0u));
+            } else if (FULL || k < sp.body) {
                 float o[V];
 #pragma unroll
                 for (int e = 0; e < V; ++e) o[e] = v[j][e] * inv;
@@ -460,14 +507,13 @@ __host__ __device__ constexpr uint32_t affine_stage_bytes() {
 template <typename T, int TPR, int VPT, int ROWS, bool FULL>
 __global__ void __launch_bounds__(TPR * ROWS)
     ln_gelu_tma_kernel(const T* x, T* y, const T* w, const T* b, float eps, int64_t M, int N, int64_t ld,
-                       int nbuf, unsigned* err, unsigned long long wait_ns, int64_t stall_row, int unit_rows) {
+                       int nbuf, unsigned* err, unsigned long long wait_ns, int64_t stall_row) {
     using E = Elem<T>;
     constexpr int V = E::kVec, H = V / 4;
     static_assert(TPR % 64 == 0, "row groups of at least two warps");
     extern __shared__ __align__(128) char smem[];
     __shared__ float red_a[ROWS][TPR / 32];
     __shared__ float red_b[ROWS][2 * TPR / 32];
-    __shared__ ClcShared cs;
     const int period = FULL ? 1 : row_phase_period(ld * E::kBytes);
     const GroupPipe p = make_group<TPR, ROWS>(smem, N, E::kBytes, nbuf, period);
     const int g = threadIdx.x / TPR, t = threadIdx.x % TPR;
@@ -478,11 +524,7 @@ __global__ void __launch_bounds__(TPR * ROWS)
     const float fN = float(N);
     // the split shared by every row of this CTA's phase class
     const RowSpan sp = row_span<T, FULL>(x + int64_t(p.cls) * ld, N);
-    const T* const src[1] = {x};
-    const bool dynamic = FULL && unit_rows > 0;  // unit_rows 0: static schedule
-    DynFeed f{};
-    if (dynamic) f = dyn_start<T, ROWS, 1>(smem, p, cs, g, src, N, ld, M, stall_row, wait_ns, err, unit_rows);
-    else start_pipes<T, FULL, ROWS>(smem, p, x, M, N, ld, stall_row);
+    start_pipes<T, FULL, ROWS>(smem, p, x, M, N, ld, stall_row);
     stage_affine_thread_major<T, TPR, VPT>(w, b, sp.head, sp.body, sw4, sb4);
     if constexpr (!FULL) {
         for (int e = threadIdx.x; e < sp.head + sp.tail; e += blockDim.x) {
@@ -495,22 +537,12 @@ __global__ void __launch_bounds__(TPR * ROWS)
     const int ecol = has_ex ? span_extra_col(sp, t, V) : 0;
 
     for (int64_t i = 0;; ++i) {
+        const int64_t row = p.first + i * p.stride;
+        if (row >= M) break;
         const int s = int(i % nbuf);
-        int64_t row;
-        int fail = 0;
-        if (dynamic) {
-            row = dyn_row(p, cs, g, i, wait_ns, fail);
-            if (row < 0) {  // the end of the work (a failed wait goes on to the reduction below)
-                dyn_finish(f, cs, wait_ns);
-                return;
-            }
-        } else {
-            row = p.first + i * p.stride;
-            if (row >= M) break;
-        }
         const T* xr = x + row * ld;
         float ex = has_ex ? E::load(xr + ecol) : 0.f;
-        if (!dynamic) fail = !mbar_wait(p.ring.bar + s, uint32_t((i / nbuf) & 1), wait_ns);
+        int fail = !mbar_wait(p.ring.bar + s, uint32_t((i / nbuf) & 1), wait_ns);
         const char* sbuf = p.ring.slot(s);
 
         float v[VPT][V];
@@ -529,15 +561,10 @@ __global__ void __launch_bounds__(TPR * ROWS)
         }
         sum = row_reduce<TPR>(sum, red_a[g], p.bar_id, OpSum(), fail);
         if (fail) {
-            if (dynamic) dyn_abandon(p, f, cs, g, i, err, wait_ns);
-            else abandon(p, i, M, err, wait_ns);
+            abandon(p, i, M, err, wait_ns);
             return;
         }
-        if (dynamic) {
-            if (p.producer) dyn_issue<T, ROWS, 1>(p, cs, f, g, s, src, N, ld, M, stall_row, wait_ns, err);
-        } else {
-            refill<T, FULL>(p, s, row, x, M, N, ld, stall_row);
-        }
+        refill<T, FULL>(p, s, row, x, M, N, ld, stall_row);
         const float mean = sum / fN;
         // centred values, their squares and the residual of the fp32 mean
         float q = 0.f, r = 0.f;

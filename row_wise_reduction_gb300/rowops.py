@@ -22,6 +22,7 @@ __all__ = [
     "library",
     "library_path",
     "rowops_softmax",
+    "rowops_softmax_causal",
     "rowops_online_softmax",
     "rowops_online_softmax_workspace_bytes",
     "rowops_online_softmax_status",
@@ -94,6 +95,8 @@ def library() -> ctypes.CDLL:
         L.rowops_layernorm_gelu.restype = ctypes.c_int
         L.rowops_layernorm_gelu.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, _i64, _i64, _i64,
                                             ctypes.c_int, _vp]
+        L.rowops_softmax_causal.restype = ctypes.c_int
+        L.rowops_softmax_causal.argtypes = [_vp, _vp, _i64, _i64, _i64, _i64, _i64, ctypes.c_int, _vp]
         L.rowops_rmsnorm.restype = ctypes.c_int
         L.rowops_rmsnorm.argtypes = [_vp, _vp, _vp, ctypes.c_float, _i64, _i64, _i64, ctypes.c_int, _vp]
         L.rowops_fused_residual_rmsnorm.restype = ctypes.c_int
@@ -291,3 +294,23 @@ def rowops_fused_residual_rmsnorm(
         M, N, ld, _dtype_code(x), _stream(stream))
     _check("rowops_fused_residual_rmsnorm", st)
     return y, residual_out
+
+
+def rowops_softmax_causal(
+    x: torch.Tensor,
+    period: Optional[int] = None,
+    offset: int = 0,
+    y: Optional[torch.Tensor] = None,
+    *,
+    stream=None,
+) -> torch.Tensor:
+    """Causal softmax: row r keeps the columns c <= (r mod period) + offset
+    (default period: N, the stacked square causal masks); masked columns are
+    not read and come out 0."""
+    M, N, ld = _rows(x, "x")
+    y = _out_like(x, y)
+    period = N if period is None else int(period)
+    st = library().rowops_softmax_causal(x.data_ptr(), y.data_ptr(), M, N, ld, period, int(offset),
+                                         _dtype_code(x), _stream(stream))
+    _check("rowops_softmax_causal", st)
+    return y

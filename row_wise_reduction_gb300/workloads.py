@@ -26,7 +26,7 @@ class Workload:
     """One synthetic workload: an operation, a dtype, a shape and a value recipe."""
 
     name: str
-    op: str  # "softmax" | "online_softmax" | "layernorm_gelu" | "rmsnorm" | "residual_rmsnorm"
+    op: str  # "softmax" | "softmax_causal" | "online_softmax" | "layernorm_gelu" | "rmsnorm" | "residual_rmsnorm"
     dtype: str  # "f32" | "bf16"
     M: int  # rows
     N: int  # columns (reduction length)
@@ -56,6 +56,10 @@ WORKLOADS: Dict[str, Workload] = {
         Workload("layernorm_gelu_bf16_65536x8192", "layernorm_gelu", "bf16", 65536, 8192, seed=4, affine=True),
         Workload("layernorm_gelu_bf16_65536x127", "layernorm_gelu", "bf16", 65536, 127, seed=4, affine=True),
         Workload("layernorm_gelu_bf16_65536x4097", "layernorm_gelu", "bf16", 65536, 4097, seed=4, affine=True),
+        # the causal softmax entry point on the causal softmax input (period N, offset 0: row r keeps
+        # columns c <= r mod N) [Triton Kernel 实现练习 §5.1]
+        Workload("softmax_causal_bf16_32768x4096", "softmax_causal", "bf16", 32768, 4096, seed=2, x_std=2.0,
+                 causal=True),
         # RMSNorm and fused residual + RMSNorm [Triton Kernel 实现练习 §4.2, §4.3], on the shapes of
         # the LayerNorm+GELU workloads
         Workload("rmsnorm_f32_4096x768", "rmsnorm", "f32", 4096, 768, seed=5, affine=True),

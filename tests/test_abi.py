@@ -33,7 +33,7 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("rowops_softmax", "rowops_online_softmax", "rowops_layernorm_gelu",
               "rowops_online_softmax_workspace_bytes", "rowops_online_softmax_status", "rowops_status_string",
-              "rowops_rmsnorm", "rowops_fused_residual_rmsnorm"):
+              "rowops_rmsnorm", "rowops_fused_residual_rmsnorm", "rowops_softmax_causal"):
         assert n in names
 
 
@@ -84,6 +84,17 @@ def test_layernorm_gelu_validation(lib):
     assert f(X, Y, None, Y + 0x40002, 1e-5, 4, 8, 8, F32, None) == INVALID  # misaligned b
     assert f(X, Y, None, None, 1e-5, 4, 8, 4, F32, None) == INVALID  # ld < N
     assert f(None, None, None, None, 1e-5, 0, 8, 8, F32, None) == OK
+
+
+def test_softmax_causal_validation(lib):
+    f = lib.rowops_softmax_causal
+    assert f(X, Y, 4, 8, 8, 0, 0, F32, None) == INVALID  # period < 1
+    assert f(X, Y, 4, 8, 8, -3, 0, F32, None) == INVALID
+    assert f(X, Y, 4, 8, 8, 8, (1 << 62) + 1, F32, None) == INVALID  # offset out of range
+    assert f(X, Y, 4, 8, 8, 8, -(1 << 62) - 1, F32, None) == INVALID
+    assert f(X, X + 16, 4, 8, 8, 8, 0, F32, None) == INVALID  # partial overlap
+    assert f(None, Y, 4, 8, 8, 8, 0, F32, None) == INVALID
+    assert f(None, None, 0, 8, 8, 8, 0, F32, None) == OK
 
 
 def test_rmsnorm_validation(lib):

@@ -34,12 +34,10 @@ def _softmax_wl():
     return workloads.Workload("timeout_softmax", "softmax", "bf16", 2000, 4096, seed=3, x_std=2.0)
 
 
-@pytest.mark.parametrize("sched", ["static", "dynamic"])
-def test_row_pipeline_wait_times_out_and_context_recovers(oracle, monkeypatch, sched):
+def test_row_pipeline_wait_times_out_and_context_recovers(oracle, monkeypatch):
     x = gu.make_x(_softmax_wl())["x"]
     assert rowops_device_status() == 0
     monkeypatch.setenv("ROWOPS_KERNEL", "tma")
-    monkeypatch.setenv("ROWOPS_SCHED", sched)
     monkeypatch.setenv("ROWOPS_WAIT_LIMIT_NS", LIMIT_NS)
     monkeypatch.setenv("ROWOPS_TEST_STALL_ROW", "777")
     rowops_softmax(x)
@@ -52,12 +50,10 @@ def test_row_pipeline_wait_times_out_and_context_recovers(oracle, monkeypatch, s
     C.assert_softmax_close(C.to_f64(y), oracle.softmax(gu.rows_f32(x)), "bf16")
 
 
-@pytest.mark.parametrize("sched", ["static", "dynamic"])
-def test_layernorm_row_groups_wait_times_out(oracle, monkeypatch, sched):
+def test_layernorm_row_groups_wait_times_out(oracle, monkeypatch):
     wl = workloads.Workload("timeout_ln", "layernorm_gelu", "bf16", 1500, 8192, seed=4, affine=True)
     inp = gu.make_x(wl)
     monkeypatch.setenv("ROWOPS_KERNEL", "tma")
-    monkeypatch.setenv("ROWOPS_SCHED", sched)
     monkeypatch.setenv("ROWOPS_WAIT_LIMIT_NS", LIMIT_NS)
     monkeypatch.setenv("ROWOPS_TEST_STALL_ROW", "3")
     rowops_layernorm_gelu(inp["x"], inp["w"], inp["b"], wl.eps)
@@ -113,3 +109,19 @@ def test_rmsnorm_pipeline_wait_times_out(oracle, monkeypatch, sched):
                                            inp["w"].float().cpu().numpy(), wl.eps, "bf16")
     np.testing.assert_array_equal(C.to_f64(ro), s_ref)
     C.assert_rms_close(C.to_f64(y), y_ref, "bf16")
+
+
+def test_causal_softmax_wait_times_out(oracle, monkeypatch):
+    """The causal row pipeline (prefix copies): the stalled row's wait gives up."""
+    from row_wise_reduction_gb300 import rowops_softmax_causal
+
+    x = gu.make_x(_softmax_wl())["x"]
+    monkeypatch.setenv("ROWOPS_KERNEL", "tma")
+    monkeypatch.setenv("ROWOPS_WAIT_LIMIT_NS", LIMIT_NS)
+    monkeypatch.setenv("ROWOPS_TEST_STALL_ROW", "1234")
+    rowops_softmax_causal(x, 4096, 0)
+    assert rowops_device_status() == TIMEOUT
+    monkeypatch.delenv("ROWOPS_TEST_STALL_ROW")
+    y = rowops_softmax_causal(x, 4096, 0)
+    assert rowops_device_status() == 0
+    C.assert_softmax_close(C.to_f64(y), oracle.softmax_causal(gu.rows_f32(x), 4096, 0), "bf16")

@@ -296,18 +296,3 @@ def test_ln_gelu_tma_fewer_rows_than_phase_classes(oracle, monkeypatch, M, rows)
     from row_wise_reduction_gb300 import rowops_device_status
 
     assert rowops_device_status() == 0
-
-
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("M,N", [(1, 4096), (3, 8192), (157, 4096), (1000, 2048), (4099, 1024)])
-@pytest.mark.parametrize("rows,unit", [("1", "1"), ("4", "2"), ("8", "3")])
-def test_ln_gelu_dynamic_schedule(oracle, monkeypatch, dtype, M, N, rows, unit):
-    """Full rows on the dynamic row schedule, one to eight row groups per CTA."""
-    monkeypatch.setenv("ROWOPS_KERNEL", "tma")
-    monkeypatch.setenv("ROWOPS_SCHED", "dynamic")
-    monkeypatch.setenv("ROWOPS_ROWS_PER_CTA", rows)
-    monkeypatch.setenv("ROWOPS_UNIT_ROWS", unit)
-    check(oracle, edge(dtype, M, N, seed=M + N))
-    from row_wise_reduction_gb300 import rowops_device_status
-
-    assert rowops_device_status() == 0

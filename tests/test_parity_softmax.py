@@ -229,19 +229,3 @@ def test_softmax_tma_general_rows(oracle, monkeypatch, dtype, N, ld, offset):
     from row_wise_reduction_gb300 import rowops_device_status
 
     assert rowops_device_status() == 0
-
-
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("M,N", [(1, 4096), (3, 8192), (157, 4096), (1000, 2048), (4099, 1024)])
-@pytest.mark.parametrize("unit", ["1", "2", "5"])
-def test_softmax_dynamic_schedule(oracle, monkeypatch, dtype, M, N, unit):
-    """Full rows on the dynamic row schedule (work units taken with cluster
-    launch control): every row exactly once, for row counts below, at and
-    above the number of units the first wave of CTAs holds."""
-    monkeypatch.setenv("ROWOPS_KERNEL", "tma")
-    monkeypatch.setenv("ROWOPS_SCHED", "dynamic")
-    monkeypatch.setenv("ROWOPS_UNIT_ROWS", unit)
-    check(oracle, edge(dtype, M, N, seed=M + N))
-    from row_wise_reduction_gb300 import rowops_device_status
-
-    assert rowops_device_status() == 0
