@@ -63,6 +63,14 @@ def lib() -> ctypes.CDLL:
                                          _c_double_p]
             getattr(L, name).restype = ctypes.c_int
         L.oracle_rmsnorm_row.argtypes = [_c_double_p, _c_double_p, ctypes.c_double, _i64, _c_double_p]
+        L.oracle_gelu_erf.argtypes = [ctypes.c_double]
+        L.oracle_gelu_erf.restype = ctypes.c_double
+        L.oracle_layernorm_gelu_erf_rows_f32.argtypes = [_c_float_p, _c_float_p, _c_float_p, ctypes.c_double, _i64,
+                                                         _i64, _i64, _c_double_p]
+        L.oracle_layernorm_gelu_erf_rows_f32.restype = ctypes.c_int
+        for name in ("oracle_row_sum_rows_f32", "oracle_row_max_rows_f32"):
+            getattr(L, name).argtypes = [_c_float_p, _i64, _i64, _i64, _c_double_p]
+            getattr(L, name).restype = ctypes.c_int
         L.oracle_causal_kept.argtypes = [_i64, _i64, _i64, _i64]
         L.oracle_causal_kept.restype = _i64
         L.oracle_softmax_causal_rows_f32.argtypes = [_c_float_p, _i64, _i64, _i64, _i64, _i64, _c_double_p]
@@ -305,3 +313,38 @@ def softmax_causal_rows_at(row, r: int, period: int, offset: int = 0) -> np.ndar
     if kept > 0:
         y[:kept] = softmax_row(xr[:kept])
     return y
+
+
+def gelu_erf(z) -> np.ndarray:
+    """Exact GELU 0.5 z (1 + erf(z / sqrt(2)))."""
+    f = lib().oracle_gelu_erf
+    zz = np.asarray(z, dtype=np.float64)
+    return np.vectorize(f, otypes=[np.float64])(zz) if zz.ndim else np.float64(f(float(zz)))
+
+
+def layernorm_gelu_erf(x, w=None, b=None, eps: float = 1e-5) -> np.ndarray:
+    """LayerNorm -> affine -> exact GELU of every row -> float64 (M, N)."""
+    xs, M, N, ld = _rows(x)
+    y = np.empty((M, N), dtype=np.float64)
+    wf, bf = _opt32(w, N), _opt32(b, N)
+    if lib().oracle_layernorm_gelu_erf_rows_f32(_fp(xs), _fp(wf), _fp(bf), float(eps), M, N, ld, _dp(y)) != 0:
+        raise ValueError("oracle_layernorm_gelu_erf_rows_f32 rejected its arguments")
+    return y
+
+
+def row_sum(x) -> np.ndarray:
+    """Sum of every row -> float64 (M,)."""
+    xs, M, N, ld = _rows(x)
+    out = np.empty(M, dtype=np.float64)
+    if lib().oracle_row_sum_rows_f32(_fp(xs), M, N, ld, _dp(out)) != 0:
+        raise ValueError("oracle_row_sum_rows_f32 rejected its arguments")
+    return out
+
+
+def row_max(x) -> np.ndarray:
+    """Maximum of every row -> float64 (M,) (NaN if the row holds a NaN)."""
+    xs, M, N, ld = _rows(x)
+    out = np.empty(M, dtype=np.float64)
+    if lib().oracle_row_max_rows_f32(_fp(xs), M, N, ld, _dp(out)) != 0:
+        raise ValueError("oracle_row_max_rows_f32 rejected its arguments")
+    return out

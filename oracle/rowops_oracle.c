@@ -169,6 +169,14 @@ double oracle_gelu_tanh(double z) {
     return 0.5 * z * (1.0 + tanh(inner));
 }
 
+/* ---------------------------------------------------------------------------
+ * Exact GELU [EX §3.4]: gelu_exact(z) = 0.5 * z * (1 + erf(z / sqrt(2))).
+ * 1 + erf(u) is evaluated as erfc(-u) (libm, double): the same function, but
+ * for z << 0 the sum 1 + erf cancels (at z = -8 it would be off by ~18%),
+ * while erfc(-u) keeps full relative precision.
+ * ------------------------------------------------------------------------- */
+double oracle_gelu_erf(double z) { return 0.5 * z * erfc(-z / sqrt(2.0)); }
+
 /* LayerNorm -> affine -> GELU, one row [FUS §三 _layer_norm_gelu_kernel]. */
 void oracle_layernorm_gelu_row(const double* x, const double* w, const double* b, double eps,
                                int64_t n, double* y) {
@@ -367,5 +375,48 @@ int oracle_softmax_causal_rows_f32(const float* x, int64_t M, int64_t N, int64_t
         for (int64_t j = kept; j < N; ++j) yr[j] = 0.0;
     }
     free(row);
+    return 0;
+}
+
+int oracle_layernorm_gelu_erf_rows_f32(const float* x, const float* w, const float* b, double eps, int64_t M,
+                                       int64_t N, int64_t ld, double* y) {
+    const int rc = layernorm_rows(x, w, b, eps, M, N, ld, y, 0);
+    if (rc != 0) return rc;
+    for (int64_t i = 0; i < M * N; ++i) y[i] = oracle_gelu_erf(y[i]);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * Row-wise sum [EX §2.2]: out[i] = sum_j x[i, j] (padding contributes 0), a
+ * plain left-to-right sum in double.
+ * ------------------------------------------------------------------------- */
+int oracle_row_sum_rows_f32(const float* x, int64_t M, int64_t N, int64_t ld, double* out) {
+    if (bad_shape(x, M, N, ld, out)) return -1;
+    for (int64_t r = 0; r < M; ++r) {
+        double s = 0.0;
+        for (int64_t j = 0; j < N; ++j) s += (double)x[r * ld + j];
+        out[r] = s;
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * Row-wise max [EX §2.3]: out[i] = max_j x[i, j] (padding is -inf); a NaN in
+ * the row makes the result NaN (as for softmax, where it poisons the row).
+ * ------------------------------------------------------------------------- */
+int oracle_row_max_rows_f32(const float* x, int64_t M, int64_t N, int64_t ld, double* out) {
+    if (bad_shape(x, M, N, ld, out)) return -1;
+    for (int64_t r = 0; r < M; ++r) {
+        double m = -INFINITY;
+        for (int64_t j = 0; j < N; ++j) {
+            const double v = (double)x[r * ld + j];
+            if (isnan(v)) {
+                m = NAN;
+                break;
+            }
+            if (v > m) m = v;
+        }
+        out[r] = m;
+    }
     return 0;
 }

@@ -55,6 +55,10 @@ void oracle_layernorm_row(const double* x, const double* w, const double* b, dou
 /* tanh-approximation GELU [KT "Triton GeLU"; EX §3.4; FUS §三]. */
 double oracle_gelu_tanh(double z);
 
+/* Exact GELU [EX §3.4]: 0.5 z (1 + erf(z / sqrt(2))), in double (1 + erf(u)
+ * evaluated as erfc(-u), without cancellation for z << 0). */
+double oracle_gelu_erf(double z);
+
 /* LayerNorm, then affine, then GELU [FUS §三 _layer_norm_gelu_kernel]. */
 void oracle_layernorm_gelu_row(const double* x, const double* w, const double* b, double eps,
                                int64_t n, double* y);
@@ -94,6 +98,14 @@ int oracle_layernorm_rows_f32(const float* x, const float* w, const float* b, do
                               int64_t N, int64_t ld, double* y);
 int oracle_rmsnorm_rows_f32(const float* x, const float* w, double eps, int64_t M, int64_t N, int64_t ld,
                             double* y);
+/* LayerNorm -> affine -> exact (erf) GELU [EX §3.4, §4.1]. */
+int oracle_layernorm_gelu_erf_rows_f32(const float* x, const float* w, const float* b, double eps, int64_t M,
+                                       int64_t N, int64_t ld, double* y);
+/* Row sum [EX §2.2]: out[i] = sum_j x[i, j], in double. */
+int oracle_row_sum_rows_f32(const float* x, int64_t M, int64_t N, int64_t ld, double* out);
+/* Row max [EX §2.3]: out[i] = max_j x[i, j]; -inf entries are padding; a NaN
+ * makes the row's max NaN. */
+int oracle_row_max_rows_f32(const float* x, int64_t M, int64_t N, int64_t ld, double* out);
 /* Causal softmax: the stable softmax of each row's kept prefix (masked
  * entries are not read), 0 on the masked columns. */
 int oracle_softmax_causal_rows_f32(const float* x, int64_t M, int64_t N, int64_t ld, int64_t period,

@@ -537,6 +537,92 @@ def test_softmax_causal_degenerate_masks(oracle):
     assert np.all(oracle.softmax_causal(x, 4, -5) == 0.0)
 
 
+# ----------------------------------------------------------------------------
+# exact GELU, row sum, row max
+# ----------------------------------------------------------------------------
+_GR = {c[0]: c for c in _golden.read_cases("gelu_erf_and_row_reductions.txt")}
+
+
+def test_gelu_erf_table_values(oracle):
+    """x * Phi(x) at printed standard normal CDF values: catches a missing
+    1/sqrt(2), the tanh approximation in its place, or a dropped 0.5."""
+    _, _, rows = _GR["gelu_table"]
+    z = [float(v) for v in rows["z"]]
+    want = [float(v) for v in rows["g"]]
+    np.testing.assert_allclose(oracle.gelu_erf(z), want, rtol=0, atol=4e-16)
+
+
+def test_gelu_erf_identities_and_libraries(oracle):
+    """GELU(x) - GELU(-x) = x; equal to x * scipy.special.ndtr(x) and torch's
+    exact GELU in float64; within the known ~5e-4 of the tanh form."""
+    sp = pytest.importorskip("scipy.special")
+    z = np.linspace(-12, 12, 2401)
+    g = oracle.gelu_erf(z)
+    np.testing.assert_allclose(g - oracle.gelu_erf(-z), z, rtol=0, atol=4e-15)
+    np.testing.assert_allclose(g, z * sp.ndtr(z), rtol=1e-13, atol=1e-300)  # relative, tail included
+    # torch evaluates 1 + erf itself, which cancels in the negative tail: absolute
+    g_t = torch.nn.functional.gelu(torch.from_numpy(z), approximate="none").numpy()
+    np.testing.assert_allclose(g, g_t, rtol=2e-15, atol=2e-15)
+    assert np.max(np.abs(g - oracle.gelu_tanh(z))) < 5e-4
+    assert np.max(np.abs(g - oracle.gelu_tanh(z))) > 1e-4  # and it is the other function
+
+
+def test_layernorm_gelu_erf_is_erf_gelu_of_layernorm(oracle):
+    rng = _rng(61)
+    x = rng.normal(0, 1, size=(5, 300)).astype(np.float32)
+    w = rng.uniform(0.5, 1.5, size=300).astype(np.float32)
+    b = rng.normal(0, 0.1, size=300).astype(np.float32)
+    np.testing.assert_array_equal(oracle.layernorm_gelu_erf(x, w, b, 1e-5), oracle.gelu_erf(oracle.layernorm(x, w, b, 1e-5)))
+    ref = torch.nn.functional.gelu(torch.nn.functional.layer_norm(torch.from_numpy(x).double(), (300,),
+                                   torch.from_numpy(w).double(), torch.from_numpy(b).double(), 1e-5),
+                                   approximate="none").numpy()
+    np.testing.assert_allclose(oracle.layernorm_gelu_erf(x, w, b, 1e-5), ref, rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("name", ["ramp", "cancelling", "negative_with_padding_values", "single"])
+def test_row_sum_and_max_worked_examples(oracle, name):
+    _, _, rows = _GR[name]
+    x = np.array([[float(v) for v in rows["x"]]], dtype=np.float32)
+    assert oracle.row_sum(x)[0] == float(rows["sum"][0])
+    assert oracle.row_max(x)[0] == float(rows["max"][0])
+
+
+def test_row_sum_matches_exactly_rounded_sum(oracle):
+    """Against math.fsum (an exactly rounded sum, a different algorithm): the
+    double left-to-right sum of fp32 inputs is within N * 2^-53 * sum|x|;
+    also sum(x + c) = sum(x) + N c."""
+    import math
+
+    rng = _rng(67)
+    for n in (1, 7, 768, 4097, 100003):
+        x = rng.normal(0, 3, size=(3, n)).astype(np.float32)
+        got = oracle.row_sum(x)
+        for i in range(3):
+            want = math.fsum(float(v) for v in x[i])
+            assert abs(got[i] - want) <= n * 2.0**-53 * float(np.abs(x[i]).astype(np.float64).sum())
+    # integer-valued rows: every partial sum is exact, so the result is too
+    xi = rng.integers(-1000, 1000, size=(4, 100003)).astype(np.float32)
+    np.testing.assert_array_equal(oracle.row_sum(xi), xi.astype(np.int64).sum(axis=1).astype(np.float64))
+
+
+def test_row_max_special_rows(oracle):
+    """Matches numpy's max on ordinary rows; a NaN anywhere makes NaN; an all
+    -inf row gives -inf; the stride's padding is never read."""
+    rng = _rng(71)
+    M, N, ld = 6, 129, 140
+    store = np.full((M, ld), np.nan, dtype=np.float32)
+    store[:, :N] = rng.normal(0, 1, size=(M, N)).astype(np.float32)
+    store[1, :N] = -np.inf
+    store[2, 77] = np.nan
+    store[3, 5] = np.inf
+    out = oracle.row_max(store[:, :N])
+    want = store[:, :N].astype(np.float64).max(axis=1)
+    np.testing.assert_array_equal(out, want)  # numpy's max propagates NaN too
+    assert out[1] == -np.inf and np.isnan(out[2]) and out[3] == np.inf
+    s = oracle.row_sum(store[:, :N])
+    assert s[1] == -np.inf and np.isnan(s[2]) and s[3] == np.inf and np.all(np.isfinite(s[[0, 4, 5]]))
+
+
 def test_batch_rejects_bad_shapes(oracle):
     with pytest.raises(ValueError):
         oracle.layernorm_gelu(np.zeros((2, 3), np.float32), np.ones(4, np.float32))
