@@ -43,8 +43,8 @@ from row_wise_reduction_gb300 import workloads  # noqa: E402
 METRIC = "row-kernel HBM GB/s (% of GB300 peak) for softmax and LayerNorm+GELU"
 STEP = ["softmax_bf16_causal_32768x4096", "online_softmax_f32_64x1048576", "layernorm_gelu_bf16_65536x8192"]
 DOMINANT = "layernorm_gelu_bf16_65536x8192"
-KERNELS_PER_CALL = {"softmax": 1, "softmax_causal": 1, "online_softmax": 2, "layernorm_gelu": 1, "rmsnorm": 1,
-                    "residual_rmsnorm": 1}
+KERNELS_PER_CALL = {"softmax": 1, "softmax_causal": 1, "online_softmax": 2, "layernorm_gelu": 1,
+                    "layernorm_gelu_erf": 1, "rmsnorm": 1, "residual_rmsnorm": 1, "row_sum": 1, "row_max": 1}
 L2_BYTES = 129 * 10**6
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "ln_gelu_bf16_65536x8192.txt")
@@ -61,8 +61,10 @@ def alg_bytes(wl: workloads.Workload) -> int:
     b) once per launch."""
     es = workloads.elem_size(wl.dtype)
     rows = 2 * wl.M * wl.N * es
-    if wl.op == "layernorm_gelu":
+    if wl.op in ("layernorm_gelu", "layernorm_gelu_erf"):
         return rows + (2 * wl.N * es if wl.affine else 0)
+    if wl.op in ("row_sum", "row_max"):  # x read, one fp32 per row written
+        return wl.M * wl.N * es + wl.M * 4
     if wl.op == "rmsnorm":
         return rows + (wl.N * es if wl.affine else 0)
     if wl.op == "residual_rmsnorm":  # x, residual in; y, residual_out out
@@ -398,9 +400,11 @@ def causal_alg_bytes(wl: workloads.Workload, period: int, offset: int = 0) -> in
 
 EXTRA = ["softmax_f32_1024x768", "layernorm_gelu_f32_4096x768", "layernorm_gelu_bf16_65536x127",
          "layernorm_gelu_bf16_65536x4097", "rmsnorm_f32_4096x768", "residual_rmsnorm_f32_4096x768",
-         "rmsnorm_bf16_65536x8192", "residual_rmsnorm_bf16_65536x8192", "softmax_causal_bf16_32768x4096"]
+         "rmsnorm_bf16_65536x8192", "residual_rmsnorm_bf16_65536x8192", "softmax_causal_bf16_32768x4096",
+         "layernorm_gelu_erf_f32_4096x768", "layernorm_gelu_erf_bf16_65536x8192", "row_sum_bf16_65536x8192",
+         "row_max_bf16_65536x8192"]
 SMALL = {"softmax_f32_1024x768", "layernorm_gelu_f32_4096x768", "rmsnorm_f32_4096x768",
-         "residual_rmsnorm_f32_4096x768"}
+         "residual_rmsnorm_f32_4096x768", "layernorm_gelu_erf_f32_4096x768"}
 
 
 def run_extras(dev, stream, iters=50):
@@ -416,10 +420,17 @@ def run_extras(dev, stream, iters=50):
         inp = workloads.make_inputs(wl, dev)
         x, y = inp["x"], torch.empty_like(inp["x"])
         r_out = torch.empty_like(x) if wl.residual else None
+        red = torch.empty(wl.M, dtype=torch.float32, device=dev)
 
         def call():
             if wl.op == "softmax":
                 ro.rowops_softmax(x, y)
+            elif wl.op == "row_sum":
+                ro.rowops_row_sum(x, red)
+            elif wl.op == "row_max":
+                ro.rowops_row_max(x, red)
+            elif wl.op == "layernorm_gelu_erf":
+                ro.rowops_layernorm_gelu_erf(x, inp.get("w"), inp.get("b"), wl.eps, y)
             elif wl.op == "softmax_causal":
                 ro.rowops_softmax_causal(x, wl.N, 0, y)
             elif wl.op == "rmsnorm":
@@ -475,7 +486,7 @@ def run_extras(dev, stream, iters=50):
             gt = a.elapsed_time(b) / iters / 1e3
             rec.update(graph_us=gt * 1e6, graph_gbs=alg_bytes(wl) / gt / 1e9, l2_resident=True)
         out[name] = rec
-        del inp, x, y, r_out
+        del inp, x, y, r_out, red
     del flush
     return out
 
@@ -584,6 +595,8 @@ def run_rowops(args):
     stream = torch.cuda.current_stream()
 
     res_out = {n: torch.empty_like(inputs[n]["x"]) for n, wl in wls.items() if wl.residual}
+    reds = {n: torch.empty(wl.M, dtype=torch.float32, device=dev) for n, wl in wls.items()
+            if wl.op in ("row_sum", "row_max")}
 
     def call(n, x, y):
         wl = wls[n]
@@ -591,6 +604,12 @@ def run_rowops(args):
             ro.rowops_softmax(x, y)
         elif wl.op == "softmax_causal":
             ro.rowops_softmax_causal(x, wl.N, 0, y)
+        elif wl.op == "row_sum":
+            ro.rowops_row_sum(x, reds[n])
+        elif wl.op == "row_max":
+            ro.rowops_row_max(x, reds[n])
+        elif wl.op == "layernorm_gelu_erf":
+            ro.rowops_layernorm_gelu_erf(x, inputs[n]["w"], inputs[n]["b"], wl.eps, y)
         elif wl.op == "online_softmax":
             ro.rowops_online_softmax(x, y, workspace=ws[n])
         elif wl.op == "rmsnorm":
@@ -643,7 +662,8 @@ def run_rowops(args):
     e2e = None
     if not args.no_e2e:
         host_in = {n: inputs[n]["x"].cpu().pin_memory() for n in names}
-        host_out = {n: torch.empty(outputs[n].shape, dtype=outputs[n].dtype).pin_memory() for n in names}
+        result = {n: reds.get(n, outputs[n]) for n in names}  # what each call produces
+        host_out = {n: torch.empty(result[n].shape, dtype=result[n].dtype).pin_memory() for n in names}
         host_wb = {n: {k: inputs[n][k].cpu().pin_memory() for k in ("w", "b", "residual") if k in inputs[n]}
                    for n in names}
         host_ro = {n: torch.empty(res_out[n].shape, dtype=res_out[n].dtype).pin_memory() for n in res_out}
@@ -659,7 +679,7 @@ def run_rowops(args):
                     inputs[n][kk].copy_(t, non_blocking=True)
                 inputs[n]["x"].copy_(host_in[n], non_blocking=True)
                 call(n, inputs[n]["x"], outputs[n])
-                host_out[n].copy_(outputs[n], non_blocking=True)
+                host_out[n].copy_(result[n], non_blocking=True)
                 if n in host_ro:
                     host_ro[n].copy_(res_out[n], non_blocking=True)
 

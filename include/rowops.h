@@ -133,6 +133,23 @@ rowops_status_t rowops_softmax_causal(const void* x, void* y, int64_t M, int64_t
                                       int64_t offset, rowops_dtype_t dtype, cudaStream_t stream);
 
 /*
+ * Row-wise sum and row-wise max [EX §2.2 Row-wise Sum, §2.3 Row-wise Max;
+ * KT "Triton Row Sum" for rows longer than one block]:
+ *   rowops_row_sum: out[i] = sum_j x[i, j]
+ *   rowops_row_max: out[i] = max_j x[i, j]   (a NaN in the row gives NaN)
+ * fp32 accumulation; out holds M fp32 results for either input dtype.
+ *
+ *   x, M, N, ld, dtype, stream   as for rowops_softmax.
+ *   out   device pointer to M floats, 4-byte aligned, not overlapping x's rows.
+ * Same kernel families as rowops_softmax (row pipeline, register row groups,
+ * looped CTA per row), reading every element once.
+ */
+rowops_status_t rowops_row_sum(const void* x, float* out, int64_t M, int64_t N, int64_t ld, rowops_dtype_t dtype,
+                               cudaStream_t stream);
+rowops_status_t rowops_row_max(const void* x, float* out, int64_t M, int64_t N, int64_t ld, rowops_dtype_t dtype,
+                               cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the library's device error word
  * on the current device. Kernels that wait on asynchronous copies (the TMA-fed
  * row pipeline behind rowops_softmax, rowops_layernorm_gelu and the RMSNorm
@@ -233,6 +250,28 @@ rowops_status_t rowops_online_softmax_noalloc(const void* x, void* y, int64_t M,
 rowops_status_t rowops_layernorm_gelu(const void* x, void* y, const void* w, const void* b,
                                       float eps, int64_t M, int64_t N, int64_t ld,
                                       rowops_dtype_t dtype, cudaStream_t stream);
+
+/*
+ * rowops_layernorm_gelu with the exact GELU [EX §3.4 gelu_exact]:
+ *   y_j = 0.5 z_j (1 + erf(z_j / sqrt(2))) = z_j Phi(z_j)
+ * (Phi the standard normal CDF), z_j as for rowops_layernorm_gelu. Same
+ * arguments, layouts, kernels and conventions.
+ */
+rowops_status_t rowops_layernorm_gelu_erf(const void* x, void* y, const void* w, const void* b, float eps,
+                                          int64_t M, int64_t N, int64_t ld, rowops_dtype_t dtype,
+                                          cudaStream_t stream);
+
+/*
+ * Elementwise GELU of n contiguous elements [EX §3.4 Approx Activation]:
+ *   approximate == 0: y = 0.5 x (1 + erf(x / sqrt(2)))             (exact)
+ *   approximate == 1: y = 0.5 x (1 + tanh(0.79788456 (x + 0.044715 x^3)))
+ *
+ *   x, y   device pointers to n elements of `dtype`; y may equal x, any other
+ *          overlap is rejected. n >= 0 (n == 0 is a no-op).
+ * fp32 arithmetic; bf16 results rounded to nearest even.
+ */
+rowops_status_t rowops_gelu(const void* x, void* y, int64_t n, int approximate, rowops_dtype_t dtype,
+                            cudaStream_t stream);
 
 /*
  * RMSNorm of every row [EX §4.2 RMSNorm]:

@@ -37,6 +37,13 @@ SOURCES = [
     "tma_rms_f32_residual.cu",
     "tma_rms_bf16_plain.cu",
     "tma_rms_bf16_residual.cu",
+    "reduce_f32.cu",
+    "reduce_bf16.cu",
+    "ln_gelu_erf_f32.cu",
+    "ln_gelu_erf_bf16.cu",
+    "tma_ln_gelu_erf_f32.cu",
+    "tma_ln_gelu_erf_bf16.cu",
+    "gelu.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -25,6 +25,34 @@ __device__ __forceinline__ float gelu_tanh_approx(float z) {
     return z * rcp_approx(1.f + ex2_approx(a));
 }
 
+// Exact GELU ["Triton Kernel 实现练习" §3.4]: 0.5 z (1 + erf(z / sqrt(2))).
+// erfc by Abramowitz & Stegun, Handbook of Mathematical Functions, 7.1.26
+// (Hastings' approximation): for x >= 0, erfc(x) = t (a1 + t (a2 + t (a3 + t (a4
+// + t a5)))) e^{-x^2} + eps, t = 1 / (1 + p x), |eps| <= 1.5e-7. With u = |z| /
+// sqrt(2) and q = erfc(u): 1 + erf(z / sqrt(2)) is 2 - q for z >= 0 and q for z
+// < 0, so the negative side needs no cancelling sum; the output error is at most
+// 0.5 |z| 1.5e-7 plus fp32 rounding (a general-purpose erf costs several times
+// as many instructions, and this kernel is bound by issue).
+__device__ __forceinline__ float gelu_erf(float z) {
+    constexpr float p = 0.3275911f, a1 = 0.254829592f, a2 = -0.284496736f, a3 = 1.421413741f,
+                    a4 = -1.453152027f, a5 = 1.061405429f;
+    const float u = fabsf(z) * 0.70710678118654752f;
+    const float t = rcp_approx(fmaf(p, u, 1.f));
+    float poly = fmaf(t, a5, a4);
+    poly = fmaf(t, poly, a3);
+    poly = fmaf(t, poly, a2);
+    poly = fmaf(t, poly, a1);
+    const float q = poly * t * ex2_approx(-(u * u) * kLog2eF);
+    return z >= 0.f ? z * fmaf(-0.5f, q, 1.f) : 0.5f * z * q;
+}
+
+// The GELU of the fused kernels: exact (ERF) or the tanh approximation.
+template <bool ERF>
+__device__ __forceinline__ float gelu_of(float z) {
+    if constexpr (ERF) return gelu_erf(z);
+    else return gelu_tanh_approx(z);
+}
+
 // Shared-memory staging of w, b as fp32 (absent -> 1, 0). `sw` and `sb` hold
 // round_up(N, 4) floats each.
 template <typename T>
@@ -53,7 +81,7 @@ __device__ __forceinline__ void stage_affine_pairs(const T* w, const T* b, int N
 
 // ALIGNED: every row starts on a 16-byte boundary (head = 0), so the columns of
 // a vector are a multiple of 4 and w, b are read from shared memory as float4.
-template <typename T, int TPR, int VPT, int BLOCK, bool ALIGNED>
+template <typename T, int TPR, int VPT, int BLOCK, bool ALIGNED, bool ERF = false>
 __global__ void __launch_bounds__(BLOCK)
     ln_gelu_reg_kernel(const T* x, T* y, const T* w, const T* b, float eps, int64_t M, int N,
                        int64_t ld) {
@@ -151,16 +179,16 @@ __global__ void __launch_bounds__(BLOCK)
                     for (int j = 0; j < V; j += 4) {
                         const float4 ww = *reinterpret_cast<const float4*>(sw + c0 + j);
                         const float4 bb = *reinterpret_cast<const float4*>(sb + c0 + j);
-                        o[j + 0] = gelu_tanh_approx(fmaf(fmaf(v[i][j + 0], rstd, shift), ww.x, bb.x));
-                        o[j + 1] = gelu_tanh_approx(fmaf(fmaf(v[i][j + 1], rstd, shift), ww.y, bb.y));
-                        o[j + 2] = gelu_tanh_approx(fmaf(fmaf(v[i][j + 2], rstd, shift), ww.z, bb.z));
-                        o[j + 3] = gelu_tanh_approx(fmaf(fmaf(v[i][j + 3], rstd, shift), ww.w, bb.w));
+                        o[j + 0] = gelu_of<ERF>(fmaf(fmaf(v[i][j + 0], rstd, shift), ww.x, bb.x));
+                        o[j + 1] = gelu_of<ERF>(fmaf(fmaf(v[i][j + 1], rstd, shift), ww.y, bb.y));
+                        o[j + 2] = gelu_of<ERF>(fmaf(fmaf(v[i][j + 2], rstd, shift), ww.z, bb.z));
+                        o[j + 3] = gelu_of<ERF>(fmaf(fmaf(v[i][j + 3], rstd, shift), ww.w, bb.w));
                     }
                 } else {
 #pragma unroll
                     for (int j = 0; j < V; ++j) {
                         const float2 wb = swb[affine_pair(c0 + j)];
-                        o[j] = gelu_tanh_approx(fmaf(fmaf(v[i][j], rstd, shift), wb.x, wb.y));
+                        o[j] = gelu_of<ERF>(fmaf(fmaf(v[i][j], rstd, shift), wb.x, wb.y));
                     }
                 }
                 st_stream16(yv + k * V, E::pack(o));
@@ -168,7 +196,7 @@ __global__ void __launch_bounds__(BLOCK)
         }
         if (has_ex) {
             const float2 wb = ALIGNED ? make_float2(sw[ecol], sb[ecol]) : swb[affine_pair(ecol)];
-            E::store(yr + ecol, gelu_tanh_approx(fmaf(fmaf(ex, rstd, shift), wb.x, wb.y)));
+            E::store(yr + ecol, gelu_of<ERF>(fmaf(fmaf(ex, rstd, shift), wb.x, wb.y)));
         }
     }
 }
@@ -179,7 +207,7 @@ __global__ void __launch_bounds__(BLOCK)
 // Pass 2 re-reads x and writes y; w and b come from global memory (L1/L2).
 // `scalar`: x and y rows differ in their offset modulo 16 bytes; one element
 // at a time.
-template <typename T, int BLOCK, int UNROLL>
+template <typename T, int BLOCK, int UNROLL, bool ERF = false>
 __global__ void __launch_bounds__(BLOCK)
     ln_gelu_looped_kernel(const T* x, T* y, const T* w, const T* b, float eps, int64_t M, int64_t N,
                           int64_t ld, bool scalar) {
@@ -244,7 +272,7 @@ __global__ void __launch_bounds__(BLOCK)
         auto affine_gelu = [&](float xv_, int64_t c) {
             const float wj = w ? E::load(w + c) : 1.f;
             const float bj = b ? E::load(b + c) : 0.f;
-            return gelu_tanh_approx(fmaf((xv_ - mean) * rstd, wj, bj));
+            return gelu_of<ERF>(fmaf((xv_ - mean) * rstd, wj, bj));
         };
         if (scalar)
             for (int64_t c = t; c < N; c += BLOCK) E::store(yr + c, affine_gelu(E::load(xr + c), c));

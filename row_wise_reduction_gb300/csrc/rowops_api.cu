@@ -504,9 +504,90 @@ rowops_status_t rowops_softmax_causal(const void* x, void* y, int64_t M, int64_t
     return finish(fn(x, y, M, N, ld, period, offset, cfg));
 }
 
+namespace {
+// Row sum (op 0) / row max (op 1): arguments checked by the callers.
+rowops_status_t reduce_dispatch(const void* x, float* out, int64_t M, int64_t N, int64_t ld, rowops_dtype_t dtype,
+                                int op, cudaStream_t stream) {
+    const Tuning tn = read_tuning();
+    LaunchCfg cfg;
+    rowops_status_t st = make_cfg(stream, tn, &cfg);
+    if (st != ROWOPS_OK) return st;
+    const int es = elem_bytes(dtype);
+    TmaChoice tc;
+    if ((tn.family == Family::Auto || tn.family == Family::Tma) &&
+        choose_tma(x, x, N, ld, es, tn, {8, 4, 2, 3, 1}, &tc)) {
+        const int nbuf = ring_buffers(N, es, 0, tn, cfg);
+        TmaReduceLaunch tf = dtype == ROWOPS_F32 ? reduce_tma_f32(tc.block_index, tc.vpt_index, tc.full, op)
+                                                 : reduce_tma_bf16(tc.block_index, tc.vpt_index, tc.full, op);
+        if (nbuf > 0 && tf) return finish(tf(x, out, M, N, ld, nbuf, cfg));
+    }
+    int tpr_index = 0, vpt = 0;
+    ReduceLaunch fn = nullptr;
+    if (tn.family != Family::Looped && choose_reg(N, es, tn, &tpr_index, &vpt))
+        fn = dtype == ROWOPS_F32 ? reduce_reg_f32(tpr_index, vpt, op) : reduce_reg_bf16(tpr_index, vpt, op);
+    if (!fn) fn = dtype == ROWOPS_F32 ? reduce_looped_f32(op) : reduce_looped_bf16(op);
+    return finish(fn(x, out, M, N, ld, cfg));
+}
+
+rowops_status_t check_reduce(const void* x, const float* out, int64_t M, int64_t N, int64_t ld, rowops_dtype_t dtype) {
+    rowops_status_t st = check_rows(x, x, M, N, ld, dtype);
+    if (st != ROWOPS_OK || M == 0) return st;
+    if (!out || !aligned(out, 4)) return ROWOPS_ERR_INVALID_VALUE;
+    // out (M floats) must not overlap the rows of x
+    const uintptr_t xa = reinterpret_cast<uintptr_t>(x), oa = reinterpret_cast<uintptr_t>(out);
+    const uintptr_t xspan = uintptr_t(((M - 1) * ld + N) * elem_bytes(dtype)), ospan = uintptr_t(M) * 4;
+    if (xa < oa + ospan && oa < xa + xspan) return ROWOPS_ERR_INVALID_VALUE;
+    return ROWOPS_OK;
+}
+}  // namespace
+
+rowops_status_t rowops_row_sum(const void* x, float* out, int64_t M, int64_t N, int64_t ld, rowops_dtype_t dtype,
+                               cudaStream_t stream) {
+    rowops_status_t st = check_reduce(x, out, M, N, ld, dtype);
+    if (st != ROWOPS_OK || M == 0) return st;
+    return reduce_dispatch(x, out, M, N, ld, dtype, 0, stream);
+}
+
+rowops_status_t rowops_row_max(const void* x, float* out, int64_t M, int64_t N, int64_t ld, rowops_dtype_t dtype,
+                               cudaStream_t stream) {
+    rowops_status_t st = check_reduce(x, out, M, N, ld, dtype);
+    if (st != ROWOPS_OK || M == 0) return st;
+    return reduce_dispatch(x, out, M, N, ld, dtype, 1, stream);
+}
+
+namespace {
+rowops_status_t ln_gelu_dispatch(const void* x, void* y, const void* w, const void* b, float eps, int64_t M,
+                                 int64_t N, int64_t ld, rowops_dtype_t dtype, cudaStream_t stream, bool erf);
+}  // namespace
+
 rowops_status_t rowops_layernorm_gelu(const void* x, void* y, const void* w, const void* b,
                                       float eps, int64_t M, int64_t N, int64_t ld,
                                       rowops_dtype_t dtype, cudaStream_t stream) {
+    return ln_gelu_dispatch(x, y, w, b, eps, M, N, ld, dtype, stream, false);
+}
+
+rowops_status_t rowops_layernorm_gelu_erf(const void* x, void* y, const void* w, const void* b, float eps,
+                                          int64_t M, int64_t N, int64_t ld, rowops_dtype_t dtype,
+                                          cudaStream_t stream) {
+    return ln_gelu_dispatch(x, y, w, b, eps, M, N, ld, dtype, stream, true);
+}
+
+rowops_status_t rowops_gelu(const void* x, void* y, int64_t n, int approximate, rowops_dtype_t dtype,
+                            cudaStream_t stream) {
+    if (!valid_dtype(dtype) || n < 0 || (approximate != 0 && approximate != 1)) return ROWOPS_ERR_INVALID_VALUE;
+    if (n == 0) return ROWOPS_OK;
+    rowops_status_t st = check_rows(x, y, 1, n, n, dtype);  // one row of n elements
+    if (st != ROWOPS_OK) return st;
+    const Tuning tn = read_tuning();
+    LaunchCfg cfg;
+    if ((st = make_cfg(stream, tn, &cfg)) != ROWOPS_OK) return st;
+    const GeluLaunch fn = dtype == ROWOPS_F32 ? gelu_f32(approximate == 0) : gelu_bf16(approximate == 0);
+    return finish(fn(x, y, n, cfg));
+}
+
+namespace {
+rowops_status_t ln_gelu_dispatch(const void* x, void* y, const void* w, const void* b, float eps, int64_t M,
+                                 int64_t N, int64_t ld, rowops_dtype_t dtype, cudaStream_t stream, bool erf) {
     rowops_status_t st = check_rows(x, y, M, N, ld, dtype);
     if (st != ROWOPS_OK) return st;
     if (!(eps >= 0.f) || eps == INFINITY) return ROWOPS_ERR_INVALID_VALUE;
@@ -522,7 +603,8 @@ rowops_status_t rowops_layernorm_gelu(const void* x, void* y, const void* w, con
         const int tpr = kTmaBlocks[tc.block_index], vpt = kTmaVpts[tc.vpt_index];
         const int nbuf = ring_buffers(N, es, tma_affine_smem(tpr, vpt, es, tc.full, N), tn, cfg);
         if (nbuf > 0) {
-            const TmaLnGeluLookup lookup = dtype == ROWOPS_F32 ? ln_gelu_tma_f32 : ln_gelu_tma_bf16;
+            const TmaLnGeluLookup lookup = dtype == ROWOPS_F32 ? (erf ? ln_gelu_erf_tma_f32 : ln_gelu_tma_f32)
+                                                               : (erf ? ln_gelu_erf_tma_bf16 : ln_gelu_tma_bf16);
             const int rows = choose_ln_rows(lookup, tpr, vpt, tc.full, N, nbuf, tn, cfg);
             const TmaLnGeluKernel k = lookup(tpr, vpt, rows, tc.full);
             if (k.launch) return finish(k.launch(x, y, w, b, eps, M, N, ld, nbuf, cfg));
@@ -534,11 +616,15 @@ rowops_status_t rowops_layernorm_gelu(const void* x, void* y, const void* w, con
     const bool smem_ok = ln_gelu_smem_bytes(N) + 256 <= size_t(cfg.max_smem_optin);
     if (tn.family != Family::Looped && smem_ok && same_phase(x, y) && choose_reg(N, es, tn, &tpr_index, &vpt)) {
         const bool al = rows_aligned(x, y, ld, es);
-        fn = dtype == ROWOPS_F32 ? ln_gelu_reg_f32(tpr_index, vpt, al) : ln_gelu_reg_bf16(tpr_index, vpt, al);
+        fn = dtype == ROWOPS_F32 ? (erf ? ln_gelu_erf_reg_f32 : ln_gelu_reg_f32)(tpr_index, vpt, al)
+                                 : (erf ? ln_gelu_erf_reg_bf16 : ln_gelu_reg_bf16)(tpr_index, vpt, al);
     }
-    if (!fn) fn = dtype == ROWOPS_F32 ? ln_gelu_looped_f32() : ln_gelu_looped_bf16();
+    if (!fn)
+        fn = dtype == ROWOPS_F32 ? (erf ? ln_gelu_erf_looped_f32 : ln_gelu_looped_f32)()
+                                 : (erf ? ln_gelu_erf_looped_bf16 : ln_gelu_looped_bf16)();
     return finish(fn(x, y, w, b, eps, M, N, ld, cfg));
 }
+}  // namespace
 
 rowops_status_t rowops_rmsnorm(const void* x, void* y, const void* w, float eps, int64_t M, int64_t N, int64_t ld,
                                rowops_dtype_t dtype, cudaStream_t stream) {

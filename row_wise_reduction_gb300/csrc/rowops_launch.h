@@ -104,6 +104,9 @@ struct TmaLnGeluKernel {
 };
 TmaLnGeluKernel ln_gelu_tma_f32(int tpr, int vpt, int rows, bool full);
 TmaLnGeluKernel ln_gelu_tma_bf16(int tpr, int vpt, int rows, bool full);
+// the same with the exact (erf) GELU
+TmaLnGeluKernel ln_gelu_erf_tma_f32(int tpr, int vpt, int rows, bool full);
+TmaLnGeluKernel ln_gelu_erf_tma_bf16(int tpr, int vpt, int rows, bool full);
 
 // RMSNorm / fused residual + RMSNorm: r, ro are the residual input and output
 // (NULL in the plain form).
@@ -142,6 +145,23 @@ inline size_t rms_tma_stage_smem(int block, int vpt, int es, bool full) {
     return size_t(vpt) * block * (16 / es) * 4 + (full ? 0 : 64);
 }
 
+// Elementwise GELU on n contiguous elements (erf: exact, else tanh approximation).
+using GeluLaunch = cudaError_t (*)(const void* x, void* y, int64_t n, const LaunchCfg& cfg);
+GeluLaunch gelu_f32(bool erf);
+GeluLaunch gelu_bf16(bool erf);
+
+// Row sum / row max (op 0 / 1): fp32 results, one per row.
+using ReduceLaunch = cudaError_t (*)(const void* x, float* out, int64_t M, int64_t N, int64_t ld,
+                                     const LaunchCfg& cfg);
+using TmaReduceLaunch = cudaError_t (*)(const void* x, float* out, int64_t M, int64_t N, int64_t ld, int nbuf,
+                                        const LaunchCfg& cfg);
+TmaReduceLaunch reduce_tma_f32(int block_index, int vpt_index, bool full, int op);
+TmaReduceLaunch reduce_tma_bf16(int block_index, int vpt_index, bool full, int op);
+ReduceLaunch reduce_reg_f32(int tpr_index, int vpt, int op);
+ReduceLaunch reduce_reg_bf16(int tpr_index, int vpt, int op);
+ReduceLaunch reduce_looped_f32(int op);
+ReduceLaunch reduce_looped_bf16(int op);
+
 // dynamic shared memory of the row-pipeline kernels
 inline size_t tma_row_bytes(int64_t N, int es) { return size_t((N * es + 127) / 128 * 128); }
 inline size_t tma_ring_smem(int64_t N, int es, int nbuf) { return kTmaRingHeader + size_t(nbuf) * tma_row_bytes(N, es); }
@@ -161,6 +181,10 @@ LnGeluLaunch ln_gelu_reg_f32(int tpr_index, int vpt, bool aligned);
 LnGeluLaunch ln_gelu_reg_bf16(int tpr_index, int vpt, bool aligned);
 LnGeluLaunch ln_gelu_looped_f32();
 LnGeluLaunch ln_gelu_looped_bf16();
+LnGeluLaunch ln_gelu_erf_reg_f32(int tpr_index, int vpt, bool aligned);
+LnGeluLaunch ln_gelu_erf_reg_bf16(int tpr_index, int vpt, bool aligned);
+LnGeluLaunch ln_gelu_erf_looped_f32();
+LnGeluLaunch ln_gelu_erf_looped_bf16();
 
 SplitLaunch split_softmax_f32();
 SplitLaunch split_softmax_bf16();

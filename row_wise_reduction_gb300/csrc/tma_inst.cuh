@@ -39,16 +39,16 @@ cudaError_t launch_softmax_tma_causal(const void* x, void* y, int64_t M, int64_t
 }
 
 // ROWS row groups per CTA share one staging of w, b; nbuf buffers per group.
-template <typename T, int TPR, int VPT, int ROWS, bool FULL>
+template <typename T, int TPR, int VPT, int ROWS, bool FULL, bool ERF = false>
 size_t ln_gelu_tma_smem(int64_t N, int nbuf) {
     return kRingHeader + size_t(ROWS) * nbuf * ring_row_bytes(N, Elem<T>::kBytes) +
            affine_stage_bytes<T, TPR, VPT, FULL>();
 }
 
-template <typename T, int TPR, int VPT, int ROWS, bool FULL>
+template <typename T, int TPR, int VPT, int ROWS, bool FULL, bool ERF = false>
 cudaError_t launch_ln_gelu_tma_rows(const void* x, void* y, const void* w, const void* b, float eps, int64_t M,
                                     int64_t N, int64_t ld, int nbuf, const LaunchCfg& cfg) {
-    auto kern = ln_gelu_tma_kernel<T, TPR, VPT, ROWS, FULL>;
+    auto kern = ln_gelu_tma_kernel<T, TPR, VPT, ROWS, FULL, ERF>;
     const size_t smem = ln_gelu_tma_smem<T, TPR, VPT, ROWS, FULL>(N, nbuf);
     cudaError_t e = allow_smem(reinterpret_cast<const void*>(kern), smem, cfg);
     if (e != cudaSuccess) return e;
@@ -63,9 +63,9 @@ cudaError_t launch_ln_gelu_tma_rows(const void* x, void* y, const void* w, const
     return cudaGetLastError();
 }
 
-template <typename T, int TPR, int VPT, int ROWS, bool FULL>
+template <typename T, int TPR, int VPT, int ROWS, bool FULL, bool ERF = false>
 int ctas_ln_gelu_tma_rows(int64_t N, int nbuf, const LaunchCfg& cfg) {
-    auto kern = ln_gelu_tma_kernel<T, TPR, VPT, ROWS, FULL>;
+    auto kern = ln_gelu_tma_kernel<T, TPR, VPT, ROWS, FULL, ERF>;
     const size_t smem = ln_gelu_tma_smem<T, TPR, VPT, ROWS, FULL>(N, nbuf);
     if (smem + 1024 > size_t(cfg.max_smem_optin)) return 0;  // 1 KB for the static reduction buffers
     if (allow_smem(reinterpret_cast<const void*>(kern), smem, cfg) != cudaSuccess) {
@@ -103,17 +103,18 @@ TmaSoftmaxLaunch softmax_tma_table(int block_index, int vpt_index, bool full) {
 // LayerNorm+GELU instantiations by (TPR, VPT, ROWS); none where TPR * ROWS
 // would exceed 512 threads with ROWS > 1 (at 1024 threads a CTA gets at most 64
 // registers per thread and these kernels spill).
-template <typename T, int P, int V, int R, bool F>
+template <typename T, int P, int V, int R, bool F, bool ERF>
 constexpr TmaLnGeluKernel ln_gelu_entry() {
     if constexpr (R == 1 || P * R <= 512)
-        return TmaLnGeluKernel{launch_ln_gelu_tma_rows<T, P, V, R, F>, ctas_ln_gelu_tma_rows<T, P, V, R, F>};
+        return TmaLnGeluKernel{launch_ln_gelu_tma_rows<T, P, V, R, F, ERF>, ctas_ln_gelu_tma_rows<T, P, V, R, F, ERF>};
     else
         return TmaLnGeluKernel{nullptr, nullptr};
 }
 #define ROWOPS_LN1(T, P, F) \
-    {ln_gelu_entry<T, P, 1, 1, F>(), ln_gelu_entry<T, P, 2, 1, F>(), ln_gelu_entry<T, P, 3, 1, F>(), \
-     ln_gelu_entry<T, P, 4, 1, F>(), ln_gelu_entry<T, P, 8, 1, F>()}
-#define ROWOPS_LN3(T, P, V, F) {ln_gelu_entry<T, P, V, 2, F>(), ln_gelu_entry<T, P, V, 4, F>(), ln_gelu_entry<T, P, V, 8, F>()}
+    {ln_gelu_entry<T, P, 1, 1, F, ERF>(), ln_gelu_entry<T, P, 2, 1, F, ERF>(), ln_gelu_entry<T, P, 3, 1, F, ERF>(), \
+     ln_gelu_entry<T, P, 4, 1, F, ERF>(), ln_gelu_entry<T, P, 8, 1, F, ERF>()}
+#define ROWOPS_LN3(T, P, V, F) \
+    {ln_gelu_entry<T, P, V, 2, F, ERF>(), ln_gelu_entry<T, P, V, 4, F, ERF>(), ln_gelu_entry<T, P, V, 8, F, ERF>()}
 #define ROWOPS_LN2(T, P, F) {ROWOPS_LN3(T, P, 2, F), ROWOPS_LN3(T, P, 4, F), ROWOPS_LN3(T, P, 8, F)}
 
 template <int N>
@@ -123,7 +124,8 @@ int index_of(const int (&a)[N], int v) {
     return -1;
 }
 
-template <typename T>
+// ERF: the exact GELU instead of the tanh approximation
+template <typename T, bool ERF = false>
 TmaLnGeluKernel ln_gelu_tma_lookup(int tpr, int vpt, int rows, bool full) {
     static const TmaLnGeluKernel one_f[kNumTmaBlocks][kNumTmaVpts] = {
         ROWOPS_LN1(T, 64, true), ROWOPS_LN1(T, 128, true), ROWOPS_LN1(T, 256, true), ROWOPS_LN1(T, 512, true)};

@@ -504,7 +504,7 @@ __host__ __device__ constexpr uint32_t affine_stage_bytes() {
     return tma_affine_bytes<T, TPR, VPT>() + (FULL ? 0u : kAffineExtraBytes);
 }
 
-template <typename T, int TPR, int VPT, int ROWS, bool FULL>
+template <typename T, int TPR, int VPT, int ROWS, bool FULL, bool ERF = false>
 __global__ void __launch_bounds__(TPR * ROWS)
     ln_gelu_tma_kernel(const T* x, T* y, const T* w, const T* b, float eps, int64_t M, int N, int64_t ld,
                        int nbuf, unsigned* err, unsigned long long wait_ns, int64_t stall_row) {
@@ -598,17 +598,17 @@ __global__ void __launch_bounds__(TPR * ROWS)
                 for (int h = 0; h < H; ++h) {
                     const float4 ww = sw4[(j * H + h) * TPR + t];
                     const float4 bb = sb4[(j * H + h) * TPR + t];
-                    o[4 * h + 0] = gelu_tanh_approx(fmaf(fmaf(v[j][4 * h + 0], rstd, shift), ww.x, bb.x));
-                    o[4 * h + 1] = gelu_tanh_approx(fmaf(fmaf(v[j][4 * h + 1], rstd, shift), ww.y, bb.y));
-                    o[4 * h + 2] = gelu_tanh_approx(fmaf(fmaf(v[j][4 * h + 2], rstd, shift), ww.z, bb.z));
-                    o[4 * h + 3] = gelu_tanh_approx(fmaf(fmaf(v[j][4 * h + 3], rstd, shift), ww.w, bb.w));
+                    o[4 * h + 0] = gelu_of<ERF>(fmaf(fmaf(v[j][4 * h + 0], rstd, shift), ww.x, bb.x));
+                    o[4 * h + 1] = gelu_of<ERF>(fmaf(fmaf(v[j][4 * h + 1], rstd, shift), ww.y, bb.y));
+                    o[4 * h + 2] = gelu_of<ERF>(fmaf(fmaf(v[j][4 * h + 2], rstd, shift), ww.z, bb.z));
+                    o[4 * h + 3] = gelu_of<ERF>(fmaf(fmaf(v[j][4 * h + 3], rstd, shift), ww.w, bb.w));
                 }
                 st_stream16(yb + size_t(k) * V, E::pack(o));
             }
         }
         if (has_ex) {
             const float2 wb = sxb[t];
-            E::store(yr + ecol, gelu_tanh_approx(fmaf(fmaf(ex, rstd, shift), wb.x, wb.y)));
+            E::store(yr + ecol, gelu_of<ERF>(fmaf(fmaf(ex, rstd, shift), wb.x, wb.y)));
         }
     }
 }

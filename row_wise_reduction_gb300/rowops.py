@@ -23,12 +23,16 @@ __all__ = [
     "library_path",
     "rowops_softmax",
     "rowops_softmax_causal",
+    "rowops_row_sum",
+    "rowops_row_max",
     "rowops_online_softmax",
     "rowops_online_softmax_workspace_bytes",
     "rowops_online_softmax_status",
     "rowops_online_softmax_noalloc",
     "rowops_device_status",
     "rowops_layernorm_gelu",
+    "rowops_layernorm_gelu_erf",
+    "rowops_gelu",
     "rowops_rmsnorm",
     "rowops_fused_residual_rmsnorm",
     "rowops_status_string",
@@ -95,8 +99,15 @@ def library() -> ctypes.CDLL:
         L.rowops_layernorm_gelu.restype = ctypes.c_int
         L.rowops_layernorm_gelu.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, _i64, _i64, _i64,
                                             ctypes.c_int, _vp]
+        for name in ("rowops_row_sum", "rowops_row_max"):
+            getattr(L, name).restype = ctypes.c_int
+            getattr(L, name).argtypes = [_vp, _vp, _i64, _i64, _i64, ctypes.c_int, _vp]
         L.rowops_softmax_causal.restype = ctypes.c_int
         L.rowops_softmax_causal.argtypes = [_vp, _vp, _i64, _i64, _i64, _i64, _i64, ctypes.c_int, _vp]
+        L.rowops_layernorm_gelu_erf.restype = ctypes.c_int
+        L.rowops_layernorm_gelu_erf.argtypes = L.rowops_layernorm_gelu.argtypes
+        L.rowops_gelu.restype = ctypes.c_int
+        L.rowops_gelu.argtypes = [_vp, _vp, _i64, ctypes.c_int, ctypes.c_int, _vp]
         L.rowops_rmsnorm.restype = ctypes.c_int
         L.rowops_rmsnorm.argtypes = [_vp, _vp, _vp, ctypes.c_float, _i64, _i64, _i64, ctypes.c_int, _vp]
         L.rowops_fused_residual_rmsnorm.restype = ctypes.c_int
@@ -247,6 +258,29 @@ def rowops_layernorm_gelu(
     return y
 
 
+def rowops_layernorm_gelu_erf(
+    x: torch.Tensor,
+    w: Optional[torch.Tensor] = None,
+    b: Optional[torch.Tensor] = None,
+    eps: float = 1e-5,
+    y: Optional[torch.Tensor] = None,
+    *,
+    stream=None,
+) -> torch.Tensor:
+    """Fused LayerNorm -> affine -> exact (erf) GELU of every row of ``x``."""
+    M, N, ld = _rows(x, "x")
+    y = _out_like(x, y)
+    for name, v in (("w", w), ("b", b)):
+        if v is not None:
+            if v.dtype != x.dtype or v.device != x.device or v.numel() != N or not v.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous CUDA tensor of N entries with x's dtype")
+    st = library().rowops_layernorm_gelu_erf(
+        x.data_ptr(), y.data_ptr(), w.data_ptr() if w is not None else None,
+        b.data_ptr() if b is not None else None, float(eps), M, N, ld, _dtype_code(x), _stream(stream))
+    _check("rowops_layernorm_gelu_erf", st)
+    return y
+
+
 def _weight(w: Optional[torch.Tensor], x: torch.Tensor, N: int, name: str = "w"):
     if w is None:
         return None
@@ -313,4 +347,43 @@ def rowops_softmax_causal(
     st = library().rowops_softmax_causal(x.data_ptr(), y.data_ptr(), M, N, ld, period, int(offset),
                                          _dtype_code(x), _stream(stream))
     _check("rowops_softmax_causal", st)
+    return y
+
+
+def _row_reduce(fn: str, x: torch.Tensor, out: Optional[torch.Tensor], stream) -> torch.Tensor:
+    M, N, ld = _rows(x, "x")
+    if out is None:
+        out = torch.empty(M, dtype=torch.float32, device=x.device)
+    elif out.dtype != torch.float32 or out.numel() != M or not out.is_contiguous() or out.device != x.device:
+        raise ValueError("out must be a contiguous float32 CUDA tensor of M entries")
+    st = getattr(library(), fn)(x.data_ptr(), out.data_ptr(), M, N, ld, _dtype_code(x), _stream(stream))
+    _check(fn, st)
+    return out
+
+
+def rowops_row_sum(x: torch.Tensor, out: Optional[torch.Tensor] = None, *, stream=None) -> torch.Tensor:
+    """Sum of every row of ``x`` as float32 (M,)."""
+    return _row_reduce("rowops_row_sum", x, out, stream)
+
+
+def rowops_row_max(x: torch.Tensor, out: Optional[torch.Tensor] = None, *, stream=None) -> torch.Tensor:
+    """Maximum of every row of ``x`` as float32 (M,); NaN where a row holds a NaN."""
+    return _row_reduce("rowops_row_max", x, out, stream)
+
+
+def rowops_gelu(x: torch.Tensor, y: Optional[torch.Tensor] = None, approximate: str = "none", *,
+                stream=None) -> torch.Tensor:
+    """Elementwise GELU of a contiguous tensor: approximate "none" (exact, erf)
+    or "tanh"."""
+    if not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA tensor")
+    if approximate not in ("none", "tanh"):
+        raise ValueError('approximate must be "none" or "tanh"')
+    if y is None:
+        y = torch.empty_like(x)
+    elif y.shape != x.shape or y.dtype != x.dtype or y.device != x.device or not y.is_contiguous():
+        raise ValueError("y must be a contiguous tensor matching x")
+    st = library().rowops_gelu(x.data_ptr(), y.data_ptr(), x.numel(), 0 if approximate == "none" else 1,
+                               _dtype_code(x), _stream(stream))
+    _check("rowops_gelu", st)
     return y

@@ -26,7 +26,8 @@ class Workload:
     """One synthetic workload: an operation, a dtype, a shape and a value recipe."""
 
     name: str
-    op: str  # "softmax" | "softmax_causal" | "online_softmax" | "layernorm_gelu" | "rmsnorm" | "residual_rmsnorm"
+    op: str  # "softmax" | "softmax_causal" | "online_softmax" | "layernorm_gelu" | "layernorm_gelu_erf" |
+    #          "rmsnorm" | "residual_rmsnorm" | "row_sum" | "row_max"
     dtype: str  # "f32" | "bf16"
     M: int  # rows
     N: int  # columns (reduction length)
@@ -68,6 +69,13 @@ WORKLOADS: Dict[str, Workload] = {
                  residual=True),
         Workload("residual_rmsnorm_bf16_65536x8192", "residual_rmsnorm", "bf16", 65536, 8192, seed=8, affine=True,
                  residual=True),
+        # LayerNorm + exact (erf) GELU [Triton Kernel 实现练习 §3.4] on the LayerNorm+GELU inputs, and
+        # the row-wise sum / max [§2.2, §2.3] on the shape of the large LayerNorm+GELU input
+        Workload("layernorm_gelu_erf_f32_4096x768", "layernorm_gelu_erf", "f32", 4096, 768, seed=1, affine=True),
+        Workload("layernorm_gelu_erf_bf16_65536x8192", "layernorm_gelu_erf", "bf16", 65536, 8192, seed=4,
+                 affine=True),
+        Workload("row_sum_bf16_65536x8192", "row_sum", "bf16", 65536, 8192, seed=9),
+        Workload("row_max_bf16_65536x8192", "row_max", "bf16", 65536, 8192, seed=10),
     ]
 }
 

@@ -33,7 +33,8 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("rowops_softmax", "rowops_online_softmax", "rowops_layernorm_gelu",
               "rowops_online_softmax_workspace_bytes", "rowops_online_softmax_status", "rowops_status_string",
-              "rowops_rmsnorm", "rowops_fused_residual_rmsnorm", "rowops_softmax_causal"):
+              "rowops_rmsnorm", "rowops_fused_residual_rmsnorm", "rowops_softmax_causal", "rowops_row_sum",
+              "rowops_row_max", "rowops_layernorm_gelu_erf", "rowops_gelu"):
         assert n in names
 
 
@@ -95,6 +96,32 @@ def test_softmax_causal_validation(lib):
     assert f(X, X + 16, 4, 8, 8, 8, 0, F32, None) == INVALID  # partial overlap
     assert f(None, Y, 4, 8, 8, 8, 0, F32, None) == INVALID
     assert f(None, None, 0, 8, 8, 8, 0, F32, None) == OK
+
+
+@pytest.mark.parametrize("fn", ["rowops_row_sum", "rowops_row_max"])
+def test_row_reduction_validation(lib, fn):
+    f = getattr(lib, fn)
+    O = 0x700000
+    assert f(X, None, 4, 8, 8, F32, None) == INVALID  # null out
+    assert f(X, O + 2, 4, 8, 8, F32, None) == INVALID  # out not 4-byte aligned
+    assert f(X, X + 8, 4, 8, 8, F32, None) == INVALID  # out overlaps the rows of x
+    assert f(None, O, 4, 8, 8, F32, None) == INVALID
+    assert f(X, O, 4, 8, 7, F32, None) == INVALID  # ld < N
+    assert f(X + 1, O, 4, 8, 8, BF16, None) == INVALID  # x not 2-byte aligned
+    assert f(None, None, 0, 8, 8, F32, None) == OK
+
+
+def test_gelu_validation(lib):
+    f = lib.rowops_gelu
+    assert f(X, Y, 16, 2, F32, None) == INVALID  # approximate must be 0 or 1
+    assert f(X, Y, -1, 0, F32, None) == INVALID
+    assert f(X, X + 16, 16, 0, F32, None) == INVALID  # partial overlap
+    assert f(None, Y, 16, 1, BF16, None) == INVALID
+    assert f(X + 1, Y, 16, 1, BF16, None) == INVALID  # misaligned bf16
+    assert f(None, None, 0, 0, F32, None) == OK
+    g = lib.rowops_layernorm_gelu_erf
+    assert g(X, Y, None, None, -1.0, 4, 8, 8, F32, None) == INVALID
+    assert g(None, None, None, None, 1e-5, 0, 8, 8, F32, None) == OK
 
 
 def test_rmsnorm_validation(lib):
