@@ -63,6 +63,14 @@ def lib() -> ctypes.CDLL:
                                          _c_double_p]
             getattr(L, name).restype = ctypes.c_int
         L.oracle_rmsnorm_row.argtypes = [_c_double_p, _c_double_p, ctypes.c_double, _i64, _c_double_p]
+        L.oracle_gelu_tanh_grad.argtypes = [ctypes.c_double]
+        L.oracle_gelu_tanh_grad.restype = ctypes.c_double
+        L.oracle_layernorm_gelu_backward_row.argtypes = [_c_double_p, _c_double_p, _c_double_p, _c_double_p,
+                                                         ctypes.c_double, _i64, _c_double_p, _c_double_p, _c_double_p]
+        L.oracle_layernorm_gelu_backward_rows_f32.argtypes = [_c_float_p, _c_float_p, _c_float_p, _c_float_p,
+                                                              ctypes.c_double, _i64, _i64, _i64, _c_double_p,
+                                                              _c_double_p, _c_double_p]
+        L.oracle_layernorm_gelu_backward_rows_f32.restype = ctypes.c_int
         L.oracle_gelu_erf.argtypes = [ctypes.c_double]
         L.oracle_gelu_erf.restype = ctypes.c_double
         L.oracle_layernorm_gelu_erf_rows_f32.argtypes = [_c_float_p, _c_float_p, _c_float_p, ctypes.c_double, _i64,
@@ -348,3 +356,35 @@ def row_max(x) -> np.ndarray:
     if lib().oracle_row_max_rows_f32(_fp(xs), M, N, ld, _dp(out)) != 0:
         raise ValueError("oracle_row_max_rows_f32 rejected its arguments")
     return out
+
+
+def gelu_tanh_grad(z) -> np.ndarray:
+    """d/dz of the tanh-approximation GELU."""
+    f = lib().oracle_gelu_tanh_grad
+    zz = np.asarray(z, dtype=np.float64)
+    return np.vectorize(f, otypes=[np.float64])(zz) if zz.ndim else np.float64(f(float(zz)))
+
+
+def layernorm_gelu_backward_row(x, dy, w=None, b=None, eps: float = 1e-5):
+    """(dx, dw, db) of one row (dw, db for this row alone)."""
+    xr, gr = _f64_row(x), _f64_row(dy)
+    n = xr.size
+    dx, dw, db = np.empty(n), np.zeros(n), np.zeros(n)
+    lib().oracle_layernorm_gelu_backward_row(_dp(xr), _dp(gr), _dp(_opt64(w, n)), _dp(_opt64(b, n)), float(eps), n,
+                                             _dp(dx), _dp(dw), _dp(db))
+    return dx, dw, db
+
+
+def layernorm_gelu_backward(x, dy, w=None, b=None, eps: float = 1e-5):
+    """(dx (M, N), dw (N,), db (N,)) of the LayerNorm -> affine -> tanh-GELU backward."""
+    xs, M, N, ld = _rows(x)
+    gs, Mg, Ng, ldg = _rows(dy)
+    if (Mg, Ng) != (M, N):
+        raise ValueError("x and dy must have the same shape")
+    if ldg != ld:
+        xs, gs, ld = np.ascontiguousarray(xs), np.ascontiguousarray(gs), N
+    dx = np.empty((M, N)); dw = np.empty(N); db = np.empty(N)
+    if lib().oracle_layernorm_gelu_backward_rows_f32(_fp(xs), _fp(gs), _fp(_opt32(w, N)), _fp(_opt32(b, N)),
+                                                     float(eps), M, N, ld, _dp(dx), _dp(dw), _dp(db)) != 0:
+        raise ValueError("oracle_layernorm_gelu_backward_rows_f32 rejected its arguments")
+    return dx, dw, db

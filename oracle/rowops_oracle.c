@@ -170,6 +170,52 @@ double oracle_gelu_tanh(double z) {
 }
 
 /* ---------------------------------------------------------------------------
+ * d/dz of the tanh-approximation GELU g(z) = 0.5 z (1 + tanh(u)),
+ * u = k0 (z + k1 z^3):
+ *   g'(z) = 0.5 (1 + tanh(u)) + 0.5 z (1 - tanh(u)^2) k0 (1 + 3 k1 z^2)
+ * ------------------------------------------------------------------------- */
+double oracle_gelu_tanh_grad(double z) {
+    const double u = GELU_SQRT_2_OVER_PI * (z + GELU_CUBIC * z * z * z);
+    const double t = tanh(u);
+    return 0.5 * (1.0 + t) + 0.5 * z * (1.0 - t * t) * GELU_SQRT_2_OVER_PI * (1.0 + 3.0 * GELU_CUBIC * z * z);
+}
+
+/* ---------------------------------------------------------------------------
+ * Backward of LayerNorm -> affine -> tanh-GELU [FUS §三 FusedLayerNormGELU].
+ * The chain rule through the forward: xh = (x - mean) rstd, z = xh w + b,
+ * y = g(z). With dz = dy g'(z) and dxh = dz w, and since mean and rstd depend
+ * on the whole row (d mean / dx_j = 1/n, d rstd / dx_j = -rstd^3 (x_j - mean) / n
+ * for the biased variance),
+ *   dx_j = rstd (dxh_j - (1/n) sum_k dxh_k - xh_j (1/n) sum_k dxh_k xh_k)
+ *   dw_j += dz_j xh_j,  db_j += dz_j.
+ * ------------------------------------------------------------------------- */
+void oracle_layernorm_gelu_backward_row(const double* x, const double* dy, const double* w, const double* b,
+                                        double eps, int64_t n, double* dx, double* dw, double* db) {
+    double s = 0.0;
+    for (int64_t j = 0; j < n; ++j) s += x[j];
+    const double mean = s / (double)n;
+    double q = 0.0;
+    for (int64_t j = 0; j < n; ++j) q += (x[j] - mean) * (x[j] - mean);
+    const double rstd = 1.0 / sqrt(q / (double)n + eps);
+    double a1 = 0.0, a2 = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+        const double xh = (x[j] - mean) * rstd;
+        const double wj = w ? w[j] : 1.0, bj = b ? b[j] : 0.0;
+        const double dz = dy[j] * oracle_gelu_tanh_grad(xh * wj + bj);
+        dw[j] += dz * xh;
+        db[j] += dz;
+        const double dxh = dz * wj;
+        a1 += dxh;
+        a2 += dxh * xh;
+        dx[j] = dxh; /* finished below */
+    }
+    for (int64_t j = 0; j < n; ++j) {
+        const double xh = (x[j] - mean) * rstd;
+        dx[j] = rstd * (dx[j] - a1 / (double)n - xh * a2 / (double)n);
+    }
+}
+
+/* ---------------------------------------------------------------------------
  * Exact GELU [EX §3.4]: gelu_exact(z) = 0.5 * z * (1 + erf(z / sqrt(2))).
  * 1 + erf(u) is evaluated as erfc(-u) (libm, double): the same function, but
  * for z << 0 the sum 1 + erf cancels (at z = -8 it would be off by ~18%),
@@ -419,4 +465,32 @@ int oracle_row_max_rows_f32(const float* x, int64_t M, int64_t N, int64_t ld, do
         out[r] = m;
     }
     return 0;
+}
+
+int oracle_layernorm_gelu_backward_rows_f32(const float* x, const float* dy, const float* w, const float* b,
+                                            double eps, int64_t M, int64_t N, int64_t ld, double* dx, double* dw,
+                                            double* db) {
+    if (bad_shape(x, M, N, ld, dx) || !dy || !dw || !db) return -1;
+    double* xr = (double*)malloc(sizeof(double) * (size_t)N);
+    double* gr = (double*)malloc(sizeof(double) * (size_t)N);
+    double* wd = widen(w, N);
+    double* bd = widen(b, N);
+    int rc = 0;
+    if (!xr || !gr || (w && !wd) || (b && !bd)) {
+        rc = -1;
+    } else {
+        for (int64_t j = 0; j < N; ++j) dw[j] = db[j] = 0.0;
+        for (int64_t i = 0; i < M; ++i) {
+            for (int64_t j = 0; j < N; ++j) {
+                xr[j] = (double)x[i * ld + j];
+                gr[j] = (double)dy[i * ld + j];
+            }
+            oracle_layernorm_gelu_backward_row(xr, gr, wd, bd, eps, N, dx + i * N, dw, db);
+        }
+    }
+    free(xr);
+    free(gr);
+    free(wd);
+    free(bd);
+    return rc;
 }

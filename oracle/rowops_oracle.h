@@ -98,9 +98,26 @@ int oracle_layernorm_rows_f32(const float* x, const float* w, const float* b, do
                               int64_t N, int64_t ld, double* y);
 int oracle_rmsnorm_rows_f32(const float* x, const float* w, double eps, int64_t M, int64_t N, int64_t ld,
                             double* y);
+/* Derivative of the tanh-approximation GELU, d/dz of oracle_gelu_tanh. */
+double oracle_gelu_tanh_grad(double z);
+
+/* Backward of LayerNorm -> affine -> tanh-GELU [FUS §三 FusedLayerNormGELU]:
+ * the exact gradient of the forward (the page's own backward is a stated
+ * shortcut). Per row, with xh = (x - mean) rstd, z = xh w + b:
+ *   dz = dy gelu'(z);  dw += dz xh;  db += dz;  dxh = dz w
+ *   dx = rstd (dxh - mean(dxh) - xh mean(dxh xh))
+ * dx for the row; dw, db ACCUMULATED (callers zero them). w, b may be NULL. */
+void oracle_layernorm_gelu_backward_row(const double* x, const double* dy, const double* w, const double* b,
+                                        double eps, int64_t n, double* dx, double* dw, double* db);
+
 /* LayerNorm -> affine -> exact (erf) GELU [EX §3.4, §4.1]. */
 int oracle_layernorm_gelu_erf_rows_f32(const float* x, const float* w, const float* b, double eps, int64_t M,
                                        int64_t N, int64_t ld, double* y);
+/* The backward over M rows of x and dy (same stride): dx (M x N), dw and db
+ * (N each) summed over the rows. */
+int oracle_layernorm_gelu_backward_rows_f32(const float* x, const float* dy, const float* w, const float* b,
+                                            double eps, int64_t M, int64_t N, int64_t ld, double* dx, double* dw,
+                                            double* db);
 /* Row sum [EX §2.2]: out[i] = sum_j x[i, j], in double. */
 int oracle_row_sum_rows_f32(const float* x, int64_t M, int64_t N, int64_t ld, double* out);
 /* Row max [EX §2.3]: out[i] = max_j x[i, j]; -inf entries are padding; a NaN

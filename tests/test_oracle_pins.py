@@ -623,6 +623,98 @@ def test_row_max_special_rows(oracle):
     assert s[1] == -np.inf and np.isnan(s[2]) and s[3] == np.inf and np.all(np.isfinite(s[[0, 4, 5]]))
 
 
+# ----------------------------------------------------------------------------
+# LayerNorm -> affine -> tanh-GELU backward
+# ----------------------------------------------------------------------------
+def test_gelu_tanh_grad_values(oracle):
+    """g'(0) = 1/2 exactly; g' -> 1 and -> 0 in the tails; the derivative of
+    the oracle's own GELU by central differences."""
+    assert oracle.gelu_tanh_grad(0.0) == 0.5
+    assert abs(oracle.gelu_tanh_grad(12.0) - 1.0) < 1e-15 and abs(oracle.gelu_tanh_grad(-12.0)) < 1e-15
+    z = np.linspace(-6, 6, 241)
+    h = 1e-5
+    fd = (oracle.gelu_tanh(z + h) - oracle.gelu_tanh(z - h)) / (2 * h)
+    np.testing.assert_allclose(oracle.gelu_tanh_grad(z), fd, rtol=0, atol=1e-9)
+
+
+def test_layernorm_gelu_backward_matches_torch_autograd(oracle):
+    """torch's float64 autograd through gelu(layer_norm(x), approximate="tanh")
+    (which uses sqrt(2/pi) for 0.79788456: a 1e-9 relative difference)."""
+    rng = _rng(73)
+    M, N = 7, 129
+    x = rng.normal(0.5, 1.5, size=(M, N)).astype(np.float32)
+    dy = rng.normal(0, 1, size=(M, N)).astype(np.float32)
+    w = rng.uniform(0.5, 1.5, size=N).astype(np.float32)
+    b = rng.normal(0, 0.1, size=N).astype(np.float32)
+    dx, dw, db = oracle.layernorm_gelu_backward(x, dy, w, b, 1e-5)
+    xt = torch.tensor(x, dtype=torch.float64, requires_grad=True)
+    wt = torch.tensor(w, dtype=torch.float64, requires_grad=True)
+    bt = torch.tensor(b, dtype=torch.float64, requires_grad=True)
+    y = torch.nn.functional.gelu(torch.nn.functional.layer_norm(xt, (N,), wt, bt, 1e-5), approximate="tanh")
+    y.backward(torch.tensor(dy, dtype=torch.float64))
+    np.testing.assert_allclose(dx, xt.grad.numpy(), rtol=0, atol=1e-8)
+    np.testing.assert_allclose(dw, wt.grad.numpy(), rtol=0, atol=1e-8)
+    np.testing.assert_allclose(db, bt.grad.numpy(), rtol=0, atol=1e-8)
+
+
+def test_layernorm_gelu_backward_central_differences(oracle):
+    """Each gradient entry against (L(p + h) - L(p - h)) / 2h of L = sum dy * y
+    with the oracle's own forward: catches a dropped GELU derivative, a dropped
+    mean or variance term, or dw / db from the wrong factor."""
+    rng = _rng(79)
+    n = 9
+    x = rng.normal(0.3, 1.2, size=n)
+    dy = rng.normal(0, 1, size=n)
+    w = rng.uniform(0.5, 1.5, size=n)
+    b = rng.normal(0, 0.3, size=n)
+    dx, dw, db = oracle.layernorm_gelu_backward_row(x, dy, w, b, 1e-3)
+    loss = lambda xx, ww, bb: float(np.dot(dy, oracle.layernorm_gelu_row(xx, ww, bb, 1e-3)))
+    h = 1e-6
+    for j in range(n):
+        e = np.zeros(n)
+        e[j] = h
+        assert abs((loss(x + e, w, b) - loss(x - e, w, b)) / (2 * h) - dx[j]) < 1e-7
+        assert abs((loss(x, w + e, b) - loss(x, w - e, b)) / (2 * h) - dw[j]) < 1e-7
+        assert abs((loss(x, w, b + e) - loss(x, w, b - e)) / (2 * h) - db[j]) < 1e-7
+
+
+def test_layernorm_gelu_backward_projections(oracle):
+    """The normalised row ignores a shift of x: sum_j dx_j = 0; with eps = 0 it
+    also ignores a scale: sum_j dx_j xh_j = 0."""
+    rng = _rng(83)
+    for n in (5, 768, 4097):
+        x = rng.normal(1.0, 2.0, size=n)
+        dy = rng.normal(0, 1, size=n)
+        w = rng.uniform(0.5, 1.5, size=n)
+        b = rng.normal(0, 0.1, size=n)
+        dx, _, _ = oracle.layernorm_gelu_backward_row(x, dy, w, b, 1e-5)
+        assert abs(dx.sum()) < 1e-12 * n
+        dx0, _, _ = oracle.layernorm_gelu_backward_row(x, dy, w, b, 0.0)
+        xh = (x - x.mean()) / x.std()
+        assert abs(np.dot(dx0, xh)) < 1e-11 * n
+
+
+def test_layernorm_gelu_backward_batch_respects_ld(oracle):
+    """Batch form on rows padded with NaN to a stride ld > N (x and dy):
+    equal to the row form; dw, db summed over the rows."""
+    rng = _rng(89)
+    M, N, ld = 4, 37, 45
+    xs = np.full((M, ld), np.nan, dtype=np.float32)
+    gs = np.full((M, ld), np.nan, dtype=np.float32)
+    xs[:, :N] = rng.normal(0, 1, size=(M, N)).astype(np.float32)
+    gs[:, :N] = rng.normal(0, 1, size=(M, N)).astype(np.float32)
+    w = rng.uniform(0.5, 1.5, size=N).astype(np.float32)
+    dx, dw, db = oracle.layernorm_gelu_backward(xs[:, :N], gs[:, :N], w, None, 1e-5)
+    dw_sum, db_sum = np.zeros(N), np.zeros(N)
+    for i in range(M):
+        dxi, dwi, dbi = oracle.layernorm_gelu_backward_row(xs[i, :N], gs[i, :N], w, None, 1e-5)
+        np.testing.assert_array_equal(dx[i], dxi)
+        dw_sum += dwi
+        db_sum += dbi
+    np.testing.assert_allclose(dw, dw_sum, rtol=1e-15, atol=1e-15)
+    np.testing.assert_allclose(db, db_sum, rtol=1e-15, atol=1e-15)
+
+
 def test_batch_rejects_bad_shapes(oracle):
     with pytest.raises(ValueError):
         oracle.layernorm_gelu(np.zeros((2, 3), np.float32), np.ones(4, np.float32))
