@@ -44,7 +44,8 @@ METRIC = "row-kernel HBM GB/s (% of GB300 peak) for softmax and LayerNorm+GELU"
 STEP = ["softmax_bf16_causal_32768x4096", "online_softmax_f32_64x1048576", "layernorm_gelu_bf16_65536x8192"]
 DOMINANT = "layernorm_gelu_bf16_65536x8192"
 KERNELS_PER_CALL = {"softmax": 1, "softmax_causal": 1, "online_softmax": 2, "layernorm_gelu": 1,
-                    "layernorm_gelu_erf": 1, "rmsnorm": 1, "residual_rmsnorm": 1, "row_sum": 1, "row_max": 1}
+                    "layernorm_gelu_erf": 1, "rmsnorm": 1, "residual_rmsnorm": 1, "row_sum": 1, "row_max": 1,
+                    "layernorm_gelu_backward": 2}
 L2_BYTES = 129 * 10**6
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "ln_gelu_bf16_65536x8192.txt")
@@ -71,6 +72,8 @@ def alg_bytes(wl: workloads.Workload) -> int:
         return 2 * rows + (wl.N * es if wl.affine else 0)
     if wl.op == "softmax_causal":  # kept entries read, every output written
         return causal_alg_bytes(wl, wl.N)
+    if wl.op == "layernorm_gelu_backward":  # x, dy in; dx out; w, b in; fp32 dw, db out
+        return 3 * wl.M * wl.N * es + (2 * wl.N * es if wl.affine else 0) + 2 * wl.N * 4
     return rows
 
 
@@ -402,9 +405,10 @@ EXTRA = ["softmax_f32_1024x768", "layernorm_gelu_f32_4096x768", "layernorm_gelu_
          "layernorm_gelu_bf16_65536x4097", "rmsnorm_f32_4096x768", "residual_rmsnorm_f32_4096x768",
          "rmsnorm_bf16_65536x8192", "residual_rmsnorm_bf16_65536x8192", "softmax_causal_bf16_32768x4096",
          "layernorm_gelu_erf_f32_4096x768", "layernorm_gelu_erf_bf16_65536x8192", "row_sum_bf16_65536x8192",
-         "row_max_bf16_65536x8192"]
+         "row_max_bf16_65536x8192", "layernorm_gelu_backward_f32_4096x768",
+         "layernorm_gelu_backward_bf16_65536x8192"]
 SMALL = {"softmax_f32_1024x768", "layernorm_gelu_f32_4096x768", "rmsnorm_f32_4096x768",
-         "residual_rmsnorm_f32_4096x768", "layernorm_gelu_erf_f32_4096x768"}
+         "residual_rmsnorm_f32_4096x768", "layernorm_gelu_erf_f32_4096x768", "layernorm_gelu_backward_f32_4096x768"}
 
 
 def run_extras(dev, stream, iters=50):
@@ -421,9 +425,16 @@ def run_extras(dev, stream, iters=50):
         x, y = inp["x"], torch.empty_like(inp["x"])
         r_out = torch.empty_like(x) if wl.residual else None
         red = torch.empty(wl.M, dtype=torch.float32, device=dev)
+        if wl.grad:
+            dw = torch.empty(wl.N, dtype=torch.float32, device=dev)
+            db = torch.empty(wl.N, dtype=torch.float32, device=dev)
+            ws = torch.empty(ro.rowops_layernorm_gelu_backward_workspace_bytes(wl.M, wl.N, x.dtype),
+                             dtype=torch.uint8, device=dev)
 
         def call():
-            if wl.op == "softmax":
+            if wl.op == "layernorm_gelu_backward":
+                ro.rowops_layernorm_gelu_backward(x, inp["dy"], inp.get("w"), inp.get("b"), wl.eps, y, dw, db, ws)
+            elif wl.op == "softmax":
                 ro.rowops_softmax(x, y)
             elif wl.op == "row_sum":
                 ro.rowops_row_sum(x, red)
@@ -454,7 +465,7 @@ def run_extras(dev, stream, iters=50):
                "hot_rows_per_s": wl.M / hot}
         if alg_bytes(wl) > L2_BYTES:
             rec["frac_of_" + measured_peak()[1]] = rec["hot_gbs"] / measured_peak()[0]
-        if wl.op in ("rmsnorm", "residual_rmsnorm") and wl.M * wl.N > 10**6:
+        if wl.op in ("rmsnorm", "residual_rmsnorm", "layernorm_gelu_backward") and wl.M * wl.N > 10**6:
             rec["torch_eager"] = torch_eager_time(wl, inp, stream)
         if name in SMALL:
             cold = []
@@ -492,12 +503,24 @@ def run_extras(dev, stream, iters=50):
 
 
 def torch_eager_time(wl, inp, stream, iters=10):
-    """PyTorch eager on an RMSNorm workload, as context: F.rms_norm, and for the
-    fused form x + residual followed by F.rms_norm (two kernels at least)."""
+    """PyTorch eager as context: on an RMSNorm workload F.rms_norm, and for the
+    fused form x + residual followed by F.rms_norm (two kernels at least); on
+    the backward workload autograd's gradients of gelu(layer_norm(x)) (tanh)
+    for x, w, b from a retained graph (the backward kernels only)."""
     import torch.nn.functional as F
 
     x, w = inp["x"], inp.get("w")
-    if wl.op == "rmsnorm":
+    if wl.op == "layernorm_gelu_backward":
+        xg = x.detach().clone().requires_grad_(True)
+        wg = w.detach().clone().requires_grad_(True)
+        bg = inp["b"].detach().clone().requires_grad_(True)
+        out = F.gelu(F.layer_norm(xg, (wl.N,), wg, bg, wl.eps), approximate="tanh")
+        dy = inp["dy"]
+
+        def call():
+            return torch.autograd.grad(out, (xg, wg, bg), dy, retain_graph=True)
+        what = "torch.autograd.grad(gelu(layer_norm(x, w, b), 'tanh'), (x, w, b), dy)"
+    elif wl.op == "rmsnorm":
         def call():
             return F.rms_norm(x, (wl.N,), w, wl.eps)
         what = "F.rms_norm(x, (N,), w, eps)"

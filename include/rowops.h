@@ -262,6 +262,33 @@ rowops_status_t rowops_layernorm_gelu_erf(const void* x, void* y, const void* w,
                                           cudaStream_t stream);
 
 /*
+ * Backward of LayerNorm -> affine -> tanh-GELU (rowops_layernorm_gelu)
+ * [FUS §三 FusedLayerNormGELU; the page's own backward is a stated shortcut
+ * without the GELU derivative and LayerNorm's mean / variance terms; this is
+ * the exact gradient]. Per row, xh = (x - mean) rstd, z = xh w + b,
+ * dz = dy g'(z), dxh = dz w:
+ *   dx = rstd (dxh - mean(dxh) - xh mean(dxh xh))
+ *   dw = sum over the rows of dz xh,   db = sum over the rows of dz
+ * The row statistics are recomputed from x. dx in `dtype`; dw, db in fp32
+ * (sums over M rows), deterministic (per-CTA partials added in a fixed order).
+ *
+ *   x, dy    device pointers to M rows of `ld` elements (inputs).
+ *   w, b     as for rowops_layernorm_gelu (NULL: 1, 0).
+ *   dx       device pointer to M rows of `ld` elements; must not overlap x or dy.
+ *   dw, db   device pointers to N floats each, 4-byte aligned, apart.
+ *   workspace, workspace_bytes   device memory, 256-byte aligned, at least
+ *            rowops_layernorm_gelu_backward_workspace_bytes(M, N, dtype) bytes
+ *            (overwritten), apart from dw and db; calls sharing it must be
+ *            ordered on one stream.
+ * M == 0 writes zeros to dw and db.
+ */
+size_t rowops_layernorm_gelu_backward_workspace_bytes(int64_t M, int64_t N, rowops_dtype_t dtype);
+rowops_status_t rowops_layernorm_gelu_backward(const void* x, const void* dy, const void* w, const void* b,
+                                               float eps, void* dx, float* dw, float* db, int64_t M, int64_t N,
+                                               int64_t ld, rowops_dtype_t dtype, void* workspace,
+                                               size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Elementwise GELU of n contiguous elements [EX §3.4 Approx Activation]:
  *   approximate == 0: y = 0.5 x (1 + erf(x / sqrt(2)))             (exact)
  *   approximate == 1: y = 0.5 x (1 + tanh(0.79788456 (x + 0.044715 x^3)))

@@ -1,7 +1,7 @@
 """rowops: row-wise reduce-then-normalise CUDA kernels for GB300 (sm_103a).
 
 Stable and causal softmax, split-row online softmax, fused LayerNorm -> affine ->
-GELU (tanh or exact), RMSNorm and fused residual + RMSNorm, row sums and row
+GELU (tanh or exact) and its backward, RMSNorm and fused residual + RMSNorm, row sums and row
 maxima, exposed through the C ABI of
 ``librowops.so`` (``include/rowops.h``) and the thin ctypes binding in
 :mod:`row_wise_reduction_gb300.rowops`.
@@ -16,6 +16,8 @@ from .rowops import (  # noqa: F401
     rowops_fused_residual_rmsnorm,
     rowops_gelu,
     rowops_layernorm_gelu,
+    rowops_layernorm_gelu_backward,
+    rowops_layernorm_gelu_backward_workspace_bytes,
     rowops_layernorm_gelu_erf,
     rowops_online_softmax,
     rowops_online_softmax_status,

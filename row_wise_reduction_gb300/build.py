@@ -44,6 +44,7 @@ SOURCES = [
     "tma_ln_gelu_erf_f32.cu",
     "tma_ln_gelu_erf_bf16.cu",
     "gelu.cu",
+    "ln_gelu_bwd.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

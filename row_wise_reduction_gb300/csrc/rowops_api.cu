@@ -653,6 +653,96 @@ rowops_status_t rowops_fused_residual_rmsnorm(const void* x, const void* residua
     return rms_dispatch(x, residual, y, residual_out, w, eps, M, N, ld, dtype, stream);
 }
 
+size_t rowops_layernorm_gelu_backward_workspace_bytes(int64_t M, int64_t N, rowops_dtype_t dtype) {
+    if (!valid_dtype(dtype) || M < 0 || N < 1 || N >= (int64_t(1) << 31)) return 0;
+    // dw, db partials of at most kBwdMaxPartials CTAs
+    return size_t(kBwdMaxPartials) * 2 * size_t(N) * sizeof(float);
+}
+
+rowops_status_t rowops_layernorm_gelu_backward(const void* x, const void* dy, const void* w, const void* b,
+                                               float eps, void* dx, float* dw, float* db, int64_t M, int64_t N,
+                                               int64_t ld, rowops_dtype_t dtype, void* workspace,
+                                               size_t workspace_bytes, cudaStream_t stream) {
+    rowops_status_t st = check_rows(x, dx, M, N, ld, dtype);
+    if (st == ROWOPS_OK) st = check_rows(dy, dx, M, N, ld, dtype);
+    if (st != ROWOPS_OK) return st;
+    if (!(eps >= 0.f) || eps == INFINITY) return ROWOPS_ERR_INVALID_VALUE;
+    const int es = elem_bytes(dtype);
+    if ((w && !aligned(w, es)) || (b && !aligned(b, es))) return ROWOPS_ERR_INVALID_VALUE;
+    if (!dw || !db || !aligned(dw, 4) || !aligned(db, 4)) return ROWOPS_ERR_INVALID_VALUE;
+    {  // dw and db: N floats each, apart from each other
+        const uintptr_t a = reinterpret_cast<uintptr_t>(dw), c = reinterpret_cast<uintptr_t>(db);
+        const uintptr_t span = uintptr_t(N) * 4;
+        if (a < c + span && c < a + span) return ROWOPS_ERR_INVALID_VALUE;
+    }
+    if (!workspace || !aligned(workspace, 256) ||
+        workspace_bytes < rowops_layernorm_gelu_backward_workspace_bytes(M, N, dtype))
+        return ROWOPS_ERR_WORKSPACE;
+    {  // the partials are read while dw and db are written
+        const uintptr_t ws = reinterpret_cast<uintptr_t>(workspace), span = uintptr_t(N) * 4;
+        for (const float* o : {dw, db}) {
+            const uintptr_t a = reinterpret_cast<uintptr_t>(o);
+            if (a < ws + workspace_bytes && ws < a + span) return ROWOPS_ERR_INVALID_VALUE;
+        }
+    }
+    // dx is written while x and dy rows may still be read by other CTAs
+    if (M > 0 && (!rows_disjoint(dx, x, M, N, ld, es) || !rows_disjoint(dx, dy, M, N, ld, es)))
+        return ROWOPS_ERR_INVALID_VALUE;
+    const Tuning tn = read_tuning();
+    LaunchCfg cfg;
+    if ((st = make_cfg(stream, tn, &cfg)) != ROWOPS_OK) return st;
+    if (M == 0) {  // no rows: zero gradients
+        if (cudaMemsetAsync(dw, 0, size_t(N) * 4, stream) != cudaSuccess ||
+            cudaMemsetAsync(db, 0, size_t(N) * 4, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return ROWOPS_ERR_CUDA;
+        }
+        return ROWOPS_OK;
+    }
+    float* part = static_cast<float*>(workspace);
+    int grid = 0;
+    cudaError_t e = cudaErrorUnknown;
+    bool launched = false;
+    // full rows on the row pipeline: x, dy, dx 16-byte aligned rows, a tile with
+    // TPR * VPT = N / vec and at most 16 columns per thread
+    const int64_t vec = 16 / es;
+    const bool full = (tn.family == Family::Auto || tn.family == Family::Tma) && N % vec == 0 &&
+                      rows_aligned(x, dx, ld, es) && aligned(dy, 16);
+    if (full) {
+        const int64_t nvec = N / vec;
+        int ti = -1, vpt = 0;
+        for (int v : {2, 4, 3, 1}) {
+            if (v * vec > 16 || nvec % v) continue;
+            for (int i = 0; i < 4; ++i)
+                if (kBwdTpr[i] == nvec / v && (!tn.tpr || tn.tpr == kBwdTpr[i]) && (!tn.vpt || tn.vpt == v)) {
+                    ti = i;
+                    vpt = v;
+                }
+            if (ti >= 0) break;
+        }
+        if (ti >= 0) {
+            const size_t affine = size_t(2) * vpt * kBwdTpr[ti] * vec * 4;
+            int nbuf = tn.ring > 0 ? (tn.ring < 2 ? 2 : (tn.ring > kTmaMaxSlots ? kTmaMaxSlots : tn.ring)) : 2;
+            auto fits = [&](int nb) {
+                return size_t(kTmaRingHeader) + size_t(nb) * 2 * tma_row_bytes(N, es) + affine + 1024 <=
+                       size_t(cfg.max_smem_optin);
+            };
+            while (nbuf > 2 && !fits(nbuf)) --nbuf;
+            const TmaBwdLaunch f = dtype == ROWOPS_F32 ? ln_gelu_bwd_tma_f32(ti, vpt) : ln_gelu_bwd_tma_bf16(ti, vpt);
+            if (fits(nbuf) && f) {
+                e = f(x, dy, w, b, eps, dx, part, M, N, ld, nbuf, &grid, cfg);
+                launched = true;
+            }
+        }
+    }
+    if (!launched) {
+        const BwdLaunch f = dtype == ROWOPS_F32 ? ln_gelu_bwd_looped_f32() : ln_gelu_bwd_looped_bf16();
+        e = f(x, dy, w, b, eps, dx, part, M, N, ld, &grid, cfg);
+    }
+    if (e != cudaSuccess) return finish(e);
+    return finish(ln_gelu_bwd_reduce(part, grid, N, dw, db, cfg));
+}
+
 size_t rowops_online_softmax_workspace_bytes(int64_t M, int64_t N, rowops_dtype_t dtype) {
     if (!valid_dtype(dtype) || M < 0 || N < 1 || N >= (int64_t(1) << 31)) return 0;
     // the larger of the two forms' needs: the single-read form's header, M row

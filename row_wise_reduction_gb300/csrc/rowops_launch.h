@@ -150,6 +150,22 @@ using GeluLaunch = cudaError_t (*)(const void* x, void* y, int64_t n, const Laun
 GeluLaunch gelu_f32(bool erf);
 GeluLaunch gelu_bf16(bool erf);
 
+// LayerNorm -> affine -> tanh-GELU backward: per-CTA dw, db partials (2 N
+// floats each, at most kBwdMaxPartials CTAs) reduced by ln_gelu_bwd_reduce.
+constexpr int kBwdMaxPartials = 512;
+constexpr int kBwdTpr[] = {64, 128, 256, 512};
+using TmaBwdLaunch = cudaError_t (*)(const void* x, const void* dy, const void* w, const void* b, float eps,
+                                     void* dx, float* part, int64_t M, int64_t N, int64_t ld, int nbuf,
+                                     int* grid_out, const LaunchCfg& cfg);
+using BwdLaunch = cudaError_t (*)(const void* x, const void* dy, const void* w, const void* b, float eps, void* dx,
+                                  float* part, int64_t M, int64_t N, int64_t ld, int* grid_out,
+                                  const LaunchCfg& cfg);
+TmaBwdLaunch ln_gelu_bwd_tma_f32(int tpr_index, int vpt);
+TmaBwdLaunch ln_gelu_bwd_tma_bf16(int tpr_index, int vpt);
+BwdLaunch ln_gelu_bwd_looped_f32();
+BwdLaunch ln_gelu_bwd_looped_bf16();
+cudaError_t ln_gelu_bwd_reduce(const float* part, int P, int64_t N, float* dw, float* db, const LaunchCfg& cfg);
+
 // Row sum / row max (op 0 / 1): fp32 results, one per row.
 using ReduceLaunch = cudaError_t (*)(const void* x, float* out, int64_t M, int64_t N, int64_t ld,
                                      const LaunchCfg& cfg);

@@ -32,6 +32,8 @@ __all__ = [
     "rowops_device_status",
     "rowops_layernorm_gelu",
     "rowops_layernorm_gelu_erf",
+    "rowops_layernorm_gelu_backward",
+    "rowops_layernorm_gelu_backward_workspace_bytes",
     "rowops_gelu",
     "rowops_rmsnorm",
     "rowops_fused_residual_rmsnorm",
@@ -113,6 +115,11 @@ def library() -> ctypes.CDLL:
         L.rowops_fused_residual_rmsnorm.restype = ctypes.c_int
         L.rowops_fused_residual_rmsnorm.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _i64, _i64, _i64,
                                                     ctypes.c_int, _vp]
+        L.rowops_layernorm_gelu_backward_workspace_bytes.restype = ctypes.c_size_t
+        L.rowops_layernorm_gelu_backward_workspace_bytes.argtypes = [_i64, _i64, ctypes.c_int]
+        L.rowops_layernorm_gelu_backward.restype = ctypes.c_int
+        L.rowops_layernorm_gelu_backward.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _i64,
+                                                     _i64, _i64, ctypes.c_int, _vp, ctypes.c_size_t, _vp]
         _lib = L
     return _lib
 
@@ -279,6 +286,56 @@ def rowops_layernorm_gelu_erf(
         b.data_ptr() if b is not None else None, float(eps), M, N, ld, _dtype_code(x), _stream(stream))
     _check("rowops_layernorm_gelu_erf", st)
     return y
+
+
+def rowops_layernorm_gelu_backward_workspace_bytes(M: int, N: int, dtype: torch.dtype) -> int:
+    code = ROWOPS_F32 if dtype == torch.float32 else ROWOPS_BF16 if dtype == torch.bfloat16 else -1
+    return int(library().rowops_layernorm_gelu_backward_workspace_bytes(int(M), int(N), code))
+
+
+def _grad_out(t: Optional[torch.Tensor], N: int, device, name: str) -> torch.Tensor:
+    if t is None:
+        return torch.empty(N, dtype=torch.float32, device=device)
+    if t.dtype != torch.float32 or t.numel() != N or not t.is_contiguous() or t.device != device:
+        raise ValueError(f"{name} must be a contiguous float32 CUDA tensor of N entries")
+    return t
+
+
+def rowops_layernorm_gelu_backward(
+    x: torch.Tensor,
+    dy: torch.Tensor,
+    w: Optional[torch.Tensor] = None,
+    b: Optional[torch.Tensor] = None,
+    eps: float = 1e-5,
+    dx: Optional[torch.Tensor] = None,
+    dw: Optional[torch.Tensor] = None,
+    db: Optional[torch.Tensor] = None,
+    workspace: Optional[torch.Tensor] = None,
+    *,
+    stream=None,
+):
+    """Gradients of rowops_layernorm_gelu (tanh GELU) for the upstream gradient
+    ``dy``: returns ``(dx, dw, db)``, dx in x's dtype and layout, dw and db
+    float32 (N,). ``workspace``: a CUDA uint8 tensor of at least
+    ``rowops_layernorm_gelu_backward_workspace_bytes(M, N, dtype)`` bytes,
+    allocated per call when omitted."""
+    M, N, ld = _rows(x, "x")
+    _out_like(x, dy)  # same shape, dtype, device and row stride
+    dx = _out_like(x, dx)
+    pw, pb = _weight(w, x, N, "w"), _weight(b, x, N, "b")
+    dw = _grad_out(dw, N, x.device, "dw")
+    db = _grad_out(db, N, x.device, "db")
+    need = rowops_layernorm_gelu_backward_workspace_bytes(M, N, x.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
+    if not workspace.is_cuda:
+        raise ValueError("workspace must be a CUDA tensor")
+    nbytes = workspace.numel() * workspace.element_size()
+    st = library().rowops_layernorm_gelu_backward(
+        x.data_ptr(), dy.data_ptr(), pw, pb, float(eps), dx.data_ptr(), dw.data_ptr(), db.data_ptr(), M, N, ld,
+        _dtype_code(x), workspace.data_ptr(), nbytes, _stream(stream))
+    _check("rowops_layernorm_gelu_backward", st)
+    return dx, dw, db
 
 
 def _weight(w: Optional[torch.Tensor], x: torch.Tensor, N: int, name: str = "w"):

@@ -27,17 +27,18 @@ class Workload:
 
     name: str
     op: str  # "softmax" | "softmax_causal" | "online_softmax" | "layernorm_gelu" | "layernorm_gelu_erf" |
-    #          "rmsnorm" | "residual_rmsnorm" | "row_sum" | "row_max"
+    #          "layernorm_gelu_backward" | "rmsnorm" | "residual_rmsnorm" | "row_sum" | "row_max"
     dtype: str  # "f32" | "bf16"
     M: int  # rows
     N: int  # columns (reduction length)
-    seed: int  # seed of x; w, b and the residual use seed + 100, + 200 and + 300
+    seed: int  # seed of x; w, b, the residual and dy use seed + 100, + 200, + 300 and + 400
     x_std: float = 1.0  # x ~ N(0, x_std^2)
     causal: bool = False  # row r keeps columns c <= r mod N, the rest are -inf
     outlier_p: float = 0.0  # fraction of entries (Bernoulli per entry) set to outlier_value
     outlier_value: float = 30.0
     affine: bool = False  # w ~ U(0.5, 1.5), b ~ N(0, 0.1^2) (RMSNorm uses w only)
     residual: bool = False  # a second input of the same shape, ~ N(0, 1)
+    grad: bool = False  # an upstream gradient dy of the same shape, ~ N(0, 1)
     eps: float = 1e-5
 
     def with_shape(self, M: Optional[int] = None, N: Optional[int] = None) -> "Workload":
@@ -76,6 +77,12 @@ WORKLOADS: Dict[str, Workload] = {
                  affine=True),
         Workload("row_sum_bf16_65536x8192", "row_sum", "bf16", 65536, 8192, seed=9),
         Workload("row_max_bf16_65536x8192", "row_max", "bf16", 65536, 8192, seed=10),
+        # the backward of LayerNorm -> affine -> tanh-GELU [PyTorch 自定义 CUDA 算子与 Triton 编程
+        # §三 FusedLayerNormGELU] on the LayerNorm+GELU inputs, with dy ~ N(0, 1)
+        Workload("layernorm_gelu_backward_f32_4096x768", "layernorm_gelu_backward", "f32", 4096, 768, seed=1,
+                 affine=True, grad=True),
+        Workload("layernorm_gelu_backward_bf16_65536x8192", "layernorm_gelu_backward", "bf16", 65536, 8192,
+                 seed=4, affine=True, grad=True),
     ]
 }
 
@@ -104,7 +111,8 @@ def make_inputs(
 
     Returns ``{"x": (M, N) view, "x_storage": (M, ld) tensor}``, for affine
     workloads ``"w"`` and ``"b"`` of length N, and for residual workloads
-    ``"residual"`` / ``"residual_storage"`` laid out like x. Values are drawn in
+    ``"residual"`` / ``"residual_storage"`` laid out like x, for gradient
+    workloads ``"dy"`` / ``"dy_storage"`` likewise. Values are drawn in
     fp32 and rounded to the workload's dtype (round to nearest even). With
     ``ld > N`` the padding columns of each row hold NaN so that any read past
     column N-1 shows up in the result. ``row_ids`` (M integers) gives the row
@@ -141,12 +149,13 @@ def make_inputs(
         b = 0.1 * torch.randn((N,), generator=gb, device=device, dtype=torch.float32)
         out["w"] = w.to(dt)
         out["b"] = b.to(dt)
-    if wl.residual:
-        gr = _gen(device, wl.seed + 300)
-        r = torch.randn((M, N), generator=gr, device=device, dtype=torch.float32)
-        rs = torch.full((M, ld), float("nan"), device=device, dtype=dt)
-        rs[:, :N] = r.to(dt)
-        del r
-        out["residual"] = rs[:, :N]
-        out["residual_storage"] = rs
+    for key, on, sd in (("residual", wl.residual, 300), ("dy", wl.grad, 400)):
+        if on:
+            gr = _gen(device, wl.seed + sd)
+            r = torch.randn((M, N), generator=gr, device=device, dtype=torch.float32)
+            rs = torch.full((M, ld), float("nan"), device=device, dtype=dt)
+            rs[:, :N] = r.to(dt)
+            del r
+            out[key] = rs[:, :N]
+            out[key + "_storage"] = rs
     return out

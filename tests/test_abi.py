@@ -34,7 +34,8 @@ def test_header_declares_the_entry_points():
     for n in ("rowops_softmax", "rowops_online_softmax", "rowops_layernorm_gelu",
               "rowops_online_softmax_workspace_bytes", "rowops_online_softmax_status", "rowops_status_string",
               "rowops_rmsnorm", "rowops_fused_residual_rmsnorm", "rowops_softmax_causal", "rowops_row_sum",
-              "rowops_row_max", "rowops_layernorm_gelu_erf", "rowops_gelu"):
+              "rowops_row_max", "rowops_layernorm_gelu_erf", "rowops_gelu",
+              "rowops_layernorm_gelu_backward", "rowops_layernorm_gelu_backward_workspace_bytes"):
         assert n in names
 
 
@@ -180,6 +181,46 @@ def test_online_softmax_validation(lib):
     assert f(X, Y, 4, 1000, 999, F32, WS, need, 0, None) == INVALID
     assert f(None, None, 0, 1000, 1000, F32, None, 0, 0, None) == OK
     assert lib.rowops_online_softmax_status(None, None) == WORKSPACE
+
+
+def test_layernorm_gelu_backward_workspace_bytes(lib):
+    q = lib.rowops_layernorm_gelu_backward_workspace_bytes
+    # dw, db partials (N floats each) of at most 512 CTAs
+    assert q(4, 8, F32) == 512 * 2 * 8 * 4
+    assert q(1 << 20, 8192, BF16) == 512 * 2 * 8192 * 4
+    assert q(0, 3, F32) == 512 * 2 * 3 * 4
+    assert q(-1, 8, F32) == 0
+    assert q(4, 0, F32) == 0
+    assert q(4, 8, 9) == 0
+
+
+def test_layernorm_gelu_backward_validation(lib):
+    f = lib.rowops_layernorm_gelu_backward
+    DY, DW, DB, WS = 0x300000, 0x500000, 0x510000, 0x1000000
+    need = lib.rowops_layernorm_gelu_backward_workspace_bytes(4, 8, F32)
+
+    def args(x=X, dy=DY, w=None, b=None, eps=1e-5, dx=Y, dw=DW, db=DB, M=4, N=8, ld=8, dt=F32, ws=WS, nb=None):
+        return (x, dy, w, b, eps, dx, dw, db, M, N, ld, dt, ws, need if nb is None else nb, None)
+
+    assert f(*args(eps=-1.0)) == INVALID
+    assert f(*args(eps=float("inf"))) == INVALID
+    assert f(*args(eps=float("nan"))) == INVALID
+    assert f(*args(dw=None)) == INVALID
+    assert f(*args(db=DB + 2)) == INVALID  # db not 4-byte aligned
+    assert f(*args(db=DW)) == INVALID  # dw and db the same
+    assert f(*args(db=DW + 16)) == INVALID  # dw and db overlap
+    assert f(*args(ws=None)) == WORKSPACE
+    assert f(*args(ws=WS + 64)) == WORKSPACE  # not 256-byte aligned
+    assert f(*args(nb=need - 1)) == WORKSPACE
+    assert f(*args(dw=WS + 1024)) == INVALID  # dw inside the workspace
+    assert f(*args(dx=X)) == INVALID  # dx must not alias x
+    assert f(*args(dx=DY)) == INVALID  # nor dy
+    assert f(*args(dx=DY + 16)) == INVALID
+    assert f(*args(dy=None)) == INVALID
+    assert f(*args(w=X + 0x40001, dt=BF16)) == INVALID  # misaligned w
+    assert f(*args(b=X + 0x40001, dt=BF16)) == INVALID  # misaligned b
+    assert f(*args(ld=7)) == INVALID
+    assert f(*args(dt=5)) == INVALID
 
 
 def test_binding_has_no_fallback(monkeypatch, tmp_path):

@@ -15,6 +15,7 @@ import torch
 from row_wise_reduction_gb300 import (
     rowops_device_status,
     rowops_layernorm_gelu,
+    rowops_layernorm_gelu_backward,
     rowops_online_softmax,
     rowops_online_softmax_status,
     rowops_online_softmax_workspace_bytes,
@@ -125,3 +126,25 @@ def test_causal_softmax_wait_times_out(oracle, monkeypatch):
     y = rowops_softmax_causal(x, 4096, 0)
     assert rowops_device_status() == 0
     C.assert_softmax_close(C.to_f64(y), oracle.softmax_causal(gu.rows_f32(x), 4096, 0), "bf16")
+
+
+def test_layernorm_gelu_backward_wait_times_out(oracle, monkeypatch):
+    """The backward's ring (x and dy rows in one slot) gives up on the stalled
+    row, records the timeout, and the next call is correct."""
+    wl = workloads.Workload("timeout_ln_bwd", "layernorm_gelu_backward", "bf16", 1200, 8192, seed=4, affine=True,
+                            grad=True)
+    inp = gu.make_x(wl)
+    monkeypatch.setenv("ROWOPS_KERNEL", "tma")
+    monkeypatch.setenv("ROWOPS_WAIT_LIMIT_NS", LIMIT_NS)
+    monkeypatch.setenv("ROWOPS_TEST_STALL_ROW", "400")
+    rowops_layernorm_gelu_backward(inp["x"], inp["dy"], inp["w"], inp["b"], wl.eps)
+    assert rowops_device_status() == TIMEOUT
+    monkeypatch.delenv("ROWOPS_TEST_STALL_ROW")
+    dx, dw, db = rowops_layernorm_gelu_backward(inp["x"], inp["dy"], inp["w"], inp["b"], wl.eps)
+    assert rowops_device_status() == 0
+    rows = gu.sample_rows(wl.M, 8)
+    ref_dx, _, _ = oracle.layernorm_gelu_backward(gu.rows_f32(inp["x"], rows), gu.rows_f32(inp["dy"], rows),
+                                                  inp["w"].float().cpu().numpy(), inp["b"].float().cpu().numpy(),
+                                                  wl.eps)
+    got = C.to_f64(dx[torch.as_tensor(rows, device=dx.device)])
+    assert np.all(np.abs(got - ref_dx) <= C.bf16_ulp(ref_dx) + 1e-3)
