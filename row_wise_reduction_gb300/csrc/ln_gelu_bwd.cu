@@ -6,11 +6,13 @@
 //   dw = sum over rows of dz xh,  db = sum over rows of dz
 // The row statistics are recomputed from x (nothing is saved by the forward).
 //
-// Full rows: the row pipeline with the x and dy rows in each ring slot, three
-// group reductions per row, and dw, db partials of each thread's columns kept in
-// registers across the CTA's rows; other layouts: a looped CTA-per-row kernel
-// that accumulates its partials in the workspace. A last kernel adds the
-// per-CTA partials in a fixed order (deterministic dw, db).
+// Full rows: the row pipeline with the x and dy rows in each ring slot and the
+// dw, db partials of each thread's columns kept in registers across the CTA's
+// rows; where the ring holds at least four slots, three rows at different
+// stages share one group reduction per row (ln_gelu_bwd_pipe_kernel), else one
+// row at a time with three reductions (ln_gelu_bwd_tma_kernel). Other layouts:
+// a looped CTA-per-row kernel that accumulates its partials in the workspace.
+// A last kernel adds the per-CTA partials in a fixed order (deterministic dw, db).
 #include "rowops_launch.h"
 #include "tma_inst.cuh"
 #include "tma_rms_kernels.cuh"
@@ -20,16 +22,237 @@ namespace rowops {
 // d/dz of gelu_tanh_approx. With e = 2^a = exp(-2u) (a as in the forward) and
 // s = 1 / (1 + e) = 0.5 (1 + tanh u): 1 - tanh(u)^2 = 4 s (1 - s) and
 // s (1 - s) = e s^2 (no cancellation), so
-//   g'(z) = s + 2 z e s^2 du/dz,   du/dz = k0 (1 + 3 k1 z^2).
+//   g'(z) = s + (e s) s (2 z du/dz),   du/dz = k0 (1 + 3 k1 z^2).
+// a is clamped at 126: below z ~ -10 e would overflow and (e s) s turn into
+// inf * 0; with the clamp g' comes out ~1e-36 there, the true value being smaller.
 __device__ __forceinline__ float gelu_tanh_grad(float z) {
-    constexpr float k0 = 0.79788456f, k1 = 0.044715f;
     constexpr float c0 = float(-2.0 * 0.79788456 * kLog2e);
     constexpr float c1 = float(-2.0 * 0.79788456 * 0.044715 * kLog2e);
+    constexpr float d0 = float(2.0 * 0.79788456), d1 = float(2.0 * 3.0 * 0.79788456 * 0.044715);
     const float z2 = z * z;
-    const float e = ex2_approx(fmaf(c1, z2, c0) * z);
+    const float e = ex2_approx(fminf(fmaf(c1, z2, c0) * z, 126.f));
     const float s = rcp_approx(1.f + e);
-    const float du = k0 * fmaf(3.f * k1, z2, 1.f);
-    return fmaf(2.f * z * e * s * s, du, s);
+    return fmaf((e * s) * s, z * fmaf(d1, z2, d0), s);
+}
+
+// Sums over the TPR threads of a row group of s and of v[0..3], with one named
+// barrier. In a warp s is added by a butterfly and v by a reduce-scatter: the
+// offsets 16 and 8 split the four values between the lane halves and quarters,
+// 4, 2 and 1 finish, so lane l holds the warp's sum of v[l / 8]. Lanes 0, 8,
+// 16 and 24 store those (lane 0 also s); after the barrier lane l loads the
+// sums of warp l mod W and a butterfly over W lanes adds the warps.
+template <int TPR>
+__device__ __forceinline__ void row_reduce_sum5(float& s, float (&v)[4], float (*red)[8], int bar_id, int& fail) {
+    constexpr int W = TPR / 32;
+    const int lane = threadIdx.x & 31;
+    const bool h16 = lane & 16, h8 = lane & 8;
+    float k0 = h16 ? v[2] : v[0], k1 = h16 ? v[3] : v[1];
+    k0 += __shfl_xor_sync(0xffffffffu, h16 ? v[0] : v[2], 16);
+    k1 += __shfl_xor_sync(0xffffffffu, h16 ? v[1] : v[3], 16);
+    float k = h8 ? k1 : k0;
+    k += __shfl_xor_sync(0xffffffffu, h8 ? k0 : k1, 8);
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) k += __shfl_xor_sync(0xffffffffu, k, o);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    const int w = (threadIdx.x % TPR) >> 5;
+    if ((lane & 7) == 0) red[w][lane >> 3] = k;
+    if (lane == 0) red[w][4] = s;
+    fail = group_bar_or(bar_id, TPR, fail);
+    const float4 r = *reinterpret_cast<const float4*>(red[lane % W]);
+    float o5[5] = {r.x, r.y, r.z, r.w, red[lane % W][4]};
+#pragma unroll
+    for (int o = W / 2; o > 0; o >>= 1)
+#pragma unroll
+        for (int q = 0; q < 5; ++q) o5[q] += __shfl_xor_sync(0xffffffffu, o5[q], o);
+    v[0] = o5[0];
+    v[1] = o5[1];
+    v[2] = o5[2];
+    v[3] = o5[3];
+    s = o5[4];
+}
+
+// gelu_tanh_grad of two values with packed fp32 pairs.
+__device__ __forceinline__ float2 gelu_tanh_grad2(float2 z) {
+    constexpr float c0 = float(-2.0 * 0.79788456 * kLog2e);
+    constexpr float c1 = float(-2.0 * 0.79788456 * 0.044715 * kLog2e);
+    constexpr float d0 = float(2.0 * 0.79788456), d1 = float(2.0 * 3.0 * 0.79788456 * 0.044715);
+    const float2 z2 = f2_mul(z, z);
+    const float2 a = f2_mul(f2_fma(f2(c1), z2, f2(c0)), z);
+    float2 e = make_float2(ex2_approx(fminf(a.x, 126.f)), ex2_approx(fminf(a.y, 126.f)));
+    const float2 e1 = f2_add(e, f2(1.f));
+    const float2 sg = make_float2(rcp_approx(e1.x), rcp_approx(e1.y));
+    e = f2_mul(f2_mul(e, sg), sg);
+    return f2_fma(e, f2_mul(f2_fma(f2(d1), z2, f2(d0)), z), sg);
+}
+
+// Full rows on a row pipeline of four stages, one row group (TPR threads) per
+// CTA, one barrier per row. At step k the group
+//   C: writes dx of row k-3 (xh, dxh kept in registers from its stage A),
+//   A: reads x, dy of row k-2 and forms xh, dz, dxh, the dw, db partials and
+//      the sums of dxh and dxh xh,
+//   Q: turns its own shifted sums of row k-1 into sum (x - mean)^2 and
+//      sum (x - mean) over its columns (no element is read again),
+//   S: waits for row k and sums x - c and (x - c)^2 over its n_t columns,
+//      c the first of them (so the terms of Q cancel at most ~2 n_t-fold:
+//      c itself contributes (c - mean)^2 to Q),
+// and one reduction adds sum x, the two sums of Q and the two of A over the
+// group. The variance of the centred row then gets the residual correction of
+// the fp32 mean, as in the forward. Rows k-2 .. k stay in the ring, the slot of
+// row k-2 is refilled after the barrier: nbuf - 3 rows are in flight beyond the
+// ones being worked on. Elementwise arithmetic runs on packed fp32 pairs.
+template <typename T, int TPR, int VPT>
+__global__ void __launch_bounds__(TPR)
+    ln_gelu_bwd_pipe_kernel(const T* x, const T* dy, const T* w, const T* b, float eps, T* dx, float* part,
+                            int64_t M, int N, int64_t ld, int nbuf, unsigned* err, unsigned long long wait_ns,
+                            int64_t stall_row) {
+    using E = Elem<T>;
+    constexpr int V = E::kVec, H = V / 4, P = V / 2;
+    constexpr float kNt = float(VPT * V);  // columns of a thread
+    static_assert(TPR % 64 == 0, "row groups of at least two warps");
+    extern __shared__ __align__(128) char smem[];
+    __shared__ __align__(16) float red[2][TPR / 32][8];
+    const GroupPipe p = make_group<TPR, 1>(smem, N, E::kBytes, nbuf, 1, 2);
+    const int t = threadIdx.x;
+    char* affine = smem + kRingHeader + size_t(nbuf) * p.ring.row_bytes;
+    const float4* sw4 = reinterpret_cast<const float4*>(affine);
+    const float4* sb4 = sw4 + VPT * H * TPR;
+    const T* const src[2] = {x, dy};
+    start_rows<T, true, 1, 2>(smem, p, src, M, N, ld, stall_row);
+    stage_affine_thread_major<T, TPR, VPT>(w, b, 0, N / V, reinterpret_cast<float4*>(affine),
+                                           reinterpret_cast<float4*>(affine) + VPT * H * TPR);
+    __syncthreads();
+    const uint32_t gstride = p.ring.row_bytes / 2;  // the dy row's place in a slot
+    const float fN = float(N);
+    const int64_t n = p.first < M ? (M - 1 - p.first) / p.stride + 1 : 0;  // rows of this CTA
+    float2 aw[VPT][P], ab[VPT][P];   // dw, db partials of this thread's columns
+    float2 xh[VPT][P], dxh[VPT][P];  // of the row between its stages A and C
+#pragma unroll
+    for (int j = 0; j < VPT; ++j)
+#pragma unroll
+        for (int q = 0; q < P; ++q) aw[j][q] = ab[j][q] = xh[j][q] = dxh[j][q] = f2(0.f);
+    float c_q = 0.f, s_q = 0.f, q_q = 0.f, mean_q = 0.f;  // stage Q's row: shift, shifted sums, mean
+    float mean_a = 0.f, rstd_a = 0.f, shift_a = 0.f;      // stage A's row
+    float rstd_c = 0.f, m1_c = 0.f, m2_c = 0.f;           // stage C's row (-m1, -m2 times rstd)
+
+    for (int64_t k = 0;; ++k) {
+        if (k >= 3) {  // C: dx of row k-3
+            T* dxr = dx + (p.first + (k - 3) * p.stride) * ld;
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                float o[V];
+#pragma unroll
+                for (int q = 0; q < P; ++q) {
+                    const float2 r = f2_fma(f2(rstd_c), dxh[j][q], f2_fma(xh[j][q], f2(m2_c), f2(m1_c)));
+                    o[2 * q] = r.x;
+                    o[2 * q + 1] = r.y;
+                }
+                st_stream16(dxr + size_t(t + j * TPR) * V, E::pack(o));
+            }
+        }
+        if (k == n + 2) break;
+        float sv[4] = {0.f, 0.f, 0.f, 0.f};  // Q: sum (x - mean)^2, sum (x - mean); A: sum dxh, sum dxh xh
+        float s1 = 0.f;                      // S: sum x
+        if (k >= 2 && k - 2 < n) {           // A: row k-2
+            const char* sb = p.ring.slot(int((k - 2) % nbuf));
+            float2 a1 = f2(0.f), a2 = f2(0.f);
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                float xv[V], gv[V];
+                E::unpack(lds16(sb + size_t(t + j * TPR) * 16), xv);
+                E::unpack(lds16(sb + gstride + size_t(t + j * TPR) * 16), gv);
+#pragma unroll
+                for (int h = 0; h < H; ++h) {
+                    const float4 ww = sw4[(j * H + h) * TPR + t];
+                    const float4 bb = sb4[(j * H + h) * TPR + t];
+                    const float2 wv[2] = {make_float2(ww.x, ww.y), make_float2(ww.z, ww.w)};
+                    const float2 bv[2] = {make_float2(bb.x, bb.y), make_float2(bb.z, bb.w)};
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        const int q = 2 * h + c;
+                        const float2 xq = make_float2(xv[2 * q], xv[2 * q + 1]);
+                        const float2 gq = make_float2(gv[2 * q], gv[2 * q + 1]);
+                        const float2 xhv = f2_fma(f2_add(xq, f2(-mean_a)), f2(rstd_a), f2(shift_a));
+                        const float2 dz = f2_mul(gq, gelu_tanh_grad2(f2_fma(xhv, wv[c], bv[c])));
+                        aw[j][q] = f2_fma(dz, xhv, aw[j][q]);
+                        ab[j][q] = f2_add(ab[j][q], dz);
+                        const float2 d = f2_mul(dz, wv[c]);
+                        a1 = f2_add(a1, d);
+                        a2 = f2_fma(d, xhv, a2);
+                        xh[j][q] = xhv;
+                        dxh[j][q] = d;
+                    }
+                }
+            }
+            sv[2] = a1.x + a1.y;
+            sv[3] = a2.x + a2.y;
+        }
+        if (k >= 1 && k - 1 < n) {  // Q: row k-1, from this thread's sums around c
+            const float d = c_q - mean_q;
+            sv[0] = fmaf(d, fmaf(kNt, d, 2.f * s_q), q_q);  // sum (x - c + d)^2
+            sv[1] = fmaf(kNt, d, s_q);                      // sum (x - c + d)
+        }
+        int fail = 0;
+        if (k < n) {  // S: row k
+            const int s = int(k % nbuf);
+            fail = !mbar_wait(p.ring.bar + s, uint32_t((k / nbuf) & 1), wait_ns);
+            const char* ss = p.ring.slot(s);
+            float2 s2 = f2(0.f), q2 = f2(0.f);
+            float xv[V];
+            E::unpack(lds16(ss + size_t(t) * 16), xv);
+            c_q = xv[0];
+            const float2 nc = f2(-c_q);
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                if (j > 0) E::unpack(lds16(ss + size_t(t + j * TPR) * 16), xv);
+#pragma unroll
+                for (int q = 0; q < P; ++q) {
+                    const float2 e = f2_add(make_float2(xv[2 * q], xv[2 * q + 1]), nc);
+                    s2 = f2_add(s2, e);
+                    q2 = f2_fma(e, e, q2);
+                }
+            }
+            s_q = s2.x + s2.y;
+            q_q = q2.x + q2.y;
+            s1 = fmaf(kNt, c_q, s_q);
+        }
+        row_reduce_sum5<TPR>(s1, sv, red[k & 1], p.bar_id, fail);
+        if (fail) {  // row k's copy never completed: wait (bounded) for the copies issued
+            if (p.producer) {
+                // issued: rows 0 .. nbuf - 1 at the start, row j - 2 + nbuf after step j >= 2
+                int64_t last = k >= 3 ? k - 3 + nbuf : int64_t(nbuf) - 1;
+                if (last > n - 1) last = n - 1;
+                for (int64_t i = k; i <= last; ++i)
+                    mbar_wait(p.ring.bar + (i % nbuf), uint32_t((i / nbuf) & 1), wait_ns);
+                atomicExch(err, kDeviceErrTimeout);
+            }
+            return;
+        }
+        if (k >= 2 && k - 2 < n)  // stage A is done with row k-2's slot
+            refill_rows<T, true, 2>(p, int((k - 2) % nbuf), p.first + (k - 2) * p.stride, src, M, N, ld,
+                                    stall_row);
+        rstd_c = rstd_a;
+        m1_c = -rstd_a * (sv[2] / fN);
+        m2_c = -rstd_a * (sv[3] / fN);
+        const float delta = sv[1] / fN;
+        mean_a = mean_q;
+        rstd_a = rsqrtf(fmaxf(sv[0] / fN - delta * delta, 0.f) + eps);
+        shift_a = -delta * rstd_a;
+        mean_q = s1 / fN;
+    }
+    float* pw = part + size_t(blockIdx.x) * 2 * N;
+    float* pb = pw + N;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int c0 = (t + j * TPR) * V;
+#pragma unroll
+        for (int h = 0; h < H; ++h) {
+            *reinterpret_cast<float4*>(pw + c0 + 4 * h) =
+                make_float4(aw[j][2 * h].x, aw[j][2 * h].y, aw[j][2 * h + 1].x, aw[j][2 * h + 1].y);
+            *reinterpret_cast<float4*>(pb + c0 + 4 * h) =
+                make_float4(ab[j][2 * h].x, ab[j][2 * h].y, ab[j][2 * h + 1].x, ab[j][2 * h + 1].y);
+        }
+    }
 }
 
 // Full rows, one row group (TPR threads) per CTA; VPT vectors per thread, so a
@@ -254,28 +477,58 @@ cudaError_t launch_bwd_looped(const void* x, const void* dy, const void* w, cons
     return cudaGetLastError();
 }
 
-// tiles of the row pipeline: TPR in {64, 128, 256, 512}, VPT in {1, 2, 3, 4} with
-// at most 16 columns per thread (the dw, db partials live in registers)
 template <typename T, int TPR, int VPT>
-constexpr TmaBwdLaunch bwd_entry() {
-    if constexpr (VPT * Elem<T>::kVec <= 16) return launch_bwd_tma<T, TPR, VPT>;
-    else return nullptr;
+cudaError_t launch_bwd_pipe(const void* x, const void* dy, const void* w, const void* b, float eps, void* dx,
+                            float* part, int64_t M, int64_t N, int64_t ld, int nbuf, int* grid_out,
+                            const LaunchCfg& cfg) {
+    auto kern = ln_gelu_bwd_pipe_kernel<T, TPR, VPT>;
+    const size_t smem = kRingHeader + size_t(nbuf) * 2 * ring_row_bytes(N, Elem<T>::kBytes) +
+                        tma_affine_bytes<T, TPR, VPT>();
+    cudaError_t e = allow_smem(reinterpret_cast<const void*>(kern), smem, cfg);
+    if (e != cudaSuccess) return e;
+    int grid = grid_for(reinterpret_cast<const void*>(kern), TPR, smem, M, cfg);
+    if (grid > kBwdMaxPartials) grid = kBwdMaxPartials;
+    *grid_out = grid;
+    kern<<<grid, TPR, smem, cfg.stream>>>(static_cast<const T*>(x), static_cast<const T*>(dy),
+                                          static_cast<const T*>(w), static_cast<const T*>(b), eps,
+                                          static_cast<T*>(dx), part, M, int(N), ld, nbuf, cfg.dev_error,
+                                          cfg.wait_ns, cfg.stall_row);
+    return cudaGetLastError();
 }
-#define ROWOPS_BWD_ROW(T, P) {bwd_entry<T, P, 1>(), bwd_entry<T, P, 2>(), bwd_entry<T, P, 3>(), bwd_entry<T, P, 4>()}
+
+// tiles of the row pipeline: TPR in {64, 128, 256, 512}, VPT in {1, 2, 3, 4} with
+// at most 16 columns per thread (the dw, db partials live in registers); TPR
+// 1024 with at most 8 columns per thread for the three-stage kernel (64
+// registers a thread)
+template <typename T, int TPR, int VPT, bool PIPE>
+constexpr TmaBwdLaunch bwd_entry() {
+    if constexpr (VPT * Elem<T>::kVec > 16 || (TPR > 512 && (!PIPE || VPT * Elem<T>::kVec > 8))) return nullptr;
+    else if constexpr (PIPE) return launch_bwd_pipe<T, TPR, VPT>;
+    else return launch_bwd_tma<T, TPR, VPT>;
+}
+#define ROWOPS_BWD_ROW(T, P, PIPE) \
+    {bwd_entry<T, P, 1, PIPE>(), bwd_entry<T, P, 2, PIPE>(), bwd_entry<T, P, 3, PIPE>(), bwd_entry<T, P, 4, PIPE>()}
 
 template <typename T>
-TmaBwdLaunch bwd_tma_table(int tpr_index, int vpt) {
-    static const TmaBwdLaunch t[4][4] = {ROWOPS_BWD_ROW(T, 64), ROWOPS_BWD_ROW(T, 128), ROWOPS_BWD_ROW(T, 256),
-                                         ROWOPS_BWD_ROW(T, 512)};
-    if (tpr_index < 0 || tpr_index >= 4 || vpt < 1 || vpt > 4) return nullptr;
-    return t[tpr_index][vpt - 1];
+TmaBwdLaunch bwd_tma_table(int tpr_index, int vpt, bool pipe) {
+    static const TmaBwdLaunch t[2][5][4] = {
+        {ROWOPS_BWD_ROW(T, 64, false), ROWOPS_BWD_ROW(T, 128, false), ROWOPS_BWD_ROW(T, 256, false),
+         ROWOPS_BWD_ROW(T, 512, false), ROWOPS_BWD_ROW(T, 1024, false)},
+        {ROWOPS_BWD_ROW(T, 64, true), ROWOPS_BWD_ROW(T, 128, true), ROWOPS_BWD_ROW(T, 256, true),
+         ROWOPS_BWD_ROW(T, 512, true), ROWOPS_BWD_ROW(T, 1024, true)}};
+    if (tpr_index < 0 || tpr_index >= 5 || vpt < 1 || vpt > 4) return nullptr;
+    return t[pipe ? 1 : 0][tpr_index][vpt - 1];
 }
 #undef ROWOPS_BWD_ROW
 
 }  // namespace
 
-TmaBwdLaunch ln_gelu_bwd_tma_f32(int tpr_index, int vpt) { return bwd_tma_table<float>(tpr_index, vpt); }
-TmaBwdLaunch ln_gelu_bwd_tma_bf16(int tpr_index, int vpt) { return bwd_tma_table<bf16_t>(tpr_index, vpt); }
+TmaBwdLaunch ln_gelu_bwd_tma_f32(int tpr_index, int vpt, bool pipe) {
+    return bwd_tma_table<float>(tpr_index, vpt, pipe);
+}
+TmaBwdLaunch ln_gelu_bwd_tma_bf16(int tpr_index, int vpt, bool pipe) {
+    return bwd_tma_table<bf16_t>(tpr_index, vpt, pipe);
+}
 BwdLaunch ln_gelu_bwd_looped_f32() { return launch_bwd_looped<float>; }
 BwdLaunch ln_gelu_bwd_looped_bf16() { return launch_bwd_looped<bf16_t>; }
 

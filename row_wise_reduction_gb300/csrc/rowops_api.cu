@@ -710,29 +710,30 @@ rowops_status_t rowops_layernorm_gelu_backward(const void* x, const void* dy, co
                       rows_aligned(x, dx, ld, es) && aligned(dy, 16);
     if (full) {
         const int64_t nvec = N / vec;
-        int ti = -1, vpt = 0;
-        for (int v : {2, 4, 3, 1}) {
-            if (v * vec > 16 || nvec % v) continue;
-            for (int i = 0; i < 4; ++i)
-                if (kBwdTpr[i] == nvec / v && (!tn.tpr || tn.tpr == kBwdTpr[i]) && (!tn.vpt || tn.vpt == v)) {
-                    ti = i;
-                    vpt = v;
-                }
-            if (ti >= 0) break;
-        }
-        if (ti >= 0) {
+        // a tile: TPR * VPT = N / vec; the three-stage pipeline where 4..6 ring
+        // slots fit (it holds three rows and wants one more in flight; or
+        // ROWOPS_RING_BUFFERS), else one row at a time on 2 slots
+        auto plan = [&](int ti, int vpt) -> bool {
             const size_t affine = size_t(2) * vpt * kBwdTpr[ti] * vec * 4;
-            int nbuf = tn.ring > 0 ? (tn.ring < 2 ? 2 : (tn.ring > kTmaMaxSlots ? kTmaMaxSlots : tn.ring)) : 2;
             auto fits = [&](int nb) {
                 return size_t(kTmaRingHeader) + size_t(nb) * 2 * tma_row_bytes(N, es) + affine + 1024 <=
                        size_t(cfg.max_smem_optin);
             };
-            while (nbuf > 2 && !fits(nbuf)) --nbuf;
-            const TmaBwdLaunch f = dtype == ROWOPS_F32 ? ln_gelu_bwd_tma_f32(ti, vpt) : ln_gelu_bwd_tma_bf16(ti, vpt);
-            if (fits(nbuf) && f) {
-                e = f(x, dy, w, b, eps, dx, part, M, N, ld, nbuf, &grid, cfg);
-                launched = true;
-            }
+            int nbuf = tn.ring > 0 ? (tn.ring > kTmaMaxSlots ? kTmaMaxSlots : tn.ring) : 6;
+            while (nbuf > 4 && !fits(nbuf)) --nbuf;
+            const bool pipe = nbuf >= 4 && fits(nbuf);
+            if (!pipe) nbuf = 2;
+            const TmaBwdLaunch f =
+                dtype == ROWOPS_F32 ? ln_gelu_bwd_tma_f32(ti, vpt, pipe) : ln_gelu_bwd_tma_bf16(ti, vpt, pipe);
+            if (!f || !fits(nbuf)) return false;
+            e = f(x, dy, w, b, eps, dx, part, M, N, ld, nbuf, &grid, cfg);
+            return true;
+        };
+        for (int v : {2, 4, 3, 1}) {
+            if (launched) break;
+            if (v * vec > 16 || nvec % v || (tn.vpt && tn.vpt != v)) continue;
+            for (int i = 0; i < 5 && !launched; ++i)
+                if (kBwdTpr[i] == nvec / v && (!tn.tpr || tn.tpr == kBwdTpr[i])) launched = plan(i, v);
         }
     }
     if (!launched) {

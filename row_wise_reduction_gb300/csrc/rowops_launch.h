@@ -153,15 +153,17 @@ GeluLaunch gelu_bf16(bool erf);
 // LayerNorm -> affine -> tanh-GELU backward: per-CTA dw, db partials (2 N
 // floats each, at most kBwdMaxPartials CTAs) reduced by ln_gelu_bwd_reduce.
 constexpr int kBwdMaxPartials = 512;
-constexpr int kBwdTpr[] = {64, 128, 256, 512};
+constexpr int kBwdTpr[] = {64, 128, 256, 512, 1024};  // 1024: three-stage kernel only
 using TmaBwdLaunch = cudaError_t (*)(const void* x, const void* dy, const void* w, const void* b, float eps,
                                      void* dx, float* part, int64_t M, int64_t N, int64_t ld, int nbuf,
                                      int* grid_out, const LaunchCfg& cfg);
 using BwdLaunch = cudaError_t (*)(const void* x, const void* dy, const void* w, const void* b, float eps, void* dx,
                                   float* part, int64_t M, int64_t N, int64_t ld, int* grid_out,
                                   const LaunchCfg& cfg);
-TmaBwdLaunch ln_gelu_bwd_tma_f32(int tpr_index, int vpt);
-TmaBwdLaunch ln_gelu_bwd_tma_bf16(int tpr_index, int vpt);
+// pipe: the three-stage kernel (one reduction per row, nbuf >= 4) instead of
+// the one-row-at-a-time kernel (three reductions per row, nbuf >= 2)
+TmaBwdLaunch ln_gelu_bwd_tma_f32(int tpr_index, int vpt, bool pipe);
+TmaBwdLaunch ln_gelu_bwd_tma_bf16(int tpr_index, int vpt, bool pipe);
 BwdLaunch ln_gelu_bwd_looped_f32();
 BwdLaunch ln_gelu_bwd_looped_bf16();
 cudaError_t ln_gelu_bwd_reduce(const float* part, int P, int64_t N, float* dw, float* db, const LaunchCfg& cfg);

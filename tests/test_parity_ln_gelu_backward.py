@@ -187,6 +187,47 @@ def test_constant_rows(oracle):
     assert_sum_close(C.to_f64(db), ref_db, Ab, wl.M, "db")
 
 
+@pytest.mark.parametrize("dtype,N", [("bf16", 8192), ("f32", 8192), ("f32", 1024), ("bf16", 4097)])
+def test_outlier_rows(oracle, dtype, N):
+    """One large negative entry per row: xh reaches about -sqrt(N) there and z
+    far below -10, where the tanh GELU's slope underflows to 0 (it must not
+    overflow into NaN)."""
+    wl = edge(dtype, 160, N)
+    inp = gu.make_x(wl)
+    x = inp["x"]
+    cols = torch.randint(0, N, (160,), generator=torch.Generator().manual_seed(3)).to(x.device)
+    x[torch.arange(160, device=x.device), cols] = -1000.0
+    dy, w, b = inp["dy"], inp["w"], inp["b"]
+    dx, dw, db = run(x, dy, w, b, wl.eps)
+    xin, gin = gu.rows_f32(x), gu.rows_f32(dy)
+    ref_dx, ref_dw, ref_db = oracle.layernorm_gelu_backward(xin, gin, host(w), host(b), wl.eps)
+    S, Aw, Ab = scales(xin, gin, host(w), wl.eps)
+    assert_dx_close(C.to_f64(dx), ref_dx, S, dtype, "outlier rows")
+    assert_sum_close(C.to_f64(dw), ref_dw, Aw, wl.M, "dw")
+    assert_sum_close(C.to_f64(db), ref_db, Ab, wl.M, "db")
+
+
+@pytest.mark.parametrize("ring", ["2", "3", "4", "5", "6"])
+@pytest.mark.parametrize("dtype,N", [("bf16", 8192), ("bf16", 2048), ("f32", 3072)])
+def test_ring_depths(oracle, monkeypatch, ring, dtype, N):
+    """ROWOPS_RING_BUFFERS below 4 selects the one-row-at-a-time kernel, 4 and
+    up the three-stage pipeline: both against the oracle, with few rows per CTA
+    and with many."""
+    monkeypatch.setenv("ROWOPS_RING_BUFFERS", ring)
+    for M in (157, 2000):
+        check_all(oracle, edge(dtype, M, N, seed=int(ring) + M))
+
+
+@pytest.mark.parametrize("dtype,N,vpt", [("bf16", 8192, "1"), ("bf16", 8192, "2"), ("f32", 4096, "1"),
+                                         ("f32", 4096, "2"), ("bf16", 4096, "1")])
+def test_row_group_widths(oracle, monkeypatch, dtype, N, vpt):
+    """ROWOPS_FORCE_VPT picks the tile: 1024 threads of 8 columns or 512 of 16
+    (bf16 8192), and so on."""
+    monkeypatch.setenv("ROWOPS_FORCE_VPT", vpt)
+    for M in (100, 1500):
+        check_all(oracle, edge(dtype, M, N, seed=int(vpt) * 7 + M))
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_zero_rows(dtype):
     wl = edge(dtype, 4, 256)
