@@ -279,7 +279,8 @@ rowops_status_t rowops_layernorm_gelu_erf(const void* x, void* y, const void* w,
  *   workspace, workspace_bytes   device memory, 256-byte aligned, at least
  *            rowops_layernorm_gelu_backward_workspace_bytes(M, N, dtype) bytes
  *            (overwritten), apart from dw and db; calls sharing it must be
- *            ordered on one stream.
+ *            ordered on one stream. It holds 2 N floats for each of at most
+ *            clamp(2^22 / N, 152, 4096) CTAs (32 MiB for N <= 27594).
  * M == 0 writes zeros to dw and db.
  */
 size_t rowops_layernorm_gelu_backward_workspace_bytes(int64_t M, int64_t N, rowops_dtype_t dtype);

@@ -427,17 +427,26 @@ __global__ void __launch_bounds__(BLOCK)
     }
 }
 
-// dw[c], db[c]: the sum over the P partials, in order p = 0, 1, ...
-__global__ void ln_gelu_bwd_reduce_kernel(const float* part, int P, int N, float* dw, float* db) {
-    const int c = blockIdx.x * blockDim.x + threadIdx.x;
-    if (c >= N) return;
-    float sw = 0.f, sb = 0.f;
-    for (int p = 0; p < P; ++p) {
-        sw += part[size_t(p) * 2 * N + c];
-        sb += part[size_t(p) * 2 * N + N + c];
+// dw[c], db[c]: the sums over the P partials. A CTA takes 32 columns of dw or
+// db; thread (x, y) adds the partials p = y, y + 32, ... of column x in order,
+// then the 32 sums are added in order of y: a fixed order, so the result does
+// not depend on scheduling.
+__global__ void __launch_bounds__(1024) ln_gelu_bwd_reduce_kernel(const float* part, int P, int N, float* dw,
+                                                                  float* db) {
+    __shared__ float acc[32][33];
+    const int c = blockIdx.x * 32 + threadIdx.x;
+    const int which = blockIdx.y;  // 0: dw, 1: db
+    float s = 0.f;
+    if (c < N)
+        for (int p = threadIdx.y; p < P; p += 32) s += part[size_t(p) * 2 * N + size_t(which) * N + c];
+    acc[threadIdx.y][threadIdx.x] = s;
+    __syncthreads();
+    if (threadIdx.y == 0 && c < N) {
+        float t = 0.f;
+#pragma unroll 8
+        for (int y = 0; y < 32; ++y) t += acc[y][threadIdx.x];
+        (which ? db : dw)[c] = t;
     }
-    dw[c] = sw;
-    db[c] = sb;
 }
 
 namespace {
@@ -452,7 +461,7 @@ cudaError_t launch_bwd_tma(const void* x, const void* dy, const void* w, const v
     cudaError_t e = allow_smem(reinterpret_cast<const void*>(kern), smem, cfg);
     if (e != cudaSuccess) return e;
     int grid = grid_for(reinterpret_cast<const void*>(kern), TPR, smem, M, cfg);
-    if (grid > kBwdMaxPartials) grid = kBwdMaxPartials;
+    if (grid > bwd_max_partials(N)) grid = bwd_max_partials(N);
     *grid_out = grid;
     kern<<<grid, TPR, smem, cfg.stream>>>(static_cast<const T*>(x), static_cast<const T*>(dy),
                                           static_cast<const T*>(w), static_cast<const T*>(b), eps,
@@ -467,7 +476,7 @@ cudaError_t launch_bwd_looped(const void* x, const void* dy, const void* w, cons
     constexpr int BLOCK = 512;
     auto kern = ln_gelu_bwd_looped_kernel<T, BLOCK>;
     int grid = grid_for(reinterpret_cast<const void*>(kern), BLOCK, 0, M, cfg);
-    if (grid > kBwdMaxPartials) grid = kBwdMaxPartials;
+    if (grid > bwd_max_partials(N)) grid = bwd_max_partials(N);
     *grid_out = grid;
     cudaError_t e = cudaMemsetAsync(part, 0, size_t(grid) * 2 * N * sizeof(float), cfg.stream);
     if (e != cudaSuccess) return e;
@@ -487,7 +496,7 @@ cudaError_t launch_bwd_pipe(const void* x, const void* dy, const void* w, const 
     cudaError_t e = allow_smem(reinterpret_cast<const void*>(kern), smem, cfg);
     if (e != cudaSuccess) return e;
     int grid = grid_for(reinterpret_cast<const void*>(kern), TPR, smem, M, cfg);
-    if (grid > kBwdMaxPartials) grid = kBwdMaxPartials;
+    if (grid > bwd_max_partials(N)) grid = bwd_max_partials(N);
     *grid_out = grid;
     kern<<<grid, TPR, smem, cfg.stream>>>(static_cast<const T*>(x), static_cast<const T*>(dy),
                                           static_cast<const T*>(w), static_cast<const T*>(b), eps,
@@ -533,9 +542,8 @@ BwdLaunch ln_gelu_bwd_looped_f32() { return launch_bwd_looped<float>; }
 BwdLaunch ln_gelu_bwd_looped_bf16() { return launch_bwd_looped<bf16_t>; }
 
 cudaError_t ln_gelu_bwd_reduce(const float* part, int P, int64_t N, float* dw, float* db, const LaunchCfg& cfg) {
-    const int block = 256;
-    const int grid = int((N + block - 1) / block);
-    ln_gelu_bwd_reduce_kernel<<<grid, block, 0, cfg.stream>>>(part, P, int(N), dw, db);
+    const dim3 grid(unsigned((N + 31) / 32), 2);
+    ln_gelu_bwd_reduce_kernel<<<grid, dim3(32, 32), 0, cfg.stream>>>(part, P, int(N), dw, db);
     return cudaGetLastError();
 }
 

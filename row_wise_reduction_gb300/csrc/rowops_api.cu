@@ -655,8 +655,8 @@ rowops_status_t rowops_fused_residual_rmsnorm(const void* x, const void* residua
 
 size_t rowops_layernorm_gelu_backward_workspace_bytes(int64_t M, int64_t N, rowops_dtype_t dtype) {
     if (!valid_dtype(dtype) || M < 0 || N < 1 || N >= (int64_t(1) << 31)) return 0;
-    // dw, db partials of at most kBwdMaxPartials CTAs
-    return size_t(kBwdMaxPartials) * 2 * size_t(N) * sizeof(float);
+    // dw, db partials of at most bwd_max_partials(N) CTAs
+    return size_t(bwd_max_partials(N)) * 2 * size_t(N) * sizeof(float);
 }
 
 rowops_status_t rowops_layernorm_gelu_backward(const void* x, const void* dy, const void* w, const void* b,

@@ -151,8 +151,12 @@ GeluLaunch gelu_f32(bool erf);
 GeluLaunch gelu_bf16(bool erf);
 
 // LayerNorm -> affine -> tanh-GELU backward: per-CTA dw, db partials (2 N
-// floats each, at most kBwdMaxPartials CTAs) reduced by ln_gelu_bwd_reduce.
-constexpr int kBwdMaxPartials = 512;
+// floats each, at most bwd_max_partials(N) CTAs) reduced by ln_gelu_bwd_reduce.
+// The cap keeps the partials within 32 MiB (at least 152, at most 4096 CTAs).
+inline int bwd_max_partials(int64_t N) {
+    const int64_t p = (int64_t(1) << 22) / (N > 0 ? N : 1);
+    return int(p < 152 ? 152 : (p > 4096 ? 4096 : p));
+}
 constexpr int kBwdTpr[] = {64, 128, 256, 512, 1024};  // 1024: three-stage kernel only
 using TmaBwdLaunch = cudaError_t (*)(const void* x, const void* dy, const void* w, const void* b, float eps,
                                      void* dx, float* part, int64_t M, int64_t N, int64_t ld, int nbuf,

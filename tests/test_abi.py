@@ -185,10 +185,13 @@ def test_online_softmax_validation(lib):
 
 def test_layernorm_gelu_backward_workspace_bytes(lib):
     q = lib.rowops_layernorm_gelu_backward_workspace_bytes
-    # dw, db partials (N floats each) of at most 512 CTAs
-    assert q(4, 8, F32) == 512 * 2 * 8 * 4
+    # dw, db partials (N floats each) of at most clamp(2^22 / N, 152, 4096) CTAs
+    assert q(4, 8, F32) == 4096 * 2 * 8 * 4
     assert q(1 << 20, 8192, BF16) == 512 * 2 * 8192 * 4
-    assert q(0, 3, F32) == 512 * 2 * 3 * 4
+    assert q(9, 768, F32) == 4096 * 2 * 768 * 4
+    assert q(9, 4097, F32) == 1023 * 2 * 4097 * 4
+    assert q(9, 1 << 20, F32) == 152 * 2 * (1 << 20) * 4
+    assert q(0, 3, F32) == 4096 * 2 * 3 * 4
     assert q(-1, 8, F32) == 0
     assert q(4, 0, F32) == 0
     assert q(4, 8, 9) == 0

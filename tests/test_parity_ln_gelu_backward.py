@@ -7,9 +7,10 @@ Tolerances (derived from fp32 arithmetic, u = 2^-24):
   + mean |dxh| + |xh| mean |dxh xh|) with |dxh| bounded by 1.2 |dy w| (the tanh
   GELU's slope stays below 1.13): the size of the terms that meet in dx.
   bf16 adds one bf16 ulp of the result (the final rounding).
-- dw, db: sums over M rows, added in two fixed levels (rows of one CTA, then at
-  most 512 CTA partials): within (u (ceil(M / min(M, 152)) + 512) + 2e-6) A
-  with A = 1.2 sum over the rows of |dy xh| (dw) or |dy| (db).
+- dw, db: sums over M rows, added in fixed order (the rows of one CTA, then
+  the CTA partials, at most 4096, in 32 strided sums and a sum of those): within
+  (u (ceil(M / min(M, 152)) + 512) + 2e-6) A with A = 1.2 sum over the rows of
+  |dy xh| (dw) or |dy| (db); 512 bounds the additions after the CTA level.
 At full size a sparse dy (zero except on sampled rows) pins every row's
 contribution: dx must be exactly 0 on the other rows and dw, db must be the
 sums over the sampled rows alone.
