@@ -53,6 +53,39 @@ __device__ __forceinline__ float gelu_of(float z) {
     else return gelu_tanh_approx(z);
 }
 
+// The same two functions on a pair of values with packed fp32 arithmetic (the
+// same operations per value, half the instructions).
+__device__ __forceinline__ float2 gelu_tanh_approx2(float2 z) {
+    constexpr float c0 = float(-2.0 * 0.79788456 * kLog2e);
+    constexpr float c1 = float(-2.0 * 0.79788456 * 0.044715 * kLog2e);
+    const float2 a = f2_mul(f2_fma(f2(c1), f2_mul(z, z), f2(c0)), z);
+    const float2 d = f2_add(make_float2(ex2_approx(a.x), ex2_approx(a.y)), f2(1.f));
+    return f2_mul(z, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
+}
+
+__device__ __forceinline__ float2 gelu_erf2(float2 z) {
+    constexpr float p = 0.3275911f, a1 = 0.254829592f, a2 = -0.284496736f, a3 = 1.421413741f,
+                    a4 = -1.453152027f, a5 = 1.061405429f;
+    const float2 u = f2_mul(make_float2(fabsf(z.x), fabsf(z.y)), f2(0.70710678118654752f));
+    const float2 d = f2_fma(f2(p), u, f2(1.f));
+    const float2 t = make_float2(rcp_approx(d.x), rcp_approx(d.y));
+    float2 poly = f2_fma(t, f2(a5), f2(a4));
+    poly = f2_fma(t, poly, f2(a3));
+    poly = f2_fma(t, poly, f2(a2));
+    poly = f2_fma(t, poly, f2(a1));
+    const float2 g = f2_mul(f2_mul(u, u), f2(-kLog2eF));
+    const float2 q = f2_mul(f2_mul(poly, t), make_float2(ex2_approx(g.x), ex2_approx(g.y)));
+    const float2 pos = f2_mul(z, f2_fma(f2(-0.5f), q, f2(1.f)));
+    const float2 neg = f2_mul(f2_mul(f2(0.5f), z), q);
+    return make_float2(z.x >= 0.f ? pos.x : neg.x, z.y >= 0.f ? pos.y : neg.y);
+}
+
+template <bool ERF>
+__device__ __forceinline__ float2 gelu_of2(float2 z) {
+    if constexpr (ERF) return gelu_erf2(z);
+    else return gelu_tanh_approx2(z);
+}
+
 // Shared-memory staging of w, b as fp32 (absent -> 1, 0). `sw` and `sb` hold
 // round_up(N, 4) floats each.
 template <typename T>

@@ -545,21 +545,26 @@ __global__ void __launch_bounds__(TPR * ROWS)
         int fail = !mbar_wait(p.ring.bar + s, uint32_t((i / nbuf) & 1), wait_ns);
         const char* sbuf = p.ring.slot(s);
 
-        float v[VPT][V];
-        float sum = ex;
+        // elementwise arithmetic on packed fp32 pairs
+        float2 v[VPT][V / 2];
+        float2 s2 = make_float2(ex, 0.f);
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
             const int k = t + j * TPR;
+            float u[V];
             if (FULL || k < sp.body) {
-                E::unpack(lds16(sbuf + size_t(k) * 16), v[j]);
+                E::unpack(lds16(sbuf + size_t(k) * 16), u);
             } else {
 #pragma unroll
-                for (int e = 0; e < V; ++e) v[j][e] = 0.f;
+                for (int e = 0; e < V; ++e) u[e] = 0.f;
             }
 #pragma unroll
-            for (int e = 0; e < V; ++e) sum += v[j][e];
+            for (int e = 0; e < V / 2; ++e) {
+                v[j][e] = make_float2(u[2 * e], u[2 * e + 1]);
+                s2 = f2_add(s2, v[j][e]);
+            }
         }
-        sum = row_reduce<TPR>(sum, red_a[g], p.bar_id, OpSum(), fail);
+        float sum = row_reduce<TPR>(s2.x + s2.y, red_a[g], p.bar_id, OpSum(), fail);
         if (fail) {
             abandon(p, i, M, err, wait_ns);
             return;
@@ -567,17 +572,18 @@ __global__ void __launch_bounds__(TPR * ROWS)
         refill<T, FULL>(p, s, row, x, M, N, ld, stall_row);
         const float mean = sum / fN;
         // centred values, their squares and the residual of the fp32 mean
-        float q = 0.f, r = 0.f;
+        float2 q2 = f2(0.f), r2 = f2(0.f);
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
             const bool ok = FULL || (t + j * TPR) < sp.body;
 #pragma unroll
-            for (int e = 0; e < V; ++e) {
-                v[j][e] = ok ? v[j][e] - mean : 0.f;
-                q = fmaf(v[j][e], v[j][e], q);
-                r += v[j][e];
+            for (int e = 0; e < V / 2; ++e) {
+                v[j][e] = ok ? f2_add(v[j][e], f2(-mean)) : f2(0.f);
+                q2 = f2_fma(v[j][e], v[j][e], q2);
+                r2 = f2_add(r2, v[j][e]);
             }
         }
+        float q = q2.x + q2.y, r = r2.x + r2.y;
         if constexpr (!FULL) {
             ex = has_ex ? ex - mean : 0.f;
             q = fmaf(ex, ex, q);
@@ -598,10 +604,15 @@ __global__ void __launch_bounds__(TPR * ROWS)
                 for (int h = 0; h < H; ++h) {
                     const float4 ww = sw4[(j * H + h) * TPR + t];
                     const float4 bb = sb4[(j * H + h) * TPR + t];
-                    o[4 * h + 0] = gelu_of<ERF>(fmaf(fmaf(v[j][4 * h + 0], rstd, shift), ww.x, bb.x));
-                    o[4 * h + 1] = gelu_of<ERF>(fmaf(fmaf(v[j][4 * h + 1], rstd, shift), ww.y, bb.y));
-                    o[4 * h + 2] = gelu_of<ERF>(fmaf(fmaf(v[j][4 * h + 2], rstd, shift), ww.z, bb.z));
-                    o[4 * h + 3] = gelu_of<ERF>(fmaf(fmaf(v[j][4 * h + 3], rstd, shift), ww.w, bb.w));
+                    const float2 z0 = f2_fma(f2_fma(v[j][2 * h], f2(rstd), f2(shift)), make_float2(ww.x, ww.y),
+                                             make_float2(bb.x, bb.y));
+                    const float2 z1 = f2_fma(f2_fma(v[j][2 * h + 1], f2(rstd), f2(shift)), make_float2(ww.z, ww.w),
+                                             make_float2(bb.z, bb.w));
+                    const float2 g0 = gelu_of2<ERF>(z0), g1 = gelu_of2<ERF>(z1);
+                    o[4 * h + 0] = g0.x;
+                    o[4 * h + 1] = g0.y;
+                    o[4 * h + 2] = g1.x;
+                    o[4 * h + 3] = g1.y;
                 }
                 st_stream16(yb + size_t(k) * V, E::pack(o));
             }
