@@ -39,7 +39,8 @@
  *   ROWOPS_FORCE_TPR=<16..1024>   threads per row (tma: 64..512)
  *   ROWOPS_FORCE_VPT=<n>          16-byte vectors per thread (reg: 1..4; tma: 1, 2, 3, 4, 8)
  *   ROWOPS_FORCE_LOOPED=1         same as ROWOPS_KERNEL=looped
- *   ROWOPS_RING_BUFFERS=<2..16>   rows in flight per row group of the row pipeline
+ *   ROWOPS_RING_BUFFERS=<2..16>   rows in flight per row group of the row pipeline (chunks per
+ *                                 CTA of the two-pass split softmax on full chunks, default 3)
  *   ROWOPS_ROWS_PER_CTA=<1|2|4|8> row groups per CTA of the LayerNorm+GELU and RMSNorm row pipelines
  *   ROWOPS_ONLINE=two_pass|single_read  split-row softmax form (default two_pass); single_read
  *                                 keeps each chunk on chip between the passes (rows of
@@ -55,7 +56,9 @@
  *   ROWOPS_WAIT_LIMIT_NS=<ns>     limit of every device-side wait (default 2 s)
  *   ROWOPS_TEST_STALL_ROW=<row>   test hook for the timeout path: the wait that concerns this
  *                                 row is made to run out (the row pipeline's bulk copy of it is
- *                                 expected to bring 16 bytes more than it does; in the
+ *                                 expected to bring 16 bytes more than it does; in the two-pass
+ *                                 split softmax on full chunks the same for work item <row>,
+ *                                 i.e. chunk (row mod nchunks) of row row / nchunks; in the
  *                                 single-read split softmax CTA 0 withholds that row's partial).
  *                                 Nothing faults or hangs: the wait gives up at its limit, the
  *                                 kernel records ROWOPS_ERR_TIMEOUT and returns.

@@ -1,6 +1,7 @@
 // Split-row online softmax: launch wrappers for both element types.
 #include "online_softmax_kernels.cuh"
 #include "online_softmax_persistent.cuh"
+#include "online_softmax_tma.cuh"
 #include "rowops_launch.h"
 
 namespace rowops {
@@ -32,6 +33,49 @@ static cudaError_t launch_split(const void* x, void* y, int64_t M, int64_t N, in
 
 SplitLaunch split_softmax_f32() { return launch_split<float>; }
 SplitLaunch split_softmax_bf16() { return launch_split<bf16_t>; }
+
+constexpr int kSplitTmaTpr = 256;
+
+template <typename T, int VPT>
+static cudaError_t launch_split_tma_v(const void* x, void* y, int64_t M, int64_t nchunks, int64_t ld, int nbuf,
+                                     void* workspace, const LaunchCfg& cfg) {
+    unsigned* status = static_cast<unsigned*>(workspace);
+    float2* partials = reinterpret_cast<float2*>(static_cast<char*>(workspace) + kWorkspaceHeader);
+    const int64_t items = M * nchunks;
+    const size_t smem = kRingHeader + size_t(nbuf) * kSplitTmaTpr * VPT * 16;
+    auto k1 = split_partial_tma_kernel<T, kSplitTmaTpr, VPT>;
+    auto k2 = split_normalise_tma_kernel<T, kSplitTmaTpr, VPT>;
+    cudaError_t e = allow_smem(reinterpret_cast<const void*>(k1), smem, cfg);
+    if (e == cudaSuccess) e = allow_smem(reinterpret_cast<const void*>(k2), smem, cfg);
+    if (e != cudaSuccess) return e;
+    const int g1 = grid_for(reinterpret_cast<const void*>(k1), kSplitTmaTpr, smem, items, cfg);
+    k1<<<g1, kSplitTmaTpr, smem, cfg.stream>>>(static_cast<const T*>(x), items, nchunks, ld, status, partials, nbuf,
+                                               cfg.wait_ns, cfg.stall_row);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int g2 = grid_for(reinterpret_cast<const void*>(k2), kSplitTmaTpr, smem, items, cfg);
+    k2<<<g2, kSplitTmaTpr, smem, cfg.stream>>>(static_cast<const T*>(x), static_cast<T*>(y), items, nchunks, ld,
+                                               partials, status, nbuf, cfg.wait_ns, cfg.stall_row);
+    return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t launch_split_tma(const void* x, void* y, int64_t M, int64_t N, int64_t ld, int64_t chunk,
+                                   int64_t nchunks, int nbuf, void* workspace, const LaunchCfg& cfg) {
+    constexpr int64_t step = int64_t(kSplitTmaTpr) * Elem<T>::kVec;
+    if (chunk % step != 0 || N % chunk != 0 || nbuf < 2 || nbuf > kMaxRingBuffers) return cudaErrorNotSupported;
+    const size_t smem = kRingHeader + size_t(nbuf) * size_t(chunk) * sizeof(T);
+    if (smem + 1024 > size_t(cfg.max_smem_optin)) return cudaErrorNotSupported;
+    switch (chunk / step) {
+        case 1: return launch_split_tma_v<T, 1>(x, y, M, nchunks, ld, nbuf, workspace, cfg);
+        case 2: return launch_split_tma_v<T, 2>(x, y, M, nchunks, ld, nbuf, workspace, cfg);
+        case 4: return launch_split_tma_v<T, 4>(x, y, M, nchunks, ld, nbuf, workspace, cfg);
+        case 8: return launch_split_tma_v<T, 8>(x, y, M, nchunks, ld, nbuf, workspace, cfg);
+        default: return cudaErrorNotSupported;
+    }
+}
+
+SplitTmaLaunch split_softmax_tma_f32() { return launch_split_tma<float>; }
+SplitTmaLaunch split_softmax_tma_bf16() { return launch_split_tma<bf16_t>; }
 
 int64_t persistent_slots(int64_t N) { return (N + 255) / 256 + 2; }
 size_t persistent_rowstat_bytes(int64_t M) { return size_t((M * 8 + 255) / 256 * 256); }

@@ -792,6 +792,14 @@ rowops_status_t rowops_online_softmax(const void* x, void* y, int64_t M, int64_t
     }
     if (chunk > n16) chunk = n16 < kMinChunk ? kMinChunk : n16;
     const int64_t nchunks = (N + chunk - 1) / chunk;
+    // chunks that are whole row-pipeline tiles of aligned rows stream through a
+    // shared-memory ring (ROWOPS_RING_BUFFERS slots, default 3)
+    if ((tn.family == Family::Auto || tn.family == Family::Tma) && rows_aligned(x, y, ld, es)) {
+        const int nbuf = tn.ring > 0 ? (tn.ring > kTmaMaxSlots ? kTmaMaxSlots : tn.ring) : 3;
+        const SplitTmaLaunch ft = dtype == ROWOPS_F32 ? split_softmax_tma_f32() : split_softmax_tma_bf16();
+        const cudaError_t e = ft(x, y, M, N, ld, chunk, nchunks, nbuf, workspace, cfg);
+        if (e != cudaErrorNotSupported) return finish(e);
+    }
     SplitLaunch fn = dtype == ROWOPS_F32 ? split_softmax_f32() : split_softmax_bf16();
     return finish(fn(x, y, M, N, ld, chunk, nchunks, workspace, cfg));
 }

@@ -210,6 +210,14 @@ LnGeluLaunch ln_gelu_erf_looped_bf16();
 
 SplitLaunch split_softmax_f32();
 SplitLaunch split_softmax_bf16();
+// The same two passes with the chunks streamed through a ring of `nbuf` slots
+// in shared memory (online_softmax_tma.cuh): rows 16-byte aligned, N a
+// multiple of the chunk, chunk = 256 threads x 1, 2, 4 or 8 16-byte vectors;
+// cudaErrorNotSupported (nothing launched) otherwise.
+using SplitTmaLaunch = cudaError_t (*)(const void* x, void* y, int64_t M, int64_t N, int64_t ld, int64_t chunk,
+                                       int64_t nchunks, int nbuf, void* workspace, const LaunchCfg& cfg);
+SplitTmaLaunch split_softmax_tma_f32();
+SplitTmaLaunch split_softmax_tma_bf16();
 
 // Single-read split-row softmax (persistent cooperative grid); returns
 // cudaErrorNotSupported, launching nothing, when the problem does not suit it.

@@ -86,6 +86,24 @@ def test_single_read_split_softmax_wait_times_out(oracle, monkeypatch, staging):
     C.assert_softmax_close(C.to_f64(y), oracle.softmax(gu.rows_f32(x)), "f32")
 
 
+def test_two_pass_split_softmax_wait_times_out(oracle, monkeypatch):
+    """The two-pass split softmax on full chunks streams them through a ring:
+    a stalled chunk (work item 37) ends both passes' waits in a recorded
+    timeout, reported through the workspace; the next call is correct."""
+    wl = workloads.Workload("timeout_two_pass", "online_softmax", "f32", 4, 1 << 16, seed=6)
+    x = gu.make_x(wl)["x"]
+    ws = torch.empty(rowops_online_softmax_workspace_bytes(4, 1 << 16, torch.float32), dtype=torch.uint8,
+                     device="cuda")
+    monkeypatch.setenv("ROWOPS_WAIT_LIMIT_NS", LIMIT_NS)
+    monkeypatch.setenv("ROWOPS_TEST_STALL_ROW", "37")
+    rowops_online_softmax(x, workspace=ws, chunk=2048)
+    assert rowops_online_softmax_status(ws) == TIMEOUT
+    monkeypatch.delenv("ROWOPS_TEST_STALL_ROW")
+    y = rowops_online_softmax(x, workspace=ws, chunk=2048)
+    assert rowops_online_softmax_status(ws) == 0
+    C.assert_softmax_close(C.to_f64(y), oracle.softmax(gu.rows_f32(x)), "f32")
+
+
 @pytest.mark.parametrize("sched", ["static", "dynamic"])
 def test_rmsnorm_pipeline_wait_times_out(oracle, monkeypatch, sched):
     """The fused residual RMSNorm ring (two input rows per slot on one

@@ -132,6 +132,31 @@ def test_online_softmax_masked_chunks(oracle):
     C.assert_softmax_close(C.to_f64(y), ref, "f32")
 
 
+@pytest.mark.parametrize("family", ["auto", "looped"])
+@pytest.mark.parametrize("dtype,chunk", [("f32", 1024), ("f32", 2048), ("f32", 4096), ("f32", 8192),
+                                         ("bf16", 2048), ("bf16", 4096), ("bf16", 8192), ("bf16", 16384)])
+def test_online_softmax_full_chunks(oracle, monkeypatch, family, dtype, chunk):
+    """Chunks that are whole 256-thread tiles of aligned rows stream through a
+    shared-memory ring (auto); ROWOPS_KERNEL=looped keeps the register-load
+    kernels. Both against the oracle, with a chunk of NaN only, one of -inf
+    only, a +inf, an all -inf row, out of place and in place."""
+    if family == "looped":
+        monkeypatch.setenv("ROWOPS_KERNEL", "looped")
+    N = 16 * chunk
+    wl = edge(dtype, 9, N, seed=chunk + len(family), outlier_p=1e-3)
+    check(oracle, wl, chunk=chunk)
+    check(oracle, wl, chunk=chunk, inplace=True)
+    x = gu.make_x(wl)["x"]
+    x[0, chunk:2 * chunk] = float("nan")
+    x[1, 3 * chunk:4 * chunk] = float("-inf")
+    x[2, 5] = float("inf")
+    x[3] = float("-inf")
+    xin = gu.rows_f32(x)
+    y = rowops_online_softmax(x, chunk=chunk)
+    torch.cuda.synchronize()
+    C.assert_softmax_close(C.to_f64(y), oracle.softmax(xin), dtype, what=f"special chunks {family} {chunk}")
+
+
 def test_online_softmax_deterministic():
     x = gu.make_x(edge("f32", 16, 300000))["x"]
     a = rowops_online_softmax(x, chunk=4096)
