@@ -93,6 +93,9 @@ def lib() -> ctypes.CDLL:
         L.oracle_residual_rmsnorm_rows_f32.argtypes = [_c_float_p, _c_float_p, _c_float_p, ctypes.c_double,
                                                        ctypes.c_int, _i64, _i64, _i64, _c_double_p, _c_double_p]
         L.oracle_residual_rmsnorm_rows_f32.restype = ctypes.c_int
+        L.oracle_bias_residual_gelu_rows_f32.argtypes = [_c_float_p, _c_float_p, _c_float_p, _i64, _i64, _i64,
+                                                          ctypes.c_int, _c_double_p]
+        L.oracle_bias_residual_gelu_rows_f32.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -337,6 +340,27 @@ def layernorm_gelu_erf(x, w=None, b=None, eps: float = 1e-5) -> np.ndarray:
     wf, bf = _opt32(w, N), _opt32(b, N)
     if lib().oracle_layernorm_gelu_erf_rows_f32(_fp(xs), _fp(wf), _fp(bf), float(eps), M, N, ld, _dp(y)) != 0:
         raise ValueError("oracle_layernorm_gelu_erf_rows_f32 rejected its arguments")
+    return y
+
+
+def bias_residual_gelu(x, residual=None, bias=None, approximate: str = "none") -> np.ndarray:
+    """GELU(x + bias + residual) of every element -> float64 (M, N); bias per
+    column, residual shaped like x (either may be None); approximate "none"
+    (exact, erf) or "tanh"."""
+    if approximate not in ("none", "tanh"):
+        raise ValueError('approximate must be "none" or "tanh"')
+    xs, M, N, ld = _rows(x)
+    rs = None
+    if residual is not None:
+        rs, Mr, Nr, ldr = _rows(residual)
+        if (Mr, Nr) != (M, N):
+            raise ValueError("residual must have x's shape")
+        if ldr != ld:
+            xs, rs, ld = np.ascontiguousarray(xs), np.ascontiguousarray(rs), N
+    y = np.empty((M, N), dtype=np.float64)
+    if lib().oracle_bias_residual_gelu_rows_f32(_fp(xs), _fp(rs), _fp(_opt32(bias, N)), M, N, ld,
+                                                0 if approximate == "none" else 1, _dp(y)) != 0:
+        raise ValueError("oracle_bias_residual_gelu_rows_f32 rejected its arguments")
     return y
 
 

@@ -494,3 +494,23 @@ int oracle_layernorm_gelu_backward_rows_f32(const float* x, const float* dy, con
     free(bd);
     return rc;
 }
+
+/* ---------------------------------------------------------------------------
+ * Fused residual + bias + GELU [EX §3.4, "fused residual + bias + GELU"]: the
+ * page names the fused kernel but gives no formula; the plain reading is the
+ * GELU of the elementwise sum x + b + residual, b broadcast along the rows.
+ * The three float inputs add exactly in double (their exponents differ by far
+ * less than 53 bits in any test), so no summation order is implied.
+ * ------------------------------------------------------------------------- */
+int oracle_bias_residual_gelu_rows_f32(const float* x, const float* residual, const float* b, int64_t M,
+                                       int64_t N, int64_t ld, int approximate, double* y) {
+    if (bad_shape(x, M, N, ld, y) || (approximate != 0 && approximate != 1)) return -1;
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < N; ++j) {
+            double s = (double)x[i * ld + j];
+            if (b) s += (double)b[j];
+            if (residual) s += (double)residual[i * ld + j];
+            y[i * N + j] = approximate ? oracle_gelu_tanh(s) : oracle_gelu_erf(s);
+        }
+    return 0;
+}

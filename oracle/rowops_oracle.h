@@ -131,6 +131,13 @@ int oracle_softmax_causal_rows_f32(const float* x, int64_t M, int64_t N, int64_t
 int oracle_residual_rmsnorm_rows_f32(const float* x, const float* r, const float* w, double eps, int storage,
                                      int64_t M, int64_t N, int64_t ld, double* s_out, double* y);
 
+/* Fused residual + bias + GELU [EX §3.4 names it without a formula; reading:
+ * y = GELU(x + b + residual), b per column, the sum exact in double].
+ * residual (rows of stride ld, like x) and b (N entries) may be NULL;
+ * approximate: 0 the exact (erf) GELU, 1 the tanh form. y is M x N. */
+int oracle_bias_residual_gelu_rows_f32(const float* x, const float* residual, const float* b, int64_t M,
+                                       int64_t N, int64_t ld, int approximate, double* y);
+
 #ifdef __cplusplus
 }
 #endif

@@ -718,3 +718,55 @@ def test_layernorm_gelu_backward_batch_respects_ld(oracle):
 def test_batch_rejects_bad_shapes(oracle):
     with pytest.raises(ValueError):
         oracle.layernorm_gelu(np.zeros((2, 3), np.float32), np.ones(4, np.float32))
+
+
+# ----------------------------------------------------------------------------
+# fused residual + bias + GELU
+# ----------------------------------------------------------------------------
+def test_bias_residual_gelu_golden_closed_form(oracle):
+    """Dyadic x, b, residual whose sums hit the exact-GELU table: catches a
+    dropped bias or residual, a bias indexed by row, and the tanh form in
+    place of the exact one."""
+    (_, _, rows), = _golden.read_cases("bias_residual_gelu_closed_forms.txt")
+    f = lambda k: np.array([float(v) for v in rows[k]], dtype=np.float64)
+    x = np.stack([f("x0"), f("x1")]).astype(np.float32)
+    r = np.stack([f("r0"), f("r1")]).astype(np.float32)
+    b = f("b").astype(np.float32)
+    want = np.stack([f("y0"), f("y1")])
+    np.testing.assert_allclose(oracle.bias_residual_gelu(x, r, b), want, rtol=0, atol=4e-16)
+
+
+@pytest.mark.parametrize("approximate", ["none", "tanh"])
+def test_bias_residual_gelu_matches_torch(oracle, approximate):
+    """torch's float64 GELU of x + b + residual on a non-square batch, with and
+    without each of the optional inputs, both GELU forms."""
+    rng = _rng(97)
+    x = rng.normal(0, 2, size=(7, 13)).astype(np.float32)
+    r = rng.normal(0, 1, size=(7, 13)).astype(np.float32)
+    b = rng.normal(0, 0.5, size=13).astype(np.float32)
+    g = lambda s: torch.nn.functional.gelu(torch.from_numpy(s), approximate=approximate).numpy()
+    xd, rd, bd = x.astype(np.float64), r.astype(np.float64), b.astype(np.float64)
+    # the tanh form: the pages' 0.79788456 against torch's sqrt(2 / pi), 1e-9 apart relatively
+    atol = 1e-14 if approximate == "none" else 1e-9
+    for res, bias, s in ((r, b, xd + bd + rd), (None, b, xd + bd), (r, None, xd + rd), (None, None, xd)):
+        np.testing.assert_allclose(oracle.bias_residual_gelu(x, res, bias, approximate), g(s), rtol=0, atol=atol)
+
+
+def test_bias_residual_gelu_strides(oracle):
+    """x padded with NaN to a stride ld > N, the residual to another stride:
+    equal to the contiguous computation."""
+    rng = _rng(101)
+    M, N = 5, 9
+    x = rng.normal(size=(M, N)).astype(np.float32)
+    r = rng.normal(size=(M, N)).astype(np.float32)
+    b = rng.normal(size=N).astype(np.float32)
+    xp = np.full((M, 12), np.nan, np.float32)
+    xp[:, :N] = x
+    rp = np.full((M, 16), np.nan, np.float32)
+    rp[:, :N] = r
+    want = oracle.bias_residual_gelu(x, r, b)
+    np.testing.assert_array_equal(oracle.bias_residual_gelu(xp[:, :N], rp[:, :N], b), want)
+    np.testing.assert_array_equal(oracle.bias_residual_gelu(xp[:, :N], r, b), want)
+    rq = np.full((M, 12), np.nan, np.float32)  # the same padded stride as x: passed through as is
+    rq[:, :N] = r
+    np.testing.assert_array_equal(oracle.bias_residual_gelu(xp[:, :N], rq[:, :N], b), want)
