@@ -45,7 +45,7 @@ STEP = ["softmax_bf16_causal_32768x4096", "online_softmax_f32_64x1048576", "laye
 DOMINANT = "layernorm_gelu_bf16_65536x8192"
 KERNELS_PER_CALL = {"softmax": 1, "softmax_causal": 1, "online_softmax": 2, "layernorm_gelu": 1,
                     "layernorm_gelu_erf": 1, "rmsnorm": 1, "residual_rmsnorm": 1, "row_sum": 1, "row_max": 1,
-                    "layernorm_gelu_backward": 2}
+                    "layernorm_gelu_backward": 2, "bias_residual_gelu": 1}
 L2_BYTES = 129 * 10**6
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "ln_gelu_bf16_65536x8192.txt")
@@ -72,6 +72,8 @@ def alg_bytes(wl: workloads.Workload) -> int:
         return 2 * rows + (wl.N * es if wl.affine else 0)
     if wl.op == "softmax_causal":  # kept entries read, every output written
         return causal_alg_bytes(wl, wl.N)
+    if wl.op == "bias_residual_gelu":  # x, residual in; y out; the bias once
+        return 3 * wl.M * wl.N * es + wl.N * es
     if wl.op == "layernorm_gelu_backward":  # x, dy in; dx out; w, b in; fp32 dw, db out
         return 3 * wl.M * wl.N * es + (2 * wl.N * es if wl.affine else 0) + 2 * wl.N * 4
     return rows
@@ -406,9 +408,11 @@ EXTRA = ["softmax_f32_1024x768", "layernorm_gelu_f32_4096x768", "layernorm_gelu_
          "rmsnorm_bf16_65536x8192", "residual_rmsnorm_bf16_65536x8192", "softmax_causal_bf16_32768x4096",
          "layernorm_gelu_erf_f32_4096x768", "layernorm_gelu_erf_bf16_65536x8192", "row_sum_bf16_65536x8192",
          "row_max_bf16_65536x8192", "layernorm_gelu_backward_f32_4096x768",
-         "layernorm_gelu_backward_bf16_65536x8192"]
+         "layernorm_gelu_backward_bf16_65536x8192", "bias_residual_gelu_f32_4096x768",
+         "bias_residual_gelu_bf16_65536x8192"]
 SMALL = {"softmax_f32_1024x768", "layernorm_gelu_f32_4096x768", "rmsnorm_f32_4096x768",
-         "residual_rmsnorm_f32_4096x768", "layernorm_gelu_erf_f32_4096x768", "layernorm_gelu_backward_f32_4096x768"}
+         "residual_rmsnorm_f32_4096x768", "layernorm_gelu_erf_f32_4096x768", "layernorm_gelu_backward_f32_4096x768",
+         "bias_residual_gelu_f32_4096x768"}
 
 
 def run_extras(dev, stream, iters=50):
@@ -434,6 +438,8 @@ def run_extras(dev, stream, iters=50):
         def call():
             if wl.op == "layernorm_gelu_backward":
                 ro.rowops_layernorm_gelu_backward(x, inp["dy"], inp.get("w"), inp.get("b"), wl.eps, y, dw, db, ws)
+            elif wl.op == "bias_residual_gelu":
+                ro.rowops_bias_residual_gelu(x, inp["residual"], inp["b"], y)
             elif wl.op == "softmax":
                 ro.rowops_softmax(x, y)
             elif wl.op == "row_sum":
@@ -465,7 +471,8 @@ def run_extras(dev, stream, iters=50):
                "hot_rows_per_s": wl.M / hot}
         if alg_bytes(wl) > L2_BYTES:
             rec["frac_of_" + measured_peak()[1]] = rec["hot_gbs"] / measured_peak()[0]
-        if wl.op in ("rmsnorm", "residual_rmsnorm", "layernorm_gelu_backward") and wl.M * wl.N > 10**6:
+        if wl.op in ("rmsnorm", "residual_rmsnorm", "layernorm_gelu_backward", "bias_residual_gelu") and \
+                wl.M * wl.N > 10**6:
             rec["torch_eager"] = torch_eager_time(wl, inp, stream)
         if name in SMALL:
             cold = []
@@ -506,11 +513,18 @@ def torch_eager_time(wl, inp, stream, iters=10):
     """PyTorch eager as context: on an RMSNorm workload F.rms_norm, and for the
     fused form x + residual followed by F.rms_norm (two kernels at least); on
     the backward workload autograd's gradients of gelu(layer_norm(x)) (tanh)
-    for x, w, b from a retained graph (the backward kernels only)."""
+    for x, w, b from a retained graph (the backward kernels only); on the fused
+    residual + bias + GELU workload F.gelu(x + b + residual) (three kernels)."""
     import torch.nn.functional as F
 
     x, w = inp["x"], inp.get("w")
-    if wl.op == "layernorm_gelu_backward":
+    if wl.op == "bias_residual_gelu":
+        r, bias = inp["residual"], inp["b"]
+
+        def call():
+            return F.gelu(x + bias + r)
+        what = "F.gelu(x + b + residual)"
+    elif wl.op == "layernorm_gelu_backward":
         xg = x.detach().clone().requires_grad_(True)
         wg = w.detach().clone().requires_grad_(True)
         bg = inp["b"].detach().clone().requires_grad_(True)

@@ -293,6 +293,26 @@ rowops_status_t rowops_layernorm_gelu_backward(const void* x, const void* dy, co
                                                size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Fused residual + bias + GELU [EX §3.4 Approx Activation names "fused residual
+ * + bias + GELU" without a formula; the plain reading]:
+ *   y[i, j] = GELU(x[i, j] + bias[j] + residual[i, j])
+ * with the sum formed in fp32 ((x + bias) + residual) and the GELU exact
+ * (approximate == 0, erf) or the tanh form (approximate == 1).
+ *
+ *   x, y       device pointers to M rows of `ld` elements; y may equal x.
+ *   residual   device pointer to M rows of `ld` elements, or NULL (no residual);
+ *              y may equal it; any other overlap with y is rejected.
+ *   bias       device pointer to N elements of `dtype`, or NULL (no bias); must
+ *              not overlap y.
+ * Aligned rows (x, residual, y at 16-byte row starts, N a multiple of the
+ * 16-byte vector, bias 16-byte aligned) take 16-byte vectors; any other layout
+ * goes element by element.
+ */
+rowops_status_t rowops_bias_residual_gelu(const void* x, const void* residual, const void* bias, void* y,
+                                          int64_t M, int64_t N, int64_t ld, int approximate, rowops_dtype_t dtype,
+                                          cudaStream_t stream);
+
+/*
  * Elementwise GELU of n contiguous elements [EX §3.4 Approx Activation]:
  *   approximate == 0: y = 0.5 x (1 + erf(x / sqrt(2)))             (exact)
  *   approximate == 1: y = 0.5 x (1 + tanh(0.79788456 (x + 0.044715 x^3)))

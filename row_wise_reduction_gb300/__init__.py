@@ -1,7 +1,7 @@
 """rowops: row-wise reduce-then-normalise CUDA kernels for GB300 (sm_103a).
 
 Stable and causal softmax, split-row online softmax, fused LayerNorm -> affine ->
-GELU (tanh or exact) and its backward, RMSNorm and fused residual + RMSNorm, row sums and row
+GELU (tanh or exact) and its backward, fused residual + bias + GELU, RMSNorm and fused residual + RMSNorm, row sums and row
 maxima, exposed through the C ABI of
 ``librowops.so`` (``include/rowops.h``) and the thin ctypes binding in
 :mod:`row_wise_reduction_gb300.rowops`.
@@ -12,6 +12,7 @@ from .rowops import (  # noqa: F401
     RowopsError,
     library,
     library_path,
+    rowops_bias_residual_gelu,
     rowops_device_status,
     rowops_fused_residual_rmsnorm,
     rowops_gelu,

@@ -555,6 +555,31 @@ rowops_status_t rowops_row_max(const void* x, float* out, int64_t M, int64_t N, 
     return reduce_dispatch(x, out, M, N, ld, dtype, 1, stream);
 }
 
+rowops_status_t rowops_bias_residual_gelu(const void* x, const void* residual, const void* bias, void* y,
+                                          int64_t M, int64_t N, int64_t ld, int approximate, rowops_dtype_t dtype,
+                                          cudaStream_t stream) {
+    if (approximate != 0 && approximate != 1) return ROWOPS_ERR_INVALID_VALUE;
+    rowops_status_t st = check_rows(x, y, M, N, ld, dtype);
+    if (st == ROWOPS_OK && residual) st = check_rows(residual, y, M, N, ld, dtype);
+    if (st != ROWOPS_OK) return st;
+    if (M == 0) return ROWOPS_OK;
+    const int es = elem_bytes(dtype);
+    if (bias) {  // read by every row while y is written: apart from y's rows
+        if (!aligned(bias, es)) return ROWOPS_ERR_INVALID_VALUE;
+        const uintptr_t pb = reinterpret_cast<uintptr_t>(bias), py = reinterpret_cast<uintptr_t>(y);
+        const uintptr_t sb = uintptr_t(N) * es, sy = uintptr_t(((M - 1) * ld + N) * es);
+        if (pb < py + sy && py < pb + sb) return ROWOPS_ERR_INVALID_VALUE;
+    }
+    const Tuning tn = read_tuning();
+    LaunchCfg cfg;
+    if ((st = make_cfg(stream, tn, &cfg)) != ROWOPS_OK) return st;
+    const bool vec = tn.family != Family::Looped && N % (16 / es) == 0 && rows_aligned(x, y, ld, es) &&
+                     (!residual || aligned(residual, 16)) && (!bias || aligned(bias, 16));
+    const BiasResidualGeluLaunch fn = dtype == ROWOPS_F32 ? bias_residual_gelu_f32(approximate == 0, vec)
+                                                          : bias_residual_gelu_bf16(approximate == 0, vec);
+    return finish(fn(x, residual, bias, y, M, N, ld, cfg));
+}
+
 namespace {
 rowops_status_t ln_gelu_dispatch(const void* x, void* y, const void* w, const void* b, float eps, int64_t M,
                                  int64_t N, int64_t ld, rowops_dtype_t dtype, cudaStream_t stream, bool erf);

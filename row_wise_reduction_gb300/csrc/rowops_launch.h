@@ -150,6 +150,13 @@ using GeluLaunch = cudaError_t (*)(const void* x, void* y, int64_t n, const Laun
 GeluLaunch gelu_f32(bool erf);
 GeluLaunch gelu_bf16(bool erf);
 
+// y = GELU(x + b + residual) over M rows of stride ld (residual, b may be NULL);
+// vec: the 16-byte vector form (aligned rows, N a multiple of the vector).
+using BiasResidualGeluLaunch = cudaError_t (*)(const void* x, const void* r, const void* b, void* y, int64_t M,
+                                               int64_t N, int64_t ld, const LaunchCfg& cfg);
+BiasResidualGeluLaunch bias_residual_gelu_f32(bool erf, bool vec);
+BiasResidualGeluLaunch bias_residual_gelu_bf16(bool erf, bool vec);
+
 // LayerNorm -> affine -> tanh-GELU backward: per-CTA dw, db partials (2 N
 // floats each, at most bwd_max_partials(N) CTAs) reduced by ln_gelu_bwd_reduce.
 // The cap keeps the partials within 32 MiB (at least 152, at most 4096 CTAs).

@@ -35,6 +35,7 @@ __all__ = [
     "rowops_layernorm_gelu_backward",
     "rowops_layernorm_gelu_backward_workspace_bytes",
     "rowops_gelu",
+    "rowops_bias_residual_gelu",
     "rowops_rmsnorm",
     "rowops_fused_residual_rmsnorm",
     "rowops_status_string",
@@ -115,6 +116,9 @@ def library() -> ctypes.CDLL:
         L.rowops_fused_residual_rmsnorm.restype = ctypes.c_int
         L.rowops_fused_residual_rmsnorm.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _i64, _i64, _i64,
                                                     ctypes.c_int, _vp]
+        L.rowops_bias_residual_gelu.restype = ctypes.c_int
+        L.rowops_bias_residual_gelu.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int,
+                                                _vp]
         L.rowops_layernorm_gelu_backward_workspace_bytes.restype = ctypes.c_size_t
         L.rowops_layernorm_gelu_backward_workspace_bytes.argtypes = [_i64, _i64, ctypes.c_int]
         L.rowops_layernorm_gelu_backward.restype = ctypes.c_int
@@ -336,6 +340,31 @@ def rowops_layernorm_gelu_backward(
         _dtype_code(x), workspace.data_ptr(), nbytes, _stream(stream))
     _check("rowops_layernorm_gelu_backward", st)
     return dx, dw, db
+
+
+def rowops_bias_residual_gelu(
+    x: torch.Tensor,
+    residual: Optional[torch.Tensor] = None,
+    bias: Optional[torch.Tensor] = None,
+    y: Optional[torch.Tensor] = None,
+    approximate: str = "none",
+    *,
+    stream=None,
+) -> torch.Tensor:
+    """y = GELU(x + bias + residual) for every row of ``x`` (bias per column;
+    residual shaped and strided like x; either may be None); approximate
+    "none" (exact, erf) or "tanh"."""
+    if approximate not in ("none", "tanh"):
+        raise ValueError('approximate must be "none" or "tanh"')
+    M, N, ld = _rows(x, "x")
+    if residual is not None:
+        _out_like(x, residual)  # same shape, dtype, device and row stride
+    y = _out_like(x, y)
+    st = library().rowops_bias_residual_gelu(
+        x.data_ptr(), residual.data_ptr() if residual is not None else None, _weight(bias, x, N, "bias"),
+        y.data_ptr(), M, N, ld, 0 if approximate == "none" else 1, _dtype_code(x), _stream(stream))
+    _check("rowops_bias_residual_gelu", st)
+    return y
 
 
 def _weight(w: Optional[torch.Tensor], x: torch.Tensor, N: int, name: str = "w"):

@@ -27,7 +27,8 @@ class Workload:
 
     name: str
     op: str  # "softmax" | "softmax_causal" | "online_softmax" | "layernorm_gelu" | "layernorm_gelu_erf" |
-    #          "layernorm_gelu_backward" | "rmsnorm" | "residual_rmsnorm" | "row_sum" | "row_max"
+    #          "layernorm_gelu_backward" | "rmsnorm" | "residual_rmsnorm" | "row_sum" | "row_max" |
+    #          "bias_residual_gelu"
     dtype: str  # "f32" | "bf16"
     M: int  # rows
     N: int  # columns (reduction length)
@@ -83,6 +84,12 @@ WORKLOADS: Dict[str, Workload] = {
                  affine=True, grad=True),
         Workload("layernorm_gelu_backward_bf16_65536x8192", "layernorm_gelu_backward", "bf16", 65536, 8192,
                  seed=4, affine=True, grad=True),
+        # fused residual + bias + GELU [Triton Kernel 实现练习 §3.4] on the LayerNorm+GELU shapes: x,
+        # residual ~ N(0, 1), the bias is the affine b ~ N(0, 0.1^2)
+        Workload("bias_residual_gelu_f32_4096x768", "bias_residual_gelu", "f32", 4096, 768, seed=11, affine=True,
+                 residual=True),
+        Workload("bias_residual_gelu_bf16_65536x8192", "bias_residual_gelu", "bf16", 65536, 8192, seed=12,
+                 affine=True, residual=True),
     ]
 }
 

@@ -35,7 +35,8 @@ def test_header_declares_the_entry_points():
               "rowops_online_softmax_workspace_bytes", "rowops_online_softmax_status", "rowops_status_string",
               "rowops_rmsnorm", "rowops_fused_residual_rmsnorm", "rowops_softmax_causal", "rowops_row_sum",
               "rowops_row_max", "rowops_layernorm_gelu_erf", "rowops_gelu",
-              "rowops_layernorm_gelu_backward", "rowops_layernorm_gelu_backward_workspace_bytes"):
+              "rowops_layernorm_gelu_backward", "rowops_layernorm_gelu_backward_workspace_bytes",
+              "rowops_bias_residual_gelu"):
         assert n in names
 
 
@@ -224,6 +225,27 @@ def test_layernorm_gelu_backward_validation(lib):
     assert f(*args(b=X + 0x40001, dt=BF16)) == INVALID  # misaligned b
     assert f(*args(ld=7)) == INVALID
     assert f(*args(dt=5)) == INVALID
+
+
+def test_bias_residual_gelu_validation(lib):
+    f = lib.rowops_bias_residual_gelu
+    R, BI = 0x300000, 0x500000
+
+    def args(x=X, r=R, b=BI, y=Y, M=4, N=8, ld=8, ap=0, dt=F32):
+        return (x, r, b, y, M, N, ld, ap, dt, None)
+
+    assert f(*args(ap=2)) == INVALID
+    assert f(*args(ap=-1)) == INVALID
+    assert f(*args(x=None)) == INVALID
+    assert f(*args(y=X + 16)) == INVALID  # y partly overlaps x
+    assert f(*args(y=R + 16)) == INVALID  # y partly overlaps the residual
+    assert f(*args(b=Y + 8)) == INVALID  # bias inside y's rows
+    assert f(*args(b=BI + 2)) == INVALID  # bias not 4-byte aligned for fp32
+    assert f(*args(r=R + 1, dt=BF16)) == INVALID  # residual not 2-byte aligned
+    assert f(*args(ld=7)) == INVALID
+    assert f(*args(dt=3)) == INVALID
+    assert f(*args(N=1 << 31, ld=1 << 31)) == UNSUPPORTED
+    assert f(*args(M=0)) == OK  # no rows: nothing to do, no CUDA call
 
 
 def test_binding_has_no_fallback(monkeypatch, tmp_path):
