@@ -239,13 +239,34 @@ def barrier():
 # ---------------------------------------------------------------------------
 # the CPU oracle on a bounded sample
 # ---------------------------------------------------------------------------
-def oracle_run(oracle, wl, xs, extra):
+def oracle_run(oracle, wl, xs, extra, lo=0, hi=None):
+    """The oracle's version of ``wl``'s operation on sampled rows xs (rows
+    lo:hi of the sample; per-row inputs and row indices in ``extra``)."""
+    hi = len(xs) if hi is None else hi
+    xs = xs[lo:hi]
+    per_row = {k: extra[k][lo:hi] for k in ("residual", "dy") if extra.get(k) is not None}
+    w, b = extra.get("w"), extra.get("b")
     if wl.op == "softmax":
         oracle.softmax(xs)
     elif wl.op == "online_softmax":
         oracle.split_softmax(xs, extra["chunk"])
+    elif wl.op == "softmax_causal":
+        for x, r in zip(xs, extra["rows"][lo:hi]):
+            oracle.softmax_causal_rows_at(x, int(r), wl.N, 0)
+    elif wl.op in ("row_sum", "row_max"):
+        getattr(oracle, wl.op)(xs)
+    elif wl.op == "rmsnorm":
+        oracle.rmsnorm(xs, w, wl.eps)
+    elif wl.op == "residual_rmsnorm":
+        oracle.residual_rmsnorm(xs, per_row["residual"], w, wl.eps, storage=wl.dtype)
+    elif wl.op == "layernorm_gelu_erf":
+        oracle.layernorm_gelu_erf(xs, w, b, wl.eps)
+    elif wl.op == "layernorm_gelu_backward":
+        oracle.layernorm_gelu_backward(xs, per_row["dy"], w, b, wl.eps)
+    elif wl.op == "bias_residual_gelu":
+        oracle.bias_residual_gelu(xs, per_row["residual"], b)
     else:
-        oracle.layernorm_gelu(xs, extra["w"], extra["b"], wl.eps)
+        oracle.layernorm_gelu(xs, w, b, wl.eps)
 
 
 def oracle_run_threads(oracle, wl, xs, extra, threads):
@@ -257,9 +278,9 @@ def oracle_run_threads(oracle, wl, xs, extra, threads):
     from concurrent.futures import ThreadPoolExecutor
 
     bounds = [len(xs) * i // threads for i in range(threads + 1)]
-    parts = [xs[a:b] for a, b in zip(bounds, bounds[1:]) if b > a]
-    with ThreadPoolExecutor(len(parts)) as ex:
-        list(ex.map(lambda part: oracle_run(oracle, wl, part, extra), parts))
+    spans = [(a, b) for a, b in zip(bounds, bounds[1:]) if b > a]
+    with ThreadPoolExecutor(len(spans)) as ex:
+        list(ex.map(lambda ab: oracle_run(oracle, wl, xs, extra, *ab), spans))
 
 
 def host_threads():
@@ -272,20 +293,26 @@ def host_threads():
 def cpu_sample_rows(wl, rows, device=None, dev_inputs=None):
     """fp32 host rows of ``wl`` (copied from the device inputs when given,
     else drawn on the CPU with the causal mask of rows spread over the
-    workload) plus w, b."""
+    workload) plus w, b, the same rows of the residual / dy where the
+    operation has them, and the row indices."""
     import numpy as np
 
     if dev_inputs is not None:
         idx = torch.as_tensor(rows, device=dev_inputs["x"].device)
-        xs = dev_inputs["x"][idx].float().cpu().numpy()
-        extra = {k: dev_inputs[k].float().cpu().numpy() for k in ("w", "b") if k in dev_inputs}
+        src = dev_inputs
     else:
-        inp = workloads.make_inputs(wl.with_shape(M=len(rows)), "cpu", row_ids=torch.as_tensor(rows))
-        xs = inp["x"].float().numpy()
-        extra = {k: inp[k].float().numpy() for k in ("w", "b") if k in inp}
+        idx = None
+        src = workloads.make_inputs(wl.with_shape(M=len(rows)), "cpu", row_ids=torch.as_tensor(rows))
+    pick = (lambda t: t[idx]) if idx is not None else (lambda t: t)
+    xs = pick(src["x"]).float().cpu().numpy()
+    extra = {k: src[k].float().cpu().numpy() for k in ("w", "b") if k in src}
+    for k in ("residual", "dy"):
+        if k in src:
+            extra[k] = np.ascontiguousarray(pick(src[k]).float().cpu().numpy())
     extra.setdefault("w", None)
     extra.setdefault("b", None)
     extra["chunk"] = 8192
+    extra["rows"] = list(rows)
     return np.ascontiguousarray(xs), extra
 
 
@@ -296,14 +323,15 @@ def spread_rows(M, k):
     return [int(i * step) for i in range(k)]
 
 
-def cpu_baseline(oracle, dev_inputs=None, budget_s=12.0, threads=1):
-    """Time the oracle on ~budget_s seconds (wall) of the step's workloads in
-    `threads` host threads; return GB/s on the same algorithmic-byte basis,
-    a description of the sample and the seconds spent."""
+def cpu_baseline(oracle, dev_inputs=None, budget_s=12.0, threads=1, wls=None):
+    """Time the oracle on ~budget_s seconds (wall) of the timed workloads
+    (`wls`, name -> Workload; default the step's) in `threads` host threads;
+    return GB/s on the same algorithmic-byte basis, a description of the
+    sample and the seconds spent."""
+    wls = wls or {n: workloads.WORKLOADS[n] for n in STEP}
     total_bytes, total_s, desc = 0, 0.0, []
-    per_op = budget_s / len(STEP)
-    for name in STEP:
-        wl = workloads.WORKLOADS[name]
+    per_op = budget_s / len(wls)
+    for name, wl in wls.items():
         # calibrate on one row, then size the sample to the budget
         xs, extra = cpu_sample_rows(wl, [wl.M // 2], dev_inputs=dev_inputs.get(name) if dev_inputs else None)
         t0 = time.perf_counter()
@@ -628,6 +656,10 @@ def run_rowops(args):
         if wl.op == "online_softmax":
             nb = ro.rowops_online_softmax_workspace_bytes(wl.M, wl.N, workloads.torch_dtype(wl.dtype))
             ws[n] = torch.empty(nb, dtype=torch.uint8, device=dev)
+        if wl.op == "layernorm_gelu_backward":
+            nb = ro.rowops_layernorm_gelu_backward_workspace_bytes(wl.M, wl.N, workloads.torch_dtype(wl.dtype))
+            ws[n] = (torch.empty(nb, dtype=torch.uint8, device=dev), torch.empty(wl.N, device=dev),
+                     torch.empty(wl.N, device=dev))
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
 
@@ -653,6 +685,12 @@ def run_rowops(args):
             ro.rowops_rmsnorm(x, inputs[n]["w"], wl.eps, y)
         elif wl.op == "residual_rmsnorm":
             ro.rowops_fused_residual_rmsnorm(x, inputs[n]["residual"], inputs[n]["w"], wl.eps, y, res_out[n])
+        elif wl.op == "bias_residual_gelu":
+            ro.rowops_bias_residual_gelu(x, inputs[n]["residual"], inputs[n]["b"], y)
+        elif wl.op == "layernorm_gelu_backward":
+            wsb, dw, db = ws[n]
+            ro.rowops_layernorm_gelu_backward(x, inputs[n]["dy"], inputs[n]["w"], inputs[n]["b"], wl.eps, y, dw, db,
+                                              wsb)
         else:
             ro.rowops_layernorm_gelu(x, inputs[n]["w"], inputs[n]["b"], wl.eps, y)
 
@@ -701,7 +739,7 @@ def run_rowops(args):
         host_in = {n: inputs[n]["x"].cpu().pin_memory() for n in names}
         result = {n: reds.get(n, outputs[n]) for n in names}  # what each call produces
         host_out = {n: torch.empty(result[n].shape, dtype=result[n].dtype).pin_memory() for n in names}
-        host_wb = {n: {k: inputs[n][k].cpu().pin_memory() for k in ("w", "b", "residual") if k in inputs[n]}
+        host_wb = {n: {k: inputs[n][k].cpu().pin_memory() for k in ("w", "b", "residual", "dy") if k in inputs[n]}
                    for n in names}
         host_ro = {n: torch.empty(res_out[n].shape, dtype=res_out[n].dtype).pin_memory() for n in res_out}
         h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + \
@@ -748,8 +786,10 @@ def run_rowops(args):
 
         oracle.build()
         threads = host_threads()
-        v, sample, spent = cpu_baseline(oracle, dev_inputs=inputs, budget_s=args.cpu_budget_s / 2, threads=threads)
-        v1, sample1, spent1 = cpu_baseline(oracle, dev_inputs=inputs, budget_s=args.cpu_budget_s / 2, threads=1)
+        v, sample, spent = cpu_baseline(oracle, dev_inputs=inputs, budget_s=args.cpu_budget_s / 2, threads=threads,
+                                        wls=wls)
+        v1, sample1, spent1 = cpu_baseline(oracle, dev_inputs=inputs, budget_s=args.cpu_budget_s / 2, threads=1,
+                                           wls=wls)
         cpu = {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample,
                "seconds": spent, "single_core": {"value": v1, "sample": sample1, "seconds": spent1}}
 
