@@ -52,10 +52,20 @@ static cudaError_t launch_split_tma_v(const void* x, void* y, int64_t M, int64_t
     k1<<<g1, kSplitTmaTpr, smem, cfg.stream>>>(static_cast<const T*>(x), items, nchunks, ld, status, partials, nbuf,
                                                cfg.wait_ns, cfg.stall_row);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const int g2 = grid_for(reinterpret_cast<const void*>(k2), kSplitTmaTpr, smem, items, cfg);
-    k2<<<g2, kSplitTmaTpr, smem, cfg.stream>>>(static_cast<const T*>(x), static_cast<T*>(y), items, nchunks, ld,
-                                               partials, status, nbuf, cfg.wait_ns, cfg.stall_row);
-    return cudaGetLastError();
+    // pass 2 as a programmatic dependent of pass 1 (it fills its ring while
+    // pass 1 drains, and waits for pass 1 before its first partial)
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(unsigned(grid_for(reinterpret_cast<const void*>(k2), kSplitTmaTpr, smem, items, cfg)));
+    lc.blockDim = dim3(kSplitTmaTpr);
+    lc.dynamicSmemBytes = smem;
+    lc.stream = cfg.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    return cudaLaunchKernelEx(&lc, k2, static_cast<const T*>(x), static_cast<T*>(y), items, nchunks, ld,
+                              const_cast<const float2*>(partials), status, nbuf, cfg.wait_ns, cfg.stall_row);
 }
 
 template <typename T>

@@ -18,6 +18,12 @@
 //           chunk of the row), y = exp(x - m) / d.
 // A wait that gives up (bounded) is reported through the workspace status
 // word after the CTA's copies in flight have landed.
+//
+// Pass 2 is launched as a programmatic dependent of pass 1: each pass-1 CTA
+// signals once it has issued its last copy, so pass-2 CTAs start as pass-1
+// CTAs leave and fill their rings with x (which pass 1 does not write); they
+// wait for pass 1 to complete (griddepcontrol.wait) before reading a partial
+// or writing y. Launched the ordinary way, the wait returns at once.
 #pragma once
 
 #include "online_softmax_kernels.cuh"
@@ -102,9 +108,14 @@ __global__ void __launch_bounds__(TPR)
     const SplitForward order;
     split_start<T, TPR, VPT>(ring, x, items, nchunks, ld, stall_row, order);
 
+    bool signalled = false;
     for (int64_t i = 0;; ++i) {
         const int64_t k = int64_t(blockIdx.x) + i * gridDim.x;
         if (k >= items) break;
+        if (!signalled && k + int64_t(nbuf) * gridDim.x >= items) {  // no copy left to issue
+            asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+            signalled = true;
+        }
         const int s = int(i % nbuf);
         int fail = !mbar_wait(ring.bar + s, uint32_t((i / nbuf) & 1), wait_ns);
         const char* sb = ring.slot(s);
@@ -149,6 +160,7 @@ __global__ void __launch_bounds__(TPR)
     const int t = threadIdx.x;
     const SplitReverse order{items};
     split_start<T, TPR, VPT>(ring, x, items, nchunks, ld, stall_row, order);
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // pass 1's partials are complete and visible
 
     for (int64_t i = 0;; ++i) {
         const int64_t k = int64_t(blockIdx.x) + i * gridDim.x;
