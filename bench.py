@@ -747,25 +747,50 @@ def run_rowops(args):
         d2h = sum(t.numel() * t.element_size() for t in host_out.values()) + \
             sum(t.numel() * t.element_size() for t in host_ro.values())
         ke = max(2, min(K, args.e2e_steps))
+        # three streams: host->device copies, the library calls, device->host
+        # copies (separate copy engines, so the two directions overlap). Per
+        # workload, a step's input copies wait until the previous step's call
+        # has read its inputs, and its call until the previous step's result
+        # has been copied out.
+        s_in, s_run, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+        called = {n: None for n in names}
+        drained = {n: None for n in names}
 
         def e2e_step():
             for n in names:
-                for kk, t in host_wb[n].items():
-                    inputs[n][kk].copy_(t, non_blocking=True)
-                inputs[n]["x"].copy_(host_in[n], non_blocking=True)
-                call(n, inputs[n]["x"], outputs[n])
-                host_out[n].copy_(result[n], non_blocking=True)
-                if n in host_ro:
-                    host_ro[n].copy_(res_out[n], non_blocking=True)
+                with torch.cuda.stream(s_in):
+                    if called[n] is not None:
+                        s_in.wait_event(called[n])
+                    for kk, t in host_wb[n].items():
+                        inputs[n][kk].copy_(t, non_blocking=True)
+                    inputs[n]["x"].copy_(host_in[n], non_blocking=True)
+                    loaded = torch.cuda.Event()
+                    loaded.record(s_in)
+                with torch.cuda.stream(s_run):
+                    s_run.wait_event(loaded)
+                    if drained[n] is not None:
+                        s_run.wait_event(drained[n])
+                    call(n, inputs[n]["x"], outputs[n])
+                    called[n] = torch.cuda.Event()
+                    called[n].record(s_run)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(called[n])
+                    host_out[n].copy_(result[n], non_blocking=True)
+                    if n in host_ro:
+                        host_ro[n].copy_(res_out[n], non_blocking=True)
+                    drained[n] = torch.cuda.Event()
+                    drained[n].record(s_out)
 
         e2e_step()
         torch.cuda.synchronize()
         barrier()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
+        a.record(s_in)
         for _ in range(ke):
             e2e_step()
-        b.record(stream)
+        s_in.wait_stream(s_run)
+        s_in.wait_stream(s_out)
+        b.record(s_in)
         torch.cuda.synchronize()
         barrier()
         es, eb = aggregate(a.elapsed_time(b) / 1e3, step_bytes * ke)
