@@ -9,6 +9,8 @@
 #include "rowops.h"
 #include "rowops_launch.h"
 
+extern char** environ;  // POSIX
+
 namespace rowops {
 namespace {
 
@@ -37,40 +39,51 @@ struct Tuning {
     int unit_rows = 0;        // dynamic schedule: rows per group in a work unit (0: automatic)
 };
 
-int env_int(const char* name, int dflt) {
-    const char* v = std::getenv(name);
+// The whole value as a decimal integer, else `dflt` (unset, empty or not a number).
+long long parse_int(const char* v, long long dflt) {
     if (!v || !*v) return dflt;
     char* end = nullptr;
-    const long r = std::strtol(v, &end, 10);
-    return (end && *end == '\0') ? int(r) : dflt;
+    const long long r = std::strtoll(v, &end, 10);
+    return (end && *end == '\0') ? r : dflt;
 }
 
+// One pass over the environment, looking only at ROWOPS_* entries (each call
+// scans it once instead of once per knob).
 Tuning read_tuning() {
     Tuning t;
-    t.tpr = env_int("ROWOPS_FORCE_TPR", 0);
-    t.vpt = env_int("ROWOPS_FORCE_VPT", 0);
-    if (env_int("ROWOPS_FORCE_LOOPED", 0) != 0) t.family = Family::Looped;
-    if (const char* k = std::getenv("ROWOPS_KERNEL")) {
-        if (!std::strcmp(k, "tma")) t.family = Family::Tma;
-        else if (!std::strcmp(k, "reg")) t.family = Family::Reg;
-        else if (!std::strcmp(k, "looped")) t.family = Family::Looped;
+    bool force_looped = false;
+    const char* kernel = nullptr;
+    for (char** e = environ; e && *e; ++e) {
+        const char* kv = *e;
+        if (std::strncmp(kv, "ROWOPS_", 7) != 0) continue;
+        const char* name = kv + 7;
+        const char* eq = std::strchr(name, '=');
+        if (!eq) continue;
+        const size_t n = size_t(eq - name);
+        const char* v = eq + 1;
+        auto is = [&](const char* key) { return std::strlen(key) == n && std::strncmp(name, key, n) == 0; };
+        if (is("FORCE_TPR")) t.tpr = int(parse_int(v, 0));
+        else if (is("FORCE_VPT")) t.vpt = int(parse_int(v, 0));
+        else if (is("FORCE_LOOPED")) force_looped = parse_int(v, 0) != 0;
+        else if (is("KERNEL")) kernel = v;
+        else if (is("CTAS_PER_SM")) t.ctas_per_sm = int(parse_int(v, 0));
+        else if (is("RING_BUFFERS")) t.ring = int(parse_int(v, 0));
+        else if (is("ROWS_PER_CTA")) t.rows = int(parse_int(v, 0));
+        else if (is("PERSIST_LOOKAHEAD")) t.lookahead = int(parse_int(v, 0));
+        else if (is("PERSIST_L2")) t.l2 = int(parse_int(v, 0));
+        else if (is("PERSIST_PREFETCH")) t.prefetch = int(parse_int(v, 0));
+        else if (is("WAIT_LIMIT_NS")) t.wait_ns = std::strtoll(v, nullptr, 10);
+        else if (is("TEST_STALL_ROW")) t.stall_row = std::strtoll(v, nullptr, 10);
+        else if (is("UNIT_ROWS")) t.unit_rows = int(parse_int(v, 0));
+        else if (is("SCHED")) t.sched = !std::strcmp(v, "static") ? 1 : (!std::strcmp(v, "dynamic") ? 2 : 0);
+        else if (is("ONLINE")) t.online = !std::strcmp(v, "two_pass") ? 1 : (!std::strcmp(v, "single_read") ? 2 : 0);
     }
-    t.ctas_per_sm = env_int("ROWOPS_CTAS_PER_SM", 0);
-    t.ring = env_int("ROWOPS_RING_BUFFERS", 0);
-    t.rows = env_int("ROWOPS_ROWS_PER_CTA", 0);
-    t.lookahead = env_int("ROWOPS_PERSIST_LOOKAHEAD", 0);
-    t.l2 = env_int("ROWOPS_PERSIST_L2", 0);
-    if (const char* v = std::getenv("ROWOPS_WAIT_LIMIT_NS")) t.wait_ns = std::strtoll(v, nullptr, 10);
-    if (const char* v = std::getenv("ROWOPS_TEST_STALL_ROW")) t.stall_row = std::strtoll(v, nullptr, 10);
-    t.prefetch = env_int("ROWOPS_PERSIST_PREFETCH", 0);
-    t.unit_rows = env_int("ROWOPS_UNIT_ROWS", 0);
-    if (const char* k = std::getenv("ROWOPS_SCHED")) {
-        if (!std::strcmp(k, "static")) t.sched = 1;
-        else if (!std::strcmp(k, "dynamic")) t.sched = 2;
-    }
-    if (const char* k = std::getenv("ROWOPS_ONLINE")) {
-        if (!std::strcmp(k, "two_pass")) t.online = 1;
-        else if (!std::strcmp(k, "single_read")) t.online = 2;
+    // ROWOPS_KERNEL, when set to a family, overrides ROWOPS_FORCE_LOOPED
+    if (force_looped) t.family = Family::Looped;
+    if (kernel) {
+        if (!std::strcmp(kernel, "tma")) t.family = Family::Tma;
+        else if (!std::strcmp(kernel, "reg")) t.family = Family::Reg;
+        else if (!std::strcmp(kernel, "looped")) t.family = Family::Looped;
     }
     return t;
 }

@@ -163,9 +163,11 @@ def _out_like(x: torch.Tensor, y: Optional[torch.Tensor]) -> torch.Tensor:
     return y
 
 
-def _stream(stream) -> int:
+def _stream(stream, device=None) -> int:
     if stream is None:
-        return torch.cuda.current_stream().cuda_stream
+        # the raw handle of the current stream (the cheap form of
+        # torch.cuda.current_stream().cuda_stream)
+        return torch._C._cuda_getCurrentRawStream(torch.cuda.current_device() if device is None else device)
     if isinstance(stream, torch.cuda.Stream):
         return stream.cuda_stream
     return int(stream)
