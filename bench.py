@@ -824,7 +824,7 @@ def run_rowops(args):
     if DOMINANT in per_op:
         ach = per_op[DOMINANT]["gbs"]
         roof = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
-                "peak_kind": peak_kind, "kernel": "ln_gelu_tma_kernel<bf16, 128 threads/row, 8 vectors/thread, 4 rows/CTA, full rows>",
+                "peak_kind": peak_kind, "kernel": "ln_gelu_tma_kernel<bf16, 128 threads/row, 8 vectors/thread, 5 rows/CTA, full rows>",
                 "traffic": profiled_traffic() if args.rows_scale == 1.0 else None,
                 "algorithmic_bytes_per_launch": alg_bytes(wls[DOMINANT])}
     line = {

@@ -41,7 +41,8 @@
  *   ROWOPS_FORCE_LOOPED=1         same as ROWOPS_KERNEL=looped
  *   ROWOPS_RING_BUFFERS=<2..16>   rows in flight per row group of the row pipeline (chunks per
  *                                 CTA of the two-pass split softmax on full chunks, default 3)
- *   ROWOPS_ROWS_PER_CTA=<1|2|4|8> row groups per CTA of the LayerNorm+GELU and RMSNorm row pipelines
+ *   ROWOPS_ROWS_PER_CTA=<1|2|4|5|8> row groups per CTA of the LayerNorm+GELU and RMSNorm row
+ *                                 pipelines (5: LayerNorm+GELU with 128 threads x 8 vectors only)
  *   ROWOPS_ONLINE=two_pass|single_read  split-row softmax form (default two_pass); single_read
  *                                 keeps each chunk on chip between the passes (rows of
  *                                 >= ~2^19.3 entries, 16-byte aligned, cooperative launch)

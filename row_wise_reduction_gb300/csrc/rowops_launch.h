@@ -89,14 +89,17 @@ SoftmaxCausalLaunch softmax_causal_looped_bf16();
 // LayerNorm+GELU instantiations: ROWS = 1 with TPR in kTmaBlocks and VPT in
 // kTmaVpts, or several row groups per CTA sharing one staging of w, b with TPR
 // in kTmaMultiTpr, VPT in kTmaMultiVpt, ROWS in kTmaMultiRows (at most 512
-// threads); full rows or general (unaligned) rows. Each comes with its launcher
+// threads; 640 for 5 groups of 128 threads x 8 vectors with the tanh GELU, the
+// tile of 8192-column bf16 / 4096-column fp32 rows, whose ~96 registers a
+// thread fit 640 threads and whose ring and w, b staging fit 5 groups); full
+// rows or general rows. Each comes with its launcher
 // and a query of how many of its CTAs an SM holds for a given N and ring depth.
 constexpr int kTmaMultiTpr[] = {64, 128, 256};
 constexpr int kNumTmaMultiTpr = 3;
 constexpr int kTmaMultiVpt[] = {2, 4, 8};
 constexpr int kNumTmaMultiVpt = 3;
-constexpr int kTmaMultiRows[] = {2, 4, 8};
-constexpr int kNumTmaMultiRows = 3;
+constexpr int kTmaMultiRows[] = {2, 4, 5, 8};
+constexpr int kNumTmaMultiRows = 4;
 using TmaCtasQuery = int (*)(int64_t N, int nbuf, const LaunchCfg& cfg);
 struct TmaLnGeluKernel {
     TmaLnGeluLaunch launch;     // nullptr: no such instantiation
