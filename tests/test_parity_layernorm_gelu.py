@@ -296,3 +296,25 @@ def test_ln_gelu_tma_fewer_rows_than_phase_classes(oracle, monkeypatch, M, rows)
     from row_wise_reduction_gb300 import rowops_device_status
 
     assert rowops_device_status() == 0
+
+
+@pytest.mark.parametrize("dtype,N,ld,offset", [("bf16", 8192, 8192, 0), ("f32", 4096, 4096, 0),
+                                               ("bf16", 8190, 8190, 0), ("bf16", 8192, 8200, 3)])
+@pytest.mark.parametrize("M", [3, 5, 777])
+def test_ln_gelu_tma_five_row_groups(oracle, monkeypatch, dtype, N, ld, offset, M):
+    """Five row groups of 128 threads x 8 vectors in a 640-thread CTA (the tile
+    of 8192-column bf16 and 4096-column fp32 rows): full and general rows,
+    fewer rows than groups, a ragged last round."""
+    monkeypatch.setenv("ROWOPS_KERNEL", "tma")
+    monkeypatch.setenv("ROWOPS_ROWS_PER_CTA", "5")
+    check(oracle, edge(dtype, M, N, seed=M + N + offset), ld=ld, offset=offset)
+    from row_wise_reduction_gb300 import rowops_device_status
+
+    assert rowops_device_status() == 0
+
+
+@pytest.mark.parametrize("dtype,M,N", [("f32", 4096, 768), ("bf16", 3000, 2048), ("f32", 300, 8192)])
+def test_ln_gelu_small_batches_take_register_rows(oracle, dtype, M, N):
+    """Batches of at most 32 MiB go to the register-resident kernel by
+    default; the result equals the row pipeline's within the tolerance."""
+    check(oracle, edge(dtype, M, N, seed=M))
