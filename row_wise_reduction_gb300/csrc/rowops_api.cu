@@ -448,14 +448,19 @@ int grid_for(const void* func, int block, size_t smem, int64_t items, const Laun
     return int(g);
 }
 
-cudaError_t allow_smem(const void* func, size_t smem, const LaunchCfg& cfg) {
-    // the default limit covers static + dynamic shared memory together; opt in
-    // well before the dynamic part alone reaches it
-    if (smem <= 32 * 1024) return cudaSuccess;
+cudaError_t allow_smem(const void* func, size_t smem, const LaunchCfg& cfg, bool max_carveout) {
+    if (smem == 0 || (smem <= 32 * 1024 && !max_carveout)) return cudaSuccess;
     std::lock_guard<std::mutex> lk(g_mu);
     for (auto& s : g_smem)
         if (s.func == func && s.device == cfg.device && s.smem >= smem) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    cudaError_t e = cudaSuccess;
+    if (max_carveout)
+        e = cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 int(cudaSharedmemCarveoutMaxShared));
+    // the default limit covers static + dynamic shared memory together; opt in
+    // well before the dynamic part alone reaches it
+    if (e == cudaSuccess && smem > 32 * 1024)
+        e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e == cudaSuccess) g_smem.push_back(SmemEntry{func, cfg.device, smem});
     return e;
 }

@@ -39,7 +39,10 @@ int grid_for(const void* func, int block, size_t smem, int64_t items, const Laun
 int ctas_per_sm(const void* func, int block, size_t smem, const LaunchCfg& cfg);
 
 // Allow `func` to use `smem` bytes of dynamic shared memory (once per device).
-cudaError_t allow_smem(const void* func, size_t smem, const LaunchCfg& cfg);
+// max_carveout: also ask for the largest shared-memory carveout (for kernels
+// with a small ring per CTA, where the driver's own choice held fewer CTAs per
+// SM than the occupancy calculator, which sizes the persistent grid, assumed)
+cudaError_t allow_smem(const void* func, size_t smem, const LaunchCfg& cfg, bool max_carveout = false);
 
 // Thread-per-row choices of the register-resident kernels.
 constexpr int kTprChoices[] = {16, 32, 64, 128, 256, 512, 1024};

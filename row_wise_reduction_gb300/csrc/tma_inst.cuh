@@ -17,7 +17,9 @@ cudaError_t launch_softmax_tma_mask(const void* x, void* y, int64_t M, int64_t N
                                     CausalMask cm, const LaunchCfg& cfg) {
     auto kern = softmax_tma_kernel<T, TPR, VPT, 1, FULL, CAUSAL>;
     const size_t smem = tma_ring_bytes<T>(N, nbuf);
-    cudaError_t e = allow_smem(reinterpret_cast<const void*>(kern), smem, cfg);
+    // softmax bf16 32768 x 4096 on GB300: 89.9 -> 84.6 us with the largest
+    // carveout (the row sum's pipeline ran slower with it and keeps the default)
+    cudaError_t e = allow_smem(reinterpret_cast<const void*>(kern), smem, cfg, true);
     if (e != cudaSuccess) return e;
     const int grid = grid_for(reinterpret_cast<const void*>(kern), TPR, smem, M, cfg);
     kern<<<grid, TPR, smem, cfg.stream>>>(static_cast<const T*>(x), static_cast<T*>(y), M, int(N), ld, nbuf,
