@@ -331,7 +331,7 @@ int ring_buffers(int64_t N, int es, size_t fixed, const Tuning& tn, const Launch
 // Row groups per CTA for the LayerNorm+GELU row pipeline: the groups of a CTA
 // share one staging of w, b, so packing several rows into a CTA raises the warps
 // an SM can hold when that staging, not registers, limits occupancy. Picks the
-// count (1, 2, 4 or 8, where that instantiation exists) that gives the most
+// count (1, 2, 4, 5 or 8, where that instantiation exists) that gives the most
 // resident warps per SM by the occupancy calculator (shared memory, registers
 // and threads of the actual kernel); ties go to fewer groups.
 // `ctas(rows)`: CTAs per SM of the instantiation with that many row groups (0
