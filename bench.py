@@ -43,7 +43,10 @@ from row_wise_reduction_gb300 import workloads  # noqa: E402
 METRIC = "row-kernel HBM GB/s (% of GB300 peak) for softmax and LayerNorm+GELU"
 STEP = ["softmax_bf16_causal_32768x4096", "online_softmax_f32_64x1048576", "layernorm_gelu_bf16_65536x8192"]
 DOMINANT = "layernorm_gelu_bf16_65536x8192"
-KERNELS_PER_CALL = {"softmax": 1, "softmax_causal": 1, "online_softmax": 2, "layernorm_gelu": 1,
+# kernels per call, the fallback when the profiler cannot count them (the
+# online softmax at these sizes: one cooperative kernel, after a memset of its
+# workspace slots)
+KERNELS_PER_CALL = {"softmax": 1, "softmax_causal": 1, "online_softmax": 1, "layernorm_gelu": 1,
                     "layernorm_gelu_erf": 1, "rmsnorm": 1, "residual_rmsnorm": 1, "row_sum": 1, "row_max": 1,
                     "layernorm_gelu_backward": 2, "bias_residual_gelu": 1}
 L2_BYTES = 129 * 10**6
@@ -212,6 +215,22 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def count_kernels(fn):
+    """Kernels that one call of fn launches, from the profiler's CUDA activity
+    trace (memsets and copies excluded); None if no activity was recorded."""
+    try:
+        from torch.profiler import ProfilerActivity, profile
+        torch.cuda.synchronize()
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            fn()
+            torch.cuda.synchronize()
+        kinds = [e.name for e in prof.events() if e.device_type == torch.autograd.DeviceType.CUDA]
+    except Exception:
+        return None
+    kernels = [k for k in kinds if not k.startswith(("Memset", "Memcpy", "cudaMemset", "cudaMemcpy"))]
+    return len(kernels) if kernels else None
 
 
 def aggregate(seconds: float, units: float, group=None):
@@ -731,7 +750,11 @@ def run_rowops(args):
     peak, peak_kind = measured_peak()
     for n in names:
         per_op[n]["frac_of_" + peak_kind] = per_op[n]["gbs"] / peak
-    launches = K * sum(KERNELS_PER_CALL[wls[n].op] for n in names)
+    # kernels of one step, counted from the CUDA activity trace after the timed region
+    per_step = count_kernels(lambda: [call(n, inputs[n]["x"], outputs[n]) for n in names])
+    if per_step is None:
+        per_step = sum(KERNELS_PER_CALL[wls[n].op] for n in names)
+    launches = K * per_step
 
     # end to end through the public API, host buffers: H2D inputs, kernels, D2H outputs
     e2e = None

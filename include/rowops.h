@@ -36,16 +36,22 @@
  * Benchmarking knobs (environment, read at every call; unset = automatic):
  *   ROWOPS_KERNEL=tma|reg|looped  kernel family: TMA-fed row pipeline, register-resident
  *                                 row groups, or the looped any-N kernels
- *   ROWOPS_FORCE_TPR=<16..1024>   threads per row (tma: 64..512)
+ *   ROWOPS_FORCE_TPR=<16..1024>   threads per row (tma: 64..512); row-group split softmax:
+ *                                 256 = two CTAs of 256 threads per SM (default one of 512)
  *   ROWOPS_FORCE_VPT=<n>          16-byte vectors per thread (reg: 1..4; tma: 1, 2, 3, 4, 8)
  *   ROWOPS_FORCE_LOOPED=1         same as ROWOPS_KERNEL=looped
  *   ROWOPS_RING_BUFFERS=<2..16>   rows in flight per row group of the row pipeline (chunks per
  *                                 CTA of the two-pass split softmax on full chunks, default 3)
  *   ROWOPS_ROWS_PER_CTA=<1|2|4|5|8> row groups per CTA of the LayerNorm+GELU and RMSNorm row
  *                                 pipelines (5: LayerNorm+GELU with 128 threads x 8 vectors only)
- *   ROWOPS_ONLINE=two_pass|single_read  split-row softmax form (default two_pass); single_read
- *                                 keeps each chunk on chip between the passes (rows of
- *                                 >= ~2^19.3 entries, 16-byte aligned, cooperative launch)
+ *   ROWOPS_ONLINE=two_pass|row_groups|single_read  split-row softmax form. Default (chunk 0):
+ *                                 row_groups for batches above 32 MiB of rows of at least
+ *                                 256 KiB, else two_pass. row_groups spreads each row over a
+ *                                 group of CTAs that keep their slices on chip and exchange
+ *                                 the slice partials; single_read gives every CTA a column
+ *                                 slice of every row. Both read x once (16-byte aligned rows,
+ *                                 a length of whole 16-byte vectors, a cooperative launch;
+ *                                 other shapes take two_pass).
  *   ROWOPS_PERSIST_L2=1           single_read staged in L2 instead of shared memory
  *   ROWOPS_PERSIST_LOOKAHEAD=<2k> / ROWOPS_PERSIST_PREFETCH=<n>  its pipeline depths
  *   ROWOPS_CTAS_PER_SM=<k>        persistent grid of k CTAs per SM (0 = occupancy limit,
@@ -60,7 +66,8 @@
  *                                 expected to bring 16 bytes more than it does; in the two-pass
  *                                 split softmax on full chunks the same for work item <row>,
  *                                 i.e. chunk (row mod nchunks) of row row / nchunks; in the
- *                                 single-read split softmax CTA 0 withholds that row's partial).
+ *                                 single-read split softmax CTA 0 withholds that row's partial,
+ *                                 in the row-group form the CTA of its first slice does).
  *                                 Nothing faults or hangs: the wait gives up at its limit, the
  *                                 kernel records ROWOPS_ERR_TIMEOUT and returns.
  */
@@ -179,6 +186,14 @@ size_t rowops_online_softmax_workspace_bytes(int64_t M, int64_t N, rowops_dtype_
  *   m = max_c m_c,   d = sum_c d_c * exp(m_c - m)      (chunks with d_c = 0 skipped)
  * and writes y = exp(x - m) / d. Results equal rowops_softmax up to fp32
  * rounding (independent of the chunk count up to rounding).
+ *
+ * With chunk 0, batches above 32 MiB of rows of at least 256 KiB run as one
+ * cooperative kernel in which every chunk stays on chip between the two
+ * passes (x is read once): the CTAs that hold a row's chunks store their
+ * partials in the workspace and each merges all of them, in chunk order,
+ * before writing its chunk of y. Other shapes, and any nonzero chunk, run as
+ * two kernels (partials, then merge + normalise). Both give the same results
+ * up to fp32 rounding.
  *
  *   x, y, M, N, ld, dtype   as for rowops_softmax.
  *   workspace   device pointer, 256-byte aligned, at least

@@ -183,4 +183,94 @@ static cudaError_t launch_persistent(const void* x, void* y, int64_t M, int64_t 
 PersistLaunch split_persistent_f32() { return launch_persistent<float>; }
 PersistLaunch split_persistent_bf16() { return launch_persistent<bf16_t>; }
 
+// The row-group form (split_grouped_kernel) with BLOCK threads per CTA and
+// 512 / BLOCK CTAs per SM, when it applies: rows 16-byte aligned with a
+// length that is a multiple of 16 bytes; a cooperative launch on the device;
+// n CTAs per row, n the smallest divisor of the CTA slots (SMs x CTAs per SM)
+// whose slices fit the block's registers (BLOCK * kGroupedMaxVpt vectors) and
+// `min_buffers` (at least 2) ring buffers in a CTA's share of shared memory,
+// raised (to a larger divisor) while M * n is below the CTA slots; at least
+// 32 vectors per slice; n at most kGroupedMaxSlots and the workspace's slots
+// per row. The ring then takes as many slices as fit (at most
+// kGroupedMaxBuffers). Returns cudaErrorNotSupported (and launches nothing)
+// otherwise.
+template <typename T, int BLOCK>
+static cudaError_t launch_grouped_block(const void* x, void* y, int64_t M, int64_t N, int64_t ld, void* workspace,
+                                        int min_buffers, const LaunchCfg& cfg) {
+    constexpr int V = Elem<T>::kVec;
+    constexpr int kPerSm = 512 / BLOCK;
+    if (!cfg.cooperative || N % V != 0 || M < 1) return cudaErrorNotSupported;
+    const int64_t nvec = N / V;
+    const int ctas = cfg.num_sms * kPerSm;  // CTA slots of the grid
+    const int want = min_buffers >= 2 ? min_buffers : 2;
+    // a CTA's share of the SM's shared memory (1 KB per CTA is the system's),
+    // minus the barriers and this kernel's static arrays
+    const int64_t avail = (int64_t(cfg.max_smem_optin) + 1024) / kPerSm - 1024 - int64_t(kRingHeader) - 512;
+    auto slot_vecs_for = [&](int d) { return ((nvec + d - 1) / d + 7) / 8 * 8; };
+    auto fits = [&](int d) {
+        return (nvec + d - 1) / d <= int64_t(BLOCK) * kGroupedMaxVpt && slot_vecs_for(d) * 16 * want <= avail;
+    };
+    int n = 0;
+    for (int d = 1; d <= ctas && n == 0; ++d)
+        if (ctas % d == 0 && fits(d)) n = d;
+    if (n == 0) return cudaErrorNotSupported;
+    while (M * n < ctas && n < ctas) {
+        int d = n + 1;
+        while (ctas % d != 0) ++d;
+        n = d;
+    }
+    if (n > kGroupedMaxSlots || nvec < int64_t(n) * 32 || n > persistent_slots(N)) return cudaErrorNotSupported;
+    const int64_t slot_vecs = slot_vecs_for(n);
+    int64_t nbuf = avail / (slot_vecs * 16);
+    if (nbuf > kGroupedMaxBuffers) nbuf = kGroupedMaxBuffers;
+    const int64_t rows_per_wave = (ctas / n) < M ? (ctas / n) : M;
+    const int64_t G = rows_per_wave * n;
+
+    auto kern = split_grouped_kernel<T, BLOCK, kGroupedMaxVpt, kGroupedLag>;
+    const size_t smem = kRingHeader + size_t(nbuf) * size_t(slot_vecs) * 16;
+    cudaError_t e = allow_smem(reinterpret_cast<const void*>(kern), smem, cfg, kPerSm > 1);
+    if (e != cudaSuccess) return e;
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, BLOCK, smem) != cudaSuccess || occ < kPerSm) {
+        cudaGetLastError();
+        return cudaErrorNotSupported;
+    }
+    char* ws = static_cast<char*>(workspace);
+    GroupedArgs a;
+    a.M = M;
+    a.N = N;
+    a.ld = ld;
+    a.n = n;
+    a.nbuf = int(nbuf);
+    a.slot_vecs = int(slot_vecs);
+    a.header = reinterpret_cast<unsigned*>(ws);
+    a.partials = reinterpret_cast<unsigned long long*>(ws + kWorkspaceHeader);
+    a.wait_ns = cfg.wait_ns;
+    a.stall_row = cfg.stall_row;
+    // header and slots in one fill: status 0, abort 0, every slot empty
+    e = cudaMemsetAsync(ws, 0, kWorkspaceHeader + size_t(M) * size_t(n) * 8, cfg.stream);
+    if (e != cudaSuccess) return e;
+    const T* xp = static_cast<const T*>(x);
+    T* yp = static_cast<T*>(y);
+    void* args[] = {&xp, &yp, &a};
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(unsigned(G)), dim3(BLOCK), args,
+                                       smem, cfg.stream);
+}
+
+// One CTA of 512 threads per SM; two of 256 with ROWOPS_FORCE_TPR=256 where
+// the shape allows (slower on GB300: 122.7 us against 112.1 for 64 x 2^20
+// fp32).
+template <typename T>
+static cudaError_t launch_grouped(const void* x, void* y, int64_t M, int64_t N, int64_t ld, void* workspace,
+                                  int min_buffers, const LaunchCfg& cfg) {
+    if (cfg.grouped_block == 256) {
+        const cudaError_t e = launch_grouped_block<T, 256>(x, y, M, N, ld, workspace, min_buffers, cfg);
+        if (e != cudaErrorNotSupported) return e;
+    }
+    return launch_grouped_block<T, 512>(x, y, M, N, ld, workspace, min_buffers, cfg);
+}
+
+GroupedLaunch split_grouped_f32() { return launch_grouped<float>; }
+GroupedLaunch split_grouped_bf16() { return launch_grouped<bf16_t>; }
+
 }  // namespace rowops

@@ -33,6 +33,7 @@
 // (64-bit, padded to 256 bytes), then 64-bit warp partials [M][G * 16].
 #pragma once
 
+#include "reduce_kernels.cuh"
 #include "row_pipeline.cuh"
 #include "softmax_kernels.cuh"
 
@@ -445,6 +446,253 @@ __global__ void __launch_bounds__(kPersistBlock, 1) split_l2_kernel(const T* x, 
             }
         }
     }
+}
+
+// ---------------------------------------------------------------------------
+// Row groups: the single-read form with each row spread over n CTAs instead
+// of all of them. The grid is R row groups of n CTAs (gridDim.x = R * n); CTA
+// c = g * n + q holds column slice q, [q nvec / n, (q + 1) nvec / n) vectors,
+// of rows g, g + R, g + 2R, ... in turn, so the n CTAs of a group always work
+// on the same row and a wave of the grid covers R whole rows. A CTA's ring
+// holds nbuf slices; step j of a CTA:
+//   1. wait (bounded) for the copy of its j-th slice; (m_q, d_q) = (max, sum
+//      exp(x - m_q)) over it, two passes over shared memory; store it in the
+//      row's slot q;
+//   2. for its slice j - L: wait (bounded) until all n slots of that row are
+//      set, merge them in slot order, m = max m_q (d_q > 0), d = sum d_q
+//      exp(m_q - m) -- every CTA of the group computes the same (m, d), in the
+//      same order;
+//   3. y = exp(x - m) / d for slice j - L from shared memory; its buffer then
+//      takes the slice nbuf rows ahead.
+// Step 2 waits only on the other CTAs of the group finishing step 1 of a row
+// L steps earlier, which never waits on anything but their own copies and
+// earlier steps: with all CTAs resident (a cooperative launch) every wait
+// ends, and the lag L lets the slots' round trip through L2 overlap the next
+// slices' work.
+// Slots are self-flagging 64-bit words over a zero sentinel (a stored pair is
+// never zero: a finite m comes with d >= 1, and m = +0 is finite), zeroed with
+// the header before the launch.
+// Workspace: [0, 256) header (word 0 status, word 1 abort), then M * n slots.
+// ---------------------------------------------------------------------------
+constexpr int kGroupedMaxBuffers = 8;
+constexpr int kGroupedLag = 2;        // steps from a slice's partial to its normalise
+constexpr int kGroupedMaxVpt = 7;     // vectors of a slice per thread (slices of at most BLOCK * 7 vectors)
+constexpr int kGroupedMaxSlots = 160;  // CTAs per row group, at most (a multiple of 32)
+
+struct GroupedArgs {
+    int64_t M, N, ld;
+    int n;                         // CTAs per row group (gridDim.x is a multiple)
+    int nbuf;                      // ring buffers per CTA
+    int slot_vecs;                 // 16-byte vectors per buffer (>= the widest slice, multiple of 8)
+    unsigned* header;              // [0] status, [1] abort
+    unsigned long long* partials;  // M * n slice partials, zero-filled
+    unsigned long long wait_ns;    // limit of every wait
+    int64_t stall_row;             // test hook: the slice-0 CTA withholds its partial of this row (-1: none)
+};
+
+// Bounded wait until *p is nonzero (the zero-sentinel form of wait_slot).
+__device__ __forceinline__ bool wait_filled(const unsigned long long* p, unsigned* header, unsigned long long* out,
+                                            unsigned long long limit_ns) {
+    unsigned long long v = ld_relaxed_u64(p);
+    if (v != 0ull) {
+        *out = v;
+        return true;
+    }
+    const unsigned long long t0 = global_ns();
+    for (uint32_t it = 0; it < (1u << 28); ++it) {
+        v = ld_relaxed_u64(p);
+        if (v != 0ull) {
+            *out = v;
+            return true;
+        }
+        if ((it & 31u) == 31u) {
+            if (ld_acquire_u32(header + 1) != 0u) return false;
+            if (global_ns() - t0 > limit_ns) {
+                atomicExch(header + 0, kDeviceErrTimeout);
+                atomicExch(header + 1, 1u);
+                return false;
+            }
+        }
+    }
+    return false;
+}
+
+// (m, d) merge of two partial states, symmetric in its arguments (both lanes
+// of a butterfly get the same bits); a state with d = 0 contributes nothing.
+__device__ __forceinline__ MD md_merge_sym(MD a, MD b) {
+    if (a.d == 0.f) return b;
+    if (b.d == 0.f) return a;
+    const float m = fmaxf(a.m, b.m);
+    return MD{m, a.d * ex2_approx((a.m - m) * kLog2eF) + b.d * ex2_approx((b.m - m) * kLog2eF)};
+}
+
+__device__ __forceinline__ MD warp_md_merge(MD v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v = md_merge_sym(v, MD{__shfl_xor_sync(0xffffffffu, v.m, o), __shfl_xor_sync(0xffffffffu, v.d, o)});
+    return v;
+}
+
+// Each slice moves from its ring buffer into registers (a thread's vectors
+// t, t + BLOCK, ...: at most MAXV of them) as soon as it has landed, and the
+// buffer takes the slice nbuf steps ahead at once. A thread therefore holds
+// L + 1 slices in registers: the one of the current step and the L waiting
+// for their rows' merge. The step loop is unrolled L + 1 times so that every
+// register array keeps a fixed role.
+template <typename T, int BLOCK, int MAXV, int L>
+__global__ void __launch_bounds__(BLOCK, 512 / BLOCK) split_grouped_kernel(const T* x, T* y, GroupedArgs a) {
+    using E = Elem<T>;
+    constexpr int V = E::kVec;
+    constexpr int W = BLOCK / 32;
+    constexpr int kLaneSlots = kGroupedMaxSlots / 32;
+    static_assert(BLOCK % 64 == 0 && BLOCK <= 1024 && L >= 2, "two warps or more; a lag of two steps or more");
+    extern __shared__ __align__(128) char smem[];
+    __shared__ MD warp_md[2][W];  // warp partials of a slice, by step parity
+    __shared__ MD row_md[2];      // merged (m, d) of the row being normalised, by step parity
+    const RowRing ring{reinterpret_cast<uint64_t*>(smem), smem + kRingHeader, uint32_t(a.slot_vecs) * 16u, a.nbuf};
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int n = a.n;
+    const int q = int(blockIdx.x % unsigned(n));
+    const int64_t R = gridDim.x / unsigned(n), r0 = blockIdx.x / unsigned(n);
+    const int64_t nvec = a.N / V;
+    const int64_t lo = q * nvec / n;
+    const int width = int((q + 1) * nvec / n - lo);
+    const uint32_t bytes = uint32_t(width) * 16u;
+    const int64_t iters = a.M > r0 ? (a.M - r0 + R - 1) / R : 0;
+    int64_t issued = 0;  // thread 0: slices 0 .. issued - 1 have been copied in or are on their way
+    auto issue = [&](int64_t item) {  // thread 0: copy slice `item` into its buffer
+        tma_load_row(ring.slot(int(item % ring.nbuf)), x + (r0 + item * R) * a.ld + lo * V, bytes,
+                     ring.bar + int(item % ring.nbuf));
+        issued = item + 1;
+    };
+
+    if (t == 0) {
+        for (int s = 0; s < ring.nbuf; ++s) mbar_init(ring.bar + s, 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    if (t == 0)
+        for (int64_t s = 0; s < ring.nbuf && s < iters; ++s) issue(s);
+
+    // warp 0: the slots of the next row to merge, loaded one step early
+    unsigned long long slot[kLaneSlots];
+    auto load_slots = [&](int64_t k) {
+        if (warp == 0 && k >= 0 && k < iters) {
+#pragma unroll
+            for (int u = 0; u < kLaneSlots; ++u)
+                slot[u] = lane + 32 * u < n ? ld_relaxed_u64(a.partials + (r0 + k * R) * n + lane + 32 * u) : 0ull;
+        }
+    };
+
+    // Step j: warp 0 merges the row of slice k = j - L (its slots loaded in
+    // the last step; waiting, bounded, only for any that were still empty)
+    // while every warp takes slice j from its buffer into registers (`cur`)
+    // and folds its part of the slice's partial; one barrier; the buffer takes
+    // slice j + nbuf, warp 1 merges the warp partials and stores the slice's
+    // slot, and every thread normalises slice k (`old`). Returns false on an
+    // error exit.
+    auto step = [&](int64_t j, uint4 (&cur)[MAXV], const uint4 (&old)[MAXV]) -> bool {
+        const int64_t k = j - L;
+        int fail = 0;
+        if (warp == 0 && k >= 0) {
+            const int64_t r = r0 + k * R;
+            MD c{-INFINITY, 0.f};
+#pragma unroll
+            for (int u = 0; u < kLaneSlots; ++u) {
+                if (lane + 32 * u >= n) break;
+                if (slot[u] == 0ull && !wait_filled(a.partials + r * n + lane + 32 * u, a.header, &slot[u], a.wait_ns)) {
+                    fail = 1;
+                    break;
+                }
+                c = md_merge_sym(c, unpack_md(slot[u]));
+            }
+            c = warp_md_merge(c);
+            if (lane == 0) row_md[k & 1] = c;
+        }
+        if (j < iters) {
+            const char* sb = ring.slot(int(j % ring.nbuf));
+            if (!mbar_wait(ring.bar + int(j % ring.nbuf), uint32_t((j / ring.nbuf) & 1), a.wait_ns)) {
+                if (t == 0) {
+                    atomicExch(a.header + 0, kDeviceErrTimeout);
+                    atomicExch(a.header + 1, 1u);
+                }
+                fail = 1;
+            }
+#pragma unroll
+            for (int u = 0; u < MAXV; ++u)
+                if (t + u * BLOCK < width) cur[u] = lds16(sb + size_t(t + u * BLOCK) * 16);
+            // this thread's (max, sum exp(x - max)) over its vectors, then the warp's
+            float m = -INFINITY, d = 0.f;
+#pragma unroll
+            for (int u = 0; u < MAXV; ++u)
+                if (t + u * BLOCK < width) {
+                    float f[V];
+                    E::unpack(cur[u], f);
+#pragma unroll
+                    for (int e = 0; e < V; ++e) m = fmax_nan(m, f[e]);
+                }
+            if (m != -INFINITY) {
+#pragma unroll
+                for (int u = 0; u < MAXV; ++u)
+                    if (t + u * BLOCK < width) {
+                        float f[V];
+                        E::unpack(cur[u], f);
+#pragma unroll
+                        for (int e = 0; e < V; ++e) d += exp_shifted(f[e], m);
+                    }
+            }
+            const MD wmd = warp_md_merge(MD{m, d});
+            if (lane == 0) warp_md[j & 1][warp] = wmd;
+        }
+        if (group_bar_or(1, BLOCK, fail)) return false;
+        if (j < iters) {
+            // every thread has slice j in registers: its buffer takes slice j + nbuf
+            if (t == 0 && j + ring.nbuf < iters) {
+                fence_proxy_async_smem();
+                issue(j + ring.nbuf);
+            }
+            if (warp == 1) {
+                const MD c = warp_md_merge(lane < W ? warp_md[j & 1][lane] : MD{-INFINITY, 0.f});
+                const int64_t r = r0 + j * R;
+                if (lane == 0 && !(q == 0 && r == a.stall_row)) st_relaxed_u64(a.partials + r * n + q, pack_md(c.m, c.d));
+            }
+        }
+        load_slots(k + 1);
+        if (k < 0) return true;
+        const MD rm = row_md[k & 1];
+        const float mm = rm.d > 0.f ? rm.m : 0.f;
+        const float inv = safe_inverse(rm.d);
+        T* yr = y + (r0 + k * R) * a.ld + lo * V;
+#pragma unroll
+        for (int u = 0; u < MAXV; ++u)
+            if (t + u * BLOCK < width) {
+                float f[V];
+                E::unpack(old[u], f);
+#pragma unroll
+                for (int e = 0; e < V; ++e) f[e] = exp_shifted(f[e], mm) * inv;
+                st_stream16(yr + size_t(t + u * BLOCK) * V, E::pack(f));
+            }
+        return true;
+    };
+
+    uint4 xs[L + 1][MAXV];
+    int64_t j = 0;
+    bool ok = true;
+    while (ok && j < iters + L) {
+        // j is a multiple of L + 1 here: step j + i fills xs[i] and normalises
+        // xs[(i + 1) % (L + 1)], which holds slice j + i - L
+#pragma unroll
+        for (int i = 0; i <= L; ++i) {
+            if (j >= iters + L) break;
+            ok = step(j, xs[i], xs[(i + 1) % (L + 1)]);
+            if (!ok) break;
+            ++j;
+        }
+    }
+    // error exit: thread 0 waits (bounded) for the copies in flight, slices j .. issued - 1
+    if (!ok && t == 0)
+        for (int64_t it = j < issued ? j : issued; it < issued; ++it)
+            mbar_wait(ring.bar + int(it % ring.nbuf), uint32_t((it / ring.nbuf) & 1), a.wait_ns);
 }
 
 }  // namespace rowops

@@ -29,7 +29,7 @@ struct Tuning {
     int ctas_per_sm = 0;
     int ring = 0;
     int rows = 0;  // row groups per CTA of the LayerNorm+GELU row pipeline (0: automatic)
-    int online = 0;  // split-row softmax form: 0 automatic, 1 two-launch, 2 single-read
+    int online = 0;  // split-row softmax form: 0 automatic, 1 two-launch, 2 single-read, 3 row groups
     int lookahead = 0;  // single-read form's lookahead in steps (0: automatic)
     int l2 = 0;         // single-read form staged in L2
     int prefetch = 0;   // its L2 prefetch distance in rows (0: automatic)
@@ -76,7 +76,10 @@ Tuning read_tuning() {
         else if (is("TEST_STALL_ROW")) t.stall_row = std::strtoll(v, nullptr, 10);
         else if (is("UNIT_ROWS")) t.unit_rows = int(parse_int(v, 0));
         else if (is("SCHED")) t.sched = !std::strcmp(v, "static") ? 1 : (!std::strcmp(v, "dynamic") ? 2 : 0);
-        else if (is("ONLINE")) t.online = !std::strcmp(v, "two_pass") ? 1 : (!std::strcmp(v, "single_read") ? 2 : 0);
+        else if (is("ONLINE"))
+            t.online = !std::strcmp(v, "two_pass") ? 1
+                     : !std::strcmp(v, "single_read") ? 2
+                     : !std::strcmp(v, "row_groups") ? 3 : 0;
     }
     // ROWOPS_KERNEL, when set to a family, overrides ROWOPS_FORCE_LOOPED
     if (force_looped) t.family = Family::Looped;
@@ -170,6 +173,7 @@ rowops_status_t make_cfg(cudaStream_t stream, const Tuning& tn, LaunchCfg* cfg) 
     cfg->dev_error = di.err;
     cfg->cooperative = di.cooperative != 0;
     cfg->persist_lookahead = tn.lookahead;
+    cfg->grouped_block = tn.tpr;
     cfg->persist_l2 = tn.l2 != 0;
     cfg->persist_prefetch = tn.prefetch;
     cfg->wait_ns = tn.wait_ns > 0 ? (unsigned long long)tn.wait_ns : 2000000000ull;
@@ -823,11 +827,23 @@ rowops_status_t rowops_online_softmax(const void* x, void* y, int64_t M, int64_t
     LaunchCfg cfg;
     if ((st = make_cfg(stream, tn, &cfg)) != ROWOPS_OK) return st;
     const int es = elem_bytes(dtype);
-    // The single-read form (x read once; see online_softmax_persistent.cuh) on
-    // request. Measured on GB300 it is no faster than the two-launch form for
-    // 64 x 2^20 fp32 (the per-row cross-CTA synchronisation on the critical
-    // path costs what the saved re-read gains), so the two-launch form is the
-    // default.
+    // The single-read forms (x read once; see online_softmax_persistent.cuh).
+    // Row groups (each row spread over a group of CTAs that exchange slice
+    // partials) are the default for batches above 32 MiB of rows of at least
+    // 256 KiB: on GB300, 64 x 2^20 fp32 takes 112 us against 125 for the
+    // two-launch form (and 125 against 133.5 between other row kernels).
+    // Column slices of every row per CTA (`single_read`) only on request: no
+    // faster than the two-launch form there.
+    const bool groups_auto = tn.online == 0 && tn.family == Family::Auto &&
+                             M * N * es > (int64_t(32) << 20) && N * es >= (int64_t(256) << 10);
+    if (chunk == 0 && (tn.online == 3 || groups_auto) && rows_aligned(x, y, ld, es)) {
+        GroupedLaunch gf = dtype == ROWOPS_F32 ? split_grouped_f32() : split_grouped_bf16();
+        const cudaError_t e = gf(x, y, M, N, ld, workspace, tn.ring, cfg);
+        if (e == cudaSuccess) return ROWOPS_OK;
+        cudaGetLastError();
+        // a grid the device will not co-schedule falls back to the two-launch form
+        if (e != cudaErrorNotSupported && e != cudaErrorCooperativeLaunchTooLarge) return ROWOPS_ERR_CUDA;
+    }
     if (chunk == 0 && tn.online == 2 && rows_aligned(x, y, ld, es)) {
         PersistLaunch pf = dtype == ROWOPS_F32 ? split_persistent_f32() : split_persistent_bf16();
         const cudaError_t e = pf(x, y, M, N, ld, workspace, cfg);

@@ -29,6 +29,7 @@ struct LaunchCfg {
     int unit_rows = 0;          // full-row pipelines: 0 static schedule, else rows per group in a work
                                 // unit taken by cluster launch control
     int64_t stall_row = -1;     // test hook: the row whose wait is made to run out (-1: none)
+    int grouped_block = 0;      // row-group split softmax: threads per CTA (0: automatic)
 };
 
 // Persistent grid size for `items` independent work items: the occupancy
@@ -238,6 +239,12 @@ using PersistLaunch = cudaError_t (*)(const void* x, void* y, int64_t M, int64_t
                                       const LaunchCfg& cfg);
 PersistLaunch split_persistent_f32();
 PersistLaunch split_persistent_bf16();
+// Single-read split-row softmax over row groups of CTAs (cooperative grid);
+// cudaErrorNotSupported when the shape or device does not suit it.
+using GroupedLaunch = cudaError_t (*)(const void* x, void* y, int64_t M, int64_t N, int64_t ld, void* workspace,
+                                      int min_buffers, const LaunchCfg& cfg);
+GroupedLaunch split_grouped_f32();
+GroupedLaunch split_grouped_bf16();
 // workspace of the single-read form: header, M row results, M * persistent_slots(N) partials
 int64_t persistent_slots(int64_t N);
 size_t persistent_rowstat_bytes(int64_t M);

@@ -67,13 +67,13 @@ def test_layernorm_row_groups_wait_times_out(oracle, monkeypatch):
     C.assert_ln_gelu_close(C.to_f64(y), ref, "bf16")
 
 
-@pytest.mark.parametrize("staging", ["smem", "l2"])
+@pytest.mark.parametrize("staging", ["smem", "l2", "groups"])
 def test_single_read_split_softmax_wait_times_out(oracle, monkeypatch, staging):
     wl = workloads.Workload("timeout_online", "online_softmax", "f32", 6, 1 << 20, seed=5)
     x = gu.make_x(wl)["x"]
     ws = torch.empty(rowops_online_softmax_workspace_bytes(6, 1 << 20, torch.float32), dtype=torch.uint8,
                      device="cuda")
-    monkeypatch.setenv("ROWOPS_ONLINE", "single_read")
+    monkeypatch.setenv("ROWOPS_ONLINE", "row_groups" if staging == "groups" else "single_read")
     if staging == "l2":
         monkeypatch.setenv("ROWOPS_PERSIST_L2", "1")
     monkeypatch.setenv("ROWOPS_WAIT_LIMIT_NS", LIMIT_NS)

@@ -56,11 +56,15 @@ def test_online_softmax_reduced_rows(oracle, chunk):
     check(oracle, W4.with_shape(M=4), chunk=chunk)
 
 
-def test_online_softmax_full_size(oracle):
-    """Full 64 x 2^20 fp32 workload, default launch configuration: 4 sampled
-    rows against the oracle; on every row the outlier entries equal
+@pytest.mark.parametrize("form", ["default", "two_pass"])
+def test_online_softmax_full_size(oracle, monkeypatch, form):
+    """Full 64 x 2^20 fp32 workload, in the default launch configuration (the
+    single-kernel row-group form at this size) and in the two-launch form: 4
+    sampled rows against the oracle; on every row the outlier entries equal
     1 / (k + S) (k outliers, S = sum of exp(x - 30) over the rest, accumulated
     here in float64) and every row sums to 1."""
+    if form == "two_pass":
+        monkeypatch.setenv("ROWOPS_ONLINE", "two_pass")
     inp = gu.make_x(W4)
     x = inp["x"]
     ws = workspace(x)
@@ -80,8 +84,8 @@ def test_online_softmax_full_size(oracle):
 
 
 def test_online_matches_two_pass_softmax():
-    """Split-row online softmax (single-read form at the automatic chunking,
-    two-launch form at two explicit chunk counts) and rowops_softmax (whose
+    """Split-row online softmax (automatic chunking and two explicit chunk
+    counts) and rowops_softmax (whose
     2^20-column rows take the in-CTA online loop) agree within the softmax
     tolerance on the same input."""
     wl = W4.with_shape(M=8)
@@ -172,26 +176,38 @@ def test_online_softmax_empty_is_noop():
     assert y.shape == (0, 4096)
 
 
+def set_single_read(monkeypatch, staging):
+    """Force a single-read form: "smem" / "l2" (column slices of every row per
+    CTA, staged in shared memory / L2) or "groups" (rows over row groups)."""
+    monkeypatch.setenv("ROWOPS_ONLINE", "row_groups" if staging.startswith("groups") else "single_read")
+    if staging == "l2":
+        monkeypatch.setenv("ROWOPS_PERSIST_L2", "1")
+    if staging == "groups256":
+        monkeypatch.setenv("ROWOPS_FORCE_TPR", "512")
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("M,N", [(1, 1 << 20), (3, 1 << 20), (2, 1 << 21), (5, 1500000), (155, 1 << 20),
                                  (64, 40000)])
-@pytest.mark.parametrize("staging", ["smem", "l2"])
+@pytest.mark.parametrize("staging", ["smem", "l2", "groups", "groups256"])
 def test_online_softmax_single_read_form(oracle, monkeypatch, dtype, M, N, staging):
-    """The persistent single-read form (column slices per CTA, warp partials,
-    one merging owner CTA per row, a ring of staged rows), forced; shapes give
-    fewer rows than the ring, more rows than CTAs (owners take several rows),
-    uneven slices, a shallow ring (2^21 columns), and rows too short for it
-    (which take the two-launch form); staged in shared memory or in L2."""
-    monkeypatch.setenv("ROWOPS_ONLINE", "single_read")
-    if staging == "l2":
-        monkeypatch.setenv("ROWOPS_PERSIST_L2", "1")
+    """The persistent single-read forms, forced. smem / l2: column slices of
+    every row per CTA, warp partials, one merging owner CTA per row, a ring of
+    staged rows in shared memory or L2; shapes give fewer rows than the ring,
+    more rows than CTAs (owners take several rows), uneven slices, a shallow
+    ring (2^21 columns), and rows too short for it (which take the two-launch
+    form). groups: rows spread over row groups of CTAs; the shapes give one row
+    over every SM, groups widened for few rows, uneven slices, a partial last
+    wave (155 rows), and short rows over groups of 4 CTAs."""
+    set_single_read(monkeypatch, staging)
     check(oracle, edge(dtype, M, N, seed=M + N, outlier_p=1e-3), chunk=0)
     check(oracle, edge(dtype, min(M, 3), N, seed=5), chunk=0, inplace=True)
 
 
-def test_online_softmax_single_read_special_rows(oracle, monkeypatch):
-    """Masked pieces, an all-masked row and a NaN row in the single-read form."""
-    monkeypatch.setenv("ROWOPS_ONLINE", "single_read")
+@pytest.mark.parametrize("staging", ["smem", "groups", "groups256"])
+def test_online_softmax_single_read_special_rows(oracle, monkeypatch, staging):
+    """Masked pieces, an all-masked row and a NaN row in the single-read forms."""
+    set_single_read(monkeypatch, staging)
     N = 1 << 20
     g = torch.Generator().manual_seed(9)
     x = torch.randn(5, N, generator=g)
@@ -207,10 +223,11 @@ def test_online_softmax_single_read_special_rows(oracle, monkeypatch):
     C.assert_softmax_close(C.to_f64(y), oracle.softmax(x.numpy()), "f32")
 
 
-def test_online_softmax_single_read_repeated_calls_reuse_workspace(oracle, monkeypatch):
+@pytest.mark.parametrize("staging", ["smem", "groups"])
+def test_online_softmax_single_read_repeated_calls_reuse_workspace(oracle, monkeypatch, staging):
     """The slots are reset before every call: calls in a row on one
     workspace, with different shapes, all match the oracle."""
-    monkeypatch.setenv("ROWOPS_ONLINE", "single_read")
+    set_single_read(monkeypatch, staging)
     wl_a = edge("f32", 6, 1 << 20, seed=1, outlier_p=1e-3)
     wl_b = edge("f32", 3, 1 << 21, seed=2)
     xa = gu.make_x(wl_a)["x"]
