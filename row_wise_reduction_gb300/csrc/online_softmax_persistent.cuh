@@ -517,20 +517,50 @@ __device__ __forceinline__ bool wait_filled(const unsigned long long* p, unsigne
     return false;
 }
 
-// (m, d) merge of two partial states, symmetric in its arguments (both lanes
-// of a butterfly get the same bits); a state with d = 0 contributes nothing.
-__device__ __forceinline__ MD md_merge_sym(MD a, MD b) {
-    if (a.d == 0.f) return b;
-    if (b.d == 0.f) return a;
-    const float m = fmaxf(a.m, b.m);
-    return MD{m, a.d * ex2_approx((a.m - m) * kLog2eF) + b.d * ex2_approx((b.m - m) * kLog2eF)};
+// Warp-wide max and sum by xor butterflies: every lane ends with the same bits
+// (each step combines the same two values in either order).
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_max_nan(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmax_nan(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
 }
 
-__device__ __forceinline__ MD warp_md_merge(MD v) {
+// Merge of the partial states (m_i, d_i) that the lanes of a warp hold, one
+// per lane: m = max m_i over d_i != 0, d = sum d_i exp(m_i - m). Every lane
+// gets the result.
+__device__ __forceinline__ MD warp_merge_states(MD p) {
+    const float m = warp_max(p.d != 0.f ? p.m : -INFINITY);
+    return MD{m, warp_sum(p.d != 0.f ? p.d * ex2_approx((p.m - m) * kLog2eF) : 0.f)};
+}
+
+// The same for K packed states per lane (self-flagging slot words), summed per
+// lane in index order and then across lanes.
+template <int K>
+__device__ __forceinline__ MD warp_merge_slots(const unsigned long long (&v)[K]) {
+    float lm = -INFINITY;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        v = md_merge_sym(v, MD{__shfl_xor_sync(0xffffffffu, v.m, o), __shfl_xor_sync(0xffffffffu, v.d, o)});
-    return v;
+    for (int u = 0; u < K; ++u) {
+        const MD p = unpack_md(v[u]);
+        if (p.d != 0.f) lm = fmaxf(lm, p.m);
+    }
+    const float m = warp_max(lm);
+    float ld = 0.f;
+#pragma unroll
+    for (int u = 0; u < K; ++u) {
+        const MD p = unpack_md(v[u]);
+        if (p.d != 0.f) ld += p.d * ex2_approx((p.m - m) * kLog2eF);
+    }
+    return MD{m, warp_sum(ld)};
 }
 
 // Each slice moves from its ring buffer into registers (a thread's vectors
@@ -596,17 +626,13 @@ __global__ void __launch_bounds__(BLOCK, 512 / BLOCK) split_grouped_kernel(const
         int fail = 0;
         if (warp == 0 && k >= 0) {
             const int64_t r = r0 + k * R;
-            MD c{-INFINITY, 0.f};
+            // (slots past n hold 0: (m, d) = (0, 0), which the merge skips)
 #pragma unroll
-            for (int u = 0; u < kLaneSlots; ++u) {
-                if (lane + 32 * u >= n) break;
-                if (slot[u] == 0ull && !wait_filled(a.partials + r * n + lane + 32 * u, a.header, &slot[u], a.wait_ns)) {
+            for (int u = 0; u < kLaneSlots; ++u)
+                if (!fail && lane + 32 * u < n && slot[u] == 0ull &&
+                    !wait_filled(a.partials + r * n + lane + 32 * u, a.header, &slot[u], a.wait_ns))
                     fail = 1;
-                    break;
-                }
-                c = md_merge_sym(c, unpack_md(slot[u]));
-            }
-            c = warp_md_merge(c);
+            const MD c = warp_merge_slots(slot);
             if (lane == 0) row_md[k & 1] = c;
         }
         if (j < iters) {
@@ -621,7 +647,8 @@ __global__ void __launch_bounds__(BLOCK, 512 / BLOCK) split_grouped_kernel(const
 #pragma unroll
             for (int u = 0; u < MAXV; ++u)
                 if (t + u * BLOCK < width) cur[u] = lds16(sb + size_t(t + u * BLOCK) * 16);
-            // this thread's (max, sum exp(x - max)) over its vectors, then the warp's
+            // the warp's (max, sum exp(x - max)) over its vectors: the max
+            // first (NaN-propagating), then the sum relative to it
             float m = -INFINITY, d = 0.f;
 #pragma unroll
             for (int u = 0; u < MAXV; ++u)
@@ -631,6 +658,7 @@ __global__ void __launch_bounds__(BLOCK, 512 / BLOCK) split_grouped_kernel(const
 #pragma unroll
                     for (int e = 0; e < V; ++e) m = fmax_nan(m, f[e]);
                 }
+            m = warp_max_nan(m);
             if (m != -INFINITY) {
 #pragma unroll
                 for (int u = 0; u < MAXV; ++u)
@@ -641,8 +669,8 @@ __global__ void __launch_bounds__(BLOCK, 512 / BLOCK) split_grouped_kernel(const
                         for (int e = 0; e < V; ++e) d += exp_shifted(f[e], m);
                     }
             }
-            const MD wmd = warp_md_merge(MD{m, d});
-            if (lane == 0) warp_md[j & 1][warp] = wmd;
+            d = warp_sum(d);
+            if (lane == 0) warp_md[j & 1][warp] = MD{m, d};
         }
         if (group_bar_or(1, BLOCK, fail)) return false;
         if (j < iters) {
@@ -652,7 +680,7 @@ __global__ void __launch_bounds__(BLOCK, 512 / BLOCK) split_grouped_kernel(const
                 issue(j + ring.nbuf);
             }
             if (warp == 1) {
-                const MD c = warp_md_merge(lane < W ? warp_md[j & 1][lane] : MD{-INFINITY, 0.f});
+                const MD c = warp_merge_states(lane < W ? warp_md[j & 1][lane] : MD{-INFINITY, 0.f});
                 const int64_t r = r0 + j * R;
                 if (lane == 0 && !(q == 0 && r == a.stall_row)) st_relaxed_u64(a.partials + r * n + q, pack_md(c.m, c.d));
             }
