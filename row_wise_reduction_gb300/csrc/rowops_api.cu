@@ -830,8 +830,8 @@ rowops_status_t rowops_online_softmax(const void* x, void* y, int64_t M, int64_t
     // The single-read forms (x read once; see online_softmax_persistent.cuh).
     // Row groups (each row spread over a group of CTAs that exchange slice
     // partials) are the default for batches above 32 MiB of rows of at least
-    // 256 KiB: on GB300, 64 x 2^20 fp32 takes 112 us against 125 for the
-    // two-launch form (and 125 against 133.5 between other row kernels).
+    // 256 KiB: on GB300, 64 x 2^20 fp32 takes 101 us against 125 for the
+    // two-launch form (and 104 against 133.5 between other row kernels).
     // Column slices of every row per CTA (`single_read`) only on request: no
     // faster than the two-launch form there.
     const bool groups_auto = tn.online == 0 && tn.family == Family::Auto &&
