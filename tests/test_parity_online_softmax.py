@@ -83,6 +83,17 @@ def test_online_softmax_full_size(oracle, monkeypatch, form):
     del x, y, inp
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_online_softmax_row_groups_strided_many_rows(oracle, dtype):
+    """Default dispatch on a batch above 32 MiB of rows of 1 MiB (fp32) or
+    512 KiB (bf16) with a padded row stride: the single-kernel row-group form
+    with groups of 19 CTAs and 8 rows per wave over 5 (fp32) or 10 (bf16)
+    waves, every row against the oracle, the output's guard band untouched."""
+    N = 1 << 18
+    M = 40 if dtype == "f32" else 80
+    check(oracle, edge(dtype, M, N, seed=77, outlier_p=1e-3), chunk=0, ld=N + 64)
+
+
 def test_online_matches_two_pass_softmax():
     """Split-row online softmax (automatic chunking and two explicit chunk
     counts) and rowops_softmax (whose
