@@ -2,10 +2,14 @@
 // §2.5 split_online_softmax; 第 6 讲 §7.2 Online Softmax].
 //
 // The two-launch form (online_softmax_kernels.cuh) reads x twice: once for the
-// chunk partials, once more to normalise. Here every chunk stays in shared
-// memory between the two passes, so x is read once and y written once.
+// chunk partials, once more to normalise. The forms here keep every chunk on
+// chip between the two passes, so x is read once and y written once:
+//   - split_grouped_kernel (below; the default for large batches of long
+//     rows): each row spread over a group of CTAs;
+//   - split_persistent_kernel / split_l2_kernel (on request): every CTA holds
+//     a column slice of every row, staged in shared memory or in L2.
 //
-// A cooperative grid of G CTAs (all resident at once). CTA c owns the column
+// Column slices: a cooperative grid of G CTAs (all resident at once). CTA c owns the column
 // slice [c nvec / G, (c + 1) nvec / G) (16-byte vectors) of every row, and warp
 // w of the CTA the w-th sixteenth of that slice. The CTA keeps its slices of NS
 // consecutive rows in a ring of shared-memory stages, filled by bulk copies,
@@ -454,24 +458,29 @@ __global__ void __launch_bounds__(kPersistBlock, 1) split_l2_kernel(const T* x, 
 // c = g * n + q holds column slice q, [q nvec / n, (q + 1) nvec / n) vectors,
 // of rows g, g + R, g + 2R, ... in turn, so the n CTAs of a group always work
 // on the same row and a wave of the grid covers R whole rows. A CTA's ring
-// holds nbuf slices; step j of a CTA:
-//   1. wait (bounded) for the copy of its j-th slice; (m_q, d_q) = (max, sum
-//      exp(x - m_q)) over it, two passes over shared memory; store it in the
-//      row's slot q;
-//   2. for its slice j - L: wait (bounded) until all n slots of that row are
-//      set, merge them in slot order, m = max m_q (d_q > 0), d = sum d_q
-//      exp(m_q - m) -- every CTA of the group computes the same (m, d), in the
-//      same order;
-//   3. y = exp(x - m) / d for slice j - L from shared memory; its buffer then
-//      takes the slice nbuf rows ahead.
+// holds nbuf slices in shared memory (bulk copies, one mbarrier each); step j
+// of a CTA:
+//   1. every thread moves its vectors of slice j from the ring into registers
+//      (the buffer then takes slice j + nbuf at once); each warp takes the
+//      maximum of its entries, then the sum of exp(x - max) relative to it;
+//      after the step's one CTA barrier warp 1 merges the warp partials into
+//      the slice's (m_q, d_q) and stores it in the row's slot q;
+//   2. meanwhile warp 0 merges the row of slice j - L from the n slots it
+//      loaded in the last step (waiting, bounded, only for any that were
+//      still empty): m = max m_q over d_q > 0, then d = sum d_q exp(m_q - m),
+//      per lane in slot order and then across lanes, so every CTA of the group
+//      computes the same (m, d);
+//   3. after the barrier every thread writes y = exp(x - m) / d for slice
+//      j - L from its registers.
 // Step 2 waits only on the other CTAs of the group finishing step 1 of a row
 // L steps earlier, which never waits on anything but their own copies and
 // earlier steps: with all CTAs resident (a cooperative launch) every wait
 // ends, and the lag L lets the slots' round trip through L2 overlap the next
 // slices' work.
 // Slots are self-flagging 64-bit words over a zero sentinel (a stored pair is
-// never zero: a finite m comes with d >= 1, and m = +0 is finite), zeroed with
-// the header before the launch.
+// never zero: a finite m comes with d >= 1, the maximal entry's own term, and
+// an all -inf slice stores (-inf, 0)), zeroed with the header before the
+// launch.
 // Workspace: [0, 256) header (word 0 status, word 1 abort), then M * n slots.
 // ---------------------------------------------------------------------------
 constexpr int kGroupedMaxBuffers = 8;
