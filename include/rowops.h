@@ -41,7 +41,9 @@
  *   ROWOPS_FORCE_VPT=<n>          16-byte vectors per thread (reg: 1..4; tma: 1, 2, 3, 4, 8)
  *   ROWOPS_FORCE_LOOPED=1         same as ROWOPS_KERNEL=looped
  *   ROWOPS_RING_BUFFERS=<2..16>   rows in flight per row group of the row pipeline (chunks per
- *                                 CTA of the two-pass split softmax on full chunks, default 3)
+ *                                 CTA of the two-pass split softmax on full chunks, default 3;
+ *                                 row-group split softmax: the fewest ring slices per CTA its
+ *                                 slice size must allow, default 2)
  *   ROWOPS_ROWS_PER_CTA=<1|2|4|5|8> row groups per CTA of the LayerNorm+GELU and RMSNorm row
  *                                 pipelines (5: LayerNorm+GELU with 128 threads x 8 vectors only)
  *   ROWOPS_ONLINE=two_pass|row_groups|single_read  split-row softmax form. Default (chunk 0):
