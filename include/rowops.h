@@ -93,7 +93,7 @@ typedef enum rowops_dtype {
 typedef enum rowops_status {
     ROWOPS_OK = 0,
     ROWOPS_ERR_INVALID_VALUE = 1, /* null pointer, bad shape / stride / dtype, misaligned pointer, overlap */
-    ROWOPS_ERR_UNSUPPORTED = 2,   /* valid but outside what this build handles (e.g. N >= 2^31) */
+    ROWOPS_ERR_UNSUPPORTED = 2,   /* valid but outside what the library handles (e.g. N >= 2^31) */
     ROWOPS_ERR_WORKSPACE = 3,     /* workspace missing, misaligned or smaller than the query says */
     ROWOPS_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
     ROWOPS_ERR_TIMEOUT = 5,       /* a device-side wait gave up (reported by the status query) */

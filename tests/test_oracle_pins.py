@@ -1,6 +1,6 @@
 """Pins for the CPU oracle: closed forms, invariants, exact-arithmetic brute
 force and library routines, so that the oracle is checked against something
-other than itself before it judges the CUDA path.
+other than itself before it is used to check the CUDA path.
 
 Each test names the mistake it would catch. Nothing here needs a GPU.
 """
