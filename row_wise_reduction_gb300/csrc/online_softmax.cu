@@ -185,46 +185,23 @@ PersistLaunch split_persistent_bf16() { return launch_persistent<bf16_t>; }
 
 // The row-group form (split_grouped_kernel) with BLOCK threads per CTA and
 // 512 / BLOCK CTAs per SM, when it applies: rows 16-byte aligned with a
-// length that is a multiple of 16 bytes; a cooperative launch on the device;
-// n CTAs per row, n the smallest divisor of the CTA slots (SMs x CTAs per SM)
-// whose slices fit the block's registers (BLOCK * kGroupedMaxVpt vectors) and
-// `min_buffers` (at least 2) ring buffers in a CTA's share of shared memory,
-// raised (to a larger divisor) while M * n is below the CTA slots; at least
-// 32 vectors per slice; n at most kGroupedMaxSlots and the workspace's slots
-// per row. The ring then takes as many slices as fit (at most
-// kGroupedMaxBuffers). Returns cudaErrorNotSupported (and launches nothing)
-// otherwise.
+// length that is a multiple of 16 bytes, a cooperative launch on the device,
+// and a plan (grouped_plan.h) for a CTA's share of shared memory. Returns
+// cudaErrorNotSupported (and launches nothing) otherwise.
 template <typename T, int BLOCK>
 static cudaError_t launch_grouped_block(const void* x, void* y, int64_t M, int64_t N, int64_t ld, void* workspace,
                                         int min_buffers, const LaunchCfg& cfg) {
     constexpr int V = Elem<T>::kVec;
     constexpr int kPerSm = 512 / BLOCK;
     if (!cfg.cooperative || N % V != 0 || M < 1) return cudaErrorNotSupported;
-    const int64_t nvec = N / V;
-    const int ctas = cfg.num_sms * kPerSm;  // CTA slots of the grid
-    const int want = min_buffers >= 2 ? min_buffers : 2;
     // a CTA's share of the SM's shared memory (1 KB per CTA is the system's),
     // minus the barriers and this kernel's static arrays
     const int64_t avail = (int64_t(cfg.max_smem_optin) + 1024) / kPerSm - 1024 - int64_t(kRingHeader) - 512;
-    auto slot_vecs_for = [&](int d) { return ((nvec + d - 1) / d + 7) / 8 * 8; };
-    auto fits = [&](int d) {
-        return (nvec + d - 1) / d <= int64_t(BLOCK) * kGroupedMaxVpt && slot_vecs_for(d) * 16 * want <= avail;
-    };
-    int n = 0;
-    for (int d = 1; d <= ctas && n == 0; ++d)
-        if (ctas % d == 0 && fits(d)) n = d;
-    if (n == 0) return cudaErrorNotSupported;
-    while (M * n < ctas && n < ctas) {
-        int d = n + 1;
-        while (ctas % d != 0) ++d;
-        n = d;
-    }
-    if (n > kGroupedMaxSlots || nvec < int64_t(n) * 32 || n > persistent_slots(N)) return cudaErrorNotSupported;
-    const int64_t slot_vecs = slot_vecs_for(n);
-    int64_t nbuf = avail / (slot_vecs * 16);
-    if (nbuf > kGroupedMaxBuffers) nbuf = kGroupedMaxBuffers;
-    const int64_t rows_per_wave = (ctas / n) < M ? (ctas / n) : M;
-    const int64_t G = rows_per_wave * n;
+    const GroupedLimits lim{BLOCK, kPerSm, kGroupedMaxVpt, kGroupedMaxSlots, kGroupedMaxBuffers, avail};
+    const GroupedPlan plan = grouped_plan(M, N / V, cfg.num_sms, min_buffers, persistent_slots(N), lim);
+    if (plan.n == 0) return cudaErrorNotSupported;
+    const int n = plan.n;
+    const int64_t slot_vecs = plan.slot_vecs, nbuf = plan.nbuf, G = plan.grid;
 
     auto kern = split_grouped_kernel<T, BLOCK, kGroupedMaxVpt, kGroupedLag>;
     const size_t smem = kRingHeader + size_t(nbuf) * size_t(slot_vecs) * 16;

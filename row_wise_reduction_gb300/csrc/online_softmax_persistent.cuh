@@ -37,6 +37,7 @@
 // (64-bit, padded to 256 bytes), then 64-bit warp partials [M][G * 16].
 #pragma once
 
+#include "grouped_plan.h"
 #include "reduce_kernels.cuh"
 #include "row_pipeline.cuh"
 #include "softmax_kernels.cuh"
@@ -483,10 +484,7 @@ __global__ void __launch_bounds__(kPersistBlock, 1) split_l2_kernel(const T* x, 
 // launch.
 // Workspace: [0, 256) header (word 0 status, word 1 abort), then M * n slots.
 // ---------------------------------------------------------------------------
-constexpr int kGroupedMaxBuffers = 8;
-constexpr int kGroupedLag = 2;        // steps from a slice's partial to its normalise
-constexpr int kGroupedMaxVpt = 7;     // vectors of a slice per thread (slices of at most BLOCK * 7 vectors)
-constexpr int kGroupedMaxSlots = 160;  // CTAs per row group, at most (a multiple of 32)
+constexpr int kGroupedLag = 2;  // steps from a slice's partial to its normalise
 
 struct GroupedArgs {
     int64_t M, N, ld;
