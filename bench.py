@@ -752,8 +752,10 @@ def run_rowops(args):
         per_op[n]["frac_of_" + peak_kind] = per_op[n]["gbs"] / peak
     # kernels of one step, counted from the CUDA activity trace after the timed region
     per_step = count_kernels(lambda: [call(n, inputs[n]["x"], outputs[n]) for n in names])
+    launches_from = "cuda activity trace of one step"
     if per_step is None:
         per_step = sum(KERNELS_PER_CALL[wls[n].op] for n in names)
+        launches_from = "per-operation table"
     launches = K * per_step
 
     # end to end through the public API, host buffers: H2D inputs, kernels, D2H outputs
@@ -870,6 +872,7 @@ def run_rowops(args):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches,
+        "gpu_launches_from": launches_from,
         "extras": extras,
         "context_torch_eager": eager,
         "clocks": clocks.summary(),
