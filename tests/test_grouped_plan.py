@@ -106,3 +106,31 @@ def test_plan_invariants(plan, block, per_sm):
             assert M * n >= ctas or n == ctas, case
         if M >= ctas // n:
             assert grid == (ctas // n) * n, case
+
+
+def test_plans_fit_the_workspace_the_library_asks_for(plan):
+    """The row-group form stores its header (256 bytes) and M * n 8-byte slots
+    in the caller's workspace: for every plan that applies, that fits in
+    rowops_online_softmax_workspace_bytes(M, N) (a host-only query)."""
+    from row_wise_reduction_gb300 import build
+    from row_wise_reduction_gb300.rowops import library
+
+    build.build()
+    q = library().rowops_online_softmax_workspace_bytes
+    F32, BF16 = 0, 1
+    cases, shapes = [], []
+    for M in [1, 3, 36, 64, 155, 4096]:
+        for N in [65536, 1 << 18, 1 << 20, 1500000, 1 << 21]:
+            for code, vec in [(F32, 4), (BF16, 8)]:
+                if N % vec:
+                    continue
+                for block, per_sm in [(512, 1), (256, 2)]:
+                    cases.append((M, N // vec, SMS, block, per_sm, ring_bytes(per_sm), 2, slots_per_row(N // vec, vec)))
+                    shapes.append((M, N, code))
+    checked = 0
+    for (M, N, code), (n, _, _, _) in zip(shapes, plan(cases)):
+        if n == 0:
+            continue
+        assert 256 + M * n * 8 <= q(M, N, code), (M, N, code, n)
+        checked += 1
+    assert checked > 50
