@@ -200,8 +200,10 @@ size_t rowops_online_softmax_workspace_bytes(int64_t M, int64_t N, rowops_dtype_
  *   x, y, M, N, ld, dtype   as for rowops_softmax.
  *   workspace   device pointer, 256-byte aligned, at least
  *               rowops_online_softmax_workspace_bytes(M, N, dtype) bytes; the call
- *               overwrites it. Calls that share a workspace must be ordered on
- *               one stream.
+ *               overwrites it. Its contents before the call do not matter (the
+ *               single-kernel form zeroes the slots it uses itself, so no fill is
+ *               enqueued). Calls that share a workspace must be ordered on one
+ *               stream.
  *   chunk       columns per chunk: 0 picks one from N and the SM count; otherwise
  *               a multiple of 16 in [256, 2^30]. Larger chunks than N are clamped.
  */

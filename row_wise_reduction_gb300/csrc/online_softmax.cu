@@ -224,9 +224,8 @@ static cudaError_t launch_grouped_block(const void* x, void* y, int64_t M, int64
     a.partials = reinterpret_cast<unsigned long long*>(ws + kWorkspaceHeader);
     a.wait_ns = cfg.wait_ns;
     a.stall_row = cfg.stall_row;
-    // header and slots in one fill: status 0, abort 0, every slot empty
-    e = cudaMemsetAsync(ws, 0, kWorkspaceHeader + size_t(M) * size_t(n) * 8, cfg.stream);
-    if (e != cudaSuccess) return e;
+    // no fill of the workspace: the kernel zeroes its own slots and the
+    // header's status and abort words before the grid's first exchange
     const T* xp = static_cast<const T*>(x);
     T* yp = static_cast<T*>(y);
     void* args[] = {&xp, &yp, &a};

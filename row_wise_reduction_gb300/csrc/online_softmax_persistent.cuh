@@ -37,6 +37,8 @@
 // (64-bit, padded to 256 bytes), then 64-bit warp partials [M][G * 16].
 #pragma once
 
+#include <cooperative_groups.h>
+
 #include "grouped_plan.h"
 #include "reduce_kernels.cuh"
 #include "row_pipeline.cuh"
@@ -466,13 +468,20 @@ __global__ void __launch_bounds__(kPersistBlock, 1) split_l2_kernel(const T* x, 
 //      maximum of its entries, then the sum of exp(x - max) relative to it;
 //      after the step's one CTA barrier warp 1 merges the warp partials into
 //      the slice's (m_q, d_q) and stores it in the row's slot q;
-//   2. meanwhile warp 0 merges the row of slice j - L from the n slots it
-//      loaded in the last step (waiting, bounded, only for any that were
-//      still empty): m = max m_q over d_q > 0, then d = sum d_q exp(m_q - m),
-//      per lane in slot order and then across lanes, so every CTA of the group
-//      computes the same (m, d);
-//   3. after the barrier every thread writes y = exp(x - m) / d for slice
-//      j - L from its registers.
+//   2. meanwhile the row of slice j - L is merged from its n slots, loaded in
+//      the last step (waiting, bounded, only for any still empty), by
+//      U = ceil(n / 32) warps at one slot per lane: the highest-numbered warp
+//      takes slots 0..31, the next 32..63, and so on; each forms its chunk's
+//      m_u = max m_q over d_q > 0 and d_u = sum d_q exp(m_q - m_u) and leaves
+//      it in shared memory for the barrier;
+//   3. after the barrier every thread combines the U chunk states in chunk
+//      order (m = max m_u over d_u > 0, d = sum d_u exp(m_u - m)), so every
+//      CTA of the group gets the same (m, d), and writes y = exp(x - m) / d
+//      for slice j - L from its registers.
+// Spreading step 2 over U warps keeps it off the barrier's critical path: one
+// warp merging all n slots (three per lane at n = 76) held every other warp
+// at the barrier for ~0.4 us per step (64 x 2^20 fp32: 99.0 -> 91.0 us; 512 x
+// 2^19 fp32: 351 -> 321 us, the measured copy bandwidth).
 // Step 2 waits only on the other CTAs of the group finishing step 1 of a row
 // L steps earlier, which never waits on anything but their own copies and
 // earlier steps: with all CTAs resident (a cooperative launch) every wait
@@ -480,8 +489,14 @@ __global__ void __launch_bounds__(kPersistBlock, 1) split_l2_kernel(const T* x, 
 // slices' work.
 // Slots are self-flagging 64-bit words over a zero sentinel (a stored pair is
 // never zero: a finite m comes with d >= 1, the maximal entry's own term, and
-// an all -inf slice stores (-inf, 0)), zeroed with the header before the
-// launch.
+// an all -inf slice stores (-inf, 0)). Nothing needs to be zeroed before the
+// launch: each CTA first zeroes its own slots (the ones it will fill) and CTA
+// 0 the header's status and abort words, then the grid meets once at the
+// cooperative launch's grid barrier, arrived at before the first copies are
+// issued and waited for (bounded, by thread 0) before the first slot access,
+// so its latency hides under the first slices' loads. A previous call's
+// leftovers in the workspace, of any shape, are therefore never mistaken for
+// this call's partials.
 // Workspace: [0, 256) header (word 0 status, word 1 abort), then M * n slots.
 // ---------------------------------------------------------------------------
 constexpr int kGroupedLag = 2;  // steps from a slice's partial to its normalise
@@ -492,7 +507,7 @@ struct GroupedArgs {
     int nbuf;                      // ring buffers per CTA
     int slot_vecs;                 // 16-byte vectors per buffer (>= the widest slice, multiple of 8)
     unsigned* header;              // [0] status, [1] abort
-    unsigned long long* partials;  // M * n slice partials, zero-filled
+    unsigned long long* partials;  // M * n slice partials
     unsigned long long wait_ns;    // limit of every wait
     int64_t stall_row;             // test hook: the slice-0 CTA withholds its partial of this row (-1: none)
 };
@@ -524,6 +539,18 @@ __device__ __forceinline__ bool wait_filled(const unsigned long long* p, unsigne
     return false;
 }
 
+// Thread 0 of a CTA, after the CTA arrived at the cooperative launch's grid
+// barrier with `token`: bounded wait until every CTA has arrived (the
+// barrier's top bit flips once all arrivals are in).
+__device__ __forceinline__ bool grid_barrier_wait(const unsigned* bar, unsigned token, unsigned long long limit_ns) {
+    const unsigned long long t0 = global_ns();
+    for (uint32_t it = 0; it < (1u << 26); ++it) {
+        if ((ld_acquire_u32(bar) ^ token) & 0x80000000u) return true;
+        if ((it & 63u) == 63u && global_ns() - t0 > limit_ns) return false;
+    }
+    return false;
+}
+
 // Warp-wide max and sum by xor butterflies: every lane ends with the same bits
 // (each step combines the same two values in either order).
 __device__ __forceinline__ float warp_max(float v) {
@@ -550,26 +577,6 @@ __device__ __forceinline__ MD warp_merge_states(MD p) {
     return MD{m, warp_sum(p.d != 0.f ? p.d * ex2_approx((p.m - m) * kLog2eF) : 0.f)};
 }
 
-// The same for K packed states per lane (self-flagging slot words), summed per
-// lane in index order and then across lanes.
-template <int K>
-__device__ __forceinline__ MD warp_merge_slots(const unsigned long long (&v)[K]) {
-    float lm = -INFINITY;
-#pragma unroll
-    for (int u = 0; u < K; ++u) {
-        const MD p = unpack_md(v[u]);
-        if (p.d != 0.f) lm = fmaxf(lm, p.m);
-    }
-    const float m = warp_max(lm);
-    float ld = 0.f;
-#pragma unroll
-    for (int u = 0; u < K; ++u) {
-        const MD p = unpack_md(v[u]);
-        if (p.d != 0.f) ld += p.d * ex2_approx((p.m - m) * kLog2eF);
-    }
-    return MD{m, warp_sum(ld)};
-}
-
 // Each slice moves from its ring buffer into registers (a thread's vectors
 // t, t + BLOCK, ...: at most MAXV of them) as soon as it has landed, and the
 // buffer takes the slice nbuf steps ahead at once. A thread therefore holds
@@ -581,14 +588,19 @@ __global__ void __launch_bounds__(BLOCK, 512 / BLOCK) split_grouped_kernel(const
     using E = Elem<T>;
     constexpr int V = E::kVec;
     constexpr int W = BLOCK / 32;
-    constexpr int kLaneSlots = kGroupedMaxSlots / 32;
+    constexpr int kChunks = (kGroupedMaxSlots + 31) / 32;  // slot chunks of 32, at most
     static_assert(BLOCK % 64 == 0 && BLOCK <= 1024 && L >= 2, "two warps or more; a lag of two steps or more");
+    static_assert(kChunks <= W - 2, "the chunk-merging warps must leave warps 0 and 1 free");
     extern __shared__ __align__(128) char smem[];
-    __shared__ MD warp_md[2][W];  // warp partials of a slice, by step parity
-    __shared__ MD row_md[2];      // merged (m, d) of the row being normalised, by step parity
+    __shared__ MD warp_md[2][W];          // warp partials of a slice, by step parity
+    __shared__ MD row_part[2][kChunks];   // chunk states of the row being normalised, by step parity
     const RowRing ring{reinterpret_cast<uint64_t*>(smem), smem + kRingHeader, uint32_t(a.slot_vecs) * 16u, a.nbuf};
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int n = a.n;
+    const int U = (n + 31) / 32;             // chunks of the row's slots
+    const int chunk = W - 1 - warp;          // this warp merges chunk `chunk` when 0 <= chunk < U
+    const bool merger = chunk < U;           // (chunk >= 0 always: warp < W)
+    const int my_slot = 32 * chunk + lane;   // this lane's slot when merger (none when >= n)
     const int q = int(blockIdx.x % unsigned(n));
     const int64_t R = gridDim.x / unsigned(n), r0 = blockIdx.x / unsigned(n);
     const int64_t nvec = a.N / V;
@@ -603,44 +615,54 @@ __global__ void __launch_bounds__(BLOCK, 512 / BLOCK) split_grouped_kernel(const
         issued = item + 1;
     };
 
+    // the grid barrier of the cooperative launch (its memory is the driver's)
+    const cooperative_groups::grid_group grid = cooperative_groups::this_grid();
+    if (!grid.is_valid()) {  // not a cooperative launch: nothing here may run
+        if (blockIdx.x == 0 && t == 0) atomicExch(a.header + 0, 1u);
+        return;
+    }
+    // this call's own slots start empty, the status and abort words at zero
+    if (blockIdx.x == 0 && t < 2) a.header[t] = 0u;
+    for (int64_t i = t; i < iters; i += BLOCK) a.partials[(r0 + i * R) * n + q] = 0ull;
     if (t == 0) {
         for (int s = 0; s < ring.nbuf; ++s) mbar_init(ring.bar + s, 1);
         mbar_init_fence();
     }
-    __syncthreads();
-    if (t == 0)
+    const unsigned token = grid.barrier_arrive();  // (a CTA barrier first, then thread 0 arrives)
+    int fail0 = 0;
+    if (t == 0) {
         for (int64_t s = 0; s < ring.nbuf && s < iters; ++s) issue(s);
-
-    // warp 0: the slots of the next row to merge, loaded one step early
-    unsigned long long slot[kLaneSlots];
-    auto load_slots = [&](int64_t k) {
-        if (warp == 0 && k >= 0 && k < iters) {
-#pragma unroll
-            for (int u = 0; u < kLaneSlots; ++u)
-                slot[u] = lane + 32 * u < n ? ld_relaxed_u64(a.partials + (r0 + k * R) * n + lane + 32 * u) : 0ull;
+        if (!grid_barrier_wait(&cooperative_groups::details::get_grid_workspace()->barrier, token, a.wait_ns)) {
+            atomicExch(a.header + 0, kDeviceErrTimeout);
+            atomicExch(a.header + 1, 1u);
+            fail0 = 1;
         }
+    }
+
+    // merging warps: this lane's slot of the next row to merge, loaded one step early
+    unsigned long long slot = 0ull;
+    auto load_slot = [&](int64_t k) {
+        if (merger && k >= 0 && k < iters)
+            slot = my_slot < n ? ld_relaxed_u64(a.partials + (r0 + k * R) * n + my_slot) : 0ull;
     };
 
-    // Step j: warp 0 merges the row of slice k = j - L (its slots loaded in
-    // the last step; waiting, bounded, only for any that were still empty)
-    // while every warp takes slice j from its buffer into registers (`cur`)
-    // and folds its part of the slice's partial; one barrier; the buffer takes
-    // slice j + nbuf, warp 1 merges the warp partials and stores the slice's
-    // slot, and every thread normalises slice k (`old`). Returns false on an
-    // error exit.
+    // Step j: the merging warps fold their chunks of the row of slice k = j - L
+    // (waiting, bounded, only for slots that were still empty) while every
+    // warp takes slice j from its buffer into registers (`cur`) and folds its
+    // part of the slice's partial; one barrier; the buffer takes slice
+    // j + nbuf, warp 1 merges the warp partials and stores the slice's slot,
+    // and every thread combines the chunk states and normalises slice k
+    // (`old`). Returns false on an error exit.
     auto step = [&](int64_t j, uint4 (&cur)[MAXV], const uint4 (&old)[MAXV]) -> bool {
         const int64_t k = j - L;
-        int fail = 0;
-        if (warp == 0 && k >= 0) {
+        int fail = j == 0 ? fail0 : 0;
+        if (merger && k >= 0) {
             const int64_t r = r0 + k * R;
-            // (slots past n hold 0: (m, d) = (0, 0), which the merge skips)
-#pragma unroll
-            for (int u = 0; u < kLaneSlots; ++u)
-                if (!fail && lane + 32 * u < n && slot[u] == 0ull &&
-                    !wait_filled(a.partials + r * n + lane + 32 * u, a.header, &slot[u], a.wait_ns))
-                    fail = 1;
-            const MD c = warp_merge_slots(slot);
-            if (lane == 0) row_md[k & 1] = c;
+            if (my_slot < n && slot == 0ull && !wait_filled(a.partials + r * n + my_slot, a.header, &slot, a.wait_ns))
+                fail = 1;
+            // (a lane past n holds (-inf, 0), which the merge skips)
+            const MD c = warp_merge_states(my_slot < n ? unpack_md(slot) : MD{-INFINITY, 0.f});
+            if (lane == 0) row_part[k & 1][chunk] = c;
         }
         if (j < iters) {
             const char* sb = ring.slot(int(j % ring.nbuf));
@@ -692,11 +714,21 @@ __global__ void __launch_bounds__(BLOCK, 512 / BLOCK) split_grouped_kernel(const
                 if (lane == 0 && !(q == 0 && r == a.stall_row)) st_relaxed_u64(a.partials + r * n + q, pack_md(c.m, c.d));
             }
         }
-        load_slots(k + 1);
+        load_slot(k + 1);
         if (k < 0) return true;
-        const MD rm = row_md[k & 1];
-        const float mm = rm.d > 0.f ? rm.m : 0.f;
-        const float inv = safe_inverse(rm.d);
+        // the row's (m, d) from the chunk states, in chunk order
+        float rm = -INFINITY;
+        for (int u = 0; u < U; ++u) {
+            const MD p = row_part[k & 1][u];
+            if (p.d != 0.f) rm = fmaxf(rm, p.m);
+        }
+        float rd = 0.f;
+        for (int u = 0; u < U; ++u) {
+            const MD p = row_part[k & 1][u];
+            if (p.d != 0.f) rd += p.d * ex2_approx((p.m - rm) * kLog2eF);
+        }
+        const float mm = rd > 0.f ? rm : 0.f;
+        const float inv = safe_inverse(rd);
         T* yr = y + (r0 + k * R) * a.ld + lo * V;
 #pragma unroll
         for (int u = 0; u < MAXV; ++u)

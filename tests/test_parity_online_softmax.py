@@ -250,3 +250,29 @@ def test_online_softmax_single_read_repeated_calls_reuse_workspace(oracle, monke
         y = rowops_online_softmax(x, workspace=ws)
         assert rowops_online_softmax_status(ws) == 0
         C.assert_softmax_close(C.to_f64(y), oracle.softmax(x.cpu().numpy()), "f32")
+
+
+def test_online_softmax_row_groups_workspace_never_cleared(oracle, monkeypatch):
+    """The single-kernel row-group form enqueues no fill of the workspace: it
+    zeroes the slots it uses itself. One workspace, first filled with random
+    bytes and then left as each call leaves it, serves calls of different
+    shapes (rows over 76, 38 and 19 CTAs, so slot layouts overlap with
+    different strides) and of both forms in turn (the two-launch form writes
+    chunk partials over the same bytes); every output matches the oracle."""
+    shapes = [(64, 1 << 20, "f32", "row_groups"), (9, 1 << 20, "f32", "two_pass"), (40, 1 << 18, "f32", "row_groups"),
+              (80, 1 << 18, "bf16", "row_groups"), (5, 1 << 21, "f32", "row_groups"), (64, 1 << 20, "f32", "row_groups")]
+    n = max(rowops_online_softmax_workspace_bytes(M, N, workloads.torch_dtype(dt)) for M, N, dt, _ in shapes)
+    g = torch.Generator(device="cuda").manual_seed(123)
+    ws = torch.randint(0, 256, (n,), dtype=torch.uint8, device="cuda", generator=g)
+    for i, (M, N, dt, form) in enumerate(shapes):
+        monkeypatch.setenv("ROWOPS_ONLINE", form)
+        wl = edge(dt, M, N, seed=100 + i, outlier_p=1e-3)
+        x = gu.make_x(wl)["x"]
+        y = rowops_online_softmax(x, workspace=ws)
+        assert rowops_online_softmax_status(ws) == 0
+        rows = gu.sample_rows(M, min(M, 6), seed=i)
+        ref = oracle.softmax(gu.rows_f32(x, rows))
+        C.assert_softmax_close(C.to_f64(y[torch.as_tensor(rows, device=y.device)]), ref, dt,
+                               what=f"call {i}: {form} {dt} {M}x{N}")
+        assert torch.all((y.double().sum(dim=1) - 1).abs() <= (1e-3 if dt == "f32" else 1e-2))
+        del x, y
