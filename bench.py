@@ -10,7 +10,12 @@ and ``value`` is the algorithmic HBM bytes of a step (each input read once,
 each output written once) times the steps, over the device time of the timed
 steps: GB/s. Each input is larger than the 129 MB L2, so no flush is needed
 between steps. The roofline entry is the dominant kernel (LayerNorm+GELU)
-against the measured copy bandwidth.
+against the measured copy bandwidth (MEASURED_PEAKS.json), with its
+fractions of a device-to-device copy timed in this same process and of the
+8 TB/s nominal HBM figure beside it. ``e2e`` repeats the step through the
+public API with pinned host buffers (inputs copied in and results copied out
+inside the timed region) and carries the host link's own ceiling, timed in the
+same run: the same copy pipeline with no kernel.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl rowops|reference]
 
@@ -44,13 +49,16 @@ METRIC = "row-kernel HBM GB/s (% of GB300 peak) for softmax and LayerNorm+GELU"
 STEP = ["softmax_bf16_causal_32768x4096", "online_softmax_f32_64x1048576", "layernorm_gelu_bf16_65536x8192"]
 DOMINANT = "layernorm_gelu_bf16_65536x8192"
 # kernels per call, the fallback when the profiler cannot count them (the
-# online softmax at these sizes: one cooperative kernel, after a memset of its
-# workspace slots)
+# online softmax at these sizes: one cooperative kernel, no memset)
 KERNELS_PER_CALL = {"softmax": 1, "softmax_causal": 1, "online_softmax": 1, "layernorm_gelu": 1,
                     "layernorm_gelu_erf": 1, "rmsnorm": 1, "residual_rmsnorm": 1, "row_sum": 1, "row_max": 1,
                     "layernorm_gelu_backward": 2, "bias_residual_gelu": 1}
 L2_BYTES = 129 * 10**6
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0  # the HBM figure the hardware table gives for this class of GPU
+COPY_PROBE_BYTES = 1 << 30  # the in-run device-to-device copy: 1 GiB, read + write counted
+# arithmetic type of the step (every operation accumulates in fp32) and the I/O types
+STEP_DTYPE = "f32 arithmetic; bf16 I/O (softmax, LayerNorm+GELU), f32 I/O (online softmax)"
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "ln_gelu_bf16_65536x8192.txt")
 DOMINANT_SOURCES = ["row_wise_reduction_gb300/csrc/tma_row_kernels.cuh",
                     "row_wise_reduction_gb300/csrc/row_pipeline.cuh",
@@ -80,6 +88,21 @@ def alg_bytes(wl: workloads.Workload) -> int:
     if wl.op == "layernorm_gelu_backward":  # x, dy in; dx out; w, b in; fp32 dw, db out
         return 3 * wl.M * wl.N * es + (2 * wl.N * es if wl.affine else 0) + 2 * wl.N * 4
     return rows
+
+
+def fractions(achieved: float, peak: float, in_run_copy, nominal: float = NOMINAL_HBM_GBS) -> dict:
+    """The achieved rate as a fraction of the measured peak, of the copy
+    ceiling measured in the same run (None when not measured) and of nominal."""
+    return {"frac": achieved / peak,
+            "frac_of_in_run_copy": achieved / in_run_copy if in_run_copy else None,
+            "frac_of_nominal": achieved / nominal}
+
+
+def link_ceiling(step_bytes: int, copies_only_s: float, steps: int) -> float:
+    """The end-to-end figure the host link allows: the step's algorithmic bytes
+    over the time of the same pipeline with the copies and without the
+    kernels (GB/s)."""
+    return step_bytes * steps / copies_only_s / 1e9
 
 
 def dominant_source_hash() -> str:
@@ -125,7 +148,7 @@ REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_c
 
 
 class ClockSampler:
-    def __init__(self, device: int, period_s: float = 0.005):
+    def __init__(self, device: int, period_s: float = 0.001):
         self.period = period_s
         self.samples = []
         self.max_mhz = None
@@ -205,6 +228,79 @@ class ClockSampler:
         power = [s[2] for s in self.samples if s[2] is not None]
         return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz, "reasons": reasons,
                 "samples": len(mhz), "power_w_max": max(power) if power else None, "source": self.src}
+
+
+def copy_ceiling(dev, reps: int = 10, nbytes: int = COPY_PROBE_BYTES):
+    """Device-to-device copy of `nbytes` (cudaMemcpyAsync through torch's
+    copy_ of same-dtype contiguous tensors), best of `reps` by CUDA events;
+    GB/s counting bytes read + written. Measured in this process, next to the
+    kernels it is the ceiling for."""
+    a = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    b = torch.empty_like(a)
+    a.fill_(1)
+    stream = torch.cuda.current_stream()
+    best = float("inf")
+    for _ in range(reps + 2):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        b.copy_(a)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1) / 1e3)
+    del a, b
+    torch.cuda.empty_cache()
+    return 2 * nbytes / best / 1e9
+
+
+HOST_COST_DRIVER = os.path.join(ROOT, "tests", "native", "host_cost.c")
+
+
+def host_cost_c(timeout_s: float = 120.0):
+    """Per-call host cost of rowops_softmax measured from C (no Python layer):
+    compiles the small driver against librowops.so and the CUDA runtime, runs
+    it and returns its JSON result, or None when no compiler or GPU is there."""
+    import shutil
+    import tempfile
+
+    from row_wise_reduction_gb300 import build as rbuild
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    cuda = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    if cc is None or not os.path.exists(rbuild.LIB):
+        return None
+    with tempfile.TemporaryDirectory() as d:
+        exe = os.path.join(d, "host_cost")
+        libdir = os.path.dirname(rbuild.LIB)
+        cmd = [cc, "-O2", "-std=c11", "-I", os.path.join(ROOT, "include"), "-I", os.path.join(cuda, "include"),
+               HOST_COST_DRIVER, "-o", exe, "-L", libdir, "-l:librowops.so", "-L", os.path.join(cuda, "lib64"),
+               "-lcudart", f"-Wl,-rpath,{libdir}", f"-Wl,-rpath,{os.path.join(cuda, 'lib64')}"]
+        if subprocess.run(cmd, capture_output=True, text=True).returncode != 0:
+            return None
+        r = subprocess.run([exe], capture_output=True, text=True, timeout=timeout_s)
+        if r.returncode != 0:
+            return None
+        return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def host_cost_python(dev, batch: int = 256, batches: int = 20):
+    """The same measurement through the Python binding: wall time of issuing
+    rowops_softmax(x, y) on fp32 1024 x 768, per call (each batch timed while
+    issuing, then synchronised)."""
+    import row_wise_reduction_gb300 as ro
+
+    x = torch.randn(1024, 768, device=dev)
+    y = torch.empty_like(x)
+    for _ in range(200):
+        ro.rowops_softmax(x, y)
+    torch.cuda.synchronize()
+    spent = 0.0
+    for _ in range(batches):
+        t0 = time.perf_counter()
+        for _ in range(batch):
+            ro.rowops_softmax(x, y)
+        spent += time.perf_counter() - t0
+        torch.cuda.synchronize()
+    return spent / (batch * batches) * 1e6
 
 
 # ---------------------------------------------------------------------------
@@ -718,6 +814,8 @@ def run_rowops(args):
         for n in names:
             call(n, inputs[n]["x"], outputs[n])
     torch.cuda.synchronize()
+    # the device-to-device copy ceiling, measured in this process before the timed region
+    copy_gbs = copy_ceiling(dev)
 
     # timed region: K steps, per-operation events on the launching stream
     ev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
@@ -749,7 +847,10 @@ def run_rowops(args):
                      "gbs": alg_bytes(wls[n]) / avg_s / 1e9, "rows_per_s": wls[n].M / avg_s}
     peak, peak_kind = measured_peak()
     for n in names:
-        per_op[n]["frac_of_" + peak_kind] = per_op[n]["gbs"] / peak
+        fr = fractions(per_op[n]["gbs"], peak, copy_gbs)
+        per_op[n]["frac_of_" + peak_kind] = fr["frac"]
+        per_op[n]["frac_of_in_run_copy"] = fr["frac_of_in_run_copy"]
+        per_op[n]["frac_of_nominal"] = fr["frac_of_nominal"]
     # kernels of one step, counted from the CUDA activity trace after the timed region
     per_step = count_kernels(lambda: [call(n, inputs[n]["x"], outputs[n]) for n in names])
     launches_from = "cuda activity trace of one step"
@@ -781,7 +882,7 @@ def run_rowops(args):
         called = {n: None for n in names}
         drained = {n: None for n in names}
 
-        def e2e_step():
+        def e2e_step(calls=True):
             for n in names:
                 with torch.cuda.stream(s_in):
                     if called[n] is not None:
@@ -795,7 +896,8 @@ def run_rowops(args):
                     s_run.wait_event(loaded)
                     if drained[n] is not None:
                         s_run.wait_event(drained[n])
-                    call(n, inputs[n]["x"], outputs[n])
+                    if calls:
+                        call(n, inputs[n]["x"], outputs[n])
                     called[n] = torch.cuda.Event()
                     called[n].record(s_run)
                 with torch.cuda.stream(s_out):
@@ -806,21 +908,31 @@ def run_rowops(args):
                     drained[n] = torch.cuda.Event()
                     drained[n].record(s_out)
 
-        e2e_step()
-        torch.cuda.synchronize()
-        barrier()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(s_in)
-        for _ in range(ke):
-            e2e_step()
-        s_in.wait_stream(s_run)
-        s_in.wait_stream(s_out)
-        b.record(s_in)
-        torch.cuda.synchronize()
-        barrier()
-        es, eb = aggregate(a.elapsed_time(b) / 1e3, step_bytes * ke)
+        def timed(calls):
+            e2e_step(calls)
+            torch.cuda.synchronize()
+            barrier()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s_in)
+            for _ in range(ke):
+                e2e_step(calls)
+            s_in.wait_stream(s_run)
+            s_in.wait_stream(s_out)
+            b.record(s_in)
+            torch.cuda.synchronize()
+            barrier()
+            return a.elapsed_time(b) / 1e3
+
+        es, eb = aggregate(timed(True), step_bytes * ke)
+        # the host link's ceiling in the same run: the same three-stream
+        # pipeline with every copy and no kernel
+        cs, _ = aggregate(timed(False), 0.0)
+        ceiling = link_ceiling(step_bytes, cs, ke)
         e2e = {"value": eb / es / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "steps": ke, "ms_per_step": es / ke * 1e3}
+               "steps": ke, "ms_per_step": es / ke * 1e3,
+               "host_link": {"copies_only_ms_per_step": cs / ke * 1e3,
+                             "h2d_plus_d2h_gbs": (h2d + d2h) * ke / cs / 1e9,
+                             "ceiling": ceiling, "frac_of_ceiling": (eb / es / 1e9) / ceiling}}
 
     extras = None
     if rank == 0 and not args.no_extras and not subset and args.rows_scale == 1.0:
@@ -829,6 +941,12 @@ def run_rowops(args):
     eager = None
     if rank == 0 and not args.no_torch_eager and not subset and args.rows_scale == 1.0:
         eager = run_torch_eager(wls, inputs, stream)
+
+    host_cost = None
+    if rank == 0 and not args.no_extras and not subset and args.rows_scale == 1.0:
+        host_cost = {"python_us_per_call": host_cost_python(dev), "c": host_cost_c(),
+                     "what": "rowops_softmax on fp32 1024 x 768: host time to issue one call (Python binding; "
+                             "C driver tests/native/host_cost.c with its event and CUDA-graph figures)"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -848,8 +966,12 @@ def run_rowops(args):
     roof = None
     if DOMINANT in per_op:
         ach = per_op[DOMINANT]["gbs"]
-        roof = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
-                "peak_kind": peak_kind, "kernel": "ln_gelu_tma_kernel<bf16, 128 threads/row, 8 vectors/thread, 5 rows/CTA, full rows>",
+        fr = fractions(ach, peak, copy_gbs)
+        roof = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": fr["frac"],
+                "peak_kind": peak_kind,
+                "in_run_copy": {"gbs": copy_gbs, "frac": fr["frac_of_in_run_copy"],
+                                "how": "cudaMemcpyAsync device to device of 1 GiB, read + write bytes, best of 10"},
+                "nominal": {"gbs": NOMINAL_HBM_GBS, "frac": fr["frac_of_nominal"]}, "kernel": "ln_gelu_tma_kernel<bf16, 128 threads/row, 8 vectors/thread, 5 rows/CTA, full rows>",
                 "traffic": profiled_traffic() if args.rows_scale == 1.0 else None,
                 "algorithmic_bytes_per_launch": alg_bytes(wls[DOMINANT])}
     line = {
@@ -863,17 +985,20 @@ def run_rowops(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32",
+        "dtype": STEP_DTYPE if not subset else "f32 arithmetic; I/O " + ", ".join(
+            sorted({wl.dtype for wl in wls.values()})),
         "data": "synthetic",
         "config": config_block() if args.rows_scale == 1.0 and not subset else
         {"workload": " + ".join(f"{wl.name}[M={wl.M}]" for wl in wls.values())},
         "roofline": roof,
+        "step_frac": fractions(total_bytes / secs_max / 1e9, peak, copy_gbs),
         "breakdown": per_op,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches,
         "gpu_launches_from": launches_from,
         "extras": extras,
+        "host_cost": host_cost,
         "context_torch_eager": eager,
         "clocks": clocks.summary(),
         "device": torch.cuda.get_device_name(dev),

@@ -33,7 +33,9 @@
  *     at the caller's next synchronisation, as for any CUDA kernel.
  *   - Thread-safe; all entry points may be called from any host thread.
  *
- * Benchmarking knobs (environment, read at every call; unset = automatic):
+ * Benchmarking knobs (environment; unset = automatic). They are read at the
+ * library's first call and kept for the process; rowops_reload_tuning()
+ * reads them again (for code that changes them between calls, e.g. tests):
  *   ROWOPS_KERNEL=tma|reg|looped  kernel family: TMA-fed row pipeline, register-resident
  *                                 row groups, or the looped any-N kernels
  *   ROWOPS_FORCE_TPR=<16..1024>   threads per row (tma: 64..512); row-group split softmax:
@@ -101,6 +103,14 @@ typedef enum rowops_status {
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* rowops_status_string(rowops_status_t status);
+
+/*
+ * Re-reads the ROWOPS_* benchmarking knobs (listed at the top of this header)
+ * from the process environment; later calls use the new values. Without it
+ * the knobs are read once, at the first call. No CUDA call; thread-safe.
+ * (No counterpart on the source pages: a knob-handling convenience.)
+ */
+void rowops_reload_tuning(void);
 
 /*
  * Stable softmax of every row [EX §2.4 Softmax; KT "Triton Softmax"]:

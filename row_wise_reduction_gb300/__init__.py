@@ -21,6 +21,7 @@ from .rowops import (  # noqa: F401
     rowops_layernorm_gelu_backward_workspace_bytes,
     rowops_layernorm_gelu_erf,
     rowops_online_softmax,
+    rowops_online_softmax_noalloc,
     rowops_online_softmax_status,
     rowops_online_softmax_workspace_bytes,
     rowops_rmsnorm,
@@ -28,5 +29,6 @@ from .rowops import (  # noqa: F401
     rowops_row_sum,
     rowops_softmax,
     rowops_softmax_causal,
+    rowops_reload_tuning,
     rowops_status_string,
 )

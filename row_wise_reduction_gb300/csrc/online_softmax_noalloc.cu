@@ -31,6 +31,7 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratch
 
 struct NoallocDevice {
     int device;
+    unsigned long long ctx;  // the context the address belongs to (current_context_id)
     void* scratch;  // device address of g_noalloc_scratch on this device
     int num_sms;
     int max_smem_optin;
@@ -39,23 +40,33 @@ struct NoallocDevice {
 std::mutex g_noalloc_mu;
 std::vector<NoallocDevice> g_noalloc_devices;
 
-// Look up (once per device, with that device current) the device address of
-// the scratch array and the SM count.
+// Look up (once per device and context, with that device current) the device
+// address of the scratch array and the SM count. A new context on the device
+// (after cudaDeviceReset) has a new id, so the address is looked up again:
+// the array of a context that is gone is never handed to a kernel.
 cudaError_t noalloc_device(int dev, NoallocDevice* out) {
+    const unsigned long long ctx = current_context_id();
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
     for (const auto& d : g_noalloc_devices)
-        if (d.device == dev) {
+        if (d.device == dev && d.ctx == ctx && ctx != 0) {
             *out = d;
             return cudaSuccess;
         }
-    NoallocDevice d{dev, nullptr, 0, 0};
+    NoallocDevice d{dev, 0, nullptr, 0, 0};
     cudaError_t e = cudaGetSymbolAddress(&d.scratch, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return e;
-    g_noalloc_devices.push_back(d);
+    d.ctx = current_context_id();  // (the symbol lookup made a context current if none was)
+    bool replaced = false;
+    for (auto& old : g_noalloc_devices)
+        if (old.device == dev) {
+            old = d;
+            replaced = true;
+        }
+    if (!replaced) g_noalloc_devices.push_back(d);
     *out = d;
     return cudaSuccess;
 }
@@ -121,6 +132,7 @@ extern "C" rowops_status_t rowops_online_softmax_noalloc(const void* x, void* y,
     LaunchCfg cfg;
     cfg.stream = stream;
     cfg.device = dev;
+    cfg.ctx = nd.ctx;
     cfg.num_sms = nd.num_sms;
     cfg.max_smem_optin = nd.max_smem_optin;
     cfg.ctas_per_sm = 0;

@@ -20,7 +20,8 @@ bool valid_dtype(rowops_dtype_t dt) { return dt == ROWOPS_F32 || dt == ROWOPS_BF
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Benchmarking knobs, read at every call (see include/rowops.h).
+// Benchmarking knobs, read from the environment at the first call and again
+// on rowops_reload_tuning() (see include/rowops.h).
 enum class Family { Auto, Tma, Reg, Looped };
 struct Tuning {
     int tpr = 0;
@@ -91,6 +92,21 @@ Tuning read_tuning() {
     return t;
 }
 
+// The process's knobs: read once, then reused (a scan of the environment per
+// call cost a measurable share of a small launch's host time).
+std::mutex g_tuning_mu;
+bool g_tuning_loaded = false;
+Tuning g_tuning;
+
+Tuning tuning() {
+    std::lock_guard<std::mutex> lk(g_tuning_mu);
+    if (!g_tuning_loaded) {
+        g_tuning = read_tuning();
+        g_tuning_loaded = true;
+    }
+    return g_tuning;
+}
+
 // Checks shared by every entry point. M == 0 passes (callers then return).
 rowops_status_t check_rows(const void* x, const void* y, int64_t M, int64_t N, int64_t ld,
                            rowops_dtype_t dt) {
@@ -117,6 +133,7 @@ rowops_status_t check_rows(const void* x, const void* y, int64_t M, int64_t N, i
 __device__ unsigned g_device_error;
 
 struct DeviceInfo {
+    unsigned long long ctx = 0;  // context the cached values belong to
     int num_sms = 0;
     int max_smem_optin = 0;
     unsigned* err = nullptr;  // device address of g_device_error on this device
@@ -128,7 +145,8 @@ std::vector<std::pair<int, DeviceInfo>> g_devices;
 
 struct OccEntry {
     const void* func;
-    int device, block;
+    unsigned long long ctx;
+    int block;
     size_t smem;
     int blocks_per_sm;
 };
@@ -136,15 +154,16 @@ std::vector<OccEntry> g_occ;
 
 struct SmemEntry {
     const void* func;
-    int device;
+    unsigned long long ctx;
     size_t smem;
 };
 std::vector<SmemEntry> g_smem;
 
 cudaError_t device_info(int dev, DeviceInfo* out) {
+    const unsigned long long ctx = current_context_id();
     std::lock_guard<std::mutex> lk(g_mu);
     for (auto& d : g_devices)
-        if (d.first == dev) {
+        if (d.first == dev && d.second.ctx == ctx && ctx != 0) {
             *out = d.second;
             return cudaSuccess;
         }
@@ -153,9 +172,19 @@ cudaError_t device_info(int dev, DeviceInfo* out) {
     if (e == cudaSuccess)
         e = cudaDeviceGetAttribute(&di.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&di.cooperative, cudaDevAttrCooperativeLaunch, dev);
+    // (the symbol lookup also makes the device's primary context current if
+    // no context was yet, so the id is taken after it)
     if (e == cudaSuccess) e = cudaGetSymbolAddress(reinterpret_cast<void**>(&di.err), g_device_error);
     if (e != cudaSuccess) return e;
-    g_devices.emplace_back(dev, di);
+    di.ctx = current_context_id();
+    // one entry per device: a reset context's entry is replaced
+    bool replaced = false;
+    for (auto& d : g_devices)
+        if (d.first == dev) {
+            d.second = di;
+            replaced = true;
+        }
+    if (!replaced) g_devices.emplace_back(dev, di);
     *out = di;
     return cudaSuccess;
 }
@@ -167,6 +196,7 @@ rowops_status_t make_cfg(cudaStream_t stream, const Tuning& tn, LaunchCfg* cfg) 
     if (device_info(dev, &di) != cudaSuccess) return ROWOPS_ERR_CUDA;
     cfg->stream = stream;
     cfg->device = dev;
+    cfg->ctx = di.ctx;
     cfg->num_sms = di.num_sms;
     cfg->max_smem_optin = di.max_smem_optin;
     cfg->ctas_per_sm = tn.ctas_per_sm;
@@ -371,7 +401,7 @@ using TmaRmsLookup = TmaRmsKernel (*)(int tpr, int vpt, int rows, bool full);
 rowops_status_t rms_dispatch(const void* x, const void* r, void* y, void* ro, const void* w, float eps, int64_t M,
                              int64_t N, int64_t ld, rowops_dtype_t dtype, cudaStream_t stream) {
     const bool res = r != nullptr;
-    const Tuning tn = read_tuning();
+    const Tuning tn = tuning();
     LaunchCfg cfg;
     rowops_status_t st = make_cfg(stream, tn, &cfg);
     if (st != ROWOPS_OK) return st;
@@ -426,14 +456,42 @@ bool rows_disjoint(const void* a, const void* b, int64_t M, int64_t N, int64_t l
 int ctas_per_sm(const void* func, int block, size_t smem, const LaunchCfg& cfg) {
     std::lock_guard<std::mutex> lk(g_mu);
     for (auto& o : g_occ)
-        if (o.func == func && o.device == cfg.device && o.block == block && o.smem == smem) return o.blocks_per_sm;
+        if (o.func == func && o.ctx == cfg.ctx && o.block == block && o.smem == smem) return o.blocks_per_sm;
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, func, block, smem) != cudaSuccess) {
         cudaGetLastError();
         n = 0;
     }
-    g_occ.push_back(OccEntry{func, cfg.device, block, smem, n});
+    g_occ.push_back(OccEntry{func, cfg.ctx, block, smem, n});
     return n;
+}
+
+namespace {
+using CtxGetCurrentFn = int (*)(void**);                  // CUresult cuCtxGetCurrent(CUcontext*)
+using CtxGetIdFn = int (*)(void*, unsigned long long*);   // CUresult cuCtxGetId(CUcontext, unsigned long long*)
+std::once_flag g_ctx_fn_once;
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+}  // namespace
+
+unsigned long long current_context_id() {
+    std::call_once(g_ctx_fn_once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(f);
+        cudaGetLastError();
+    });
+    if (!g_ctx_get_current || !g_ctx_get_id) return 0;
+    void* ctx = nullptr;
+    unsigned long long id = 0;
+    if (g_ctx_get_current(&ctx) != 0 || ctx == nullptr || g_ctx_get_id(ctx, &id) != 0) return 0;
+    return id;
 }
 
 int grid_for(const void* func, int block, size_t smem, int64_t items, const LaunchCfg& cfg) {
@@ -456,7 +514,7 @@ cudaError_t allow_smem(const void* func, size_t smem, const LaunchCfg& cfg, bool
     if (smem == 0 || (smem <= 32 * 1024 && !max_carveout)) return cudaSuccess;
     std::lock_guard<std::mutex> lk(g_mu);
     for (auto& s : g_smem)
-        if (s.func == func && s.device == cfg.device && s.smem >= smem) return cudaSuccess;
+        if (s.func == func && s.ctx == cfg.ctx && s.smem >= smem) return cudaSuccess;
     cudaError_t e = cudaSuccess;
     if (max_carveout)
         e = cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -465,7 +523,7 @@ cudaError_t allow_smem(const void* func, size_t smem, const LaunchCfg& cfg, bool
     // well before the dynamic part alone reaches it
     if (e == cudaSuccess && smem > 32 * 1024)
         e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e == cudaSuccess) g_smem.push_back(SmemEntry{func, cfg.device, smem});
+    if (e == cudaSuccess) g_smem.push_back(SmemEntry{func, cfg.ctx, smem});
     return e;
 }
 
@@ -474,6 +532,13 @@ cudaError_t allow_smem(const void* func, size_t smem, const LaunchCfg& cfg, bool
 using namespace rowops;
 
 extern "C" {
+
+void rowops_reload_tuning(void) {
+    const Tuning t = read_tuning();
+    std::lock_guard<std::mutex> lk(g_tuning_mu);
+    g_tuning = t;
+    g_tuning_loaded = true;
+}
 
 const char* rowops_status_string(rowops_status_t status) {
     switch (status) {
@@ -491,7 +556,7 @@ rowops_status_t rowops_softmax(const void* x, void* y, int64_t M, int64_t N, int
                                rowops_dtype_t dtype, cudaStream_t stream) {
     rowops_status_t st = check_rows(x, y, M, N, ld, dtype);
     if (st != ROWOPS_OK || M == 0) return st;
-    const Tuning tn = read_tuning();
+    const Tuning tn = tuning();
     LaunchCfg cfg;
     if ((st = make_cfg(stream, tn, &cfg)) != ROWOPS_OK) return st;
     const int es = elem_bytes(dtype);
@@ -518,7 +583,7 @@ rowops_status_t rowops_softmax_causal(const void* x, void* y, int64_t M, int64_t
     const int64_t lim = int64_t(1) << 62;  // keeps (r mod period) + offset + 1 in range
     if (period < 1 || offset > lim || offset < -lim) return ROWOPS_ERR_INVALID_VALUE;
     if (M == 0) return ROWOPS_OK;
-    const Tuning tn = read_tuning();
+    const Tuning tn = tuning();
     LaunchCfg cfg;
     if ((st = make_cfg(stream, tn, &cfg)) != ROWOPS_OK) return st;
     const int es = elem_bytes(dtype);
@@ -540,7 +605,7 @@ namespace {
 // Row sum (op 0) / row max (op 1): arguments checked by the callers.
 rowops_status_t reduce_dispatch(const void* x, float* out, int64_t M, int64_t N, int64_t ld, rowops_dtype_t dtype,
                                 int op, cudaStream_t stream) {
-    const Tuning tn = read_tuning();
+    const Tuning tn = tuning();
     LaunchCfg cfg;
     rowops_status_t st = make_cfg(stream, tn, &cfg);
     if (st != ROWOPS_OK) return st;
@@ -602,7 +667,7 @@ rowops_status_t rowops_bias_residual_gelu(const void* x, const void* residual, c
         const uintptr_t sb = uintptr_t(N) * es, sy = uintptr_t(((M - 1) * ld + N) * es);
         if (pb < py + sy && py < pb + sb) return ROWOPS_ERR_INVALID_VALUE;
     }
-    const Tuning tn = read_tuning();
+    const Tuning tn = tuning();
     LaunchCfg cfg;
     if ((st = make_cfg(stream, tn, &cfg)) != ROWOPS_OK) return st;
     const bool vec = tn.family != Family::Looped && N % (16 / es) == 0 && rows_aligned(x, y, ld, es) &&
@@ -635,7 +700,7 @@ rowops_status_t rowops_gelu(const void* x, void* y, int64_t n, int approximate, 
     if (n == 0) return ROWOPS_OK;
     rowops_status_t st = check_rows(x, y, 1, n, n, dtype);  // one row of n elements
     if (st != ROWOPS_OK) return st;
-    const Tuning tn = read_tuning();
+    const Tuning tn = tuning();
     LaunchCfg cfg;
     if ((st = make_cfg(stream, tn, &cfg)) != ROWOPS_OK) return st;
     const GeluLaunch fn = dtype == ROWOPS_F32 ? gelu_f32(approximate == 0) : gelu_bf16(approximate == 0);
@@ -651,7 +716,7 @@ rowops_status_t ln_gelu_dispatch(const void* x, void* y, const void* w, const vo
     if (M == 0) return ROWOPS_OK;
     const int es = elem_bytes(dtype);
     if ((w && !aligned(w, es)) || (b && !aligned(b, es))) return ROWOPS_ERR_INVALID_VALUE;
-    const Tuning tn = read_tuning();
+    const Tuning tn = tuning();
     LaunchCfg cfg;
     if ((st = make_cfg(stream, tn, &cfg)) != ROWOPS_OK) return st;
     TmaChoice tc;
@@ -745,7 +810,7 @@ rowops_status_t rowops_layernorm_gelu_backward(const void* x, const void* dy, co
     // dx is written while x and dy rows may still be read by other CTAs
     if (M > 0 && (!rows_disjoint(dx, x, M, N, ld, es) || !rows_disjoint(dx, dy, M, N, ld, es)))
         return ROWOPS_ERR_INVALID_VALUE;
-    const Tuning tn = read_tuning();
+    const Tuning tn = tuning();
     LaunchCfg cfg;
     if ((st = make_cfg(stream, tn, &cfg)) != ROWOPS_OK) return st;
     if (M == 0) {  // no rows: zero gradients
@@ -823,7 +888,7 @@ rowops_status_t rowops_online_softmax(const void* x, void* y, int64_t M, int64_t
     if (!workspace || !aligned(workspace, 256) ||
         workspace_bytes < rowops_online_softmax_workspace_bytes(M, N, dtype))
         return ROWOPS_ERR_WORKSPACE;
-    const Tuning tn = read_tuning();
+    const Tuning tn = tuning();
     LaunchCfg cfg;
     if ((st = make_cfg(stream, tn, &cfg)) != ROWOPS_OK) return st;
     const int es = elem_bytes(dtype);

@@ -14,9 +14,18 @@ __host__ __device__ constexpr int row_phase_period(int64_t row_bytes) {
     return (row_bytes & 15) == 0 ? 1 : 16 / int(row_bytes & -row_bytes & 15);
 }
 
+// The unique id of the CUDA context current on this thread (cuCtxGetId of
+// cuCtxGetCurrent, reached through the runtime's driver entry points), 0 when
+// no context is current yet. Per-device caches are keyed on it as well as the
+// device: after cudaDeviceReset the next context gets a new id, so symbol
+// addresses and function attributes are looked up and set again instead of
+// reusing values of a context that no longer exists.
+unsigned long long current_context_id();
+
 struct LaunchCfg {
     cudaStream_t stream;
     int device;
+    unsigned long long ctx = 0;  // current_context_id() of the call
     int num_sms;
     int max_smem_optin;  // bytes of dynamic shared memory a CTA may opt in to
     int ctas_per_sm;     // 0: occupancy limit; -1: one CTA per work item; k > 0: k per SM

@@ -39,6 +39,7 @@ __all__ = [
     "rowops_rmsnorm",
     "rowops_fused_residual_rmsnorm",
     "rowops_status_string",
+    "rowops_reload_tuning",
     "ROWOPS_F32",
     "ROWOPS_BF16",
     "STATUS",
@@ -86,6 +87,8 @@ def library() -> ctypes.CDLL:
         L = ctypes.CDLL(_LIB_PATH)
         L.rowops_status_string.restype = ctypes.c_char_p
         L.rowops_status_string.argtypes = [ctypes.c_int]
+        L.rowops_reload_tuning.restype = None
+        L.rowops_reload_tuning.argtypes = []
         L.rowops_softmax.restype = ctypes.c_int
         L.rowops_softmax.argtypes = [_vp, _vp, _i64, _i64, _i64, ctypes.c_int, _vp]
         L.rowops_online_softmax_workspace_bytes.restype = ctypes.c_size_t
@@ -130,6 +133,12 @@ def library() -> ctypes.CDLL:
 
 def rowops_status_string(status: int) -> str:
     return library().rowops_status_string(int(status)).decode()
+
+
+def rowops_reload_tuning() -> None:
+    """Make the library read the ROWOPS_* knobs from the environment again
+    (it reads them once, at its first call, otherwise)."""
+    library().rowops_reload_tuning()
 
 
 def _dtype_code(t: torch.Tensor) -> int:

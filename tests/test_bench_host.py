@@ -89,3 +89,39 @@ def test_kernel_count_without_gpu_activity_falls_back():
     import bench
     assert bench.count_kernels(lambda: None) is None
     assert set(bench.KERNELS_PER_CALL) >= {"softmax_causal", "online_softmax", "layernorm_gelu"}
+
+
+def test_fractions_of_the_three_ceilings():
+    """The bench line reports one rate against the measured peak, the
+    copy measured in the same run and nominal HBM; a missing in-run copy gives
+    no fraction rather than a wrong one."""
+    import bench
+
+    f = bench.fractions(6000.0, 6690.5, 6500.0)
+    assert f["frac"] == 6000.0 / 6690.5
+    assert f["frac_of_in_run_copy"] == 6000.0 / 6500.0
+    assert f["frac_of_nominal"] == 6000.0 / bench.NOMINAL_HBM_GBS == 0.75
+    assert bench.fractions(6000.0, 6690.5, None)["frac_of_in_run_copy"] is None
+
+
+def test_host_link_ceiling_arithmetic():
+    """The end-to-end ceiling is the step's algorithmic bytes over the time of
+    the copy-only pipeline: 3.22 GB per step, 5 steps in 50 ms -> 322 GB/s."""
+    import bench
+
+    step = sum(bench.alg_bytes(bench.workloads.WORKLOADS[n]) for n in bench.STEP)
+    assert step == 3221258240
+    assert abs(bench.link_ceiling(step, 0.050, 5) - step * 5 / 0.050 / 1e9) < 1e-9
+    assert abs(bench.link_ceiling(step, 0.050, 5) - 322.125824) < 1e-6
+
+
+def test_step_dtype_label_names_both_io_types():
+    """The step computes in fp32 with bf16 and fp32 inputs and outputs; the
+    label says so instead of a single type."""
+    import bench
+    from row_wise_reduction_gb300 import workloads
+
+    io = {workloads.WORKLOADS[n].dtype for n in bench.STEP}
+    assert io == {"bf16", "f32"}
+    assert bench.STEP_DTYPE.startswith("f32 arithmetic")
+    assert "bf16" in bench.STEP_DTYPE and "f32 I/O" in bench.STEP_DTYPE
