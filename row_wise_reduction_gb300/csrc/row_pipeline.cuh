@@ -187,8 +187,8 @@ struct RowRing {
 };
 
 // Bytes of dynamic shared memory before the row buffers: the mbarriers of all
-// row groups' rings (ROWS * nbuf <= 16), padded.
-constexpr uint32_t kRingHeader = 128;
+// row groups' rings (ROWS * nbuf <= 32), padded.
+constexpr uint32_t kRingHeader = 256;
 constexpr int kMaxRingBuffers = 16;
 
 __host__ __device__ constexpr uint32_t ring_row_bytes(int64_t N, int es) {

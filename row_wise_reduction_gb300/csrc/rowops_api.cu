@@ -375,7 +375,7 @@ int choose_group_rows(int tpr, int nbuf, const Tuning& tn, CtasOf ctas) {
     auto warps = [&](int rows) { return rows * nbuf > kTmaMaxSlots ? 0 : ctas(rows) * tpr * rows / 32; };
     if (tn.rows >= 1) return warps(tn.rows) > 0 ? tn.rows : 1;
     int best = 1, best_warps = warps(1);
-    for (int r : {2, 4, 5, 8}) {
+    for (int r : {2, 4, 5, 8, 10}) {
         const int w = warps(r);
         if (w > best_warps) {
             best = r;

@@ -74,8 +74,8 @@ constexpr int kTmaBlocks[] = {64, 128, 256, 512};
 constexpr int kNumTmaBlocks = 4;
 constexpr int kTmaVpts[] = {1, 2, 3, 4, 8};
 constexpr int kNumTmaVpts = 5;
-constexpr int kTmaRingHeader = 128;
-constexpr int kTmaMaxSlots = 16;  // ring slots of all row groups of a CTA (mbarriers in the ring header)
+constexpr int kTmaRingHeader = 256;
+constexpr int kTmaMaxSlots = 32;  // ring slots of all row groups of a CTA (mbarriers in the ring header)
 // dynamic schedule: one CTA per work unit of rows_per_cta * unit_rows rows
 inline int dyn_grid(int64_t M, int rows_per_cta, int unit_rows) {
     const int64_t unit = int64_t(rows_per_cta) * unit_rows;
@@ -111,8 +111,8 @@ constexpr int kTmaMultiTpr[] = {64, 128, 256};
 constexpr int kNumTmaMultiTpr = 3;
 constexpr int kTmaMultiVpt[] = {2, 4, 8};
 constexpr int kNumTmaMultiVpt = 3;
-constexpr int kTmaMultiRows[] = {2, 4, 5, 8};
-constexpr int kNumTmaMultiRows = 4;
+constexpr int kTmaMultiRows[] = {2, 4, 5, 8, 10};
+constexpr int kNumTmaMultiRows = 5;
 using TmaCtasQuery = int (*)(int64_t N, int nbuf, const LaunchCfg& cfg);
 struct TmaLnGeluKernel {
     TmaLnGeluLaunch launch;     // nullptr: no such instantiation

@@ -110,7 +110,8 @@ constexpr TmaLnGeluKernel ln_gelu_entry() {
     // 5 groups of 128 x 8 for the tanh form only: the exact form's extra
     // registers spill at 640 threads (443.6 us with 4 groups, 462.5 with 5,
     // bf16 65536 x 8192)
-    if constexpr (R == 1 || (P * R <= 512 && R != 5) || (P == 128 && V == 8 && R == 5 && !ERF))
+    if constexpr (R == 1 || (P * R <= 512 && R != 5) || (P == 128 && V == 8 && R == 5 && !ERF) ||
+                  (P == 128 && V == 4 && R == 5 && !ERF) || (P == 64 && V == 8 && R == 10 && !ERF))
         return TmaLnGeluKernel{launch_ln_gelu_tma_rows<T, P, V, R, F, ERF>, ctas_ln_gelu_tma_rows<T, P, V, R, F, ERF>};
     else
         return TmaLnGeluKernel{nullptr, nullptr};
@@ -120,7 +121,7 @@ constexpr TmaLnGeluKernel ln_gelu_entry() {
      ln_gelu_entry<T, P, 4, 1, F, ERF>(), ln_gelu_entry<T, P, 8, 1, F, ERF>()}
 #define ROWOPS_LN3(T, P, V, F) \
     {ln_gelu_entry<T, P, V, 2, F, ERF>(), ln_gelu_entry<T, P, V, 4, F, ERF>(), ln_gelu_entry<T, P, V, 5, F, ERF>(), \
-     ln_gelu_entry<T, P, V, 8, F, ERF>()}
+     ln_gelu_entry<T, P, V, 8, F, ERF>(), ln_gelu_entry<T, P, V, 10, F, ERF>()}
 #define ROWOPS_LN2(T, P, F) {ROWOPS_LN3(T, P, 2, F), ROWOPS_LN3(T, P, 4, F), ROWOPS_LN3(T, P, 8, F)}
 
 template <int N>

@@ -150,33 +150,41 @@ def _dtype_code(t: torch.Tensor) -> int:
 
 
 def _rows(t: torch.Tensor, name: str):
-    """(M, N, ld) of a 2-D CUDA tensor with unit column stride."""
+    """(M, N, ld) of a 2-D CUDA tensor with unit column stride. (Each tensor
+    property is read once: at the small, launch-bound sizes the binding's own
+    checks are a visible share of a call.)"""
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
-    if t.dim() != 2:
+    sh = t.shape
+    if len(sh) != 2:
         raise ValueError(f"{name} must be 2-D (M, N)")
-    M, N = t.shape
-    if N > 0 and t.stride(1) != 1:
+    M, N = sh
+    st = t.stride()
+    if N > 0 and st[1] != 1:
         raise ValueError(f"{name} must have unit column stride")
-    ld = t.stride(0) if M > 1 else max(N, t.stride(0))
-    return M, N, ld
+    return M, N, (st[0] if M > 1 else max(N, st[0]))
 
 
 def _out_like(x: torch.Tensor, y: Optional[torch.Tensor]) -> torch.Tensor:
     if y is None:
         return torch.empty_strided(x.shape, x.stride(), dtype=x.dtype, device=x.device)
-    if y.shape != x.shape or y.dtype != x.dtype or y.device != x.device:
+    if y.dtype is not x.dtype or y.get_device() != x.get_device() or y.shape != x.shape:
         raise ValueError("y must match x in shape, dtype and device")
     if y.shape[0] > 1 and y.stride() != x.stride():
         raise ValueError("x and y must share the row stride")
     return y
 
 
+_current_device = getattr(torch._C, "_cuda_getDevice", None) or torch.cuda.current_device
+_current_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream, device=None) -> int:
     if stream is None:
-        # the raw handle of the current stream (the cheap form of
-        # torch.cuda.current_stream().cuda_stream)
-        return torch._C._cuda_getCurrentRawStream(torch.cuda.current_device() if device is None else device)
+        # the raw handle of the current device's current stream (the cheap
+        # form of torch.cuda.current_stream().cuda_stream; the tensors passed
+        # in are CUDA tensors, so CUDA is initialised already)
+        return _current_raw_stream(_current_device() if device is None else device)
     if isinstance(stream, torch.cuda.Stream):
         return stream.cuda_stream
     return int(stream)

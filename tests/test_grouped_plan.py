@@ -22,7 +22,7 @@ OPTIN = 232448  # bytes of dynamic shared memory a CTA may opt in to on GB300
 
 def ring_bytes(per_sm):
     """A CTA's share of the SM's shared memory, as the launcher computes it."""
-    return (OPTIN + 1024) // per_sm - 1024 - 128 - 512
+    return (OPTIN + 1024) // per_sm - 1024 - 256 - 512
 
 
 def slots_per_row(nvec, vec):
