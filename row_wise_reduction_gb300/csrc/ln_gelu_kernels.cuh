@@ -64,20 +64,23 @@ __device__ __forceinline__ float2 gelu_tanh_approx2(float2 z) {
 }
 
 __device__ __forceinline__ float2 gelu_erf2(float2 z) {
-    constexpr float p = 0.3275911f, a1 = 0.254829592f, a2 = -0.284496736f, a3 = 1.421413741f,
-                    a4 = -1.453152027f, a5 = 1.061405429f;
-    const float2 u = f2_mul(make_float2(fabsf(z.x), fabsf(z.y)), f2(0.70710678118654752f));
-    const float2 d = f2_fma(f2(p), u, f2(1.f));
+    // the same evaluation as gelu_erf with the constants folded: t = 1 / (1 +
+    // (p / sqrt 2) |z|), h = (q / 2) from coefficients a_i / 2, and e^{-u^2} =
+    // 2^{z^2 (-log2(e) / 2)}, so neither u nor the factor 1/2 costs an instruction
+    constexpr float ps = float(0.3275911 * 0.70710678118654752), b1 = float(0.5 * 0.254829592),
+                    b2 = float(0.5 * -0.284496736), b3 = float(0.5 * 1.421413741), b4 = float(0.5 * -1.453152027),
+                    b5 = float(0.5 * 1.061405429), ce = float(-0.5 * kLog2e);
+    const float2 d = f2_fma(f2(ps), make_float2(fabsf(z.x), fabsf(z.y)), f2(1.f));
     const float2 t = make_float2(rcp_approx(d.x), rcp_approx(d.y));
-    float2 poly = f2_fma(t, f2(a5), f2(a4));
-    poly = f2_fma(t, poly, f2(a3));
-    poly = f2_fma(t, poly, f2(a2));
-    poly = f2_fma(t, poly, f2(a1));
-    const float2 g = f2_mul(f2_mul(u, u), f2(-kLog2eF));
-    const float2 q = f2_mul(f2_mul(poly, t), make_float2(ex2_approx(g.x), ex2_approx(g.y)));
-    const float2 pos = f2_mul(z, f2_fma(f2(-0.5f), q, f2(1.f)));
-    const float2 neg = f2_mul(f2_mul(f2(0.5f), z), q);
-    return make_float2(z.x >= 0.f ? pos.x : neg.x, z.y >= 0.f ? pos.y : neg.y);
+    float2 poly = f2_fma(t, f2(b5), f2(b4));
+    poly = f2_fma(t, poly, f2(b3));
+    poly = f2_fma(t, poly, f2(b2));
+    poly = f2_fma(t, poly, f2(b1));
+    const float2 g = f2_mul(f2_mul(z, z), f2(ce));
+    const float2 h = f2_mul(f2_mul(poly, t), make_float2(ex2_approx(g.x), ex2_approx(g.y)));  // erfc(u) / 2
+    const float2 zh = f2_mul(z, h);
+    const float2 pos = f2_fma(zh, f2(-1.f), z);  // z (1 - q/2)
+    return make_float2(z.x >= 0.f ? pos.x : zh.x, z.y >= 0.f ? pos.y : zh.y);
 }
 
 template <bool ERF>
