@@ -135,7 +135,9 @@ __global__ void __launch_bounds__(TPR)
     float mean_a = 0.f, rstd_a = 0.f, shift_a = 0.f;      // stage A's row
     float rstd_c = 0.f, m1_c = 0.f, m2_c = 0.f;           // stage C's row (-m1, -m2 times rstd)
 
-    for (int64_t k = 0;; ++k) {
+    RingCursor rk;  // ring slot and phase parity of row k
+    for (int64_t k = 0;; ++k, rk.next(nbuf)) {
+        const int sa = rk.slot >= 2 ? rk.slot - 2 : rk.slot - 2 + nbuf;  // slot of row k-2 (nbuf >= 4)
         if (k >= 3) {  // C: dx of row k-3
             T* dxr = dx + (p.first + (k - 3) * p.stride) * ld;
 #pragma unroll
@@ -154,7 +156,7 @@ __global__ void __launch_bounds__(TPR)
         float sv[4] = {0.f, 0.f, 0.f, 0.f};  // Q: sum (x - mean)^2, sum (x - mean); A: sum dxh, sum dxh xh
         float s1 = 0.f;                      // S: sum x
         if (k >= 2 && k - 2 < n) {           // A: row k-2
-            const char* sb = p.ring.slot(int((k - 2) % nbuf));
+            const char* sb = p.ring.slot(sa);
             float2 a1 = f2(0.f), a2 = f2(0.f);
 #pragma unroll
             for (int j = 0; j < VPT; ++j) {
@@ -194,9 +196,8 @@ __global__ void __launch_bounds__(TPR)
         }
         int fail = 0;
         if (k < n) {  // S: row k
-            const int s = int(k % nbuf);
-            fail = !mbar_wait(p.ring.bar + s, uint32_t((k / nbuf) & 1), wait_ns);
-            const char* ss = p.ring.slot(s);
+            fail = !mbar_wait(p.ring.bar + rk.slot, rk.parity, wait_ns);
+            const char* ss = p.ring.slot(rk.slot);
             float2 s2 = f2(0.f), q2 = f2(0.f);
             float xv[V];
             E::unpack(lds16(ss + size_t(t) * 16), xv);
@@ -229,8 +230,7 @@ __global__ void __launch_bounds__(TPR)
             return;
         }
         if (k >= 2 && k - 2 < n)  // stage A is done with row k-2's slot
-            refill_rows<T, true, 2>(p, int((k - 2) % nbuf), p.first + (k - 2) * p.stride, src, M, N, ld,
-                                    stall_row);
+            refill_rows<T, true, 2>(p, sa, p.first + (k - 2) * p.stride, src, M, N, ld, stall_row);
         rstd_c = rstd_a;
         m1_c = -rstd_a * (sv[2] / fN);
         m2_c = -rstd_a * (sv[3] / fN);
@@ -286,11 +286,12 @@ __global__ void __launch_bounds__(TPR)
 #pragma unroll
         for (int e = 0; e < V; ++e) aw[j][e] = ab[j][e] = 0.f;
 
-    for (int64_t i = 0;; ++i) {
+    RingCursor rc;
+    for (int64_t i = 0;; ++i, rc.next(nbuf)) {
         const int64_t row = p.first + i * p.stride;
         if (row >= M) break;
-        const int s = int(i % nbuf);
-        int fail = !mbar_wait(p.ring.bar + s, uint32_t((i / nbuf) & 1), wait_ns);
+        const int s = rc.slot;
+        int fail = !mbar_wait(p.ring.bar + s, rc.parity, wait_ns);
         const char* sbuf = p.ring.slot(s);
         float v[VPT][V], g[VPT][V];
         float sum = 0.f;

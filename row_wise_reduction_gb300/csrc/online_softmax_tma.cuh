@@ -109,15 +109,16 @@ __global__ void __launch_bounds__(TPR)
     split_start<T, TPR, VPT>(ring, x, items, nchunks, ld, stall_row, order);
 
     bool signalled = false;
-    for (int64_t i = 0;; ++i) {
+    RingCursor rc;
+    for (int64_t i = 0;; ++i, rc.next(nbuf)) {
         const int64_t k = int64_t(blockIdx.x) + i * gridDim.x;
         if (k >= items) break;
         if (!signalled && k + int64_t(nbuf) * gridDim.x >= items) {  // no copy left to issue
             asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
             signalled = true;
         }
-        const int s = int(i % nbuf);
-        int fail = !mbar_wait(ring.bar + s, uint32_t((i / nbuf) & 1), wait_ns);
+        const int s = rc.slot;
+        int fail = !mbar_wait(ring.bar + s, rc.parity, wait_ns);
         const char* sb = ring.slot(s);
         float v[VPT][V];
         float m = -INFINITY;
@@ -162,18 +163,19 @@ __global__ void __launch_bounds__(TPR)
     split_start<T, TPR, VPT>(ring, x, items, nchunks, ld, stall_row, order);
     asm volatile("griddepcontrol.wait;" ::: "memory");  // pass 1's partials are complete and visible
 
-    for (int64_t i = 0;; ++i) {
+    RingCursor rc;
+    for (int64_t i = 0;; ++i, rc.next(nbuf)) {
         const int64_t k = int64_t(blockIdx.x) + i * gridDim.x;
         if (k >= items) break;
         const int64_t item = order(k), r = item / nchunks;
-        const int s = int(i % nbuf);
+        const int s = rc.slot;
         // this thread's share of the row's partials (issued before the wait)
         MD pm{-INFINITY, 0.f};
         for (int64_t q = t; q < nchunks; q += TPR) {
             const float2 pv = partials[r * nchunks + q];
             pm = md_merge(pm, MD{pv.x, pv.y});
         }
-        int fail = !mbar_wait(ring.bar + s, uint32_t((i / nbuf) & 1), wait_ns);
+        int fail = !mbar_wait(ring.bar + s, rc.parity, wait_ns);
         const char* sb = ring.slot(s);
         float v[VPT][V];
 #pragma unroll

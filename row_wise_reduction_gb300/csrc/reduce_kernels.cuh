@@ -51,15 +51,16 @@ __global__ void __launch_bounds__(TPR)
     const int t = threadIdx.x;
     start_pipes<T, FULL, 1>(smem, p, x, M, N, ld, stall_row);
 
-    for (int64_t i = 0;; ++i) {
+    RingCursor rc;
+    for (int64_t i = 0;; ++i, rc.next(nbuf)) {
         const int64_t row = p.first + i * p.stride;
         if (row >= M) break;
-        const int s = int(i % nbuf);
+        const int s = rc.slot;
         const T* xr = x + row * ld;
         const RowSpan sp = row_span<T, FULL>(xr, N);
         const bool has_ex = !FULL && t < sp.head + sp.tail;
         float acc = has_ex ? E::load(xr + span_extra_col(sp, t, V)) : Op::kIdentity;
-        int fail = !mbar_wait(p.ring.bar + s, uint32_t((i / nbuf) & 1), wait_ns);
+        int fail = !mbar_wait(p.ring.bar + s, rc.parity, wait_ns);
         const char* sb = p.ring.slot(s);
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {

@@ -186,6 +186,20 @@ struct RowRing {
     __device__ __forceinline__ char* slot(int s) const { return buf + size_t(s) * row_bytes; }
 };
 
+// Ring slot and phase parity of iteration i (i % nbuf and (i / nbuf) & 1),
+// advanced one iteration at a time: the loops over rows would otherwise pay a
+// 64-bit division by the run-time ring depth per row and thread.
+struct RingCursor {
+    int slot = 0;
+    uint32_t parity = 0;
+    __device__ __forceinline__ void next(int nbuf) {
+        if (++slot == nbuf) {
+            slot = 0;
+            parity ^= 1u;
+        }
+    }
+};
+
 // Bytes of dynamic shared memory before the row buffers: the mbarriers of all
 // row groups' rings (ROWS * nbuf <= 32), padded.
 constexpr uint32_t kRingHeader = 256;

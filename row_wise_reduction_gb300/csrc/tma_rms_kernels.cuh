@@ -123,12 +123,13 @@ __global__ void __launch_bounds__(TPR * ROWS)
     const bool has_ex = !FULL && t < sp.head + sp.tail;
     const int ecol = has_ex ? span_extra_col(sp, t, V) : 0;
 
-    for (int64_t i = 0;; ++i) {
-        const int s = int(i % nbuf);
+    RingCursor rc;
+    for (int64_t i = 0;; ++i, rc.next(nbuf)) {
+        const int s = rc.slot;
         int64_t row;
         int fail = 0;
         if (dynamic) {
-            row = dyn_row(p, cs, g, i, wait_ns, fail);
+            row = dyn_row(p, cs, g, rc, wait_ns, fail);
             if (row < 0) {  // the end of the work (a failed wait goes on to the reduction below)
                 dyn_finish(f, cs, wait_ns);
                 return;
@@ -143,7 +144,7 @@ __global__ void __launch_bounds__(TPR * ROWS)
             ex = E::load(x + off + ecol);
             if constexpr (RES) ex = E::round(ex + E::load(res + off + ecol));
         }
-        if (!dynamic) fail = !mbar_wait(p.ring.bar + s, uint32_t((i / nbuf) & 1), wait_ns);
+        if (!dynamic) fail = !mbar_wait(p.ring.bar + s, rc.parity, wait_ns);
         const char* sbuf = p.ring.slot(s);
 
         float v[VPT][V];

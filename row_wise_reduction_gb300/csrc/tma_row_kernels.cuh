@@ -328,16 +328,16 @@ __device__ __forceinline__ DynFeed dyn_start(char* smem, const GroupPipe& p, Clc
     return f;
 }
 
-// Consumer side, iteration i: wait for the slot and read its row; -1: the
+// Consumer side, iteration i (at cursor rc): wait for the slot and read its row; -1: the
 // work has ended (every thread of the group sees it: an end mark completes its
 // slot's phase when it is written). A wait that gave up sets `fail` and hands
 // back the slot's row as written, so the thread goes on to the group's first
 // reduction, whose barrier tells the whole group to stop.
-__device__ __forceinline__ int64_t dyn_row(const GroupPipe& p, const ClcShared& cs, int g, int64_t i,
+__device__ __forceinline__ int64_t dyn_row(const GroupPipe& p, const ClcShared& cs, int g, const RingCursor& rc,
                                            unsigned long long wait_ns, int& fail) {
-    const int nbuf = p.ring.nbuf, s = int(i % nbuf);
-    fail = !mbar_wait(p.ring.bar + s, uint32_t((i / nbuf) & 1), wait_ns);
-    const int64_t row = cs.slot_row[g * nbuf + s];
+    const int s = rc.slot;
+    fail = !mbar_wait(p.ring.bar + s, rc.parity, wait_ns);
+    const int64_t row = cs.slot_row[g * p.ring.nbuf + s];
     return fail && row < 0 ? 0 : row;
 }
 
@@ -384,17 +384,18 @@ __global__ void __launch_bounds__(TPR * ROWS)
     const int64_t step = CAUSAL ? p.stride % cm.period : 0;
     const int64_t ring_step = CAUSAL ? (int64_t(nbuf) * step) % cm.period : 0;
 
-    for (int64_t i = 0;; ++i) {
+    RingCursor rc;
+    for (int64_t i = 0;; ++i, rc.next(nbuf)) {
         const int64_t row = p.first + i * p.stride;
         if (row >= M) break;
-        const int s = int(i % nbuf);
+        const int s = rc.slot;
         const T* xr = x + row * ld;
         const RowSpan sp = row_span<T, FULL>(xr, N);
         // unaligned head / tail elements: plain loads, in flight during the wait
         const bool has_ex = !FULL && t < sp.head + sp.tail;
         const int ecol = has_ex ? span_extra_col(sp, t, V) : 0;
         float ex = has_ex ? E::load(xr + ecol) : -INFINITY;
-        int fail = !mbar_wait(p.ring.bar + s, uint32_t((i / nbuf) & 1), wait_ns);
+        int fail = !mbar_wait(p.ring.bar + s, rc.parity, wait_ns);
         const char* sb = p.ring.slot(s);
         const int kept = CAUSAL ? cm.kept_at(rm, N) : N;
 
@@ -543,13 +544,14 @@ __global__ void __launch_bounds__(TPR * ROWS)
     const bool has_ex = !FULL && t < sp.head + sp.tail;
     const int ecol = has_ex ? span_extra_col(sp, t, V) : 0;
 
-    for (int64_t i = 0;; ++i) {
+    RingCursor rc;
+    for (int64_t i = 0;; ++i, rc.next(nbuf)) {
         const int64_t row = p.first + i * p.stride;
         if (row >= M) break;
-        const int s = int(i % nbuf);
+        const int s = rc.slot;
         const T* xr = x + row * ld;
         float ex = has_ex ? E::load(xr + ecol) : 0.f;
-        int fail = !mbar_wait(p.ring.bar + s, uint32_t((i / nbuf) & 1), wait_ns);
+        int fail = !mbar_wait(p.ring.bar + s, rc.parity, wait_ns);
         const char* sbuf = p.ring.slot(s);
 
         // elementwise arithmetic on packed fp32 pairs
