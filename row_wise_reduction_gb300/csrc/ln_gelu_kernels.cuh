@@ -25,25 +25,37 @@ __device__ __forceinline__ float gelu_tanh_approx(float z) {
     return z * rcp_approx(1.f + ex2_approx(a));
 }
 
-// Exact GELU ["Triton Kernel 实现练习" §3.4]: 0.5 z (1 + erf(z / sqrt(2))).
-// erfc by Abramowitz & Stegun, Handbook of Mathematical Functions, 7.1.26
-// (Hastings' approximation): for x >= 0, erfc(x) = t (a1 + t (a2 + t (a3 + t (a4
-// + t a5)))) e^{-x^2} + eps, t = 1 / (1 + p x), |eps| <= 1.5e-7. With u = |z| /
-// sqrt(2) and q = erfc(u): 1 + erf(z / sqrt(2)) is 2 - q for z >= 0 and q for z
-// < 0, so the negative side needs no cancelling sum; the output error is at most
-// 0.5 |z| 1.5e-7 plus fp32 rounding (a general-purpose erf costs several times
-// as many instructions, and this kernel is bound by issue).
+// Exact GELU ["Triton Kernel 实现练习" §3.4]: z Phi(z), Phi(z) = 0.5 (1 + erf(z /
+// sqrt(2))). Evaluated in the shape of the tanh form above, Phi(z) ~ 1 / (1 +
+// exp(-P(z))), with P an odd polynomial of degree 13 instead of 3: c_k are the
+// minimax fit of the GELU's absolute error over |z| <= 8 (printed by
+// row_wise_reduction_gb300/gelu_erf_fit.py; P increasing beyond, so the limits
+// z -> +-inf are those of GELU). The fit is within 7e-8 of z Phi(z); the fp32
+// evaluation adds the same kind of rounding as the tanh form (its exp2
+// argument |z| (2.3 + 0.105 z^2) carries a relative error of ~2^-24). One exp2
+// and one reciprocal per value, like the tanh form: an erfc approximation needs
+// a reciprocal and an exponential as well and a longer polynomial, and these
+// kernels are bound by issue when they take the exact form.
+// exp(-P(z)) = 2^(z q(z^2)), q_k = -log2(e) c_k.
+struct GeluErfFit {
+    static constexpr double c0 = 1.595768432225e+00, c1 = 7.266856705396e-02, c2 = -6.626000741970e-05,
+                            c3 = -1.104803108419e-04, c4 = 7.938218056236e-06, c5 = -2.668927628528e-07,
+                            c6 = 3.611231485973e-09;
+    static constexpr float q0 = float(-kLog2e * c0), q1 = float(-kLog2e * c1), q2 = float(-kLog2e * c2),
+                           q3 = float(-kLog2e * c3), q4 = float(-kLog2e * c4), q5 = float(-kLog2e * c5),
+                           q6 = float(-kLog2e * c6);
+};
+
 __device__ __forceinline__ float gelu_erf(float z) {
-    constexpr float p = 0.3275911f, a1 = 0.254829592f, a2 = -0.284496736f, a3 = 1.421413741f,
-                    a4 = -1.453152027f, a5 = 1.061405429f;
-    const float u = fabsf(z) * 0.70710678118654752f;
-    const float t = rcp_approx(fmaf(p, u, 1.f));
-    float poly = fmaf(t, a5, a4);
-    poly = fmaf(t, poly, a3);
-    poly = fmaf(t, poly, a2);
-    poly = fmaf(t, poly, a1);
-    const float q = poly * t * ex2_approx(-(u * u) * kLog2eF);
-    return z >= 0.f ? z * fmaf(-0.5f, q, 1.f) : 0.5f * z * q;
+    using F = GeluErfFit;
+    const float z2 = z * z;
+    float q = fmaf(z2, F::q6, F::q5);
+    q = fmaf(z2, q, F::q4);
+    q = fmaf(z2, q, F::q3);
+    q = fmaf(z2, q, F::q2);
+    q = fmaf(z2, q, F::q1);
+    q = fmaf(z2, q, F::q0);
+    return z * rcp_approx(1.f + ex2_approx(q * z));
 }
 
 // The GELU of the fused kernels: exact (ERF) or the tanh approximation.
@@ -64,23 +76,17 @@ __device__ __forceinline__ float2 gelu_tanh_approx2(float2 z) {
 }
 
 __device__ __forceinline__ float2 gelu_erf2(float2 z) {
-    // the same evaluation as gelu_erf with the constants folded: t = 1 / (1 +
-    // (p / sqrt 2) |z|), h = (q / 2) from coefficients a_i / 2, and e^{-u^2} =
-    // 2^{z^2 (-log2(e) / 2)}, so neither u nor the factor 1/2 costs an instruction
-    constexpr float ps = float(0.3275911 * 0.70710678118654752), b1 = float(0.5 * 0.254829592),
-                    b2 = float(0.5 * -0.284496736), b3 = float(0.5 * 1.421413741), b4 = float(0.5 * -1.453152027),
-                    b5 = float(0.5 * 1.061405429), ce = float(-0.5 * kLog2e);
-    const float2 d = f2_fma(f2(ps), make_float2(fabsf(z.x), fabsf(z.y)), f2(1.f));
-    const float2 t = make_float2(rcp_approx(d.x), rcp_approx(d.y));
-    float2 poly = f2_fma(t, f2(b5), f2(b4));
-    poly = f2_fma(t, poly, f2(b3));
-    poly = f2_fma(t, poly, f2(b2));
-    poly = f2_fma(t, poly, f2(b1));
-    const float2 g = f2_mul(f2_mul(z, z), f2(ce));
-    const float2 h = f2_mul(f2_mul(poly, t), make_float2(ex2_approx(g.x), ex2_approx(g.y)));  // erfc(u) / 2
-    const float2 zh = f2_mul(z, h);
-    const float2 pos = f2_fma(zh, f2(-1.f), z);  // z (1 - q/2)
-    return make_float2(z.x >= 0.f ? pos.x : zh.x, z.y >= 0.f ? pos.y : zh.y);
+    using F = GeluErfFit;
+    const float2 z2 = f2_mul(z, z);
+    float2 q = f2_fma(z2, f2(F::q6), f2(F::q5));
+    q = f2_fma(z2, q, f2(F::q4));
+    q = f2_fma(z2, q, f2(F::q3));
+    q = f2_fma(z2, q, f2(F::q2));
+    q = f2_fma(z2, q, f2(F::q1));
+    q = f2_fma(z2, q, f2(F::q0));
+    const float2 a = f2_mul(q, z);
+    const float2 d = f2_add(make_float2(ex2_approx(a.x), ex2_approx(a.y)), f2(1.f));
+    return f2_mul(z, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
 }
 
 template <bool ERF>

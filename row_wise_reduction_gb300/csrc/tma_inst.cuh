@@ -107,9 +107,9 @@ TmaSoftmaxLaunch softmax_tma_table(int block_index, int vpt_index, bool full) {
 // registers per thread and these kernels spill).
 template <typename T, int P, int V, int R, bool F, bool ERF>
 constexpr TmaLnGeluKernel ln_gelu_entry() {
-    // 5 groups of 128 x 8 for the tanh form only: the exact form's extra
-    // registers spill at 640 threads (443.6 us with 4 groups, 462.5 with 5,
-    // bf16 65536 x 8192)
+    // 5 groups of 128 x 8 for the tanh form only: the exact form's longer
+    // polynomial spills at 640 threads (bf16 65536 x 8192: 381.6 us with 4
+    // groups, 400.2 with 5)
     if constexpr (R == 1 || (P * R <= 512 && R != 5) || (P == 128 && V == 8 && R == 5 && !ERF) ||
                   (P == 128 && V == 4 && R == 5 && !ERF) || (P == 64 && V == 8 && R == 10 && !ERF))
         return TmaLnGeluKernel{launch_ln_gelu_tma_rows<T, P, V, R, F, ERF>, ctas_ln_gelu_tma_rows<T, P, V, R, F, ERF>};
