@@ -64,6 +64,11 @@
  *                                 (each row group a fixed share) or dynamic (default: work units
  *                                 taken with cluster launch control)
  *   ROWOPS_UNIT_ROWS=<n>          dynamic schedule: rows per row group in one work unit (default 1)
+ *   ROWOPS_BWD_PARTIALS=tmem|registers  LayerNorm+GELU backward on full rows: the per-column dw, db
+ *                                 partials in tensor memory (default where a 512-thread CTA of
+ *                                 two row groups of 256 threads, or four of 128, covers a row
+ *                                 with at most 32 columns a thread) or in registers (one row
+ *                                 group of up to 1024 threads per CTA)
  *   ROWOPS_WAIT_LIMIT_NS=<ns>     limit of every device-side wait (default 2 s)
  *   ROWOPS_TEST_STALL_ROW=<row>   test hook for the timeout path: the wait that concerns this
  *                                 row is made to run out (the row pipeline's bulk copy of it is

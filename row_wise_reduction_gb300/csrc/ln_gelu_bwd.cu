@@ -16,6 +16,7 @@
 #include "rowops_launch.h"
 #include "tma_inst.cuh"
 #include "tma_rms_kernels.cuh"
+#include "tmem.cuh"
 
 namespace rowops {
 
@@ -84,6 +85,26 @@ __device__ __forceinline__ float2 gelu_tanh_grad2(float2 z) {
     const float2 sg = make_float2(rcp_approx(e1.x), rcp_approx(e1.y));
     e = f2_mul(f2_mul(e, sg), sg);
     return f2_fma(e, f2_mul(f2_fma(f2(d1), z2, f2(d0)), z), sg);
+}
+
+// -gelu_tanh_grad of two values, with fewer instructions: n = -s comes from
+// the reciprocal of -(1 + e), and s (1 - s) = -(n + n^2) is one fused
+// multiply-add with an exact product, so
+//   -g'(z) = n + (n + n^2) (2 z du/dz).
+// Below z ~ -10 e overflows to +inf and n = -0: -g' = -0, with no clamp (no
+// inf * 0 arises). For large z, 1 + e carries the rounding of 1 (2^-24
+// absolute), which the small 1 - s takes in relative terms: the slope is then
+// off by at most ~1.2e-6 relative (z ~ 4, where e reaches 2^-24; the clamped
+// form above is exact there up to the approximate exp2 and reciprocal).
+__device__ __forceinline__ float2 gelu_tanh_grad2_neg(float2 z) {
+    constexpr float c0 = float(-2.0 * 0.79788456 * kLog2e);
+    constexpr float c1 = float(-2.0 * 0.79788456 * 0.044715 * kLog2e);
+    constexpr float d0 = float(2.0 * 0.79788456), d1 = float(2.0 * 3.0 * 0.79788456 * 0.044715);
+    const float2 z2 = f2_mul(z, z);
+    const float2 a = f2_mul(f2_fma(f2(c1), z2, f2(c0)), z);
+    const float2 nd = f2_fma(make_float2(ex2_approx(a.x), ex2_approx(a.y)), f2(-1.f), f2(-1.f));
+    const float2 n = make_float2(rcp_approx(nd.x), rcp_approx(nd.y));
+    return f2_fma(f2_fma(n, n, n), f2_mul(f2_fma(f2(d1), z2, f2(d0)), z), n);
 }
 
 // Full rows on a row pipeline of four stages, one row group (TPR threads) per
@@ -375,6 +396,201 @@ __global__ void __launch_bounds__(TPR)
     }
 }
 
+// TMEM columns of the TMEM-partials kernel: 2 VPT V per warp (the dw and db
+// partials of its threads' columns), warps w and w + 4 in the same lane
+// quarter, rounded up to a power of two >= 32 (the allocation unit).
+template <typename T, int TPR, int VPT, int ROWS>
+__host__ __device__ constexpr uint32_t bwd_tmem_cols() {
+    const uint32_t need = uint32_t(TPR * ROWS / 128) * 2u * uint32_t(VPT * Elem<T>::kVec);
+    uint32_t c = 32;
+    while (c < need) c <<= 1;
+    return c;
+}
+
+// Full rows, ROWS row groups of TPR threads per CTA, each group one row at a
+// time with three group reductions per row (as ln_gelu_bwd_tma_kernel), and
+// the dw, db partials of each thread's columns kept in tensor memory (TMEM)
+// across the CTA's rows instead of in registers. Registers then hold one row
+// (x and dy, later xh and dxh) and no partials, so a CTA of 512 threads runs
+// two or four independent row groups: while one group waits at a reduction's
+// barrier, the others compute, where the register-partial kernels have one
+// group of 512 threads per SM and idle during each of its reductions. Per row
+// and vector of a thread, the partials of its V columns come in with one TMEM
+// load issued before that vector's arithmetic, and go back with one store.
+// Each group's partials go to their own slot of `part` (blockIdx.x * ROWS + g).
+// Every thread reaches the final CTA barrier (a group whose wait gave up
+// leaves its row loop, it does not return), after which warp 0 frees TMEM.
+template <typename T, int TPR, int VPT, int ROWS>
+__global__ void __launch_bounds__(TPR * ROWS, 1)
+    ln_gelu_bwd_tmem_kernel(const T* x, const T* dy, const T* w, const T* b, float eps, T* dx, float* part,
+                            int64_t M, int N, int64_t ld, int nbuf, unsigned* err, unsigned long long wait_ns,
+                            int64_t stall_row) {
+    using E = Elem<T>;
+    constexpr int V = E::kVec, H = V / 4, P = V / 2, NE = VPT * V;
+    constexpr uint32_t kCols = bwd_tmem_cols<T, TPR, VPT, ROWS>();
+    static_assert(TPR % 128 == 0, "a row group spans the four TMEM lane quarters");
+    static_assert(kCols <= 256, "at most half of TMEM, so two CTAs on one SM never wait for each other");
+    extern __shared__ __align__(128) char smem[];
+    __shared__ float red_a[ROWS][TPR / 32];
+    __shared__ __align__(16) float2 red_b[ROWS][TPR / 32];
+    __shared__ __align__(16) float2 red_c[ROWS][TPR / 32];
+    __shared__ uint32_t tmem_base;
+    const GroupPipe p = make_group<TPR, ROWS>(smem, N, E::kBytes, nbuf, 1, 2);
+    const int g = threadIdx.x / TPR, t = threadIdx.x % TPR, warp = threadIdx.x >> 5;
+    char* affine = smem + kRingHeader + size_t(ROWS) * nbuf * p.ring.row_bytes;
+    const float4* sw4 = reinterpret_cast<const float4*>(affine);
+    const float4* sb4 = sw4 + VPT * H * TPR;
+    const T* const src[2] = {x, dy};
+    if (warp == 0) tmem_alloc(&tmem_base, kCols);
+    start_rows<T, true, ROWS, 2>(smem, p, src, M, N, ld, stall_row);
+    stage_affine_thread_major<T, TPR, VPT>(w, b, 0, N / V, reinterpret_cast<float4*>(affine),
+                                           reinterpret_cast<float4*>(affine) + VPT * H * TPR);
+    tmem_fence_before();
+    __syncthreads();
+    tmem_fence_after();
+    // this thread's lane and its 2 NE columns: per vector j, the dw then the db
+    // partials of the vector's V columns
+    const uint32_t tm = tmem_base + ((32u * uint32_t(warp & 3)) << 16) + uint32_t(warp >> 2) * (2u * NE);
+    {
+        float zero[2 * V];
+#pragma unroll
+        for (int e = 0; e < 2 * V; ++e) zero[e] = 0.f;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) tmem_st<2 * V>(tm + 2u * V * j, zero);
+        tmem_wait_st();
+    }
+    const uint32_t gstride = p.ring.row_bytes / 2;  // the dy row's place in a slot
+    const float fN = float(N);
+    bool ok = true;
+    RingCursor rc;
+    for (int64_t i = 0;; ++i, rc.next(nbuf)) {
+        const int64_t row = p.first + i * p.stride;
+        if (row >= M) break;
+        const int s = rc.slot;
+        int fail = !mbar_wait(p.ring.bar + s, rc.parity, wait_ns);
+        const char* sbuf = p.ring.slot(s);
+        float2 v[VPT][P], gd[VPT][P];  // x then xh; dy then dxh
+        float2 s2 = f2(0.f);
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int k = t + j * TPR;
+            float xv[V], gv[V];
+            E::unpack(lds16(sbuf + size_t(k) * 16), xv);
+            E::unpack(lds16(sbuf + gstride + size_t(k) * 16), gv);
+#pragma unroll
+            for (int q = 0; q < P; ++q) {
+                v[j][q] = make_float2(xv[2 * q], xv[2 * q + 1]);
+                gd[j][q] = make_float2(gv[2 * q], gv[2 * q + 1]);
+                s2 = f2_add(s2, v[j][q]);
+            }
+        }
+        const float sum = row_reduce<TPR>(s2.x + s2.y, red_a[g], p.bar_id, OpSum(), fail);
+        if (fail) {
+            abandon(p, i, M, err, wait_ns);
+            ok = false;
+            break;
+        }
+        refill_rows<T, true, 2>(p, s, row, src, M, N, ld, stall_row);
+        // statistics as in the forward: variance of the centred row with the
+        // residual correction of the fp32 mean
+        const float mean = sum / fN;
+        float2 q2 = f2(0.f), r2 = f2(0.f);
+#pragma unroll
+        for (int j = 0; j < VPT; ++j)
+#pragma unroll
+            for (int q = 0; q < P; ++q) {
+                v[j][q] = f2_add(v[j][q], f2(-mean));
+                q2 = f2_fma(v[j][q], v[j][q], q2);
+                r2 = f2_add(r2, v[j][q]);
+            }
+        float qs = q2.x + q2.y, rs = r2.x + r2.y;
+        row_reduce_sum2_packed<TPR>(qs, rs, red_b[g], p.bar_id, fail);
+        const float delta = rs / fN;
+        const float rstd = rsqrtf(fmaxf(qs / fN - delta * delta, 0.f) + eps);
+        const float shift = -delta * rstd;
+        // xh into v, -dxh into gd; the sums of -dxh and -dxh xh; the partials,
+        // negated (from -dz = dy (-g'), gelu_tanh_grad2_neg: every sign flip is
+        // exact, so dx and the sums are those of the positive form)
+        float2 a1 = f2(0.f), a2 = f2(0.f);
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            float acc[2 * V];
+            tmem_ld<2 * V>(tm + 2u * V * j, acc);
+            float2 dz[P];
+#pragma unroll
+            for (int h = 0; h < H; ++h) {
+                const float4 ww = sw4[(j * H + h) * TPR + t];
+                const float4 bb = sb4[(j * H + h) * TPR + t];
+                const float2 wv[2] = {make_float2(ww.x, ww.y), make_float2(ww.z, ww.w)};
+                const float2 bv[2] = {make_float2(bb.x, bb.y), make_float2(bb.z, bb.w)};
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int q = 2 * h + c;
+                    const float2 xhv = f2_fma(v[j][q], f2(rstd), f2(shift));
+                    dz[q] = f2_mul(gd[j][q], gelu_tanh_grad2_neg(f2_fma(xhv, wv[c], bv[c])));
+                    const float2 d = f2_mul(dz[q], wv[c]);
+                    a1 = f2_add(a1, d);
+                    a2 = f2_fma(d, xhv, a2);
+                    v[j][q] = xhv;
+                    gd[j][q] = d;
+                }
+            }
+            tmem_wait_ld(acc);
+#pragma unroll
+            for (int q = 0; q < P; ++q) {
+                const float2 aw = f2_fma(dz[q], v[j][q], make_float2(acc[2 * q], acc[2 * q + 1]));
+                const float2 ab = f2_add(dz[q], make_float2(acc[V + 2 * q], acc[V + 2 * q + 1]));
+                acc[2 * q] = aw.x;
+                acc[2 * q + 1] = aw.y;
+                acc[V + 2 * q] = ab.x;
+                acc[V + 2 * q + 1] = ab.y;
+            }
+            tmem_st<2 * V>(tm + 2u * V * j, acc);
+        }
+        float s1 = a1.x + a1.y, s2b = a2.x + a2.y;  // -sum dxh, -sum dxh xh
+        row_reduce_sum2_packed<TPR>(s1, s2b, red_c[g], p.bar_id, fail);
+        // dx = rstd (dxh - mean(dxh) - xh mean(dxh xh)) from the negated terms
+        const float nm1 = rstd * (s1 / fN), nm2 = rstd * (s2b / fN);
+        T* dxr = dx + row * ld;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            float o[V];
+#pragma unroll
+            for (int q = 0; q < P; ++q) {
+                const float2 r = f2_fma(f2(-rstd), gd[j][q], f2_fma(v[j][q], f2(nm2), f2(nm1)));
+                o[2 * q] = r.x;
+                o[2 * q + 1] = r.y;
+            }
+            st_stream16(dxr + size_t(t + j * TPR) * V, E::pack(o));
+        }
+        tmem_wait_st();  // the next row's loads read these columns
+    }
+    if (ok) {  // this group's partials: part[blockIdx.x * ROWS + g] holds dw then db, N floats each
+        float* pw = part + (size_t(blockIdx.x) * ROWS + g) * 2 * N;
+        float* pb = pw + N;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            float acc[2 * V];
+            tmem_ld<2 * V>(tm + 2u * V * j, acc);
+            tmem_wait_ld(acc);
+            const int c0 = (t + j * TPR) * V;
+#pragma unroll
+            for (int h = 0; h < H; ++h) {  // the partials were kept negated
+                *reinterpret_cast<float4*>(pw + c0 + 4 * h) =
+                    make_float4(-acc[4 * h], -acc[4 * h + 1], -acc[4 * h + 2], -acc[4 * h + 3]);
+                *reinterpret_cast<float4*>(pb + c0 + 4 * h) =
+                    make_float4(-acc[V + 4 * h], -acc[V + 4 * h + 1], -acc[V + 4 * h + 2], -acc[V + 4 * h + 3]);
+            }
+        }
+    }
+    tmem_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tmem_fence_after();
+        tmem_free(tmem_base, kCols);
+    }
+}
+
 // Any layout: one CTA per row (grid-stride), element-wise coalesced passes.
 // Pass 1: shifted sums around x0 (mean, variance without cancellation); pass 2:
 // dz, dxh, the row sums of dxh and dxh xh, and this CTA's dw, db partials (the
@@ -506,6 +722,44 @@ cudaError_t launch_bwd_pipe(const void* x, const void* dy, const void* w, const 
     return cudaGetLastError();
 }
 
+template <typename T, int TPR, int VPT, int ROWS>
+cudaError_t launch_bwd_tmem(const void* x, const void* dy, const void* w, const void* b, float eps, void* dx,
+                            float* part, int64_t M, int64_t N, int64_t ld, int nbuf, int* grid_out,
+                            const LaunchCfg& cfg) {
+    auto kern = ln_gelu_bwd_tmem_kernel<T, TPR, VPT, ROWS>;
+    const size_t smem = kRingHeader + size_t(ROWS) * nbuf * 2 * ring_row_bytes(N, Elem<T>::kBytes) +
+                        tma_affine_bytes<T, TPR, VPT>();
+    cudaError_t e = allow_smem(reinterpret_cast<const void*>(kern), smem, cfg);
+    if (e != cudaSuccess) return e;
+    int grid = grid_for(reinterpret_cast<const void*>(kern), TPR * ROWS, smem, (M + ROWS - 1) / ROWS, cfg);
+    const int cap = bwd_max_partials(N) / ROWS;  // each group leaves its own partials
+    if (grid > cap) grid = cap;
+    *grid_out = grid * ROWS;
+    kern<<<grid, TPR * ROWS, smem, cfg.stream>>>(static_cast<const T*>(x), static_cast<const T*>(dy),
+                                                 static_cast<const T*>(w), static_cast<const T*>(b), eps,
+                                                 static_cast<T*>(dx), part, M, int(N), ld, nbuf, cfg.dev_error,
+                                                 cfg.wait_ns, cfg.stall_row);
+    return cudaGetLastError();
+}
+
+// TMEM-partials tiles: 512 threads per CTA as two groups of 256 or four of
+// 128, VPT in {1, 2, 4} with at most 32 columns per thread
+template <typename T, int TPR, int VPT>
+constexpr TmaBwdLaunch bwd_tmem_entry() {
+    if constexpr (VPT * Elem<T>::kVec > 32) return nullptr;
+    else return launch_bwd_tmem<T, TPR, VPT, 512 / TPR>;
+}
+
+template <typename T>
+TmaBwdLaunch bwd_tmem_table(int tpr, int vpt) {
+    static const TmaBwdLaunch t[2][3] = {
+        {bwd_tmem_entry<T, 128, 1>(), bwd_tmem_entry<T, 128, 2>(), bwd_tmem_entry<T, 128, 4>()},
+        {bwd_tmem_entry<T, 256, 1>(), bwd_tmem_entry<T, 256, 2>(), bwd_tmem_entry<T, 256, 4>()}};
+    const int i = tpr == 128 ? 0 : (tpr == 256 ? 1 : -1);
+    const int j = vpt == 1 ? 0 : (vpt == 2 ? 1 : (vpt == 4 ? 2 : -1));
+    return i < 0 || j < 0 ? nullptr : t[i][j];
+}
+
 // tiles of the row pipeline: TPR in {64, 128, 256, 512}, VPT in {1, 2, 3, 4} with
 // at most 16 columns per thread (the dw, db partials live in registers); TPR
 // 1024 with at most 8 columns per thread for the three-stage kernel (64
@@ -539,6 +793,8 @@ TmaBwdLaunch ln_gelu_bwd_tma_f32(int tpr_index, int vpt, bool pipe) {
 TmaBwdLaunch ln_gelu_bwd_tma_bf16(int tpr_index, int vpt, bool pipe) {
     return bwd_tma_table<bf16_t>(tpr_index, vpt, pipe);
 }
+TmaBwdLaunch ln_gelu_bwd_tmem_f32(int tpr, int vpt) { return bwd_tmem_table<float>(tpr, vpt); }
+TmaBwdLaunch ln_gelu_bwd_tmem_bf16(int tpr, int vpt) { return bwd_tmem_table<bf16_t>(tpr, vpt); }
 BwdLaunch ln_gelu_bwd_looped_f32() { return launch_bwd_looped<float>; }
 BwdLaunch ln_gelu_bwd_looped_bf16() { return launch_bwd_looped<bf16_t>; }
 

@@ -177,6 +177,34 @@ __device__ __forceinline__ void row_reduce_sum2(float& a, float& b, float* red, 
     }
 }
 
+// row_reduce_sum2 on packed pairs: one add per butterfly step and per warp
+// partial for both sums (the additions in the order of two separate sums), and
+// two warps' partials per 16-byte load. `red`: 16-byte aligned, TPR / 32 pairs.
+// (The row pipelines of the forward kernels keep the scalar form: at their
+// register caps the packed one spilled and ran slower.)
+template <int TPR>
+__device__ __forceinline__ void row_reduce_sum2_packed(float& a, float& b, float2* red, int bar_id, int& fail) {
+    float2 v = make_float2(a, b);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v = f2_add(v, make_float2(__shfl_xor_sync(0xffffffffu, v.x, o), __shfl_xor_sync(0xffffffffu, v.y, o)));
+    constexpr int W = TPR / 32;
+    static_assert(W % 2 == 0, "pairs of warps");
+    const int w = (threadIdx.x % TPR) >> 5;
+    if ((threadIdx.x & 31) == 0) red[w] = v;
+    fail = group_bar_or(bar_id, TPR, fail);
+    const float4* r4 = reinterpret_cast<const float4*>(red);
+    float4 q = r4[0];
+    v = f2_add(make_float2(q.x, q.y), make_float2(q.z, q.w));
+#pragma unroll
+    for (int i = 1; i < W / 2; ++i) {
+        q = r4[i];
+        v = f2_add(f2_add(v, make_float2(q.x, q.y)), make_float2(q.z, q.w));
+    }
+    a = v.x;
+    b = v.y;
+}
+
 // The ring: nbuf buffers of `row_bytes` (a multiple of 128) after the barriers.
 struct RowRing {
     uint64_t* bar;    // nbuf mbarriers

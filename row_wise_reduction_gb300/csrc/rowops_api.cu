@@ -38,6 +38,7 @@ struct Tuning {
     long long stall_row = -1; // test hook (see include/rowops.h)
     int sched = 0;            // full-row pipelines: 0 automatic, 1 static, 2 dynamic (cluster launch control)
     int unit_rows = 0;        // dynamic schedule: rows per group in a work unit (0: automatic)
+    int bwd = 0;              // LayerNorm+GELU backward partials: 0 automatic, 1 registers, 2 tensor memory
 };
 
 // The whole value as a decimal integer, else `dflt` (unset, empty or not a number).
@@ -77,6 +78,7 @@ Tuning read_tuning() {
         else if (is("TEST_STALL_ROW")) t.stall_row = std::strtoll(v, nullptr, 10);
         else if (is("UNIT_ROWS")) t.unit_rows = int(parse_int(v, 0));
         else if (is("SCHED")) t.sched = !std::strcmp(v, "static") ? 1 : (!std::strcmp(v, "dynamic") ? 2 : 0);
+        else if (is("BWD_PARTIALS")) t.bwd = !std::strcmp(v, "registers") ? 1 : (!std::strcmp(v, "tmem") ? 2 : 0);
         else if (is("ONLINE"))
             t.online = !std::strcmp(v, "two_pass") ? 1
                      : !std::strcmp(v, "single_read") ? 2
@@ -830,7 +832,25 @@ rowops_status_t rowops_layernorm_gelu_backward(const void* x, const void* dy, co
     const int64_t vec = 16 / es;
     const bool full = (tn.family == Family::Auto || tn.family == Family::Tma) && N % vec == 0 &&
                       rows_aligned(x, dx, ld, es) && aligned(dy, 16);
-    if (full) {
+    if (full && tn.bwd != 1 && !tn.tpr && !tn.vpt) {
+        // the dw, db partials in tensor memory: 512 threads as two row groups of
+        // 256 (or four of 128) with TPR * VPT = N / vec, two ring slots per group,
+        // every group's partials within the workspace's partial slots
+        const int64_t nvec = N / vec;
+        for (int tpr : {256, 128}) {
+            if (launched || nvec % tpr) continue;
+            const int vpt = int(nvec / tpr);
+            const TmaBwdLaunch f = dtype == ROWOPS_F32 ? ln_gelu_bwd_tmem_f32(tpr, vpt) : ln_gelu_bwd_tmem_bf16(tpr, vpt);
+            const int rows = 512 / tpr;
+            const int nbuf = tn.ring >= 2 && tn.ring <= 4 ? tn.ring : 2;
+            const size_t smem = size_t(kTmaRingHeader) + size_t(rows) * nbuf * 2 * tma_row_bytes(N, es) +
+                                size_t(2) * vpt * tpr * vec * 4 + 1024;
+            if (!f || smem > size_t(cfg.max_smem_optin) || bwd_max_partials(N) / rows < cfg.num_sms) continue;
+            e = f(x, dy, w, b, eps, dx, part, M, N, ld, nbuf, &grid, cfg);
+            launched = true;
+        }
+    }
+    if (full && !launched) {
         const int64_t nvec = N / vec;
         // a tile: TPR * VPT = N / vec; the three-stage pipeline where 4..6 ring
         // slots fit (it holds three rows and wants one more in flight; or

@@ -191,6 +191,11 @@ using BwdLaunch = cudaError_t (*)(const void* x, const void* dy, const void* w, 
 // the one-row-at-a-time kernel (three reductions per row, nbuf >= 2)
 TmaBwdLaunch ln_gelu_bwd_tma_f32(int tpr_index, int vpt, bool pipe);
 TmaBwdLaunch ln_gelu_bwd_tma_bf16(int tpr_index, int vpt, bool pipe);
+// Full rows with the dw, db partials in tensor memory: 512-thread CTAs of
+// 512 / tpr row groups (tpr 128 or 256), vpt in {1, 2, 4}; nullptr otherwise.
+// grid_out: the partial slots written (CTAs x row groups).
+TmaBwdLaunch ln_gelu_bwd_tmem_f32(int tpr, int vpt);
+TmaBwdLaunch ln_gelu_bwd_tmem_bf16(int tpr, int vpt);
 BwdLaunch ln_gelu_bwd_looped_f32();
 BwdLaunch ln_gelu_bwd_looped_bf16();
 cudaError_t ln_gelu_bwd_reduce(const float* part, int P, int64_t N, float* dw, float* db, const LaunchCfg& cfg);

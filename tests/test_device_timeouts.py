@@ -146,13 +146,17 @@ def test_causal_softmax_wait_times_out(oracle, monkeypatch):
     C.assert_softmax_close(C.to_f64(y), oracle.softmax_causal(gu.rows_f32(x), 4096, 0), "bf16")
 
 
-def test_layernorm_gelu_backward_wait_times_out(oracle, monkeypatch):
+@pytest.mark.parametrize("partials", ["tmem", "registers"])
+def test_layernorm_gelu_backward_wait_times_out(oracle, monkeypatch, partials):
     """The backward's ring (x and dy rows in one slot) gives up on the stalled
-    row, records the timeout, and the next call is correct."""
+    row, records the timeout, and the next call is correct; with the partials
+    in tensor memory the group that gave up leaves its row loop and the CTA
+    still frees its tensor memory (the next call allocates it again)."""
     wl = workloads.Workload("timeout_ln_bwd", "layernorm_gelu_backward", "bf16", 1200, 8192, seed=4, affine=True,
                             grad=True)
     inp = gu.make_x(wl)
     monkeypatch.setenv("ROWOPS_KERNEL", "tma")
+    monkeypatch.setenv("ROWOPS_BWD_PARTIALS", partials)
     monkeypatch.setenv("ROWOPS_WAIT_LIMIT_NS", LIMIT_NS)
     monkeypatch.setenv("ROWOPS_TEST_STALL_ROW", "400")
     rowops_layernorm_gelu_backward(inp["x"], inp["dy"], inp["w"], inp["b"], wl.eps)
