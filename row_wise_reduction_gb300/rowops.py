@@ -190,6 +190,37 @@ def _stream(stream, device=None) -> int:
     return int(stream)
 
 
+_DTYPE_CODES = {torch.float32: ROWOPS_F32, torch.bfloat16: ROWOPS_BF16}
+
+
+def _xy(x: torch.Tensor, y: Optional[torch.Tensor]):
+    """_rows(x) and _out_like(x, y) in one pass over the tensors' properties,
+    for the entry points whose small calls are bound by host time: returns
+    (M, N, ld, y, dtype code, device index)."""
+    sh = x.shape
+    if len(sh) != 2:
+        raise ValueError("x must be 2-D (M, N)")
+    dev = x.get_device()
+    if dev < 0:
+        raise ValueError("x must be a CUDA tensor")
+    M, N = sh
+    st = x.stride()
+    if N > 0 and st[1] != 1:
+        raise ValueError("x must have unit column stride")
+    dt = x.dtype
+    code = _DTYPE_CODES.get(dt)
+    if code is None:
+        raise TypeError(f"rowops supports float32 and bfloat16, not {dt}")
+    if y is None:
+        y = torch.empty_strided(sh, st, dtype=dt, device=x.device)
+    else:
+        if y.dtype is not dt or y.get_device() != dev or y.shape != sh:
+            raise ValueError("y must match x in shape, dtype and device")
+        if M > 1 and y.stride() != st:
+            raise ValueError("x and y must share the row stride")
+    return M, N, (st[0] if M > 1 else max(N, st[0])), y, code, dev
+
+
 def _check(fn: str, status: int):
     if status != 0:
         raise RowopsError(fn, status)
@@ -197,10 +228,11 @@ def _check(fn: str, status: int):
 
 def rowops_softmax(x: torch.Tensor, y: Optional[torch.Tensor] = None, *, stream=None) -> torch.Tensor:
     """Stable softmax of every row of ``x`` (M, N) into ``y`` (may be ``x``)."""
-    M, N, ld = _rows(x, "x")
-    y = _out_like(x, y)
-    st = library().rowops_softmax(x.data_ptr(), y.data_ptr(), M, N, ld, _dtype_code(x), _stream(stream))
-    _check("rowops_softmax", st)
+    M, N, ld, y, code, dev = _xy(x, y)
+    st = (_lib or library()).rowops_softmax(x.data_ptr(), y.data_ptr(), M, N, ld, code,
+                                            _current_raw_stream(dev) if stream is None else _stream(stream))
+    if st:
+        raise RowopsError("rowops_softmax", st)
     return y
 
 
@@ -275,16 +307,12 @@ def rowops_layernorm_gelu(
     stream=None,
 ) -> torch.Tensor:
     """Fused LayerNorm -> affine -> tanh-GELU of every row of ``x``."""
-    M, N, ld = _rows(x, "x")
-    y = _out_like(x, y)
-    for name, v in (("w", w), ("b", b)):
-        if v is not None:
-            if v.dtype != x.dtype or v.device != x.device or v.numel() != N or not v.is_contiguous():
-                raise ValueError(f"{name} must be a contiguous CUDA tensor of N entries with x's dtype")
-    st = library().rowops_layernorm_gelu(
-        x.data_ptr(), y.data_ptr(), w.data_ptr() if w is not None else None,
-        b.data_ptr() if b is not None else None, float(eps), M, N, ld, _dtype_code(x), _stream(stream))
-    _check("rowops_layernorm_gelu", st)
+    M, N, ld, y, code, dev = _xy(x, y)
+    st = (_lib or library()).rowops_layernorm_gelu(
+        x.data_ptr(), y.data_ptr(), _affine(w, x, N, dev, "w"), _affine(b, x, N, dev, "b"), float(eps), M, N, ld,
+        code, _current_raw_stream(dev) if stream is None else _stream(stream))
+    if st:
+        raise RowopsError("rowops_layernorm_gelu", st)
     return y
 
 
@@ -298,16 +326,12 @@ def rowops_layernorm_gelu_erf(
     stream=None,
 ) -> torch.Tensor:
     """Fused LayerNorm -> affine -> exact (erf) GELU of every row of ``x``."""
-    M, N, ld = _rows(x, "x")
-    y = _out_like(x, y)
-    for name, v in (("w", w), ("b", b)):
-        if v is not None:
-            if v.dtype != x.dtype or v.device != x.device or v.numel() != N or not v.is_contiguous():
-                raise ValueError(f"{name} must be a contiguous CUDA tensor of N entries with x's dtype")
-    st = library().rowops_layernorm_gelu_erf(
-        x.data_ptr(), y.data_ptr(), w.data_ptr() if w is not None else None,
-        b.data_ptr() if b is not None else None, float(eps), M, N, ld, _dtype_code(x), _stream(stream))
-    _check("rowops_layernorm_gelu_erf", st)
+    M, N, ld, y, code, dev = _xy(x, y)
+    st = (_lib or library()).rowops_layernorm_gelu_erf(
+        x.data_ptr(), y.data_ptr(), _affine(w, x, N, dev, "w"), _affine(b, x, N, dev, "b"), float(eps), M, N, ld,
+        code, _current_raw_stream(dev) if stream is None else _stream(stream))
+    if st:
+        raise RowopsError("rowops_layernorm_gelu_erf", st)
     return y
 
 
@@ -384,6 +408,15 @@ def rowops_bias_residual_gelu(
         y.data_ptr(), M, N, ld, 0 if approximate == "none" else 1, _dtype_code(x), _stream(stream))
     _check("rowops_bias_residual_gelu", st)
     return y
+
+
+def _affine(v: Optional[torch.Tensor], x: torch.Tensor, N: int, dev: int, name: str):
+    """Device pointer of an optional per-column vector (w, b) of x's dtype."""
+    if v is None:
+        return None
+    if v.dtype is not x.dtype or v.get_device() != dev or v.numel() != N or not v.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor of N entries with x's dtype")
+    return v.data_ptr()
 
 
 def _weight(w: Optional[torch.Tensor], x: torch.Tensor, N: int, name: str = "w"):
