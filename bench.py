@@ -19,8 +19,9 @@ same run: the same copy pipeline with no kernel.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl rowops|reference]
 
-Under torchrun every rank runs its own copy of the workload (weak scaling,
-no collective on the data path); rank 0 prints one JSON line.
+Under torchrun rank r takes the contiguous row block [r M, (r + 1) M) of each
+workload's (world M)-row problem (weak scaling, no collective on the data
+path); rank 0 prints one JSON line.
 ``--impl reference`` times the double-precision CPU oracle on host cores on a
 bounded sample of the same workload (rank 0 only).
 """
@@ -524,9 +525,17 @@ def run_reference(args):
     return 0
 
 
-def config_block():
+def parallelism(world: int) -> str:
+    if world == 1:
+        return "one GPU"
+    return (f"row blocks: rank r takes rows [r M, (r + 1) M) of each workload's {world} M-row problem; "
+            "no collective on the data path")
+
+
+def config_block(world: int = 1):
     return {
         "workload": " + ".join(STEP),
+        "parallelism": parallelism(world),
         "per_step_bytes": {n: alg_bytes(workloads.WORKLOADS[n]) for n in STEP},
         "l2": "no flush: every input (268 MB, 268 MB, 1074 MB) is larger than the 129 MB L2",
         "bytes_basis": "algorithmic: each input element read once, each output element written once (+ w, b)",
@@ -766,7 +775,8 @@ def run_rowops(args):
         wls = {n: wl.with_shape(M=max(1, int(wl.M * args.rows_scale))) for n, wl in wls.items()}
     inputs, outputs, ws = {}, {}, {}
     for n, wl in wls.items():
-        inputs[n] = workloads.make_inputs(wl, dev)
+        # rank r: the contiguous row block [r M, (r + 1) M) of a (world M)-row problem
+        inputs[n] = workloads.make_inputs(wl, dev, block=rank)
         outputs[n] = torch.empty_like(inputs[n]["x"])
         if wl.op == "online_softmax":
             nb = ro.rowops_online_softmax_workspace_bytes(wl.M, wl.N, workloads.torch_dtype(wl.dtype))
@@ -988,8 +998,8 @@ def run_rowops(args):
         "dtype": STEP_DTYPE if not subset else "f32 arithmetic; I/O " + ", ".join(
             sorted({wl.dtype for wl in wls.values()})),
         "data": "synthetic",
-        "config": config_block() if args.rows_scale == 1.0 and not subset else
-        {"workload": " + ".join(f"{wl.name}[M={wl.M}]" for wl in wls.values())},
+        "config": config_block(world) if args.rows_scale == 1.0 and not subset else
+        {"workload": " + ".join(f"{wl.name}[M={wl.M}]" for wl in wls.values()), "parallelism": parallelism(world)},
         "roofline": roof,
         "step_frac": fractions(total_bytes / secs_max / 1e9, peak, copy_gbs),
         "breakdown": per_op,

@@ -113,6 +113,7 @@ def make_inputs(
     device: str | torch.device = "cpu",
     ld: Optional[int] = None,
     row_ids: Optional[torch.Tensor] = None,
+    block: int = 0,
 ) -> Dict[str, torch.Tensor]:
     """Draw the inputs of ``wl`` on ``device``.
 
@@ -125,6 +126,10 @@ def make_inputs(
     column N-1 shows up in the result. ``row_ids`` (M integers) gives the row
     index each generated row stands for in the causal mask pattern, so that a
     small sample can carry the mask of rows spread over a large workload.
+    ``block`` b > 0: rows [b M, (b + 1) M) of a larger problem made of such
+    blocks (one per rank of a multi-GPU run): its own draw (seed + 7919 b) and,
+    for causal workloads, the mask of those global row indices; w and b are
+    the problem's, shared by every block.
     """
     device = torch.device(device)
     M, N = wl.M, wl.N
@@ -132,7 +137,7 @@ def make_inputs(
     if ld < N:
         raise ValueError("ld must be >= N")
     dt = torch_dtype(wl.dtype)
-    g = _gen(device, wl.seed)
+    g = _gen(device, wl.seed + 7919 * block)
     x = torch.randn((M, N), generator=g, device=device, dtype=torch.float32)
     if wl.x_std != 1.0:
         x.mul_(wl.x_std)
@@ -142,7 +147,8 @@ def make_inputs(
         del hit
     if wl.causal:
         cols = torch.arange(N, device=device).unsqueeze(0)
-        ids = torch.arange(M, device=device) if row_ids is None else torch.as_tensor(row_ids, device=device)
+        ids = (torch.arange(M, device=device) + int(block) * M if row_ids is None
+               else torch.as_tensor(row_ids, device=device))
         keep = (ids % N).unsqueeze(1)
         x.masked_fill_(cols > keep, float("-inf"))
     storage = torch.full((M, ld), float("nan"), device=device, dtype=dt)
@@ -158,7 +164,7 @@ def make_inputs(
         out["b"] = b.to(dt)
     for key, on, sd in (("residual", wl.residual, 300), ("dy", wl.grad, 400)):
         if on:
-            gr = _gen(device, wl.seed + sd)
+            gr = _gen(device, wl.seed + sd + 7919 * block)
             r = torch.randn((M, N), generator=gr, device=device, dtype=torch.float32)
             rs = torch.full((M, ld), float("nan"), device=device, dtype=dt)
             rs[:, :N] = r.to(dt)

@@ -125,3 +125,24 @@ def test_step_dtype_label_names_both_io_types():
     assert io == {"bf16", "f32"}
     assert bench.STEP_DTYPE.startswith("f32 arithmetic")
     assert "bf16" in bench.STEP_DTYPE and "f32 I/O" in bench.STEP_DTYPE
+
+
+def test_row_blocks_of_a_larger_problem():
+    """Under torchrun rank r draws rows [r M, (r + 1) M) of the workload's
+    (world M)-row problem: its own data, the causal mask of its global row
+    indices, the problem's w and b."""
+    import torch
+    from row_wise_reduction_gb300 import workloads
+
+    wl = workloads.Workload("blk", "softmax_causal", "f32", 6, 4, seed=3, causal=True)
+    b0 = workloads.make_inputs(wl, "cpu", block=0)["x"]
+    b1 = workloads.make_inputs(wl, "cpu", block=1)["x"]
+    kept = lambda x: (~torch.isinf(x)).sum(dim=1).tolist()  # noqa: E731
+    assert kept(b0) == [1, 2, 3, 4, 1, 2]  # rows 0..5: r mod 4 + 1 columns
+    assert kept(b1) == [3, 4, 1, 2, 3, 4]  # rows 6..11
+    assert not torch.equal(b0[:, 0], b1[:, 0])
+    aff = workloads.Workload("blk_ln", "layernorm_gelu", "f32", 3, 8, seed=5, affine=True)
+    a0, a1 = workloads.make_inputs(aff, "cpu", block=0), workloads.make_inputs(aff, "cpu", block=2)
+    assert torch.equal(a0["w"], a1["w"]) and torch.equal(a0["b"], a1["b"])
+    assert not torch.equal(a0["x"], a1["x"])
+    assert torch.equal(workloads.make_inputs(aff, "cpu")["x"], a0["x"])  # block 0 is the one-GPU workload
