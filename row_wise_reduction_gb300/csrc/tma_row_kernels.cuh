@@ -621,8 +621,8 @@ __global__ void __launch_bounds__(TPR * ROWS)
                 float o[V];
 #pragma unroll
                 for (int h = 0; h < H; ++h) {
-                    const float4 ww = sw4[(j * H + h) * TPR + t];
-                    const float4 bb = sb4[(j * H + h) * TPR + t];
+                    const float4 ww = ERF ? ldsf4(sw4 + (j * H + h) * TPR + t) : sw4[(j * H + h) * TPR + t];
+                    const float4 bb = ERF ? ldsf4(sb4 + (j * H + h) * TPR + t) : sb4[(j * H + h) * TPR + t];
                     const float2 z0 = f2_fma(f2_fma(v[j][2 * h], f2(rstd), f2(shift)), make_float2(ww.x, ww.y),
                                              make_float2(bb.x, bb.y));
                     const float2 z1 = f2_fma(f2_fma(v[j][2 * h + 1], f2(rstd), f2(shift)), make_float2(ww.z, ww.w),
