@@ -286,7 +286,8 @@ def host_cost_c(timeout_s: float = 120.0):
 def host_cost_python(dev, batch: int = 256, batches: int = 20):
     """The same measurement through the Python binding: wall time of issuing
     rowops_softmax(x, y) on fp32 1024 x 768, per call (each batch timed while
-    issuing, then synchronised)."""
+    issuing, then synchronised); the median over the batches, so that a batch
+    disturbed by other host work does not set the figure."""
     import row_wise_reduction_gb300 as ro
 
     x = torch.randn(1024, 768, device=dev)
@@ -294,14 +295,14 @@ def host_cost_python(dev, batch: int = 256, batches: int = 20):
     for _ in range(200):
         ro.rowops_softmax(x, y)
     torch.cuda.synchronize()
-    spent = 0.0
+    per_call = []
     for _ in range(batches):
         t0 = time.perf_counter()
         for _ in range(batch):
             ro.rowops_softmax(x, y)
-        spent += time.perf_counter() - t0
+        per_call.append((time.perf_counter() - t0) / batch * 1e6)
         torch.cuda.synchronize()
-    return spent / (batch * batches) * 1e6
+    return statistics.median(per_call)
 
 
 # ---------------------------------------------------------------------------
