@@ -308,7 +308,8 @@ rowops_status_t rowops_layernorm_gelu_erf(const void* x, void* y, const void* w,
  *   dx = rstd (dxh - mean(dxh) - xh mean(dxh xh))
  *   dw = sum over the rows of dz xh,   db = sum over the rows of dz
  * The row statistics are recomputed from x. dx in `dtype`; dw, db in fp32
- * (sums over M rows), deterministic (per-CTA partials added in a fixed order).
+ * (sums over M rows), deterministic (partial sums per CTA, or per row group of a
+ * CTA, added in a fixed order).
  *
  *   x, dy    device pointers to M rows of `ld` elements (inputs).
  *   w, b     as for rowops_layernorm_gelu (NULL: 1, 0).
@@ -318,7 +319,7 @@ rowops_status_t rowops_layernorm_gelu_erf(const void* x, void* y, const void* w,
  *            rowops_layernorm_gelu_backward_workspace_bytes(M, N, dtype) bytes
  *            (overwritten), apart from dw and db; calls sharing it must be
  *            ordered on one stream. It holds 2 N floats for each of at most
- *            clamp(2^22 / N, 152, 4096) CTAs (32 MiB for N <= 27594).
+ *            clamp(2^22 / N, 152, 4096) partial slots (32 MiB for N <= 27594).
  * M == 0 writes zeros to dw and db.
  */
 size_t rowops_layernorm_gelu_backward_workspace_bytes(int64_t M, int64_t N, rowops_dtype_t dtype);
