@@ -677,7 +677,7 @@ cudaError_t launch_bwd_tma(const void* x, const void* dy, const void* w, const v
                         tma_affine_bytes<T, TPR, VPT>();
     cudaError_t e = allow_smem(reinterpret_cast<const void*>(kern), smem, cfg);
     if (e != cudaSuccess) return e;
-    int grid = grid_for(reinterpret_cast<const void*>(kern), TPR, smem, M, cfg);
+    int grid = cap_ctas(grid_for(reinterpret_cast<const void*>(kern), TPR, smem, M, cfg), 4, cfg);  // as before
     if (grid > bwd_max_partials(N)) grid = bwd_max_partials(N);
     *grid_out = grid;
     kern<<<grid, TPR, smem, cfg.stream>>>(static_cast<const T*>(x), static_cast<const T*>(dy),
@@ -712,7 +712,7 @@ cudaError_t launch_bwd_pipe(const void* x, const void* dy, const void* w, const 
                         tma_affine_bytes<T, TPR, VPT>();
     cudaError_t e = allow_smem(reinterpret_cast<const void*>(kern), smem, cfg);
     if (e != cudaSuccess) return e;
-    int grid = grid_for(reinterpret_cast<const void*>(kern), TPR, smem, M, cfg);
+    int grid = cap_ctas(grid_for(reinterpret_cast<const void*>(kern), TPR, smem, M, cfg), 4, cfg);  // as before
     if (grid > bwd_max_partials(N)) grid = bwd_max_partials(N);
     *grid_out = grid;
     kern<<<grid, TPR, smem, cfg.stream>>>(static_cast<const T*>(x), static_cast<const T*>(dy),

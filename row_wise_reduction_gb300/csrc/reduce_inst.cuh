@@ -16,7 +16,8 @@ cudaError_t launch_reduce_tma(const void* x, float* out, int64_t M, int64_t N, i
     const size_t smem = tma_ring_bytes<T>(N, nbuf);
     cudaError_t e = allow_smem(reinterpret_cast<const void*>(kern), smem, cfg);
     if (e != cudaSuccess) return e;
-    const int grid = grid_for(reinterpret_cast<const void*>(kern), TPR, smem, M, cfg);
+    // 4 CTAs per SM: bf16 65536 x 8192 row sums 149.5 us against 152.4 with the occupancy limit
+    const int grid = cap_ctas(grid_for(reinterpret_cast<const void*>(kern), TPR, smem, M, cfg), 4, cfg);
     kern<<<grid, TPR, smem, cfg.stream>>>(static_cast<const T*>(x), out, M, int(N), ld, nbuf, cfg.dev_error,
                                           cfg.wait_ns, cfg.stall_row);
     return cudaGetLastError();

@@ -45,6 +45,17 @@ struct LaunchCfg {
 // limit (or the forced CTAs per SM) times the SM count, capped at `items`.
 int grid_for(const void* func, int block, size_t smem, int64_t items, const LaunchCfg& cfg);
 
+// A persistent grid capped at `cap` CTAs per SM unless ROWOPS_CTAS_PER_SM
+// chose the count. The one-group row-pipeline kernels hold more CTAs per SM
+// than they run best with (a constant named-barrier id leaves the registers
+// and shared memory as the only limits); their launchers pass the measured
+// best count.
+inline int cap_ctas(int grid, int cap, const LaunchCfg& cfg) {
+    if (cfg.ctas_per_sm != 0) return grid;
+    const int64_t c = int64_t(cap) * cfg.num_sms;
+    return grid > c ? int(c) : grid;
+}
+
 // CTAs of `func` one SM can hold at once (occupancy API, cached per device).
 int ctas_per_sm(const void* func, int block, size_t smem, const LaunchCfg& cfg);
 

@@ -21,7 +21,10 @@ cudaError_t launch_softmax_tma_mask(const void* x, void* y, int64_t M, int64_t N
     // carveout (the row sum's pipeline ran slower with it and keeps the default)
     cudaError_t e = allow_smem(reinterpret_cast<const void*>(kern), smem, cfg, true);
     if (e != cudaSuccess) return e;
-    const int grid = grid_for(reinterpret_cast<const void*>(kern), TPR, smem, M, cfg);
+    // CTAs per SM, side by side on bf16 32768 x 4096: the causal softmax 68.2 us with 5 (75.0 with
+    // 4, 69.8 with 6); the softmax inside the bench step 89.7 us with 4 (91.5 with 3, although 3
+    // is faster alone: 88.7 against 92.0; 93.5 alone with the 10 that fit)
+    const int grid = cap_ctas(grid_for(reinterpret_cast<const void*>(kern), TPR, smem, M, cfg), CAUSAL ? 5 : 4, cfg);
     kern<<<grid, TPR, smem, cfg.stream>>>(static_cast<const T*>(x), static_cast<T*>(y), M, int(N), ld, nbuf,
                                           cfg.dev_error, cfg.wait_ns, cfg.stall_row, cm);
     return cudaGetLastError();
@@ -55,6 +58,7 @@ cudaError_t launch_ln_gelu_tma_rows(const void* x, void* y, const void* w, const
     cudaError_t e = allow_smem(reinterpret_cast<const void*>(kern), smem, cfg);
     if (e != cudaSuccess) return e;
     int grid = grid_for(reinterpret_cast<const void*>(kern), TPR * ROWS, smem, (M + ROWS - 1) / ROWS, cfg);
+    if (ROWS == 1) grid = cap_ctas(grid, 4, cfg);  // one group per CTA: as before the constant barrier id
     if (!FULL) {  // whole phase classes: every class needs a CTA, and they share the grid evenly
         const int period = row_phase_period(ld * int64_t(Elem<T>::kBytes));
         grid = grid >= period ? grid - grid % period : period;

@@ -24,6 +24,7 @@ cudaError_t launch_rms_tma(const void* x, const void* r, void* y, void* ro, cons
     const int unit = FULL ? cfg.unit_rows : 0;  // 0: static schedule
     int grid = unit ? dyn_grid(M, ROWS, unit)
                     : grid_for(reinterpret_cast<const void*>(kern), TPR * ROWS, smem, (M + ROWS - 1) / ROWS, cfg);
+    if (!unit && ROWS == 1) grid = cap_ctas(grid, 4, cfg);  // one group per CTA: as before the constant barrier id
     if (!FULL) {  // whole phase classes: every class needs a CTA, and they share the grid evenly
         const int period = row_phase_period(ld * int64_t(Elem<T>::kBytes));
         grid = grid >= period ? grid - grid % period : period;

@@ -62,7 +62,7 @@ __device__ __forceinline__ GroupPipe make_group(char* smem, int64_t N, int es, i
     p.cls = cls;
     p.first = cls + int64_t(period) * (int64_t(local) * ROWS + g);
     p.stride = int64_t(period) * ctas * ROWS;
-    p.bar_id = 1 + g;
+    p.bar_id = ROWS == 1 ? 1 : 1 + g;  // a constant id lets a one-group CTA reserve two barriers, not 16
     p.producer = (threadIdx.x % TPR) == 0;
     return p;
 }
