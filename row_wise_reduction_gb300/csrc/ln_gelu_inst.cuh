@@ -19,6 +19,17 @@ cudaError_t launch_ln_gelu_reg(const void* x, void* y, const void* w, const void
     if (e != cudaSuccess) return e;
     const int64_t groups = (M + ROWS - 1) / ROWS;
     const int grid = grid_for(reinterpret_cast<const void*>(kern), BLOCK, smem, groups, cfg);
+    const auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };  // NULL passes
+    if constexpr (ALIGNED) {
+        // at most two row groups per CTA: w, b straight from global memory, no staging
+        if (2 * int64_t(grid) >= groups && a16(w) && a16(b)) {
+            auto direct = ln_gelu_reg_kernel<T, TPR, VPT, BLOCK, true, ERF, true>;
+            direct<<<grid, BLOCK, 0, cfg.stream>>>(static_cast<const T*>(x), static_cast<T*>(y),
+                                                   static_cast<const T*>(w), static_cast<const T*>(b), eps, M,
+                                                   int(N), ld);
+            return cudaGetLastError();
+        }
+    }
     kern<<<grid, BLOCK, smem, cfg.stream>>>(static_cast<const T*>(x), static_cast<T*>(y),
                                             static_cast<const T*>(w), static_cast<const T*>(b), eps,
                                             M, int(N), ld);

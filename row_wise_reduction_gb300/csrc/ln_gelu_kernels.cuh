@@ -123,7 +123,12 @@ __device__ __forceinline__ void stage_affine_pairs(const T* w, const T* b, int N
 
 // ALIGNED: every row starts on a 16-byte boundary (head = 0), so the columns of
 // a vector are a multiple of 4 and w, b are read from shared memory as float4.
-template <typename T, int TPR, int VPT, int BLOCK, bool ALIGNED, bool ERF = false>
+// DIRECT (ALIGNED only; w, b 16-byte aligned or absent): no staging; each
+// thread loads the w, b vectors of its columns from global memory where it
+// uses them (L1 hits after the SM's first row group). For launches where a CTA
+// takes one or two row groups, the staging (a shared-memory fill and a CTA
+// barrier before the first load of x) is a large share of its critical path.
+template <typename T, int TPR, int VPT, int BLOCK, bool ALIGNED, bool ERF = false, bool DIRECT = false>
 __global__ void __launch_bounds__(BLOCK)
     ln_gelu_reg_kernel(const T* x, T* y, const T* w, const T* b, float eps, int64_t M, int N,
                        int64_t ld) {
@@ -131,6 +136,7 @@ __global__ void __launch_bounds__(BLOCK)
     constexpr int V = E::kVec;
     constexpr int ROWS = BLOCK / TPR;
     static_assert(BLOCK % TPR == 0 && TPR >= 16, "row group must be at least a half warp");
+    static_assert(ALIGNED || !DIRECT, "direct w, b loads need 16-byte vectors of columns");
     extern __shared__ float4 smem_affine[];
     float* sw = reinterpret_cast<float*>(smem_affine);
     float* sb = sw + affine_pad(N);
@@ -138,9 +144,11 @@ __global__ void __launch_bounds__(BLOCK)
     __shared__ float red_b[BLOCK / 32 > 0 ? 2 * BLOCK / 32 : 2];
 
     const float2* swb = reinterpret_cast<const float2*>(smem_affine);
-    if constexpr (ALIGNED) stage_affine(w, b, N, sw, sb);
-    else stage_affine_pairs(w, b, N, reinterpret_cast<float2*>(smem_affine));
-    __syncthreads();
+    if constexpr (!DIRECT) {
+        if constexpr (ALIGNED) stage_affine(w, b, N, sw, sb);
+        else stage_affine_pairs(w, b, N, reinterpret_cast<float2*>(smem_affine));
+        __syncthreads();
+    }
 
     const int t = threadIdx.x % TPR;
     const int slot = threadIdx.x / TPR;
@@ -216,7 +224,23 @@ __global__ void __launch_bounds__(BLOCK)
             if (k < geo.nvec) {
                 const int c0 = geo.head + int(k) * V;
                 float o[V];
-                if constexpr (ALIGNED) {
+                if constexpr (DIRECT) {
+                    float wf[V], bf[V];
+                    if (w) {
+                        E::unpack(__ldg(reinterpret_cast<const uint4*>(w + c0)), wf);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < V; ++j) wf[j] = 1.f;
+                    }
+                    if (b) {
+                        E::unpack(__ldg(reinterpret_cast<const uint4*>(b + c0)), bf);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < V; ++j) bf[j] = 0.f;
+                    }
+#pragma unroll
+                    for (int j = 0; j < V; ++j) o[j] = gelu_of<ERF>(fmaf(fmaf(v[i][j], rstd, shift), wf[j], bf[j]));
+                } else if constexpr (ALIGNED) {
 #pragma unroll
                     for (int j = 0; j < V; j += 4) {
                         const float4 ww = *reinterpret_cast<const float4*>(sw + c0 + j);
@@ -237,7 +261,9 @@ __global__ void __launch_bounds__(BLOCK)
             }
         }
         if (has_ex) {
-            const float2 wb = ALIGNED ? make_float2(sw[ecol], sb[ecol]) : swb[affine_pair(ecol)];
+            const float2 wb = DIRECT    ? make_float2(w ? E::load(w + ecol) : 1.f, b ? E::load(b + ecol) : 0.f)
+                              : ALIGNED ? make_float2(sw[ecol], sb[ecol])
+                                        : swb[affine_pair(ecol)];
             E::store(yr + ecol, gelu_of<ERF>(fmaf(fmaf(ex, rstd, shift), wb.x, wb.y)));
         }
     }
