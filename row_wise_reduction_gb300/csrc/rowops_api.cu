@@ -1,5 +1,6 @@
 // C ABI of librowops.so: argument validation, kernel selection and launch.
 // The operations themselves are documented in include/rowops.h.
+#include <algorithm>
 #include <cstdlib>
 #include <cstring>
 #include <initializer_list>
@@ -355,13 +356,17 @@ bool choose_tma(const void* x, const void* y, int64_t N, int64_t ld, int es, con
 // Ring depth: two rows in flight per CTA by default (deeper rings measured no
 // faster on GB300: the several CTAs per SM already keep enough bytes in
 // flight), fewer if shared memory would not hold them next to `fixed` bytes.
-int ring_buffers(int64_t N, int es, size_t fixed, const Tuning& tn, const LaunchCfg& cfg) {
+// `min_slot`: a floor on the slot size (the whole tile, for kernels that keep
+// the vectors past a row's body zero in every slot).
+int ring_buffers(int64_t N, int es, size_t fixed, const Tuning& tn, const LaunchCfg& cfg, size_t min_slot = 0) {
     int nbuf = tn.ring > 0 ? tn.ring : 2;
     if (nbuf < 2) nbuf = 2;
     if (nbuf > 16) nbuf = 16;
     const size_t limit = size_t(cfg.max_smem_optin) - 1024;  // room for static reduction buffers
-    while (nbuf > 2 && tma_ring_smem(N, es, nbuf) + fixed > limit) --nbuf;
-    return tma_ring_smem(N, es, nbuf) + fixed <= limit ? nbuf : 0;
+    const size_t slot = std::max(tma_row_bytes(N, es), min_slot);
+    auto ring = [&](int nb) { return size_t(kTmaRingHeader) + size_t(nb) * slot; };
+    while (nbuf > 2 && ring(nbuf) + fixed > limit) --nbuf;
+    return ring(nbuf) + fixed <= limit ? nbuf : 0;
 }
 
 // Row groups per CTA for the LayerNorm+GELU row pipeline: the groups of a CTA
@@ -725,7 +730,8 @@ rowops_status_t ln_gelu_dispatch(const void* x, void* y, const void* w, const vo
     if (pipeline_pays(tn, M, N, es) &&
         choose_tma(x, y, N, ld, es, tn, {8, 4, 2, 3, 1}, &tc)) {
         const int tpr = kTmaBlocks[tc.block_index], vpt = kTmaVpts[tc.vpt_index];
-        const int nbuf = ring_buffers(N, es, tma_affine_smem(tpr, vpt, es, tc.full, N), tn, cfg);
+        const int nbuf = ring_buffers(N, es, tma_affine_smem(tpr, vpt, es, tc.full, N), tn, cfg,
+                                      tc.full ? 0 : size_t(tpr) * vpt * 16);
         if (nbuf > 0) {
             const TmaLnGeluLookup lookup = dtype == ROWOPS_F32 ? (erf ? ln_gelu_erf_tma_f32 : ln_gelu_tma_f32)
                                                                : (erf ? ln_gelu_erf_tma_bf16 : ln_gelu_tma_bf16);

@@ -46,7 +46,7 @@ cudaError_t launch_softmax_tma_causal(const void* x, void* y, int64_t M, int64_t
 // ROWS row groups per CTA share one staging of w, b; nbuf buffers per group.
 template <typename T, int TPR, int VPT, int ROWS, bool FULL, bool ERF = false>
 size_t ln_gelu_tma_smem(int64_t N, int nbuf) {
-    return kRingHeader + size_t(ROWS) * nbuf * ring_row_bytes(N, Elem<T>::kBytes) +
+    return kRingHeader + size_t(ROWS) * nbuf * ln_slot_bytes<T, TPR, VPT, FULL>(N) +
            affine_stage_bytes<T, TPR, VPT, FULL>();
 }
 

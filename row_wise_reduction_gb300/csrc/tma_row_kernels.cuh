@@ -46,12 +46,13 @@ struct GroupPipe {
 };
 
 // `period`: number of phase classes (1: every CTA takes every kind of row);
-// `streams`: rows of that many inputs share each ring slot.
+// `streams`: rows of that many inputs share each ring slot; `min_row_bytes`:
+// a floor on the slot size (a multiple of 128).
 template <int TPR, int ROWS>
 __device__ __forceinline__ GroupPipe make_group(char* smem, int64_t N, int es, int nbuf, int period = 1,
-                                                int streams = 1) {
+                                                int streams = 1, uint32_t min_row_bytes = 0) {
     const int g = threadIdx.x / TPR;
-    const uint32_t rb = uint32_t(streams) * ring_row_bytes(N, es);
+    const uint32_t rb = uint32_t(streams) * max(ring_row_bytes(N, es), min_row_bytes);
     GroupPipe p;
     p.ring = RowRing{reinterpret_cast<uint64_t*>(smem) + g * nbuf, smem + kRingHeader + size_t(g) * nbuf * rb, rb,
                      nbuf};
@@ -505,6 +506,15 @@ __host__ __device__ constexpr uint32_t affine_stage_bytes() {
     return tma_affine_bytes<T, TPR, VPT>() + (FULL ? 0u : kAffineExtraBytes);
 }
 
+// Ring slot of LayerNorm+GELU: general rows reserve the whole tile (TPR * VPT
+// vectors) so that the vectors past the body can stay zero in every slot.
+template <typename T, int TPR, int VPT, bool FULL>
+__host__ __device__ constexpr uint32_t ln_slot_bytes(int64_t N) {
+    return FULL ? ring_row_bytes(N, Elem<T>::kBytes)
+                : (ring_row_bytes(N, Elem<T>::kBytes) > uint32_t(TPR * VPT * 16) ? ring_row_bytes(N, Elem<T>::kBytes)
+                                                                                  : uint32_t(TPR * VPT * 16));
+}
+
 template <typename T, int TPR, int VPT, int ROWS, bool FULL, bool ERF = false>
 __global__ void __launch_bounds__(TPR * ROWS)
     ln_gelu_tma_kernel(const T* x, T* y, const T* w, const T* b, float eps, int64_t M, int N, int64_t ld,
@@ -516,7 +526,8 @@ __global__ void __launch_bounds__(TPR * ROWS)
     __shared__ float red_a[ROWS][TPR / 32];
     __shared__ float red_b[ROWS][2 * TPR / 32];
     const int period = FULL ? 1 : row_phase_period(ld * E::kBytes);
-    const GroupPipe p = make_group<TPR, ROWS>(smem, N, E::kBytes, nbuf, period);
+    const GroupPipe p =
+        make_group<TPR, ROWS>(smem, N, E::kBytes, nbuf, period, 1, ln_slot_bytes<T, TPR, VPT, FULL>(N));
     const int g = threadIdx.x / TPR, t = threadIdx.x % TPR;
     char* affine = smem + kRingHeader + size_t(ROWS) * nbuf * p.ring.row_bytes;
     float4* sw4 = reinterpret_cast<float4*>(affine);
@@ -539,6 +550,11 @@ __global__ void __launch_bounds__(TPR * ROWS)
             const int c = span_extra_col(sp, e, V);
             sxb[e] = make_float2(w ? E::load(w + c) : 1.f, b ? E::load(b + c) : 0.f);
         }
+        // the vectors past the body read as zeros in every slot: the copies
+        // (the body only) never write them, so the load pass needs no predicate
+        for (int s = 0; s < nbuf; ++s)
+            for (int k = sp.body + t; k < TPR * VPT; k += TPR)
+                *reinterpret_cast<uint4*>(p.ring.slot(s) + size_t(k) * 16) = make_uint4(0u, 0u, 0u, 0u);
     }
     __syncthreads();
     const bool has_ex = !FULL && t < sp.head + sp.tail;
@@ -559,14 +575,8 @@ __global__ void __launch_bounds__(TPR * ROWS)
         float2 s2 = make_float2(ex, 0.f);
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
-            const int k = t + j * TPR;
             float u[V];
-            if (FULL || k < sp.body) {
-                E::unpack(lds16(sbuf + size_t(k) * 16), u);
-            } else {
-#pragma unroll
-                for (int e = 0; e < V; ++e) u[e] = 0.f;
-            }
+            E::unpack(lds16(sbuf + size_t(t + j * TPR) * 16), u);
 #pragma unroll
             for (int e = 0; e < V / 2; ++e) {
                 v[j][e] = make_float2(u[2 * e], u[2 * e + 1]);
