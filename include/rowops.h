@@ -36,10 +36,15 @@
  * Benchmarking knobs (environment; unset = automatic). They are read at the
  * library's first call and kept for the process; rowops_reload_tuning()
  * reads them again (for code that changes them between calls, e.g. tests):
- *   ROWOPS_KERNEL=tma|reg|looped  kernel family: TMA-fed row pipeline, register-resident
- *                                 row groups, or the looped any-N kernels
- *   ROWOPS_FORCE_TPR=<16..1024>   threads per row (tma: 64..512); row-group split softmax:
- *                                 256 = two CTAs of 256 threads per SM (default one of 512)
+ *   ROWOPS_KERNEL=tma|reg|looped|flat  kernel family: TMA-fed row pipeline, register-resident
+ *                                 row groups, or the looped any-N kernels; flat: LayerNorm+GELU
+ *                                 by chunks of back-to-back rows (ld == N <= 256, x and y
+ *                                 16-byte aligned; the default there when N is not a whole
+ *                                 number of 16-byte vectors, N <= 128, or the batch is above
+ *                                 32 MiB), other operations as reg
+ *   ROWOPS_FORCE_TPR=<16..1024>   threads per row (tma: 64..512; flat: 8, 16, 32); row-group
+ *                                 split softmax: 256 = two CTAs of 256 threads per SM (default
+ *                                 one of 512)
  *   ROWOPS_FORCE_VPT=<n>          16-byte vectors per thread (reg: 1..4; tma: 1, 2, 3, 4, 8)
  *   ROWOPS_FORCE_LOOPED=1         same as ROWOPS_KERNEL=looped
  *   ROWOPS_RING_BUFFERS=<2..16>   rows in flight per row group of the row pipeline (chunks per
@@ -181,7 +186,7 @@ rowops_status_t rowops_row_max(const void* x, float* out, int64_t M, int64_t N, 
  * Synchronises `stream`, then reads and clears the library's device error word
  * on the current device. Kernels that wait on asynchronous copies (the TMA-fed
  * row pipeline behind rowops_softmax, rowops_layernorm_gelu and the RMSNorm
- * entry points) bound every
+ * entry points, and the chunked LayerNorm+GELU of short rows) bound every
  * wait; if one gives up, the kernel stops, records ROWOPS_ERR_TIMEOUT there,
  * and the outputs of that call are unspecified. Returns ROWOPS_OK,
  * ROWOPS_ERR_TIMEOUT, or ROWOPS_ERR_CUDA if a CUDA call fails.
@@ -283,7 +288,12 @@ rowops_status_t rowops_online_softmax_noalloc(const void* x, void* y, int64_t M,
  *   eps    added to the variance (the pages' default is 1e-5); must be >= 0 and finite.
  * Kernel choice as for rowops_softmax (row pipeline / registers / looped); w and
  * b are staged once per CTA as fp32 in shared memory, and the row pipeline runs
- * up to 8 rows per CTA over that one staging.
+ * up to 8 rows per CTA over that one staging. Short back-to-back rows (ld == N
+ * <= 256, x and y 16-byte aligned) whose length is not a whole number of
+ * 16-byte vectors (e.g. bf16 N = 127), or is at most 128, or whose batch is
+ * above 32 MiB, go by chunks of rows instead: whole chunks move between global
+ * and shared memory as bulk copies, and teams of lanes normalise the rows in
+ * shared memory (its bounded waits as above).
  */
 rowops_status_t rowops_layernorm_gelu(const void* x, void* y, const void* w, const void* b,
                                       float eps, int64_t M, int64_t N, int64_t ld,

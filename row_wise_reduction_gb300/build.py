@@ -45,6 +45,7 @@ SOURCES = [
     "tma_ln_gelu_erf_bf16.cu",
     "gelu.cu",
     "ln_gelu_bwd.cu",
+    "ln_gelu_flat.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

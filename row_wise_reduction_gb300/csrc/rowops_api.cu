@@ -23,7 +23,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 // Benchmarking knobs, read from the environment at the first call and again
 // on rowops_reload_tuning() (see include/rowops.h).
-enum class Family { Auto, Tma, Reg, Looped };
+enum class Family { Auto, Tma, Reg, Looped, Flat };
 struct Tuning {
     int tpr = 0;
     int vpt = 0;
@@ -91,6 +91,7 @@ Tuning read_tuning() {
         if (!std::strcmp(kernel, "tma")) t.family = Family::Tma;
         else if (!std::strcmp(kernel, "reg")) t.family = Family::Reg;
         else if (!std::strcmp(kernel, "looped")) t.family = Family::Looped;
+        else if (!std::strcmp(kernel, "flat")) t.family = Family::Flat;
     }
     return t;
 }
@@ -726,6 +727,20 @@ rowops_status_t ln_gelu_dispatch(const void* x, void* y, const void* w, const vo
     const Tuning tn = tuning();
     LaunchCfg cfg;
     if ((st = make_cfg(stream, tn, &cfg)) != ROWOPS_OK) return st;
+    // Short back-to-back rows by chunks of rows: those that are not whole
+    // 16-byte vectors, those of at most 128 columns, and batches past 32 MiB
+    // (where the row pipeline's per-row costs dominate). GB300, CUDA graphs,
+    // 65536 rows, against the default before: bf16 N = 127 11.8 us (13.2), 33
+    // 7.2 (13.0), 64 8.6 (12.5), 128 11.8 (12.6); fp32 N = 127 11.7 (13.9),
+    // 255 20.9 (23.1), 256 21.0 (76.0). Aligned bf16 N = 200 and 256 stay
+    // with the register rows (17.1 and 17.6 against 19.0 and 20.2).
+    const bool short_rows = ld == N && N <= kFlatMaxN && aligned(x, 16) && aligned(y, 16);
+    if (short_rows && (tn.family == Family::Flat ||
+                       (tn.family == Family::Auto &&
+                        ((N * es) % 16 != 0 || N <= 128 || pipeline_pays(tn, M, N, es))))) {
+        if (const LnGeluLaunch fl = ln_gelu_flat(es, erf, N, tn.tpr))
+            return finish(fl(x, y, w, b, eps, M, N, ld, cfg));
+    }
     TmaChoice tc;
     if (pipeline_pays(tn, M, N, es) &&
         choose_tma(x, y, N, ld, es, tn, {8, 4, 2, 3, 1}, &tc)) {

@@ -246,6 +246,11 @@ LnGeluLaunch ln_gelu_erf_reg_f32(int tpr_index, int vpt, bool aligned);
 LnGeluLaunch ln_gelu_erf_reg_bf16(int tpr_index, int vpt, bool aligned);
 LnGeluLaunch ln_gelu_erf_looped_f32();
 LnGeluLaunch ln_gelu_erf_looped_bf16();
+// short back-to-back rows (ld == N, N <= kFlatMaxN) by chunks of rows; es: 4
+// (fp32) or 2 (bf16); lanes per row 8, 16 or 32 (else automatic); nullptr when
+// N is too long for those lanes
+constexpr int64_t kFlatMaxN = 256;
+LnGeluLaunch ln_gelu_flat(int es, bool erf, int64_t N, int lanes);
 
 SplitLaunch split_softmax_f32();
 SplitLaunch split_softmax_bf16();

@@ -67,6 +67,24 @@ def test_layernorm_row_groups_wait_times_out(oracle, monkeypatch):
     C.assert_ln_gelu_close(C.to_f64(y), ref, "bf16")
 
 
+def test_layernorm_flat_chunks_wait_times_out(oracle, monkeypatch):
+    """The chunked kernel for short back-to-back rows: the copy of the chunk
+    holding row 1000 never completes its phase."""
+    wl = workloads.Workload("timeout_ln_flat", "layernorm_gelu", "bf16", 2001, 127, seed=6, affine=True)
+    inp = gu.make_x(wl)
+    monkeypatch.setenv("ROWOPS_KERNEL", "flat")
+    monkeypatch.setenv("ROWOPS_WAIT_LIMIT_NS", LIMIT_NS)
+    monkeypatch.setenv("ROWOPS_TEST_STALL_ROW", "1000")
+    rowops_layernorm_gelu(inp["x"], inp["w"], inp["b"], wl.eps)
+    assert rowops_device_status() == TIMEOUT
+    monkeypatch.delenv("ROWOPS_TEST_STALL_ROW")
+    y = rowops_layernorm_gelu(inp["x"], inp["w"], inp["b"], wl.eps)
+    assert rowops_device_status() == 0
+    ref = oracle.layernorm_gelu(gu.rows_f32(inp["x"]), inp["w"].float().cpu().numpy(),
+                                inp["b"].float().cpu().numpy(), wl.eps)
+    C.assert_ln_gelu_close(C.to_f64(y), ref, "bf16")
+
+
 @pytest.mark.parametrize("staging", ["smem", "l2", "groups"])
 def test_single_read_split_softmax_wait_times_out(oracle, monkeypatch, staging):
     wl = workloads.Workload("timeout_online", "online_softmax", "f32", 6, 1 << 20, seed=5)

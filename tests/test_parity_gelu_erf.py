@@ -45,6 +45,16 @@ def test_ln_gelu_erf_ragged(oracle, dtype, N):
     check_ln(oracle, edge(dtype, 23, N, seed=N))
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("N", [1, 33, 127, 200, 256])
+@pytest.mark.parametrize("M", [5, 1001])
+def test_ln_gelu_erf_flat_chunks(oracle, monkeypatch, dtype, N, M):
+    """The exact form of the kernel for short back-to-back rows by chunks of
+    rows (forced)."""
+    monkeypatch.setenv("ROWOPS_KERNEL", "flat")
+    check_ln(oracle, edge(dtype, M, N, seed=N + M))
+
+
 @pytest.mark.parametrize("env", [{"ROWOPS_KERNEL": "tma"}, {"ROWOPS_KERNEL": "reg"}, {"ROWOPS_KERNEL": "looped"},
                                  {"ROWOPS_KERNEL": "tma", "ROWOPS_ROWS_PER_CTA": "1"},
                                  {"ROWOPS_KERNEL": "tma", "ROWOPS_ROWS_PER_CTA": "4"}],

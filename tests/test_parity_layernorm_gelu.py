@@ -318,3 +318,52 @@ def test_ln_gelu_small_batches_take_register_rows(oracle, dtype, M, N):
     """Batches of at most 32 MiB go to the register-resident kernel by
     default; the result equals the row pipeline's within the tolerance."""
     check(oracle, edge(dtype, M, N, seed=M))
+
+
+FLAT_N = [1, 7, 32, 33, 64, 65, 100, 127, 128, 129, 200, 255, 256, 257]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("N", FLAT_N)
+@pytest.mark.parametrize("M", [1, 5, 1001])
+def test_ln_gelu_flat_chunks(oracle, monkeypatch, dtype, N, M):
+    """The kernel for short back-to-back rows by chunks of rows, forced (so
+    also on rows of whole 16-byte vectors): one row, fewer rows than a chunk,
+    and a last chunk whose bytes end off a 16-byte boundary (its final
+    elements moved with plain loads and stores); guard bands untouched. N =
+    257 is past the kernel's widths: the forced choice falls back to the
+    register rows."""
+    monkeypatch.setenv("ROWOPS_KERNEL", "flat")
+    check(oracle, edge(dtype, M, N, seed=N + M))
+    from row_wise_reduction_gb300 import rowops_device_status
+
+    assert rowops_device_status() == 0
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("ctas", ["1", "-1"])
+def test_ln_gelu_flat_many_chunks_per_cta(oracle, monkeypatch, dtype, ctas):
+    """One CTA per SM: every CTA takes many chunks through its two buffers,
+    each refilled once the bulk store of its previous chunk has read it; and
+    one CTA per chunk."""
+    monkeypatch.setenv("ROWOPS_CTAS_PER_SM", ctas)
+    check(oracle, edge(dtype, 20001, 127, seed=3))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_ln_gelu_flat_in_place_and_null_affine(oracle, dtype):
+    """Default choice on short unaligned back-to-back rows: in place, and with
+    NULL weight or bias."""
+    check(oracle, edge(dtype, 3001, 127), inplace=True)
+    check(oracle, edge(dtype, 301, 127, seed=2), use_w=False)
+    check(oracle, edge(dtype, 301, 127, seed=3), use_b=False)
+    check(oracle, edge(dtype, 301, 129, seed=4), use_w=False, use_b=False)
+
+
+@pytest.mark.parametrize("dtype,M,N", [("f32", 65536, 256), ("bf16", 5000, 64), ("f32", 3000, 128),
+                                       ("bf16", 65536, 127)])
+def test_ln_gelu_flat_default_choices(oracle, dtype, M, N):
+    """Shapes the chunked kernel takes by default: a batch above 32 MiB of
+    256-column fp32 rows, rows of at most 128 columns, and the 127-column bf16
+    tail at full size, each compared in full."""
+    check(oracle, edge(dtype, M, N, seed=M + N))
