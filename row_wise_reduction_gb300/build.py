@@ -1,7 +1,8 @@
 """Build librowops.so in-tree with nvcc for sm_103a.
 
 Compiles each translation unit under ``csrc/`` in parallel into ``_build/``
-and links them (static CUDA runtime) into ``librowops.so`` next to this file.
+and links them (static CUDA runtime) into ``librowops.so`` next to this file;
+with gcc, also the binding's small CPython call module ``_rowops_call``.
 Run ``python -m row_wise_reduction_gb300.build`` or call :func:`build`.
 """
 from __future__ import annotations
@@ -10,7 +11,9 @@ import os
 import shutil
 import subprocess
 import sys
+import sysconfig
 from concurrent.futures import ThreadPoolExecutor
+from typing import Optional
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
@@ -71,8 +74,32 @@ def _stale() -> bool:
     return any(os.path.getmtime(d) > t for d in _inputs() + [os.path.abspath(__file__)])
 
 
+PYCALL_SRC = os.path.join(CSRC, "pycall.c")
+PYCALL = os.path.join(PKG, "_rowops_call" + (sysconfig.get_config_var("EXT_SUFFIX") or ".so"))
+
+
+def build_pycall(force: bool = False) -> Optional[str]:
+    """Compile the binding's CPython call module (gcc, Python headers); None
+    where either is missing, in which case the binding calls the library
+    through ctypes alone."""
+    if not force and os.path.exists(PYCALL) and os.path.getmtime(PYCALL) >= os.path.getmtime(PYCALL_SRC):
+        return PYCALL
+    inc = sysconfig.get_paths().get("include")
+    gcc = shutil.which("gcc") or shutil.which("cc")
+    if not gcc or not inc or not os.path.exists(os.path.join(inc, "Python.h")):
+        return None
+    tmp = PYCALL + f".tmp{os.getpid()}"
+    r = subprocess.run([gcc, "-O2", "-shared", "-fPIC", "-I", inc, PYCALL_SRC, "-o", tmp], capture_output=True,
+                       text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"gcc failed on pycall.c:\n{r.stderr[-4000:]}")
+    os.replace(tmp, PYCALL)
+    return PYCALL
+
+
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
     """Compile (if sources changed) and return the path of librowops.so."""
+    build_pycall(force)
     if not (force or ptxas_info or _stale()):
         return LIB
     os.makedirs(BUILD, exist_ok=True)

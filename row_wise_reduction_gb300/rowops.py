@@ -128,7 +128,44 @@ def library() -> ctypes.CDLL:
         L.rowops_layernorm_gelu_backward.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _i64,
                                                      _i64, _i64, ctypes.c_int, _vp, ctypes.c_size_t, _vp]
         _lib = L
+        _bind_calls(L)
     return _lib
+
+
+class _Calls:
+    """The entry points whose small calls are bound by host time: through the
+    CPython call module ``_rowops_call`` where it was built (about 0.1 us of
+    marshalling per call), else through ctypes (about 2 us)."""
+
+    __slots__ = ("softmax", "layernorm_gelu", "layernorm_gelu_erf", "module")
+
+
+_calls: Optional[_Calls] = None
+
+
+def _bind_calls(L: ctypes.CDLL) -> None:
+    global _calls
+    c = _Calls()
+    try:
+        from . import _rowops_call as fast
+    except ImportError:
+        fast = None
+    if fast is not None:
+        def addr(f):
+            return ctypes.cast(f, ctypes.c_void_p).value
+
+        fast.bind(addr(L.rowops_softmax), addr(L.rowops_layernorm_gelu), addr(L.rowops_layernorm_gelu_erf))
+        c.softmax, c.layernorm_gelu, c.layernorm_gelu_erf = fast.softmax, fast.layernorm_gelu, fast.layernorm_gelu_erf
+    else:
+        c.softmax, c.layernorm_gelu, c.layernorm_gelu_erf = (L.rowops_softmax, L.rowops_layernorm_gelu,
+                                                              L.rowops_layernorm_gelu_erf)
+    c.module = fast
+    _calls = c
+
+
+def _hot_calls() -> _Calls:
+    library()
+    return _calls
 
 
 def rowops_status_string(status: int) -> str:
@@ -229,8 +266,8 @@ def _check(fn: str, status: int):
 def rowops_softmax(x: torch.Tensor, y: Optional[torch.Tensor] = None, *, stream=None) -> torch.Tensor:
     """Stable softmax of every row of ``x`` (M, N) into ``y`` (may be ``x``)."""
     M, N, ld, y, code, dev = _xy(x, y)
-    st = (_lib or library()).rowops_softmax(x.data_ptr(), y.data_ptr(), M, N, ld, code,
-                                            _current_raw_stream(dev) if stream is None else _stream(stream))
+    st = (_calls or _hot_calls()).softmax(x.data_ptr(), y.data_ptr(), M, N, ld, code,
+                                          _current_raw_stream(dev) if stream is None else _stream(stream))
     if st:
         raise RowopsError("rowops_softmax", st)
     return y
@@ -308,7 +345,7 @@ def rowops_layernorm_gelu(
 ) -> torch.Tensor:
     """Fused LayerNorm -> affine -> tanh-GELU of every row of ``x``."""
     M, N, ld, y, code, dev = _xy(x, y)
-    st = (_lib or library()).rowops_layernorm_gelu(
+    st = (_calls or _hot_calls()).layernorm_gelu(
         x.data_ptr(), y.data_ptr(), _affine(w, x, N, dev, "w"), _affine(b, x, N, dev, "b"), float(eps), M, N, ld,
         code, _current_raw_stream(dev) if stream is None else _stream(stream))
     if st:
@@ -327,7 +364,7 @@ def rowops_layernorm_gelu_erf(
 ) -> torch.Tensor:
     """Fused LayerNorm -> affine -> exact (erf) GELU of every row of ``x``."""
     M, N, ld, y, code, dev = _xy(x, y)
-    st = (_lib or library()).rowops_layernorm_gelu_erf(
+    st = (_calls or _hot_calls()).layernorm_gelu_erf(
         x.data_ptr(), y.data_ptr(), _affine(w, x, N, dev, "w"), _affine(b, x, N, dev, "b"), float(eps), M, N, ld,
         code, _current_raw_stream(dev) if stream is None else _stream(stream))
     if st:

@@ -257,3 +257,27 @@ def test_binding_has_no_fallback(monkeypatch, tmp_path):
     monkeypatch.setattr(r, "_LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="no fallback"):
         r.library()
+
+
+def test_call_module_marshals_like_ctypes(lib):
+    """The binding's CPython call module passes the same arguments to the same
+    entry points as ctypes: identical statuses on the validation cases (none
+    of which reaches the GPU)."""
+    from row_wise_reduction_gb300 import rowops as r
+
+    r.library()
+    fast = r._calls.module
+    if fast is None:
+        pytest.skip("the call module was not built (no gcc or Python headers)")
+    for args in [(X, Y, 4, 8, 8, 7, None), (X, Y, 4, 0, 8, F32, None), (None, Y, 4, 8, 8, F32, None),
+                 (X, X + 16, 4, 8, 8, F32, None), (X, Y, 1 << 62, 8, 1 << 40, F32, None),
+                 (None, None, 0, 8, 8, F32, None)]:
+        assert fast.softmax(*args) == lib.rowops_softmax(*args)
+    for f, g in [(fast.layernorm_gelu, lib.rowops_layernorm_gelu), (fast.layernorm_gelu_erf,
+                                                                     lib.rowops_layernorm_gelu_erf)]:
+        for args in [(X, Y, None, None, -1.0, 4, 8, 8, F32, None), (X, Y, None, None, float("nan"), 4, 8, 8, F32, None),
+                     (X, Y, X + 0x40001, None, 1e-5, 4, 8, 8, BF16, None), (X, Y, None, None, 1e-5, 4, 8, 4, F32, None),
+                     (None, None, None, None, 1e-5, 0, 8, 8, F32, None)]:
+            assert f(*args) == g(*args)
+    with pytest.raises(TypeError):
+        fast.softmax(X, Y, 4, 8, 8)
