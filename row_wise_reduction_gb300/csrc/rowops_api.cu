@@ -260,15 +260,33 @@ bool same_phase(const void* x, const void* y) {
     return ((reinterpret_cast<uintptr_t>(x) - reinterpret_cast<uintptr_t>(y)) & 15u) == 0;
 }
 
+// batches above 32 MiB: more than L2 keeps for a few rows per SM
+bool big_batch(int64_t M, int64_t N, int es) { return M * N * es > (int64_t(32) << 20); }
+
 // The row pipeline (bulk copies through a shared-memory ring) pays its ring's
-// fill latency once per CTA; on a batch of at most 32 MiB, L2-resident and only
-// a few rows per SM, the register-resident kernels are faster (GB300, CUDA
-// graphs: LayerNorm+GELU fp32 4096 x 768 6.2 us against 9.0, softmax fp32
-// 1024 x 768 2.6 against 2.9). Applies when the family is left automatic.
-bool pipeline_pays(const Tuning& tn, int64_t M, int64_t N, int es) {
+// fill latency once per CTA and a wait, its group reductions and a refill on
+// every row. On a batch of at most 32 MiB (L2-resident, a few rows per SM) the
+// register-resident kernels are faster (GB300, CUDA graphs: LayerNorm+GELU
+// fp32 4096 x 768 6.2 us against 9.0, softmax fp32 1024 x 768 2.6 against
+// 2.9), and so they are on larger batches of rows shorter than `min_row_bytes`
+// (each operation's crossover, measured back to back on GB300: e.g. softmax
+// fp32 262144 x 256 89 us against 248, LayerNorm+GELU bf16 131072 x 1024 120
+// against 197, row sum bf16 65536 x 2048 41 against 60). Applies when the
+// family is left automatic.
+bool pipeline_pays(const Tuning& tn, int64_t M, int64_t N, int es, int64_t min_row_bytes) {
     if (tn.family == Family::Tma) return true;
-    return tn.family == Family::Auto && M * N * es > (int64_t(32) << 20);
+    return tn.family == Family::Auto && big_batch(M, N, es) && N * es >= min_row_bytes;
 }
+
+// Rows from which each operation's row pipeline beats its register kernel on
+// large batches (GB300): LayerNorm+GELU and RMSNorm 4 KB (bf16 65536 x 2048
+// RMSNorm 84 against 105 us; 2 KB rows 91 against 95 the other way); softmax
+// 8 KB in bf16 (65536 x 4096: 178 against 188 us) and 16 KB in fp32 (8 KB
+// rows: 162 against 174 the other way); row sum / max 16 KB (8 KB rows: 78
+// against 83 us the other way; 16 KB within 1%).
+constexpr int64_t kPipeRowsNorm = 4096;
+constexpr int64_t kPipeRowsReduce = 16384;
+inline int64_t pipe_rows_softmax(int es) { return es == 4 ? 16384 : 8192; }
 
 // all rows of x (and, being in phase, of y) start on 16-byte boundaries
 bool rows_aligned(const void* x, const void* y, int64_t ld, int es) {
@@ -421,7 +439,7 @@ rowops_status_t rms_dispatch(const void* x, const void* r, void* y, void* ro, co
     // every row pointer at the same offset modulo 16 bytes
     const bool phase = same_phase(x, y) && (!res || (same_phase(x, r) && same_phase(x, ro)));
     TmaChoice tc;
-    if (pipeline_pays(tn, M, N, es) && phase &&
+    if (pipeline_pays(tn, M, N, es, kPipeRowsNorm) && phase &&
         choose_tma(x, y, N, ld, es, tn, {8, 4, 2, 1}, &tc)) {
         const int tpr = kTmaBlocks[tc.block_index], vpt = kTmaVpts[tc.vpt_index];
         const int S = res ? 2 : 1;
@@ -569,7 +587,7 @@ rowops_status_t rowops_softmax(const void* x, void* y, int64_t M, int64_t N, int
     if ((st = make_cfg(stream, tn, &cfg)) != ROWOPS_OK) return st;
     const int es = elem_bytes(dtype);
     TmaChoice tc;
-    if (pipeline_pays(tn, M, N, es) &&
+    if (pipeline_pays(tn, M, N, es, pipe_rows_softmax(es)) &&
         choose_tma(x, y, N, ld, es, tn, {8, 4, 2, 3, 1}, &tc)) {
         const int nbuf = ring_buffers(N, es, 0, tn, cfg);
         TmaSoftmaxLaunch tf = dtype == ROWOPS_F32 ? softmax_tma_f32(tc.block_index, tc.vpt_index, tc.full)
@@ -619,7 +637,7 @@ rowops_status_t reduce_dispatch(const void* x, float* out, int64_t M, int64_t N,
     if (st != ROWOPS_OK) return st;
     const int es = elem_bytes(dtype);
     TmaChoice tc;
-    if (pipeline_pays(tn, M, N, es) &&
+    if (pipeline_pays(tn, M, N, es, kPipeRowsReduce) &&
         choose_tma(x, x, N, ld, es, tn, {8, 4, 2, 3, 1}, &tc)) {
         const int nbuf = ring_buffers(N, es, 0, tn, cfg);
         TmaReduceLaunch tf = dtype == ROWOPS_F32 ? reduce_tma_f32(tc.block_index, tc.vpt_index, tc.full, op)
@@ -737,12 +755,12 @@ rowops_status_t ln_gelu_dispatch(const void* x, void* y, const void* w, const vo
     const bool short_rows = ld == N && N <= kFlatMaxN && aligned(x, 16) && aligned(y, 16);
     if (short_rows && (tn.family == Family::Flat ||
                        (tn.family == Family::Auto &&
-                        ((N * es) % 16 != 0 || N <= 128 || pipeline_pays(tn, M, N, es))))) {
+                        ((N * es) % 16 != 0 || N <= 128 || big_batch(M, N, es))))) {
         if (const LnGeluLaunch fl = ln_gelu_flat(es, erf, N, tn.tpr))
             return finish(fl(x, y, w, b, eps, M, N, ld, cfg));
     }
     TmaChoice tc;
-    if (pipeline_pays(tn, M, N, es) &&
+    if (pipeline_pays(tn, M, N, es, kPipeRowsNorm) &&
         choose_tma(x, y, N, ld, es, tn, {8, 4, 2, 3, 1}, &tc)) {
         const int tpr = kTmaBlocks[tc.block_index], vpt = kTmaVpts[tc.vpt_index];
         const int nbuf = ring_buffers(N, es, tma_affine_smem(tpr, vpt, es, tc.full, N), tn, cfg,
