@@ -153,7 +153,9 @@ __global__ void __launch_bounds__(BLOCK)
     const int t = threadIdx.x % TPR;
     const int slot = threadIdx.x / TPR;
     const int64_t ngroups = (M + ROWS - 1) / ROWS;
-    const float fN = float(N);
+    // 1/N once instead of three divisions per row (the mean's rounding is
+    // taken out by the residual either way); arithmetic on packed fp32 pairs
+    const float inv_n = 1.f / float(N);
 
     for (int64_t g = blockIdx.x; g < ngroups; g += gridDim.x) {
         const int64_t row = g * ROWS + slot;
@@ -177,7 +179,7 @@ __global__ void __launch_bounds__(BLOCK)
 
         // mean (padding contributes 0)
         float v[VPT][V];
-        float s = ex;
+        float2 s2 = make_float2(ex, 0.f);
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
             const int64_t k = t + int64_t(i) * TPR;
@@ -188,33 +190,37 @@ __global__ void __launch_bounds__(BLOCK)
                 for (int j = 0; j < V; ++j) v[i][j] = 0.f;
             }
 #pragma unroll
-            for (int j = 0; j < V; ++j) s += v[i][j];
+            for (int j = 0; j < V; j += 2) s2 = f2_add(s2, make_float2(v[i][j], v[i][j + 1]));
         }
-        s = group_reduce<TPR>(s, red_a, OpSum());
-        const float mean = s / fN;
+        const float s = group_reduce<TPR>(s2.x + s2.y, red_a, OpSum());
+        const float mean = s * inv_n;
 
         // variance of the centred values; padding stays out of it. The fp32
         // mean carries a rounding error of order |mean| 2^-24; the residual
         // r = sum(x - mean) measures it, delta = r / N, so that
         // x - true mean = (x - mean) - delta and var = q / N - delta^2.
-        float q = 0.f, r = 0.f;
+        float2 q2 = f2(0.f), r2 = f2(0.f);
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
             const int64_t k = t + int64_t(i) * TPR;
             const bool ok = k < geo.nvec;
 #pragma unroll
-            for (int j = 0; j < V; ++j) {
-                v[i][j] = ok ? v[i][j] - mean : 0.f;
-                q = fmaf(v[i][j], v[i][j], q);
-                r += v[i][j];
+            for (int j = 0; j < V; j += 2) {
+                float2 d = f2_add(make_float2(v[i][j], v[i][j + 1]), f2(-mean));
+                if (!ok) d = f2(0.f);
+                v[i][j] = d.x;
+                v[i][j + 1] = d.y;
+                q2 = f2_fma(d, d, q2);
+                r2 = f2_add(r2, d);
             }
         }
+        float q = q2.x + q2.y, r = r2.x + r2.y;
         ex = has_ex ? ex - mean : 0.f;
         q = fmaf(ex, ex, q);
         r += ex;
         group_reduce_sum2<TPR>(q, r, red_b);
-        const float delta = r / fN;
-        const float rstd = rsqrtf(fmaxf(q / fN - delta * delta, 0.f) + eps);
+        const float delta = r * inv_n;
+        const float rstd = rsqrtf(fmaxf(q * inv_n - delta * delta, 0.f) + eps);
         const float shift = -delta * rstd;  // (x - mean - delta) * rstd = fma(x - mean, rstd, shift)
 
         // affine + GELU + store
@@ -239,22 +245,35 @@ __global__ void __launch_bounds__(BLOCK)
                         for (int j = 0; j < V; ++j) bf[j] = 0.f;
                     }
 #pragma unroll
-                    for (int j = 0; j < V; ++j) o[j] = gelu_of<ERF>(fmaf(fmaf(v[i][j], rstd, shift), wf[j], bf[j]));
+                    for (int j = 0; j < V; j += 2) {
+                        const float2 z = f2_fma(make_float2(v[i][j], v[i][j + 1]), f2(rstd), f2(shift));
+                        const float2 g = gelu_of2<ERF>(
+                            f2_fma(z, make_float2(wf[j], wf[j + 1]), make_float2(bf[j], bf[j + 1])));
+                        o[j] = g.x;
+                        o[j + 1] = g.y;
+                    }
                 } else if constexpr (ALIGNED) {
 #pragma unroll
                     for (int j = 0; j < V; j += 4) {
                         const float4 ww = *reinterpret_cast<const float4*>(sw + c0 + j);
                         const float4 bb = *reinterpret_cast<const float4*>(sb + c0 + j);
-                        o[j + 0] = gelu_of<ERF>(fmaf(fmaf(v[i][j + 0], rstd, shift), ww.x, bb.x));
-                        o[j + 1] = gelu_of<ERF>(fmaf(fmaf(v[i][j + 1], rstd, shift), ww.y, bb.y));
-                        o[j + 2] = gelu_of<ERF>(fmaf(fmaf(v[i][j + 2], rstd, shift), ww.z, bb.z));
-                        o[j + 3] = gelu_of<ERF>(fmaf(fmaf(v[i][j + 3], rstd, shift), ww.w, bb.w));
+                        const float2 z0 = f2_fma(make_float2(v[i][j], v[i][j + 1]), f2(rstd), f2(shift));
+                        const float2 z1 = f2_fma(make_float2(v[i][j + 2], v[i][j + 3]), f2(rstd), f2(shift));
+                        const float2 g0 = gelu_of2<ERF>(f2_fma(z0, make_float2(ww.x, ww.y), make_float2(bb.x, bb.y)));
+                        const float2 g1 = gelu_of2<ERF>(f2_fma(z1, make_float2(ww.z, ww.w), make_float2(bb.z, bb.w)));
+                        o[j + 0] = g0.x;
+                        o[j + 1] = g0.y;
+                        o[j + 2] = g1.x;
+                        o[j + 3] = g1.y;
                     }
                 } else {
 #pragma unroll
-                    for (int j = 0; j < V; ++j) {
-                        const float2 wb = swb[affine_pair(c0 + j)];
-                        o[j] = gelu_of<ERF>(fmaf(fmaf(v[i][j], rstd, shift), wb.x, wb.y));
+                    for (int j = 0; j < V; j += 2) {
+                        const float2 wb0 = swb[affine_pair(c0 + j)], wb1 = swb[affine_pair(c0 + j + 1)];
+                        const float2 z = f2_fma(make_float2(v[i][j], v[i][j + 1]), f2(rstd), f2(shift));
+                        const float2 g = gelu_of2<ERF>(f2_fma(z, make_float2(wb0.x, wb1.x), make_float2(wb0.y, wb1.y)));
+                        o[j] = g.x;
+                        o[j + 1] = g.y;
                     }
                 }
                 st_stream16(yv + k * V, E::pack(o));
