@@ -72,7 +72,8 @@ __global__ void __launch_bounds__(BLOCK)
     const int t = threadIdx.x % TPR;
     const int slot = threadIdx.x / TPR;
     const int64_t ngroups = (M + ROWS - 1) / ROWS;
-    const float fN = float(N);
+    // 1/N once; arithmetic on packed fp32 pairs
+    const float inv_n = 1.f / float(N);
 
     for (int64_t g = blockIdx.x; g < ngroups; g += gridDim.x) {
         const int64_t row = g * ROWS + slot;
@@ -99,7 +100,7 @@ __global__ void __launch_bounds__(BLOCK)
         }
 
         float v[VPT][V];
-        float q = ex * ex;
+        float2 q2 = make_float2(ex * ex, 0.f);
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
             const int64_t k = t + int64_t(i) * TPR;
@@ -111,10 +112,13 @@ __global__ void __launch_bounds__(BLOCK)
                 for (int j = 0; j < V; ++j) v[i][j] = 0.f;
             }
 #pragma unroll
-            for (int j = 0; j < V; ++j) q = fmaf(v[i][j], v[i][j], q);
+            for (int j = 0; j < V; j += 2) {
+                const float2 p2 = make_float2(v[i][j], v[i][j + 1]);
+                q2 = f2_fma(p2, p2, q2);
+            }
         }
-        q = group_reduce<TPR>(q, red[(g / gridDim.x) & 1], OpSum());
-        const float inv = rsqrtf(q / fN + eps);
+        const float q = group_reduce<TPR>(q2.x + q2.y, red[(g / gridDim.x) & 1], OpSum());
+        const float inv = rsqrtf(q * inv_n + eps);
 
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
@@ -123,7 +127,12 @@ __global__ void __launch_bounds__(BLOCK)
                 const int c0 = geo.head + int(k) * V;
                 float o[V];
 #pragma unroll
-                for (int j = 0; j < V; ++j) o[j] = v[i][j] * inv * sw[weight_slot(c0 + j, V)];
+                for (int j = 0; j < V; j += 2) {
+                    const float2 p2 = f2_mul(f2_mul(make_float2(v[i][j], v[i][j + 1]), f2(inv)),
+                                             make_float2(sw[weight_slot(c0 + j, V)], sw[weight_slot(c0 + j + 1, V)]));
+                    o[j] = p2.x;
+                    o[j + 1] = p2.y;
+                }
                 st_stream16(y + off + c0, E::pack(o));
             }
         }
