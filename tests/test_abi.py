@@ -281,3 +281,32 @@ def test_call_module_marshals_like_ctypes(lib):
             assert f(*args) == g(*args)
     with pytest.raises(TypeError):
         fast.softmax(X, Y, 4, 8, 8)
+
+
+def test_binding_calls_through_ctypes_without_the_call_module(lib, monkeypatch):
+    """Where the CPython call module is absent, the three launch-bound entry
+    points bind to the library's ctypes functions instead: the same native
+    code, never a Python computation."""
+    import builtins
+
+    from row_wise_reduction_gb300 import rowops as r
+
+    real_import = builtins.__import__
+
+    def no_call_module(name, *args, **kwargs):
+        if name.endswith("_rowops_call") or (args and args[2] and "_rowops_call" in args[2]):
+            raise ImportError("no call module")
+        return real_import(name, *args, **kwargs)
+
+    saved = r._calls
+    monkeypatch.setattr(builtins, "__import__", no_call_module)
+    try:
+        r._bind_calls(r.library())
+        c = r._calls
+        assert c.module is None
+        assert c.softmax is lib.rowops_softmax or c.softmax.__name__ == "rowops_softmax"
+        assert c.softmax(None, None, 0, 8, 8, F32, None) == OK
+        assert c.layernorm_gelu(X, Y, None, None, -1.0, 4, 8, 8, F32, None) == INVALID
+    finally:
+        monkeypatch.setattr(builtins, "__import__", real_import)
+        r._calls = saved
