@@ -1,12 +1,14 @@
-// LayerNorm+GELU on short rows stored back to back (ld == N) whose length is
-// not a whole number of 16-byte vectors, e.g. bf16 rows of 127 elements.
+// LayerNorm+GELU on short rows stored back to back (ld == N <= 256): rows
+// whose length is not a whole number of 16-byte vectors (e.g. bf16 rows of 127
+// elements), rows of at most 128 columns, and large batches of such rows.
 //
-// Row-by-row kernels meet such rows at a different offset modulo 16 bytes each
-// time, so every row costs a head and a tail of scalar accesses and a per-row
-// split. Here the unit of memory traffic is a chunk of R consecutive rows
-// instead: R is a multiple of 16 / gcd(16, N * es), so every chunk starts on a
-// 16-byte boundary and all but the matrix's last chunk are whole 16-byte
-// vectors. A chunk moves global -> shared with one bulk copy and back with one
+// Row-by-row kernels meet unaligned rows at a different offset modulo 16 bytes
+// each time, so every row costs a head and a tail of scalar accesses and a
+// per-row split, and on short rows their per-row costs (group reductions,
+// waits) outweigh the arithmetic. Here the unit of memory traffic is a chunk
+// of R consecutive rows instead: R is a multiple of 16 / gcd(16, N * es), so
+// every chunk starts on a 16-byte boundary and all but the matrix's last chunk
+// are whole 16-byte vectors. A chunk moves global -> shared with one bulk copy and back with one
 // bulk store; in shared memory, teams of L lanes normalise its rows in place
 // (lane l takes the columns l, l + L, ...: consecutive lanes, consecutive
 // elements), with w, b held in registers for the whole kernel.
