@@ -127,8 +127,8 @@ def library() -> ctypes.CDLL:
         L.rowops_layernorm_gelu_backward.restype = ctypes.c_int
         L.rowops_layernorm_gelu_backward.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _i64,
                                                      _i64, _i64, ctypes.c_int, _vp, ctypes.c_size_t, _vp]
+        _bind_calls(L)  # before _lib: a thread that sees _lib set finds _calls set too
         _lib = L
-        _bind_calls(L)
     return _lib
 
 
