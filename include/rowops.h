@@ -131,13 +131,16 @@ void rowops_reload_tuning(void);
  *
  *   x, y   device pointers to M rows of `ld` elements of `dtype`; y may equal x.
  *   M      rows (>= 0); N columns (1 <= N < 2^31); ld row stride in elements (>= N).
- * Rows of 64 to 4096 16-byte vectors (256..16384 fp32, 512..32768 bf16
- * entries) whose x and y share their offset modulo 16 bytes stream through
- * shared memory: bulk asynchronous copies fill a ring of row buffers while
- * earlier rows are reduced and written (one HBM read, one write). Shorter rows
- * are held in registers by row groups of 16..1024 threads; longer rows, and x
- * and y at different offsets modulo 16 bytes, use an in-CTA online (m, d) loop
- * that reads the row twice [L6 §7.2].
+ * In batches above 32 MiB, rows of at least 8 KB (bf16) or 16 KB (fp32) and
+ * at most 4096 16-byte vectors whose x and y share their offset modulo 16
+ * bytes stream through shared memory: bulk asynchronous copies fill a ring of
+ * row buffers while earlier rows are reduced and written (one HBM read, one
+ * write). Smaller batches and shorter rows are held in registers by row groups
+ * of 16..1024 threads (the faster choice there); longer rows, and x and y at
+ * different offsets modulo 16 bytes, use an in-CTA online (m, d) loop that
+ * reads the row twice [L6 §7.2]. The other row operations choose the same
+ * way, with their own row sizes: 4 KB for LayerNorm+GELU and RMSNorm, 16 KB
+ * for row sum and max.
  */
 rowops_status_t rowops_softmax(const void* x, void* y, int64_t M, int64_t N, int64_t ld,
                                rowops_dtype_t dtype, cudaStream_t stream);
